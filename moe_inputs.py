@@ -1,0 +1,194 @@
+"""Seeded synthetic inputs for the sparse MoE FFN layer.
+
+This module is the one thing the GPU library's callers and the fp64 oracle's
+callers share: it draws random tensors and names the workload shapes.  It holds
+none of the layer's arithmetic (no scores, no selection, no FFN), only random
+numbers with the stated distributions.
+
+Workloads (shapes and distributions; names by what they are):
+
+  tiny_f32            T=64, d=256, E=8, K=2, I=512, no shared expert, fp32.
+                      x ~ N(0,1); router and expert weights ~ N(0, 1/d).
+  mixtral_prefill     T=4096, d=4096, E=8, K=2, I=14336, no shared expert, bf16.
+                      x ~ N(0,1); w_g, w_gate, w_up ~ N(0, 1/d); w_down ~ N(0, 1/I).
+  dsv3_decode         T=8, d=7168, E=256, K=8, I=2048, one shared expert Is=2048, bf16.
+                      x ~ N(0,1); all weights ~ N(0, 1/d).
+  dsv3_prefill_zipf   T=16384, otherwise dsv3_decode shapes, plus a per-expert bias
+                      b_e = -s * beta * ln(r_e) on the router scores, r a seeded
+                      permutation of 1..E, s = 1.2, beta = ZIPF_BETA, so expert
+                      popularity falls off like a Zipf law in rank.
+  dsv3_sweep_T{n}     dsv3_decode shapes at T = n, n in {1, 8, 64, 512, 4096}.
+
+Every tensor has its own sub-seed, splitmix64(seed ^ fnv1a64(name)), so adding
+or resizing one tensor never changes another.  Large weights are drawn one
+expert at a time from a single generator (deterministic for a given device
+type and torch build), on whatever device the caller names.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field, replace
+
+import torch
+
+MASK64 = (1 << 64) - 1
+ZIPF_S = 1.2
+# Scale of the log-rank bias (in units of the router score's standard deviation,
+# which is 1 for x ~ N(0,1) and w_g ~ N(0,1/d)).  With top-8 of 256 experts this
+# gives a log-log slope of the sorted expert counts near -1.2 over ranks 1..64 and
+# a hottest expert with more than 10x the mean count (checked by a test).
+ZIPF_BETA = 0.65
+
+
+@dataclass(frozen=True)
+class LayerConfig:
+    name: str
+    T: int
+    d: int
+    E: int
+    K: int
+    I: int
+    Is: int = 0           # 0 = no shared expert
+    dtype: str = "bf16"   # "bf16" or "f32"
+    down_std: str = "d"   # "d": w_down ~ N(0,1/d); "inter": N(0,1/I)
+    zipf_bias: bool = False
+    seed: int = 0
+    extra: dict = field(default_factory=dict, compare=False)
+
+    def with_T(self, T: int) -> "LayerConfig":
+        return replace(self, T=T, name=f"{self.name}@T{T}")
+
+
+CONFIGS: dict[str, LayerConfig] = {
+    "tiny_f32": LayerConfig("tiny_f32", T=64, d=256, E=8, K=2, I=512, Is=0, dtype="f32"),
+    "mixtral_prefill": LayerConfig("mixtral_prefill", T=4096, d=4096, E=8, K=2, I=14336, Is=0,
+                                   dtype="bf16", down_std="inter"),
+    "dsv3_decode": LayerConfig("dsv3_decode", T=8, d=7168, E=256, K=8, I=2048, Is=2048),
+    "dsv3_prefill_zipf": LayerConfig("dsv3_prefill_zipf", T=16384, d=7168, E=256, K=8, I=2048,
+                                     Is=2048, zipf_bias=True),
+}
+SWEEP_T = (1, 8, 64, 512, 4096)
+for _t in SWEEP_T:
+    CONFIGS[f"dsv3_sweep_T{_t}"] = LayerConfig(f"dsv3_sweep_T{_t}", T=_t, d=7168, E=256, K=8,
+                                               I=2048, Is=2048)
+
+
+def fnv1a64(s: str) -> int:
+    h = 0xCBF29CE484222325
+    for b in s.encode():
+        h ^= b
+        h = (h * 0x100000001B3) & MASK64
+    return h
+
+
+def splitmix64(z: int) -> int:
+    z = (z + 0x9E3779B97F4A7C15) & MASK64
+    z = ((z ^ (z >> 30)) * 0xBF58476D1CE4E5B9) & MASK64
+    z = ((z ^ (z >> 27)) * 0x94D049BB133111EB) & MASK64
+    return z ^ (z >> 31)
+
+
+def sub_seed(seed: int, name: str) -> int:
+    # torch.Generator.manual_seed takes a 64-bit value; keep it non-negative 63-bit
+    return splitmix64((seed & MASK64) ^ fnv1a64(name)) & ((1 << 63) - 1)
+
+
+def _gen(device, seed: int, name: str) -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed(sub_seed(seed, name))
+    return g
+
+
+def torch_dtype(dtype: str) -> torch.dtype:
+    return {"bf16": torch.bfloat16, "f32": torch.float32}[dtype]
+
+
+def normal(shape, std: float, dtype: str, device, seed: int, name: str,
+           chunk_dim0: bool = False) -> torch.Tensor:
+    """N(0, std^2) samples in the storage dtype, drawn in fp32 and rounded once.
+
+    With chunk_dim0 the tensor is drawn one leading index at a time (bounded
+    temporary memory for the expert weight stacks)."""
+    g = _gen(device, seed, name)
+    out = torch.empty(shape, dtype=torch_dtype(dtype), device=device)
+    if chunk_dim0:
+        for i in range(shape[0]):
+            out[i].copy_(torch.randn(shape[1:], generator=g, device=device,
+                                     dtype=torch.float32).mul_(std))
+    else:
+        out.copy_(torch.randn(shape, generator=g, device=device, dtype=torch.float32).mul_(std))
+    return out
+
+
+def zipf_bias(E: int, seed: int, s: float = ZIPF_S, beta: float = ZIPF_BETA) -> torch.Tensor:
+    """b_e = -s * beta * ln(r_e), r a seeded permutation of 1..E (fp32, CPU)."""
+    g = _gen("cpu", seed, "zipf_rank")
+    r = torch.randperm(E, generator=g).to(torch.float64) + 1.0
+    return (-s * beta * torch.log(r)).to(torch.float32)
+
+
+def make_weights(cfg: LayerConfig, device="cpu") -> dict:
+    """Router, routed-expert and shared-expert weights, stored [out][in]."""
+    d, E, I, Is, dt, sd = cfg.d, cfg.E, cfg.I, cfg.Is, cfg.dtype, cfg.seed
+    std_d = 1.0 / math.sqrt(d)
+    std_down = 1.0 / math.sqrt(I) if cfg.down_std == "inter" else std_d
+    p = {
+        "w_g": normal((E, d), std_d, dt, device, sd, "w_g"),
+        "w_gate": normal((E, I, d), std_d, dt, device, sd, "w_gate", chunk_dim0=True),
+        "w_up": normal((E, I, d), std_d, dt, device, sd, "w_up", chunk_dim0=True),
+        "w_down": normal((E, d, I), std_down, dt, device, sd, "w_down", chunk_dim0=True),
+    }
+    if Is:
+        std_sdown = 1.0 / math.sqrt(Is) if cfg.down_std == "inter" else std_d
+        p["ws_gate"] = normal((Is, d), std_d, dt, device, sd, "ws_gate")
+        p["ws_up"] = normal((Is, d), std_d, dt, device, sd, "ws_up")
+        p["ws_down"] = normal((d, Is), std_sdown, dt, device, sd, "ws_down")
+    return p
+
+
+def make_x(cfg: LayerConfig, device="cpu", name: str = "x") -> torch.Tensor:
+    return normal((cfg.T, cfg.d), 1.0, cfg.dtype, device, cfg.seed, name)
+
+
+def make_bias(cfg: LayerConfig, device="cpu"):
+    if not cfg.zipf_bias:
+        return None
+    return zipf_bias(cfg.E, cfg.seed).to(device)
+
+
+def redraw_rows(x: torch.Tensor, rows, cfg: LayerConfig, attempt: int) -> torch.Tensor:
+    """Replace the listed token rows of x with fresh N(0,1) draws from the
+    sub-seed (seed, "x_redraw/<attempt>/<row>") (deterministic)."""
+    x = x.clone()
+    for r in rows:
+        g = _gen(x.device, cfg.seed, f"x_redraw/{attempt}/{int(r)}")
+        x[int(r)].copy_(torch.randn((cfg.d,), generator=g, device=x.device, dtype=torch.float32))
+    return x
+
+
+def grid_logits(T: int, E: int, seed: int, scale: int = 512, name: str = "logits",
+                device="cpu") -> torch.Tensor:
+    """Router scores on the grid round(N(0,1) * scale) / scale, exact in fp32.
+
+    Distinct values differ by at least 1/scale (>= 1e-3 at scale 512); equal
+    values occur and are decided only by the tie rule."""
+    g = _gen(device, seed, name)
+    z = torch.randn((T, E), generator=g, device=device, dtype=torch.float64)
+    return (torch.round(z * scale) / scale).to(torch.float32)
+
+
+def sample_tokens(T: int, n: int, seed: int, name: str = "sample") -> torch.Tensor:
+    """A seeded sample of n distinct token ids in [0, T), sorted (int32, CPU)."""
+    if n >= T:
+        return torch.arange(T, dtype=torch.int32)
+    g = _gen("cpu", seed, name)
+    return torch.sort(torch.randperm(T, generator=g)[:n]).values.to(torch.int32)
+
+
+def to_host_array(t: torch.Tensor):
+    """Host numpy view of a tensor for the oracle: bf16 -> uint16 bit patterns,
+    fp32 -> float32, anything else as is."""
+    t = t.detach().to("cpu").contiguous()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view("uint16")
+    return t.numpy()

@@ -1,0 +1,250 @@
+"""fp64 CPU oracle for one sparse MoE FFN layer forward -- TEST INFRASTRUCTURE.
+
+Only the tests, the package smoke check and the benchmark's CPU-baseline arm may
+import this module.  The GPU library never imports, links or calls it, and it
+never imports the GPU library: the two share no code.  The arithmetic lives in
+``moe_oracle.c`` (plain C, double precision on the exact stored inputs); this
+file compiles it with gcc and marshals numpy arrays through ctypes.
+
+Every function here follows the definitions cited in ``moe_oracle.c``:
+router scores, top-K with ties to the lower expert index, softmax over the K
+selected scores, a stable counting-sort permutation with exclusive offsets, the
+SwiGLU expert FFN and the weighted combine plus the shared expert.
+
+Inputs: ``dtype`` is ``"f32"`` (numpy float32 arrays) or ``"bf16"`` (numpy
+uint16 arrays holding bf16 bit patterns).  Outputs are float64 / int32 numpy
+arrays.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "moe_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_DT = {"f32": 0, "bf16": 1}
+
+
+def compile_c(src: str, out: str) -> str:
+    """gcc, no -ffast-math and no FMA contraction, so results match across x86
+    and Arm hosts."""
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fPIC", "-shared",
+           "-pthread", "-o", tmp, src, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def build_oracle(force: bool = False) -> str:
+    """Compile moe_oracle.c into liboracle.so next to it when it is stale."""
+    stale = force or not os.path.exists(_LIB_PATH) or (
+        os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
+    if stale:
+        compile_c(_SRC, _LIB_PATH)
+    return _LIB_PATH
+
+
+def bind(lib):
+    """Declare the C signatures on a loaded liboracle handle."""
+    i64, i32, vp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
+    lib.oracle_default_threads.restype = i32
+    lib.oracle_route.argtypes = [i64, i64, i64, i64, i32, vp, vp, vp, vp, vp, vp, vp, i32]
+    lib.oracle_permute.argtypes = [i64, i64, i64, vp, vp, vp, vp, vp]
+    lib.oracle_expert_ffn.argtypes = [i64, i64, i64, i32, vp, vp, vp, vp, vp, vp, i32]
+    lib.oracle_combine.argtypes = [i64, i64, i64, vp, vp, vp, vp, vp]
+    lib.oracle_shared_ffn.argtypes = [i64, i64, i64, i32, vp, vp, vp, vp, vp, i32]
+    lib.oracle_forward.argtypes = [i64] * 6 + [i32] + [vp] * 16 + [i32]
+    lib.oracle_forward_tokens.argtypes = [i64, vp] + [i64] * 6 + [i32] + [vp] * 13 + [i32]
+    for f in ("oracle_route", "oracle_permute", "oracle_expert_ffn", "oracle_combine",
+              "oracle_shared_ffn", "oracle_forward", "oracle_forward_tokens"):
+        getattr(lib, f).restype = i32
+    return lib
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build_oracle()
+            _lib = bind(ctypes.CDLL(_LIB_PATH))
+    return _lib
+
+
+def default_threads() -> int:
+    return int(_load().oracle_default_threads())
+
+
+def _arr(a, dtype):
+    """Contiguous numpy array of the given dtype (or None)."""
+    if a is None:
+        return None
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _in(a, dtype: str):
+    if a is None:
+        return None
+    return _arr(a, np.uint16 if dtype == "bf16" else np.float32)
+
+
+def _check(rc: int, name: str):
+    if rc != 0:
+        raise ValueError(f"{name}: oracle rejected its arguments (rc={rc})")
+
+
+def route(x, w_g, K: int, dtype: str = "f32", bias=None, logits_in=None, threads: int = 0):
+    """Top-K routing.  Returns (topk_idx [T,K] int32, topk_w [T,K] f64, logits [T,E] f64).
+
+    With ``logits_in`` (fp32 [T,E]) those scores are used as given."""
+    lib = _load()
+    if logits_in is not None:
+        logits_in = _arr(logits_in, np.float32)
+        T, E = logits_in.shape
+        d = 1
+        x = w_g = None
+    else:
+        x, w_g = _in(x, dtype), _in(w_g, dtype)
+        T, d = x.shape
+        E = w_g.shape[0]
+    bias = _arr(bias, np.float64)
+    idx = np.zeros((T, K), np.int32)
+    w = np.zeros((T, K), np.float64)
+    logits = np.zeros((T, E), np.float64)
+    _check(lib.oracle_route(T, d, E, K, _DT[dtype], _ptr(x), _ptr(w_g), _ptr(bias),
+                            _ptr(logits_in), _ptr(logits), _ptr(idx), _ptr(w), threads),
+           "oracle_route")
+    return idx, w, logits
+
+
+def permute(topk_idx, E: int):
+    """Returns (counts [E], offsets [E+1], perm [T*K], inv_perm [T*K]) as int32."""
+    lib = _load()
+    idx = _arr(topk_idx, np.int32)
+    T, K = idx.shape
+    counts = np.zeros(E, np.int32)
+    offsets = np.zeros(E + 1, np.int32)
+    perm = np.zeros(T * K, np.int32)
+    inv = np.zeros(T * K, np.int32)
+    _check(lib.oracle_permute(T, E, K, _ptr(idx), _ptr(counts), _ptr(offsets), _ptr(perm),
+                              _ptr(inv)), "oracle_permute")
+    return counts, offsets, perm, inv
+
+
+def expert_ffn(x_perm, offsets, w_gate, w_up, w_down, dtype: str = "f32", threads: int = 0):
+    """SwiGLU per expert over expert-contiguous rows.  Returns y_perm [rows, d] f64."""
+    lib = _load()
+    x_perm = _in(x_perm, dtype)
+    offsets = _arr(offsets, np.int32)
+    w_gate, w_up, w_down = _in(w_gate, dtype), _in(w_up, dtype), _in(w_down, dtype)
+    E, I, d = w_gate.shape
+    rows = int(offsets[E])
+    y = np.zeros((max(rows, 0), d), np.float64)
+    _check(lib.oracle_expert_ffn(d, E, I, _DT[dtype], _ptr(x_perm), _ptr(offsets), _ptr(w_gate),
+                                 _ptr(w_up), _ptr(w_down), _ptr(y), threads),
+           "oracle_expert_ffn")
+    return y
+
+
+def shared_ffn(x, ws_gate, ws_up, ws_down, dtype: str = "f32", threads: int = 0):
+    """The always-on shared expert for every token.  Returns y_s [T, d] f64."""
+    lib = _load()
+    x = _in(x, dtype)
+    ws_gate, ws_up, ws_down = _in(ws_gate, dtype), _in(ws_up, dtype), _in(ws_down, dtype)
+    T, d = x.shape
+    Is = ws_gate.shape[0]
+    y = np.zeros((T, d), np.float64)
+    _check(lib.oracle_shared_ffn(T, d, Is, _DT[dtype], _ptr(x), _ptr(ws_gate), _ptr(ws_up),
+                                 _ptr(ws_down), _ptr(y), threads), "oracle_shared_ffn")
+    return y
+
+
+def combine(y_perm, inv_perm, topk_w, y_shared=None):
+    """y[t] = y_shared[t] + sum_j w[t,j] * y_perm[inv_perm[t*K+j]].  Returns y [T, d] f64."""
+    lib = _load()
+    y_perm = _arr(y_perm, np.float64)
+    inv = _arr(inv_perm, np.int32)
+    w = _arr(topk_w, np.float64)
+    T, K = w.shape
+    d = y_perm.shape[1]
+    ys = _arr(y_shared, np.float64)
+    y = np.zeros((T, d), np.float64)
+    _check(lib.oracle_combine(T, d, K, _ptr(y_perm), _ptr(inv), _ptr(w), _ptr(ys), _ptr(y)),
+           "oracle_combine")
+    return y
+
+
+def _weights(p: dict, dtype: str):
+    names = ("w_g", "w_gate", "w_up", "w_down", "ws_gate", "ws_up", "ws_down")
+    return {n: _in(p.get(n), dtype) for n in names}
+
+
+def forward(x, params: dict, K: int, dtype: str = "f32", bias=None, threads: int = 0):
+    """The whole layer for all T tokens (route, permute, expert FFN, shared, combine).
+
+    ``params`` holds w_g [E,d], w_gate/w_up [E,I,d], w_down [E,d,I] and optionally
+    ws_gate/ws_up [Is,d], ws_down [d,Is].  Returns a dict of numpy arrays:
+    y, topk_idx, topk_w, counts, offsets, perm, inv_perm."""
+    lib = _load()
+    x = _in(x, dtype)
+    w = _weights(params, dtype)
+    T, d = x.shape
+    E, I, _ = w["w_gate"].shape
+    Is = 0 if w["ws_gate"] is None else w["ws_gate"].shape[0]
+    bias = _arr(bias, np.float64)
+    out = {
+        "y": np.zeros((T, d), np.float64),
+        "topk_idx": np.zeros((T, K), np.int32),
+        "topk_w": np.zeros((T, K), np.float64),
+        "counts": np.zeros(E, np.int32),
+        "offsets": np.zeros(E + 1, np.int32),
+        "perm": np.zeros(T * K, np.int32),
+        "inv_perm": np.zeros(T * K, np.int32),
+    }
+    _check(lib.oracle_forward(
+        T, d, E, K, I, Is, _DT[dtype], _ptr(x), _ptr(w["w_g"]), _ptr(bias), _ptr(w["w_gate"]),
+        _ptr(w["w_up"]), _ptr(w["w_down"]), _ptr(w["ws_gate"]), _ptr(w["ws_up"]),
+        _ptr(w["ws_down"]), _ptr(out["y"]), _ptr(out["topk_idx"]), _ptr(out["topk_w"]),
+        _ptr(out["counts"]), _ptr(out["offsets"]), _ptr(out["perm"]), _ptr(out["inv_perm"]),
+        threads), "oracle_forward")
+    return out
+
+
+def forward_tokens(tokens, x, params: dict, K: int, dtype: str = "f32", bias=None,
+                   threads: int = 0):
+    """The layer output for the listed tokens only, from the per-token definition.
+
+    Returns a dict: y [n,d], topk_idx [n,K], topk_w [n,K], logits [n,E]."""
+    lib = _load()
+    tokens = _arr(tokens, np.int32)
+    x = _in(x, dtype)
+    w = _weights(params, dtype)
+    T, d = x.shape
+    E, I, _ = w["w_gate"].shape
+    Is = 0 if w["ws_gate"] is None else w["ws_gate"].shape[0]
+    n = tokens.shape[0]
+    bias = _arr(bias, np.float64)
+    out = {
+        "y": np.zeros((n, d), np.float64),
+        "topk_idx": np.zeros((n, K), np.int32),
+        "topk_w": np.zeros((n, K), np.float64),
+        "logits": np.zeros((n, E), np.float64),
+    }
+    _check(lib.oracle_forward_tokens(
+        n, _ptr(tokens), T, d, E, K, I, Is, _DT[dtype], _ptr(x), _ptr(w["w_g"]), _ptr(bias),
+        _ptr(w["w_gate"]), _ptr(w["w_up"]), _ptr(w["w_down"]), _ptr(w["ws_gate"]),
+        _ptr(w["ws_up"]), _ptr(w["ws_down"]), _ptr(out["y"]), _ptr(out["topk_idx"]),
+        _ptr(out["topk_w"]), _ptr(out["logits"]), threads), "oracle_forward_tokens")
+    return out

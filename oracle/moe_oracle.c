@@ -1,0 +1,573 @@
+/*
+ * moe_oracle.c -- plain fp64 CPU oracle for the forward pass of one sparse
+ * Mixture-of-Experts FFN layer.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the checker the GPU library is
+ * measured against.  It shares no code, header, table or helper with the CUDA
+ * library; only tests, the package's smoke check and the benchmark's CPU
+ * baseline load it.  Nothing here is tuned: every loop is the definition
+ * written out, accumulated in double precision on the exact values of the
+ * stored inputs (bf16 or fp32), with no intermediate rounding.
+ *
+ * The layer (sources, by page title and section):
+ *   - "Sparse MoE inference kernels: expert parallelism, dynamic routing gates
+ *     and all-to-all overlap" (blog.llmgo.top), section 1.1: a shared expert
+ *     that every token passes through plus K routed experts picked by the gate
+ *     network W_g; each expert is a gated FFN with W_gate, W_up, W_down
+ *     (section 1.2).
+ *   - adg.csdn.net sparse-MoE explainer ("1.8T parameters, 2% active"),
+ *     section 2.2: scoring s = Router(h), selection of the K best scores,
+ *     softmax over only the K selected scores, output = sum_i w_i*Expert_i(h).
+ *   - Same llmgo page, section 4.3: flatten the [T,K] expert ids, order the
+ *     slots by expert id, gather the rows, per-expert counts and offsets for a
+ *     grouped GEMM.  (The page's code uses an unstable argsort and an
+ *     inclusive cumsum; this oracle uses the stable order by flat slot and an
+ *     exclusive scan with E+1 entries.)
+ *   - "Computation and Data Movement for Inference", section 4: expert outputs
+ *     go back to token order, are weighted and summed.
+ *
+ * Readings taken where the pages are silent (each is listed in the design
+ * notes): ties in top-K go to the lower expert index; the K selected experts
+ * of a token are ordered by descending score, which defines slot j; the
+ * expert FFN is SwiGLU, h = SiLU(W_gate x) * (W_up x), y = W_down h, with
+ * SiLU(z) = z / (1 + exp(-z)); the optional per-expert bias b is added to the
+ * logits before both selection and softmax; the combine adds the shared
+ * expert first, then slots j = 0..K-1 in order.
+ *
+ * Storage: row-major; weights are stored [out][in] like nn.Linear:
+ *   x [T][d], w_g [E][d], w_gate/w_up [E][I][d], w_down [E][d][I],
+ *   shared ws_gate/ws_up [Is][d], ws_down [d][Is].
+ * dtype 0 = fp32 (float), 1 = bf16 (uint16_t bit patterns).
+ *
+ * Every entry point returns 0 on success and a negative number on a bad
+ * argument; nothing is allocated that is not freed before return.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <unistd.h>
+
+#define ORC_F32 0
+#define ORC_BF16 1
+
+/* ------------------------------------------------------------------------ */
+/* element access: the exact stored value, widened to double                */
+/* ------------------------------------------------------------------------ */
+
+static double bf16_bits_to_double(uint16_t b)
+{
+    /* a bf16 value is the upper half of an IEEE binary32 */
+    uint32_t u = ((uint32_t)b) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+static double load_elem(const void *base, int dtype, int64_t i)
+{
+    if (dtype == ORC_BF16)
+        return bf16_bits_to_double(((const uint16_t *)base)[i]);
+    return (double)((const float *)base)[i];
+}
+
+static size_t elem_size(int dtype) { return dtype == ORC_BF16 ? 2u : 4u; }
+
+/* ------------------------------------------------------------------------ */
+/* a plain parallel-for over independent rows (tokens or permuted rows)     */
+/* ------------------------------------------------------------------------ */
+
+typedef void (*row_fn)(void *ctx, int64_t row);
+
+typedef struct {
+    row_fn fn;
+    void *ctx;
+    int64_t begin, end;
+} par_slice;
+
+static void *par_worker(void *arg)
+{
+    par_slice *s = (par_slice *)arg;
+    for (int64_t r = s->begin; r < s->end; ++r)
+        s->fn(s->ctx, r);
+    return NULL;
+}
+
+int oracle_default_threads(void)
+{
+    long n = sysconf(_SC_NPROCESSORS_ONLN);
+    return n > 0 ? (int)n : 1;
+}
+
+static void par_for(int64_t n, int nthreads, row_fn fn, void *ctx)
+{
+    if (nthreads <= 0)
+        nthreads = oracle_default_threads();
+    if (nthreads > n)
+        nthreads = (int)(n > 0 ? n : 1);
+    if (nthreads <= 1) {
+        for (int64_t r = 0; r < n; ++r)
+            fn(ctx, r);
+        return;
+    }
+    pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
+    par_slice *sl = (par_slice *)malloc(sizeof(par_slice) * (size_t)nthreads);
+    int started = 0;
+    for (int i = 0; i < nthreads; ++i) {
+        sl[i].fn = fn;
+        sl[i].ctx = ctx;
+        sl[i].begin = n * i / nthreads;
+        sl[i].end = n * (i + 1) / nthreads;
+        if (pthread_create(&th[i], NULL, par_worker, &sl[i]) != 0) {
+            /* could not start a thread: run this slice here */
+            par_worker(&sl[i]);
+            th[i] = 0;
+        } else {
+            ++started;
+        }
+    }
+    for (int i = 0; i < nthreads; ++i)
+        if (th[i])
+            pthread_join(th[i], NULL);
+    (void)started;
+    free(th);
+    free(sl);
+}
+
+/* ------------------------------------------------------------------------ */
+/* stage 1: router scores, top-K, softmax over the K selected               */
+/* ------------------------------------------------------------------------ */
+
+/* s_e = sum_k x[k] * w_g[e][k] (+ b_e).  The gate network is a linear map
+ * with one score per expert (explainer section 2.2, step 1; llmgo page
+ * section 2.1). */
+static void router_scores(int64_t d, int64_t E, int dtype, const void *x,
+                          int64_t t, const void *w_g, const double *bias,
+                          double *s)
+{
+    for (int64_t e = 0; e < E; ++e) {
+        double acc = 0.0;
+        for (int64_t k = 0; k < d; ++k)
+            acc += load_elem(x, dtype, t * d + k) * load_elem(w_g, dtype, e * d + k);
+        s[e] = acc + (bias ? bias[e] : 0.0);
+    }
+}
+
+/* Pick the K largest scores one at a time; a strictly larger score replaces
+ * the current best while scanning e upward, so among equal scores the lower
+ * index is kept.  Slot j holds the j-th pick (descending score).  Then
+ * w_j = exp(s_{i_j} - s_{i_0}) / sum_j' exp(s_{i_j'} - s_{i_0}), the softmax
+ * over only the K selected scores (explainer section 2.2, steps 2-3). */
+static void select_and_weigh(int64_t E, int64_t K, const double *s,
+                             unsigned char *taken, int32_t *idx, double *w)
+{
+    memset(taken, 0, (size_t)E);
+    for (int64_t j = 0; j < K; ++j) {
+        int64_t best = -1;
+        for (int64_t e = 0; e < E; ++e) {
+            if (taken[e])
+                continue;
+            if (best < 0 || s[e] > s[best])
+                best = e;
+        }
+        taken[best] = 1;
+        idx[j] = (int32_t)best;
+    }
+    const double smax = s[idx[0]];
+    double denom = 0.0;
+    for (int64_t j = 0; j < K; ++j) {
+        w[j] = exp(s[idx[j]] - smax);
+        denom += w[j];
+    }
+    for (int64_t j = 0; j < K; ++j)
+        w[j] /= denom;
+}
+
+typedef struct {
+    int64_t d, E, K;
+    int dtype;
+    const void *x, *w_g;
+    const double *bias;
+    const float *logits_in;
+    double *logits_out;
+    int32_t *topk_idx;
+    double *topk_w;
+} route_ctx;
+
+static void route_row(void *vctx, int64_t t)
+{
+    route_ctx *c = (route_ctx *)vctx;
+    double *s = (double *)malloc(sizeof(double) * (size_t)c->E);
+    unsigned char *taken = (unsigned char *)malloc((size_t)c->E);
+    if (c->logits_in) {
+        for (int64_t e = 0; e < c->E; ++e)
+            s[e] = (double)c->logits_in[t * c->E + e];
+    } else {
+        router_scores(c->d, c->E, c->dtype, c->x, t, c->w_g, c->bias, s);
+    }
+    if (c->logits_out)
+        memcpy(c->logits_out + t * c->E, s, sizeof(double) * (size_t)c->E);
+    select_and_weigh(c->E, c->K, s, taken, c->topk_idx + t * c->K, c->topk_w + t * c->K);
+    free(s);
+    free(taken);
+}
+
+/*
+ * oracle_route: scores, top-K and K-way softmax for T tokens.
+ * If logits_in is non-NULL its fp32 values are the scores (x, w_g and bias are
+ * then ignored); otherwise scores are x . w_g^T (+ bias) in fp64.
+ * logits_out [T][E] (optional) receives the scores used.
+ */
+int oracle_route(int64_t T, int64_t d, int64_t E, int64_t K, int dtype,
+                 const void *x, const void *w_g, const double *bias,
+                 const float *logits_in, double *logits_out,
+                 int32_t *topk_idx, double *topk_w, int nthreads)
+{
+    if (T < 0 || E < 1 || K < 1 || K > E || !topk_idx || !topk_w)
+        return -1;
+    if (!logits_in && (!x || !w_g || d < 1))
+        return -1;
+    route_ctx c = {d, E, K, dtype, x, w_g, bias, logits_in, logits_out, topk_idx, topk_w};
+    par_for(T, nthreads, route_row, &c);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* stage 2: counts, exclusive offsets, stable permutation                   */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Flat slot f = t*K + j.  counts[e] = #{f : idx[f] == e}; offsets is the
+ * exclusive scan (offsets[0] = 0, offsets[E] = T*K); perm lists the slots of
+ * expert 0 in increasing f, then expert 1, ... (a counting sort, stable by
+ * construction); inv_perm[perm[p]] = p.  llmgo page section 4.3 (flatten,
+ * order by expert id, bincount, offsets); "Computation and Data Movement for
+ * Inference" section 15 (sort the routing records by expert).
+ */
+int oracle_permute(int64_t T, int64_t E, int64_t K, const int32_t *topk_idx,
+                   int32_t *counts, int32_t *offsets, int32_t *perm,
+                   int32_t *inv_perm)
+{
+    if (T < 0 || E < 1 || K < 1 || !counts || !offsets)
+        return -1;
+    const int64_t n = T * K;
+    for (int64_t e = 0; e < E; ++e)
+        counts[e] = 0;
+    for (int64_t f = 0; f < n; ++f) {
+        int32_t e = topk_idx[f];
+        if (e < 0 || e >= E)
+            return -2;
+        counts[e] += 1;
+    }
+    offsets[0] = 0;
+    for (int64_t e = 0; e < E; ++e)
+        offsets[e + 1] = offsets[e] + counts[e];
+    int32_t *cursor = (int32_t *)malloc(sizeof(int32_t) * (size_t)E);
+    for (int64_t e = 0; e < E; ++e)
+        cursor[e] = offsets[e];
+    for (int64_t f = 0; f < n; ++f) {
+        int32_t p = cursor[topk_idx[f]]++;
+        if (perm)
+            perm[p] = (int32_t)f;
+        if (inv_perm)
+            inv_perm[f] = p;
+    }
+    free(cursor);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* stage 3: SwiGLU expert FFN over expert-contiguous rows                   */
+/* ------------------------------------------------------------------------ */
+
+/* y = W_down . (SiLU(W_gate . x) * (W_up . x)) for one row x of length d,
+ * expert matrices given by their base element offsets.  The gated FFN with
+ * W_gate, W_up, W_down is the expert of the llmgo page (section 1.2) and the
+ * gated MLP "up, gate, down" of "LLM from scratch, ch. 6" (MLP roofline). */
+static void swiglu_row(int64_t d, int64_t I, int dtype, const void *xrow_base,
+                       int64_t xrow_off, const void *w_gate, const void *w_up,
+                       const void *w_down, int64_t wg_off, int64_t wu_off,
+                       int64_t wd_off, double *h, double *y)
+{
+    for (int64_t i = 0; i < I; ++i) {
+        double g = 0.0, u = 0.0;
+        for (int64_t k = 0; k < d; ++k) {
+            double xv = load_elem(xrow_base, dtype, xrow_off + k);
+            g += load_elem(w_gate, dtype, wg_off + i * d + k) * xv;
+            u += load_elem(w_up, dtype, wu_off + i * d + k) * xv;
+        }
+        double silu = g / (1.0 + exp(-g));
+        h[i] = silu * u;
+    }
+    for (int64_t j = 0; j < d; ++j) {
+        double acc = 0.0;
+        for (int64_t i = 0; i < I; ++i)
+            acc += load_elem(w_down, dtype, wd_off + j * I + i) * h[i];
+        y[j] = acc;
+    }
+}
+
+typedef struct {
+    int64_t d, E, I;
+    int dtype;
+    const void *x_perm;
+    const int32_t *offsets;
+    const void *w_gate, *w_up, *w_down;
+    double *y_perm;
+} ffn_ctx;
+
+static int64_t expert_of_row(const int32_t *offsets, int64_t E, int64_t p)
+{
+    /* the expert e with offsets[e] <= p < offsets[e+1] (empty experts have
+     * offsets[e] == offsets[e+1] and never match) */
+    for (int64_t e = 0; e < E; ++e)
+        if (p >= offsets[e] && p < offsets[e + 1])
+            return e;
+    return -1;
+}
+
+static void ffn_row(void *vctx, int64_t p)
+{
+    ffn_ctx *c = (ffn_ctx *)vctx;
+    int64_t e = expert_of_row(c->offsets, c->E, p);
+    double *h = (double *)malloc(sizeof(double) * (size_t)c->I);
+    const int64_t wgu = e * c->I * c->d, wd = e * c->d * c->I;
+    swiglu_row(c->d, c->I, c->dtype, c->x_perm, p * c->d, c->w_gate, c->w_up,
+               c->w_down, wgu, wgu, wd, h, c->y_perm + p * c->d);
+    free(h);
+}
+
+/*
+ * oracle_expert_ffn: rows [0, offsets[E]) of x_perm belong to experts by the
+ * offsets array (grouped-GEMM form, llmgo page section 4.2); y_perm [rows][d]
+ * in fp64.  Experts with zero rows contribute nothing and read nothing
+ * (llmgo page, FAQ Q1).
+ */
+int oracle_expert_ffn(int64_t d, int64_t E, int64_t I, int dtype,
+                      const void *x_perm, const int32_t *offsets,
+                      const void *w_gate, const void *w_up, const void *w_down,
+                      double *y_perm, int nthreads)
+{
+    if (d < 1 || E < 1 || I < 1 || !offsets || !y_perm)
+        return -1;
+    if (offsets[0] != 0)
+        return -1;
+    for (int64_t e = 0; e < E; ++e)
+        if (offsets[e + 1] < offsets[e])
+            return -1;
+    ffn_ctx c = {d, E, I, dtype, x_perm, offsets, w_gate, w_up, w_down, y_perm};
+    par_for(offsets[E], nthreads, ffn_row, &c);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* stage 4: combine                                                         */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * y[t] = y_shared[t] + sum_{j=0..K-1} w[t][j] * y_perm[inv_perm[t*K+j]],
+ * the shared term first, then j ascending.  Explainer section 2.2 step 4
+ * (weighted sum of the selected experts); llmgo page section 1.1 (shared
+ * expert output added to the routed sum); "Computation and Data Movement for
+ * Inference" section 4 (back to token order, weighted, merged).
+ */
+int oracle_combine(int64_t T, int64_t d, int64_t K, const double *y_perm,
+                   const int32_t *inv_perm, const double *topk_w,
+                   const double *y_shared, double *y)
+{
+    if (T < 0 || d < 1 || K < 1 || !y)
+        return -1;
+    for (int64_t t = 0; t < T; ++t) {
+        for (int64_t c = 0; c < d; ++c) {
+            double acc = y_shared ? y_shared[t * d + c] : 0.0;
+            for (int64_t j = 0; j < K; ++j) {
+                int64_t p = inv_perm[t * K + j];
+                acc += topk_w[t * K + j] * y_perm[p * d + c];
+            }
+            y[t * d + c] = acc;
+        }
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* the shared expert                                                         */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+    int64_t d, Is;
+    int dtype;
+    const void *x, *ws_gate, *ws_up, *ws_down;
+    const int32_t *tokens;
+    double *y_s;
+} shared_ctx;
+
+static void shared_row(void *vctx, int64_t r)
+{
+    shared_ctx *c = (shared_ctx *)vctx;
+    int64_t t = c->tokens ? c->tokens[r] : r;
+    double *h = (double *)malloc(sizeof(double) * (size_t)c->Is);
+    swiglu_row(c->d, c->Is, c->dtype, c->x, t * c->d, c->ws_gate, c->ws_up,
+               c->ws_down, 0, 0, 0, h, c->y_s + r * c->d);
+    free(h);
+}
+
+/* y_s[t] = SwiGLU_shared(x[t]) for every token (weight 1, no routing):
+ * the always-active shared expert of the llmgo page, section 1.1. */
+int oracle_shared_ffn(int64_t T, int64_t d, int64_t Is, int dtype,
+                      const void *x, const void *ws_gate, const void *ws_up,
+                      const void *ws_down, double *y_s, int nthreads)
+{
+    if (T < 0 || d < 1 || Is < 1 || !y_s)
+        return -1;
+    shared_ctx c = {d, Is, dtype, x, ws_gate, ws_up, ws_down, NULL, y_s};
+    par_for(T, nthreads, shared_row, &c);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* the whole layer, four stages                                             */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * oracle_forward: route -> permute (+ gather x rows into expert order) ->
+ * expert FFN -> shared expert -> combine, for all T tokens.  Outputs in fp64:
+ * y [T][d]; optional topk_idx [T][K], topk_w [T][K], counts [E],
+ * offsets [E+1], perm / inv_perm [T*K].  Is == 0 means no shared expert.
+ */
+int oracle_forward(int64_t T, int64_t d, int64_t E, int64_t K, int64_t I,
+                   int64_t Is, int dtype, const void *x, const void *w_g,
+                   const double *bias, const void *w_gate, const void *w_up,
+                   const void *w_down, const void *ws_gate, const void *ws_up,
+                   const void *ws_down, double *y, int32_t *topk_idx_out,
+                   double *topk_w_out, int32_t *counts_out,
+                   int32_t *offsets_out, int32_t *perm_out,
+                   int32_t *inv_perm_out, int nthreads)
+{
+    if (T < 0 || d < 1 || E < 1 || K < 1 || K > E || I < 1 || Is < 0 || !y)
+        return -1;
+    const int64_t n = T * K;
+    const size_t es = elem_size(dtype);
+    int32_t *idx = (int32_t *)malloc(sizeof(int32_t) * (size_t)(n ? n : 1));
+    double *w = (double *)malloc(sizeof(double) * (size_t)(n ? n : 1));
+    int32_t *counts = (int32_t *)malloc(sizeof(int32_t) * (size_t)E);
+    int32_t *offsets = (int32_t *)malloc(sizeof(int32_t) * (size_t)(E + 1));
+    int32_t *perm = (int32_t *)malloc(sizeof(int32_t) * (size_t)(n ? n : 1));
+    int32_t *inv = (int32_t *)malloc(sizeof(int32_t) * (size_t)(n ? n : 1));
+    unsigned char *x_perm = (unsigned char *)malloc(es * (size_t)(n ? n : 1) * (size_t)d);
+    double *y_perm = (double *)malloc(sizeof(double) * (size_t)(n ? n : 1) * (size_t)d);
+    double *y_s = Is ? (double *)malloc(sizeof(double) * (size_t)(T ? T : 1) * (size_t)d) : NULL;
+    int rc = oracle_route(T, d, E, K, dtype, x, w_g, bias, NULL, NULL, idx, w, nthreads);
+    if (rc == 0)
+        rc = oracle_permute(T, E, K, idx, counts, offsets, perm, inv);
+    if (rc == 0) {
+        /* gather: row p of x_perm is the token row perm[p] / K (an exact copy) */
+        for (int64_t p = 0; p < n; ++p)
+            memcpy(x_perm + (size_t)p * (size_t)d * es,
+                   (const unsigned char *)x + (size_t)(perm[p] / K) * (size_t)d * es,
+                   (size_t)d * es);
+        rc = oracle_expert_ffn(d, E, I, dtype, x_perm, offsets, w_gate, w_up,
+                               w_down, y_perm, nthreads);
+    }
+    if (rc == 0 && Is)
+        rc = oracle_shared_ffn(T, d, Is, dtype, x, ws_gate, ws_up, ws_down, y_s, nthreads);
+    if (rc == 0)
+        rc = oracle_combine(T, d, K, y_perm, inv, w, y_s, y);
+    if (rc == 0) {
+        if (topk_idx_out) memcpy(topk_idx_out, idx, sizeof(int32_t) * (size_t)n);
+        if (topk_w_out) memcpy(topk_w_out, w, sizeof(double) * (size_t)n);
+        if (counts_out) memcpy(counts_out, counts, sizeof(int32_t) * (size_t)E);
+        if (offsets_out) memcpy(offsets_out, offsets, sizeof(int32_t) * (size_t)(E + 1));
+        if (perm_out) memcpy(perm_out, perm, sizeof(int32_t) * (size_t)n);
+        if (inv_perm_out) memcpy(inv_perm_out, inv, sizeof(int32_t) * (size_t)n);
+    }
+    free(idx); free(w); free(counts); free(offsets); free(perm); free(inv);
+    free(x_perm); free(y_perm); free(y_s);
+    return rc;
+}
+
+/* ------------------------------------------------------------------------ */
+/* the layer for a sample of tokens, straight from the definition           */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+    int64_t d, E, K, I, Is;
+    int dtype;
+    const void *x, *w_g;
+    const double *bias;
+    const void *w_gate, *w_up, *w_down, *ws_gate, *ws_up, *ws_down;
+    const int32_t *tokens;
+    double *y, *logits;
+    int32_t *idx;
+    double *w;
+} tok_ctx;
+
+static void token_row(void *vctx, int64_t r)
+{
+    tok_ctx *c = (tok_ctx *)vctx;
+    const int64_t t = c->tokens[r];
+    const int64_t d = c->d;
+    int64_t hmax = c->I > c->Is ? c->I : c->Is;
+    double *s = (double *)malloc(sizeof(double) * (size_t)c->E);
+    unsigned char *taken = (unsigned char *)malloc((size_t)c->E);
+    double *h = (double *)malloc(sizeof(double) * (size_t)hmax);
+    double *ye = (double *)malloc(sizeof(double) * (size_t)d);
+    int32_t *idx = c->idx + r * c->K;
+    double *w = c->w + r * c->K;
+    double *y = c->y + r * d;
+
+    router_scores(d, c->E, c->dtype, c->x, t, c->w_g, c->bias, s);
+    if (c->logits)
+        memcpy(c->logits + r * c->E, s, sizeof(double) * (size_t)c->E);
+    select_and_weigh(c->E, c->K, s, taken, idx, w);
+
+    /* y = SharedExpert(x_t) + sum_j w_j * Expert_{i_j}(x_t) */
+    if (c->Is) {
+        swiglu_row(d, c->Is, c->dtype, c->x, t * d, c->ws_gate, c->ws_up,
+                   c->ws_down, 0, 0, 0, h, y);
+    } else {
+        for (int64_t k = 0; k < d; ++k)
+            y[k] = 0.0;
+    }
+    for (int64_t j = 0; j < c->K; ++j) {
+        const int64_t e = idx[j];
+        const int64_t wgu = e * c->I * d, wd = e * d * c->I;
+        swiglu_row(d, c->I, c->dtype, c->x, t * d, c->w_gate, c->w_up,
+                   c->w_down, wgu, wgu, wd, h, ye);
+        for (int64_t k = 0; k < d; ++k)
+            y[k] += w[j] * ye[k];
+    }
+    free(s); free(taken); free(h); free(ye);
+}
+
+/*
+ * oracle_forward_tokens: the layer output for the listed tokens only,
+ * y_r = SharedExpert(x_t) + sum_{j} w_j Expert_{i_j}(x_t) with t = tokens[r].
+ * Each token's output depends on its own row only (routing and the expert
+ * weights do not depend on the other tokens; "Computation and Data Movement
+ * for Inference", sections 5 and 16), so a sample of rows is checked
+ * exactly as in the full layer.  Outputs: y [n][d], topk_idx [n][K],
+ * topk_w [n][K], logits [n][E] (optional).
+ */
+int oracle_forward_tokens(int64_t n, const int32_t *tokens, int64_t T,
+                          int64_t d, int64_t E, int64_t K, int64_t I,
+                          int64_t Is, int dtype, const void *x,
+                          const void *w_g, const double *bias,
+                          const void *w_gate, const void *w_up,
+                          const void *w_down, const void *ws_gate,
+                          const void *ws_up, const void *ws_down, double *y,
+                          int32_t *topk_idx, double *topk_w, double *logits,
+                          int nthreads)
+{
+    if (n < 0 || d < 1 || E < 1 || K < 1 || K > E || I < 1 || Is < 0 || !y ||
+        !topk_idx || !topk_w || (n > 0 && !tokens))
+        return -1;
+    for (int64_t r = 0; r < n; ++r)
+        if (tokens[r] < 0 || tokens[r] >= T)
+            return -1;
+    tok_ctx c = {d, E, K, I, Is, dtype, x, w_g, bias, w_gate, w_up, w_down,
+                 ws_gate, ws_up, ws_down, tokens, y, logits, topk_idx, topk_w};
+    par_for(n, nthreads, token_row, &c);
+    return 0;
+}

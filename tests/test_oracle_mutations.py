@@ -1,0 +1,74 @@
+"""Plant plausible mistakes in a copy of the oracle (on the CPU) and check that
+the pins in test_oracle_pins.py catch every one of them."""
+import ctypes
+import os
+
+import pytest
+
+import oracle
+from tests import test_oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "moe_oracle.c")
+
+# (name, exact text in moe_oracle.c, replacement)
+MUTATIONS = [
+    ("ties_to_higher_index", "if (best < 0 || s[e] > s[best])", "if (best < 0 || s[e] >= s[best])"),
+    ("softmax_sign", "w[j] = exp(s[idx[j]] - smax);", "w[j] = exp(smax - s[idx[j]]);"),
+    ("silu_sign", "double silu = g / (1.0 + exp(-g));", "double silu = g / (1.0 + exp(g));"),
+    ("dropped_up_projection", "h[i] = silu * u;", "h[i] = silu;"),
+    ("transposed_down_projection", "load_elem(w_down, dtype, wd_off + j * I + i)",
+     "load_elem(w_down, dtype, wd_off + i * d + j)"),
+    ("swapped_gate_and_up", "double silu = g / (1.0 + exp(-g));\n        h[i] = silu * u;",
+     "double silu = u / (1.0 + exp(-u));\n        h[i] = silu * g;"),
+    ("dropped_bias", "s[e] = acc + (bias ? bias[e] : 0.0);", "s[e] = acc;"),
+    ("dropped_shared_in_combine", "double acc = y_shared ? y_shared[t * d + c] : 0.0;",
+     "double acc = 0.0;"),
+    ("first_weight_for_all_slots", "acc += topk_w[t * K + j] * y_perm[p * d + c];",
+     "acc += topk_w[t * K] * y_perm[p * d + c];"),
+    ("reversed_order_within_expert", "int32_t p = cursor[topk_idx[f]]++;",
+     "int32_t p = offsets[topk_idx[f] + 1] - 1 - (cursor[topk_idx[f]]++ - offsets[topk_idx[f]]);"),
+    ("router_reads_wrong_row", "load_elem(w_g, dtype, e * d + k)", "load_elem(w_g, dtype, ((e + 1) % E) * d + k)"),
+]
+
+PIN_TESTS = [
+    lambda: pins.test_topk_matches_exhaustive_sort(40, 256, 8, 2),
+    lambda: pins.test_ties_go_to_lower_index_and_signed_zero_is_a_tie(),
+    lambda: pins.test_K_equals_E_is_full_softmax(),
+    lambda: pins.test_weights_sum_to_one(),
+    lambda: pins.test_scores_are_x_times_wg_transposed(),
+    lambda: pins.test_bias_enters_selection_and_weights(),
+    lambda: pins.test_forward_matches_dense_masked_evaluation("f32", 9, 24, 6, 3, 40, 16),
+    lambda: pins.test_single_expert_is_a_dense_swiglu_mlp(),
+    lambda: pins.test_hand_built_layer_closed_form(),
+    lambda: pins.test_combine_is_linear_in_the_weights(),
+    lambda: pins.test_permutation_is_the_stable_expert_order(37, 3, 3),
+]
+
+
+def _caught(lib) -> bool:
+    saved = oracle._lib
+    oracle._lib = lib
+    try:
+        for t in PIN_TESTS:
+            try:
+                t()
+            except (AssertionError, ValueError):
+                return True
+        return False
+    finally:
+        oracle._lib = saved
+
+
+@pytest.mark.parametrize("name,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_pins_catch_planted_mistake(tmp_path, name, old, new):
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation anchor for {name} not unique/absent"
+    mutated = tmp_path / "mutant.c"
+    mutated.write_text(src.replace(old, new))
+    so = oracle.compile_c(str(mutated), str(tmp_path / "libmutant.so"))
+    lib = oracle.bind(ctypes.CDLL(so))
+    assert _caught(lib), f"no pin caught the planted mistake '{name}'"
+
+
+def test_unmutated_oracle_passes_every_pin():
+    assert not _caught(oracle._load())
