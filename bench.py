@@ -1,0 +1,531 @@
+"""Benchmark of the sparse MoE FFN layer forward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--no-decode] [--no-cpu-baseline] [--all]
+
+One step = one moe_forward (router + top-K + softmax, dispatch, routed and
+shared expert FFN, combine) over one batch of the workload's synthetic tokens,
+inputs resident in HBM.  Default workload: the Mixtral-shaped prefill layer
+(T=4096, d=4096, E=8, K=2, I=14336, bf16).  Every weight set is larger than the
+129 MB L2, so no flush is needed between steps.  Also reported: the
+DeepSeek-V3-shaped decode layer (T=8) in microseconds per call against the HBM
+roofline, the end-to-end number through the C ABI with host buffers, the
+dominant stage against its roofline, and the fp64 CPU oracle on a bounded
+sample of the same workload.  Under torchrun every rank runs an independent
+replica on its own tokens (weak scaling, no collective on the data path).
+
+``--impl reference`` times the CPU oracle (the only reference this layer has)
+on the host cores for the same workload and metric.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import moe_inputs as mi  # noqa: E402
+
+DEFAULT_WORKLOAD = "mixtral_prefill"
+DECODE_WORKLOAD = "dsv3_decode"
+
+
+# --------------------------------------------------------------------------- work accounting
+
+def layer_flops(cfg) -> int:
+    """Router GEMM + routed SwiGLU experts (K per token) + shared expert."""
+    return (2 * cfg.T * cfg.d * cfg.E + 6 * cfg.T * cfg.K * cfg.d * cfg.I
+            + 6 * cfg.T * cfg.d * cfg.Is)
+
+
+def ffn_flops(cfg) -> int:
+    return 6 * cfg.T * cfg.K * cfg.d * cfg.I + 6 * cfg.T * cfg.d * cfg.Is
+
+
+def elem_bytes(cfg) -> int:
+    return 2 if cfg.dtype == "bf16" else 4
+
+
+def layer_bytes(cfg, n_active: int) -> int:
+    """Algorithmic HBM bytes of one call: router weights, the weights of every
+    expert that got at least one token, the shared expert, x in and y out.
+    Permuted copies and intermediates are implementation traffic, not counted."""
+    s = elem_bytes(cfg)
+    return s * (cfg.E * cfg.d + n_active * 3 * cfg.d * cfg.I + 3 * cfg.d * cfg.Is
+                + 2 * cfg.T * cfg.d)
+
+
+def launches_per_forward(cfg, gemv_limit: int = 16) -> int:
+    """Kernels libmoe launches for one moe_forward (mirrors the host logic in
+    moe_api.cu): router (GEMV or tcgen05) + top-K, 3 dispatch kernels, the row
+    gather when the tensor-core path may run, the FFN plan, 2 GEMV kernels,
+    2 tcgen05 GEMMs when needed, combine."""
+    need_tc = cfg.dtype == "bf16" and cfg.T > gemv_limit
+    return 2 + 3 + (1 if need_tc else 0) + 1 + 2 + (2 if need_tc else 0) + 1
+
+
+# --------------------------------------------------------------------------- helpers
+
+def load_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines: list[str] = []
+        self.reader = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.reader = threading.Thread(target=self._read, daemon=True)
+            self.reader.start()
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            if self.reader:
+                self.reader.join(timeout=2)
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(v: float, ws: int) -> float:
+    if ws <= 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64,
+                     device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws: int):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# --------------------------------------------------------------------------- CPU oracle timing
+
+def oracle_tokens_per_s(cfg, x_host, p_host, bias_host, budget_s: float = 15.0,
+                        seed_name: str = "cpu_sample"):
+    """The fp64 oracle as it stands on the host cores: the layer for a growing
+    seeded sample of tokens until about budget_s of CPU time has been spent."""
+    import oracle
+    threads = oracle.default_threads()
+    n, spent, done = max(1, threads), 0.0, 0
+    t_start = time.perf_counter()
+    while True:
+        tokens = mi.sample_tokens(cfg.T, n, seed=cfg.seed, name=f"{seed_name}/{n}").numpy()
+        t0 = time.perf_counter()
+        oracle.forward_tokens(tokens, x_host, p_host, cfg.K, dtype=cfg.dtype, bias=bias_host)
+        dt = time.perf_counter() - t0
+        spent += dt
+        done = len(tokens)
+        rate = done / dt
+        if spent >= budget_s * 0.4 or n >= cfg.T:
+            return {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                    "sample": f"{done} seeded tokens of {cfg.name} (T={cfg.T}), full layer per "
+                              f"token (router over all E, K routed experts, shared expert) in fp64; "
+                              f"{time.perf_counter() - t_start:.1f} s of wall time"}
+        n = min(cfg.T, max(n + 1, int(n * max(2.0, (budget_s * 0.5) / max(dt, 1e-3)))))
+
+
+# --------------------------------------------------------------------------- our arm
+
+def run_ours(args):
+    import torch
+
+    ws_n, rank, local = dist_env()
+    if ws_n > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    import sparse_expert_ffn_moe_gb300 as moe
+
+    peaks = load_peaks()
+    cfg = mi.CONFIGS[args.workload]
+    # every rank draws its own tokens (a replica serving a different batch)
+    cfg_r = mi.LayerConfig(**{**cfg.__dict__, "seed": cfg.seed + rank})
+    p = mi.make_weights(cfg_r, "cuda")
+    x = mi.make_x(cfg_r, "cuda")
+    bias = mi.make_bias(cfg_r, "cuda")
+    s = moe.make_shape(cfg.T, cfg.d, cfg.E, cfg.K, cfg.I, cfg.Is, cfg.dtype)
+    ws = moe.alloc_workspace(s)
+    y = torch.empty_like(x)
+    stream = torch.cuda.Stream()
+
+    def fwd(xx=x, yy=y):
+        moe.moe_forward(s, xx, p["w_g"], bias, p["w_gate"], p["w_up"], p["w_down"],
+                        p.get("ws_gate"), p.get("ws_up"), p.get("ws_down"), yy, ws, stream=stream)
+
+    # active experts of this batch (for the byte count), from the library's own routing
+    n_active = count_active(moe, cfg, x, p, bias, stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            fwd()
+    torch.cuda.synchronize()
+    code = moe.moe_get_device_error(ws)
+    if code:
+        raise RuntimeError(f"device error during warm-up: {moe.status_string(code)}")
+
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        barrier(ws_n)
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for _ in range(args.steps):
+            fwd()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        barrier(ws_n)
+        # dominant stage, timed alone on the same stream: the expert FFN (tcgen05
+        # gate/up GEMM with fused SiLU*mul, then the down GEMM) of this batch
+        stage = time_expert_ffn(moe, cfg, x, p, bias, stream, args.steps)
+    t_ms = ev0.elapsed_time(ev1) / args.steps
+    t_ms_max = max_over_ranks(t_ms, ws_n)
+    code = moe.moe_get_device_error(ws)
+    if code:
+        raise RuntimeError(f"device error in the timed region: {moe.status_string(code)}")
+
+    tokens_per_s = cfg.T * ws_n / (t_ms_max / 1e3)
+    e2e = time_e2e(moe, cfg, s, p, bias, ws, stream, args.steps, x)
+    e2e_ms = max_over_ranks(e2e["ms"], ws_n)
+
+    result = {
+        "metric": "MoE layer tokens/s",
+        "value": tokens_per_s,
+        "unit": "tokens/s",
+        "n_gpus": ws_n,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": t_ms_max,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": cfg.dtype,
+        "data": "synthetic (seeded N(0,1) tokens, N(0,1/d) weights; no trained weights)",
+        "config": {"workload": cfg.name, "T": cfg.T, "d": cfg.d, "E": cfg.E, "K": cfg.K,
+                   "inter": cfg.I, "inter_shared": cfg.Is, "active_experts": n_active,
+                   "l2": "inputs larger than L2 (expert weights "
+                         f"{3 * cfg.E * cfg.d * cfg.I * elem_bytes(cfg) / 1e9:.2f} GB), no flush",
+                   "parallelism": f"replicas x{ws_n} (independent batches, no collective)"},
+        "layer": {"tflops": layer_flops(cfg) / (t_ms_max / 1e3) / 1e12,
+                  "gbs": layer_bytes(cfg, n_active) / (t_ms_max / 1e3) / 1e9,
+                  "flops": layer_flops(cfg), "alg_bytes": layer_bytes(cfg, n_active)},
+        "roofline": stage_roofline(cfg, stage, peaks),
+        "e2e": {"value": cfg.T * ws_n / (e2e_ms / 1e3), "unit": "tokens/s",
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": e2e["h2d"],
+                "d2h_bytes_per_step": e2e["d2h"]},
+        "gpu_launches": launches_per_forward(cfg) * args.steps,
+        "clocks": clk.summary(),
+        "peaks": peaks,
+    }
+    if not args.no_decode and rank == 0:
+        result["decode"] = bench_decode(moe, peaks, args)
+    if args.all and rank == 0:
+        result["workloads"] = bench_all(moe, peaks, args)
+    if not args.no_cpu_baseline and rank == 0:
+        torch.cuda.synchronize()
+        hp = {k: mi.to_host_array(v) for k, v in p.items()}
+        result["cpu_baseline"] = oracle_tokens_per_s(
+            cfg_r, mi.to_host_array(x), hp,
+            None if bias is None else bias.double().cpu().numpy(), budget_s=args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if ws_n > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def count_active(moe, cfg, x, p, bias, stream) -> int:
+    import torch
+    s = moe.make_shape(cfg.T, cfg.d, cfg.E, cfg.K, cfg.I, cfg.Is, cfg.dtype)
+    ws = moe.alloc_workspace(s)
+    idx = torch.empty((cfg.T, cfg.K), dtype=torch.int32, device="cuda")
+    w = torch.empty((cfg.T, cfg.K), dtype=torch.float32, device="cuda")
+    moe.moe_route(s, x, p["w_g"], bias, None, None, idx, w, ws, stream=stream)
+    torch.cuda.synchronize()
+    return int(torch.unique(idx).numel())
+
+
+def time_expert_ffn(moe, cfg, x, p, bias, stream, steps: int) -> dict:
+    """Events around moe_expert_ffn alone (routed experts of this batch)."""
+    import torch
+    s = moe.make_shape(cfg.T, cfg.d, cfg.E, cfg.K, cfg.I, 0, cfg.dtype)
+    ws = moe.alloc_workspace(s)
+    n = cfg.T * cfg.K
+    idx = torch.empty((cfg.T, cfg.K), dtype=torch.int32, device="cuda")
+    w = torch.empty((cfg.T, cfg.K), dtype=torch.float32, device="cuda")
+    counts = torch.empty(cfg.E, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(cfg.E + 1, dtype=torch.int32, device="cuda")
+    x_perm = torch.empty((n, cfg.d), dtype=x.dtype, device="cuda")
+    y_perm = torch.empty((n, cfg.d), dtype=x.dtype, device="cuda")
+    moe.moe_route(s, x, p["w_g"], bias, None, None, idx, w, ws, stream=stream)
+    moe.moe_permute(s, idx, x, counts, offsets, None, None, x_perm, ws, stream=stream)
+
+    def run():
+        moe.moe_expert_ffn(s, x_perm, offsets, p["w_gate"], p["w_up"], p["w_down"], y_perm, ws,
+                           stream=stream)
+    for _ in range(3):
+        run()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(steps):
+        run()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    return {"ms": ms, "flops": 6 * n * cfg.d * cfg.I}
+
+
+def stage_roofline(cfg, stage, peaks) -> dict:
+    achieved = stage["flops"] / (stage["ms"] / 1e3) / 1e12
+    peak = peaks["bf16_tflops"]
+    return {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+            "frac": achieved / peak, "traffic": None,
+            "kernel": "expert FFN stage: tcgen05 gate/up GEMM (SiLU*mul epilogue) + tcgen05 "
+                      "down GEMM (+ plan, empty GEMV launches)",
+            "per_launch_flops": stage["flops"], "ms_per_launch": stage["ms"],
+            "peak_kind": f"bf16 dense, burst, {peaks['source']}"}
+
+
+def time_e2e(moe, cfg, s, p, bias, ws, stream, steps, x_dev) -> dict:
+    """Through the C ABI with host buffers: pinned x -> device, moe_forward,
+    y -> pinned host, every step inside the timed region."""
+    import torch
+    xh = x_dev.cpu().pin_memory()
+    yh = torch.empty_like(xh).pin_memory()
+    xd = torch.empty_like(x_dev)
+    yd = torch.empty_like(x_dev)
+
+    def step():
+        with torch.cuda.stream(stream):
+            xd.copy_(xh, non_blocking=True)
+            moe.moe_forward(s, xd, p["w_g"], bias, p["w_gate"], p["w_up"], p["w_down"],
+                            p.get("ws_gate"), p.get("ws_up"), p.get("ws_down"), yd, ws,
+                            stream=stream)
+            yh.copy_(yd, non_blocking=True)
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    nbytes = xh.numel() * xh.element_size()
+    return {"ms": e0.elapsed_time(e1) / steps, "h2d": nbytes, "d2h": nbytes}
+
+
+def bench_decode(moe, peaks, args) -> dict:
+    """DeepSeek-V3-shaped decode (T=8): microseconds per call against HBM, eager
+    and as a replayed CUDA graph."""
+    import torch
+    cfg = mi.CONFIGS[DECODE_WORKLOAD]
+    r = bench_workload(moe, cfg, peaks, steps=max(50, args.steps * 5), graph=True)
+    return r
+
+
+def bench_workload(moe, cfg, peaks, steps: int, graph: bool = False) -> dict:
+    import torch
+    p = mi.make_weights(cfg, "cuda")
+    x = mi.make_x(cfg, "cuda")
+    bias = mi.make_bias(cfg, "cuda")
+    s = moe.make_shape(cfg.T, cfg.d, cfg.E, cfg.K, cfg.I, cfg.Is, cfg.dtype)
+    ws = moe.alloc_workspace(s)
+    y = torch.empty_like(x)
+    st = torch.cuda.Stream()
+    n_active = count_active(moe, cfg, x, p, bias, st)
+
+    def fwd():
+        moe.moe_forward(s, x, p["w_g"], bias, p["w_gate"], p["w_up"], p["w_down"],
+                        p.get("ws_gate"), p.get("ws_up"), p.get("ws_down"), y, ws, stream=st)
+    for _ in range(5):
+        fwd()
+    torch.cuda.synchronize()
+
+    def timed(fn):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        for _ in range(steps):
+            fn()
+        e1.record(st)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps
+
+    ms = timed(fwd)
+    out = {"workload": cfg.name, "T": cfg.T, "us_per_call": ms * 1e3,
+           "tokens_per_s": cfg.T / (ms / 1e3), "active_experts": n_active,
+           "alg_bytes": layer_bytes(cfg, n_active), "flops": layer_flops(cfg)}
+    if graph:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=st):
+            fwd()
+        g.replay()
+        torch.cuda.synchronize()
+        gms = timed(g.replay)
+        out["us_per_call_graph"] = gms * 1e3
+        ms = min(ms, gms)
+    gbs = out["alg_bytes"] / (ms / 1e3) / 1e9
+    tfs = out["flops"] / (ms / 1e3) / 1e12
+    out["hbm_gbs"] = gbs
+    out["hbm_frac"] = gbs / peaks["hbm_gbs"]
+    out["tensor_tflops"] = tfs
+    out["tensor_frac"] = tfs / peaks["bf16_tflops"]
+    code = moe.moe_get_device_error(ws)
+    if code:
+        raise RuntimeError(f"device error in {cfg.name}: {moe.status_string(code)}")
+    del p, x, y, ws
+    torch.cuda.empty_cache()
+    return out
+
+
+def bench_all(moe, peaks, args) -> list:
+    res = []
+    for name in ("tiny_f32", "mixtral_prefill", "dsv3_decode", "dsv3_prefill_zipf",
+                 *[f"dsv3_sweep_T{t}" for t in mi.SWEEP_T]):
+        cfg = mi.CONFIGS[name]
+        res.append(bench_workload(moe, cfg, peaks, steps=max(10, args.steps),
+                                  graph=cfg.T <= 64))
+    return res
+
+
+# --------------------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    """The CPU oracle timed on the host cores, same workload and metric."""
+    ws_n, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import torch
+    cfg = mi.CONFIGS[args.workload]
+    import oracle
+    p = mi.make_weights(cfg, "cpu")
+    x = mi.make_x(cfg, "cpu")
+    bias = mi.make_bias(cfg, "cpu")
+    hp = {k: mi.to_host_array(v) for k, v in p.items()}
+    xh = mi.to_host_array(x)
+    bh = None if bias is None else bias.double().numpy()
+    del p
+    threads = oracle.default_threads()
+    # per-step sample sized so that warm-up + steps end within a few minutes
+    per_step = max(threads, 16)
+    times = []
+    for i in range(args.warmup + args.steps):
+        tokens = mi.sample_tokens(cfg.T, per_step, seed=cfg.seed, name=f"ref_step/{i}").numpy()
+        t0 = time.perf_counter()
+        oracle.forward_tokens(tokens, xh, hp, cfg.K, dtype=cfg.dtype, bias=bh)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append(dt)
+    ms = 1e3 * sum(times) / len(times)
+    value = per_step / (ms / 1e3)
+    sample = (f"{per_step} seeded tokens of {cfg.name} per step, full layer per token in fp64 "
+              f"(router, K routed experts, shared expert)")
+    print(json.dumps({
+        "impl": "reference", "metric": "MoE layer tokens/s", "value": value, "unit": "tokens/s",
+        "n_gpus": ws_n, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": cfg.name, "T": cfg.T, "d": cfg.d, "E": cfg.E,
+                                        "K": cfg.K, "inter": cfg.I, "inter_shared": cfg.Is},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(mi.CONFIGS))
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--all", action="store_true", help="also time every workload")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

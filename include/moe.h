@@ -1,0 +1,180 @@
+/*
+ * moe.h -- C ABI of libmoe, the GB300 (sm_103a) forward pass of one sparse
+ * Mixture-of-Experts FFN layer:
+ *
+ *     y = SharedExpert(x) + sum_{i in TopK(x . W_g^T + b)} w_i * Expert_i(x),
+ *     w = softmax over only the K selected scores,
+ *     Expert(x) = W_down (SiLU(W_gate x) * (W_up x))          (SwiGLU).
+ *
+ * Sources, by page title and section:
+ *   [R] adg.csdn.net sparse-MoE explainer ("1.8T parameters, 2% active"),
+ *       section 2.2: score every expert with a small linear router, keep the
+ *       K best scores, softmax over those K, weighted sum of the K experts.
+ *   [S] "Sparse MoE inference kernels: expert parallelism, dynamic routing
+ *       gates and all-to-all overlap" (blog.llmgo.top): section 1.1 shared
+ *       expert plus routed experts; section 1.2 W_gate/W_up/W_down experts
+ *       and the decode (GEMV-like) vs prefill (GEMM) regimes; section 4.2
+ *       grouped GEMM over an offsets array; section 4.3 token permutation
+ *       (flatten, order by expert, gather, counts, offsets); FAQ Q1 experts
+ *       with zero tokens are skipped.
+ *   [C] "Computation and Data Movement for Inference", sections 4 and 15:
+ *       routing records sorted by expert id so one weight load serves the
+ *       whole bucket; outputs returned to token order, weighted and merged.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All pointers except `shape` and `code_out` are DEVICE pointers on the
+ *    current CUDA device, 16-byte aligned.  Storage is row-major; weights are
+ *    [out][in] (nn.Linear layout):
+ *        x [T][d], w_g [E][d], w_gate, w_up [E][I][d], w_down [E][d][I],
+ *        ws_gate, ws_up [Is][d], ws_down [d][Is], bias [E] (fp32).
+ *  - dtype: MOE_F32 (every activation and weight fp32; fp32 FMA arithmetic,
+ *    no TF32) or MOE_BF16 (bf16 storage, fp32 accumulation).  Router scores
+ *    and routing weights are always fp32; indices are int32.
+ *  - Ownership: the caller allocates every buffer, including `workspace`
+ *    (size from moe_workspace_bytes).  The library never allocates, frees or
+ *    synchronises; all work is enqueued on `stream` in order.
+ *  - Errors: argument errors return a non-zero moe_status immediately and
+ *    enqueue nothing.  A failed launch returns MOE_ERR_CUDA.  Errors found
+ *    on the device (index out of range, a bounded wait that ran out) are
+ *    recorded in the workspace's error word and read with
+ *    moe_get_device_error after the stream has been synchronised; each entry
+ *    point that takes a workspace clears that word first.
+ *  - Limits: 0 <= T, T*K < 2^31; 1 <= K <= min(E, 32); E <= 1024;
+ *    d and I (and Is when > 0) multiples of 64; d <= 65536, I, Is <= 65536.
+ *    T == 0 is a no-op returning MOE_OK.
+ *  - Routing rule: top-K picks the largest scores, ties to the LOWER expert
+ *    index (scores compared as floats, so -0.0 == +0.0); slot j of a token
+ *    holds its j-th pick (descending score).  Flat slot f = t*K + j.
+ *  - Threading: entry points are reentrant and keep no mutable global state
+ *    beyond per-device attributes cached on first use.
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1, /* null pointer, bad size, K > E, ...          */
+    MOE_ERR_UNSUPPORTED = 2, /* legal but outside the limits above          */
+    MOE_ERR_WORKSPACE = 3,   /* workspace missing or smaller than required  */
+    MOE_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed        */
+    MOE_ERR_TIMEOUT = 5,     /* device: a bounded wait ran out              */
+    MOE_ERR_BOUNDS = 6       /* device: an index was out of range           */
+} moe_status;
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
+
+typedef struct {
+    int32_t T;            /* tokens                                         */
+    int32_t d;            /* hidden size                                    */
+    int32_t E;            /* routed experts                                 */
+    int32_t K;            /* experts per token                              */
+    int32_t inter;        /* routed expert intermediate size I              */
+    int32_t inter_shared; /* shared expert intermediate size Is; 0 = none   */
+    int32_t dtype;        /* moe_dtype                                      */
+} moe_shape;
+
+/* Text for a status code (static storage, never NULL). */
+const char *moe_status_string(int32_t status);
+
+/*
+ * Bytes of workspace that every entry point below accepts for `shape`
+ * (one size serves all of them).  Returns 0 for an invalid shape.
+ */
+size_t moe_workspace_bytes(const moe_shape *shape);
+
+/*
+ * Stage 1, routing [R section 2.2; S section 2.1].
+ *   scores[t][e] = sum_k x[t][k] * w_g[e][k] + bias[e]   (fp32 accumulate)
+ *   topk_idx[t][j], topk_w[t][j]: the K best scores with ties to the lower
+ *   index, and w = softmax over those K scores.
+ * bias may be NULL (no bias).  If logits_in [T][E] (fp32) is non-NULL it is
+ * used as the scores and x, w_g, bias are ignored (may be NULL).
+ * logits_out [T][E] (fp32) receives the scores if non-NULL.
+ * Outputs: topk_idx [T][K] int32, topk_w [T][K] fp32.
+ */
+moe_status moe_route(const moe_shape *shape, const void *x, const void *w_g,
+                     const float *bias, const float *logits_in,
+                     float *logits_out, int32_t *topk_idx, float *topk_w,
+                     void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * Stage 2, dispatch [S section 4.3; C section 15].
+ *   counts[e]  = number of flat slots f with topk_idx[f] == e      [E]
+ *   offsets    = exclusive scan of counts, offsets[E] = T*K         [E+1]
+ *   perm[p]    = flat slot at sorted position p; slots ordered by expert
+ *                id, and by increasing f within an expert (stable)   [T*K]
+ *   inv_perm[f]= p with perm[p] == f                                 [T*K]
+ *   x_perm[p]  = x[perm[p] / K]   (row gather; skipped if x or x_perm is
+ *                NULL)                                        [T*K][d]
+ * perm and inv_perm may be NULL if not wanted.  An expert id outside
+ * [0, E) is recorded as MOE_ERR_BOUNDS on the device and its slot dropped.
+ */
+moe_status moe_permute(const moe_shape *shape, const int32_t *topk_idx,
+                       const void *x, int32_t *counts, int32_t *offsets,
+                       int32_t *perm, int32_t *inv_perm, void *x_perm,
+                       void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * Stage 3, grouped expert FFN [S sections 1.2, 4.2; C section 15].
+ * For each expert e and each row p in [offsets[e], offsets[e+1]):
+ *   h = SiLU(w_gate[e] . x_perm[p]) * (w_up[e] . x_perm[p]),
+ *   y_perm[p] = w_down[e] . h.
+ * offsets [E+1] is a device array (as written by moe_permute); nothing on
+ * the host reads it.  Experts with no rows read no weights.  Rows with few
+ * tokens per expert stream each selected expert's weights once (GEMV path);
+ * experts with many rows run on the tcgen05 tensor-core grouped GEMM.
+ * Shape fields used: d, E, inter, dtype, T and K (rows = T*K).
+ * inter_shared is ignored here: the shared expert is the same operation
+ * with E = 1, K = 1, offsets = {0, T} and x in place of x_perm.
+ * Output: y_perm [T*K][d] in the layer dtype.
+ */
+moe_status moe_expert_ffn(const moe_shape *shape, const void *x_perm,
+                          const int32_t *offsets, const void *w_gate,
+                          const void *w_up, const void *w_down, void *y_perm,
+                          void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * Stage 4, combine [R section 2.2 step 4; S section 1.1; C section 4].
+ *   y[t] = y_shared[t] + sum_{j=0..K-1} topk_w[t][j] * y_perm[inv_perm[t*K+j]]
+ * accumulated in fp32 (shared term first, then j ascending) and rounded
+ * once to the layer dtype.  y_shared [T][d] may be NULL (no shared expert).
+ * Deterministic: a gather per token, no atomics.
+ */
+moe_status moe_combine(const moe_shape *shape, const void *y_perm,
+                       const int32_t *inv_perm, const float *topk_w,
+                       const void *y_shared, void *y, void *stream);
+
+/*
+ * The whole layer: route, dispatch, routed and shared expert FFN, combine,
+ * enqueued on `stream` with no host synchronisation and no host read of
+ * device data (usable inside CUDA graph capture).  ws_gate/ws_up/ws_down
+ * must be non-NULL iff shape->inter_shared > 0.  bias may be NULL.
+ * Output: y [T][d] in the layer dtype.
+ */
+moe_status moe_forward(const moe_shape *shape, const void *x, const void *w_g,
+                       const float *bias, const void *w_gate, const void *w_up,
+                       const void *w_down, const void *ws_gate,
+                       const void *ws_up, const void *ws_down, void *y,
+                       void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * Reads the device error word of `workspace` (a device pointer passed to a
+ * previous call) into *code_out (a HOST pointer): MOE_OK, MOE_ERR_TIMEOUT or
+ * MOE_ERR_BOUNDS.  Synchronous (a 4-byte device-to-host copy); call it after
+ * the stream that ran the work has been synchronised.
+ */
+moe_status moe_get_device_error(const void *workspace, int32_t *code_out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H */

@@ -127,23 +127,27 @@ def zipf_bias(E: int, seed: int, s: float = ZIPF_S, beta: float = ZIPF_BETA) -> 
     return (-s * beta * torch.log(r)).to(torch.float32)
 
 
-def make_weights(cfg: LayerConfig, device="cpu") -> dict:
-    """Router, routed-expert and shared-expert weights, stored [out][in]."""
+def make_weights(cfg: LayerConfig, device="cpu", only=None) -> dict:
+    """Router, routed-expert and shared-expert weights, stored [out][in].
+
+    ``only`` (a set of names) draws just those tensors; each has its own
+    sub-seed, so the values are the same as in a full draw."""
     d, E, I, Is, dt, sd = cfg.d, cfg.E, cfg.I, cfg.Is, cfg.dtype, cfg.seed
     std_d = 1.0 / math.sqrt(d)
     std_down = 1.0 / math.sqrt(I) if cfg.down_std == "inter" else std_d
-    p = {
-        "w_g": normal((E, d), std_d, dt, device, sd, "w_g"),
-        "w_gate": normal((E, I, d), std_d, dt, device, sd, "w_gate", chunk_dim0=True),
-        "w_up": normal((E, I, d), std_d, dt, device, sd, "w_up", chunk_dim0=True),
-        "w_down": normal((E, d, I), std_down, dt, device, sd, "w_down", chunk_dim0=True),
+    std_sdown = (1.0 / math.sqrt(Is) if cfg.down_std == "inter" else std_d) if Is else 0.0
+    recipe = {
+        "w_g": ((E, d), std_d, False),
+        "w_gate": ((E, I, d), std_d, True),
+        "w_up": ((E, I, d), std_d, True),
+        "w_down": ((E, d, I), std_down, True),
     }
     if Is:
-        std_sdown = 1.0 / math.sqrt(Is) if cfg.down_std == "inter" else std_d
-        p["ws_gate"] = normal((Is, d), std_d, dt, device, sd, "ws_gate")
-        p["ws_up"] = normal((Is, d), std_d, dt, device, sd, "ws_up")
-        p["ws_down"] = normal((d, Is), std_sdown, dt, device, sd, "ws_down")
-    return p
+        recipe["ws_gate"] = ((Is, d), std_d, False)
+        recipe["ws_up"] = ((Is, d), std_d, False)
+        recipe["ws_down"] = ((d, Is), std_sdown, False)
+    return {name: normal(shape, std, dt, device, sd, name, chunk_dim0=chunk)
+            for name, (shape, std, chunk) in recipe.items() if only is None or name in only}
 
 
 def make_x(cfg: LayerConfig, device="cpu", name: str = "x") -> torch.Tensor:

@@ -1,0 +1,162 @@
+"""Python binding of libmoe, the GB300 (sm_103a) sparse MoE FFN layer forward.
+
+Argument marshalling only: every step of the layer runs in the CUDA kernels of
+libmoe.so (built from csrc/ by ``_build.build``).  The functions have the names
+and argument order of the C ABI in include/moe.h; tensors are torch CUDA
+tensors (or None for a NULL pointer), ``stream`` defaults to torch's current
+stream.  A non-OK status raises MoeError.  There is no CPU path: importing the
+binding without the built library raises ImportError.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmoe.so")
+
+MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE = 0, 1, 2, 3
+MOE_ERR_CUDA, MOE_ERR_TIMEOUT, MOE_ERR_BOUNDS = 4, 5, 6
+MOE_F32, MOE_BF16 = 0, 1
+
+EXPORTED = ("moe_status_string", "moe_workspace_bytes", "moe_route", "moe_permute",
+            "moe_expert_ffn", "moe_combine", "moe_forward", "moe_get_device_error")
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+class moe_shape(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int32), ("d", ctypes.c_int32), ("E", ctypes.c_int32),
+                ("K", ctypes.c_int32), ("inter", ctypes.c_int32),
+                ("inter_shared", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+
+
+def _load_lib() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"libmoe.so is not built ({LIB_PATH}); run sparse_expert_ffn_moe_gb300._build.build() "
+            "-- there is no CPU fallback")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, sz, i32 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int32
+    sp = ctypes.POINTER(moe_shape)
+    lib.moe_status_string.argtypes = [i32]
+    lib.moe_status_string.restype = ctypes.c_char_p
+    lib.moe_workspace_bytes.argtypes = [sp]
+    lib.moe_workspace_bytes.restype = sz
+    lib.moe_route.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.moe_permute.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.moe_expert_ffn.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.moe_combine.argtypes = [sp, vp, vp, vp, vp, vp, vp]
+    lib.moe_forward.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.moe_get_device_error.argtypes = [vp, ctypes.POINTER(i32)]
+    for f in ("moe_route", "moe_permute", "moe_expert_ffn", "moe_combine", "moe_forward",
+              "moe_get_device_error"):
+        getattr(lib, f).restype = i32
+    return lib
+
+
+_lib = _load_lib()
+
+
+def library() -> ctypes.CDLL:
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return _lib.moe_status_string(int(status)).decode()
+
+
+def make_shape(T: int, d: int, E: int, K: int, inter: int, inter_shared: int = 0,
+               dtype: str | int = "bf16") -> moe_shape:
+    if isinstance(dtype, str):
+        dtype = {"bf16": MOE_BF16, "f32": MOE_F32}[dtype]
+    return moe_shape(T, d, E, K, inter, inter_shared, dtype)
+
+
+def _p(t):
+    """Device pointer of a tensor (None -> NULL).  Host tensors are refused."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if not t.is_cuda:
+        raise ValueError("libmoe takes device tensors only")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(rc: int, where: str):
+    if rc != MOE_OK:
+        raise MoeError(rc, where)
+
+
+def _ws(workspace):
+    if workspace is None:
+        return None, 0
+    return _p(workspace), workspace.numel() * workspace.element_size()
+
+
+def moe_workspace_bytes(shape: moe_shape) -> int:
+    return int(_lib.moe_workspace_bytes(ctypes.byref(shape)))
+
+
+def alloc_workspace(shape: moe_shape, device=None) -> torch.Tensor:
+    n = moe_workspace_bytes(shape)
+    if n == 0:
+        raise MoeError(MOE_ERR_INVALID_ARG, "moe_workspace_bytes")
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def moe_route(shape, x, w_g, bias, logits_in, logits_out, topk_idx, topk_w, workspace,
+              stream=None):
+    ws, nws = _ws(workspace)
+    _check(_lib.moe_route(ctypes.byref(shape), _p(x), _p(w_g), _p(bias), _p(logits_in),
+                          _p(logits_out), _p(topk_idx), _p(topk_w), ws, nws, _stream(stream)),
+           "moe_route")
+
+
+def moe_permute(shape, topk_idx, x, counts, offsets, perm, inv_perm, x_perm, workspace,
+                stream=None):
+    ws, nws = _ws(workspace)
+    _check(_lib.moe_permute(ctypes.byref(shape), _p(topk_idx), _p(x), _p(counts), _p(offsets),
+                            _p(perm), _p(inv_perm), _p(x_perm), ws, nws, _stream(stream)),
+           "moe_permute")
+
+
+def moe_expert_ffn(shape, x_perm, offsets, w_gate, w_up, w_down, y_perm, workspace, stream=None):
+    ws, nws = _ws(workspace)
+    _check(_lib.moe_expert_ffn(ctypes.byref(shape), _p(x_perm), _p(offsets), _p(w_gate),
+                               _p(w_up), _p(w_down), _p(y_perm), ws, nws, _stream(stream)),
+           "moe_expert_ffn")
+
+
+def moe_combine(shape, y_perm, inv_perm, topk_w, y_shared, y, stream=None):
+    _check(_lib.moe_combine(ctypes.byref(shape), _p(y_perm), _p(inv_perm), _p(topk_w),
+                            _p(y_shared), _p(y), _stream(stream)), "moe_combine")
+
+
+def moe_forward(shape, x, w_g, bias, w_gate, w_up, w_down, ws_gate, ws_up, ws_down, y,
+                workspace, stream=None):
+    ws, nws = _ws(workspace)
+    _check(_lib.moe_forward(ctypes.byref(shape), _p(x), _p(w_g), _p(bias), _p(w_gate), _p(w_up),
+                            _p(w_down), _p(ws_gate), _p(ws_up), _p(ws_down), _p(y), ws, nws,
+                            _stream(stream)), "moe_forward")
+
+
+def moe_get_device_error(workspace) -> int:
+    code = ctypes.c_int32(0)
+    _check(_lib.moe_get_device_error(_p(workspace), ctypes.byref(code)), "moe_get_device_error")
+    return int(code.value)

@@ -1,0 +1,189 @@
+// dispatch.cu -- stage 2: per-expert histogram, exclusive scan, stable
+// permutation and row gather.
+//
+// "Sparse MoE inference kernels ..." (blog.llmgo.top), section 4.3: flatten
+// the [T, K] expert ids, order the slots by expert id, gather the token rows
+// into one contiguous buffer, count tokens per expert and build the offsets a
+// grouped GEMM consumes.  "Computation and Data Movement for Inference",
+// section 15: sorting the routing records by expert lets one weight load serve
+// the whole bucket.  The page's code sorts with an unstable argsort and an
+// inclusive cumsum; here the order is stable by flat slot f = t*K + j and the
+// offsets are exclusive with E+1 entries.
+//
+// Three kernels over chunks of 1024 slots:
+//   hist    -- per-chunk expert histogram (shared-memory atomics; counts only,
+//              so the order of the atomics does not matter)
+//   scan    -- one block: counts, exclusive offsets, and each chunk's base
+//              position per expert (chunk-major running sums)
+//   scatter -- per chunk, the stable rank of every slot among the earlier
+//              slots of its expert: rank inside the warp from __match_any_sync,
+//              plus the exclusive sum over earlier warps of the chunk, plus the
+//              chunk base.  Writes perm, inv_perm and the token of every row.
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kChunk = 1024;  // slots per block (one per thread)
+
+__device__ __forceinline__ bool valid_expert(int e, int E) { return e >= 0 && e < E; }
+
+__global__ void __launch_bounds__(kChunk)
+dispatch_hist_kernel(const int32_t* __restrict__ idx, int64_t n, int E,
+                     int32_t* __restrict__ blk_hist, DevError* err) {
+    extern __shared__ int32_t hist[];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+    __syncthreads();
+    const int64_t f = (int64_t)blockIdx.x * kChunk + threadIdx.x;
+    if (f < n) {
+        const int e = idx[f];
+        if (valid_expert(e, E)) atomicAdd(&hist[e], 1);
+        else record_error(err, MOE_ERR_BOUNDS, 200);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x)
+        blk_hist[(int64_t)blockIdx.x * E + e] = hist[e];
+}
+
+// Exclusive scan of one value per thread over a 1024-thread block.
+__device__ int32_t block_exclusive_scan(int32_t v, int32_t* warp_tot, int32_t* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int32_t incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int32_t w = lane < (int)(blockDim.x >> 5) ? warp_tot[lane] : 0;
+        int32_t wi = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t t = __shfl_up_sync(0xffffffffu, wi, o);
+            if (lane >= o) wi += t;
+        }
+        warp_tot[lane] = wi - w;  // exclusive prefix of warp totals
+        if (lane == 31) *total = wi;
+    }
+    __syncthreads();
+    const int32_t r = warp_tot[warp] + incl - v;
+    __syncthreads();
+    return r;
+}
+
+// one block of 1024 threads; E <= 1024
+__global__ void __launch_bounds__(1024)
+dispatch_scan_kernel(int32_t* __restrict__ blk_hist, int nb, int E, int32_t* __restrict__ counts,
+                     int32_t* __restrict__ offsets) {
+    __shared__ int32_t warp_tot[32];
+    __shared__ int32_t total;
+    const int e = threadIdx.x;
+    int32_t c = 0;
+    if (e < E)
+        for (int b = 0; b < nb; ++b) c += blk_hist[(int64_t)b * E + e];
+    const int32_t off = block_exclusive_scan(e < E ? c : 0, warp_tot, &total);
+    if (e < E) {
+        counts[e] = c;
+        offsets[e] = off;
+        int32_t run = off;
+        for (int b = 0; b < nb; ++b) {
+            const int32_t t = blk_hist[(int64_t)b * E + e];
+            blk_hist[(int64_t)b * E + e] = run;  // base position of chunk b for expert e
+            run += t;
+        }
+    }
+    if (threadIdx.x == 0) offsets[E] = total;
+}
+
+__global__ void __launch_bounds__(kChunk)
+dispatch_scatter_kernel(const int32_t* __restrict__ idx, int64_t n, int E, int K,
+                        const int32_t* __restrict__ blk_base, int32_t* __restrict__ perm,
+                        int32_t* __restrict__ inv_perm, int32_t* __restrict__ tok_of) {
+    extern __shared__ int32_t wcnt[];  // [32 warps][E]: counts, then exclusive prefix over warps
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int i = threadIdx.x; i < 32 * E; i += blockDim.x) wcnt[i] = 0;
+    __syncthreads();
+    const int64_t f = (int64_t)blockIdx.x * kChunk + threadIdx.x;
+    int e = f < n ? idx[f] : -1;
+    if (!valid_expert(e, E)) e = -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    if (e >= 0 && rank == 0) wcnt[warp * E + e] = __popc(peers);
+    __syncthreads();
+    for (int x = threadIdx.x; x < E; x += blockDim.x) {
+        int32_t run = 0;
+        for (int w = 0; w < 32; ++w) {
+            const int32_t t = wcnt[w * E + x];
+            wcnt[w * E + x] = run;
+            run += t;
+        }
+    }
+    __syncthreads();
+    if (f < n) {
+        if (e >= 0) {
+            const int32_t p = blk_base[(int64_t)blockIdx.x * E + e] + wcnt[warp * E + e] + rank;
+            if (perm) perm[p] = (int32_t)f;
+            inv_perm[f] = p;
+            tok_of[p] = (int32_t)(f / K);
+        } else {
+            inv_perm[f] = -1;  // dropped slot (out-of-range expert id)
+        }
+    }
+}
+
+template <int V>
+__global__ void __launch_bounds__(256)
+gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ tok_of,
+                   uint4* __restrict__ x_perm, int64_t rows, int vec_per_row, int Tn) {
+    const int lane = threadIdx.x & 31;
+    for (int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); r < rows;
+         r += (int64_t)gridDim.x * 8) {
+        const int t = tok_of[r];
+        if (t < 0 || t >= Tn) continue;
+        const uint4* src = x + (int64_t)t * vec_per_row;
+        uint4* dst = x_perm + r * vec_per_row;
+        for (int v = lane; v < vec_per_row; v += 32) dst[v] = __ldg(src + v);
+    }
+}
+
+}  // namespace
+
+int dispatch_blocks_for(int64_t n_slots) { return (int)ceil_div(n_slots > 0 ? n_slots : 1, kChunk); }
+
+cudaError_t launch_dispatch(const moe_shape& s, const int32_t* topk_idx, int32_t* counts,
+                            int32_t* offsets, int32_t* perm, int32_t* inv_perm, int32_t* tok_of,
+                            int32_t* blk_hist, DevError* err, cudaStream_t st) {
+    const int64_t n = (int64_t)s.T * s.K;
+    const int nb = dispatch_blocks_for(n);
+    const size_t hist_smem = (size_t)s.E * sizeof(int32_t);
+    const size_t scat_smem = (size_t)32 * s.E * sizeof(int32_t);
+    // the scatter kernel's per-warp table needs up to 128 KB of shared memory
+    cudaError_t ae = cudaFuncSetAttribute(dispatch_scatter_kernel,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          (int)(32 * 1024 * sizeof(int32_t)));
+    if (ae != cudaSuccess) return ae;
+    dispatch_hist_kernel<<<nb, kChunk, hist_smem, st>>>(topk_idx, n, s.E, blk_hist, err);
+    dispatch_scan_kernel<<<1, 1024, 0, st>>>(blk_hist, nb, s.E, counts, offsets);
+    dispatch_scatter_kernel<<<nb, kChunk, scat_smem, st>>>(topk_idx, n, s.E, s.K, blk_hist, perm,
+                                                           inv_perm, tok_of);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gather_rows(const moe_shape& s, const void* x, const int32_t* tok_of,
+                               void* x_perm, cudaStream_t st) {
+    const int64_t rows = (int64_t)s.T * s.K;
+    const int esz = s.dtype == MOE_BF16 ? 2 : 4;
+    const int vpr = s.d * esz / 16;
+    int64_t blocks = ceil_div(rows, 8);
+    const int64_t cap = (int64_t)device_sm_count() * 8;
+    if (blocks > cap) blocks = cap;
+    gather_rows_kernel<1><<<(unsigned)blocks, 256, 0, st>>>((const uint4*)x, tok_of, (uint4*)x_perm,
+                                                            rows, vpr, s.T);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

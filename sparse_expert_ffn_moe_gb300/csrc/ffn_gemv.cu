@@ -1,0 +1,336 @@
+// ffn_gemv.cu -- stage 3 for groups with few rows: the SwiGLU expert FFN as a
+// weight-streaming GEMV, plus the device-side work plan for stage 3.
+//
+// "Sparse MoE inference kernels ..." (blog.llmgo.top), section 1.2: in decode
+// an expert gets ~0.25 tokens on average, so its W_gate, W_up and W_down are
+// loaded from HBM to multiply one or two vectors -- the work is a GEMV bound
+// by memory bandwidth; FAQ Q1: experts with zero tokens are skipped.
+// "Computation and Data Movement for Inference", section 16: decode experts
+// share little, so what matters is streaming each selected expert once.
+//
+// Plan kernel (one block): from offsets[], split the groups (routed experts
+// and the shared expert) into those with 1..limit rows (GEMV list) and those
+// with more (list of 128-row tiles for the tensor-core GEMM).  Nothing on the
+// host reads the counts.
+//
+// GEMV kernels: a work unit is (group, block of output rows).  The unit's
+// activation rows (up to MT of them at a time) are staged in shared memory;
+// each warp streams whole weight rows with 16-byte non-allocating loads,
+// several in flight per lane, and reduces with shuffles.  Gate and up rows of
+// the same index are streamed together so SiLU(g) * u is formed in registers.
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
+constexpr int kRowsGU = 16;   // gate/up output rows per unit (2 per warp)
+constexpr int kRowsDown = 16; // down output rows per unit
+constexpr int kTileM = 128;   // rows per tensor-core tile
+
+__device__ int32_t scan_1024(int32_t v, int32_t* sh, int32_t* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int32_t incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+    }
+    if (lane == 31) sh[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const int32_t w = lane < (int)(blockDim.x >> 5) ? sh[lane] : 0;
+        int32_t wi = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t t = __shfl_up_sync(0xffffffffu, wi, o);
+            if (lane >= o) wi += t;
+        }
+        sh[lane] = wi - w;
+        if (lane == 31) *total = wi;
+    }
+    __syncthreads();
+    const int32_t r = sh[warp] + incl - v;
+    __syncthreads();
+    return r;
+}
+
+// groups: E routed (+1 shared).  One block of 1024 threads, two groups per thread.
+__global__ void __launch_bounds__(1024)
+ffn_plan_kernel(const int32_t* __restrict__ offsets, int E, int has_shared, int T, int limit,
+                FfnPlanHeader* __restrict__ hdr, int32_t* __restrict__ gemv_list,
+                int4* __restrict__ mtile_list, int max_mtiles) {
+    __shared__ int32_t sh[32];
+    __shared__ int32_t tot_g, tot_t, base_g, base_t;
+    if (threadIdx.x == 0) { base_g = 0; base_t = 0; }
+    __syncthreads();
+    const int G = E + (has_shared ? 1 : 0);
+    for (int g0 = 0; g0 < G; g0 += blockDim.x) {
+        const int g = g0 + threadIdx.x;
+        int32_t rows = 0, row0 = 0;
+        if (g < E) { row0 = offsets[g]; rows = offsets[g + 1] - row0; }
+        else if (g < G) { row0 = 0; rows = T; }
+        const bool to_gemv = rows > 0 && rows <= limit;
+        const int32_t tiles = (rows > limit) ? (rows + kTileM - 1) / kTileM : 0;
+        const int32_t pg = scan_1024(to_gemv ? 1 : 0, sh, &tot_g);
+        const int32_t pt = scan_1024(tiles, sh, &tot_t);
+        if (to_gemv) gemv_list[base_g + pg] = g;
+        for (int32_t i = 0; i < tiles; ++i) {
+            const int32_t slot = base_t + pt + i;
+            // (group, first row of the group, rows of the group, index of this m-tile)
+            if (slot < max_mtiles) mtile_list[slot] = make_int4(g, row0, rows, i);
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) { base_g += tot_g; base_t += tot_t; }
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        hdr->n_gemv = base_g;
+        hdr->n_mtiles = min(base_t, max_mtiles);
+    }
+}
+
+struct GroupView {
+    int rows;          // rows of this group
+    int inter;         // intermediate size
+    int64_t row0;      // first row in the routed row space (or 0 for shared)
+    bool shared;
+    const void *wg, *wu, *wd;
+};
+
+template <typename T>
+__device__ __forceinline__ GroupView group_view(const FfnGroups& g, int grp) {
+    GroupView v;
+    if (grp < g.E) {
+        const int32_t o0 = g.offsets[grp];
+        v.rows = g.offsets[grp + 1] - o0;
+        v.row0 = o0;
+        v.inter = g.I;
+        v.shared = false;
+        const int64_t wgu = (int64_t)grp * g.I * g.d;
+        v.wg = (const T*)g.w_gate + wgu;
+        v.wu = (const T*)g.w_up + wgu;
+        v.wd = (const T*)g.w_down + wgu;  // [E][d][I]: same stride d*I
+    } else {
+        v.rows = g.T;
+        v.row0 = 0;
+        v.inter = g.Is;
+        v.shared = true;
+        v.wg = g.ws_gate;
+        v.wu = g.ws_up;
+        v.wd = g.ws_down;
+    }
+    return v;
+}
+
+// h = SiLU(Wg x) * (Wu x) for a block of kRowsGU intermediate rows.
+template <typename T, int MT, int U>
+__global__ void __launch_bounds__(kThreads)
+gemv_gate_up_kernel(FfnGroups g, const FfnPlanHeader* __restrict__ hdr,
+                    const int32_t* __restrict__ gemv_list) {
+    constexpr int V = Elem<T>::kPerVec;
+    extern __shared__ uint4 xs[];  // [MT][d / V]
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nvec = g.d / V;
+    const int n_groups = hdr->n_gemv;
+    const int max_inter = g.has_shared && g.Is > g.I ? g.Is : g.I;
+    const int nrb = (max_inter + kRowsGU - 1) / kRowsGU;
+    const int64_t units = (int64_t)n_groups * nrb;
+    for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
+        const int a = (int)(u / nrb), rb = (int)(u % nrb);
+        const GroupView gv = group_view<T>(g, gemv_list[a]);
+        if (rb * kRowsGU >= gv.inter) continue;  // uniform across the block
+        for (int c0 = 0; c0 < gv.rows; c0 += MT) {
+            const int nt = min(MT, gv.rows - c0);
+            __syncthreads();  // previous readers of xs are done
+            for (int i = threadIdx.x; i < nt * nvec; i += kThreads) {
+                const int m = i / nvec, v = i - m * nvec;
+                int64_t src_row;
+                const T* base;
+                if (gv.shared) { src_row = c0 + m; base = (const T*)g.a_shared; }
+                else {
+                    const int64_t p = gv.row0 + c0 + m;
+                    src_row = g.row_src ? g.row_src[p] : p;
+                    base = (const T*)g.a_routed;
+                }
+                xs[m * nvec + v] = ld_ro(base + src_row * g.d + (int64_t)v * V);
+            }
+            __syncthreads();
+            for (int r = warp; r < kRowsGU; r += kWarps) {
+                const int i = rb * kRowsGU + r;
+                if (i >= gv.inter) break;
+                const T* wg = (const T*)gv.wg + (int64_t)i * g.d;
+                const T* wu = (const T*)gv.wu + (int64_t)i * g.d;
+                float ag[MT], au[MT];
+#pragma unroll
+                for (int m = 0; m < MT; ++m) { ag[m] = 0.f; au[m] = 0.f; }
+                for (int v0 = lane; v0 < nvec; v0 += 32 * U) {
+                    uint4 rg[U], ru[U];
+#pragma unroll
+                    for (int q = 0; q < U; ++q) {
+                        const int v = v0 + 32 * q;
+                        if (v < nvec) {
+                            rg[q] = ld_stream(wg + (int64_t)v * V);
+                            ru[q] = ld_stream(wu + (int64_t)v * V);
+                        }
+                    }
+#pragma unroll
+                    for (int q = 0; q < U; ++q) {
+                        const int v = v0 + 32 * q;
+                        if (v < nvec) {
+                            float fg[V], fu[V];
+                            unpack(rg[q], fg, (const T*)nullptr);
+                            unpack(ru[q], fu, (const T*)nullptr);
+#pragma unroll
+                            for (int m = 0; m < MT; ++m) {
+                                if (m < nt) {
+                                    float fx[V];
+                                    unpack(xs[m * nvec + v], fx, (const T*)nullptr);
+#pragma unroll
+                                    for (int k = 0; k < V; ++k) {
+                                        ag[m] = fmaf(fg[k], fx[k], ag[m]);
+                                        au[m] = fmaf(fu[k], fx[k], au[m]);
+                                    }
+                                }
+                            }
+                        }
+                    }
+                }
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    const float sg = warp_sum(ag[m]);
+                    const float su = warp_sum(au[m]);
+                    if (lane == m && m < nt) {
+                        const T hv = Elem<T>::from_f32(silu_mul(sg, su));
+                        if (gv.shared) ((T*)g.h_s)[(int64_t)(c0 + m) * gv.inter + i] = hv;
+                        else ((T*)g.h)[(gv.row0 + c0 + m) * gv.inter + i] = hv;
+                    }
+                }
+            }
+        }
+    }
+}
+
+// y = Wd h for a block of kRowsDown output rows.
+template <typename T, int MT, int U>
+__global__ void __launch_bounds__(kThreads)
+gemv_down_kernel(FfnGroups g, const FfnPlanHeader* __restrict__ hdr,
+                 const int32_t* __restrict__ gemv_list) {
+    constexpr int V = Elem<T>::kPerVec;
+    extern __shared__ uint4 hs[];  // [MT][inter / V]
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int n_groups = hdr->n_gemv;
+    const int nrb = (g.d + kRowsDown - 1) / kRowsDown;
+    const int64_t units = (int64_t)n_groups * nrb;
+    for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
+        const int a = (int)(u / nrb), rb = (int)(u % nrb);
+        const GroupView gv = group_view<T>(g, gemv_list[a]);
+        const int nvec = gv.inter / V;
+        for (int c0 = 0; c0 < gv.rows; c0 += MT) {
+            const int nt = min(MT, gv.rows - c0);
+            __syncthreads();
+            for (int i = threadIdx.x; i < nt * nvec; i += kThreads) {
+                const int m = i / nvec, v = i - m * nvec;
+                const T* src = gv.shared ? (const T*)g.h_s + (int64_t)(c0 + m) * gv.inter
+                                         : (const T*)g.h + (gv.row0 + c0 + m) * gv.inter;
+                hs[m * nvec + v] = ld_ro(src + (int64_t)v * V);
+            }
+            __syncthreads();
+            for (int r = warp; r < kRowsDown; r += kWarps) {
+                const int j = rb * kRowsDown + r;
+                if (j >= g.d) break;
+                const T* wd = (const T*)gv.wd + (int64_t)j * gv.inter;
+                float acc[MT];
+#pragma unroll
+                for (int m = 0; m < MT; ++m) acc[m] = 0.f;
+                for (int v0 = lane; v0 < nvec; v0 += 32 * U) {
+                    uint4 rw[U];
+#pragma unroll
+                    for (int q = 0; q < U; ++q) {
+                        const int v = v0 + 32 * q;
+                        if (v < nvec) rw[q] = ld_stream(wd + (int64_t)v * V);
+                    }
+#pragma unroll
+                    for (int q = 0; q < U; ++q) {
+                        const int v = v0 + 32 * q;
+                        if (v < nvec) {
+                            float fw[V];
+                            unpack(rw[q], fw, (const T*)nullptr);
+#pragma unroll
+                            for (int m = 0; m < MT; ++m) {
+                                if (m < nt) {
+                                    float fh[V];
+                                    unpack(hs[m * nvec + v], fh, (const T*)nullptr);
+#pragma unroll
+                                    for (int k = 0; k < V; ++k) acc[m] = fmaf(fw[k], fh[k], acc[m]);
+                                }
+                            }
+                        }
+                    }
+                }
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    const float s = warp_sum(acc[m]);
+                    if (lane == m && m < nt) {
+                        const T yv = Elem<T>::from_f32(s);
+                        if (gv.shared) ((T*)g.y_s)[(int64_t)(c0 + m) * g.d + j] = yv;
+                        else ((T*)g.y)[(gv.row0 + c0 + m) * g.d + j] = yv;
+                    }
+                }
+            }
+        }
+    }
+}
+
+template <typename T, int MT, int U>
+cudaError_t launch_gemv_t(const FfnGroups& g, const FfnPlanHeader* hdr, const int32_t* list,
+                          cudaStream_t st) {
+    const int max_inter = g.has_shared && g.Is > g.I ? g.Is : g.I;
+    const size_t smem_gu = (size_t)MT * g.d * sizeof(T);
+    const size_t smem_dn = (size_t)MT * max_inter * sizeof(T);
+    cudaError_t e;
+    e = cudaFuncSetAttribute(gemv_gate_up_kernel<T, MT, U>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_gu);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(gemv_down_kernel<T, MT, U>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_dn);
+    if (e != cudaSuccess) return e;
+    int occ_gu = 1, occ_dn = 1;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_gu, gemv_gate_up_kernel<T, MT, U>, kThreads,
+                                                  smem_gu);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_dn, gemv_down_kernel<T, MT, U>, kThreads,
+                                                  smem_dn);
+    const int sms = device_sm_count();
+    gemv_gate_up_kernel<T, MT, U><<<sms * (occ_gu > 0 ? occ_gu : 1), kThreads, smem_gu, st>>>(g, hdr, list);
+    gemv_down_kernel<T, MT, U><<<sms * (occ_dn > 0 ? occ_dn : 1), kThreads, smem_dn, st>>>(g, hdr, list);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+// Read on every call so a process can compare both paths on the same inputs.
+int gemv_max_rows() {
+    const char* s = getenv("MOE_GEMV_MAX_ROWS");
+    const int x = s ? atoi(s) : 16;
+    return x < 0 ? 0 : x;
+}
+
+cudaError_t launch_ffn_plan(const FfnGroups& g, int dtype, FfnPlanHeader* hdr, int32_t* gemv_list,
+                            int4* mtile_list, int max_mtiles, int gemv_limit, cudaStream_t st) {
+    // fp32 layers never use the tensor cores (no TF32): every group streams
+    const int limit = dtype == MOE_F32 ? 0x7fffffff : gemv_limit;
+    ffn_plan_kernel<<<1, 1024, 0, st>>>(g.offsets, g.E, g.has_shared, g.T, limit, hdr, gemv_list,
+                                        mtile_list, max_mtiles);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_ffn_gemv(const FfnGroups& g, int dtype, const FfnPlanHeader* hdr,
+                            const int32_t* gemv_list, cudaStream_t st) {
+    if (dtype == MOE_BF16) return launch_gemv_t<bf16, 4, 4>(g, hdr, gemv_list, st);
+    return launch_gemv_t<float, 2, 4>(g, hdr, gemv_list, st);
+}
+
+}  // namespace moe

@@ -1,0 +1,94 @@
+// internal.h -- host-side interfaces between the C-ABI layer (moe_api.cu) and
+// the kernel files.  Not installed; not part of the ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "moe.h"
+
+namespace moe {
+
+struct DevError;
+
+// Device-built work plan for the grouped expert FFN.  Group g < E is routed
+// expert g with rows [offsets[g], offsets[g+1]) of the permuted row space;
+// group E (when present) is the shared expert, whose rows are the T tokens.
+struct FfnPlanHeader {
+    int32_t n_gemv;    // groups handled by the streaming GEMV kernels
+    int32_t n_mtiles;  // 128-row tiles handled by the tensor-core GEMM
+    int32_t pad[2];
+};
+
+// One routed/shared expert group as the FFN kernels see it.
+struct FfnGroups {
+    int E;             // routed experts (group E = shared, if has_shared)
+    int has_shared;
+    int d;             // hidden size
+    int I, Is;         // intermediate sizes (routed, shared)
+    int n_routed_rows; // T*K (rows of x_perm / h / y_perm)
+    int T;             // tokens (rows of the shared group)
+    const int32_t* offsets;  // [E+1] device
+    const int32_t* row_src;  // [n_routed_rows] token of each routed row, or
+                             // null: routed row p reads A row p directly
+    const void* a_routed;    // rows of x_perm (or x when row_src is set)
+    const void* a_shared;    // x [T][d] (shared group input)
+    const void* w_gate;      // [E][I][d]
+    const void* w_up;
+    const void* w_down;      // [E][d][I]
+    const void* ws_gate;     // [Is][d]
+    const void* ws_up;
+    const void* ws_down;     // [d][Is]
+    void* h;                 // [n_routed_rows][I]
+    void* h_s;               // [T][Is]
+    void* y;                 // [n_routed_rows][d]
+    void* y_s;               // [T][d]
+};
+
+// Workspace carving (all offsets 256-byte aligned).
+struct WsLayout {
+    size_t err, router_part, logits, topk_idx, topk_w, counts, offsets, perm, inv_perm,
+        tok_of, blk_hist, plan, gemv_list, mtile_list, x_perm, h, h_s, y_perm, y_s, total;
+    int router_splits, dispatch_blocks, max_mtiles;
+};
+WsLayout ws_layout(const moe_shape& s);
+
+// ---- router.cu ----
+int router_splits_for(const moe_shape& s);
+cudaError_t launch_router_gemv(const moe_shape& s, const void* x, const void* w_g, float* part,
+                               int splits, cudaStream_t st);
+cudaError_t launch_topk_softmax(const moe_shape& s, const float* part, int splits,
+                                const float* bias, float* logits_out, int32_t* topk_idx,
+                                float* topk_w, cudaStream_t st);
+
+// ---- dispatch.cu ----
+int dispatch_blocks_for(int64_t n_slots);
+cudaError_t launch_dispatch(const moe_shape& s, const int32_t* topk_idx, int32_t* counts,
+                            int32_t* offsets, int32_t* perm, int32_t* inv_perm, int32_t* tok_of,
+                            int32_t* blk_hist, DevError* err, cudaStream_t st);
+cudaError_t launch_gather_rows(const moe_shape& s, const void* x, const int32_t* tok_of,
+                               void* x_perm, cudaStream_t st);
+
+// ---- ffn_plan + ffn_gemv.cu ----
+int gemv_max_rows();  // groups with at most this many rows take the GEMV path
+cudaError_t launch_ffn_plan(const FfnGroups& g, int dtype, FfnPlanHeader* hdr,
+                            int32_t* gemv_list, int4* mtile_list, int max_mtiles,
+                            int gemv_limit, cudaStream_t st);
+cudaError_t launch_ffn_gemv(const FfnGroups& g, int dtype, const FfnPlanHeader* hdr,
+                            const int32_t* gemv_list, cudaStream_t st);
+
+// ---- ffn_tc.cu (tcgen05 grouped GEMM) ----
+bool tc_available();
+cudaError_t launch_ffn_tc(const FfnGroups& g, const FfnPlanHeader* hdr, const int4* mtile_list,
+                          int max_mtiles, DevError* err, cudaStream_t st);
+cudaError_t launch_router_tc(const moe_shape& s, const void* x, const void* w_g, float* scores,
+                             DevError* err, cudaStream_t st);
+
+// ---- combine.cu ----
+cudaError_t launch_combine(const moe_shape& s, const void* y_perm, const int32_t* inv_perm,
+                           const float* topk_w, const void* y_shared, void* y, cudaStream_t st);
+
+int device_sm_count();
+
+}  // namespace moe

@@ -1,0 +1,359 @@
+// moe_api.cu -- the C ABI declared in include/moe.h: argument checks,
+// workspace carving and the launch sequence of each stage.  Host code only;
+// the kernels live in router.cu, dispatch.cu, ffn_gemv.cu, ffn_tc.cu and
+// combine.cu.  No entry point allocates, frees or synchronises (except
+// moe_get_device_error, which is documented as synchronous).
+#include <stdint.h>
+#include <stdlib.h>
+
+#include <atomic>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+namespace {
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sm_count[kMaxDevices];
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+moe_status check_shape(const moe_shape* s) {
+    if (!s) return MOE_ERR_INVALID_ARG;
+    if (s->T < 0 || s->d <= 0 || s->E <= 0 || s->K <= 0 || s->inter <= 0 || s->inter_shared < 0)
+        return MOE_ERR_INVALID_ARG;
+    if (s->K > s->E) return MOE_ERR_INVALID_ARG;
+    if (s->dtype != MOE_F32 && s->dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+    if (s->K > 32 || s->E > 1024) return MOE_ERR_UNSUPPORTED;
+    if (s->d % 64 || s->inter % 64 || s->inter_shared % 64) return MOE_ERR_UNSUPPORTED;
+    if (s->d > 16384 || s->inter > 16384 || s->inter_shared > 16384) return MOE_ERR_UNSUPPORTED;
+    if ((int64_t)s->T * s->K >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+
+size_t esize(const moe_shape& s) { return s.dtype == MOE_BF16 ? 2 : 4; }
+
+moe_status check_ws(const moe_shape& s, const void* ws, size_t bytes) {
+    if (!ws || !aligned16(ws)) return MOE_ERR_WORKSPACE;
+    if (bytes < ws_layout(s).total) return MOE_ERR_WORKSPACE;
+    return MOE_OK;
+}
+
+moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+template <typename P>
+P* at(void* ws, size_t off) {
+    return reinterpret_cast<P*>(static_cast<uint8_t*>(ws) + off);
+}
+
+// Groups whose row count exceeds this take the tensor-core path.
+int gemv_limit() { return gemv_max_rows(); }
+
+bool use_tc_router(const moe_shape& s) {
+    return s.dtype == MOE_BF16 && s.T >= 128 && s.E >= 64;
+}
+
+}  // namespace
+
+int device_sm_count() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 1;
+    if (dev >= kMaxDevices) {
+        int n = 1;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        return n > 0 ? n : 1;
+    }
+    int n = g_sm_count[dev].load(std::memory_order_relaxed);
+    if (n <= 0) {
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (n <= 0) n = 1;
+        g_sm_count[dev].store(n, std::memory_order_relaxed);
+    }
+    return n;
+}
+
+WsLayout ws_layout(const moe_shape& s) {
+    WsLayout L{};
+    const int64_t T = s.T, E = s.E, K = s.K, d = s.d, I = s.inter, Is = s.inter_shared;
+    const int64_t n = T * K;
+    const size_t es = esize(s);
+    L.router_splits = router_splits_for(s);
+    L.dispatch_blocks = dispatch_blocks_for(n);
+    L.max_mtiles = (int)(n / 128 + E + T / 128 + 2);
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at_ = o;
+        o = align_up(o + (bytes ? bytes : 1));
+        return at_;
+    };
+    L.err = take(sizeof(DevError));
+    L.router_part = take(sizeof(float) * (size_t)(L.router_splits > 1 ? L.router_splits : 1) * T * E);
+    L.logits = 0;
+    L.topk_idx = take(sizeof(int32_t) * n);
+    L.topk_w = take(sizeof(float) * n);
+    L.counts = take(sizeof(int32_t) * (E + 1));
+    L.offsets = take(sizeof(int32_t) * (E + 2));
+    L.perm = take(sizeof(int32_t) * n);
+    L.inv_perm = take(sizeof(int32_t) * n);
+    L.tok_of = take(sizeof(int32_t) * n);
+    L.blk_hist = take(sizeof(int32_t) * (size_t)L.dispatch_blocks * E);
+    L.plan = take(sizeof(FfnPlanHeader));
+    L.gemv_list = take(sizeof(int32_t) * (E + 1));
+    L.mtile_list = take(sizeof(int4) * (size_t)L.max_mtiles);
+    L.x_perm = take(es * n * d);
+    L.h = take(es * n * I);
+    L.h_s = take(es * T * Is);
+    L.y_perm = take(es * n * d);
+    L.y_s = take(es * T * d);
+    L.total = o;
+    return L;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+const char* moe_status_string(int32_t status) {
+    switch (status) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_INVALID_ARG: return "invalid argument";
+        case MOE_ERR_UNSUPPORTED: return "unsupported shape or device";
+        case MOE_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+        case MOE_ERR_CUDA: return "CUDA error";
+        case MOE_ERR_TIMEOUT: return "device wait timed out";
+        case MOE_ERR_BOUNDS: return "index out of range on the device";
+        default: return "unknown status";
+    }
+}
+
+size_t moe_workspace_bytes(const moe_shape* shape) {
+    if (check_shape(shape) != MOE_OK) return 0;
+    return ws_layout(*shape).total;
+}
+
+moe_status moe_route(const moe_shape* shape, const void* x, const void* w_g, const float* bias,
+                     const float* logits_in, float* logits_out, int32_t* topk_idx, float* topk_w,
+                     void* workspace, size_t ws_bytes, void* stream) {
+    moe_status st = check_shape(shape);
+    if (st != MOE_OK) return st;
+    const moe_shape& s = *shape;
+    if (!topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
+    if (!logits_in && (!x || !w_g)) return MOE_ERR_INVALID_ARG;
+    if ((x && !aligned16(x)) || (w_g && !aligned16(w_g))) return MOE_ERR_INVALID_ARG;
+    if ((st = check_ws(s, workspace, ws_bytes)) != MOE_OK) return st;
+    if (s.T == 0) return MOE_OK;
+    cudaStream_t cs = (cudaStream_t)stream;
+    const WsLayout L = ws_layout(s);
+    DevError* err = at<DevError>(workspace, L.err);
+    cudaError_t e = cudaMemsetAsync(err, 0, sizeof(DevError), cs);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    if (logits_in)
+        return cuda_status(launch_topk_softmax(s, logits_in, 1, nullptr, logits_out, topk_idx, topk_w, cs));
+    float* part = at<float>(workspace, L.router_part);
+    int splits = L.router_splits;
+    if (use_tc_router(s) && tc_available()) {
+        e = launch_router_tc(s, x, w_g, part, err, cs);
+        splits = 1;
+    } else {
+        e = launch_router_gemv(s, x, w_g, part, splits, cs);
+    }
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    return cuda_status(launch_topk_softmax(s, part, splits, bias, logits_out, topk_idx, topk_w, cs));
+}
+
+moe_status moe_permute(const moe_shape* shape, const int32_t* topk_idx, const void* x,
+                       int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv_perm,
+                       void* x_perm, void* workspace, size_t ws_bytes, void* stream) {
+    moe_status st = check_shape(shape);
+    if (st != MOE_OK) return st;
+    const moe_shape& s = *shape;
+    if (!topk_idx || !counts || !offsets) return MOE_ERR_INVALID_ARG;
+    if ((x && !aligned16(x)) || (x_perm && !aligned16(x_perm))) return MOE_ERR_INVALID_ARG;
+    if ((st = check_ws(s, workspace, ws_bytes)) != MOE_OK) return st;
+    cudaStream_t cs = (cudaStream_t)stream;
+    const WsLayout L = ws_layout(s);
+    DevError* err = at<DevError>(workspace, L.err);
+    cudaError_t e = cudaMemsetAsync(err, 0, sizeof(DevError), cs);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    if (s.T == 0) {
+        // no slots: every count is zero and every offset is zero
+        e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * s.E, cs);
+        if (e == cudaSuccess) e = cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (s.E + 1), cs);
+        return cuda_status(e);
+    }
+    int32_t* inv = inv_perm ? inv_perm : at<int32_t>(workspace, L.inv_perm);
+    int32_t* tok = at<int32_t>(workspace, L.tok_of);
+    e = launch_dispatch(s, topk_idx, counts, offsets, perm, inv, tok, at<int32_t>(workspace, L.blk_hist),
+                        err, cs);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    if (x && x_perm) e = launch_gather_rows(s, x, tok, x_perm, cs);
+    return cuda_status(e);
+}
+
+moe_status moe_expert_ffn(const moe_shape* shape, const void* x_perm, const int32_t* offsets,
+                          const void* w_gate, const void* w_up, const void* w_down, void* y_perm,
+                          void* workspace, size_t ws_bytes, void* stream) {
+    moe_status st = check_shape(shape);
+    if (st != MOE_OK) return st;
+    const moe_shape& s = *shape;
+    if (!x_perm || !offsets || !w_gate || !w_up || !w_down || !y_perm) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x_perm) || !aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down) ||
+        !aligned16(y_perm))
+        return MOE_ERR_INVALID_ARG;
+    if ((st = check_ws(s, workspace, ws_bytes)) != MOE_OK) return st;
+    if (s.T == 0) return MOE_OK;
+    const int64_t rows = (int64_t)s.T * s.K;
+    const bool need_tc = s.dtype == MOE_BF16 && rows > gemv_limit();
+    if (need_tc && !tc_available()) return MOE_ERR_UNSUPPORTED;
+    cudaStream_t cs = (cudaStream_t)stream;
+    const WsLayout L = ws_layout(s);
+    DevError* err = at<DevError>(workspace, L.err);
+    cudaError_t e = cudaMemsetAsync(err, 0, sizeof(DevError), cs);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    FfnGroups g{};
+    g.E = s.E;
+    g.has_shared = 0;
+    g.d = s.d;
+    g.I = s.inter;
+    g.Is = 0;
+    g.n_routed_rows = (int)rows;
+    g.T = s.T;
+    g.offsets = offsets;
+    g.row_src = nullptr;
+    g.a_routed = x_perm;
+    g.a_shared = x_perm;
+    g.w_gate = w_gate;
+    g.w_up = w_up;
+    g.w_down = w_down;
+    g.h = at<void>(workspace, L.h);
+    g.h_s = nullptr;
+    g.y = y_perm;
+    g.y_s = nullptr;
+    FfnPlanHeader* hdr = at<FfnPlanHeader>(workspace, L.plan);
+    int32_t* glist = at<int32_t>(workspace, L.gemv_list);
+    int4* mtiles = at<int4>(workspace, L.mtile_list);
+    e = launch_ffn_plan(g, s.dtype, hdr, glist, mtiles, L.max_mtiles, gemv_limit(), cs);
+    if (e == cudaSuccess) e = launch_ffn_gemv(g, s.dtype, hdr, glist, cs);
+    if (e == cudaSuccess && need_tc) e = launch_ffn_tc(g, hdr, mtiles, L.max_mtiles, err, cs);
+    return cuda_status(e);
+}
+
+moe_status moe_combine(const moe_shape* shape, const void* y_perm, const int32_t* inv_perm,
+                       const float* topk_w, const void* y_shared, void* y, void* stream) {
+    moe_status st = check_shape(shape);
+    if (st != MOE_OK) return st;
+    const moe_shape& s = *shape;
+    if (!y_perm || !inv_perm || !topk_w || !y) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(y_perm) || !aligned16(y) || (y_shared && !aligned16(y_shared)))
+        return MOE_ERR_INVALID_ARG;
+    if (s.T == 0) return MOE_OK;
+    return cuda_status(launch_combine(s, y_perm, inv_perm, topk_w, y_shared, y, (cudaStream_t)stream));
+}
+
+moe_status moe_forward(const moe_shape* shape, const void* x, const void* w_g, const float* bias,
+                       const void* w_gate, const void* w_up, const void* w_down,
+                       const void* ws_gate, const void* ws_up, const void* ws_down, void* y,
+                       void* workspace, size_t ws_bytes, void* stream) {
+    moe_status st = check_shape(shape);
+    if (st != MOE_OK) return st;
+    const moe_shape& s = *shape;
+    if (!x || !w_g || !w_gate || !w_up || !w_down || !y) return MOE_ERR_INVALID_ARG;
+    const bool shared = s.inter_shared > 0;
+    if (shared != (ws_gate && ws_up && ws_down)) return MOE_ERR_INVALID_ARG;
+    if (shared && (ws_gate == nullptr || ws_up == nullptr || ws_down == nullptr)) return MOE_ERR_INVALID_ARG;
+    const void* ptrs[] = {x, w_g, w_gate, w_up, w_down, y};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return MOE_ERR_INVALID_ARG;
+    if (shared && (!aligned16(ws_gate) || !aligned16(ws_up) || !aligned16(ws_down)))
+        return MOE_ERR_INVALID_ARG;
+    if ((st = check_ws(s, workspace, ws_bytes)) != MOE_OK) return st;
+    if (s.T == 0) return MOE_OK;
+    const bool need_tc = s.dtype == MOE_BF16 && s.T > gemv_limit();
+    if (need_tc && !tc_available()) return MOE_ERR_UNSUPPORTED;
+    cudaStream_t cs = (cudaStream_t)stream;
+    const WsLayout L = ws_layout(s);
+    DevError* err = at<DevError>(workspace, L.err);
+    cudaError_t e = cudaMemsetAsync(err, 0, sizeof(DevError), cs);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+
+    // 1. router scores, top-K, softmax over the K
+    float* part = at<float>(workspace, L.router_part);
+    int32_t* topk_idx = at<int32_t>(workspace, L.topk_idx);
+    float* topk_w = at<float>(workspace, L.topk_w);
+    int splits = L.router_splits;
+    if (use_tc_router(s) && tc_available()) {
+        e = launch_router_tc(s, x, w_g, part, err, cs);
+        splits = 1;
+    } else {
+        e = launch_router_gemv(s, x, w_g, part, splits, cs);
+    }
+    if (e == cudaSuccess) e = launch_topk_softmax(s, part, splits, bias, nullptr, topk_idx, topk_w, cs);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+
+    // 2. dispatch
+    int32_t* counts = at<int32_t>(workspace, L.counts);
+    int32_t* offsets = at<int32_t>(workspace, L.offsets);
+    int32_t* inv = at<int32_t>(workspace, L.inv_perm);
+    int32_t* tok = at<int32_t>(workspace, L.tok_of);
+    e = launch_dispatch(s, topk_idx, counts, offsets, at<int32_t>(workspace, L.perm), inv, tok,
+                        at<int32_t>(workspace, L.blk_hist), err, cs);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    void* x_perm = at<void>(workspace, L.x_perm);
+    if (need_tc) {
+        // the tensor-core path loads expert-contiguous rows with TMA
+        e = launch_gather_rows(s, x, tok, x_perm, cs);
+        if (e != cudaSuccess) return MOE_ERR_CUDA;
+    }
+
+    // 3. routed experts and the shared expert
+    FfnGroups g{};
+    g.E = s.E;
+    g.has_shared = shared ? 1 : 0;
+    g.d = s.d;
+    g.I = s.inter;
+    g.Is = s.inter_shared;
+    g.n_routed_rows = s.T * s.K;
+    g.T = s.T;
+    g.offsets = offsets;
+    g.row_src = need_tc ? nullptr : tok;
+    g.a_routed = need_tc ? x_perm : x;
+    g.a_shared = x;
+    g.w_gate = w_gate;
+    g.w_up = w_up;
+    g.w_down = w_down;
+    g.ws_gate = ws_gate;
+    g.ws_up = ws_up;
+    g.ws_down = ws_down;
+    g.h = at<void>(workspace, L.h);
+    g.h_s = at<void>(workspace, L.h_s);
+    g.y = at<void>(workspace, L.y_perm);
+    g.y_s = at<void>(workspace, L.y_s);
+    FfnPlanHeader* hdr = at<FfnPlanHeader>(workspace, L.plan);
+    int32_t* glist = at<int32_t>(workspace, L.gemv_list);
+    int4* mtiles = at<int4>(workspace, L.mtile_list);
+    e = launch_ffn_plan(g, s.dtype, hdr, glist, mtiles, L.max_mtiles, gemv_limit(), cs);
+    if (e == cudaSuccess) e = launch_ffn_gemv(g, s.dtype, hdr, glist, cs);
+    if (e == cudaSuccess && need_tc) e = launch_ffn_tc(g, hdr, mtiles, L.max_mtiles, err, cs);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+
+    // 4. combine
+    return cuda_status(launch_combine(s, g.y, inv, topk_w, shared ? g.y_s : nullptr, y, cs));
+}
+
+moe_status moe_get_device_error(const void* workspace, int32_t* code_out) {
+    if (!workspace || !code_out) return MOE_ERR_INVALID_ARG;
+    DevError h{};
+    if (cudaMemcpy(&h, workspace, sizeof(DevError), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    *code_out = h.code;
+    return MOE_OK;
+}
+
+}  // extern "C"

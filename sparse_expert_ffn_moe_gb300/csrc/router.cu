@@ -1,0 +1,170 @@
+// router.cu -- stage 1: router scores, top-K with lower-index ties, softmax
+// over the K selected scores.
+//
+// adg.csdn.net sparse-MoE explainer, section 2.2 (steps 1-3: a linear router
+// scores every expert, the K best are kept, softmax over those K);
+// "Sparse MoE inference kernels ..." (blog.llmgo.top), section 2.1 (linear
+// gate projection followed by top-k).
+//
+// Scores are fp32 partial dot products written by a split-K streaming GEMV
+// (W_g is read once per 8-token chunk; x through L1), summed in a fixed order
+// by the top-K kernel so the result is deterministic.  For large bf16 batches
+// the tensor-core GEMM in ffn_tc.cu produces the scores instead (split = 1).
+#include <float.h>
+#include <math.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kRouterWarps = 8;
+constexpr int kRouterTok = 8;  // tokens per pass
+
+// part[s][t][e] = sum_{k in split s} x[t][k] * w_g[e][k]
+template <typename T>
+__global__ void __launch_bounds__(kRouterWarps * 32)
+router_gemv_kernel(const T* __restrict__ x, const T* __restrict__ w_g, float* __restrict__ part,
+                   int Tn, int d, int E, int splits) {
+    constexpr int V = Elem<T>::kPerVec;
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int nvec = d / V;                       // 16-byte vectors per row
+    const int vps = (nvec + splits - 1) / splits; // vectors per split
+    const int64_t n_chunks = (Tn + kRouterTok - 1) / kRouterTok;
+    const int64_t units = n_chunks * E * splits;
+    for (int64_t u = (int64_t)blockIdx.x * kRouterWarps + warp; u < units;
+         u += (int64_t)gridDim.x * kRouterWarps) {
+        const int s = (int)(u % splits);
+        const int e = (int)((u / splits) % E);
+        const int c = (int)(u / ((int64_t)splits * E));
+        const int v0 = s * vps;
+        const int v1 = min(nvec, v0 + vps);
+        const int t0 = c * kRouterTok;
+        const int nt = min(kRouterTok, Tn - t0);
+        float acc[kRouterTok];
+#pragma unroll
+        for (int m = 0; m < kRouterTok; ++m) acc[m] = 0.f;
+        const T* wrow = w_g + (int64_t)e * d;
+        for (int v = v0 + lane; v < v1; v += 32) {
+            float wf[V];
+            unpack(ld_stream(wrow + (int64_t)v * V), wf, (const T*)nullptr);
+#pragma unroll
+            for (int m = 0; m < kRouterTok; ++m) {
+                if (m < nt) {
+                    float xf[V];
+                    unpack(ld_ro(x + (int64_t)(t0 + m) * d + (int64_t)v * V), xf, (const T*)nullptr);
+#pragma unroll
+                    for (int q = 0; q < V; ++q) acc[m] = fmaf(wf[q], xf[q], acc[m]);
+                }
+            }
+        }
+#pragma unroll
+        for (int m = 0; m < kRouterTok; ++m) {
+            float r = warp_sum(acc[m]);
+            if (lane == 0 && m < nt) part[((int64_t)s * Tn + t0 + m) * E + e] = r;
+        }
+    }
+}
+
+struct Cand {
+    float v;
+    int e;
+};
+// a beats b: larger score, or equal score and lower index
+__device__ __forceinline__ bool beats(const Cand& a, const Cand& b) {
+    return a.e >= 0 && (b.e < 0 || a.v > b.v || (a.v == b.v && a.e < b.e));
+}
+
+// One warp per token.  Lane l holds experts e = l + 32*m.
+template <int MAXM>
+__global__ void __launch_bounds__(256)
+topk_softmax_kernel(const float* __restrict__ part, int splits, const float* __restrict__ bias,
+                    float* __restrict__ logits_out, int32_t* __restrict__ topk_idx,
+                    float* __restrict__ topk_w, int Tn, int E, int K) {
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (t >= Tn) return;
+    float v[MAXM];
+#pragma unroll
+    for (int m = 0; m < MAXM; ++m) {
+        const int e = lane + 32 * m;
+        float s = 0.f;
+        if (e < E) {
+            s = part[(int64_t)t * E + e];
+            for (int q = 1; q < splits; ++q) s += part[((int64_t)q * Tn + t) * E + e];
+            if (bias) s += bias[e];
+            if (logits_out) logits_out[(int64_t)t * E + e] = s;
+        }
+        v[m] = s;
+    }
+    uint32_t taken = 0;
+    float my_s = 0.f;  // lane j keeps the j-th selected score
+    float s0 = 0.f;
+    for (int j = 0; j < K; ++j) {
+        Cand best{0.f, -1};
+#pragma unroll
+        for (int m = 0; m < MAXM; ++m) {
+            const int e = lane + 32 * m;
+            if (e < E && !(taken & (1u << m)) && (best.e < 0 || v[m] > best.v)) best = Cand{v[m], e};
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            Cand other{__shfl_xor_sync(0xffffffffu, best.v, o), __shfl_xor_sync(0xffffffffu, best.e, o)};
+            if (beats(other, best)) best = other;
+        }
+        if ((best.e & 31) == lane) taken |= 1u << (best.e >> 5);
+        if (lane == j) my_s = best.v;
+        if (j == 0) s0 = best.v;
+        if (lane == 0) topk_idx[(int64_t)t * K + j] = best.e;
+    }
+    const float ex = lane < K ? expf(my_s - s0) : 0.f;
+    const float denom = warp_sum(ex);
+    if (lane < K) topk_w[(int64_t)t * K + lane] = ex / denom;
+}
+
+}  // namespace
+
+int router_splits_for(const moe_shape& s) {
+    const int V = s.dtype == MOE_BF16 ? 8 : 4;
+    int splits = (s.d / V) / 64;
+    return splits < 1 ? 1 : (splits > 16 ? 16 : splits);
+}
+
+cudaError_t launch_router_gemv(const moe_shape& s, const void* x, const void* w_g, float* part,
+                               int splits, cudaStream_t st) {
+    const int64_t units = ceil_div(s.T, kRouterTok) * (int64_t)s.E * splits;
+    int64_t blocks = ceil_div(units, kRouterWarps);
+    const int64_t cap = (int64_t)device_sm_count() * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    if (s.dtype == MOE_BF16)
+        router_gemv_kernel<bf16><<<(unsigned)blocks, kRouterWarps * 32, 0, st>>>(
+            (const bf16*)x, (const bf16*)w_g, part, s.T, s.d, s.E, splits);
+    else
+        router_gemv_kernel<float><<<(unsigned)blocks, kRouterWarps * 32, 0, st>>>(
+            (const float*)x, (const float*)w_g, part, s.T, s.d, s.E, splits);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_topk_softmax(const moe_shape& s, const float* part, int splits,
+                                const float* bias, float* logits_out, int32_t* topk_idx,
+                                float* topk_w, cudaStream_t st) {
+    const unsigned blocks = (unsigned)ceil_div(s.T, 8);
+    const int m = (int)ceil_div(s.E, 32);
+#define MOE_TOPK(M)                                                                              \
+    topk_softmax_kernel<M><<<blocks, 256, 0, st>>>(part, splits, bias, logits_out, topk_idx, \
+                                                   topk_w, s.T, s.E, s.K)
+    if (m <= 1) MOE_TOPK(1);
+    else if (m <= 2) MOE_TOPK(2);
+    else if (m <= 4) MOE_TOPK(4);
+    else if (m <= 8) MOE_TOPK(8);
+    else if (m <= 16) MOE_TOPK(16);
+    else MOE_TOPK(32);
+#undef MOE_TOPK
+    return cudaGetLastError();
+}
+
+}  // namespace moe

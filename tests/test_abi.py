@@ -1,0 +1,133 @@
+"""The C ABI library builds, loads and exports every symbol include/moe.h declares,
+and its host-side argument checks reject bad calls before touching the device
+(no GPU needed: nothing here launches work)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from sparse_expert_ffn_moe_gb300 import _build
+    path = _build.build()
+    return ctypes.CDLL(path)
+
+
+@pytest.fixture(scope="module")
+def moe(lib):
+    import sparse_expert_ffn_moe_gb300 as m
+    return m
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "moe.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_stage_entry_points():
+    names = _declared_functions()
+    for n in ("moe_route", "moe_permute", "moe_expert_ffn", "moe_combine", "moe_forward",
+              "moe_workspace_bytes", "moe_get_device_error", "moe_status_string"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_binding_names_match_the_header(moe):
+    assert set(moe.EXPORTED) == set(_declared_functions())
+    for n in moe.EXPORTED:
+        assert hasattr(moe.library(), n)
+
+
+def test_status_strings(moe):
+    assert moe.status_string(0) == "ok"
+    assert "workspace" in moe.status_string(3)
+    assert moe.status_string(99) == "unknown status"
+
+
+def test_workspace_bytes_and_shape_limits(moe):
+    s = moe.make_shape(8, 7168, 256, 8, 2048, 2048, "bf16")
+    n = moe.moe_workspace_bytes(s)
+    # at least the permuted activations, h and y_perm of 64 rows
+    assert n >= 64 * 7168 * 2 * 2 + 64 * 2048 * 2
+    bad = [moe.make_shape(8, 7168, 256, 9, 2048, 0, "bf16"),     # K > E? no: K=9 ok -> check below
+           moe.make_shape(8, 7168, 4, 8, 2048, 0, "bf16"),       # K > E
+           moe.make_shape(8, 7100, 256, 8, 2048, 0, "bf16"),     # d not a multiple of 64
+           moe.make_shape(8, 7168, 2048, 8, 2048, 0, "bf16"),    # E > 1024
+           moe.make_shape(8, 7168, 256, 33, 2048, 0, "bf16"),    # K > 32
+           moe.make_shape(-1, 7168, 256, 8, 2048, 0, "bf16"),    # T < 0
+           moe.make_shape(8, 7168, 256, 8, 2048, 0, 7)]          # dtype
+    assert moe.moe_workspace_bytes(bad[0]) > 0
+    for s in bad[1:]:
+        assert moe.moe_workspace_bytes(s) == 0
+
+
+def test_argument_errors_return_before_any_launch(lib, moe):
+    """Null/misaligned pointers and a short workspace are refused on the host."""
+    s = moe.make_shape(4, 64, 8, 2, 64, 0, "f32")
+    sp = ctypes.byref(s)
+    lib.moe_forward.restype = ctypes.c_int32
+    lib.moe_route.restype = ctypes.c_int32
+    lib.moe_combine.restype = ctypes.c_int32
+    lib.moe_permute.restype = ctypes.c_int32
+    lib.moe_expert_ffn.restype = ctypes.c_int32
+    vp = ctypes.c_void_p
+    z = ctypes.c_size_t
+    fake = vp(1 << 20)          # aligned, never dereferenced: validation fails first
+    odd = vp((1 << 20) + 4)     # misaligned
+    # null x
+    rc = lib.moe_forward(sp, None, fake, None, fake, fake, fake, None, None, None, fake,
+                         fake, z(1 << 30), None)
+    assert rc == moe.MOE_ERR_INVALID_ARG
+    # misaligned weight
+    rc = lib.moe_forward(sp, fake, odd, None, fake, fake, fake, None, None, None, fake,
+                         fake, z(1 << 30), None)
+    assert rc == moe.MOE_ERR_INVALID_ARG
+    # shared weights given but inter_shared == 0
+    rc = lib.moe_forward(sp, fake, fake, None, fake, fake, fake, fake, fake, fake, fake,
+                         fake, z(1 << 30), None)
+    assert rc == moe.MOE_ERR_INVALID_ARG
+    # workspace too small
+    rc = lib.moe_forward(sp, fake, fake, None, fake, fake, fake, None, None, None, fake,
+                         fake, z(16), None)
+    assert rc == moe.MOE_ERR_WORKSPACE
+    # no workspace
+    rc = lib.moe_route(sp, fake, fake, None, None, None, fake, fake, None, z(0), None)
+    assert rc == moe.MOE_ERR_WORKSPACE
+    # route without outputs
+    rc = lib.moe_route(sp, fake, fake, None, None, None, None, fake, fake, z(1 << 30), None)
+    assert rc == moe.MOE_ERR_INVALID_ARG
+    # combine without inv_perm
+    rc = lib.moe_combine(sp, fake, None, fake, None, fake, None)
+    assert rc == moe.MOE_ERR_INVALID_ARG
+    # permute without counts
+    rc = lib.moe_permute(sp, fake, None, None, fake, None, None, None, fake, z(1 << 30), None)
+    assert rc == moe.MOE_ERR_INVALID_ARG
+    # expert ffn with a null weight
+    rc = lib.moe_expert_ffn(sp, fake, fake, None, fake, fake, fake, fake, z(1 << 30), None)
+    assert rc == moe.MOE_ERR_INVALID_ARG
+    # K > E is invalid; K > 32 unsupported
+    s2 = moe.make_shape(4, 64, 8, 9, 64, 0, "f32")
+    rc = lib.moe_forward(ctypes.byref(s2), fake, fake, None, fake, fake, fake, None, None, None,
+                         fake, fake, z(1 << 30), None)
+    assert rc == moe.MOE_ERR_INVALID_ARG
+    s3 = moe.make_shape(4, 64, 64, 33, 64, 0, "f32")
+    rc = lib.moe_forward(ctypes.byref(s3), fake, fake, None, fake, fake, fake, None, None, None,
+                         fake, fake, z(1 << 30), None)
+    assert rc == moe.MOE_ERR_UNSUPPORTED
+
+
+def test_binding_refuses_host_tensors(moe):
+    import torch
+    s = moe.make_shape(2, 64, 4, 2, 64, 0, "f32")
+    x = torch.zeros(2, 64)
+    with pytest.raises(ValueError):
+        moe.moe_combine(s, x, x, x, None, x, stream=0)

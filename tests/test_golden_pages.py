@@ -50,3 +50,18 @@ def test_zipf_bias_gives_the_stated_imbalance():
     assert -1.25 <= slope <= -1.15, slope
     assert srt[0] / counts.mean() > 10
     assert np.all(counts > 0)
+
+
+def test_benchmark_work_accounting_matches_the_gated_mlp_formula():
+    """The benchmark's FLOP and byte counts reduce, for one expert with K = 1 and
+    no router, to the page's gated-MLP formulas (FLOPs 6BTDF; bytes
+    4BTD + 4BTF + 6DF, of which the 4BTF of the intermediate h is implementation
+    traffic that the algorithmic byte count leaves out)."""
+    import bench
+    for c in GOLDEN["gated_mlp_work"]["cases"]:
+        T = c["B"] * c["T"]
+        cfg = mi.LayerConfig("mlp", T=T, d=c["D"], E=1, K=1, I=c["F"], Is=0)
+        router_flops = 2 * T * c["D"] * 1
+        assert bench.layer_flops(cfg) - router_flops == c["flops"]
+        router_bytes = 2 * c["D"] * 1
+        assert bench.layer_bytes(cfg, 1) - router_bytes + 4 * T * c["F"] == c["bytes"]

@@ -1,0 +1,86 @@
+"""Stage 3 on the GPU (moe_expert_ffn): both the weight-streaming GEMV path and the
+tcgen05 tensor-core grouped GEMM against the oracle's fp64 SwiGLU experts, on
+ragged expert groups (empty experts, one-row experts, groups that are not a
+multiple of the 128-row tile, one expert holding most rows)."""
+import numpy as np
+import pytest
+import torch
+
+import moe_inputs as mi
+import oracle
+from tests.gpu_util import BF16_REL_L2, F32_MAX_REL_RMS, gemv_limit, host, max_abs_over_rms, rel_l2, to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def moe():
+    import sparse_expert_ffn_moe_gb300 as m
+    return m
+
+
+def _counts_to_offsets(counts):
+    return np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+
+
+def _run(moe, counts, d, I, dtype, limit, seed=0):
+    E = len(counts)
+    offsets = _counts_to_offsets(counts)
+    rows = int(offsets[-1])
+    cfg = mi.LayerConfig("ffn_case", T=rows, d=d, E=E, K=1, I=I, dtype=dtype, seed=seed)
+    p = mi.make_weights(cfg, "cuda", only={"w_gate", "w_up", "w_down"})
+    x_perm = mi.normal((rows, d), 1.0, dtype, "cuda", seed, "x_perm")
+    s = moe.make_shape(rows, d, E, 1, I, 0, dtype)
+    ws = moe.alloc_workspace(s)
+    y = torch.full((rows, d), float("nan"), dtype=x_perm.dtype, device="cuda")
+    off_d = torch.from_numpy(offsets).cuda()
+    with gemv_limit(limit):
+        moe.moe_expert_ffn(s, x_perm, off_d, p["w_gate"], p["w_up"], p["w_down"], y, ws)
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_error(ws) == 0
+    ref = oracle.expert_ffn(host(x_perm), offsets, host(p["w_gate"]), host(p["w_up"]),
+                            host(p["w_down"]), dtype=dtype)
+    return to_f64(y), ref
+
+
+CASES = [
+    # counts per expert, d, I
+    ([16, 16, 16, 16, 16, 16, 16, 16], 256, 512),
+    ([0, 1, 0, 3, 200, 0, 129, 7], 256, 512),
+    ([5, 0, 0, 1], 7168, 2048),
+    ([300, 2, 130, 0], 1024, 384),
+]
+
+
+@pytest.mark.parametrize("counts,d,I", CASES)
+def test_fp32_streaming_path(moe, counts, d, I):
+    y, ref = _run(moe, counts, d, I, "f32", limit=1 << 30)
+    assert max_abs_over_rms(y, ref) <= F32_MAX_REL_RMS
+
+
+@pytest.mark.parametrize("counts,d,I", CASES)
+@pytest.mark.parametrize("path,limit", [("gemv", 1 << 30), ("tcgen05", 0), ("mixed", 16)])
+def test_bf16_paths(moe, counts, d, I, path, limit):
+    y, ref = _run(moe, counts, d, I, "bf16", limit=limit)
+    assert np.all(np.isfinite(y))
+    assert rel_l2(y, ref) <= BF16_REL_L2
+    # every row individually, too (a wrong row cannot hide in the total)
+    for r in range(y.shape[0]):
+        assert rel_l2(y[r], ref[r]) <= 2 * BF16_REL_L2, r
+
+
+def test_tcgen05_large_groups_deepseek_shape(moe):
+    """Many 128-row tiles per expert, bands of m-tiles, ragged last tiles."""
+    counts = [1100, 0, 257, 640, 1, 128, 0, 900]
+    y, ref = _run(moe, counts, 7168, 2048, "bf16", limit=0, seed=3)
+    assert rel_l2(y, ref) <= BF16_REL_L2
+    worst = max(rel_l2(y[r], ref[r]) for r in range(0, y.shape[0], 7))
+    assert worst <= 2 * BF16_REL_L2
+
+
+def test_paths_agree_closely(moe):
+    counts = [40, 3, 0, 77]
+    y_g, ref = _run(moe, counts, 512, 256, "bf16", limit=1 << 30)
+    y_t, _ = _run(moe, counts, 512, 256, "bf16", limit=0)
+    assert rel_l2(y_g, y_t) <= 1e-2
+    assert rel_l2(y_t, ref) <= BF16_REL_L2

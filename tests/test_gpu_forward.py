@@ -1,0 +1,148 @@
+"""The whole layer on the GPU (moe_forward) against the oracle, on every workload:
+all tokens where the oracle finishes in seconds, a seeded sample of 256 tokens
+on the large ones.  Tokens whose top-K boundary gap (fp64 scores) is below 1e-3
+have no unique routing at fp32 precision and are left out of the sample (their
+count is reported); on the small workloads such rows are re-drawn instead."""
+import numpy as np
+import pytest
+import torch
+
+import moe_inputs as mi
+import oracle
+from tests.gpu_util import (BF16_REL_L2, F32_MAX_REL_RMS, MARGIN, Layer, boundary_margin,
+                            gemv_limit, host, max_abs_over_rms, rel_l2, to_f64)
+
+pytestmark = pytest.mark.gpu
+
+SAMPLE = 256
+
+
+@pytest.fixture(scope="module")
+def moe():
+    import sparse_expert_ffn_moe_gb300 as m
+    return m
+
+
+def _clean_x(L: Layer):
+    """Re-draw rows of x until every token has a unique routing (small T only)."""
+    cfg = L.cfg
+    x = L.x
+    for attempt in range(1, 20):
+        _, _, logits = oracle.route(host(x), L.hp["w_g"], cfg.K, dtype=cfg.dtype,
+                                    bias=L.bias_host())
+        bad = np.nonzero(boundary_margin(logits, cfg.K) < MARGIN)[0]
+        if bad.size == 0:
+            return x
+        x = mi.redraw_rows(x, bad, cfg, attempt)
+    raise AssertionError("could not draw well-separated router scores")
+
+
+def _check(cfg, y, ref):
+    if cfg.dtype == "f32":
+        assert max_abs_over_rms(y, ref) <= F32_MAX_REL_RMS
+    else:
+        assert rel_l2(y, ref) <= BF16_REL_L2
+        for r in range(y.shape[0]):
+            assert rel_l2(y[r], ref[r]) <= 2 * BF16_REL_L2, r
+
+
+@pytest.mark.parametrize("name", ["tiny_f32", "dsv3_decode", "dsv3_sweep_T1", "dsv3_sweep_T8",
+                                  "dsv3_sweep_T64"])
+def test_forward_all_tokens(moe, name):
+    cfg = mi.CONFIGS[name]
+    L = Layer(cfg)
+    L.x = _clean_x(L)
+    y = to_f64(L.forward(moe))
+    ref = oracle.forward(host(L.x), L.hp, cfg.K, dtype=cfg.dtype, bias=L.bias_host())
+    _check(cfg, y, ref["y"])
+
+
+@pytest.mark.parametrize("name", ["mixtral_prefill", "dsv3_prefill_zipf", "dsv3_sweep_T512",
+                                  "dsv3_sweep_T4096"])
+def test_forward_sampled_tokens(moe, name):
+    cfg = mi.CONFIGS[name]
+    L = Layer(cfg)
+    y = L.forward(moe)
+    tokens = mi.sample_tokens(cfg.T, SAMPLE, seed=cfg.seed).numpy()
+    ref = oracle.forward_tokens(tokens, host(L.x), L.hp, cfg.K, dtype=cfg.dtype,
+                                bias=L.bias_host())
+    ok = boundary_margin(ref["logits"], cfg.K) >= MARGIN
+    print(f"{name}: {int((~ok).sum())} of {len(tokens)} sampled tokens skipped (margin < {MARGIN})")
+    assert ok.mean() >= 0.9
+    _check(cfg, to_f64(y[torch.from_numpy(tokens[ok]).long().cuda()]), ref["y"][ok])
+
+
+def test_forward_small_ragged_shapes_both_paths(moe):
+    """Shapes off the workload grid: E=12, K=3, d=192, I=320, Is=128, T=37 (ragged
+    tiles everywhere), through the GEMV path and the tensor-core path."""
+    cfg = mi.LayerConfig("ragged", T=37, d=192, E=12, K=3, I=320, Is=128)
+    L = Layer(cfg)
+    L.x = _clean_x(L)
+    ref = oracle.forward(host(L.x), L.hp, cfg.K, dtype=cfg.dtype)["y"]
+    for limit in (1 << 30, 0, 4):
+        with gemv_limit(limit):
+            y = to_f64(L.forward(moe))
+        _check(cfg, y, ref)
+
+
+def test_forward_K_equals_E_and_single_expert(moe):
+    for cfg in (mi.LayerConfig("k_eq_e", T=20, d=128, E=4, K=4, I=128, Is=64),
+                mi.LayerConfig("dense", T=300, d=256, E=1, K=1, I=192, Is=0)):
+        L = Layer(cfg)
+        ref = oracle.forward(host(L.x), L.hp, cfg.K, dtype=cfg.dtype)["y"]
+        _check(cfg, to_f64(L.forward(moe)), ref)
+
+
+def test_forward_zero_input_and_zero_tokens(moe):
+    cfg = mi.LayerConfig("zeros", T=16, d=128, E=8, K=2, I=128, Is=64)
+    L = Layer(cfg)
+    y = L.forward(moe, x=torch.zeros_like(L.x))
+    assert torch.count_nonzero(y).item() == 0
+    y0 = L.forward(moe, x=L.x[:0])
+    assert y0.shape == (0, cfg.d)
+
+
+def test_forward_is_deterministic_and_graph_capturable(moe):
+    cfg = mi.CONFIGS["dsv3_sweep_T64"]
+    L = Layer(cfg)
+    s = L.shape(moe)
+    ws = moe.alloc_workspace(s)
+    y1 = L.forward(moe, ws=ws)
+    y2 = L.forward(moe, ws=ws)
+    assert torch.equal(y1, y2)
+    p = L.p
+    y3 = torch.empty_like(y1)
+    st = torch.cuda.Stream()
+    with torch.cuda.stream(st):
+        # the first call outside capture sets kernel attributes
+        moe.moe_forward(s, L.x, p["w_g"], None, p["w_gate"], p["w_up"], p["w_down"],
+                        p["ws_gate"], p["ws_up"], p["ws_down"], y3, ws, stream=st)
+    st.synchronize()
+    g = torch.cuda.CUDAGraph()
+    y3.zero_()
+    with torch.cuda.graph(g, stream=st):
+        moe.moe_forward(s, L.x, p["w_g"], None, p["w_gate"], p["w_up"], p["w_down"],
+                        p["ws_gate"], p["ws_up"], p["ws_down"], y3, ws, stream=st)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(y3, y1)
+
+
+def test_combine_matches_oracle(moe):
+    for dtype in ("f32", "bf16"):
+        T, d, K = 50, 256, 3
+        rng = np.random.default_rng(4)
+        yp = mi.normal((T * K, d), 1.0, dtype, "cuda", 1, "yp")
+        ys = mi.normal((T, d), 1.0, dtype, "cuda", 1, "ys")
+        inv = torch.from_numpy(rng.permutation(T * K).astype(np.int32)).cuda()
+        w = torch.from_numpy(rng.random((T, K)).astype(np.float32)).cuda()
+        s = moe.make_shape(T, d, 8, K, 64, 0, dtype)
+        y = torch.empty_like(ys)
+        moe.moe_combine(s, yp, inv, w, ys, y)
+        torch.cuda.synchronize()
+        ref = oracle.combine(to_f64(yp), inv.cpu().numpy(), w.cpu().numpy().astype(np.float64),
+                             to_f64(ys))
+        if dtype == "f32":
+            assert max_abs_over_rms(to_f64(y), ref) <= 1e-6
+        else:
+            assert rel_l2(to_f64(y), ref) <= 4e-3

@@ -1,0 +1,98 @@
+"""Stage 1 on the GPU (moe_route) against the oracle.
+
+Bit-exact routing: both sides get the same fp32 scores on a 1/512 grid (distinct
+values differ by >= 1.95e-3, equal values are decided only by the tie rule).
+Scores computed from x . w_g: compared within the fp32 accumulation error, and
+the selection compared on tokens whose top-K boundary gap is >= 1e-3."""
+import numpy as np
+import pytest
+import torch
+
+import moe_inputs as mi
+import oracle
+from tests.gpu_util import MARGIN, W_RTOL, Layer, boundary_margin, host
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def moe():
+    import sparse_expert_ffn_moe_gb300 as m
+    return m
+
+
+def _route_logits(moe, logits: torch.Tensor, K: int):
+    T, E = logits.shape
+    s = moe.make_shape(T, 64, E, K, 64, 0, "f32")
+    ws = moe.alloc_workspace(s)
+    idx = torch.full((T, K), -7, dtype=torch.int32, device="cuda")
+    w = torch.full((T, K), -1.0, dtype=torch.float32, device="cuda")
+    out = torch.empty((T, E), dtype=torch.float32, device="cuda")
+    moe.moe_route(s, None, None, None, logits.cuda(), out, idx, w, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(out.cpu(), logits.cpu())
+    return idx.cpu().numpy(), w.cpu().numpy().astype(np.float64)
+
+
+@pytest.mark.parametrize("T,E,K,scale", [
+    (64, 8, 2, 512), (8, 256, 8, 512), (4096, 8, 2, 512), (16384, 256, 8, 512),
+    (1, 256, 8, 512), (100, 256, 8, 2), (37, 1024, 32, 4), (5, 3, 3, 8), (9, 1, 1, 1),
+    (77, 33, 32, 16), (513, 64, 1, 512)])
+def test_route_is_bit_exact_from_the_same_scores(moe, T, E, K, scale):
+    logits = mi.grid_logits(T, E, seed=101, scale=scale)
+    idx, w = _route_logits(moe, logits, K)
+    ref_idx, ref_w, _ = oracle.route(None, None, K, logits_in=logits.numpy())
+    assert np.array_equal(idx, ref_idx)
+    assert np.allclose(w, ref_w, rtol=W_RTOL, atol=0)
+
+
+def test_route_bit_exact_with_zipf_bias_and_all_ties(moe):
+    cfg = mi.CONFIGS["dsv3_prefill_zipf"]
+    z = mi.grid_logits(cfg.T, cfg.E, seed=102).double()
+    b = mi.make_bias(cfg).double()
+    logits = (torch.round((z + b) * 512) / 512).float()
+    idx, w = _route_logits(moe, logits, cfg.K)
+    ref_idx, ref_w, _ = oracle.route(None, None, cfg.K, logits_in=logits.numpy())
+    assert np.array_equal(idx, ref_idx)
+    assert np.allclose(w, ref_w, rtol=W_RTOL)
+    # every score equal: experts 0..K-1 with weight 1/K; -0.0 ties with +0.0
+    zero = torch.zeros(64, 256)
+    zero[::2, 5] = -0.0
+    idx, w = _route_logits(moe, zero, 8)
+    assert np.array_equal(idx, np.tile(np.arange(8), (64, 1)))
+    assert np.allclose(w, 1 / 8, rtol=1e-7)
+
+
+@pytest.mark.parametrize("name,T", [("tiny_f32", None), ("dsv3_decode", None),
+                                    ("dsv3_prefill_zipf", 512), ("dsv3_sweep_T4096", None),
+                                    ("mixtral_prefill", 256)])
+def test_route_from_x(moe, name, T):
+    """Scores from x . w_g (GEMV router, or the tensor-core router for large bf16 batches)."""
+    cfg = mi.CONFIGS[name]
+    if T is not None:
+        cfg = cfg.with_T(T)
+    L = Layer(cfg, only={"w_g"})
+    s = L.shape(moe)
+    ws = moe.alloc_workspace(s)
+    idx = torch.empty((cfg.T, cfg.K), dtype=torch.int32, device="cuda")
+    w = torch.empty((cfg.T, cfg.K), dtype=torch.float32, device="cuda")
+    out = torch.empty((cfg.T, cfg.E), dtype=torch.float32, device="cuda")
+    moe.moe_route(s, L.x, L.p["w_g"], L.bias, None, out, idx, w, ws)
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_error(ws) == 0
+    ref_idx, ref_w, ref_logits = oracle.route(host(L.x), L.hp["w_g"], cfg.K, dtype=cfg.dtype,
+                                              bias=L.bias_host())
+    got = out.cpu().numpy().astype(np.float64)
+    # fp32 accumulation of exact products: error well under 1e-4 of the score scale
+    assert np.max(np.abs(got - ref_logits)) <= 1e-4 * max(1.0, np.max(np.abs(ref_logits)))
+    ok = boundary_margin(ref_logits, cfg.K) >= MARGIN
+    assert ok.mean() > 0.9
+    gi = idx.cpu().numpy()
+    assert np.array_equal(np.sort(gi[ok], axis=1), np.sort(ref_idx[ok], axis=1))
+    # the selected set decides the weights; compare per expert id
+    gw = w.cpu().numpy().astype(np.float64)
+    for t in np.nonzero(ok)[0][:200]:
+        a = dict(zip(gi[t].tolist(), gw[t].tolist()))
+        b = dict(zip(ref_idx[t].tolist(), ref_w[t].tolist()))
+        for e in b:
+            assert abs(a[e] - b[e]) <= 1e-4 * b[e] + 1e-6
