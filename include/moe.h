@@ -41,8 +41,9 @@
  *    moe_get_device_error after the stream has been synchronised; each entry
  *    point that takes a workspace clears that word first.
  *  - Limits: 0 <= T, T*K < 2^31; 1 <= K <= min(E, 32); E <= 1024;
- *    d and I (and Is when > 0) multiples of 64; d <= 65536, I, Is <= 65536.
- *    T == 0 is a no-op returning MOE_OK.
+ *    d and I (and Is when > 0) multiples of 64; d, I, Is <= 16384.
+ *    T == 0 is a no-op returning MOE_OK (pointers to T-sized arrays may
+ *    then be NULL; moe_permute still zeroes counts and offsets).
  *  - Routing rule: top-K picks the largest scores, ties to the LOWER expert
  *    index (scores compared as floats, so -0.0 == +0.0); slot j of a token
  *    holds its j-th pick (descending score).  Flat slot f = t*K + j.

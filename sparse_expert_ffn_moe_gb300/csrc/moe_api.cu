@@ -144,11 +144,11 @@ moe_status moe_route(const moe_shape* shape, const void* x, const void* w_g, con
     moe_status st = check_shape(shape);
     if (st != MOE_OK) return st;
     const moe_shape& s = *shape;
+    if (s.T == 0) return MOE_OK;
     if (!topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
     if (!logits_in && (!x || !w_g)) return MOE_ERR_INVALID_ARG;
     if ((x && !aligned16(x)) || (w_g && !aligned16(w_g))) return MOE_ERR_INVALID_ARG;
     if ((st = check_ws(s, workspace, ws_bytes)) != MOE_OK) return st;
-    if (s.T == 0) return MOE_OK;
     cudaStream_t cs = (cudaStream_t)stream;
     const WsLayout L = ws_layout(s);
     DevError* err = at<DevError>(workspace, L.err);
@@ -174,7 +174,7 @@ moe_status moe_permute(const moe_shape* shape, const int32_t* topk_idx, const vo
     moe_status st = check_shape(shape);
     if (st != MOE_OK) return st;
     const moe_shape& s = *shape;
-    if (!topk_idx || !counts || !offsets) return MOE_ERR_INVALID_ARG;
+    if (!counts || !offsets || (s.T > 0 && !topk_idx)) return MOE_ERR_INVALID_ARG;
     if ((x && !aligned16(x)) || (x_perm && !aligned16(x_perm))) return MOE_ERR_INVALID_ARG;
     if ((st = check_ws(s, workspace, ws_bytes)) != MOE_OK) return st;
     cudaStream_t cs = (cudaStream_t)stream;
@@ -203,6 +203,7 @@ moe_status moe_expert_ffn(const moe_shape* shape, const void* x_perm, const int3
     moe_status st = check_shape(shape);
     if (st != MOE_OK) return st;
     const moe_shape& s = *shape;
+    if (s.T == 0) return MOE_OK;
     if (!x_perm || !offsets || !w_gate || !w_up || !w_down || !y_perm) return MOE_ERR_INVALID_ARG;
     if (!aligned16(x_perm) || !aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down) ||
         !aligned16(y_perm))
@@ -250,6 +251,7 @@ moe_status moe_combine(const moe_shape* shape, const void* y_perm, const int32_t
     moe_status st = check_shape(shape);
     if (st != MOE_OK) return st;
     const moe_shape& s = *shape;
+    if (s.T == 0) return MOE_OK;
     if (!y_perm || !inv_perm || !topk_w || !y) return MOE_ERR_INVALID_ARG;
     if (!aligned16(y_perm) || !aligned16(y) || (y_shared && !aligned16(y_shared)))
         return MOE_ERR_INVALID_ARG;
@@ -264,8 +266,9 @@ moe_status moe_forward(const moe_shape* shape, const void* x, const void* w_g, c
     moe_status st = check_shape(shape);
     if (st != MOE_OK) return st;
     const moe_shape& s = *shape;
-    if (!x || !w_g || !w_gate || !w_up || !w_down || !y) return MOE_ERR_INVALID_ARG;
     const bool shared = s.inter_shared > 0;
+    if (s.T == 0) return MOE_OK;
+    if (!x || !w_g || !w_gate || !w_up || !w_down || !y) return MOE_ERR_INVALID_ARG;
     if (shared != (ws_gate && ws_up && ws_down)) return MOE_ERR_INVALID_ARG;
     if (shared && (ws_gate == nullptr || ws_up == nullptr || ws_down == nullptr)) return MOE_ERR_INVALID_ARG;
     const void* ptrs[] = {x, w_g, w_gate, w_up, w_down, y};
