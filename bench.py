@@ -66,7 +66,7 @@ def layer_bytes(cfg, n_active: int) -> int:
                 + 2 * cfg.T * cfg.d)
 
 
-def launches_per_forward(cfg, gemv_limit: int = 16) -> int:
+def launches_per_forward(cfg, gemv_limit: int = 0) -> int:
     """Kernels libmoe launches for one moe_forward (mirrors the host logic in
     moe_api.cu): router (GEMV or tcgen05) + top-K, 3 dispatch kernels, the row
     gather when the tensor-core path may run, the FFN plan, 2 GEMV kernels,
@@ -106,10 +106,14 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.reader = threading.Thread(target=self._read, daemon=True)
             self.reader.start()
+            # the timed region starts once samples are flowing
+            t0 = time.time()
+            while not self.lines and time.time() - t0 < 10:
+                time.sleep(0.02)
         except (OSError, ValueError):
             self.proc = None
         return self
@@ -433,9 +437,12 @@ def bench_workload(moe, cfg, peaks, steps: int, graph: bool = False) -> dict:
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=st):
             fwd()
-        g.replay()
+        def replay():
+            with torch.cuda.stream(st):
+                g.replay()
+        replay()
         torch.cuda.synchronize()
-        gms = timed(g.replay)
+        gms = timed(replay)
         out["us_per_call_graph"] = gms * 1e3
         ms = min(ms, gms)
     gbs = out["alg_bytes"] / (ms / 1e3) / 1e9
@@ -510,7 +517,7 @@ def run_reference(args):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(mi.CONFIGS))

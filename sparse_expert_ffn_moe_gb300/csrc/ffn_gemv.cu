@@ -311,10 +311,14 @@ cudaError_t launch_gemv_t(const FfnGroups& g, const FfnPlanHeader* hdr, const in
 
 }  // namespace
 
+// bf16 groups with more rows than this take the tcgen05 GEMM.  Measured on
+// GB300: the tensor-core path streams expert weights at 88-100% of HBM
+// bandwidth even for one-row groups (its MMAs are idle most of the time), so
+// the default sends every bf16 group there; the GEMV kernels serve fp32.
 // Read on every call so a process can compare both paths on the same inputs.
 int gemv_max_rows() {
     const char* s = getenv("MOE_GEMV_MAX_ROWS");
-    const int x = s ? atoi(s) : 16;
+    const int x = s ? atoi(s) : 0;
     return x < 0 ? 0 : x;
 }
 
