@@ -124,6 +124,30 @@ moe_status moe_permute(const moe_shape *shape, const int32_t *topk_idx,
                        void *workspace, size_t ws_bytes, void *stream);
 
 /*
+ * moe_permute without a workspace, for callers that cannot allocate device
+ * memory (a runtime that reserves all of HBM for its own pool at start-up and
+ * allows no cudaMalloc afterwards, or a plug-in handed only the tensors it
+ * works on).  The pages have no counterpart: this is an interface variant,
+ * not part of the layer.  Arguments and results are those of moe_permute.
+ * Its scratch (error word, per-chunk histogram, token of each row, and the
+ * inverse permutation when inv_perm is NULL) lives in a fixed 4 MiB device
+ * array inside the library, which every GPU that loads the library holds
+ * until the process exits.  Shapes whose scratch would exceed it -- about
+ * (T*K + T*K/1024*E) * 4 bytes, doubled for T*K when inv_perm is NULL -- are
+ * refused with MOE_ERR_UNSUPPORTED.  Nothing is allocated: no cudaMalloc,
+ * cudaFree or allocating library call.  The first call on a device looks up
+ * the array's device address (once per device, with that device current);
+ * make that first call before any stream capture.  All calls share the
+ * array, and calls whose work overlaps on the GPU race on it.  Device-side
+ * errors are not reported: a dropped slot (expert id outside [0, E)) shows as
+ * offsets[E] < T*K and inv_perm[f] == -1.
+ */
+moe_status moe_permute_noalloc(const moe_shape *shape, const int32_t *topk_idx,
+                               const void *x, int32_t *counts, int32_t *offsets,
+                               int32_t *perm, int32_t *inv_perm, void *x_perm,
+                               void *stream);
+
+/*
  * Stage 3, grouped expert FFN [S sections 1.2, 4.2; C section 15].
  * For each expert e and each row p in [offsets[e], offsets[e+1]):
  *   h = SiLU(w_gate[e] . x_perm[p]) * (w_up[e] . x_perm[p]),

@@ -22,7 +22,8 @@ MOE_ERR_CUDA, MOE_ERR_TIMEOUT, MOE_ERR_BOUNDS = 4, 5, 6
 MOE_F32, MOE_BF16 = 0, 1
 
 EXPORTED = ("moe_status_string", "moe_workspace_bytes", "moe_route", "moe_permute",
-            "moe_expert_ffn", "moe_combine", "moe_forward", "moe_get_device_error")
+            "moe_permute_noalloc", "moe_expert_ffn", "moe_combine", "moe_forward",
+            "moe_get_device_error")
 
 
 class MoeError(RuntimeError):
@@ -51,12 +52,13 @@ def _load_lib() -> ctypes.CDLL:
     lib.moe_workspace_bytes.restype = sz
     lib.moe_route.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.moe_permute.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.moe_permute_noalloc.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.moe_expert_ffn.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.moe_combine.argtypes = [sp, vp, vp, vp, vp, vp, vp]
     lib.moe_forward.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.moe_get_device_error.argtypes = [vp, ctypes.POINTER(i32)]
-    for f in ("moe_route", "moe_permute", "moe_expert_ffn", "moe_combine", "moe_forward",
-              "moe_get_device_error"):
+    for f in ("moe_route", "moe_permute", "moe_permute_noalloc", "moe_expert_ffn", "moe_combine",
+              "moe_forward", "moe_get_device_error"):
         getattr(lib, f).restype = i32
     return lib
 
@@ -134,6 +136,15 @@ def moe_permute(shape, topk_idx, x, counts, offsets, perm, inv_perm, x_perm, wor
     _check(_lib.moe_permute(ctypes.byref(shape), _p(topk_idx), _p(x), _p(counts), _p(offsets),
                             _p(perm), _p(inv_perm), _p(x_perm), ws, nws, _stream(stream)),
            "moe_permute")
+
+
+def moe_permute_noalloc(shape, topk_idx, x, counts, offsets, perm, inv_perm, x_perm,
+                        stream=None):
+    """moe_permute without a workspace: its scratch is a fixed array inside the
+    library, for callers that cannot allocate device memory."""
+    _check(_lib.moe_permute_noalloc(ctypes.byref(shape), _p(topk_idx), _p(x), _p(counts),
+                                    _p(offsets), _p(perm), _p(inv_perm), _p(x_perm),
+                                    _stream(stream)), "moe_permute_noalloc")
 
 
 def moe_expert_ffn(shape, x_perm, offsets, w_gate, w_up, w_down, y_perm, workspace, stream=None):

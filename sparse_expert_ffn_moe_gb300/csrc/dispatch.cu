@@ -187,3 +187,100 @@ cudaError_t launch_gather_rows(const moe_shape& s, const void* x, const int32_t*
 }
 
 }  // namespace moe
+
+// ---------------------------------------------------------------------------
+// moe_permute_noalloc: the dispatch stage for callers that cannot allocate.
+//
+// Some callers have no way to allocate device memory: a serving runtime that
+// reserves all of HBM for its own pool at start-up and allows no cudaMalloc
+// afterwards (cudaMalloc can also stall every stream of the device), or a
+// plug-in that is handed only the tensors it works on and no allocator.  For
+// them this entry point keeps the dispatch kernels' scratch -- the device error
+// word, the per-chunk expert histogram, the token of every permuted row and,
+// when the caller passes no inv_perm, the inverse permutation -- in the
+// file-scope array below instead of a caller-provided workspace.
+//
+// The array (kNoAllocScratchBytes, 4 MiB) is held by every GPU that loads the
+// library until the process exits.  In host code its name is a host-side
+// stand-in, not a device address: the address the kernels get comes from
+// cudaGetSymbolAddress, looked up once per device, with that device current,
+// on the first call made on that device (make that first call before any
+// stream capture).  Every call shares the array and it keeps the last call's
+// contents, so the error word is cleared at the start of every call; calls
+// whose work overlaps on the GPU (other streams, other threads) race on it.
+// ---------------------------------------------------------------------------
+static constexpr size_t kNoAllocScratchBytes = (size_t)4 << 20;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+#include <mutex>
+
+namespace moe {
+namespace {
+
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kNoAllocMaxDevices] = {};
+
+// Device address of g_noalloc_scratch on the current device (looked up once per device).
+cudaError_t noalloc_scratch(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kNoAllocMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (g_noalloc_addr[dev] == nullptr) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        g_noalloc_addr[dev] = p;
+    }
+    *out = g_noalloc_addr[dev];
+    return cudaSuccess;
+}
+
+size_t noalloc_align(size_t v) { return (v + 255) / 256 * 256; }
+
+}  // namespace
+}  // namespace moe
+
+extern "C" moe_status moe_permute_noalloc(const moe_shape* shape, const int32_t* topk_idx,
+                                          const void* x, int32_t* counts, int32_t* offsets,
+                                          int32_t* perm, int32_t* inv_perm, void* x_perm,
+                                          void* stream) {
+    using namespace moe;
+    if (!shape) return MOE_ERR_INVALID_ARG;
+    const moe_shape& s = *shape;
+    if (s.T < 0 || s.d <= 0 || s.E <= 0 || s.K <= 0 || s.K > s.E ||
+        (s.dtype != MOE_F32 && s.dtype != MOE_BF16))
+        return MOE_ERR_INVALID_ARG;
+    if (s.K > 32 || s.E > 1024 || s.d % 64 || s.d > 16384 || (int64_t)s.T * s.K >= ((int64_t)1 << 31))
+        return MOE_ERR_UNSUPPORTED;
+    if (!counts || !offsets || (s.T > 0 && !topk_idx)) return MOE_ERR_INVALID_ARG;
+    if (((uintptr_t)x & 15u) || ((uintptr_t)x_perm & 15u)) return MOE_ERR_INVALID_ARG;
+    // scratch carving: error word | per-chunk histogram | token of each row | inverse permutation
+    const int64_t n = (int64_t)s.T * s.K;
+    const int nb = dispatch_blocks_for(n);
+    const size_t off_hist = 256;
+    const size_t off_tok = off_hist + noalloc_align(sizeof(int32_t) * (size_t)nb * s.E);
+    const size_t off_inv = off_tok + noalloc_align(sizeof(int32_t) * (size_t)n);
+    const size_t need = off_inv + (inv_perm ? 0 : noalloc_align(sizeof(int32_t) * (size_t)n));
+    if (need > kNoAllocScratchBytes) return MOE_ERR_UNSUPPORTED;  // beyond the fixed scratch
+    void* base = nullptr;
+    if (noalloc_scratch(&base) != cudaSuccess) return MOE_ERR_CUDA;
+    uint8_t* b = static_cast<uint8_t*>(base);
+    cudaStream_t cs = (cudaStream_t)stream;
+    DevError* err = reinterpret_cast<DevError*>(b);
+    cudaError_t e = cudaMemsetAsync(err, 0, sizeof(DevError), cs);  // last call's contents linger
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    if (s.T == 0) {
+        e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * s.E, cs);
+        if (e == cudaSuccess) e = cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (s.E + 1), cs);
+        return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+    }
+    int32_t* hist = reinterpret_cast<int32_t*>(b + off_hist);
+    int32_t* tok = reinterpret_cast<int32_t*>(b + off_tok);
+    int32_t* inv = inv_perm ? inv_perm : reinterpret_cast<int32_t*>(b + off_inv);
+    e = launch_dispatch(s, topk_idx, counts, offsets, perm, inv, tok, hist, err, cs);
+    if (e == cudaSuccess && x && x_perm) e = launch_gather_rows(s, x, tok, x_perm, cs);
+    return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
