@@ -57,8 +57,16 @@ constexpr uint32_t kTmemCols = 512;
 
 enum Epi { EPI_SWIGLU = 0, EPI_STORE_BF16 = 1, EPI_STORE_F32 = 2 };
 
+// Activation maps come in four box heights; a tile loads the smallest box that
+// covers its valid rows, so a one-token expert does not pull 128 rows of
+// other experts' activations through L2 for every k-block.  The MMA still
+// reads all 128 rows of the stage: rows past the box hold stale data that
+// only reach accumulator rows which are never stored.
+constexpr int kABoxes = 4;  // 16, 32, 64, 128 rows
+__host__ __device__ constexpr int abox_rows(int i) { return 16 << i; }
+
 struct TcParams {
-    CUtensorMap a[2];   // activations: [0] routed rows, [1] shared / dense rows
+    CUtensorMap a[2][kABoxes];  // activations: [0] routed rows, [1] shared / dense rows
     CUtensorMap b0[2];  // weights (gate / down / router)
     CUtensorMap b1[2];  // up weights (SWIGLU only)
     const FfnPlanHeader* hdr;
@@ -176,7 +184,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
     }
     if (warp == 0 && lane == 0) {
         for (int k = 0; k < 2; ++k) {
-            ptx::prefetch_tmap(&p.a[k]);
+            for (int b = 0; b < kABoxes; ++b) ptx::prefetch_tmap(&p.a[k][b]);
             ptx::prefetch_tmap(&p.b0[k]);
             if (EPI == EPI_SWIGLU) ptx::prefetch_tmap(&p.b1[k]);
         }
@@ -202,12 +210,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
             for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
                 const Tile tl = decode_tile<EPI>(p, t);
                 if (!tl.valid) continue;
-                const CUtensorMap* ma = &p.a[tl.kind];
+                const int ab = tl.rows <= 16 ? 0 : tl.rows <= 32 ? 1 : tl.rows <= 64 ? 2 : 3;
+                const uint32_t a_bytes = (uint32_t)abox_rows(ab) * BK * 2;
+                const CUtensorMap* ma = &p.a[tl.kind][ab];
                 const CUtensorMap* mb0 = &p.b0[tl.kind];
                 const CUtensorMap* mb1 = &p.b1[tl.kind];
                 for (int kb = 0; kb < tl.kblocks; ++kb) {
                     if (!wait_bounded(&ctl->empty[stage], phase ^ 1u, ctl, p, 100)) { ok = false; break; }
-                    ptx::mbar_arrive_expect_tx(&ctl->full[stage], kStageBytes);
+                    ptx::mbar_arrive_expect_tx(&ctl->full[stage], kBBytes + a_bytes);
                     const int k0 = kb * BK;
                     ptx::tma_load_2d(sA + stage * kABytes, ma, &ctl->full[stage], k0, tl.row0);
                     if (EPI == EPI_SWIGLU) {
@@ -393,8 +403,6 @@ EncodeTiledFn encode_fn() {
 bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int box_rows) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
-    static const uint16_t dummy_host = 0;
-    (void)dummy_host;
     if (rows <= 0) rows = 1;
     const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
     const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
@@ -405,6 +413,13 @@ bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int 
                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+// the four activation maps of one matrix (box heights 16, 32, 64, 128 rows)
+bool make_amaps(CUtensorMap (&m)[kABoxes], const void* base, int64_t rows, int64_t cols) {
+    bool ok = true;
+    for (int b = 0; b < kABoxes; ++b) ok &= make_map(&m[b], base, rows, cols, abox_rows(b));
+    return ok;
 }
 
 unsigned long long timeout_ns() {
@@ -449,15 +464,16 @@ cudaError_t launch_ffn_tc(const FfnGroups& g, const FfnPlanHeader* hdr, const in
     // ---- gate/up: h = SiLU(x W_gate^T) * (x W_up^T)
     TcParams p{};
     bool ok = true;
-    ok &= make_map(&p.a[0], g.a_routed, R, g.d, BM);
+    ok &= make_amaps(p.a[0], g.a_routed, R, g.d);
     ok &= make_map(&p.b0[0], g.w_gate, (int64_t)g.E * g.I, g.d, BN / 2);
     ok &= make_map(&p.b1[0], g.w_up, (int64_t)g.E * g.I, g.d, BN / 2);
     if (g.has_shared) {
-        ok &= make_map(&p.a[1], g.a_shared, g.T, g.d, BM);
+        ok &= make_amaps(p.a[1], g.a_shared, g.T, g.d);
         ok &= make_map(&p.b0[1], g.ws_gate, g.Is, g.d, BN / 2);
         ok &= make_map(&p.b1[1], g.ws_up, g.Is, g.d, BN / 2);
     } else {
-        p.a[1] = p.a[0]; p.b0[1] = p.b0[0]; p.b1[1] = p.b1[0];
+        for (int b = 0; b < kABoxes; ++b) p.a[1][b] = p.a[0][b];
+        p.b0[1] = p.b0[0]; p.b1[1] = p.b1[0];
     }
     if (!ok) return cudaErrorInvalidValue;
     p.hdr = hdr;
@@ -481,13 +497,14 @@ cudaError_t launch_ffn_tc(const FfnGroups& g, const FfnPlanHeader* hdr, const in
     // ---- down: y = h W_down^T
     TcParams q{};
     ok = true;
-    ok &= make_map(&q.a[0], g.h, R, g.I, BM);
+    ok &= make_amaps(q.a[0], g.h, R, g.I);
     ok &= make_map(&q.b0[0], g.w_down, (int64_t)g.E * g.d, g.I, BN);
     if (g.has_shared) {
-        ok &= make_map(&q.a[1], g.h_s, g.T, g.Is, BM);
+        ok &= make_amaps(q.a[1], g.h_s, g.T, g.Is);
         ok &= make_map(&q.b0[1], g.ws_down, g.d, g.Is, BN);
     } else {
-        q.a[1] = q.a[0]; q.b0[1] = q.b0[0];
+        for (int b = 0; b < kABoxes; ++b) q.a[1][b] = q.a[0][b];
+        q.b0[1] = q.b0[0];
     }
     q.b1[0] = q.b0[0]; q.b1[1] = q.b0[1];
     if (!ok) return cudaErrorInvalidValue;
@@ -513,10 +530,11 @@ cudaError_t launch_router_tc(const moe_shape& s, const void* x, const void* w_g,
                              DevError* err, cudaStream_t st) {
     TcParams p{};
     bool ok = true;
-    ok &= make_map(&p.a[1], x, s.T, s.d, BM);
+    ok &= make_amaps(p.a[1], x, s.T, s.d);
     ok &= make_map(&p.b0[1], w_g, s.E, s.d, BN);
     if (!ok) return cudaErrorInvalidValue;
-    p.a[0] = p.a[1]; p.b0[0] = p.b0[1]; p.b1[0] = p.b0[1]; p.b1[1] = p.b0[1];
+    for (int b = 0; b < kABoxes; ++b) p.a[0][b] = p.a[1][b];
+    p.b0[0] = p.b0[1]; p.b1[0] = p.b0[1]; p.b1[1] = p.b0[1];
     p.hdr = nullptr;
     p.mtiles = nullptr;
     p.dense_rows = s.T;

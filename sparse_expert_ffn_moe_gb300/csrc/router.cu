@@ -22,6 +22,7 @@ namespace {
 
 constexpr int kRouterWarps = 8;
 constexpr int kRouterTok = 8;  // tokens per pass
+constexpr int kMaxSplits = 8;  // split-K partials per score
 
 // part[s][t][e] = sum_{k in split s} x[t][k] * w_g[e][k]
 template <typename T>
@@ -48,6 +49,7 @@ router_gemv_kernel(const T* __restrict__ x, const T* __restrict__ w_g, float* __
 #pragma unroll
         for (int m = 0; m < kRouterTok; ++m) acc[m] = 0.f;
         const T* wrow = w_g + (int64_t)e * d;
+#pragma unroll 4
         for (int v = v0 + lane; v < v1; v += 32) {
             float wf[V];
             unpack(ld_stream(wrow + (int64_t)v * V), wf, (const T*)nullptr);
@@ -93,8 +95,15 @@ topk_softmax_kernel(const float* __restrict__ part, int splits, const float* __r
         const int e = lane + 32 * m;
         float s = 0.f;
         if (e < E) {
-            s = part[(int64_t)t * E + e];
-            for (int q = 1; q < splits; ++q) s += part[((int64_t)q * Tn + t) * E + e];
+            // fixed summation order over the split-K partials (deterministic)
+            float pq[kMaxSplits];
+#pragma unroll
+            for (int q = 0; q < kMaxSplits; ++q)
+                pq[q] = q < splits ? part[((int64_t)q * Tn + t) * E + e] : 0.f;
+            s = pq[0];
+#pragma unroll
+            for (int q = 1; q < kMaxSplits; ++q)
+                if (q < splits) s += pq[q];
             if (bias) s += bias[e];
             if (logits_out) logits_out[(int64_t)t * E + e] = s;
         }
@@ -127,10 +136,11 @@ topk_softmax_kernel(const float* __restrict__ part, int splits, const float* __r
 
 }  // namespace
 
+// about 224 16-byte vectors (7 per lane) of a W_g row per split
 int router_splits_for(const moe_shape& s) {
     const int V = s.dtype == MOE_BF16 ? 8 : 4;
-    int splits = (s.d / V) / 64;
-    return splits < 1 ? 1 : (splits > 16 ? 16 : splits);
+    int splits = (s.d / V) / 224;
+    return splits < 1 ? 1 : (splits > kMaxSplits ? kMaxSplits : splits);
 }
 
 cudaError_t launch_router_gemv(const moe_shape& s, const void* x, const void* w_g, float* part,
