@@ -353,11 +353,31 @@ def time_expert_ffn(moe, cfg, x, p, bias, stream, steps: int) -> dict:
     return {"ms": ms, "flops": 6 * n * cfg.d * cfg.I}
 
 
+# DRAM bytes (read + write) of one expert-FFN stage (both tcgen05 launches), from one
+# ncu capture per workload (profiles/ffn_stage_traffic_<workload>.md), valid only for
+# the ffn_tc.cu source it was taken on (sha256 prefix).
+STAGE_TRAFFIC = {
+    "mixtral_prefill": {"bytes": 4386545408, "ffn_tc_sha256": "c9900769c6fa0a63"},
+}
+
+
+def stage_traffic(workload: str):
+    import hashlib
+    rec = STAGE_TRAFFIC.get(workload)
+    if rec is None:
+        return None
+    path = os.path.join(ROOT, "sparse_expert_ffn_moe_gb300", "csrc", "ffn_tc.cu")
+    with open(path, "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()[:16]
+    return rec["bytes"] if sha == rec["ffn_tc_sha256"] else None
+
+
 def stage_roofline(cfg, stage, peaks) -> dict:
     achieved = stage["flops"] / (stage["ms"] / 1e3) / 1e12
     peak = peaks["bf16_tflops"]
     return {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-            "frac": achieved / peak, "traffic": None,
+            "frac": achieved / peak, "traffic": stage_traffic(cfg.name),
+            "traffic_unit": "bytes per launch pair (DRAM read + write, ncu)",
             "kernel": "expert FFN stage: tcgen05 gate/up GEMM (SiLU*mul epilogue) + tcgen05 "
                       "down GEMM (+ plan, empty GEMV launches)",
             "per_launch_flops": stage["flops"], "ms_per_launch": stage["ms"],
