@@ -66,13 +66,15 @@ def layer_bytes(cfg, n_active: int) -> int:
                 + 2 * cfg.T * cfg.d)
 
 
-def launches_per_forward(cfg, gemv_limit: int = 0) -> int:
+def launches_per_forward(cfg, gemv_limit: int = 0, pair_min: int = 512) -> int:
     """Kernels libmoe launches for one moe_forward (mirrors the host logic in
     moe_api.cu): router (GEMV or tcgen05) + top-K, 3 dispatch kernels, the row
     gather when the tensor-core path may run, the FFN plan, 2 GEMV kernels,
-    2 tcgen05 GEMMs when needed, combine."""
+    the single-SM tcgen05 gate/up and down GEMMs when needed, and the CTA-pair
+    ones too when a group can reach pair_min rows, combine."""
     need_tc = cfg.dtype == "bf16" and cfg.T > gemv_limit
-    return 2 + 3 + (1 if need_tc else 0) + 1 + 2 + (2 if need_tc else 0) + 1
+    pair = need_tc and cfg.T >= pair_min
+    return 2 + 3 + (1 if need_tc else 0) + 1 + 2 + (2 if need_tc else 0) + (2 if pair else 0) + 1
 
 
 # --------------------------------------------------------------------------- helpers

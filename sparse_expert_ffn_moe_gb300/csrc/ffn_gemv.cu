@@ -29,7 +29,6 @@ constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 constexpr int kRowsGU = 16;   // gate/up output rows per unit (2 per warp)
 constexpr int kRowsDown = 16; // down output rows per unit
-constexpr int kTileM = 128;   // rows per tensor-core tile
 
 __device__ int32_t scan_1024(int32_t v, int32_t* sh, int32_t* total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -58,15 +57,20 @@ __device__ int32_t scan_1024(int32_t v, int32_t* sh, int32_t* total) {
     return r;
 }
 
-// groups: E routed (+1 shared).  One block of 1024 threads, two groups per thread.
+// groups: E routed (+1 shared), up to 1024 per pass of one 1024-thread block.
+// A group goes to the GEMV list (1..limit rows), to the pair-tile list (at
+// least pair_min rows, tiles of pair_m rows) or to the single-tile list
+// (tiles of single_m rows).  Entries are (group, first row of the group, rows
+// of the group, index of the m-tile within the group).
 __global__ void __launch_bounds__(1024)
 ffn_plan_kernel(const int32_t* __restrict__ offsets, int E, int has_shared, int T, int limit,
-                FfnPlanHeader* __restrict__ hdr, int32_t* __restrict__ gemv_list,
-                int4* __restrict__ mtile_list, int max_mtiles) {
+                int single_m, int pair_min, int pair_m, FfnPlanHeader* __restrict__ hdr,
+                int32_t* __restrict__ gemv_list, int4* __restrict__ mtile_list, int max_mtiles) {
     __shared__ int32_t sh[32];
-    __shared__ int32_t tot_g, tot_t, base_g, base_t;
-    if (threadIdx.x == 0) { base_g = 0; base_t = 0; }
+    __shared__ int32_t tot_g, tot_s, tot_p, base_g, base_s, base_p;
+    if (threadIdx.x == 0) { base_g = 0; base_s = 0; base_p = 0; }
     __syncthreads();
+    int4* pair_list = mtile_list + max_mtiles;
     const int G = E + (has_shared ? 1 : 0);
     for (int g0 = 0; g0 < G; g0 += blockDim.x) {
         const int g = g0 + threadIdx.x;
@@ -74,22 +78,29 @@ ffn_plan_kernel(const int32_t* __restrict__ offsets, int E, int has_shared, int 
         if (g < E) { row0 = offsets[g]; rows = offsets[g + 1] - row0; }
         else if (g < G) { row0 = 0; rows = T; }
         const bool to_gemv = rows > 0 && rows <= limit;
-        const int32_t tiles = (rows > limit) ? (rows + kTileM - 1) / kTileM : 0;
+        const bool to_pair = rows > limit && rows >= pair_min;
+        const int32_t st = (rows > limit && !to_pair) ? (rows + single_m - 1) / single_m : 0;
+        const int32_t pt = to_pair ? (rows + pair_m - 1) / pair_m : 0;
         const int32_t pg = scan_1024(to_gemv ? 1 : 0, sh, &tot_g);
-        const int32_t pt = scan_1024(tiles, sh, &tot_t);
+        const int32_t ps = scan_1024(st, sh, &tot_s);
+        const int32_t pp = scan_1024(pt, sh, &tot_p);
         if (to_gemv) gemv_list[base_g + pg] = g;
-        for (int32_t i = 0; i < tiles; ++i) {
-            const int32_t slot = base_t + pt + i;
-            // (group, first row of the group, rows of the group, index of this m-tile)
+        for (int32_t i = 0; i < st; ++i) {
+            const int32_t slot = base_s + ps + i;
             if (slot < max_mtiles) mtile_list[slot] = make_int4(g, row0, rows, i);
         }
+        for (int32_t i = 0; i < pt; ++i) {
+            const int32_t slot = base_p + pp + i;
+            if (slot < max_mtiles) pair_list[slot] = make_int4(g, row0, rows, i);
+        }
         __syncthreads();
-        if (threadIdx.x == 0) { base_g += tot_g; base_t += tot_t; }
+        if (threadIdx.x == 0) { base_g += tot_g; base_s += tot_s; base_p += tot_p; }
         __syncthreads();
     }
     if (threadIdx.x == 0) {
         hdr->n_gemv = base_g;
-        hdr->n_mtiles = min(base_t, max_mtiles);
+        hdr->n_mtiles = min(base_s, max_mtiles);
+        hdr->n_ptiles = min(base_p, max_mtiles);
     }
 }
 
@@ -326,7 +337,8 @@ cudaError_t launch_ffn_plan(const FfnGroups& g, int dtype, FfnPlanHeader* hdr, i
                             int4* mtile_list, int max_mtiles, int gemv_limit, cudaStream_t st) {
     // fp32 layers never use the tensor cores (no TF32): every group streams
     const int limit = dtype == MOE_F32 ? 0x7fffffff : gemv_limit;
-    ffn_plan_kernel<<<1, 1024, 0, st>>>(g.offsets, g.E, g.has_shared, g.T, limit, hdr, gemv_list,
+    ffn_plan_kernel<<<1, 1024, 0, st>>>(g.offsets, g.E, g.has_shared, g.T, limit, tc_tile_rows(false),
+                                        tc_pair_min_rows(), tc_tile_rows(true), hdr, gemv_list,
                                         mtile_list, max_mtiles);
     return cudaGetLastError();
 }

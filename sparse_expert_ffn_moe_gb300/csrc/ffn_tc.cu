@@ -1,10 +1,5 @@
-// ffn_tc.cu -- stage 3 for groups with many rows (and the router GEMM of
-// large batches): a persistent grouped GEMM on the 5th-generation tensor
-// cores.  TMA streams 128-row activation tiles and 256-row weight tiles into a
-// 4-stage shared-memory ring; one thread issues tcgen05.mma into a TMEM
-// accumulator (two 128x256 fp32 accumulators, double-buffered so the epilogue
-// of one tile overlaps the main loop of the next); four epilogue warps read
-// TMEM with tcgen05.ld and write the result.
+// ffn_tc.cu -- stage 3 for bf16 expert groups (and the router GEMM of large
+// batches): a persistent grouped GEMM on the 5th-generation tensor cores.
 //
 // "Sparse MoE inference kernels ..." (blog.llmgo.top), section 4.2: one
 // launch computes many GEMMs whose M differs per expert while K and N are
@@ -12,24 +7,48 @@
 // with no tokens are skipped (FAQ Q1).  "Computation and Data Movement for
 // Inference", section 15: one weight load serves every token of the bucket.
 //
-// Tiles are (group, 128-row m-tile, n-block).  Within a group the m-tiles of
-// a band of 8 vary fastest, so the CTAs working at the same moment share the
-// same weight tiles through L2 and every weight tile is read from HBM about
-// once per band.  Rows of an m-tile past its group's end belong to the next
-// group (or lie past the tensor and read as zero): they are computed and
-// never stored.
+// Two tile shapes, one kernel template (every tcgen05 instruction of one
+// kernel uses the same CTA-group size):
+//   single (PAIR = false)  128 rows x 256 columns per CTA; a 4-stage ring of
+//                          48 KB stages (128 activation rows + 256 weight
+//                          rows of a 64-deep K step); tcgen05.mma.cta_group::1.
+//   pair   (PAIR = true)   256 rows x 256 columns per cluster of 2 CTAs; each
+//                          CTA holds 128 activation rows and 128 of the 256
+//                          weight rows of a K step in a 6-stage ring of 32 KB
+//                          stages; the even CTA issues tcgen05.mma.cta_group::2,
+//                          which reads both CTAs' operands and leaves each
+//                          CTA's 128 accumulator rows in its own tensor memory.
+// A pair tile needs 32 KB per SM per K step instead of 48 KB, so the ring
+// hides ~1.5x more memory latency and large groups run faster; but it pads
+// ragged groups to 256 rows.  The plan kernel therefore sends groups of at
+// least MOE_PAIR_MIN_ROWS rows (default 512) to pair tiles and the rest to
+// single tiles; each GEMM is two launches (pair list, then single list).
+//
+// Both shapes keep two 128x256 fp32 accumulators per CTA in tensor memory
+// (all 512 columns), double-buffered so the epilogue of one tile overlaps the
+// main loop of the next.  Roles (192 threads per CTA): warp 0 TMA producer;
+// warp 1 MMA issuer and tensor-memory owner; warps 2-5 epilogue.
+//
+// Tiles are (group, m-tile, n-block).  Within a group the m-tiles of a band
+// (1024 rows) vary fastest, so the CTAs working at the same moment share the
+// same weight tiles through L2.  Rows of an m-tile past its group's end belong
+// to the next group (or lie past the tensor and read as zero): they are
+// computed and never stored.  The activation box is 16/32/64/128 rows, the
+// smallest covering a CTA's valid rows (no load when a CTA has none).
 //
 // Epilogues:
-//   SWIGLU     B = [W_gate rows n..n+127 ; W_up rows n..n+127], so columns
-//              0..127 of the accumulator hold gate and 128..255 up for the
-//              same 128 intermediate indices: h = SiLU(g) * u -> bf16.
+//   SWIGLU     the 256 weight rows of an n-block are W_gate rows n..n+127
+//              followed by W_up rows n..n+127 (in a pair: even CTA gate, odd
+//              CTA up), so accumulator columns 0..127 are gate and 128..255
+//              up for the same intermediate indices: h = SiLU(g) * u -> bf16.
 //   STORE_BF16 plain product -> bf16 (down projection).
 //   STORE_F32  plain product -> fp32 (router scores).
 //
 // Every wait on an mbarrier is bounded (MOE_TC_TIMEOUT_MS, default 1000 ms
 // of wall time); when one runs out the CTA records MOE_ERR_TIMEOUT in the
-// workspace error word, all roles leave their loops, outstanding copies and
-// MMAs are drained with bounded waits, TMEM is freed and the kernel returns.
+// workspace error word, its roles leave their loops, outstanding copies and
+// MMAs are drained with bounded waits, tensor memory is freed (a pair always
+// reaches the collective free) and the kernel returns.
 #include <cuda.h>
 #include <stdio.h>
 #include <stdlib.h>
@@ -44,34 +63,48 @@ namespace moe {
 
 namespace {
 
-constexpr int BM = 128;
-constexpr int BN = 256;
+constexpr int BMC = 128;  // accumulator rows per CTA
+constexpr int BN = 256;   // MMA N
 constexpr int BK = 64;
-constexpr int kStages = 4;
-constexpr int kBand = 8;
-constexpr uint32_t kABytes = BM * BK * 2;     // 16 KB
-constexpr uint32_t kBBytes = BN * BK * 2;     // 32 KB
-constexpr uint32_t kStageBytes = kABytes + kBBytes;
-constexpr int kThreadsTc = 192;               // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+constexpr int kMaxStages = 6;
+constexpr uint32_t kABytes = BMC * BK * 2;  // 16 KB
+constexpr uint32_t kRingBytes = 192 * 1024; // 4 x 48 KB (single) = 6 x 32 KB (pair)
+constexpr int kThreadsTc = 192;
 constexpr uint32_t kTmemCols = 512;
+
+template <bool PAIR> struct Shape {
+    static constexpr int kTileRows = PAIR ? 256 : 128;  // rows per tile
+    static constexpr int kBRows = PAIR ? 128 : 256;     // weight rows per CTA per K step
+    static constexpr int kStages = PAIR ? 6 : 4;
+    static constexpr int kBand = PAIR ? 4 : 8;          // m-tiles per band (1024 rows)
+    static constexpr uint32_t kBBytes = kBRows * BK * 2;
+    static constexpr uint32_t kStageBytes = kABytes + kBBytes;
+    static constexpr uint32_t kEpiArrivals = PAIR ? 8 : 4;  // epilogue warps per tile
+    static_assert(kStages * kStageBytes == kRingBytes, "ring size");
+};
 
 enum Epi { EPI_SWIGLU = 0, EPI_STORE_BF16 = 1, EPI_STORE_F32 = 2 };
 
-// Activation maps come in four box heights; a tile loads the smallest box that
-// covers its valid rows, so a one-token expert does not pull 128 rows of
-// other experts' activations through L2 for every k-block.  The MMA still
-// reads all 128 rows of the stage: rows past the box hold stale data that
-// only reach accumulator rows which are never stored.
+// Activation maps come in four box heights; a CTA loads the smallest box that
+// covers its valid rows.  The MMA still reads all 128 rows of the stage: rows
+// past the box hold stale data that only reach accumulator rows which are
+// never stored.
 constexpr int kABoxes = 4;  // 16, 32, 64, 128 rows
 __host__ __device__ constexpr int abox_rows(int i) { return 16 << i; }
+__device__ __forceinline__ int abox_for(int rows) {
+    return rows <= 16 ? 0 : rows <= 32 ? 1 : rows <= 64 ? 2 : 3;
+}
+__device__ __forceinline__ uint32_t abytes_for(int rows) {
+    return rows <= 0 ? 0u : (uint32_t)abox_rows(abox_for(rows)) * BK * 2;
+}
 
 struct TcParams {
     CUtensorMap a[2][kABoxes];  // activations: [0] routed rows, [1] shared / dense rows
-    CUtensorMap b0[2];  // weights (gate / down / router)
-    CUtensorMap b1[2];  // up weights (SWIGLU only)
+    CUtensorMap b0[2];          // weights (gate / down / router), box 128 rows
+    CUtensorMap b1[2];          // up weights (SWIGLU only), box 128 rows
+    CUtensorMap bw[2];          // weights, box 256 rows (single tiles, non-SWIGLU)
     const FfnPlanHeader* hdr;
     const int4* mtiles;
-    const int32_t* offsets;
     int E;
     int max_mtiles;
     int dense_rows;     // > 0: one dense group of this many rows on the [1] maps
@@ -86,17 +119,18 @@ struct TcParams {
 };
 
 struct Tile {
-    int kind;       // 0 routed, 1 shared/dense
-    int row0;       // first activation row (in the map of `kind`)
-    int rows;       // valid rows (<= BM)
-    int wrow0;      // first weight row of this n-block in the stacked matrix
-    int n0;         // first output column
+    int kind;   // 0 routed, 1 shared/dense
+    int row0;   // first activation row of the tile (in the map of `kind`)
+    int rows;   // valid rows of the tile
+    int wrow0;  // first weight row of this n-block in the stacked matrix
+    int n0;     // first output column
     int kblocks;
     bool valid;
 };
 
-template <int EPI>
-__device__ __forceinline__ Tile decode_tile(const TcParams& p, int t) {
+template <int EPI, bool PAIR>
+__device__ __forceinline__ Tile decode_tile(const TcParams& p, int n_tiles_in_list, int t) {
+    using S = Shape<PAIR>;
     constexpr int kNCols = EPI == EPI_SWIGLU ? BN / 2 : BN;  // output columns per n-block
     Tile tl;
     const int NB = p.NB;
@@ -107,18 +141,19 @@ __device__ __forceinline__ Tile decode_tile(const TcParams& p, int t) {
         const int4 e = p.mtiles[t / NB];
         g = e.x; gr0 = e.y; Mg = e.z; i = e.w;
     }
+    (void)n_tiles_in_list;
     const int q = t / NB;
-    const int cnt = (Mg + BM - 1) / BM;
-    const int tt = t - (q - i) * NB;               // index inside this group's tiles
-    const int band = tt / (kBand * NB);
-    const int bstart = band * kBand;
-    const int bcnt = min(kBand, cnt - bstart);
-    const int r = tt - band * kBand * NB;
+    const int cnt = (Mg + S::kTileRows - 1) / S::kTileRows;
+    const int tt = t - (q - i) * NB;  // index inside this group's tiles
+    const int band = tt / (S::kBand * NB);
+    const int bstart = band * S::kBand;
+    const int bcnt = min(S::kBand, cnt - bstart);
+    const int r = tt - band * S::kBand * NB;
     const int nb = r / bcnt;
     const int mi = bstart + r % bcnt;
     tl.kind = (p.dense_rows > 0 || g >= p.E) ? 1 : 0;
-    tl.row0 = gr0 + mi * BM;
-    tl.rows = min(BM, Mg - mi * BM);
+    tl.row0 = gr0 + mi * S::kTileRows;
+    tl.rows = min(S::kTileRows, Mg - mi * S::kTileRows);
     tl.n0 = nb * kNCols;
     tl.wrow0 = (tl.kind == 0 ? g * p.wrows[0] : 0) + tl.n0;
     tl.kblocks = (p.kdim[tl.kind] + BK - 1) / BK;
@@ -127,17 +162,17 @@ __device__ __forceinline__ Tile decode_tile(const TcParams& p, int t) {
 }
 
 struct SmemCtl {
-    uint64_t full[kStages];
-    uint64_t empty[kStages];
-    uint64_t tfull[2];
-    uint64_t tempty[2];
+    uint64_t full[kMaxStages];   // stage s landed (a pair: both CTAs' copies, on the even CTA)
+    uint64_t empty[kMaxStages];  // the MMAs reading stage s completed (each CTA)
+    uint64_t tfull[2];           // accumulator a is ready (each CTA)
+    uint64_t tempty[2];          // the epilogue warps drained accumulator a (a pair: even CTA, 8 warps)
     uint64_t drain;
     uint32_t tmem_base;
     volatile int abort_flag;
 };
 
 // Bounded wait: false (and the CTA-wide abort flag set) when the budget runs out
-// or another role already gave up.
+// or another role of this CTA already gave up.
 __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, SmemCtl* ctl,
                                              const TcParams& p, int where) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
@@ -155,27 +190,43 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, Sme
     }
 }
 
-template <int EPI>
+template <bool PAIR>
+__device__ __forceinline__ void cta_sync_all() {
+    if constexpr (PAIR) {
+        __syncwarp();  // the cluster barrier needs every warp converged
+        ptx::cluster_sync();
+    } else {
+        __syncthreads();
+    }
+}
+
+template <int EPI, bool PAIR>
 __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
+    using S = Shape<PAIR>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    // 1024-byte alignment for the 128-byte-swizzle atoms
+    // 1024-byte alignment for the 128-byte-swizzle atoms (the same offset in both CTAs of a pair)
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t* sA = smem;
-    uint8_t* sB = smem + kStages * kABytes;
-    SmemCtl* ctl = (SmemCtl*)(smem + kStages * kStageBytes);
+    uint8_t* sB = smem + S::kStages * kABytes;
+    SmemCtl* ctl = (SmemCtl*)(smem + kRingBytes);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n_tiles = (p.dense_rows > 0 ? (p.dense_rows + BM - 1) / BM
-                                          : min(p.hdr->n_mtiles, p.max_mtiles)) * p.NB;
+    const uint32_t rank = PAIR ? ptx::cluster_ctarank() : 0u;  // 0 issues the MMAs
+    const int unit = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+    const int n_units = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+    const int list_len = p.dense_rows > 0
+        ? (p.dense_rows + S::kTileRows - 1) / S::kTileRows
+        : min(PAIR ? p.hdr->n_ptiles : p.hdr->n_mtiles, p.max_mtiles);
+    const int n_tiles = list_len * p.NB;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < S::kStages; ++s) {
             ptx::mbar_init(&ctl->full[s], 1);
             ptx::mbar_init(&ctl->empty[s], 1);
         }
         for (int a = 0; a < 2; ++a) {
             ptx::mbar_init(&ctl->tfull[a], 1);
-            ptx::mbar_init(&ctl->tempty[a], 4);
+            ptx::mbar_init(&ctl->tempty[a], S::kEpiArrivals);
         }
         ptx::mbar_init(&ctl->drain, 1);
         ctl->abort_flag = 0;
@@ -185,16 +236,25 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
     if (warp == 0 && lane == 0) {
         for (int k = 0; k < 2; ++k) {
             for (int b = 0; b < kABoxes; ++b) ptx::prefetch_tmap(&p.a[k][b]);
-            ptx::prefetch_tmap(&p.b0[k]);
-            if (EPI == EPI_SWIGLU) ptx::prefetch_tmap(&p.b1[k]);
+            if (PAIR || EPI == EPI_SWIGLU) {
+                ptx::prefetch_tmap(&p.b0[k]);
+                if (EPI == EPI_SWIGLU) ptx::prefetch_tmap(&p.b1[k]);
+            } else {
+                ptx::prefetch_tmap(&p.bw[k]);
+            }
         }
     }
     if (warp == 1) {
-        ptx::tmem_alloc(&ctl->tmem_base, kTmemCols);
-        ptx::tmem_relinquish();
+        if constexpr (PAIR) {
+            ptx::tmem_alloc_pair(&ctl->tmem_base, kTmemCols);
+            ptx::tmem_relinquish_pair();
+        } else {
+            ptx::tmem_alloc(&ctl->tmem_base, kTmemCols);
+            ptx::tmem_relinquish();
+        }
     }
     ptx::tc_fence_before();
-    __syncthreads();
+    cta_sync_all<PAIR>();  // barriers initialised (in both CTAs of a pair), tensor memory allocated
     ptx::tc_fence_after();
     const uint32_t tmem = ctl->tmem_base;
 
@@ -203,58 +263,83 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
-            uint32_t issued_phase[kStages];
-            bool issued[kStages];
-            for (int s = 0; s < kStages; ++s) { issued[s] = false; issued_phase[s] = 0; }
+            uint32_t issued_phase[kMaxStages];
+            bool issued[kMaxStages];
+            for (int s = 0; s < kMaxStages; ++s) { issued[s] = false; issued_phase[s] = 0; }
+            const uint32_t full0 = PAIR ? ptx::map_to_rank(&ctl->full[0], 0) : 0u;
             bool ok = true;
-            for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
-                const Tile tl = decode_tile<EPI>(p, t);
+            for (int t = unit; t < n_tiles && ok; t += n_units) {
+                const Tile tl = decode_tile<EPI, PAIR>(p, list_len, t);
                 if (!tl.valid) continue;
-                const int ab = tl.rows <= 16 ? 0 : tl.rows <= 32 ? 1 : tl.rows <= 64 ? 2 : 3;
-                const uint32_t a_bytes = (uint32_t)abox_rows(ab) * BK * 2;
-                const CUtensorMap* ma = &p.a[tl.kind][ab];
-                const CUtensorMap* mb0 = &p.b0[tl.kind];
-                const CUtensorMap* mb1 = &p.b1[tl.kind];
+                const int rows_me = max(0, min(BMC, tl.rows - (int)rank * BMC));
+                const CUtensorMap* ma = &p.a[tl.kind][abox_for(rows_me)];
+                const int arow = tl.row0 + (int)rank * BMC;
+                uint32_t tx;
+                const CUtensorMap* mb;
+                int brow;
+                if constexpr (PAIR) {
+                    tx = abytes_for(min(BMC, tl.rows)) + abytes_for(tl.rows - BMC) + 2 * S::kBBytes;
+                    mb = (EPI == EPI_SWIGLU && rank == 1) ? &p.b1[tl.kind] : &p.b0[tl.kind];
+                    brow = tl.wrow0 + ((EPI == EPI_SWIGLU) ? 0 : (int)rank * S::kBRows);
+                } else {
+                    tx = abytes_for(rows_me) + S::kBBytes;
+                    mb = EPI == EPI_SWIGLU ? &p.b0[tl.kind] : &p.bw[tl.kind];
+                    brow = tl.wrow0;
+                }
                 for (int kb = 0; kb < tl.kblocks; ++kb) {
                     if (!wait_bounded(&ctl->empty[stage], phase ^ 1u, ctl, p, 100)) { ok = false; break; }
-                    ptx::mbar_arrive_expect_tx(&ctl->full[stage], kBBytes + a_bytes);
                     const int k0 = kb * BK;
-                    ptx::tma_load_2d(sA + stage * kABytes, ma, &ctl->full[stage], k0, tl.row0);
-                    if (EPI == EPI_SWIGLU) {
-                        ptx::tma_load_2d(sB + stage * kBBytes, mb0, &ctl->full[stage], k0, tl.wrow0);
-                        ptx::tma_load_2d(sB + stage * kBBytes + kBBytes / 2, mb1, &ctl->full[stage], k0,
-                                         tl.wrow0);
+                    uint8_t* a_dst = sA + stage * kABytes;
+                    uint8_t* b_dst = sB + stage * S::kBBytes;
+                    if constexpr (PAIR) {
+                        if (rank == 0) ptx::mbar_arrive_expect_tx(&ctl->full[stage], tx);
+                        const uint32_t fb = full0 + (uint32_t)(stage * sizeof(uint64_t));
+                        if (rows_me > 0) ptx::tma_load_2d_pair(a_dst, ma, fb, k0, arow);
+                        ptx::tma_load_2d_pair(b_dst, mb, fb, k0, brow);
                     } else {
-                        ptx::tma_load_2d(sB + stage * kBBytes, mb0, &ctl->full[stage], k0, tl.wrow0);
+                        ptx::mbar_arrive_expect_tx(&ctl->full[stage], tx);
+                        ptx::tma_load_2d(a_dst, ma, &ctl->full[stage], k0, arow);
+                        ptx::tma_load_2d(b_dst, mb, &ctl->full[stage], k0, brow);
+                        if (EPI == EPI_SWIGLU)
+                            ptx::tma_load_2d(b_dst + S::kBBytes / 2, &p.b1[tl.kind], &ctl->full[stage], k0, brow);
                     }
                     issued[stage] = true;
                     issued_phase[stage] = phase;
-                    if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                    if (++stage == S::kStages) { stage = 0; phase ^= 1u; }
                 }
             }
             if (!ok) {
-                // drain: every copy issued lands before the CTA exits
-                for (int s = 0; s < kStages; ++s) {
-                    if (!issued[s]) continue;
+                if (rank == 0) {
+                    // drain: every copy issued (for a pair, both CTAs' copies land on
+                    // this CTA's full barriers) lands before teardown
+                    for (int s = 0; s < S::kStages; ++s) {
+                        if (!issued[s]) continue;
+                        const uint64_t t0 = ptx::globaltimer_ns();
+                        while (!ptx::mbar_try_wait(&ctl->full[s], issued_phase[s]) &&
+                               ptx::globaltimer_ns() - t0 < p.timeout_ns) {
+                        }
+                    }
+                } else {
+                    // the odd CTA of a pair cannot observe the even CTA's barriers: give
+                    // its copies in flight a bounded time to land before teardown
                     const uint64_t t0 = ptx::globaltimer_ns();
-                    while (!ptx::mbar_try_wait(&ctl->full[s], issued_phase[s]) &&
-                           ptx::globaltimer_ns() - t0 < p.timeout_ns) {
+                    while (ptx::globaltimer_ns() - t0 < 2000000ull) {
                     }
                 }
             }
         }
     } else if (warp == 1) {
-        // ------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idesc = ptx::idesc_bf16_f32(BM, BN);
+        // ------------------------------------------------ MMA issuer (rank 0)
+        if (lane == 0 && rank == 0) {
+            constexpr uint32_t idesc = ptx::idesc_bf16_f32(S::kTileRows, BN);
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
             bool any = false;
-            for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
-                const Tile tl = decode_tile<EPI>(p, t);
+            for (int t = unit; t < n_tiles && ok; t += n_units) {
+                const Tile tl = decode_tile<EPI, PAIR>(p, list_len, t);
                 if (!tl.valid) continue;
                 if (!wait_bounded(&ctl->tempty[acc], acc_phase ^ 1u, ctl, p, 200)) { ok = false; break; }
                 ptx::tc_fence_after();
@@ -263,24 +348,29 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
                     if (!wait_bounded(&ctl->full[stage], phase, ctl, p, 201)) { ok = false; break; }
                     ptx::tc_fence_after();
                     const uint32_t a_base = ptx::smem_u32(sA + stage * kABytes);
-                    const uint32_t b_base = ptx::smem_u32(sB + stage * kBBytes);
+                    const uint32_t b_base = ptx::smem_u32(sB + stage * S::kBBytes);
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk) {
                         const uint64_t ad = ptx::sw128_kmajor_desc(a_base + kk * 32);
                         const uint64_t bd = ptx::sw128_kmajor_desc(b_base + kk * 32);
-                        ptx::tc_mma_f16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+                        const uint32_t accum = (kb | kk) != 0 ? 1u : 0u;
+                        if constexpr (PAIR) ptx::tc_mma_f16_pair(d_tmem, ad, bd, idesc, accum);
+                        else ptx::tc_mma_f16(d_tmem, ad, bd, idesc, accum);
                     }
                     any = true;
-                    ptx::tc_commit(&ctl->empty[stage]);
-                    if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                    if constexpr (PAIR) ptx::tc_commit_pair(&ctl->empty[stage], 0x3);
+                    else ptx::tc_commit(&ctl->empty[stage]);
+                    if (++stage == S::kStages) { stage = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
-                ptx::tc_commit(&ctl->tfull[acc]);
+                if constexpr (PAIR) ptx::tc_commit_pair(&ctl->tfull[acc], 0x3);
+                else ptx::tc_commit(&ctl->tfull[acc]);
                 if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
             }
             if (!ok && any) {
-                // drain: every MMA issued completes before TMEM is freed
-                ptx::tc_commit(&ctl->drain);
+                // drain: every MMA issued completes before tensor memory is freed
+                if constexpr (PAIR) ptx::tc_commit_pair(&ctl->drain, 0x3);
+                else ptx::tc_commit(&ctl->drain);
                 const uint64_t t0 = ptx::globaltimer_ns();
                 while (!ptx::mbar_try_wait(&ctl->drain, 0) &&
                        ptx::globaltimer_ns() - t0 < p.timeout_ns) {
@@ -289,20 +379,22 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
         }
     } else {
         // ------------------------------------------------ epilogue (warps 2..5)
-        const int quad = warp & 3;               // TMEM lanes 32*quad .. 32*quad+31
-        const int r = quad * 32 + lane;          // tile row owned by this thread
+        const int quad = warp & 3;       // TMEM lanes 32*quad .. 32*quad+31
+        const int r = quad * 32 + lane;  // accumulator row owned by this thread
+        const uint32_t tempty0 = PAIR ? ptx::map_to_rank(&ctl->tempty[0], 0) : 0u;
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
-            const Tile tl = decode_tile<EPI>(p, t);
+        for (int t = unit; t < n_tiles; t += n_units) {
+            const Tile tl = decode_tile<EPI, PAIR>(p, list_len, t);
             if (!tl.valid) continue;
             // one lane waits, the warp follows its verdict (tcgen05.ld needs the whole warp)
             const int ok = lane == 0 ? (int)wait_bounded(&ctl->tfull[acc], acc_phase, ctl, p, 300) : 0;
             if (!__shfl_sync(0xffffffffu, ok, 0)) break;
             ptx::tc_fence_after();
             const uint32_t tbase = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * BN);
-            const bool row_ok = r < tl.rows;
-            const int64_t orow = (int64_t)tl.row0 + r;
+            const int rows_me = max(0, min(BMC, tl.rows - (int)rank * BMC));
+            const bool row_ok = r < rows_me;
+            const int64_t orow = (int64_t)tl.row0 + (int64_t)rank * BMC + r;
             const int nvalid = p.n_out[tl.kind];
             if (EPI == EPI_SWIGLU) {
                 bf16* out = (bf16*)p.out[tl.kind] + orow * p.ld_out[tl.kind] + tl.n0;
@@ -362,18 +454,23 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
             }
             ptx::tc_fence_before();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&ctl->tempty[acc]);
+            if (lane == 0) {
+                if constexpr (PAIR) ptx::mbar_arrive_cluster(tempty0 + (uint32_t)(acc * sizeof(uint64_t)));
+                else ptx::mbar_arrive(&ctl->tempty[acc]);
+            }
             if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
         }
     }
 
     ptx::tc_fence_before();
-    __syncthreads();
+    cta_sync_all<PAIR>();  // no role touches the other CTA's memory after this
     if (warp == 1) {
         __syncwarp();
         ptx::tc_fence_after();
-        ptx::tmem_dealloc(tmem, kTmemCols);
+        if constexpr (PAIR) ptx::tmem_dealloc_pair(tmem, kTmemCols);
+        else ptx::tmem_dealloc(tmem, kTmemCols);
     }
+    if constexpr (PAIR) cta_sync_all<PAIR>();
 }
 
 // ------------------------------------------------------------------ host side
@@ -422,6 +519,11 @@ bool make_amaps(CUtensorMap (&m)[kABoxes], const void* base, int64_t rows, int64
     return ok;
 }
 
+// weight maps: box 128 rows (pair tiles and SWIGLU halves) and box 256 rows
+bool make_wmaps(TcParams& p, int k, const void* base, int64_t rows, int64_t cols) {
+    return make_map(&p.b0[k], base, rows, cols, 128) && make_map(&p.bw[k], base, rows, cols, 256);
+}
+
 unsigned long long timeout_ns() {
     static const unsigned long long v = [] {
         const char* s = getenv("MOE_TC_TIMEOUT_MS");
@@ -431,20 +533,38 @@ unsigned long long timeout_ns() {
     return v;
 }
 
-constexpr size_t kSmemBytes = 1024 + kStages * kStageBytes + sizeof(SmemCtl) + 64;
+constexpr size_t kSmemBytes = 1024 + kRingBytes + sizeof(SmemCtl) + 64;
 
-template <int EPI>
+template <int EPI, bool PAIR>
 cudaError_t launch_tc(const TcParams& p, cudaStream_t st) {
-    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<EPI>,
+    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<EPI, PAIR>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
-    int grid = device_sm_count();
+    const int sms = device_sm_count();
+    int units = PAIR ? sms / 2 : sms;
     if (p.dense_rows > 0) {
-        const int tiles = (p.dense_rows + BM - 1) / BM * p.NB;
-        if (tiles < grid) grid = tiles;
+        const int tiles = (p.dense_rows + Shape<PAIR>::kTileRows - 1) / Shape<PAIR>::kTileRows * p.NB;
+        if (tiles < units) units = tiles;
     }
-    if (grid < 1) grid = 1;
-    tc_gemm_kernel<EPI><<<grid, kThreadsTc, kSmemBytes, st>>>(p);
+    if (units < 1) units = 1;
+    if constexpr (PAIR) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2 * units);
+        cfg.blockDim = dim3(kThreadsTc);
+        cfg.dynamicSmemBytes = kSmemBytes;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel<EPI, PAIR>, p);
+        if (e != cudaSuccess) return e;
+    } else {
+        tc_gemm_kernel<EPI, PAIR><<<units, kThreadsTc, kSmemBytes, st>>>(p);
+    }
     return cudaGetLastError();
 }
 
@@ -458,27 +578,37 @@ bool tc_available() {
     return major == 10 && minor == 3 && encode_fn() != nullptr;
 }
 
+int tc_tile_rows(bool pair) { return pair ? Shape<true>::kTileRows : Shape<false>::kTileRows; }
+
+// Groups with at least this many rows take 256-row pair tiles.
+int tc_pair_min_rows() {
+    const char* s = getenv("MOE_PAIR_MIN_ROWS");
+    const int x = s ? atoi(s) : 512;
+    return x < 1 ? 1 : x;
+}
+
 cudaError_t launch_ffn_tc(const FfnGroups& g, const FfnPlanHeader* hdr, const int4* mtile_list,
-                          int max_mtiles, DevError* err, cudaStream_t st) {
+                          int max_mtiles, bool may_pair, DevError* err, cudaStream_t st) {
     const int64_t R = g.n_routed_rows;
+    const int4* single_list = mtile_list;
+    const int4* pair_list = mtile_list + max_mtiles;
     // ---- gate/up: h = SiLU(x W_gate^T) * (x W_up^T)
     TcParams p{};
     bool ok = true;
     ok &= make_amaps(p.a[0], g.a_routed, R, g.d);
-    ok &= make_map(&p.b0[0], g.w_gate, (int64_t)g.E * g.I, g.d, BN / 2);
-    ok &= make_map(&p.b1[0], g.w_up, (int64_t)g.E * g.I, g.d, BN / 2);
+    ok &= make_map(&p.b0[0], g.w_gate, (int64_t)g.E * g.I, g.d, 128);
+    ok &= make_map(&p.b1[0], g.w_up, (int64_t)g.E * g.I, g.d, 128);
     if (g.has_shared) {
         ok &= make_amaps(p.a[1], g.a_shared, g.T, g.d);
-        ok &= make_map(&p.b0[1], g.ws_gate, g.Is, g.d, BN / 2);
-        ok &= make_map(&p.b1[1], g.ws_up, g.Is, g.d, BN / 2);
+        ok &= make_map(&p.b0[1], g.ws_gate, g.Is, g.d, 128);
+        ok &= make_map(&p.b1[1], g.ws_up, g.Is, g.d, 128);
     } else {
         for (int b = 0; b < kABoxes; ++b) p.a[1][b] = p.a[0][b];
         p.b0[1] = p.b0[0]; p.b1[1] = p.b1[0];
     }
+    p.bw[0] = p.b0[0]; p.bw[1] = p.b0[1];  // unused by the SWIGLU epilogue
     if (!ok) return cudaErrorInvalidValue;
     p.hdr = hdr;
-    p.mtiles = mtile_list;
-    p.offsets = g.offsets;
     p.E = g.E;
     p.max_mtiles = max_mtiles;
     p.dense_rows = 0;
@@ -491,26 +621,31 @@ cudaError_t launch_ffn_tc(const FfnGroups& g, const FfnPlanHeader* hdr, const in
     p.ld_out[0] = g.I; p.ld_out[1] = g.Is;
     p.err = err;
     p.timeout_ns = timeout_ns();
-    cudaError_t e = launch_tc<EPI_SWIGLU>(p, st);
+    cudaError_t e = cudaSuccess;
+    if (may_pair) {
+        p.mtiles = pair_list;
+        e = launch_tc<EPI_SWIGLU, true>(p, st);
+        if (e != cudaSuccess) return e;
+    }
+    p.mtiles = single_list;
+    e = launch_tc<EPI_SWIGLU, false>(p, st);
     if (e != cudaSuccess) return e;
 
     // ---- down: y = h W_down^T
     TcParams q{};
     ok = true;
     ok &= make_amaps(q.a[0], g.h, R, g.I);
-    ok &= make_map(&q.b0[0], g.w_down, (int64_t)g.E * g.d, g.I, BN);
+    ok &= make_wmaps(q, 0, g.w_down, (int64_t)g.E * g.d, g.I);
     if (g.has_shared) {
         ok &= make_amaps(q.a[1], g.h_s, g.T, g.Is);
-        ok &= make_map(&q.b0[1], g.ws_down, g.d, g.Is, BN);
+        ok &= make_wmaps(q, 1, g.ws_down, g.d, g.Is);
     } else {
         for (int b = 0; b < kABoxes; ++b) q.a[1][b] = q.a[0][b];
-        q.b0[1] = q.b0[0];
+        q.b0[1] = q.b0[0]; q.bw[1] = q.bw[0];
     }
     q.b1[0] = q.b0[0]; q.b1[1] = q.b0[1];
     if (!ok) return cudaErrorInvalidValue;
     q.hdr = hdr;
-    q.mtiles = mtile_list;
-    q.offsets = g.offsets;
     q.E = g.E;
     q.max_mtiles = max_mtiles;
     q.dense_rows = 0;
@@ -522,19 +657,25 @@ cudaError_t launch_ffn_tc(const FfnGroups& g, const FfnPlanHeader* hdr, const in
     q.ld_out[0] = g.d; q.ld_out[1] = g.d;
     q.err = err;
     q.timeout_ns = timeout_ns();
-    return launch_tc<EPI_STORE_BF16>(q, st);
+    if (may_pair) {
+        q.mtiles = pair_list;
+        e = launch_tc<EPI_STORE_BF16, true>(q, st);
+        if (e != cudaSuccess) return e;
+    }
+    q.mtiles = single_list;
+    return launch_tc<EPI_STORE_BF16, false>(q, st);
 }
 
-// scores[T][E] (fp32) = x w_g^T on the tensor cores
+// scores[T][E] (fp32) = x w_g^T on the tensor cores (single tiles)
 cudaError_t launch_router_tc(const moe_shape& s, const void* x, const void* w_g, float* scores,
                              DevError* err, cudaStream_t st) {
     TcParams p{};
     bool ok = true;
     ok &= make_amaps(p.a[1], x, s.T, s.d);
-    ok &= make_map(&p.b0[1], w_g, s.E, s.d, BN);
+    ok &= make_wmaps(p, 1, w_g, s.E, s.d);
     if (!ok) return cudaErrorInvalidValue;
     for (int b = 0; b < kABoxes; ++b) p.a[0][b] = p.a[1][b];
-    p.b0[0] = p.b0[1]; p.b1[0] = p.b0[1]; p.b1[1] = p.b0[1];
+    p.b0[0] = p.b0[1]; p.bw[0] = p.bw[1]; p.b1[0] = p.b0[1]; p.b1[1] = p.b0[1];
     p.hdr = nullptr;
     p.mtiles = nullptr;
     p.dense_rows = s.T;
@@ -546,7 +687,7 @@ cudaError_t launch_router_tc(const moe_shape& s, const void* x, const void* w_g,
     p.ld_out[0] = p.ld_out[1] = s.E;
     p.err = err;
     p.timeout_ns = timeout_ns();
-    return launch_tc<EPI_STORE_F32>(p, st);
+    return launch_tc<EPI_STORE_F32, false>(p, st);
 }
 
 }  // namespace moe

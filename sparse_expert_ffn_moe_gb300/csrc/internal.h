@@ -17,8 +17,9 @@ struct DevError;
 // group E (when present) is the shared expert, whose rows are the T tokens.
 struct FfnPlanHeader {
     int32_t n_gemv;    // groups handled by the streaming GEMV kernels
-    int32_t n_mtiles;  // 128-row tiles handled by the tensor-core GEMM
-    int32_t pad[2];
+    int32_t n_mtiles;  // 128-row tiles of the single-SM tensor-core GEMM
+    int32_t n_ptiles;  // 256-row tiles of the CTA-pair tensor-core GEMM
+    int32_t pad;
 };
 
 // One routed/shared expert group as the FFN kernels see it.
@@ -72,6 +73,7 @@ cudaError_t launch_gather_rows(const moe_shape& s, const void* x, const int32_t*
 
 // ---- ffn_plan + ffn_gemv.cu ----
 int gemv_max_rows();  // groups with at most this many rows take the GEMV path
+// mtile_list holds 2 * max_mtiles entries: single-SM tiles, then pair tiles.
 cudaError_t launch_ffn_plan(const FfnGroups& g, int dtype, FfnPlanHeader* hdr,
                             int32_t* gemv_list, int4* mtile_list, int max_mtiles,
                             int gemv_limit, cudaStream_t st);
@@ -80,8 +82,12 @@ cudaError_t launch_ffn_gemv(const FfnGroups& g, int dtype, const FfnPlanHeader* 
 
 // ---- ffn_tc.cu (tcgen05 grouped GEMM) ----
 bool tc_available();
+int tc_tile_rows(bool pair);  // rows per tensor-core m-tile (single-SM or CTA pair)
+int tc_pair_min_rows();       // groups with at least this many rows take pair tiles
+// may_pair: some group can reach tc_pair_min_rows() rows (else the pair
+// launches are skipped)
 cudaError_t launch_ffn_tc(const FfnGroups& g, const FfnPlanHeader* hdr, const int4* mtile_list,
-                          int max_mtiles, DevError* err, cudaStream_t st);
+                          int max_mtiles, bool may_pair, DevError* err, cudaStream_t st);
 cudaError_t launch_router_tc(const moe_shape& s, const void* x, const void* w_g, float* scores,
                              DevError* err, cudaStream_t st);
 

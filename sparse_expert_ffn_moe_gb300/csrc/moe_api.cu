@@ -104,7 +104,7 @@ WsLayout ws_layout(const moe_shape& s) {
     L.blk_hist = take(sizeof(int32_t) * (size_t)L.dispatch_blocks * E);
     L.plan = take(sizeof(FfnPlanHeader));
     L.gemv_list = take(sizeof(int32_t) * (E + 1));
-    L.mtile_list = take(sizeof(int4) * (size_t)L.max_mtiles);
+    L.mtile_list = take(sizeof(int4) * 2 * (size_t)L.max_mtiles);  // single, then pair tiles
     L.x_perm = take(es * n * d);
     L.h = take(es * n * I);
     L.h_s = take(es * T * Is);
@@ -242,7 +242,8 @@ moe_status moe_expert_ffn(const moe_shape* shape, const void* x_perm, const int3
     int4* mtiles = at<int4>(workspace, L.mtile_list);
     e = launch_ffn_plan(g, s.dtype, hdr, glist, mtiles, L.max_mtiles, gemv_limit(), cs);
     if (e == cudaSuccess) e = launch_ffn_gemv(g, s.dtype, hdr, glist, cs);
-    if (e == cudaSuccess && need_tc) e = launch_ffn_tc(g, hdr, mtiles, L.max_mtiles, err, cs);
+    if (e == cudaSuccess && need_tc)
+        e = launch_ffn_tc(g, hdr, mtiles, L.max_mtiles, rows >= tc_pair_min_rows(), err, cs);
     return cuda_status(e);
 }
 
@@ -343,7 +344,9 @@ moe_status moe_forward(const moe_shape* shape, const void* x, const void* w_g, c
     int4* mtiles = at<int4>(workspace, L.mtile_list);
     e = launch_ffn_plan(g, s.dtype, hdr, glist, mtiles, L.max_mtiles, gemv_limit(), cs);
     if (e == cudaSuccess) e = launch_ffn_gemv(g, s.dtype, hdr, glist, cs);
-    if (e == cudaSuccess && need_tc) e = launch_ffn_tc(g, hdr, mtiles, L.max_mtiles, err, cs);
+    // a group has at most T rows (a token picks an expert once)
+    if (e == cudaSuccess && need_tc)
+        e = launch_ffn_tc(g, hdr, mtiles, L.max_mtiles, s.T >= tc_pair_min_rows(), err, cs);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
 
     // 4. combine

@@ -89,3 +89,17 @@ class Layer:
         torch.cuda.synchronize()
         assert moe.moe_get_device_error(ws) == 0
         return y
+
+
+@contextmanager
+def pair_min_rows(n: int):
+    """Groups with at least n rows take the 256-row CTA-pair tiles (read per call)."""
+    old = os.environ.get("MOE_PAIR_MIN_ROWS")
+    os.environ["MOE_PAIR_MIN_ROWS"] = str(n)
+    try:
+        yield
+    finally:
+        if old is None:
+            del os.environ["MOE_PAIR_MIN_ROWS"]
+        else:
+            os.environ["MOE_PAIR_MIN_ROWS"] = old

@@ -84,3 +84,16 @@ def test_paths_agree_closely(moe):
     y_t, _ = _run(moe, counts, 512, 256, "bf16", limit=0)
     assert rel_l2(y_g, y_t) <= 1e-2
     assert rel_l2(y_t, ref) <= BF16_REL_L2
+
+
+@pytest.mark.parametrize("counts,d,I", CASES + [([1100, 0, 257, 640, 1, 128, 0, 900], 512, 256)])
+@pytest.mark.parametrize("pair_min", [1, 1 << 30])
+def test_tensor_core_tile_shapes(moe, counts, d, I, pair_min):
+    """Every group on 256-row CTA-pair tiles (pair_min=1) or on 128-row single-SM
+    tiles (pair_min huge)."""
+    from tests.gpu_util import pair_min_rows
+    with pair_min_rows(pair_min):
+        y, ref = _run(moe, counts, d, I, "bf16", limit=0, seed=5)
+    assert rel_l2(y, ref) <= BF16_REL_L2
+    for r in range(y.shape[0]):
+        assert rel_l2(y[r], ref[r]) <= 2 * BF16_REL_L2, r
