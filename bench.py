@@ -69,12 +69,15 @@ def layer_bytes(cfg, n_active: int) -> int:
 def launches_per_forward(cfg, gemv_limit: int = 0, pair_min: int = 512) -> int:
     """Kernels libmoe launches for one moe_forward (mirrors the host logic in
     moe_api.cu): router (GEMV or tcgen05) + top-K, 3 dispatch kernels, the row
-    gather when the tensor-core path may run, the FFN plan, 2 GEMV kernels,
-    the single-SM tcgen05 gate/up and down GEMMs when needed, and the CTA-pair
+    gather when the tensor-core path may run, the FFN plan,
+    (2 GEMV kernels only for fp32 layers or a non-zero GEMV row limit), the
+    single-SM tcgen05 gate/up and down GEMMs when needed, and the CTA-pair
     ones too when a group can reach pair_min rows, combine."""
     need_tc = cfg.dtype == "bf16" and cfg.T > gemv_limit
+    gemv = cfg.dtype == "f32" or gemv_limit > 0
     pair = need_tc and cfg.T >= pair_min
-    return 2 + 3 + (1 if need_tc else 0) + 1 + 2 + (2 if need_tc else 0) + (2 if pair else 0) + 1
+    return (2 + 3 + (1 if need_tc else 0) + 1 + (2 if gemv else 0) + (2 if need_tc else 0)
+            + (2 if pair else 0) + 1)
 
 
 # --------------------------------------------------------------------------- helpers
@@ -228,6 +231,7 @@ def run_ours(args):
     ws = moe.alloc_workspace(s)
     y = torch.empty_like(x)
     stream = torch.cuda.Stream()
+    torch.cuda.synchronize()  # every input is written before the side stream reads it
 
     def fwd(xx=x, yy=y):
         moe.moe_forward(s, xx, p["w_g"], bias, p["w_gate"], p["w_up"], p["w_down"],
@@ -300,6 +304,10 @@ def run_ours(args):
         result["decode"] = bench_decode(moe, peaks, args)
     if args.all and rank == 0:
         result["workloads"] = bench_all(moe, peaks, args)
+    if args.sweep_T and rank == 0:
+        result["sweep"] = [bench_workload(moe, cfg.with_T(int(t)), peaks, steps=max(10, args.steps),
+                                          graph=False)
+                           for t in args.sweep_T.split(",")]
     if not args.no_cpu_baseline and rank == 0:
         torch.cuda.synchronize()
         hp = {k: mi.to_host_array(v) for k, v in p.items()}
@@ -315,6 +323,7 @@ def run_ours(args):
 
 def count_active(moe, cfg, x, p, bias, stream) -> int:
     import torch
+    torch.cuda.synchronize()  # inputs were drawn on torch's current stream
     s = moe.make_shape(cfg.T, cfg.d, cfg.E, cfg.K, cfg.I, cfg.Is, cfg.dtype)
     ws = moe.alloc_workspace(s)
     idx = torch.empty((cfg.T, cfg.K), dtype=torch.int32, device="cuda")
@@ -336,6 +345,7 @@ def time_expert_ffn(moe, cfg, x, p, bias, stream, steps: int) -> dict:
     offsets = torch.empty(cfg.E + 1, dtype=torch.int32, device="cuda")
     x_perm = torch.empty((n, cfg.d), dtype=x.dtype, device="cuda")
     y_perm = torch.empty((n, cfg.d), dtype=x.dtype, device="cuda")
+    torch.cuda.synchronize()
     moe.moe_route(s, x, p["w_g"], bias, None, None, idx, w, ws, stream=stream)
     moe.moe_permute(s, idx, x, counts, offsets, None, None, x_perm, ws, stream=stream)
 
@@ -433,6 +443,7 @@ def bench_workload(moe, cfg, peaks, steps: int, graph: bool = False) -> dict:
     ws = moe.alloc_workspace(s)
     y = torch.empty_like(x)
     st = torch.cuda.Stream()
+    torch.cuda.synchronize()  # every input is written before the side stream reads it
     n_active = count_active(moe, cfg, x, p, bias, st)
 
     def fwd():
@@ -547,6 +558,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--all", action="store_true", help="also time every workload")
+    ap.add_argument("--sweep-T", default="", help="comma-separated token counts: time the "
+                    "workload's shapes at each T (one JSON object per T under 'sweep')")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3

@@ -54,6 +54,9 @@ P* at(void* ws, size_t off) {
 // Groups whose row count exceeds this take the tensor-core path.
 int gemv_limit() { return gemv_max_rows(); }
 
+// The GEMV kernels can get work only for fp32 layers or with a non-zero row limit.
+bool gemv_possible(const moe_shape& s) { return s.dtype == MOE_F32 || gemv_limit() > 0; }
+
 bool use_tc_router(const moe_shape& s) {
     return s.dtype == MOE_BF16 && s.T >= 128 && s.E >= 64;
 }
@@ -241,7 +244,7 @@ moe_status moe_expert_ffn(const moe_shape* shape, const void* x_perm, const int3
     int32_t* glist = at<int32_t>(workspace, L.gemv_list);
     int4* mtiles = at<int4>(workspace, L.mtile_list);
     e = launch_ffn_plan(g, s.dtype, hdr, glist, mtiles, L.max_mtiles, gemv_limit(), cs);
-    if (e == cudaSuccess) e = launch_ffn_gemv(g, s.dtype, hdr, glist, cs);
+    if (e == cudaSuccess && gemv_possible(s)) e = launch_ffn_gemv(g, s.dtype, hdr, glist, cs);
     if (e == cudaSuccess && need_tc)
         e = launch_ffn_tc(g, hdr, mtiles, L.max_mtiles, rows >= tc_pair_min_rows(), err, cs);
     return cuda_status(e);
@@ -343,7 +346,7 @@ moe_status moe_forward(const moe_shape* shape, const void* x, const void* w_g, c
     int32_t* glist = at<int32_t>(workspace, L.gemv_list);
     int4* mtiles = at<int4>(workspace, L.mtile_list);
     e = launch_ffn_plan(g, s.dtype, hdr, glist, mtiles, L.max_mtiles, gemv_limit(), cs);
-    if (e == cudaSuccess) e = launch_ffn_gemv(g, s.dtype, hdr, glist, cs);
+    if (e == cudaSuccess && gemv_possible(s)) e = launch_ffn_gemv(g, s.dtype, hdr, glist, cs);
     // a group has at most T rows (a token picks an expert once)
     if (e == cudaSuccess && need_tc)
         e = launch_ffn_tc(g, hdr, mtiles, L.max_mtiles, s.T >= tc_pair_min_rows(), err, cs);
