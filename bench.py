@@ -369,7 +369,7 @@ def time_expert_ffn(moe, cfg, x, p, bias, stream, steps: int) -> dict:
 # ncu capture per workload (profiles/ffn_stage_traffic_<workload>.md), valid only for
 # the ffn_tc.cu source it was taken on (sha256 prefix).
 STAGE_TRAFFIC = {
-    "mixtral_prefill": {"bytes": 4386545408, "ffn_tc_sha256": "c9900769c6fa0a63"},
+    "mixtral_prefill": {"bytes": 4507861760, "ffn_tc_sha256": "50a74337d372d7dc"},
 }
 
 
