@@ -116,6 +116,7 @@ struct TcParams {
     int64_t ld_out[2];  // output row stride (elements)
     DevError* err;
     unsigned long long timeout_ns;
+    int test_stall;  // test hook: the producer issues no copy, so the bounded waits run out
 };
 
 struct Tile {
@@ -267,7 +268,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
             bool issued[kMaxStages];
             for (int s = 0; s < kMaxStages; ++s) { issued[s] = false; issued_phase[s] = 0; }
             const uint32_t full0 = PAIR ? ptx::map_to_rank(&ctl->full[0], 0) : 0u;
-            bool ok = true;
+            bool ok = p.test_stall == 0;
             for (int t = unit; t < n_tiles && ok; t += n_units) {
                 const Tile tl = decode_tile<EPI, PAIR>(p, list_len, t);
                 if (!tl.valid) continue;
@@ -524,13 +525,19 @@ bool make_wmaps(TcParams& p, int k, const void* base, int64_t rows, int64_t cols
     return make_map(&p.b0[k], base, rows, cols, 128) && make_map(&p.bw[k], base, rows, cols, 256);
 }
 
+// Read on every call (a test shortens it to see a wait run out quickly).
 unsigned long long timeout_ns() {
-    static const unsigned long long v = [] {
-        const char* s = getenv("MOE_TC_TIMEOUT_MS");
-        const long long ms = s ? atoll(s) : 1000;
-        return (unsigned long long)(ms > 0 ? ms : 1000) * 1000000ull;
-    }();
-    return v;
+    const char* s = getenv("MOE_TC_TIMEOUT_MS");
+    const long long ms = s ? atoll(s) : 1000;
+    return (unsigned long long)(ms > 0 ? ms : 1000) * 1000000ull;
+}
+
+// Test hook (off unless MOE_TC_TEST_STALL is set to a non-zero value): the
+// producer issues no copy, so the MMA's bounded wait runs out and the kernel
+// must report MOE_ERR_TIMEOUT and return with the context intact.
+int test_stall() {
+    const char* s = getenv("MOE_TC_TEST_STALL");
+    return (s && atoi(s) != 0) ? 1 : 0;
 }
 
 constexpr size_t kSmemBytes = 1024 + kRingBytes + sizeof(SmemCtl) + 64;
@@ -621,6 +628,7 @@ cudaError_t launch_ffn_tc(const FfnGroups& g, const FfnPlanHeader* hdr, const in
     p.ld_out[0] = g.I; p.ld_out[1] = g.Is;
     p.err = err;
     p.timeout_ns = timeout_ns();
+    p.test_stall = test_stall();
     cudaError_t e = cudaSuccess;
     if (may_pair) {
         p.mtiles = pair_list;
@@ -657,6 +665,7 @@ cudaError_t launch_ffn_tc(const FfnGroups& g, const FfnPlanHeader* hdr, const in
     q.ld_out[0] = g.d; q.ld_out[1] = g.d;
     q.err = err;
     q.timeout_ns = timeout_ns();
+    q.test_stall = test_stall();
     if (may_pair) {
         q.mtiles = pair_list;
         e = launch_tc<EPI_STORE_BF16, true>(q, st);
@@ -687,6 +696,7 @@ cudaError_t launch_router_tc(const moe_shape& s, const void* x, const void* w_g,
     p.ld_out[0] = p.ld_out[1] = s.E;
     p.err = err;
     p.timeout_ns = timeout_ns();
+    p.test_stall = test_stall();
     return launch_tc<EPI_STORE_F32, false>(p, st);
 }
 

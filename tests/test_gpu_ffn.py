@@ -97,3 +97,31 @@ def test_tensor_core_tile_shapes(moe, counts, d, I, pair_min):
     assert rel_l2(y, ref) <= BF16_REL_L2
     for r in range(y.shape[0]):
         assert rel_l2(y[r], ref[r]) <= 2 * BF16_REL_L2, r
+
+
+def test_bounded_wait_reports_timeout_and_the_context_survives(moe, monkeypatch):
+    """Failure detection without a fault: a test-only flag makes the tcgen05
+    producer issue no copy, so the MMA's wait (limited to 50 ms here) runs out.
+    The kernel must record MOE_ERR_TIMEOUT in the workspace error word, free its
+    tensor memory and return; the next call on the same context must succeed."""
+    counts = [40, 3, 0, 77]
+    with gemv_limit(0):
+        monkeypatch.setenv("MOE_PAIR_MIN_ROWS", str(1 << 30))  # single-SM tiles only
+        monkeypatch.setenv("MOE_TC_TIMEOUT_MS", "50")
+        monkeypatch.setenv("MOE_TC_TEST_STALL", "1")
+        offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+        rows = int(offsets[-1])
+        cfg = mi.LayerConfig("stall", T=rows, d=256, E=4, K=1, I=256)
+        p = mi.make_weights(cfg, "cuda", only={"w_gate", "w_up", "w_down"})
+        x_perm = mi.normal((rows, 256), 1.0, "bf16", "cuda", 0, "x_perm")
+        s = moe.make_shape(rows, 256, 4, 1, 256, 0, "bf16")
+        ws = moe.alloc_workspace(s)
+        y = torch.zeros((rows, 256), dtype=torch.bfloat16, device="cuda")
+        off_d = torch.from_numpy(offsets).cuda()
+        moe.moe_expert_ffn(s, x_perm, off_d, p["w_gate"], p["w_up"], p["w_down"], y, ws)
+        torch.cuda.synchronize()
+        assert moe.moe_get_device_error(ws) == moe.MOE_ERR_TIMEOUT
+        monkeypatch.delenv("MOE_TC_TEST_STALL")
+        monkeypatch.delenv("MOE_TC_TIMEOUT_MS")
+        y_ok, ref = _run(moe, counts, 256, 256, "bf16", limit=0)
+    assert rel_l2(y_ok, ref) <= BF16_REL_L2
