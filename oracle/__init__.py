@@ -31,6 +31,9 @@ _lock = threading.Lock()
 _lib = None
 
 _DT = {"f32": 0, "bf16": 1}
+# router: "softmax" = softmax over the K selected scores (+ bias);
+# "sigmoid" = DeepSeek-V3 affinities, bias for selection only, a / (sum a + 1e-6)
+_ROUTER = {"softmax": 0, "sigmoid": 1}
 
 
 def compile_c(src: str, out: str) -> str:
@@ -57,13 +60,13 @@ def bind(lib):
     """Declare the C signatures on a loaded liboracle handle."""
     i64, i32, vp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
     lib.oracle_default_threads.restype = i32
-    lib.oracle_route.argtypes = [i64, i64, i64, i64, i32, vp, vp, vp, vp, vp, vp, vp, i32]
+    lib.oracle_route.argtypes = [i64, i64, i64, i64, i32, i32, vp, vp, vp, vp, vp, vp, vp, i32]
     lib.oracle_permute.argtypes = [i64, i64, i64, vp, vp, vp, vp, vp]
     lib.oracle_expert_ffn.argtypes = [i64, i64, i64, i32, vp, vp, vp, vp, vp, vp, i32]
     lib.oracle_combine.argtypes = [i64, i64, i64, vp, vp, vp, vp, vp]
     lib.oracle_shared_ffn.argtypes = [i64, i64, i64, i32, vp, vp, vp, vp, vp, i32]
-    lib.oracle_forward.argtypes = [i64] * 6 + [i32] + [vp] * 16 + [i32]
-    lib.oracle_forward_tokens.argtypes = [i64, vp] + [i64] * 6 + [i32] + [vp] * 13 + [i32]
+    lib.oracle_forward.argtypes = [i64] * 6 + [i32, i32] + [vp] * 16 + [i32]
+    lib.oracle_forward_tokens.argtypes = [i64, vp] + [i64] * 6 + [i32, i32] + [vp] * 13 + [i32]
     for f in ("oracle_route", "oracle_permute", "oracle_expert_ffn", "oracle_combine",
               "oracle_shared_ffn", "oracle_forward", "oracle_forward_tokens"):
         getattr(lib, f).restype = i32
@@ -105,10 +108,13 @@ def _check(rc: int, name: str):
         raise ValueError(f"{name}: oracle rejected its arguments (rc={rc})")
 
 
-def route(x, w_g, K: int, dtype: str = "f32", bias=None, logits_in=None, threads: int = 0):
-    """Top-K routing.  Returns (topk_idx [T,K] int32, topk_w [T,K] f64, logits [T,E] f64).
+def route(x, w_g, K: int, dtype: str = "f32", bias=None, logits_in=None, threads: int = 0,
+          router: str = "softmax"):
+    """Top-K routing.  Returns (topk_idx [T,K] int32, topk_w [T,K] f64, keys [T,E] f64),
+    keys being the values the selection compares (softmax: score + bias; sigmoid:
+    sigmoid(score) + bias).
 
-    With ``logits_in`` (fp32 [T,E]) those scores are used as given."""
+    With ``logits_in`` (fp32 [T,E]) those raw scores replace x . w_g^T."""
     lib = _load()
     if logits_in is not None:
         logits_in = _arr(logits_in, np.float32)
@@ -123,7 +129,7 @@ def route(x, w_g, K: int, dtype: str = "f32", bias=None, logits_in=None, threads
     idx = np.zeros((T, K), np.int32)
     w = np.zeros((T, K), np.float64)
     logits = np.zeros((T, E), np.float64)
-    _check(lib.oracle_route(T, d, E, K, _DT[dtype], _ptr(x), _ptr(w_g), _ptr(bias),
+    _check(lib.oracle_route(T, d, E, K, _DT[dtype], _ROUTER[router], _ptr(x), _ptr(w_g), _ptr(bias),
                             _ptr(logits_in), _ptr(logits), _ptr(idx), _ptr(w), threads),
            "oracle_route")
     return idx, w, logits
@@ -191,7 +197,8 @@ def _weights(p: dict, dtype: str):
     return {n: _in(p.get(n), dtype) for n in names}
 
 
-def forward(x, params: dict, K: int, dtype: str = "f32", bias=None, threads: int = 0):
+def forward(x, params: dict, K: int, dtype: str = "f32", bias=None, threads: int = 0,
+            router: str = "softmax"):
     """The whole layer for all T tokens (route, permute, expert FFN, shared, combine).
 
     ``params`` holds w_g [E,d], w_gate/w_up [E,I,d], w_down [E,d,I] and optionally
@@ -214,7 +221,8 @@ def forward(x, params: dict, K: int, dtype: str = "f32", bias=None, threads: int
         "inv_perm": np.zeros(T * K, np.int32),
     }
     _check(lib.oracle_forward(
-        T, d, E, K, I, Is, _DT[dtype], _ptr(x), _ptr(w["w_g"]), _ptr(bias), _ptr(w["w_gate"]),
+        T, d, E, K, I, Is, _DT[dtype], _ROUTER[router], _ptr(x), _ptr(w["w_g"]), _ptr(bias),
+        _ptr(w["w_gate"]),
         _ptr(w["w_up"]), _ptr(w["w_down"]), _ptr(w["ws_gate"]), _ptr(w["ws_up"]),
         _ptr(w["ws_down"]), _ptr(out["y"]), _ptr(out["topk_idx"]), _ptr(out["topk_w"]),
         _ptr(out["counts"]), _ptr(out["offsets"]), _ptr(out["perm"]), _ptr(out["inv_perm"]),
@@ -223,7 +231,7 @@ def forward(x, params: dict, K: int, dtype: str = "f32", bias=None, threads: int
 
 
 def forward_tokens(tokens, x, params: dict, K: int, dtype: str = "f32", bias=None,
-                   threads: int = 0):
+                   threads: int = 0, router: str = "softmax"):
     """The layer output for the listed tokens only, from the per-token definition.
 
     Returns a dict: y [n,d], topk_idx [n,K], topk_w [n,K], logits [n,E]."""
@@ -243,7 +251,8 @@ def forward_tokens(tokens, x, params: dict, K: int, dtype: str = "f32", bias=Non
         "logits": np.zeros((n, E), np.float64),
     }
     _check(lib.oracle_forward_tokens(
-        n, _ptr(tokens), T, d, E, K, I, Is, _DT[dtype], _ptr(x), _ptr(w["w_g"]), _ptr(bias),
+        n, _ptr(tokens), T, d, E, K, I, Is, _DT[dtype], _ROUTER[router], _ptr(x), _ptr(w["w_g"]),
+        _ptr(bias),
         _ptr(w["w_gate"]), _ptr(w["w_up"]), _ptr(w["w_down"]), _ptr(w["ws_gate"]),
         _ptr(w["ws_up"]), _ptr(w["ws_down"]), _ptr(out["y"]), _ptr(out["topk_idx"]),
         _ptr(out["topk_w"]), _ptr(out["logits"]), threads), "oracle_forward_tokens")

@@ -139,45 +139,74 @@ static void par_for(int64_t n, int nthreads, row_fn fn, void *ctx)
 /* stage 1: router scores, top-K, softmax over the K selected               */
 /* ------------------------------------------------------------------------ */
 
-/* s_e = sum_k x[k] * w_g[e][k] (+ b_e).  The gate network is a linear map
- * with one score per expert (explainer section 2.2, step 1; llmgo page
- * section 2.1). */
+#define ORC_ROUTER_SOFTMAX 0
+#define ORC_ROUTER_SIGMOID 1
+
+/* s_e = sum_k x[k] * w_g[e][k], the raw router score.  The gate network is a
+ * linear map with one score per expert (explainer section 2.2, step 1; llmgo
+ * page section 2.1). */
 static void router_scores(int64_t d, int64_t E, int dtype, const void *x,
-                          int64_t t, const void *w_g, const double *bias,
-                          double *s)
+                          int64_t t, const void *w_g, double *s)
 {
     for (int64_t e = 0; e < E; ++e) {
         double acc = 0.0;
         for (int64_t k = 0; k < d; ++k)
             acc += load_elem(x, dtype, t * d + k) * load_elem(w_g, dtype, e * d + k);
-        s[e] = acc + (bias ? bias[e] : 0.0);
+        s[e] = acc;
     }
 }
 
-/* Pick the K largest scores one at a time; a strictly larger score replaces
- * the current best while scanning e upward, so among equal scores the lower
- * index is kept.  Slot j holds the j-th pick (descending score).  Then
- * w_j = exp(s_{i_j} - s_{i_0}) / sum_j' exp(s_{i_j'} - s_{i_0}), the softmax
- * over only the K selected scores (explainer section 2.2, steps 2-3). */
-static void select_and_weigh(int64_t E, int64_t K, const double *s,
+/* Selection keys, then the K picks and their weights.
+ *
+ * Softmax router (explainer section 2.2, steps 2-3): key_e = s_e + b_e;
+ * w_j = exp(key_{i_j} - key_{i_0}) / sum_j' exp(key_{i_j'} - key_{i_0}), the
+ * softmax over only the K selected keys.
+ *
+ * Sigmoid router (DeepSeek-V3 auxiliary-loss-free routing, llmgo page section
+ * 2.2 and the dispatcher code of section 4.3): affinity a_e = 1/(1+exp(-s_e));
+ * key_e = a_e + b_e, the bias steering the selection only; the weights use
+ * the affinities alone, w_j = a_{i_j} / (sum_j' a_{i_j'} + 1e-6) (the code's
+ * form; the section's formula omits the 1e-6 guard).
+ *
+ * Picks: the K largest keys one at a time; a strictly larger key replaces the
+ * current best while scanning e upward, so among equal keys the lower index is
+ * kept.  Slot j holds the j-th pick (descending key). */
+static void select_and_weigh(int mode, int64_t E, int64_t K, const double *s,
+                             const double *bias, double *key, double *aff,
                              unsigned char *taken, int32_t *idx, double *w)
 {
+    for (int64_t e = 0; e < E; ++e) {
+        const double b = bias ? bias[e] : 0.0;
+        if (mode == ORC_ROUTER_SIGMOID) {
+            aff[e] = 1.0 / (1.0 + exp(-s[e]));
+            key[e] = aff[e] + b;
+        } else {
+            key[e] = s[e] + b;
+        }
+    }
     memset(taken, 0, (size_t)E);
     for (int64_t j = 0; j < K; ++j) {
         int64_t best = -1;
         for (int64_t e = 0; e < E; ++e) {
             if (taken[e])
                 continue;
-            if (best < 0 || s[e] > s[best])
+            if (best < 0 || key[e] > key[best])
                 best = e;
         }
         taken[best] = 1;
         idx[j] = (int32_t)best;
     }
-    const double smax = s[idx[0]];
     double denom = 0.0;
+    if (mode == ORC_ROUTER_SIGMOID) {
+        for (int64_t j = 0; j < K; ++j)
+            denom += aff[idx[j]];
+        for (int64_t j = 0; j < K; ++j)
+            w[j] = aff[idx[j]] / (denom + 1e-6);
+        return;
+    }
+    const double kmax = key[idx[0]];
     for (int64_t j = 0; j < K; ++j) {
-        w[j] = exp(s[idx[j]] - smax);
+        w[j] = exp(key[idx[j]] - kmax);
         denom += w[j];
     }
     for (int64_t j = 0; j < K; ++j)
@@ -186,7 +215,7 @@ static void select_and_weigh(int64_t E, int64_t K, const double *s,
 
 typedef struct {
     int64_t d, E, K;
-    int dtype;
+    int dtype, mode;
     const void *x, *w_g;
     const double *bias;
     const float *logits_in;
@@ -198,37 +227,42 @@ typedef struct {
 static void route_row(void *vctx, int64_t t)
 {
     route_ctx *c = (route_ctx *)vctx;
-    double *s = (double *)malloc(sizeof(double) * (size_t)c->E);
+    double *s = (double *)malloc(sizeof(double) * (size_t)c->E * 3);
+    double *key = s + c->E, *aff = s + 2 * c->E;
     unsigned char *taken = (unsigned char *)malloc((size_t)c->E);
     if (c->logits_in) {
         for (int64_t e = 0; e < c->E; ++e)
             s[e] = (double)c->logits_in[t * c->E + e];
     } else {
-        router_scores(c->d, c->E, c->dtype, c->x, t, c->w_g, c->bias, s);
+        router_scores(c->d, c->E, c->dtype, c->x, t, c->w_g, s);
     }
+    select_and_weigh(c->mode, c->E, c->K, s, c->bias, key, aff, taken,
+                     c->topk_idx + t * c->K, c->topk_w + t * c->K);
     if (c->logits_out)
-        memcpy(c->logits_out + t * c->E, s, sizeof(double) * (size_t)c->E);
-    select_and_weigh(c->E, c->K, s, taken, c->topk_idx + t * c->K, c->topk_w + t * c->K);
+        memcpy(c->logits_out + t * c->E, key, sizeof(double) * (size_t)c->E);
     free(s);
     free(taken);
 }
 
 /*
- * oracle_route: scores, top-K and K-way softmax for T tokens.
- * If logits_in is non-NULL its fp32 values are the scores (x, w_g and bias are
- * then ignored); otherwise scores are x . w_g^T (+ bias) in fp64.
- * logits_out [T][E] (optional) receives the scores used.
+ * oracle_route: scores, top-K and weights for T tokens; mode 0 = softmax
+ * router, 1 = sigmoid router (see select_and_weigh).  Raw scores are
+ * x . w_g^T in fp64, or the fp32 values of logits_in when it is non-NULL
+ * (x and w_g are then ignored); bias (may be NULL) enters the keys either way.
+ * logits_out [T][E] (optional) receives the selection keys.
  */
 int oracle_route(int64_t T, int64_t d, int64_t E, int64_t K, int dtype,
-                 const void *x, const void *w_g, const double *bias,
+                 int mode, const void *x, const void *w_g, const double *bias,
                  const float *logits_in, double *logits_out,
                  int32_t *topk_idx, double *topk_w, int nthreads)
 {
     if (T < 0 || E < 1 || K < 1 || K > E || !topk_idx || !topk_w)
         return -1;
+    if (mode != ORC_ROUTER_SOFTMAX && mode != ORC_ROUTER_SIGMOID)
+        return -1;
     if (!logits_in && (!x || !w_g || d < 1))
         return -1;
-    route_ctx c = {d, E, K, dtype, x, w_g, bias, logits_in, logits_out, topk_idx, topk_w};
+    route_ctx c = {d, E, K, dtype, mode, x, w_g, bias, logits_in, logits_out, topk_idx, topk_w};
     par_for(T, nthreads, route_row, &c);
     return 0;
 }
@@ -434,10 +468,11 @@ int oracle_shared_ffn(int64_t T, int64_t d, int64_t Is, int dtype,
  * oracle_forward: route -> permute (+ gather x rows into expert order) ->
  * expert FFN -> shared expert -> combine, for all T tokens.  Outputs in fp64:
  * y [T][d]; optional topk_idx [T][K], topk_w [T][K], counts [E],
- * offsets [E+1], perm / inv_perm [T*K].  Is == 0 means no shared expert.
+ * offsets [E+1], perm / inv_perm [T*K].  Is == 0 means no shared expert;
+ * mode selects the router (0 softmax, 1 sigmoid; see select_and_weigh).
  */
 int oracle_forward(int64_t T, int64_t d, int64_t E, int64_t K, int64_t I,
-                   int64_t Is, int dtype, const void *x, const void *w_g,
+                   int64_t Is, int dtype, int mode, const void *x, const void *w_g,
                    const double *bias, const void *w_gate, const void *w_up,
                    const void *w_down, const void *ws_gate, const void *ws_up,
                    const void *ws_down, double *y, int32_t *topk_idx_out,
@@ -458,7 +493,7 @@ int oracle_forward(int64_t T, int64_t d, int64_t E, int64_t K, int64_t I,
     unsigned char *x_perm = (unsigned char *)malloc(es * (size_t)(n ? n : 1) * (size_t)d);
     double *y_perm = (double *)malloc(sizeof(double) * (size_t)(n ? n : 1) * (size_t)d);
     double *y_s = Is ? (double *)malloc(sizeof(double) * (size_t)(T ? T : 1) * (size_t)d) : NULL;
-    int rc = oracle_route(T, d, E, K, dtype, x, w_g, bias, NULL, NULL, idx, w, nthreads);
+    int rc = oracle_route(T, d, E, K, dtype, mode, x, w_g, bias, NULL, NULL, idx, w, nthreads);
     if (rc == 0)
         rc = oracle_permute(T, E, K, idx, counts, offsets, perm, inv);
     if (rc == 0) {
@@ -493,7 +528,7 @@ int oracle_forward(int64_t T, int64_t d, int64_t E, int64_t K, int64_t I,
 
 typedef struct {
     int64_t d, E, K, I, Is;
-    int dtype;
+    int dtype, mode;
     const void *x, *w_g;
     const double *bias;
     const void *w_gate, *w_up, *w_down, *ws_gate, *ws_up, *ws_down;
@@ -509,7 +544,8 @@ static void token_row(void *vctx, int64_t r)
     const int64_t t = c->tokens[r];
     const int64_t d = c->d;
     int64_t hmax = c->I > c->Is ? c->I : c->Is;
-    double *s = (double *)malloc(sizeof(double) * (size_t)c->E);
+    double *s = (double *)malloc(sizeof(double) * (size_t)c->E * 3);
+    double *key = s + c->E, *aff = s + 2 * c->E;
     unsigned char *taken = (unsigned char *)malloc((size_t)c->E);
     double *h = (double *)malloc(sizeof(double) * (size_t)hmax);
     double *ye = (double *)malloc(sizeof(double) * (size_t)d);
@@ -517,10 +553,10 @@ static void token_row(void *vctx, int64_t r)
     double *w = c->w + r * c->K;
     double *y = c->y + r * d;
 
-    router_scores(d, c->E, c->dtype, c->x, t, c->w_g, c->bias, s);
+    router_scores(d, c->E, c->dtype, c->x, t, c->w_g, s);
+    select_and_weigh(c->mode, c->E, c->K, s, c->bias, key, aff, taken, idx, w);
     if (c->logits)
-        memcpy(c->logits + r * c->E, s, sizeof(double) * (size_t)c->E);
-    select_and_weigh(c->E, c->K, s, taken, idx, w);
+        memcpy(c->logits + r * c->E, key, sizeof(double) * (size_t)c->E);
 
     /* y = SharedExpert(x_t) + sum_j w_j * Expert_{i_j}(x_t) */
     if (c->Is) {
@@ -548,11 +584,12 @@ static void token_row(void *vctx, int64_t r)
  * weights do not depend on the other tokens; "Computation and Data Movement
  * for Inference", sections 5 and 16), so a sample of rows is checked
  * exactly as in the full layer.  Outputs: y [n][d], topk_idx [n][K],
- * topk_w [n][K], logits [n][E] (optional).
+ * topk_w [n][K], logits [n][E] (optional: the selection keys); mode selects
+ * the router (0 softmax, 1 sigmoid).
  */
 int oracle_forward_tokens(int64_t n, const int32_t *tokens, int64_t T,
                           int64_t d, int64_t E, int64_t K, int64_t I,
-                          int64_t Is, int dtype, const void *x,
+                          int64_t Is, int dtype, int mode, const void *x,
                           const void *w_g, const double *bias,
                           const void *w_gate, const void *w_up,
                           const void *w_down, const void *ws_gate,
@@ -561,12 +598,13 @@ int oracle_forward_tokens(int64_t n, const int32_t *tokens, int64_t T,
                           int nthreads)
 {
     if (n < 0 || d < 1 || E < 1 || K < 1 || K > E || I < 1 || Is < 0 || !y ||
-        !topk_idx || !topk_w || (n > 0 && !tokens))
+        !topk_idx || !topk_w || (n > 0 && !tokens) ||
+        (mode != ORC_ROUTER_SOFTMAX && mode != ORC_ROUTER_SIGMOID))
         return -1;
     for (int64_t r = 0; r < n; ++r)
         if (tokens[r] < 0 || tokens[r] >= T)
             return -1;
-    tok_ctx c = {d, E, K, I, Is, dtype, x, w_g, bias, w_gate, w_up, w_down,
+    tok_ctx c = {d, E, K, I, Is, dtype, mode, x, w_g, bias, w_gate, w_up, w_down,
                  ws_gate, ws_up, ws_down, tokens, y, logits, topk_idx, topk_w};
     par_for(n, nthreads, token_row, &c);
     return 0;

@@ -12,21 +12,24 @@ SRC = os.path.join(os.path.dirname(oracle.__file__), "moe_oracle.c")
 
 # (name, exact text in moe_oracle.c, replacement)
 MUTATIONS = [
-    ("ties_to_higher_index", "if (best < 0 || s[e] > s[best])", "if (best < 0 || s[e] >= s[best])"),
-    ("softmax_sign", "w[j] = exp(s[idx[j]] - smax);", "w[j] = exp(smax - s[idx[j]]);"),
+    ("ties_to_higher_index", "if (best < 0 || key[e] > key[best])", "if (best < 0 || key[e] >= key[best])"),
+    ("softmax_sign", "w[j] = exp(key[idx[j]] - kmax);", "w[j] = exp(kmax - key[idx[j]]);"),
     ("silu_sign", "double silu = g / (1.0 + exp(-g));", "double silu = g / (1.0 + exp(g));"),
     ("dropped_up_projection", "h[i] = silu * u;", "h[i] = silu;"),
     ("transposed_down_projection", "load_elem(w_down, dtype, wd_off + j * I + i)",
      "load_elem(w_down, dtype, wd_off + i * d + j)"),
     ("swapped_gate_and_up", "double silu = g / (1.0 + exp(-g));\n        h[i] = silu * u;",
      "double silu = u / (1.0 + exp(-u));\n        h[i] = silu * g;"),
-    ("dropped_bias", "s[e] = acc + (bias ? bias[e] : 0.0);", "s[e] = acc;"),
+    ("dropped_bias", "const double b = bias ? bias[e] : 0.0;", "const double b = 0.0;"),
     ("dropped_shared_in_combine", "double acc = y_shared ? y_shared[t * d + c] : 0.0;",
      "double acc = 0.0;"),
     ("first_weight_for_all_slots", "acc += topk_w[t * K + j] * y_perm[p * d + c];",
      "acc += topk_w[t * K] * y_perm[p * d + c];"),
     ("reversed_order_within_expert", "int32_t p = cursor[topk_idx[f]]++;",
      "int32_t p = offsets[topk_idx[f] + 1] - 1 - (cursor[topk_idx[f]]++ - offsets[topk_idx[f]]);"),
+    ("sigmoid_sign", "aff[e] = 1.0 / (1.0 + exp(-s[e]));", "aff[e] = 1.0 / (1.0 + exp(s[e]));"),
+    ("bias_leaks_into_sigmoid_weights", "w[j] = aff[idx[j]] / (denom + 1e-6);",
+     "w[j] = key[idx[j]] / (denom + 1e-6);"),
     ("router_reads_wrong_row", "load_elem(w_g, dtype, e * d + k)", "load_elem(w_g, dtype, ((e + 1) % E) * d + k)"),
 ]
 
@@ -42,6 +45,9 @@ PIN_TESTS = [
     lambda: pins.test_hand_built_layer_closed_form(),
     lambda: pins.test_combine_is_linear_in_the_weights(),
     lambda: pins.test_permutation_is_the_stable_expert_order(37, 3, 3),
+    lambda: pins.test_sigmoid_router_matches_brute_force(40, 64, 6, 4),
+    lambda: pins.test_sigmoid_bias_steers_selection_but_not_weights(),
+    lambda: pins.test_sigmoid_forward_matches_dense_masked_evaluation("f32"),
 ]
 
 

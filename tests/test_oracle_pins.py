@@ -292,3 +292,75 @@ def test_hand_built_layer_closed_form():
              ws_down=np.array([[1.0], [0.0]], np.float32))
     out = oracle.forward(x, p, 2, dtype="f32")
     assert abs(out["y"][0][0] - (expect + silu(1.0))) < 1e-15
+
+
+# ---------------------------------------------------------------- sigmoid router (DeepSeek-V3)
+
+def _sigmoid(z):
+    return 1.0 / (1.0 + np.exp(-z))
+
+
+@pytest.mark.parametrize("T,E,K,scale", [(50, 256, 8, 512), (40, 64, 6, 4), (9, 8, 8, 8), (20, 5, 1, 2)])
+def test_sigmoid_router_matches_brute_force(T, E, K, scale):
+    logits = mi.grid_logits(T, E, seed=31, scale=scale).numpy()
+    bias = np.round(np.random.default_rng(3).standard_normal(E) * 8) / 32
+    idx, w, keys = oracle.route(None, None, K, logits_in=logits, bias=bias, router="sigmoid")
+    for t in range(T):
+        a = _sigmoid(logits[t].astype(np.float64))
+        key = a + bias
+        assert np.allclose(keys[t], key, rtol=0, atol=1e-15)
+        ref = _brute_topk(key, K)
+        assert np.array_equal(idx[t], ref)
+        assert np.allclose(w[t], a[ref] / (a[ref].sum() + 1e-6), rtol=1e-14)
+
+
+def test_sigmoid_bias_steers_selection_but_not_weights():
+    s = np.array([[2.0, 1.0, 0.5, -1.0]], np.float32)
+    bias = np.array([0.0, 0.0, 0.0, 5.0])
+    idx, w, _ = oracle.route(None, None, 2, logits_in=s, bias=bias, router="sigmoid")
+    assert idx[0].tolist() == [3, 0]          # the bias lifts expert 3 into the top 2
+    a3, a0 = 1 / (1 + math.exp(1.0)), 1 / (1 + math.exp(-2.0))
+    assert np.allclose(w[0], [a3 / (a3 + a0 + 1e-6), a0 / (a3 + a0 + 1e-6)], rtol=1e-15)
+    assert w[0].sum() < 1.0                   # a / (sum a + 1e-6) sums to just under 1
+
+
+def test_sigmoid_zero_input_ties_everything():
+    rng = np.random.default_rng(12)
+    x, p = _rand_layer(rng, 5, 32, 12, 16, 0, "f32")
+    idx, w, keys = oracle.route(np.zeros_like(x), p["w_g"], 4, dtype="f32", router="sigmoid")
+    assert np.all(keys == 0.5)
+    assert np.array_equal(idx, np.tile(np.arange(4, dtype=np.int32), (5, 1)))
+    assert np.allclose(w, 0.5 / (4 * 0.5 + 1e-6), rtol=1e-15)
+
+
+def _dense_masked_sigmoid(x, p, K, dtype, bias):
+    xs = _as_f64(x, dtype)
+    P = {k: _as_f64(v, dtype) for k, v in p.items()}
+    T, d = xs.shape
+    E = P["w_g"].shape[0]
+    y = np.zeros((T, d))
+    for t in range(T):
+        a = _sigmoid(P["w_g"] @ xs[t])
+        sel = _brute_topk(a + bias, K)
+        mask = np.zeros(E)
+        mask[sel] = a[sel] / (a[sel].sum() + 1e-6)
+        acc = np.zeros(d)
+        if "ws_gate" in P:
+            acc += _expert_dense(xs[t], P["ws_gate"], P["ws_up"], P["ws_down"])
+        for e in range(E):
+            acc += mask[e] * _expert_dense(xs[t], P["w_gate"][e], P["w_up"][e], P["w_down"][e])
+        y[t] = acc
+    return y
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_sigmoid_forward_matches_dense_masked_evaluation(dtype):
+    rng = np.random.default_rng(13)
+    T, d, E, K, I, Is = 9, 24, 6, 3, 40, 16
+    x, p = _rand_layer(rng, T, d, E, I, Is, dtype)
+    bias = rng.standard_normal(E) * 0.3
+    out = oracle.forward(x, p, K, dtype=dtype, bias=bias, router="sigmoid")
+    ref = _dense_masked_sigmoid(x, p, K, dtype, bias)
+    assert np.max(np.abs(out["y"] - ref)) <= 1e-12 * np.max(np.abs(ref))
+    tok = oracle.forward_tokens(np.arange(T), x, p, K, dtype=dtype, bias=bias, router="sigmoid")
+    assert np.max(np.abs(tok["y"] - ref)) <= 1e-12 * np.max(np.abs(ref))
