@@ -227,7 +227,7 @@ def run_ours(args):
     p = mi.make_weights(cfg_r, "cuda")
     x = mi.make_x(cfg_r, "cuda")
     bias = mi.make_bias(cfg_r, "cuda")
-    s = moe.make_shape(cfg.T, cfg.d, cfg.E, cfg.K, cfg.I, cfg.Is, cfg.dtype)
+    s = moe.make_shape(cfg.T, cfg.d, cfg.E, cfg.K, cfg.I, cfg.Is, cfg.dtype, cfg.router)
     ws = moe.alloc_workspace(s)
     y = torch.empty_like(x)
     stream = torch.cuda.Stream()
@@ -324,7 +324,7 @@ def run_ours(args):
 def count_active(moe, cfg, x, p, bias, stream) -> int:
     import torch
     torch.cuda.synchronize()  # inputs were drawn on torch's current stream
-    s = moe.make_shape(cfg.T, cfg.d, cfg.E, cfg.K, cfg.I, cfg.Is, cfg.dtype)
+    s = moe.make_shape(cfg.T, cfg.d, cfg.E, cfg.K, cfg.I, cfg.Is, cfg.dtype, cfg.router)
     ws = moe.alloc_workspace(s)
     idx = torch.empty((cfg.T, cfg.K), dtype=torch.int32, device="cuda")
     w = torch.empty((cfg.T, cfg.K), dtype=torch.float32, device="cuda")
@@ -336,7 +336,7 @@ def count_active(moe, cfg, x, p, bias, stream) -> int:
 def time_expert_ffn(moe, cfg, x, p, bias, stream, steps: int) -> dict:
     """Events around moe_expert_ffn alone (routed experts of this batch)."""
     import torch
-    s = moe.make_shape(cfg.T, cfg.d, cfg.E, cfg.K, cfg.I, 0, cfg.dtype)
+    s = moe.make_shape(cfg.T, cfg.d, cfg.E, cfg.K, cfg.I, 0, cfg.dtype, cfg.router)
     ws = moe.alloc_workspace(s)
     n = cfg.T * cfg.K
     idx = torch.empty((cfg.T, cfg.K), dtype=torch.int32, device="cuda")
@@ -439,7 +439,7 @@ def bench_workload(moe, cfg, peaks, steps: int, graph: bool = False) -> dict:
     p = mi.make_weights(cfg, "cuda")
     x = mi.make_x(cfg, "cuda")
     bias = mi.make_bias(cfg, "cuda")
-    s = moe.make_shape(cfg.T, cfg.d, cfg.E, cfg.K, cfg.I, cfg.Is, cfg.dtype)
+    s = moe.make_shape(cfg.T, cfg.d, cfg.E, cfg.K, cfg.I, cfg.Is, cfg.dtype, cfg.router)
     ws = moe.alloc_workspace(s)
     y = torch.empty_like(x)
     st = torch.cuda.Stream()
@@ -495,7 +495,7 @@ def bench_workload(moe, cfg, peaks, steps: int, graph: bool = False) -> dict:
 def bench_all(moe, peaks, args) -> list:
     res = []
     for name in ("tiny_f32", "mixtral_prefill", "dsv3_decode", "dsv3_prefill_zipf",
-                 *[f"dsv3_sweep_T{t}" for t in mi.SWEEP_T]):
+                 *[f"dsv3_sweep_T{t}" for t in mi.SWEEP_T], "dsv3_decode_sigmoid"):
         cfg = mi.CONFIGS[name]
         res.append(bench_workload(moe, cfg, peaks, steps=max(10, args.steps),
                                   graph=cfg.T <= 64))

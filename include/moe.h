@@ -72,6 +72,18 @@ typedef enum {
 
 typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
 
+/*
+ * Router rule (s = x . w_g^T, the raw score; b = bias or 0):
+ *   MOE_ROUTER_SOFTMAX  key = s + b; the K largest keys; w = softmax over the
+ *                       K selected keys [R section 2.2].
+ *   MOE_ROUTER_SIGMOID  a = sigmoid(s); key = a + b (the bias steers the
+ *                       selection only); the K largest keys;
+ *                       w = a / (sum of the K selected a + 1e-6) -- the
+ *                       DeepSeek-V3 auxiliary-loss-free routing [S section
+ *                       2.2 and the dispatcher code of section 4.3].
+ */
+typedef enum { MOE_ROUTER_SOFTMAX = 0, MOE_ROUTER_SIGMOID = 1 } moe_router;
+
 typedef struct {
     int32_t T;            /* tokens                                         */
     int32_t d;            /* hidden size                                    */
@@ -80,6 +92,7 @@ typedef struct {
     int32_t inter;        /* routed expert intermediate size I              */
     int32_t inter_shared; /* shared expert intermediate size Is; 0 = none   */
     int32_t dtype;        /* moe_dtype                                      */
+    int32_t router;       /* moe_router (0 = softmax over the K selected)   */
 } moe_shape;
 
 /* Text for a status code (static storage, never NULL). */
@@ -92,13 +105,14 @@ const char *moe_status_string(int32_t status);
 size_t moe_workspace_bytes(const moe_shape *shape);
 
 /*
- * Stage 1, routing [R section 2.2; S section 2.1].
- *   scores[t][e] = sum_k x[t][k] * w_g[e][k] + bias[e]   (fp32 accumulate)
- *   topk_idx[t][j], topk_w[t][j]: the K best scores with ties to the lower
- *   index, and w = softmax over those K scores.
- * bias may be NULL (no bias).  If logits_in [T][E] (fp32) is non-NULL it is
- * used as the scores and x, w_g, bias are ignored (may be NULL).
- * logits_out [T][E] (fp32) receives the scores if non-NULL.
+ * Stage 1, routing [R section 2.2; S sections 2.1-2.2].
+ *   s[t][e] = sum_k x[t][k] * w_g[e][k]   (fp32 accumulate)
+ *   keys and weights by shape->router (see moe_router above);
+ *   topk_idx[t][j], topk_w[t][j]: the K largest keys with ties to the lower
+ *   index, slot j = j-th pick, and their weights.
+ * bias [E] (fp32) may be NULL (no bias).  If logits_in [T][E] (fp32) is
+ * non-NULL it replaces s (x and w_g are then ignored and may be NULL); the
+ * bias still applies.  logits_out [T][E] (fp32) receives the keys if non-NULL.
  * Outputs: topk_idx [T][K] int32, topk_w [T][K] fp32.
  */
 moe_status moe_route(const moe_shape *shape, const void *x, const void *w_g,

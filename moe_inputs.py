@@ -18,6 +18,8 @@ Workloads (shapes and distributions; names by what they are):
                       permutation of 1..E, s = 1.2, beta = ZIPF_BETA, so expert
                       popularity falls off like a Zipf law in rank.
   dsv3_sweep_T{n}     dsv3_decode shapes at T = n, n in {1, 8, 64, 512, 4096}.
+  dsv3_decode_sigmoid dsv3_decode with the DeepSeek-V3 router (sigmoid affinities,
+                      weights a / (sum a + 1e-6)).
 
 Every tensor has its own sub-seed, splitmix64(seed ^ fnv1a64(name)), so adding
 or resizing one tensor never changes another.  Large weights are drawn one
@@ -52,6 +54,7 @@ class LayerConfig:
     dtype: str = "bf16"   # "bf16" or "f32"
     down_std: str = "d"   # "d": w_down ~ N(0,1/d); "inter": N(0,1/I)
     zipf_bias: bool = False
+    router: str = "softmax"   # "softmax" or "sigmoid" (DeepSeek-V3 affinities)
     seed: int = 0
     extra: dict = field(default_factory=dict, compare=False)
 
@@ -67,6 +70,9 @@ CONFIGS: dict[str, LayerConfig] = {
     "dsv3_prefill_zipf": LayerConfig("dsv3_prefill_zipf", T=16384, d=7168, E=256, K=8, I=2048,
                                      Is=2048, zipf_bias=True),
 }
+# DeepSeek-V3 decode with its own router: sigmoid affinities, weights a / (sum a + 1e-6)
+CONFIGS["dsv3_decode_sigmoid"] = LayerConfig("dsv3_decode_sigmoid", T=8, d=7168, E=256, K=8,
+                                             I=2048, Is=2048, router="sigmoid")
 SWEEP_T = (1, 8, 64, 512, 4096)
 for _t in SWEEP_T:
     CONFIGS[f"dsv3_sweep_T{_t}"] = LayerConfig(f"dsv3_sweep_T{_t}", T=_t, d=7168, E=256, K=8,

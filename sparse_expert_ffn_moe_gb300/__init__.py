@@ -20,6 +20,7 @@ LIB_PATH = os.path.join(_PKG, "libmoe.so")
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE = 0, 1, 2, 3
 MOE_ERR_CUDA, MOE_ERR_TIMEOUT, MOE_ERR_BOUNDS = 4, 5, 6
 MOE_F32, MOE_BF16 = 0, 1
+MOE_ROUTER_SOFTMAX, MOE_ROUTER_SIGMOID = 0, 1
 
 EXPORTED = ("moe_status_string", "moe_workspace_bytes", "moe_route", "moe_permute",
             "moe_permute_noalloc", "moe_expert_ffn", "moe_combine", "moe_forward",
@@ -35,7 +36,8 @@ class MoeError(RuntimeError):
 class moe_shape(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int32), ("d", ctypes.c_int32), ("E", ctypes.c_int32),
                 ("K", ctypes.c_int32), ("inter", ctypes.c_int32),
-                ("inter_shared", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+                ("inter_shared", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("router", ctypes.c_int32)]
 
 
 def _load_lib() -> ctypes.CDLL:
@@ -75,10 +77,12 @@ def status_string(status: int) -> str:
 
 
 def make_shape(T: int, d: int, E: int, K: int, inter: int, inter_shared: int = 0,
-               dtype: str | int = "bf16") -> moe_shape:
+               dtype: str | int = "bf16", router: str | int = "softmax") -> moe_shape:
     if isinstance(dtype, str):
         dtype = {"bf16": MOE_BF16, "f32": MOE_F32}[dtype]
-    return moe_shape(T, d, E, K, inter, inter_shared, dtype)
+    if isinstance(router, str):
+        router = {"softmax": MOE_ROUTER_SOFTMAX, "sigmoid": MOE_ROUTER_SIGMOID}[router]
+    return moe_shape(T, d, E, K, inter, inter_shared, dtype, router)
 
 
 def _p(t):

@@ -29,6 +29,7 @@ moe_status check_shape(const moe_shape* s) {
         return MOE_ERR_INVALID_ARG;
     if (s->K > s->E) return MOE_ERR_INVALID_ARG;
     if (s->dtype != MOE_F32 && s->dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+    if (s->router != MOE_ROUTER_SOFTMAX && s->router != MOE_ROUTER_SIGMOID) return MOE_ERR_INVALID_ARG;
     if (s->K > 32 || s->E > 1024) return MOE_ERR_UNSUPPORTED;
     if (s->d % 64 || s->inter % 64 || s->inter_shared % 64) return MOE_ERR_UNSUPPORTED;
     if (s->d > 16384 || s->inter > 16384 || s->inter_shared > 16384) return MOE_ERR_UNSUPPORTED;
@@ -158,7 +159,7 @@ moe_status moe_route(const moe_shape* shape, const void* x, const void* w_g, con
     cudaError_t e = cudaMemsetAsync(err, 0, sizeof(DevError), cs);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     if (logits_in)
-        return cuda_status(launch_topk_softmax(s, logits_in, 1, nullptr, logits_out, topk_idx, topk_w, cs));
+        return cuda_status(launch_topk_softmax(s, logits_in, 1, bias, logits_out, topk_idx, topk_w, cs));
     float* part = at<float>(workspace, L.router_part);
     int splits = L.router_splits;
     if (use_tc_router(s) && tc_available()) {

@@ -72,66 +72,90 @@ router_gemv_kernel(const T* __restrict__ x, const T* __restrict__ w_g, float* __
 }
 
 struct Cand {
-    float v;
+    float key;  // what the selection compares
+    float val;  // what the weights are formed from
     int e;
 };
-// a beats b: larger score, or equal score and lower index
+// a beats b: larger key, or equal key and lower index
 __device__ __forceinline__ bool beats(const Cand& a, const Cand& b) {
-    return a.e >= 0 && (b.e < 0 || a.v > b.v || (a.v == b.v && a.e < b.e));
+    return a.e >= 0 && (b.e < 0 || a.key > b.key || (a.key == b.key && a.e < b.e));
 }
 
 // One warp per token.  Lane l holds experts e = l + 32*m.
-template <int MAXM>
+//   MODE 0 (softmax router; explainer section 2.2): key = score + bias, and
+//          w = softmax over the K selected keys.
+//   MODE 1 (sigmoid router; llmgo page section 2.2 and the dispatcher code of
+//          section 4.3): a = sigmoid(score), key = a + bias (the bias only
+//          steers the selection), w = a / (sum of the selected a + 1e-6).
+// logits_out receives the keys.
+template <int MAXM, int MODE>
 __global__ void __launch_bounds__(256)
-topk_softmax_kernel(const float* __restrict__ part, int splits, const float* __restrict__ bias,
-                    float* __restrict__ logits_out, int32_t* __restrict__ topk_idx,
-                    float* __restrict__ topk_w, int Tn, int E, int K) {
+topk_route_kernel(const float* __restrict__ part, int splits, const float* __restrict__ bias,
+                  float* __restrict__ logits_out, int32_t* __restrict__ topk_idx,
+                  float* __restrict__ topk_w, int Tn, int E, int K) {
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (t >= Tn) return;
-    float v[MAXM];
+    float key[MAXM], val[MAXM];
 #pragma unroll
     for (int m = 0; m < MAXM; ++m) {
         const int e = lane + 32 * m;
-        float s = 0.f;
+        float k = 0.f, v = 0.f;
         if (e < E) {
             // fixed summation order over the split-K partials (deterministic)
             float pq[kMaxSplits];
 #pragma unroll
             for (int q = 0; q < kMaxSplits; ++q)
                 pq[q] = q < splits ? part[((int64_t)q * Tn + t) * E + e] : 0.f;
-            s = pq[0];
+            float s = pq[0];
 #pragma unroll
             for (int q = 1; q < kMaxSplits; ++q)
                 if (q < splits) s += pq[q];
-            if (bias) s += bias[e];
-            if (logits_out) logits_out[(int64_t)t * E + e] = s;
+            const float b = bias ? bias[e] : 0.f;
+            if (MODE == 1) {
+                v = 1.f / (1.f + expf(-s));
+                k = v + b;
+            } else {
+                k = s + b;
+                v = k;
+            }
+            if (logits_out) logits_out[(int64_t)t * E + e] = k;
         }
-        v[m] = s;
+        key[m] = k;
+        val[m] = v;
     }
     uint32_t taken = 0;
-    float my_s = 0.f;  // lane j keeps the j-th selected score
-    float s0 = 0.f;
+    float my_v = 0.f;  // lane j keeps the value of the j-th pick
+    float k0 = 0.f;    // key of the first pick
     for (int j = 0; j < K; ++j) {
-        Cand best{0.f, -1};
+        Cand best{0.f, 0.f, -1};
 #pragma unroll
         for (int m = 0; m < MAXM; ++m) {
             const int e = lane + 32 * m;
-            if (e < E && !(taken & (1u << m)) && (best.e < 0 || v[m] > best.v)) best = Cand{v[m], e};
+            if (e < E && !(taken & (1u << m)) && (best.e < 0 || key[m] > best.key))
+                best = Cand{key[m], val[m], e};
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
-            Cand other{__shfl_xor_sync(0xffffffffu, best.v, o), __shfl_xor_sync(0xffffffffu, best.e, o)};
+            Cand other{__shfl_xor_sync(0xffffffffu, best.key, o),
+                       __shfl_xor_sync(0xffffffffu, best.val, o),
+                       __shfl_xor_sync(0xffffffffu, best.e, o)};
             if (beats(other, best)) best = other;
         }
         if ((best.e & 31) == lane) taken |= 1u << (best.e >> 5);
-        if (lane == j) my_s = best.v;
-        if (j == 0) s0 = best.v;
+        if (lane == j) my_v = best.val;
+        if (j == 0) k0 = best.key;
         if (lane == 0) topk_idx[(int64_t)t * K + j] = best.e;
     }
-    const float ex = lane < K ? expf(my_s - s0) : 0.f;
-    const float denom = warp_sum(ex);
-    if (lane < K) topk_w[(int64_t)t * K + lane] = ex / denom;
+    if (MODE == 1) {
+        const float a = lane < K ? my_v : 0.f;
+        const float denom = warp_sum(a) + 1e-6f;
+        if (lane < K) topk_w[(int64_t)t * K + lane] = a / denom;
+    } else {
+        const float ex = lane < K ? expf(my_v - k0) : 0.f;
+        const float denom = warp_sum(ex);
+        if (lane < K) topk_w[(int64_t)t * K + lane] = ex / denom;
+    }
 }
 
 }  // namespace
@@ -164,15 +188,22 @@ cudaError_t launch_topk_softmax(const moe_shape& s, const float* part, int split
                                 float* topk_w, cudaStream_t st) {
     const unsigned blocks = (unsigned)ceil_div(s.T, 8);
     const int m = (int)ceil_div(s.E, 32);
-#define MOE_TOPK(M)                                                                              \
-    topk_softmax_kernel<M><<<blocks, 256, 0, st>>>(part, splits, bias, logits_out, topk_idx, \
-                                                   topk_w, s.T, s.E, s.K)
-    if (m <= 1) MOE_TOPK(1);
-    else if (m <= 2) MOE_TOPK(2);
-    else if (m <= 4) MOE_TOPK(4);
-    else if (m <= 8) MOE_TOPK(8);
-    else if (m <= 16) MOE_TOPK(16);
-    else MOE_TOPK(32);
+#define MOE_TOPK(M, MODE)                                                                      \
+    topk_route_kernel<M, MODE><<<blocks, 256, 0, st>>>(part, splits, bias, logits_out, topk_idx, \
+                                                       topk_w, s.T, s.E, s.K)
+#define MOE_TOPK_M(MODE)                    \
+    if (m <= 1) MOE_TOPK(1, MODE);          \
+    else if (m <= 2) MOE_TOPK(2, MODE);     \
+    else if (m <= 4) MOE_TOPK(4, MODE);     \
+    else if (m <= 8) MOE_TOPK(8, MODE);     \
+    else if (m <= 16) MOE_TOPK(16, MODE);   \
+    else MOE_TOPK(32, MODE)
+    if (s.router == MOE_ROUTER_SIGMOID) {
+        MOE_TOPK_M(1);
+    } else {
+        MOE_TOPK_M(0);
+    }
+#undef MOE_TOPK_M
 #undef MOE_TOPK
     return cudaGetLastError();
 }

@@ -76,7 +76,7 @@ class Layer:
 
     def shape(self, moe, T=None):
         c = self.cfg
-        return moe.make_shape(c.T if T is None else T, c.d, c.E, c.K, c.I, c.Is, c.dtype)
+        return moe.make_shape(c.T if T is None else T, c.d, c.E, c.K, c.I, c.Is, c.dtype, c.router)
 
     def forward(self, moe, x=None, ws=None):
         x = self.x if x is None else x

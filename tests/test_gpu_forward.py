@@ -146,3 +146,21 @@ def test_combine_matches_oracle(moe):
             assert max_abs_over_rms(to_f64(y), ref) <= 1e-6
         else:
             assert rel_l2(to_f64(y), ref) <= 4e-3
+
+
+@pytest.mark.parametrize("name,T", [("dsv3_decode", None), ("dsv3_sweep_T4096", None)])
+def test_forward_sigmoid_router(moe, name, T):
+    """The whole layer with the DeepSeek-V3 router (sigmoid affinities, a
+    selection-only bias, weights a / (sum a + 1e-6))."""
+    import dataclasses
+    cfg = dataclasses.replace(mi.CONFIGS[name], router="sigmoid")
+    L = Layer(cfg)
+    L.bias = (torch.from_numpy(np.round(np.random.default_rng(9).standard_normal(cfg.E) * 4) / 64)
+              .float().cuda())
+    y = L.forward(moe)
+    tokens = mi.sample_tokens(cfg.T, SAMPLE, seed=cfg.seed).numpy()
+    ref = oracle.forward_tokens(tokens, host(L.x), L.hp, cfg.K, dtype=cfg.dtype,
+                                bias=L.bias_host(), router="sigmoid")
+    ok = boundary_margin(ref["logits"], cfg.K) >= 1e-4
+    assert ok.mean() >= 0.75
+    _check(cfg, to_f64(y[torch.from_numpy(tokens[ok]).long().cuda()]), ref["y"][ok])

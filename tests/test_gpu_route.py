@@ -96,3 +96,69 @@ def test_route_from_x(moe, name, T):
         b = dict(zip(ref_idx[t].tolist(), ref_w[t].tolist()))
         for e in b:
             assert abs(a[e] - b[e]) <= 1e-4 * b[e] + 1e-6
+
+
+# ---------------------------------------------------------------- sigmoid router (DeepSeek-V3)
+
+def _route_logits_mode(moe, logits: torch.Tensor, K: int, router: str, bias=None):
+    T, E = logits.shape
+    s = moe.make_shape(T, 64, E, K, 64, 0, "f32", router)
+    ws = moe.alloc_workspace(s)
+    idx = torch.full((T, K), -7, dtype=torch.int32, device="cuda")
+    w = torch.full((T, K), -1.0, dtype=torch.float32, device="cuda")
+    keys = torch.empty((T, E), dtype=torch.float32, device="cuda")
+    b = None if bias is None else torch.as_tensor(bias, dtype=torch.float32).cuda()
+    moe.moe_route(s, None, None, b, logits.cuda(), keys, idx, w, ws)
+    torch.cuda.synchronize()
+    return idx.cpu().numpy(), w.cpu().numpy().astype(np.float64), keys.cpu().numpy().astype(np.float64)
+
+
+@pytest.mark.parametrize("T,E,K,with_bias", [(8, 256, 8, False), (4096, 256, 8, True),
+                                             (16384, 256, 8, True), (100, 64, 6, True),
+                                             (33, 8, 8, False), (50, 20, 1, True)])
+def test_sigmoid_route_matches_oracle(moe, T, E, K, with_bias):
+    """Same fp32 scores on both sides.  Without a bias the sigmoid keeps the
+    order of the scores, so the selection is bit-exact including ties; with a
+    bias (1/32 grid) keys of different experts can nearly coincide, so tokens
+    whose fp64 boundary gap is below 1e-5 are left out (and counted)."""
+    logits = mi.grid_logits(T, E, seed=111, scale=512)
+    bias = (np.round(np.random.default_rng(5).standard_normal(E) * 8) / 32) if with_bias else None
+    idx, w, keys = _route_logits_mode(moe, logits, K, "sigmoid", bias)
+    ref_idx, ref_w, ref_keys = oracle.route(None, None, K, logits_in=logits.numpy(), bias=bias,
+                                            router="sigmoid")
+    assert np.max(np.abs(keys - ref_keys)) <= 1e-6
+    ok = boundary_margin(ref_keys, K) >= (1e-5 if with_bias else 0.0)
+    if with_bias:
+        assert ok.mean() >= 0.95
+    assert np.array_equal(idx[ok], ref_idx[ok])
+    assert np.allclose(w[ok], ref_w[ok], rtol=2e-6, atol=0)
+
+
+@pytest.mark.parametrize("name,T", [("dsv3_decode", None), ("dsv3_prefill_zipf", 512)])
+def test_sigmoid_route_from_x(moe, name, T):
+    cfg = mi.CONFIGS[name]
+    if T is not None:
+        cfg = cfg.with_T(T)
+    import dataclasses
+    cfg = dataclasses.replace(cfg, router="sigmoid")
+    L = Layer(cfg, only={"w_g"})
+    bias = None if L.bias is None else (L.bias / 8).contiguous()  # keys live in (0, 1)
+    s = L.shape(moe)
+    ws = moe.alloc_workspace(s)
+    idx = torch.empty((cfg.T, cfg.K), dtype=torch.int32, device="cuda")
+    w = torch.empty((cfg.T, cfg.K), dtype=torch.float32, device="cuda")
+    keys = torch.empty((cfg.T, cfg.E), dtype=torch.float32, device="cuda")
+    moe.moe_route(s, L.x, L.p["w_g"], bias, None, keys, idx, w, ws)
+    torch.cuda.synchronize()
+    ref_idx, ref_w, ref_keys = oracle.route(host(L.x), L.hp["w_g"], cfg.K, dtype=cfg.dtype,
+                                            bias=None if bias is None else bias.double().cpu().numpy(),
+                                            router="sigmoid")
+    assert np.max(np.abs(keys.cpu().numpy() - ref_keys)) <= 1e-5
+    ok = boundary_margin(ref_keys, cfg.K) >= 1e-4
+    assert ok.mean() > 0.9
+    gi, gw = idx.cpu().numpy(), w.cpu().numpy().astype(np.float64)
+    assert np.array_equal(np.sort(gi[ok], axis=1), np.sort(ref_idx[ok], axis=1))
+    for t in np.nonzero(ok)[0][:200]:
+        a = dict(zip(gi[t].tolist(), gw[t].tolist()))
+        for e, wr in zip(ref_idx[t].tolist(), ref_w[t].tolist()):
+            assert abs(a[e] - wr) <= 1e-4 * wr + 1e-6
