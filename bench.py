@@ -74,9 +74,10 @@ def launches_per_forward(cfg, gemv_limit: int = 0, pair_min: int = 512) -> int:
     single-SM tcgen05 gate/up and down GEMMs when needed, and the CTA-pair
     ones too when a group can reach pair_min rows, combine."""
     need_tc = cfg.dtype == "bf16" and cfg.T > gemv_limit
+    gather = need_tc and cfg.T > int(os.environ.get("MOE_GATHER_MAX_ROWS", "0"))
     gemv = cfg.dtype == "f32" or gemv_limit > 0
     pair = need_tc and cfg.T >= pair_min
-    return (2 + 3 + (1 if need_tc else 0) + 1 + (2 if gemv else 0) + (2 if need_tc else 0)
+    return (2 + 3 + (1 if gather else 0) + 1 + (2 if gemv else 0) + (2 if need_tc else 0)
             + (2 if pair else 0) + 1)
 
 

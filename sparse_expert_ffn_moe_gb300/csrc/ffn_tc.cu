@@ -98,11 +98,23 @@ __device__ __forceinline__ uint32_t abytes_for(int rows) {
     return rows <= 0 ? 0u : (uint32_t)abox_rows(abox_for(rows)) * BK * 2;
 }
 
+// Routed rows of at most MOE_GATHER_MAX_ROWS per CTA can be gathered from x
+// with tile::gather4 inside the GEMM instead of being copied into expert order
+// first; larger row blocks load the contiguous permuted copy.  Measured on
+// GB300 (interleaved A/B, every workload): gathering is never faster -- 4-7%
+// slower on prefill shapes, even at <= 32 rows per CTA (128 rows per CTA
+// took ~2.5x the MMA time per stage) -- so the default is 0 (off); the path
+// stays selectable and parity-tested.
+constexpr int kGatherMaxRows = 0;
+
 struct TcParams {
     CUtensorMap a[2][kABoxes];  // activations: [0] routed rows, [1] shared / dense rows
     CUtensorMap b0[2];          // weights (gate / down / router), box 128 rows
     CUtensorMap b1[2];          // up weights (SWIGLU only), box 128 rows
     CUtensorMap bw[2];          // weights, box 256 rows (single tiles, non-SWIGLU)
+    CUtensorMap ag;             // x with a one-row box, for tile::gather4 of routed rows
+    const int32_t* row_src;     // token of each routed row (gather from x), or null
+    int gather_max;             // gather a CTA's routed rows when it has at most this many
     const FfnPlanHeader* hdr;
     const int4* mtiles;
     int E;
@@ -235,6 +247,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
         ptx::fence_proxy_async_smem();
     }
     if (warp == 0 && lane == 0) {
+        if (p.row_src) ptx::prefetch_tmap(&p.ag);
         for (int k = 0; k < 2; ++k) {
             for (int b = 0; b < kABoxes; ++b) ptx::prefetch_tmap(&p.a[k][b]);
             if (PAIR || EPI == EPI_SWIGLU) {
@@ -260,8 +273,13 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
     const uint32_t tmem = ctl->tmem_base;
 
     if (warp == 0) {
-        // ------------------------------------------------ TMA producer
-        if (lane == 0) {
+        // ------------------------------------------------ TMA producer (warp 0)
+        // Lane 0 runs the barrier handshake and the weight loads.  Routed
+        // activation rows of moe_forward are gathered straight from x with
+        // tile::gather4 (the row -> token map of the dispatch gives the rows):
+        // lane l loads rows 4l..4l+3 of this CTA's block, so one stage takes up
+        // to 32 gather instructions issued in parallel.
+        {
             int stage = 0;
             uint32_t phase = 0;
             uint32_t issued_phase[kMaxStages];
@@ -275,41 +293,96 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
                 const int rows_me = max(0, min(BMC, tl.rows - (int)rank * BMC));
                 const CUtensorMap* ma = &p.a[tl.kind][abox_for(rows_me)];
                 const int arow = tl.row0 + (int)rank * BMC;
+                const bool gather = tl.kind == 0 && p.row_src != nullptr && rows_me <= p.gather_max;
+                const int n4 = gather ? (rows_me + 3) / 4 : 0;
+                int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
+                if (lane < n4) {  // padding rows repeat the last valid row
+                    const int b = 4 * lane, last = rows_me - 1;
+                    r0 = p.row_src[arow + min(b, last)];
+                    r1 = p.row_src[arow + min(b + 1, last)];
+                    r2 = p.row_src[arow + min(b + 2, last)];
+                    r3 = p.row_src[arow + min(b + 3, last)];
+                }
+                // bytes of one CTA's activation rows (each CTA of a pair decides by its own rows)
+                const bool can_gather = tl.kind == 0 && p.row_src != nullptr;
+                const int gmax = p.gather_max;
+                const auto a_bytes = [can_gather, gmax](int rows) -> uint32_t {
+                    return (can_gather && rows <= gmax) ? (uint32_t)((rows + 3) / 4) * 512u
+                                                        : abytes_for(rows);
+                };
                 uint32_t tx;
                 const CUtensorMap* mb;
                 int brow;
                 if constexpr (PAIR) {
-                    tx = abytes_for(min(BMC, tl.rows)) + abytes_for(tl.rows - BMC) + 2 * S::kBBytes;
+                    tx = a_bytes(min(BMC, tl.rows)) + a_bytes(max(0, tl.rows - BMC)) + 2 * S::kBBytes;
                     mb = (EPI == EPI_SWIGLU && rank == 1) ? &p.b1[tl.kind] : &p.b0[tl.kind];
                     brow = tl.wrow0 + ((EPI == EPI_SWIGLU) ? 0 : (int)rank * S::kBRows);
                 } else {
-                    tx = abytes_for(rows_me) + S::kBBytes;
+                    tx = a_bytes(rows_me) + S::kBBytes;
                     mb = EPI == EPI_SWIGLU ? &p.b0[tl.kind] : &p.bw[tl.kind];
                     brow = tl.wrow0;
                 }
-                for (int kb = 0; kb < tl.kblocks; ++kb) {
-                    if (!wait_bounded(&ctl->empty[stage], phase ^ 1u, ctl, p, 100)) { ok = false; break; }
-                    const int k0 = kb * BK;
-                    uint8_t* a_dst = sA + stage * kABytes;
-                    uint8_t* b_dst = sB + stage * S::kBBytes;
-                    if constexpr (PAIR) {
-                        if (rank == 0) ptx::mbar_arrive_expect_tx(&ctl->full[stage], tx);
-                        const uint32_t fb = full0 + (uint32_t)(stage * sizeof(uint64_t));
-                        if (rows_me > 0) ptx::tma_load_2d_pair(a_dst, ma, fb, k0, arow);
-                        ptx::tma_load_2d_pair(b_dst, mb, fb, k0, brow);
+                if (!gather) {
+                    // lane 0 alone; the other lanes only keep the ring position
+                    if (lane == 0) {
+                        for (int kb = 0; kb < tl.kblocks; ++kb) {
+                            if (!wait_bounded(&ctl->empty[stage], phase ^ 1u, ctl, p, 100)) { ok = false; break; }
+                            const int k0 = kb * BK;
+                            uint8_t* a_dst = sA + stage * kABytes;
+                            uint8_t* b_dst = sB + stage * S::kBBytes;
+                            if constexpr (PAIR) {
+                                const uint32_t fb = full0 + (uint32_t)(stage * sizeof(uint64_t));
+                                if (rank == 0) ptx::mbar_arrive_expect_tx(&ctl->full[stage], tx);
+                                if (rows_me > 0) ptx::tma_load_2d_pair(a_dst, ma, fb, k0, arow);
+                                ptx::tma_load_2d_pair(b_dst, mb, fb, k0, brow);
+                            } else {
+                                ptx::mbar_arrive_expect_tx(&ctl->full[stage], tx);
+                                ptx::tma_load_2d(a_dst, ma, &ctl->full[stage], k0, arow);
+                                ptx::tma_load_2d(b_dst, mb, &ctl->full[stage], k0, brow);
+                                if (EPI == EPI_SWIGLU)
+                                    ptx::tma_load_2d(b_dst + S::kBBytes / 2, &p.b1[tl.kind], &ctl->full[stage], k0, brow);
+                            }
+                            issued[stage] = true;
+                            issued_phase[stage] = phase;
+                            if (++stage == S::kStages) { stage = 0; phase ^= 1u; }
+                        }
                     } else {
-                        ptx::mbar_arrive_expect_tx(&ctl->full[stage], tx);
-                        ptx::tma_load_2d(a_dst, ma, &ctl->full[stage], k0, arow);
-                        ptx::tma_load_2d(b_dst, mb, &ctl->full[stage], k0, brow);
-                        if (EPI == EPI_SWIGLU)
-                            ptx::tma_load_2d(b_dst + S::kBBytes / 2, &p.b1[tl.kind], &ctl->full[stage], k0, brow);
+                        const int adv = stage + tl.kblocks;
+                        phase ^= (uint32_t)((adv / S::kStages) & 1);
+                        stage = adv % S::kStages;
                     }
-                    issued[stage] = true;
-                    issued_phase[stage] = phase;
-                    if (++stage == S::kStages) { stage = 0; phase ^= 1u; }
+                } else {
+                    for (int kb = 0; kb < tl.kblocks; ++kb) {
+                        const int okw = lane == 0 ? (int)wait_bounded(&ctl->empty[stage], phase ^ 1u, ctl, p, 100) : 0;
+                        if (!__shfl_sync(0xffffffffu, okw, 0)) { ok = false; break; }
+                        const int k0 = kb * BK;
+                        uint8_t* a_dst = sA + stage * kABytes;
+                        uint8_t* b_dst = sB + stage * S::kBBytes;
+                        if constexpr (PAIR) {
+                            const uint32_t fb = full0 + (uint32_t)(stage * sizeof(uint64_t));
+                            if (lane == 0 && rank == 0) ptx::mbar_arrive_expect_tx(&ctl->full[stage], tx);
+                            __syncwarp();
+                            if (lane < n4) ptx::tma_gather4_pair(a_dst + lane * 512, &p.ag, fb, k0, r0, r1, r2, r3);
+                            if (lane == 0) ptx::tma_load_2d_pair(b_dst, mb, fb, k0, brow);
+                        } else {
+                            if (lane == 0) ptx::mbar_arrive_expect_tx(&ctl->full[stage], tx);
+                            __syncwarp();  // the byte count is posted before any gathered row lands
+                            if (lane < n4)
+                                ptx::tma_gather4(a_dst + lane * 512, &p.ag, &ctl->full[stage], k0, r0, r1, r2, r3);
+                            if (lane == 0) {
+                                ptx::tma_load_2d(b_dst, mb, &ctl->full[stage], k0, brow);
+                                if (EPI == EPI_SWIGLU)
+                                    ptx::tma_load_2d(b_dst + S::kBBytes / 2, &p.b1[tl.kind], &ctl->full[stage], k0, brow);
+                            }
+                        }
+                        issued[stage] = true;
+                        issued_phase[stage] = phase;
+                        if (++stage == S::kStages) { stage = 0; phase ^= 1u; }
+                    }
                 }
+                ok = __shfl_sync(0xffffffffu, (int)ok, 0) != 0;  // every lane agrees to stop
             }
-            if (!ok) {
+            if (!ok && lane == 0) {
                 if (rank == 0) {
                     // drain: every copy issued (for a pair, both CTAs' copies land on
                     // this CTA's full barriers) lands before teardown
@@ -587,6 +660,14 @@ bool tc_available() {
 
 int tc_tile_rows(bool pair) { return pair ? Shape<true>::kTileRows : Shape<false>::kTileRows; }
 
+// Read on every call: MOE_GATHER_MAX_ROWS (0 disables the in-GEMM gather;
+// capped at 128, the rows of one CTA's block).
+int tc_gather_max_rows() {
+    const char* s = getenv("MOE_GATHER_MAX_ROWS");
+    const int x = s ? atoi(s) : kGatherMaxRows;
+    return x < 0 ? 0 : (x > BMC ? BMC : x);
+}
+
 // Groups with at least this many rows take 256-row pair tiles.
 int tc_pair_min_rows() {
     const char* s = getenv("MOE_PAIR_MIN_ROWS");
@@ -602,7 +683,20 @@ cudaError_t launch_ffn_tc(const FfnGroups& g, const FfnPlanHeader* hdr, const in
     // ---- gate/up: h = SiLU(x W_gate^T) * (x W_up^T)
     TcParams p{};
     bool ok = true;
-    ok &= make_amaps(p.a[0], g.a_routed, R, g.d);
+    if (g.row_src) {
+        // small routed row blocks are gathered from x [T][d] by token index,
+        // large ones loaded from the permuted copy (present whenever a group
+        // can exceed the gather limit)
+        ok &= make_map(&p.ag, g.a_routed, g.T, g.d, 1);
+        if (g.a_perm) ok &= make_amaps(p.a[0], g.a_perm, R, g.d);
+        else ok &= make_amaps(p.a[0], g.a_routed, g.T, g.d);
+        p.row_src = g.row_src;
+        p.gather_max = tc_gather_max_rows();
+    } else {
+        ok &= make_amaps(p.a[0], g.a_routed, R, g.d);
+        p.ag = p.a[0][0];
+        p.row_src = nullptr;
+    }
     ok &= make_map(&p.b0[0], g.w_gate, (int64_t)g.E * g.I, g.d, 128);
     ok &= make_map(&p.b1[0], g.w_up, (int64_t)g.E * g.I, g.d, 128);
     if (g.has_shared) {

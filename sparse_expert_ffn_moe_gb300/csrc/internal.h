@@ -34,6 +34,9 @@ struct FfnGroups {
     const int32_t* row_src;  // [n_routed_rows] token of each routed row, or
                              // null: routed row p reads A row p directly
     const void* a_routed;    // rows of x_perm (or x when row_src is set)
+    const void* a_perm;      // contiguous permuted rows for the tensor-core path's
+                             // large row blocks when row_src is set (or null when
+                             // no group can exceed tc_gather_max_rows())
     const void* a_shared;    // x [T][d] (shared group input)
     const void* w_gate;      // [E][I][d]
     const void* w_up;
@@ -84,6 +87,7 @@ cudaError_t launch_ffn_gemv(const FfnGroups& g, int dtype, const FfnPlanHeader* 
 bool tc_available();
 int tc_tile_rows(bool pair);  // rows per tensor-core m-tile (single-SM or CTA pair)
 int tc_pair_min_rows();       // groups with at least this many rows take pair tiles
+int tc_gather_max_rows();     // per-CTA routed row blocks up to this size are gathered from x
 // may_pair: some group can reach tc_pair_min_rows() rows (else the pair
 // launches are skipped)
 cudaError_t launch_ffn_tc(const FfnGroups& g, const FfnPlanHeader* hdr, const int4* mtile_list,

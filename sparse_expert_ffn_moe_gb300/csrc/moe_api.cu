@@ -233,6 +233,7 @@ moe_status moe_expert_ffn(const moe_shape* shape, const void* x_perm, const int3
     g.offsets = offsets;
     g.row_src = nullptr;
     g.a_routed = x_perm;
+    g.a_perm = x_perm;
     g.a_shared = x_perm;
     g.w_gate = w_gate;
     g.w_up = w_up;
@@ -313,9 +314,14 @@ moe_status moe_forward(const moe_shape* shape, const void* x, const void* w_g, c
     e = launch_dispatch(s, topk_idx, counts, offsets, at<int32_t>(workspace, L.perm), inv, tok,
                         at<int32_t>(workspace, L.blk_hist), err, cs);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
-    void* x_perm = at<void>(workspace, L.x_perm);
-    if (need_tc) {
-        // the tensor-core path loads expert-contiguous rows with TMA
+    // Both expert paths read routed rows from x through the row -> token map
+    // (the tensor-core path with TMA gather4 for row blocks of at most
+    // tc_gather_max_rows() rows).  Larger blocks need the contiguous permuted
+    // copy, which is only built when a group can be that large (a group has at
+    // most T rows: a token picks an expert once).
+    void* x_perm = nullptr;
+    if (need_tc && s.T > tc_gather_max_rows()) {
+        x_perm = at<void>(workspace, L.x_perm);
         e = launch_gather_rows(s, x, tok, x_perm, cs);
         if (e != cudaSuccess) return MOE_ERR_CUDA;
     }
@@ -330,8 +336,9 @@ moe_status moe_forward(const moe_shape* shape, const void* x, const void* w_g, c
     g.n_routed_rows = s.T * s.K;
     g.T = s.T;
     g.offsets = offsets;
-    g.row_src = need_tc ? nullptr : tok;
-    g.a_routed = need_tc ? x_perm : x;
+    g.row_src = tok;
+    g.a_routed = x;
+    g.a_perm = x_perm;
     g.a_shared = x;
     g.w_gate = w_gate;
     g.w_up = w_up;

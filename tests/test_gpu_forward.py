@@ -164,3 +164,22 @@ def test_forward_sigmoid_router(moe, name, T):
     ok = boundary_margin(ref["logits"], cfg.K) >= 1e-4
     assert ok.mean() >= 0.75
     _check(cfg, to_f64(y[torch.from_numpy(tokens[ok]).long().cuda()]), ref["y"][ok])
+
+
+@pytest.mark.parametrize("gather_max", [0, 32, 128])
+def test_forward_skewed_groups_cover_every_activation_path(moe, monkeypatch, gather_max):
+    """Expert groups from a few rows to >1000 rows in one call, on single-SM and
+    CTA-pair tiles (pair remainders included); with the in-GEMM gather enabled,
+    row blocks of <= gather_max rows come straight from x (tile::gather4) and
+    larger ones from the permuted copy."""
+    monkeypatch.setenv("MOE_GATHER_MAX_ROWS", str(gather_max))
+    cfg = mi.LayerConfig("skewed", T=2048, d=256, E=16, K=2, I=256, Is=128, seed=4)
+    L = Layer(cfg)
+    L.bias = (torch.linspace(2.5, -2.5, cfg.E)).float().cuda()   # expert 0 hot, 15 cold
+    L.x = _clean_x(L)
+    _, _, keys = oracle.route(host(L.x), L.hp["w_g"], cfg.K, dtype=cfg.dtype, bias=L.bias_host())
+    counts = np.bincount(np.argsort(-keys, axis=1, kind="stable")[:, :cfg.K].ravel(),
+                         minlength=cfg.E)
+    assert counts.max() >= 512 and counts.min() <= 32 and ((counts > 32) & (counts < 512)).any()
+    ref = oracle.forward(host(L.x), L.hp, cfg.K, dtype=cfg.dtype, bias=L.bias_host())["y"]
+    _check(cfg, to_f64(L.forward(moe)), ref)
