@@ -135,18 +135,33 @@ dispatch_scatter_kernel(const int32_t* __restrict__ idx, int64_t n, int E, int K
     }
 }
 
-template <int V>
+// One warp per token: the token's row of x is read once (four 16-byte loads in
+// flight per lane) and written to the K permuted positions inv_perm[t*K + j],
+// so x crosses HBM once even when it does not fit in L2.
 __global__ void __launch_bounds__(256)
-gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ tok_of,
-                   uint4* __restrict__ x_perm, int64_t rows, int vec_per_row, int Tn) {
+gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ inv_perm,
+                   uint4* __restrict__ x_perm, int Tn, int K, int vec_per_row, int64_t n_rows) {
     const int lane = threadIdx.x & 31;
-    for (int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); r < rows;
-         r += (int64_t)gridDim.x * 8) {
-        const int t = tok_of[r];
-        if (t < 0 || t >= Tn) continue;
-        const uint4* src = x + (int64_t)t * vec_per_row;
-        uint4* dst = x_perm + r * vec_per_row;
-        for (int v = lane; v < vec_per_row; v += 32) dst[v] = __ldg(src + v);
+    for (int64_t t = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); t < Tn;
+         t += (int64_t)gridDim.x * 8) {
+        const int32_t my_p = lane < K ? inv_perm[t * K + lane] : -1;
+        const uint4* src = x + t * vec_per_row;
+        // warp-uniform trip count: every lane reaches the shuffles below
+        for (int b = 0; b < vec_per_row; b += 32 * 4) {
+            const int v0 = b + lane;
+            uint4 tmp[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if (v0 + 32 * q < vec_per_row) tmp[q] = __ldg(src + v0 + 32 * q);
+            for (int j = 0; j < K; ++j) {
+                const int32_t p = __shfl_sync(0xffffffffu, my_p, j);
+                if (p < 0 || p >= n_rows) continue;  // dropped slot
+                uint4* dst = x_perm + (int64_t)p * vec_per_row;
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    if (v0 + 32 * q < vec_per_row) dst[v0 + 32 * q] = tmp[q];
+            }
+        }
     }
 }
 
@@ -173,16 +188,17 @@ cudaError_t launch_dispatch(const moe_shape& s, const int32_t* topk_idx, int32_t
     return cudaGetLastError();
 }
 
-cudaError_t launch_gather_rows(const moe_shape& s, const void* x, const int32_t* tok_of,
+cudaError_t launch_gather_rows(const moe_shape& s, const void* x, const int32_t* inv_perm,
                                void* x_perm, cudaStream_t st) {
     const int64_t rows = (int64_t)s.T * s.K;
     const int esz = s.dtype == MOE_BF16 ? 2 : 4;
     const int vpr = s.d * esz / 16;
-    int64_t blocks = ceil_div(rows, 8);
+    int64_t blocks = ceil_div(s.T, 8);
     const int64_t cap = (int64_t)device_sm_count() * 8;
     if (blocks > cap) blocks = cap;
-    gather_rows_kernel<1><<<(unsigned)blocks, 256, 0, st>>>((const uint4*)x, tok_of, (uint4*)x_perm,
-                                                            rows, vpr, s.T);
+    if (blocks < 1) blocks = 1;
+    gather_rows_kernel<<<(unsigned)blocks, 256, 0, st>>>((const uint4*)x, inv_perm, (uint4*)x_perm,
+                                                         s.T, s.K, vpr, rows);
     return cudaGetLastError();
 }
 
@@ -281,6 +297,6 @@ extern "C" moe_status moe_permute_noalloc(const moe_shape* shape, const int32_t*
     int32_t* tok = reinterpret_cast<int32_t*>(b + off_tok);
     int32_t* inv = inv_perm ? inv_perm : reinterpret_cast<int32_t*>(b + off_inv);
     e = launch_dispatch(s, topk_idx, counts, offsets, perm, inv, tok, hist, err, cs);
-    if (e == cudaSuccess && x && x_perm) e = launch_gather_rows(s, x, tok, x_perm, cs);
+    if (e == cudaSuccess && x && x_perm) e = launch_gather_rows(s, x, inv, x_perm, cs);
     return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

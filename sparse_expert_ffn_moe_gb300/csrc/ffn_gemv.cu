@@ -78,7 +78,12 @@ ffn_plan_kernel(const int32_t* __restrict__ offsets, int E, int has_shared, int 
         if (g < E) { row0 = offsets[g]; rows = offsets[g + 1] - row0; }
         else if (g < G) { row0 = 0; rows = T; }
         const bool to_gemv = rows > 0 && rows <= limit;
-        const bool to_pair = rows > limit && rows >= pair_min;
+        // pair_min > 0: fixed threshold.  0: the cheaper shape by padded rows
+        // over the measured tensor-pipe activity of each shape (pair ~85%,
+        // single ~70% on GB300): pair if ceil(r/256)*256/85 < ceil(r/128)*128/70.
+        const int64_t pad_p = (int64_t)(rows + pair_m - 1) / pair_m * pair_m;
+        const int64_t pad_s = (int64_t)(rows + single_m - 1) / single_m * single_m;
+        const bool to_pair = rows > limit && (pair_min > 0 ? rows >= pair_min : pad_p * 70 < pad_s * 85);
         const int32_t st = (rows > limit && !to_pair) ? (rows + single_m - 1) / single_m : 0;
         const int32_t pt = to_pair ? (rows + pair_m - 1) / pair_m : 0;
         const int32_t pg = scan_1024(to_gemv ? 1 : 0, sh, &tot_g);

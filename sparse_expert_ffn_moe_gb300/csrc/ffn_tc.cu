@@ -669,10 +669,18 @@ int tc_gather_max_rows() {
 }
 
 // Groups with at least this many rows take 256-row pair tiles.
+// MOE_PAIR_MIN_ROWS > 0 sets a fixed threshold; unset or 0 lets the plan pick
+// the cheaper tile shape per group (padding over measured efficiency).
 int tc_pair_min_rows() {
     const char* s = getenv("MOE_PAIR_MIN_ROWS");
-    const int x = s ? atoi(s) : 512;
-    return x < 1 ? 1 : x;
+    const int x = s ? atoi(s) : 0;
+    return x < 0 ? 0 : x;
+}
+
+// Some group with at most max_rows rows could take pair tiles.
+bool tc_pair_possible(int64_t max_rows) {
+    const int pm = tc_pair_min_rows();
+    return pm > 0 ? max_rows >= pm : max_rows > Shape<false>::kTileRows;
 }
 
 cudaError_t launch_ffn_tc(const FfnGroups& g, const FfnPlanHeader* hdr, const int4* mtile_list,

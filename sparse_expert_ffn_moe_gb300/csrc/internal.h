@@ -71,7 +71,7 @@ int dispatch_blocks_for(int64_t n_slots);
 cudaError_t launch_dispatch(const moe_shape& s, const int32_t* topk_idx, int32_t* counts,
                             int32_t* offsets, int32_t* perm, int32_t* inv_perm, int32_t* tok_of,
                             int32_t* blk_hist, DevError* err, cudaStream_t st);
-cudaError_t launch_gather_rows(const moe_shape& s, const void* x, const int32_t* tok_of,
+cudaError_t launch_gather_rows(const moe_shape& s, const void* x, const int32_t* inv_perm,
                                void* x_perm, cudaStream_t st);
 
 // ---- ffn_plan + ffn_gemv.cu ----
@@ -86,7 +86,8 @@ cudaError_t launch_ffn_gemv(const FfnGroups& g, int dtype, const FfnPlanHeader* 
 // ---- ffn_tc.cu (tcgen05 grouped GEMM) ----
 bool tc_available();
 int tc_tile_rows(bool pair);  // rows per tensor-core m-tile (single-SM or CTA pair)
-int tc_pair_min_rows();       // groups with at least this many rows take pair tiles
+int tc_pair_min_rows();       // fixed pair threshold (0: the plan picks the cheaper shape)
+bool tc_pair_possible(int64_t max_rows);  // a group of at most max_rows rows may take pair tiles
 int tc_gather_max_rows();     // per-CTA routed row blocks up to this size are gathered from x
 // may_pair: some group can reach tc_pair_min_rows() rows (else the pair
 // launches are skipped)

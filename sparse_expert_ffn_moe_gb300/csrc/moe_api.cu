@@ -197,7 +197,7 @@ moe_status moe_permute(const moe_shape* shape, const int32_t* topk_idx, const vo
     e = launch_dispatch(s, topk_idx, counts, offsets, perm, inv, tok, at<int32_t>(workspace, L.blk_hist),
                         err, cs);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
-    if (x && x_perm) e = launch_gather_rows(s, x, tok, x_perm, cs);
+    if (x && x_perm) e = launch_gather_rows(s, x, inv, x_perm, cs);
     return cuda_status(e);
 }
 
@@ -248,7 +248,7 @@ moe_status moe_expert_ffn(const moe_shape* shape, const void* x_perm, const int3
     e = launch_ffn_plan(g, s.dtype, hdr, glist, mtiles, L.max_mtiles, gemv_limit(), cs);
     if (e == cudaSuccess && gemv_possible(s)) e = launch_ffn_gemv(g, s.dtype, hdr, glist, cs);
     if (e == cudaSuccess && need_tc)
-        e = launch_ffn_tc(g, hdr, mtiles, L.max_mtiles, rows >= tc_pair_min_rows(), err, cs);
+        e = launch_ffn_tc(g, hdr, mtiles, L.max_mtiles, tc_pair_possible(rows), err, cs);
     return cuda_status(e);
 }
 
@@ -322,7 +322,7 @@ moe_status moe_forward(const moe_shape* shape, const void* x, const void* w_g, c
     void* x_perm = nullptr;
     if (need_tc && s.T > tc_gather_max_rows()) {
         x_perm = at<void>(workspace, L.x_perm);
-        e = launch_gather_rows(s, x, tok, x_perm, cs);
+        e = launch_gather_rows(s, x, inv, x_perm, cs);
         if (e != cudaSuccess) return MOE_ERR_CUDA;
     }
 
@@ -357,7 +357,7 @@ moe_status moe_forward(const moe_shape* shape, const void* x, const void* w_g, c
     if (e == cudaSuccess && gemv_possible(s)) e = launch_ffn_gemv(g, s.dtype, hdr, glist, cs);
     // a group has at most T rows (a token picks an expert once)
     if (e == cudaSuccess && need_tc)
-        e = launch_ffn_tc(g, hdr, mtiles, L.max_mtiles, s.T >= tc_pair_min_rows(), err, cs);
+        e = launch_ffn_tc(g, hdr, mtiles, L.max_mtiles, tc_pair_possible(s.T), err, cs);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
 
     // 4. combine
