@@ -66,17 +66,19 @@ def layer_bytes(cfg, n_active: int) -> int:
                 + 2 * cfg.T * cfg.d)
 
 
-def launches_per_forward(cfg, gemv_limit: int = 0, pair_min: int = 512) -> int:
+def launches_per_forward(cfg, gemv_limit: int = 0) -> int:
     """Kernels libmoe launches for one moe_forward (mirrors the host logic in
     moe_api.cu): router (GEMV or tcgen05) + top-K, 3 dispatch kernels, the row
     gather when the tensor-core path may run, the FFN plan,
     (2 GEMV kernels only for fp32 layers or a non-zero GEMV row limit), the
     single-SM tcgen05 gate/up and down GEMMs when needed, and the CTA-pair
-    ones too when a group can reach pair_min rows, combine."""
+    ones too when a group can hold more rows than one 128-row tile (or, with
+    MOE_PAIR_MIN_ROWS set, at least that many rows), combine."""
     need_tc = cfg.dtype == "bf16" and cfg.T > gemv_limit
     gather = need_tc and cfg.T > int(os.environ.get("MOE_GATHER_MAX_ROWS", "0"))
     gemv = cfg.dtype == "f32" or gemv_limit > 0
-    pair = need_tc and cfg.T >= pair_min
+    pair_min = int(os.environ.get("MOE_PAIR_MIN_ROWS", "0"))
+    pair = need_tc and (cfg.T >= pair_min if pair_min > 0 else cfg.T > 128)
     return (2 + 3 + (1 if gather else 0) + 1 + (2 if gemv else 0) + (2 if need_tc else 0)
             + (2 if pair else 0) + 1)
 
