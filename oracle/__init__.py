@@ -13,7 +13,8 @@ SwiGLU expert FFN and the weighted combine plus the shared expert.
 
 Inputs: ``dtype`` is ``"f32"`` (numpy float32 arrays) or ``"bf16"`` (numpy
 uint16 arrays holding bf16 bit patterns).  Outputs are float64 / int32 numpy
-arrays.
+arrays.  8-bit expert weights are numpy uint8 arrays of E4M3 codes with one
+float32 scale per weight row (``*_fp8`` functions).
 """
 from __future__ import annotations
 
@@ -67,8 +68,16 @@ def bind(lib):
     lib.oracle_shared_ffn.argtypes = [i64, i64, i64, i32, vp, vp, vp, vp, vp, i32]
     lib.oracle_forward.argtypes = [i64] * 6 + [i32, i32] + [vp] * 16 + [i32]
     lib.oracle_forward_tokens.argtypes = [i64, vp] + [i64] * 6 + [i32, i32] + [vp] * 13 + [i32]
+    lib.oracle_expert_ffn_fp8.argtypes = [i64, i64, i64, i32] + [vp] * 9 + [i32]
+    lib.oracle_forward_tokens_fp8.argtypes = ([i64, vp] + [i64] * 6 + [i32, i32] + [vp] * 19
+                                              + [i32])
+    lib.oracle_e4m3_decode.argtypes = [i64, vp, vp]
+    lib.oracle_e4m3_encode.argtypes = [i64, vp, vp]
+    lib.oracle_quantize_fp8_rows.argtypes = [i64, i64, i32, vp, vp, vp]
     for f in ("oracle_route", "oracle_permute", "oracle_expert_ffn", "oracle_combine",
-              "oracle_shared_ffn", "oracle_forward", "oracle_forward_tokens"):
+              "oracle_shared_ffn", "oracle_forward", "oracle_forward_tokens",
+              "oracle_expert_ffn_fp8", "oracle_forward_tokens_fp8", "oracle_e4m3_decode",
+              "oracle_e4m3_encode", "oracle_quantize_fp8_rows"):
         getattr(lib, f).restype = i32
     return lib
 
@@ -256,4 +265,99 @@ def forward_tokens(tokens, x, params: dict, K: int, dtype: str = "f32", bias=Non
         _ptr(w["w_gate"]), _ptr(w["w_up"]), _ptr(w["w_down"]), _ptr(w["ws_gate"]),
         _ptr(w["ws_up"]), _ptr(w["ws_down"]), _ptr(out["y"]), _ptr(out["topk_idx"]),
         _ptr(out["topk_w"]), _ptr(out["logits"]), threads), "oracle_forward_tokens")
+    return out
+
+
+# ---------------------------------------------------------------- 8-bit weights
+
+def e4m3_decode(codes):
+    """The exact value of every E4M3 code (float64; NaN for the NaN codes)."""
+    lib = _load()
+    c = _arr(codes, np.uint8)
+    out = np.zeros(c.shape, np.float64)
+    _check(lib.oracle_e4m3_decode(c.size, _ptr(c), _ptr(out)), "oracle_e4m3_decode")
+    return out
+
+
+def e4m3_encode(v):
+    """Nearest E4M3 code of each float32 value (ties to even, clamped to +-448)."""
+    lib = _load()
+    v = _arr(v, np.float32)
+    out = np.zeros(v.shape, np.uint8)
+    _check(lib.oracle_e4m3_encode(v.size, _ptr(v), _ptr(out)), "oracle_e4m3_encode")
+    return out
+
+
+def quantize_fp8_rows(w, dtype: str = "f32"):
+    """Per-row E4M3 quantisation of a [..., cols] matrix: returns (codes uint8 of
+    w's shape, scales float32 of w's leading shape)."""
+    lib = _load()
+    w = _in(w, dtype)
+    cols = w.shape[-1]
+    rows = w.size // cols
+    codes = np.zeros(w.shape, np.uint8)
+    scales = np.zeros(w.shape[:-1], np.float32)
+    _check(lib.oracle_quantize_fp8_rows(rows, cols, _DT[dtype], _ptr(w), _ptr(codes),
+                                        _ptr(scales)), "oracle_quantize_fp8_rows")
+    return codes, scales
+
+
+_FP8_NAMES = ("w_gate", "w_up", "w_down", "ws_gate", "ws_up", "ws_down")
+
+
+def _fp8_weights(q: dict):
+    """Codes (uint8) and row scales (float32) of the expert weights: keys w_gate,
+    s_gate, ... as in the C signature (shared ones optional)."""
+    out = {}
+    for n in _FP8_NAMES:
+        out[n] = _arr(q.get(n), np.uint8)
+        sn = "s" + n[1:] if n.startswith("w_") else "ss" + n[2:]
+        out[sn] = _arr(q.get(sn), np.float32)
+    return out
+
+
+def expert_ffn_fp8(x_perm, offsets, q: dict, dtype: str = "bf16", threads: int = 0):
+    """SwiGLU per expert with E4M3 weights (q: w_gate, w_up, w_down codes and
+    s_gate, s_up, s_down row scales).  Returns y_perm [rows, d] f64."""
+    lib = _load()
+    x_perm = _in(x_perm, dtype)
+    offsets = _arr(offsets, np.int32)
+    w = _fp8_weights(q)
+    E, I, d = w["w_gate"].shape
+    rows = int(offsets[E])
+    y = np.zeros((max(rows, 0), d), np.float64)
+    _check(lib.oracle_expert_ffn_fp8(
+        d, E, I, _DT[dtype], _ptr(x_perm), _ptr(offsets), _ptr(w["w_gate"]), _ptr(w["w_up"]),
+        _ptr(w["w_down"]), _ptr(w["s_gate"]), _ptr(w["s_up"]), _ptr(w["s_down"]), _ptr(y),
+        threads), "oracle_expert_ffn_fp8")
+    return y
+
+
+def forward_tokens_fp8(tokens, x, w_g, q: dict, K: int, dtype: str = "bf16", bias=None,
+                       threads: int = 0, router: str = "softmax"):
+    """forward_tokens with E4M3 expert weights (routed and, when present, shared):
+    q holds w_gate/w_up/w_down (+ ws_*) codes and s_gate/s_up/s_down (+ ss_*)
+    row scales; x and w_g are in dtype.  Returns the same dict as forward_tokens."""
+    lib = _load()
+    tokens = _arr(tokens, np.int32)
+    x, w_g = _in(x, dtype), _in(w_g, dtype)
+    w = _fp8_weights(q)
+    T, d = x.shape
+    E, I, _ = w["w_gate"].shape
+    Is = 0 if w["ws_gate"] is None else w["ws_gate"].shape[0]
+    n = tokens.shape[0]
+    bias = _arr(bias, np.float64)
+    out = {
+        "y": np.zeros((n, d), np.float64),
+        "topk_idx": np.zeros((n, K), np.int32),
+        "topk_w": np.zeros((n, K), np.float64),
+        "logits": np.zeros((n, E), np.float64),
+    }
+    _check(lib.oracle_forward_tokens_fp8(
+        n, _ptr(tokens), T, d, E, K, I, Is, _DT[dtype], _ROUTER[router], _ptr(x), _ptr(w_g),
+        _ptr(bias), _ptr(w["w_gate"]), _ptr(w["w_up"]), _ptr(w["w_down"]), _ptr(w["s_gate"]),
+        _ptr(w["s_up"]), _ptr(w["s_down"]), _ptr(w["ws_gate"]), _ptr(w["ws_up"]),
+        _ptr(w["ws_down"]), _ptr(w["ss_gate"]), _ptr(w["ss_up"]), _ptr(w["ss_down"]),
+        _ptr(out["y"]), _ptr(out["topk_idx"]), _ptr(out["topk_w"]), _ptr(out["logits"]),
+        threads), "oracle_forward_tokens_fp8")
     return out

@@ -39,6 +39,19 @@
  *   shared ws_gate/ws_up [Is][d], ws_down [d][Is].
  * dtype 0 = fp32 (float), 1 = bf16 (uint16_t bit patterns).
  *
+ * 8-bit expert weights ("LLM inference optimisation" page, section "make
+ * every byte cheaper": x_q = round(x / s) + z, x_hat = (x_q - z) s, with the
+ * scale per tensor, per channel or per group): codes are OCP E4M3 floats
+ * (1 sign bit, 4 exponent bits with bias 7, 3 mantissa bits; largest finite
+ * magnitude 448; S.1111.111 is NaN; no infinities), zero point 0, one fp32
+ * scale per weight row (output channel).  The dequantised weight is
+ * w_hat[r][c] = value(code[r][c]) * scale[r]; the fp8 layer is the layer
+ * above with every expert matrix replaced by w_hat (router weights stay in
+ * the activation dtype).  Readings: "round" is round-to-nearest, ties to an
+ * even mantissa, onto the E4M3 grid, clamped to +-448; the row scale maps the
+ * row's largest magnitude to 448 (scale = amax / 448 in fp32, 1 for a row of
+ * zeros).
+ *
  * Every entry point returns 0 on success and a negative number on a bad
  * argument; nothing is allocated that is not freed before return.
  */
@@ -51,6 +64,7 @@
 
 #define ORC_F32 0
 #define ORC_BF16 1
+#define ORC_E4M3 2 /* weight codes only: 8-bit E4M3 float times a per-row scale */
 
 /* ------------------------------------------------------------------------ */
 /* element access: the exact stored value, widened to double                */
@@ -73,6 +87,81 @@ static double load_elem(const void *base, int dtype, int64_t i)
 }
 
 static size_t elem_size(int dtype) { return dtype == ORC_BF16 ? 2u : 4u; }
+
+/* ------------------------------------------------------------------------ */
+/* E4M3 codes                                                               */
+/* ------------------------------------------------------------------------ */
+
+/* The value of an E4M3 code: exponent field E (bias 7), mantissa M (3 bits);
+ * E = 0 is the subnormal range M/8 * 2^-6; S.1111.111 is NaN. */
+static double e4m3_value(uint8_t c)
+{
+    const int sgn = c >> 7, E = (c >> 3) & 15, M = c & 7;
+    double v;
+    if (E == 15 && M == 7)
+        return NAN;
+    if (E == 0)
+        v = ldexp((double)M, -9);
+    else
+        v = ldexp(8.0 + M, E - 10); /* (1 + M/8) * 2^(E-7) */
+    return sgn ? -v : v;
+}
+
+/* Round-to-nearest-even onto the E4M3 grid; magnitudes above 448 (and
+ * infinities) clamp to 448, NaN gives S.1111.111.  The grid spacing is 2^-9
+ * below 2^-6 (subnormals) and 2^(e-3) in the binade [2^e, 2^(e+1)). */
+static uint8_t e4m3_code(float f)
+{
+    const uint8_t sgn = signbit(f) ? 0x80 : 0x00;
+    if (isnan(f))
+        return sgn | 0x7F;
+    const double a = fabs((double)f);
+    if (a >= 448.0)
+        return sgn | 0x7E;
+    double unit;
+    if (a < ldexp(1.0, -6)) {
+        unit = ldexp(1.0, -9);
+    } else {
+        int ex;
+        frexp(a, &ex); /* a = m 2^ex, 0.5 <= m < 1: the binade is [2^(ex-1), 2^ex) */
+        unit = ldexp(1.0, ex - 1 - 3);
+    }
+    const double v = nearbyint(a / unit) * unit; /* ties to even (default mode) */
+    if (v < ldexp(1.0, -6))
+        return sgn | (uint8_t)(v * 512.0); /* zero or subnormal: M = v / 2^-9 */
+    int ex;
+    const double m = frexp(v, &ex);
+    return sgn | (uint8_t)(((ex - 1 + 7) << 3) | (int)(m * 16.0 - 8.0));
+}
+
+/* A weight matrix as the FFN reads it: fp32 / bf16 elements, or E4M3 codes
+ * with one scale per row of row_len elements. */
+typedef struct {
+    const void *base;
+    int fmt; /* ORC_F32, ORC_BF16 or ORC_E4M3 */
+    const float *scale;
+    int64_t row_len;
+} orc_weight;
+
+static orc_weight plain_weight(const void *base, int dtype)
+{
+    orc_weight w = {base, dtype, NULL, 1};
+    return w;
+}
+
+static orc_weight fp8_weight(const void *codes, const float *scale, int64_t row_len)
+{
+    orc_weight w = {codes, ORC_E4M3, scale, row_len};
+    return w;
+}
+
+/* w_hat[i] = value(code[i]) * scale[row of i], or the stored element */
+static double load_weight(const orc_weight *w, int64_t i)
+{
+    if (w->fmt == ORC_E4M3)
+        return e4m3_value(((const uint8_t *)w->base)[i]) * (double)w->scale[i / w->row_len];
+    return load_elem(w->base, w->fmt, i);
+}
 
 /* ------------------------------------------------------------------------ */
 /* a plain parallel-for over independent rows (tokens or permuted rows)     */
@@ -320,16 +409,16 @@ int oracle_permute(int64_t T, int64_t E, int64_t K, const int32_t *topk_idx,
  * W_gate, W_up, W_down is the expert of the llmgo page (section 1.2) and the
  * gated MLP "up, gate, down" of "LLM from scratch, ch. 6" (MLP roofline). */
 static void swiglu_row(int64_t d, int64_t I, int dtype, const void *xrow_base,
-                       int64_t xrow_off, const void *w_gate, const void *w_up,
-                       const void *w_down, int64_t wg_off, int64_t wu_off,
+                       int64_t xrow_off, const orc_weight *w_gate, const orc_weight *w_up,
+                       const orc_weight *w_down, int64_t wg_off, int64_t wu_off,
                        int64_t wd_off, double *h, double *y)
 {
     for (int64_t i = 0; i < I; ++i) {
         double g = 0.0, u = 0.0;
         for (int64_t k = 0; k < d; ++k) {
             double xv = load_elem(xrow_base, dtype, xrow_off + k);
-            g += load_elem(w_gate, dtype, wg_off + i * d + k) * xv;
-            u += load_elem(w_up, dtype, wu_off + i * d + k) * xv;
+            g += load_weight(w_gate, wg_off + i * d + k) * xv;
+            u += load_weight(w_up, wu_off + i * d + k) * xv;
         }
         double silu = g / (1.0 + exp(-g));
         h[i] = silu * u;
@@ -337,7 +426,7 @@ static void swiglu_row(int64_t d, int64_t I, int dtype, const void *xrow_base,
     for (int64_t j = 0; j < d; ++j) {
         double acc = 0.0;
         for (int64_t i = 0; i < I; ++i)
-            acc += load_elem(w_down, dtype, wd_off + j * I + i) * h[i];
+            acc += load_weight(w_down, wd_off + j * I + i) * h[i];
         y[j] = acc;
     }
 }
@@ -347,7 +436,7 @@ typedef struct {
     int dtype;
     const void *x_perm;
     const int32_t *offsets;
-    const void *w_gate, *w_up, *w_down;
+    orc_weight w_gate, w_up, w_down;
     double *y_perm;
 } ffn_ctx;
 
@@ -367,8 +456,8 @@ static void ffn_row(void *vctx, int64_t p)
     int64_t e = expert_of_row(c->offsets, c->E, p);
     double *h = (double *)malloc(sizeof(double) * (size_t)c->I);
     const int64_t wgu = e * c->I * c->d, wd = e * c->d * c->I;
-    swiglu_row(c->d, c->I, c->dtype, c->x_perm, p * c->d, c->w_gate, c->w_up,
-               c->w_down, wgu, wgu, wd, h, c->y_perm + p * c->d);
+    swiglu_row(c->d, c->I, c->dtype, c->x_perm, p * c->d, &c->w_gate, &c->w_up,
+               &c->w_down, wgu, wgu, wd, h, c->y_perm + p * c->d);
     free(h);
 }
 
@@ -378,10 +467,9 @@ static void ffn_row(void *vctx, int64_t p)
  * in fp64.  Experts with zero rows contribute nothing and read nothing
  * (llmgo page, FAQ Q1).
  */
-int oracle_expert_ffn(int64_t d, int64_t E, int64_t I, int dtype,
-                      const void *x_perm, const int32_t *offsets,
-                      const void *w_gate, const void *w_up, const void *w_down,
-                      double *y_perm, int nthreads)
+static int expert_ffn(int64_t d, int64_t E, int64_t I, int dtype, const void *x_perm,
+                      const int32_t *offsets, orc_weight w_gate, orc_weight w_up,
+                      orc_weight w_down, double *y_perm, int nthreads)
 {
     if (d < 1 || E < 1 || I < 1 || !offsets || !y_perm)
         return -1;
@@ -393,6 +481,32 @@ int oracle_expert_ffn(int64_t d, int64_t E, int64_t I, int dtype,
     ffn_ctx c = {d, E, I, dtype, x_perm, offsets, w_gate, w_up, w_down, y_perm};
     par_for(offsets[E], nthreads, ffn_row, &c);
     return 0;
+}
+
+int oracle_expert_ffn(int64_t d, int64_t E, int64_t I, int dtype,
+                      const void *x_perm, const int32_t *offsets,
+                      const void *w_gate, const void *w_up, const void *w_down,
+                      double *y_perm, int nthreads)
+{
+    return expert_ffn(d, E, I, dtype, x_perm, offsets, plain_weight(w_gate, dtype),
+                      plain_weight(w_up, dtype), plain_weight(w_down, dtype), y_perm, nthreads);
+}
+
+/* The same with E4M3 expert weights: codes w_gate/w_up [E][I][d] with scales
+ * s_gate/s_up [E][I], w_down [E][d][I] with s_down [E][d] (one scale per
+ * weight row); x_perm in dtype. */
+int oracle_expert_ffn_fp8(int64_t d, int64_t E, int64_t I, int dtype,
+                          const void *x_perm, const int32_t *offsets,
+                          const uint8_t *w_gate, const uint8_t *w_up,
+                          const uint8_t *w_down, const float *s_gate,
+                          const float *s_up, const float *s_down,
+                          double *y_perm, int nthreads)
+{
+    if (!w_gate || !w_up || !w_down || !s_gate || !s_up || !s_down)
+        return -1;
+    return expert_ffn(d, E, I, dtype, x_perm, offsets, fp8_weight(w_gate, s_gate, d),
+                      fp8_weight(w_up, s_up, d), fp8_weight(w_down, s_down, I), y_perm,
+                      nthreads);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -432,7 +546,8 @@ int oracle_combine(int64_t T, int64_t d, int64_t K, const double *y_perm,
 typedef struct {
     int64_t d, Is;
     int dtype;
-    const void *x, *ws_gate, *ws_up, *ws_down;
+    const void *x;
+    orc_weight ws_gate, ws_up, ws_down;
     const int32_t *tokens;
     double *y_s;
 } shared_ctx;
@@ -442,8 +557,8 @@ static void shared_row(void *vctx, int64_t r)
     shared_ctx *c = (shared_ctx *)vctx;
     int64_t t = c->tokens ? c->tokens[r] : r;
     double *h = (double *)malloc(sizeof(double) * (size_t)c->Is);
-    swiglu_row(c->d, c->Is, c->dtype, c->x, t * c->d, c->ws_gate, c->ws_up,
-               c->ws_down, 0, 0, 0, h, c->y_s + r * c->d);
+    swiglu_row(c->d, c->Is, c->dtype, c->x, t * c->d, &c->ws_gate, &c->ws_up,
+               &c->ws_down, 0, 0, 0, h, c->y_s + r * c->d);
     free(h);
 }
 
@@ -455,7 +570,8 @@ int oracle_shared_ffn(int64_t T, int64_t d, int64_t Is, int dtype,
 {
     if (T < 0 || d < 1 || Is < 1 || !y_s)
         return -1;
-    shared_ctx c = {d, Is, dtype, x, ws_gate, ws_up, ws_down, NULL, y_s};
+    shared_ctx c = {d, Is, dtype, x, plain_weight(ws_gate, dtype), plain_weight(ws_up, dtype),
+                    plain_weight(ws_down, dtype), NULL, y_s};
     par_for(T, nthreads, shared_row, &c);
     return 0;
 }
@@ -531,7 +647,7 @@ typedef struct {
     int dtype, mode;
     const void *x, *w_g;
     const double *bias;
-    const void *w_gate, *w_up, *w_down, *ws_gate, *ws_up, *ws_down;
+    orc_weight w_gate, w_up, w_down, ws_gate, ws_up, ws_down;
     const int32_t *tokens;
     double *y, *logits;
     int32_t *idx;
@@ -560,8 +676,8 @@ static void token_row(void *vctx, int64_t r)
 
     /* y = SharedExpert(x_t) + sum_j w_j * Expert_{i_j}(x_t) */
     if (c->Is) {
-        swiglu_row(d, c->Is, c->dtype, c->x, t * d, c->ws_gate, c->ws_up,
-                   c->ws_down, 0, 0, 0, h, y);
+        swiglu_row(d, c->Is, c->dtype, c->x, t * d, &c->ws_gate, &c->ws_up,
+                   &c->ws_down, 0, 0, 0, h, y);
     } else {
         for (int64_t k = 0; k < d; ++k)
             y[k] = 0.0;
@@ -569,8 +685,8 @@ static void token_row(void *vctx, int64_t r)
     for (int64_t j = 0; j < c->K; ++j) {
         const int64_t e = idx[j];
         const int64_t wgu = e * c->I * d, wd = e * d * c->I;
-        swiglu_row(d, c->I, c->dtype, c->x, t * d, c->w_gate, c->w_up,
-                   c->w_down, wgu, wgu, wd, h, ye);
+        swiglu_row(d, c->I, c->dtype, c->x, t * d, &c->w_gate, &c->w_up,
+                   &c->w_down, wgu, wgu, wd, h, ye);
         for (int64_t k = 0; k < d; ++k)
             y[k] += w[j] * ye[k];
     }
@@ -587,13 +703,10 @@ static void token_row(void *vctx, int64_t r)
  * topk_w [n][K], logits [n][E] (optional: the selection keys); mode selects
  * the router (0 softmax, 1 sigmoid).
  */
-int oracle_forward_tokens(int64_t n, const int32_t *tokens, int64_t T,
-                          int64_t d, int64_t E, int64_t K, int64_t I,
-                          int64_t Is, int dtype, int mode, const void *x,
-                          const void *w_g, const double *bias,
-                          const void *w_gate, const void *w_up,
-                          const void *w_down, const void *ws_gate,
-                          const void *ws_up, const void *ws_down, double *y,
+static int forward_tokens(int64_t n, const int32_t *tokens, int64_t T, int64_t d,
+                          int64_t E, int64_t K, int64_t I, int64_t Is, int dtype,
+                          int mode, const void *x, const void *w_g,
+                          const double *bias, const orc_weight w[6], double *y,
                           int32_t *topk_idx, double *topk_w, double *logits,
                           int nthreads)
 {
@@ -604,8 +717,107 @@ int oracle_forward_tokens(int64_t n, const int32_t *tokens, int64_t T,
     for (int64_t r = 0; r < n; ++r)
         if (tokens[r] < 0 || tokens[r] >= T)
             return -1;
-    tok_ctx c = {d, E, K, I, Is, dtype, mode, x, w_g, bias, w_gate, w_up, w_down,
-                 ws_gate, ws_up, ws_down, tokens, y, logits, topk_idx, topk_w};
+    tok_ctx c = {d, E, K, I, Is, dtype, mode, x, w_g, bias, w[0], w[1], w[2],
+                 w[3], w[4], w[5], tokens, y, logits, topk_idx, topk_w};
     par_for(n, nthreads, token_row, &c);
+    return 0;
+}
+
+int oracle_forward_tokens(int64_t n, const int32_t *tokens, int64_t T,
+                          int64_t d, int64_t E, int64_t K, int64_t I,
+                          int64_t Is, int dtype, int mode, const void *x,
+                          const void *w_g, const double *bias,
+                          const void *w_gate, const void *w_up,
+                          const void *w_down, const void *ws_gate,
+                          const void *ws_up, const void *ws_down, double *y,
+                          int32_t *topk_idx, double *topk_w, double *logits,
+                          int nthreads)
+{
+    const orc_weight w[6] = {plain_weight(w_gate, dtype), plain_weight(w_up, dtype),
+                             plain_weight(w_down, dtype), plain_weight(ws_gate, dtype),
+                             plain_weight(ws_up, dtype), plain_weight(ws_down, dtype)};
+    return forward_tokens(n, tokens, T, d, E, K, I, Is, dtype, mode, x, w_g, bias, w, y,
+                          topk_idx, topk_w, logits, nthreads);
+}
+
+/*
+ * oracle_forward_tokens_fp8: oracle_forward_tokens with E4M3 expert weights
+ * (routed and shared), one fp32 scale per weight row: s_gate/s_up [E][I],
+ * s_down [E][d], ss_gate/ss_up [Is], ss_down [d].  x and w_g are in dtype.
+ */
+int oracle_forward_tokens_fp8(int64_t n, const int32_t *tokens, int64_t T,
+                              int64_t d, int64_t E, int64_t K, int64_t I,
+                              int64_t Is, int dtype, int mode, const void *x,
+                              const void *w_g, const double *bias,
+                              const uint8_t *w_gate, const uint8_t *w_up,
+                              const uint8_t *w_down, const float *s_gate,
+                              const float *s_up, const float *s_down,
+                              const uint8_t *ws_gate, const uint8_t *ws_up,
+                              const uint8_t *ws_down, const float *ss_gate,
+                              const float *ss_up, const float *ss_down,
+                              double *y, int32_t *topk_idx, double *topk_w,
+                              double *logits, int nthreads)
+{
+    if (!w_gate || !w_up || !w_down || !s_gate || !s_up || !s_down)
+        return -1;
+    if (Is > 0 && (!ws_gate || !ws_up || !ws_down || !ss_gate || !ss_up || !ss_down))
+        return -1;
+    const orc_weight w[6] = {fp8_weight(w_gate, s_gate, d), fp8_weight(w_up, s_up, d),
+                             fp8_weight(w_down, s_down, I), fp8_weight(ws_gate, ss_gate, d),
+                             fp8_weight(ws_up, ss_up, d), fp8_weight(ws_down, ss_down, Is)};
+    return forward_tokens(n, tokens, T, d, E, K, I, Is, dtype, mode, x, w_g, bias, w, y,
+                          topk_idx, topk_w, logits, nthreads);
+}
+
+/* ------------------------------------------------------------------------ */
+/* E4M3 codes and row quantisation                                          */
+/* ------------------------------------------------------------------------ */
+
+/* out[i] = value(codes[i]) (NaN for the NaN codes) */
+int oracle_e4m3_decode(int64_t n, const uint8_t *codes, double *out)
+{
+    if (n < 0 || (n > 0 && (!codes || !out)))
+        return -1;
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = e4m3_value(codes[i]);
+    return 0;
+}
+
+/* codes[i] = the E4M3 code nearest to v[i] (ties to even, clamped to +-448) */
+int oracle_e4m3_encode(int64_t n, const float *v, uint8_t *codes)
+{
+    if (n < 0 || (n > 0 && (!v || !codes)))
+        return -1;
+    for (int64_t i = 0; i < n; ++i)
+        codes[i] = e4m3_code(v[i]);
+    return 0;
+}
+
+/*
+ * oracle_quantize_fp8_rows: per-channel quantisation of a row-major
+ * [rows][cols] weight matrix (fp32 or bf16) to E4M3 codes with one fp32
+ * scale per row (the x_q = round(x / s) + z form of the quantisation section
+ * with z = 0): scale[r] = amax_r / 448 (1 when the row is all zeros), computed
+ * in fp32; code = nearest E4M3 to (w / scale[r]) computed as an fp32 division.
+ */
+int oracle_quantize_fp8_rows(int64_t rows, int64_t cols, int dtype, const void *w,
+                             uint8_t *codes, float *scale)
+{
+    if (rows < 0 || cols < 1 || (rows > 0 && (!w || !codes || !scale)))
+        return -1;
+    for (int64_t r = 0; r < rows; ++r) {
+        float amax = 0.0f;
+        for (int64_t c = 0; c < cols; ++c) {
+            const float a = fabsf((float)load_elem(w, dtype, r * cols + c));
+            if (a > amax)
+                amax = a;
+        }
+        const float s = amax > 0.0f ? amax / 448.0f : 1.0f;
+        scale[r] = s;
+        for (int64_t c = 0; c < cols; ++c) {
+            const float q = (float)load_elem(w, dtype, r * cols + c) / s;
+            codes[r * cols + c] = e4m3_code(q);
+        }
+    }
     return 0;
 }

@@ -6,6 +6,7 @@ import os
 import pytest
 
 import oracle
+from tests import test_oracle_fp8 as pins8
 from tests import test_oracle_pins as pins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "moe_oracle.c")
@@ -16,8 +17,8 @@ MUTATIONS = [
     ("softmax_sign", "w[j] = exp(key[idx[j]] - kmax);", "w[j] = exp(kmax - key[idx[j]]);"),
     ("silu_sign", "double silu = g / (1.0 + exp(-g));", "double silu = g / (1.0 + exp(g));"),
     ("dropped_up_projection", "h[i] = silu * u;", "h[i] = silu;"),
-    ("transposed_down_projection", "load_elem(w_down, dtype, wd_off + j * I + i)",
-     "load_elem(w_down, dtype, wd_off + i * d + j)"),
+    ("transposed_down_projection", "load_weight(w_down, wd_off + j * I + i)",
+     "load_weight(w_down, wd_off + i * d + j)"),
     ("swapped_gate_and_up", "double silu = g / (1.0 + exp(-g));\n        h[i] = silu * u;",
      "double silu = u / (1.0 + exp(-u));\n        h[i] = silu * g;"),
     ("dropped_bias", "const double b = bias ? bias[e] : 0.0;", "const double b = 0.0;"),
@@ -31,6 +32,14 @@ MUTATIONS = [
     ("bias_leaks_into_sigmoid_weights", "w[j] = aff[idx[j]] / (denom + 1e-6);",
      "w[j] = key[idx[j]] / (denom + 1e-6);"),
     ("router_reads_wrong_row", "load_elem(w_g, dtype, e * d + k)", "load_elem(w_g, dtype, ((e + 1) % E) * d + k)"),
+    ("e4m3_exponent_bias", "v = ldexp(8.0 + M, E - 10);", "v = ldexp(8.0 + M, E - 11);"),
+    ("e4m3_subnormal_step", "v = ldexp((double)M, -9);", "v = ldexp((double)M, -10);"),
+    ("e4m3_round_half_up", "nearbyint(a / unit)", "floor(a / unit + 0.5)"),
+    ("e4m3_no_saturation", "return sgn | 0x7E;", "return sgn | 0x7F;"),
+    ("fp8_scale_by_column", "(double)w->scale[i / w->row_len]", "(double)w->scale[i % w->row_len]"),
+    ("fp8_down_scale_row_length", "fp8_weight(w_down, s_down, I), fp8_weight(ws_gate",
+     "fp8_weight(w_down, s_down, d), fp8_weight(ws_gate"),
+    ("quant_scale_not_amax", "amax / 448.0f", "amax / 240.0f"),
 ]
 
 PIN_TESTS = [
@@ -48,6 +57,11 @@ PIN_TESTS = [
     lambda: pins.test_sigmoid_router_matches_brute_force(40, 64, 6, 4),
     lambda: pins.test_sigmoid_bias_steers_selection_but_not_weights(),
     lambda: pins.test_sigmoid_forward_matches_dense_masked_evaluation("f32"),
+    lambda: pins8.test_decode_matches_torch_float8_for_every_code(),
+    lambda: pins8.test_encode_is_the_nearest_code_with_ties_to_even(),
+    lambda: pins8.test_encode_saturates_and_keeps_nan(),
+    lambda: pins8.test_quantised_rows_meet_the_format_error_bound("f32"),
+    lambda: pins8.test_fp8_layer_equals_the_layer_on_dequantised_weights("bf16", 0),
 ]
 
 
