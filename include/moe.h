@@ -205,6 +205,75 @@ moe_status moe_forward(const moe_shape *shape, const void *x, const void *w_g,
                        void *workspace, size_t ws_bytes, void *stream);
 
 /*
+ * ---- 8-bit expert weights ------------------------------------------------
+ * [Q] "LLM from scratch, ch. 6" (foundations of inference optimisation),
+ * section "second route: make every byte cheaper": weight quantisation
+ * x_q = round(x / s) + z, x_hat = (x_q - z) s,
+ * with the scale per tensor, per channel or per group; for memory-bound
+ * decode one byte per weight instead of two halves the streamed bytes.
+ *
+ * Format: OCP E4M3 codes (1 sign bit, 4 exponent bits with bias 7, 3
+ * mantissa bits; largest finite magnitude 448; S.1111.111 is NaN), zero
+ * point 0, one fp32 scale per weight ROW (output channel):
+ *     w_hat[r][c] = e4m3_value(code[r][c]) * scale[r].
+ * The layer is the bf16 layer above with every expert matrix (routed and
+ * shared) replaced by w_hat; x, w_g, y and the intermediates stay bf16.
+ * The kernels widen codes to bf16 (exact), multiply on the tensor cores
+ * with fp32 accumulation and apply the row scale to the fp32 sums.
+ */
+typedef struct moe_fp8_experts {
+    const uint8_t *w_gate;  /* [E][I][d] codes                       */
+    const uint8_t *w_up;    /* [E][I][d] codes                       */
+    const uint8_t *w_down;  /* [E][d][I] codes                       */
+    const float *s_gate;    /* [E][I] row scales                     */
+    const float *s_up;      /* [E][I]                                */
+    const float *s_down;    /* [E][d]                                */
+    const uint8_t *ws_gate; /* [Is][d] shared-expert codes, or NULL  */
+    const uint8_t *ws_up;   /* [Is][d]                               */
+    const uint8_t *ws_down; /* [d][Is]                               */
+    const float *ss_gate;   /* [Is]                                  */
+    const float *ss_up;     /* [Is]                                  */
+    const float *ss_down;   /* [d]                                   */
+} moe_fp8_experts;
+
+/*
+ * Per-row quantisation [Q]: for each row r of the row-major [rows][cols]
+ * matrix w (dtype MOE_F32 or MOE_BF16), scale[r] = max_c |w[r][c]| / 448
+ * (fp32 division; 1 for a row of zeros) and code[r][c] = the E4M3 value
+ * nearest to w[r][c] / scale[r] (fp32 division; ties to an even mantissa;
+ * magnitudes past 448 saturate).  w must be finite.  codes [rows][cols]
+ * (uint8) and scales [rows] (fp32) are device buffers.  Limits: rows < 2^31,
+ * cols a multiple of 16.  rows == 0 is a no-op.  An offline step (a user
+ * converting bf16 checkpoints); enqueued on `stream`, no workspace.
+ */
+moe_status moe_quantize_fp8_rows(int64_t rows, int64_t cols, int32_t dtype,
+                                 const void *w, uint8_t *codes, float *scales,
+                                 void *stream);
+
+/*
+ * moe_expert_ffn with 8-bit expert weights: *w is a HOST struct of device
+ * pointers (the ws_* / ss_* members are ignored here).  shape->dtype must be
+ * MOE_BF16 and d, inter multiples of 128 (else MOE_ERR_UNSUPPORTED); scale
+ * arrays 16-byte aligned.  Every group runs on the tensor cores (128-row
+ * tiles).  Same workspace size as moe_expert_ffn.
+ */
+moe_status moe_expert_ffn_fp8(const moe_shape *shape, const void *x_perm,
+                              const int32_t *offsets, const moe_fp8_experts *w,
+                              void *y_perm, void *workspace, size_t ws_bytes,
+                              void *stream);
+
+/*
+ * moe_forward with 8-bit expert weights (routed and shared): *w is a HOST
+ * struct of device pointers; the ws_* / ss_* members must be non-NULL iff
+ * shape->inter_shared > 0.  w_g stays bf16.  shape->dtype must be MOE_BF16
+ * and d, inter, inter_shared multiples of 128 (else MOE_ERR_UNSUPPORTED).
+ * Same workspace size as moe_forward; graph-capturable like moe_forward.
+ */
+moe_status moe_forward_fp8(const moe_shape *shape, const void *x, const void *w_g,
+                           const float *bias, const moe_fp8_experts *w, void *y,
+                           void *workspace, size_t ws_bytes, void *stream);
+
+/*
  * Reads the device error word of `workspace` (a device pointer passed to a
  * previous call) into *code_out (a HOST pointer): MOE_OK, MOE_ERR_TIMEOUT or
  * MOE_ERR_BOUNDS.  Synchronous (a 4-byte device-to-host copy); call it after

@@ -20,6 +20,14 @@ Workloads (shapes and distributions; names by what they are):
   dsv3_sweep_T{n}     dsv3_decode shapes at T = n, n in {1, 8, 64, 512, 4096}.
   dsv3_decode_sigmoid dsv3_decode with the DeepSeek-V3 router (sigmoid affinities,
                       weights a / (sum a + 1e-6)).
+  dsv3_decode_fp8     dsv3_decode with 8-bit expert weights (routed and shared):
+  mixtral_prefill_fp8 mixtral_prefill likewise.  Each weight is an E4M3 code drawn
+                      as random bits -- sign uniform, exponent field uniform in
+                      9..15, mantissa uniform, the NaN pattern S.1111.111 redrawn
+                      as S.1111.110 -- so magnitudes are log-uniform over [4, 448]
+                      with an RMS of about 162; each weight row has its own fp32
+                      scale std / 162 * U(0.8, 1.2), std being the bf16 workload's
+                      weight std.  The router weights stay bf16.
 
 Every tensor has its own sub-seed, splitmix64(seed ^ fnv1a64(name)), so adding
 or resizing one tensor never changes another.  Large weights are drawn one
@@ -55,6 +63,7 @@ class LayerConfig:
     down_std: str = "d"   # "d": w_down ~ N(0,1/d); "inter": N(0,1/I)
     zipf_bias: bool = False
     router: str = "softmax"   # "softmax" or "sigmoid" (DeepSeek-V3 affinities)
+    weights: str = "act"      # "act": experts in dtype; "e4m3": 8-bit codes + row scales
     seed: int = 0
     extra: dict = field(default_factory=dict, compare=False)
 
@@ -73,6 +82,11 @@ CONFIGS: dict[str, LayerConfig] = {
 # DeepSeek-V3 decode with its own router: sigmoid affinities, weights a / (sum a + 1e-6)
 CONFIGS["dsv3_decode_sigmoid"] = LayerConfig("dsv3_decode_sigmoid", T=8, d=7168, E=256, K=8,
                                              I=2048, Is=2048, router="sigmoid")
+# 8-bit expert weights (E4M3 codes, one fp32 scale per weight row)
+CONFIGS["dsv3_decode_fp8"] = replace(CONFIGS["dsv3_decode"], name="dsv3_decode_fp8",
+                                     weights="e4m3")
+CONFIGS["mixtral_prefill_fp8"] = replace(CONFIGS["mixtral_prefill"], name="mixtral_prefill_fp8",
+                                         weights="e4m3")
 SWEEP_T = (1, 8, 64, 512, 4096)
 for _t in SWEEP_T:
     CONFIGS[f"dsv3_sweep_T{_t}"] = LayerConfig(f"dsv3_sweep_T{_t}", T=_t, d=7168, E=256, K=8,
@@ -133,9 +147,43 @@ def zipf_bias(E: int, seed: int, s: float = ZIPF_S, beta: float = ZIPF_BETA) -> 
     return (-s * beta * torch.log(r)).to(torch.float32)
 
 
+E4M3_RMS = 162.0  # RMS of the code values drawn by e4m3_codes (162.13)
+
+
+def e4m3_codes(shape, device, seed: int, name: str, chunk_dim0: bool = False) -> torch.Tensor:
+    """Random E4M3 bit patterns (uint8): sign uniform, exponent field uniform in
+    9..15, mantissa uniform, NaN (S.1111.111) replaced by S.1111.110."""
+    g = _gen(device, seed, name)
+    out = torch.empty(shape, dtype=torch.uint8, device=device)
+
+    def draw(sh):
+        e = torch.randint(9, 16, sh, generator=g, device=device, dtype=torch.int32)
+        m = torch.randint(0, 8, sh, generator=g, device=device, dtype=torch.int32)
+        sg = torch.randint(0, 2, sh, generator=g, device=device, dtype=torch.int32)
+        m = torch.where((e == 15) & (m == 7), torch.full_like(m, 6), m)
+        return (sg * 128 + e * 8 + m).to(torch.uint8)
+
+    if chunk_dim0:
+        for i in range(shape[0]):
+            out[i].copy_(draw(tuple(shape[1:])))
+    else:
+        out.copy_(draw(tuple(shape)))
+    return out
+
+
+def row_scales(shape, std: float, device, seed: int, name: str) -> torch.Tensor:
+    """One fp32 scale per weight row: std / E4M3_RMS * U(0.8, 1.2)."""
+    g = _gen(device, seed, name)
+    u = torch.rand(shape, generator=g, device=device, dtype=torch.float32)
+    return (u * 0.4 + 0.8) * (std / E4M3_RMS)
+
+
 def make_weights(cfg: LayerConfig, device="cpu", only=None) -> dict:
     """Router, routed-expert and shared-expert weights, stored [out][in].
 
+    For cfg.weights == "e4m3" the expert matrices are uint8 E4M3 codes and the
+    dict also holds their row scales: s_gate, s_up [E][I], s_down [E][d] (ss_*
+    for the shared expert); w_g stays in cfg.dtype.
     ``only`` (a set of names) draws just those tensors; each has its own
     sub-seed, so the values are the same as in a full draw."""
     d, E, I, Is, dt, sd = cfg.d, cfg.E, cfg.I, cfg.Is, cfg.dtype, cfg.seed
@@ -152,6 +200,19 @@ def make_weights(cfg: LayerConfig, device="cpu", only=None) -> dict:
         recipe["ws_gate"] = ((Is, d), std_d, False)
         recipe["ws_up"] = ((Is, d), std_d, False)
         recipe["ws_down"] = ((d, Is), std_sdown, False)
+    if cfg.weights == "e4m3":
+        out = {}
+        for name, (shape, std, chunk) in recipe.items():
+            sname = "s" + name[1:] if name.startswith("w_") else "ss" + name[2:]
+            if name == "w_g":
+                if only is None or name in only:
+                    out[name] = normal(shape, std, dt, device, sd, name)
+                continue
+            if only is None or name in only:
+                out[name] = e4m3_codes(shape, device, sd, name, chunk_dim0=chunk)
+            if only is None or sname in only:
+                out[sname] = row_scales(shape[:-1], std, device, sd, sname)
+        return out
     return {name: normal(shape, std, dt, device, sd, name, chunk_dim0=chunk)
             for name, (shape, std, chunk) in recipe.items() if only is None or name in only}
 

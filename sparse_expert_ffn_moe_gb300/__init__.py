@@ -24,6 +24,7 @@ MOE_ROUTER_SOFTMAX, MOE_ROUTER_SIGMOID = 0, 1
 
 EXPORTED = ("moe_status_string", "moe_workspace_bytes", "moe_route", "moe_permute",
             "moe_permute_noalloc", "moe_expert_ffn", "moe_combine", "moe_forward",
+            "moe_quantize_fp8_rows", "moe_expert_ffn_fp8", "moe_forward_fp8",
             "moe_get_device_error")
 
 
@@ -38,6 +39,13 @@ class moe_shape(ctypes.Structure):
                 ("K", ctypes.c_int32), ("inter", ctypes.c_int32),
                 ("inter_shared", ctypes.c_int32), ("dtype", ctypes.c_int32),
                 ("router", ctypes.c_int32)]
+
+
+class moe_fp8_experts(ctypes.Structure):
+    """E4M3 expert weight codes (uint8) and fp32 row scales: device pointers."""
+    _fields_ = [(n, ctypes.c_void_p) for n in (
+        "w_gate", "w_up", "w_down", "s_gate", "s_up", "s_down",
+        "ws_gate", "ws_up", "ws_down", "ss_gate", "ss_up", "ss_down")]
 
 
 def _load_lib() -> ctypes.CDLL:
@@ -58,9 +66,14 @@ def _load_lib() -> ctypes.CDLL:
     lib.moe_expert_ffn.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.moe_combine.argtypes = [sp, vp, vp, vp, vp, vp, vp]
     lib.moe_forward.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    fp = ctypes.POINTER(moe_fp8_experts)
+    lib.moe_quantize_fp8_rows.argtypes = [ctypes.c_int64, ctypes.c_int64, i32, vp, vp, vp, vp]
+    lib.moe_expert_ffn_fp8.argtypes = [sp, vp, vp, fp, vp, vp, sz, vp]
+    lib.moe_forward_fp8.argtypes = [sp, vp, vp, vp, fp, vp, vp, sz, vp]
     lib.moe_get_device_error.argtypes = [vp, ctypes.POINTER(i32)]
     for f in ("moe_route", "moe_permute", "moe_permute_noalloc", "moe_expert_ffn", "moe_combine",
-              "moe_forward", "moe_get_device_error"):
+              "moe_forward", "moe_quantize_fp8_rows", "moe_expert_ffn_fp8", "moe_forward_fp8",
+              "moe_get_device_error"):
         getattr(lib, f).restype = i32
     return lib
 
@@ -169,6 +182,36 @@ def moe_forward(shape, x, w_g, bias, w_gate, w_up, w_down, ws_gate, ws_up, ws_do
     _check(_lib.moe_forward(ctypes.byref(shape), _p(x), _p(w_g), _p(bias), _p(w_gate), _p(w_up),
                             _p(w_down), _p(ws_gate), _p(ws_up), _p(ws_down), _p(y), ws, nws,
                             _stream(stream)), "moe_forward")
+
+
+def moe_quantize_fp8_rows(w, codes, scales, stream=None):
+    """Per-row E4M3 quantisation of the last dimension of w (bf16 or fp32):
+    codes (uint8, w's shape) and scales (fp32, w's leading shape)."""
+    dtype = {torch.bfloat16: MOE_BF16, torch.float32: MOE_F32}[w.dtype]
+    cols = w.shape[-1]
+    rows = w.numel() // cols if cols else 0
+    _check(_lib.moe_quantize_fp8_rows(rows, cols, dtype, _p(w), _p(codes), _p(scales),
+                                      _stream(stream)), "moe_quantize_fp8_rows")
+
+
+def make_fp8_experts(q: dict) -> moe_fp8_experts:
+    """A moe_fp8_experts from a dict of device tensors (w_gate, w_up, w_down codes,
+    s_gate, s_up, s_down scales; ws_* / ss_* for the shared expert, optional).
+    The caller keeps the tensors alive while the struct is in use."""
+    return moe_fp8_experts(*[_p(q.get(n)) for n, _ in moe_fp8_experts._fields_])
+
+
+def moe_expert_ffn_fp8(shape, x_perm, offsets, w: moe_fp8_experts, y_perm, workspace,
+                       stream=None):
+    ws, nws = _ws(workspace)
+    _check(_lib.moe_expert_ffn_fp8(ctypes.byref(shape), _p(x_perm), _p(offsets), ctypes.byref(w),
+                                   _p(y_perm), ws, nws, _stream(stream)), "moe_expert_ffn_fp8")
+
+
+def moe_forward_fp8(shape, x, w_g, bias, w: moe_fp8_experts, y, workspace, stream=None):
+    ws, nws = _ws(workspace)
+    _check(_lib.moe_forward_fp8(ctypes.byref(shape), _p(x), _p(w_g), _p(bias), ctypes.byref(w),
+                                _p(y), ws, nws, _stream(stream)), "moe_forward_fp8")
 
 
 def moe_get_device_error(workspace) -> int:

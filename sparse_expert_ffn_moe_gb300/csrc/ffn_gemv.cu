@@ -339,11 +339,14 @@ int gemv_max_rows() {
 }
 
 cudaError_t launch_ffn_plan(const FfnGroups& g, int dtype, FfnPlanHeader* hdr, int32_t* gemv_list,
-                            int4* mtile_list, int max_mtiles, int gemv_limit, cudaStream_t st) {
+                            int4* mtile_list, int max_mtiles, int gemv_limit, bool allow_pair,
+                            cudaStream_t st) {
     // fp32 layers never use the tensor cores (no TF32): every group streams
     const int limit = dtype == MOE_F32 ? 0x7fffffff : gemv_limit;
+    // a pair threshold no group can reach keeps every group on single tiles
+    const int pair_min = allow_pair ? tc_pair_min_rows() : 0x7fffffff;
     ffn_plan_kernel<<<1, 1024, 0, st>>>(g.offsets, g.E, g.has_shared, g.T, limit, tc_tile_rows(false),
-                                        tc_pair_min_rows(), tc_tile_rows(true), hdr, gemv_list,
+                                        pair_min, tc_tile_rows(true), hdr, gemv_list,
                                         mtile_list, max_mtiles);
     return cudaGetLastError();
 }

@@ -50,6 +50,8 @@
 // MMAs are drained with bounded waits, tensor memory is freed (a pair always
 // reaches the collective free) and the kernel returns.
 #include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <stdio.h>
 #include <stdlib.h>
 
@@ -85,6 +87,19 @@ template <bool PAIR> struct Shape {
 
 enum Epi { EPI_SWIGLU = 0, EPI_STORE_BF16 = 1, EPI_STORE_F32 = 2 };
 
+// 8-bit weights (W8, single-SM tiles only).  TMA streams E4M3 weight tiles of
+// 256 rows x 128 codes (32 KB, two 64-deep K steps) into a 4-stage raw ring;
+// four converter warps widen each K step to bf16 (exact: every E4M3 value is
+// a bf16 value) into a 2-stage ring of 48 KB MMA stages, whose activation
+// tile the first converter warp requests by TMA.  The per-row weight scale
+// factors out of the K sum and is applied in the epilogue.
+constexpr int kW8ConvStages = 2;
+constexpr int kW8RawStages = 4;
+constexpr uint32_t kW8RawBytes = 256 * 128;  // 32 KB
+constexpr int kThreadsW8 = 320;              // + warps 6..9: converters
+constexpr uint32_t kW8RingBytes =
+    kW8ConvStages * (kABytes + Shape<false>::kBBytes) + kW8RawStages * kW8RawBytes;  // 224 KB
+
 // Activation maps come in four box heights; a CTA loads the smallest box that
 // covers its valid rows.  The MMA still reads all 128 rows of the stage: rows
 // past the box hold stale data that only reach accumulator rows which are
@@ -113,6 +128,11 @@ struct TcParams {
     CUtensorMap b1[2];          // up weights (SWIGLU only), box 128 rows
     CUtensorMap bw[2];          // weights, box 256 rows (single tiles, non-SWIGLU)
     CUtensorMap ag;             // x with a one-row box, for tile::gather4 of routed rows
+    CUtensorMap q0[2];          // W8: E4M3 gate / down codes, box 128 rows x 128 codes
+    CUtensorMap q1[2];          // W8: E4M3 up codes (SWIGLU only)
+    CUtensorMap qw[2];          // W8: E4M3 codes, box 256 rows x 128 codes (non-SWIGLU)
+    const float* sc0[2];        // W8: scale of each gate / down weight row
+    const float* sc1[2];        // W8: scale of each up weight row
     const int32_t* row_src;     // token of each routed row (gather from x), or null
     int gather_max;             // gather a CTA's routed rows when it has at most this many
     const FfnPlanHeader* hdr;
@@ -180,6 +200,9 @@ struct SmemCtl {
     uint64_t tfull[2];           // accumulator a is ready (each CTA)
     uint64_t tempty[2];          // the epilogue warps drained accumulator a (a pair: even CTA, 8 warps)
     uint64_t drain;
+    uint64_t afull[kW8ConvStages];   // W8: the activation tile of MMA stage s landed
+    uint64_t rfull[kW8RawStages];    // W8: raw code tile r landed
+    uint64_t rempty[kW8RawStages];   // W8: the 4 converter warps are done with raw tile r
     uint32_t tmem_base;
     volatile int abort_flag;
 };
@@ -213,15 +236,65 @@ __device__ __forceinline__ void cta_sync_all() {
     }
 }
 
-template <int EPI, bool PAIR>
-__global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
+// two E4M3 codes (low byte first) -> two bf16 (low half first); exact
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two) {
+    const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two & 0xFFFFu), __NV_E4M3);
+    const float2 f = __half22float2(__half2(hr));
+    const __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
+    return *reinterpret_cast<const uint32_t*>(&b);
+}
+
+// W8 converter warp cw (0..3): rows 64*cw .. 64*cw+63 of K half h (codes
+// 64h .. 64h+63 of each 128-code row) of a raw tile -> the bf16 weight tile of
+// an MMA stage.  Both tiles use the 128-byte swizzle (16-byte chunk c of row r
+// at chunk c ^ (r & 7)); lane (r % 8, q) reads code chunk 4h+q of row r and
+// writes bf16 chunks 2q and 2q+1, so every shared-memory access of a warp
+// spreads evenly over the banks.
+__device__ __forceinline__ void convert_rows_w8(const uint8_t* raw, uint8_t* dst, int h, int cw,
+                                                int lane) {
+    const int q = lane & 3, rsub = lane >> 2;
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+        const int r = cw * 64 + it * 8 + rsub;
+        const int x = r & 7;
+        const uint4 v = *reinterpret_cast<const uint4*>(raw + r * 128 + (((h * 4 + q) ^ x) << 4));
+        uint4 lo, hi;
+        lo.x = e4m3x2_to_bf16x2(v.x);
+        lo.y = e4m3x2_to_bf16x2(v.x >> 16);
+        lo.z = e4m3x2_to_bf16x2(v.y);
+        lo.w = e4m3x2_to_bf16x2(v.y >> 16);
+        hi.x = e4m3x2_to_bf16x2(v.z);
+        hi.y = e4m3x2_to_bf16x2(v.z >> 16);
+        hi.z = e4m3x2_to_bf16x2(v.w);
+        hi.w = e4m3x2_to_bf16x2(v.w >> 16);
+        *reinterpret_cast<uint4*>(dst + r * 128 + (((2 * q) ^ x) << 4)) = lo;
+        *reinterpret_cast<uint4*>(dst + r * 128 + (((2 * q + 1) ^ x) << 4)) = hi;
+    }
+}
+
+// 16 consecutive row scales (64-byte aligned), the same for every lane
+__device__ __forceinline__ void ld_scale16(const float* src, float (&s)[16]) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float4 v = __ldg(reinterpret_cast<const float4*>(src) + k);
+        s[4 * k] = v.x; s[4 * k + 1] = v.y; s[4 * k + 2] = v.z; s[4 * k + 3] = v.w;
+    }
+}
+
+template <int EPI, bool PAIR, bool W8 = false>
+__global__ void __launch_bounds__(W8 ? kThreadsW8 : kThreadsTc, 1)
+tc_gemm_kernel(const __grid_constant__ TcParams p) {
+    static_assert(!(W8 && PAIR), "8-bit weights run on single-SM tiles");
+    static_assert(!(W8 && EPI == EPI_STORE_F32), "8-bit weights feed the expert GEMMs only");
     using S = Shape<PAIR>;
+    constexpr int kStages = W8 ? kW8ConvStages : S::kStages;  // MMA stages
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte alignment for the 128-byte-swizzle atoms (the same offset in both CTAs of a pair)
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t* sA = smem;
-    uint8_t* sB = smem + S::kStages * kABytes;
-    SmemCtl* ctl = (SmemCtl*)(smem + kRingBytes);
+    uint8_t* sB = smem + kStages * kABytes;
+    uint8_t* sRaw = smem + kStages * (kABytes + S::kBBytes);  // W8 only
+    SmemCtl* ctl = (SmemCtl*)(smem + (W8 ? kW8RingBytes : kRingBytes));
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = PAIR ? ptx::cluster_ctarank() : 0u;  // 0 issues the MMAs
@@ -233,9 +306,17 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
     const int n_tiles = list_len * p.NB;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < S::kStages; ++s) {
-            ptx::mbar_init(&ctl->full[s], 1);
+        for (int s = 0; s < kStages; ++s) {
+            // W8: full = the 4 converter warps wrote the bf16 weight tile
+            ptx::mbar_init(&ctl->full[s], W8 ? 4 : 1);
             ptx::mbar_init(&ctl->empty[s], 1);
+        }
+        if constexpr (W8) {
+            for (int s = 0; s < kW8ConvStages; ++s) ptx::mbar_init(&ctl->afull[s], 1);
+            for (int r = 0; r < kW8RawStages; ++r) {
+                ptx::mbar_init(&ctl->rfull[r], 1);
+                ptx::mbar_init(&ctl->rempty[r], 4);
+            }
         }
         for (int a = 0; a < 2; ++a) {
             ptx::mbar_init(&ctl->tfull[a], 1);
@@ -250,7 +331,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
         if (p.row_src) ptx::prefetch_tmap(&p.ag);
         for (int k = 0; k < 2; ++k) {
             for (int b = 0; b < kABoxes; ++b) ptx::prefetch_tmap(&p.a[k][b]);
-            if (PAIR || EPI == EPI_SWIGLU) {
+            if (W8) {
+                if (EPI == EPI_SWIGLU) {
+                    ptx::prefetch_tmap(&p.q0[k]);
+                    ptx::prefetch_tmap(&p.q1[k]);
+                } else {
+                    ptx::prefetch_tmap(&p.qw[k]);
+                }
+            } else if (PAIR || EPI == EPI_SWIGLU) {
                 ptx::prefetch_tmap(&p.b0[k]);
                 if (EPI == EPI_SWIGLU) ptx::prefetch_tmap(&p.b1[k]);
             } else {
@@ -279,7 +367,49 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
         // tile::gather4 (the row -> token map of the dispatch gives the rows):
         // lane l loads rows 4l..4l+3 of this CTA's block, so one stage takes up
         // to 32 gather instructions issued in parallel.
-        {
+        if constexpr (W8) {
+            // W8: lane 0 streams the raw code tiles, two K steps per tile
+            if (lane == 0) {
+                int rs = 0;
+                uint32_t rph = 0;
+                bool issued[kW8RawStages];
+                uint32_t issued_phase[kW8RawStages];
+                for (int r = 0; r < kW8RawStages; ++r) { issued[r] = false; issued_phase[r] = 0; }
+                bool ok = p.test_stall == 0;
+                for (int t = unit; t < n_tiles && ok; t += n_units) {
+                    const Tile tl = decode_tile<EPI, PAIR>(p, list_len, t);
+                    if (!tl.valid) continue;
+                    const int nraw = (tl.kblocks + 1) / 2;
+                    for (int kr = 0; kr < nraw; ++kr) {
+                        if (!wait_bounded(&ctl->rempty[rs], rph ^ 1u, ctl, p, 110)) { ok = false; break; }
+                        uint8_t* dst = sRaw + rs * kW8RawBytes;
+                        // a box past the end of K or of the weight rows is zero-filled
+                        // and still counts its full size
+                        ptx::mbar_arrive_expect_tx(&ctl->rfull[rs], kW8RawBytes);
+                        if (EPI == EPI_SWIGLU) {
+                            ptx::tma_load_2d(dst, &p.q0[tl.kind], &ctl->rfull[rs], kr * 128, tl.wrow0);
+                            ptx::tma_load_2d(dst + kW8RawBytes / 2, &p.q1[tl.kind], &ctl->rfull[rs],
+                                             kr * 128, tl.wrow0);
+                        } else {
+                            ptx::tma_load_2d(dst, &p.qw[tl.kind], &ctl->rfull[rs], kr * 128, tl.wrow0);
+                        }
+                        issued[rs] = true;
+                        issued_phase[rs] = rph;
+                        if (++rs == kW8RawStages) { rs = 0; rph ^= 1u; }
+                    }
+                }
+                if (!ok || ctl->abort_flag) {
+                    // every raw copy issued lands before teardown
+                    for (int r = 0; r < kW8RawStages; ++r) {
+                        if (!issued[r]) continue;
+                        const uint64_t t0 = ptx::globaltimer_ns();
+                        while (!ptx::mbar_try_wait(&ctl->rfull[r], issued_phase[r]) &&
+                               ptx::globaltimer_ns() - t0 < p.timeout_ns) {
+                        }
+                    }
+                }
+            }
+        } else {
             int stage = 0;
             uint32_t phase = 0;
             uint32_t issued_phase[kMaxStages];
@@ -420,6 +550,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
                 const uint32_t d_tmem = tmem + (uint32_t)(acc * BN);
                 for (int kb = 0; kb < tl.kblocks; ++kb) {
                     if (!wait_bounded(&ctl->full[stage], phase, ctl, p, 201)) { ok = false; break; }
+                    if (W8 && !wait_bounded(&ctl->afull[stage], phase, ctl, p, 202)) { ok = false; break; }
                     ptx::tc_fence_after();
                     const uint32_t a_base = ptx::smem_u32(sA + stage * kABytes);
                     const uint32_t b_base = ptx::smem_u32(sB + stage * S::kBBytes);
@@ -434,7 +565,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
                     any = true;
                     if constexpr (PAIR) ptx::tc_commit_pair(&ctl->empty[stage], 0x3);
                     else ptx::tc_commit(&ctl->empty[stage]);
-                    if (++stage == S::kStages) { stage = 0; phase ^= 1u; }
+                    if (++stage == kStages) { stage = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
                 if constexpr (PAIR) ptx::tc_commit_pair(&ctl->tfull[acc], 0x3);
@@ -451,7 +582,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
                 }
             }
         }
-    } else {
+    } else if (!W8 || warp < 6) {
         // ------------------------------------------------ epilogue (warps 2..5)
         const int quad = warp & 3;       // TMEM lanes 32*quad .. 32*quad+31
         const int r = quad * 32 + lane;  // accumulator row owned by this thread
@@ -479,11 +610,21 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
                     ptx::tmem_ld16(tbase + BN / 2 + c, u);
                     ptx::tmem_ld_wait();
                     if (row_ok && tl.n0 + c < nvalid) {
+                        float gs[16], us[16];
+                        if constexpr (W8) {
+                            ld_scale16(p.sc0[tl.kind] + tl.wrow0 + c, gs);
+                            ld_scale16(p.sc1[tl.kind] + tl.wrow0 + c, us);
+                        } else {
+#pragma unroll
+                            for (int k = 0; k < 16; ++k) { gs[k] = 1.0f; us[k] = 1.0f; }
+                        }
                         uint32_t w[8];
 #pragma unroll
                         for (int k = 0; k < 8; ++k) {
-                            const float h0 = silu_mul(__uint_as_float(g[2 * k]), __uint_as_float(u[2 * k]));
-                            const float h1 = silu_mul(__uint_as_float(g[2 * k + 1]), __uint_as_float(u[2 * k + 1]));
+                            const float h0 = silu_mul(__uint_as_float(g[2 * k]) * gs[2 * k],
+                                                      __uint_as_float(u[2 * k]) * us[2 * k]);
+                            const float h1 = silu_mul(__uint_as_float(g[2 * k + 1]) * gs[2 * k + 1],
+                                                      __uint_as_float(u[2 * k + 1]) * us[2 * k + 1]);
                             const __nv_bfloat162 b2 = __floats2bfloat162_rn(h0, h1);
                             w[k] = *reinterpret_cast<const uint32_t*>(&b2);
                         }
@@ -500,11 +641,18 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
                     ptx::tmem_ld16(tbase + c, v);
                     ptx::tmem_ld_wait();
                     if (row_ok && tl.n0 + c < nvalid) {
+                        float ds[16];
+                        if constexpr (W8) {
+                            ld_scale16(p.sc0[tl.kind] + tl.wrow0 + c, ds);
+                        } else {
+#pragma unroll
+                            for (int k = 0; k < 16; ++k) ds[k] = 1.0f;
+                        }
                         uint32_t w[8];
 #pragma unroll
                         for (int k = 0; k < 8; ++k) {
-                            const __nv_bfloat162 b2 =
-                                __floats2bfloat162_rn(__uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1]));
+                            const __nv_bfloat162 b2 = __floats2bfloat162_rn(
+                                __uint_as_float(v[2 * k]) * ds[2 * k], __uint_as_float(v[2 * k + 1]) * ds[2 * k + 1]);
                             w[k] = *reinterpret_cast<const uint32_t*>(&b2);
                         }
                         uint4* dst = reinterpret_cast<uint4*>(out + c);
@@ -533,6 +681,63 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_gemm_kernel(const __grid_con
                 else ptx::mbar_arrive(&ctl->tempty[acc]);
             }
             if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        }
+    } else {
+        if constexpr (W8) {
+            // -------------------------------------------- W8 converters (warps 6..9)
+            // Per K step: wait for the raw tile (first half) and a free MMA
+            // stage; warp 6 requests the activation tile; every warp widens its
+            // 64 weight rows to bf16, makes the writes visible to the tensor
+            // core (async proxy) and arrives on full; after the second half
+            // the raw tile is released.
+            const int cw = warp - 6;
+            int rs = 0, cs = 0;
+            uint32_t rph = 0, cph = 0;
+            bool a_issued[kW8ConvStages];
+            uint32_t a_phase[kW8ConvStages];
+            for (int i = 0; i < kW8ConvStages; ++i) { a_issued[i] = false; a_phase[i] = 0; }
+            bool ok = true;
+            for (int t = unit; t < n_tiles && ok; t += n_units) {
+                const Tile tl = decode_tile<EPI, PAIR>(p, list_len, t);
+                if (!tl.valid) continue;
+                const int rows_me = min(BMC, tl.rows);
+                const CUtensorMap* ma = &p.a[tl.kind][abox_for(rows_me)];
+                const uint32_t abytes = abytes_for(rows_me);
+                for (int kb = 0; kb < tl.kblocks; ++kb) {
+                    const int h = kb & 1;
+                    if (h == 0) {
+                        const int okr = lane == 0 ? (int)wait_bounded(&ctl->rfull[rs], rph, ctl, p, 400) : 0;
+                        if (!__shfl_sync(0xffffffffu, okr, 0)) { ok = false; break; }
+                    }
+                    const int oke = lane == 0 ? (int)wait_bounded(&ctl->empty[cs], cph ^ 1u, ctl, p, 401) : 0;
+                    if (!__shfl_sync(0xffffffffu, oke, 0)) { ok = false; break; }
+                    if (cw == 0 && lane == 0) {
+                        ptx::mbar_arrive_expect_tx(&ctl->afull[cs], abytes);
+                        ptx::tma_load_2d(sA + cs * kABytes, ma, &ctl->afull[cs], kb * BK, tl.row0);
+                        a_issued[cs] = true;
+                        a_phase[cs] = cph;
+                    }
+                    convert_rows_w8(sRaw + rs * kW8RawBytes, sB + cs * S::kBBytes, h, cw, lane);
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(&ctl->full[cs]);
+                    if (++cs == kW8ConvStages) { cs = 0; cph ^= 1u; }
+                    if (h == 1 || kb == tl.kblocks - 1) {
+                        if (lane == 0) ptx::mbar_arrive(&ctl->rempty[rs]);
+                        if (++rs == kW8RawStages) { rs = 0; rph ^= 1u; }
+                    }
+                }
+            }
+            if ((!ok || ctl->abort_flag) && cw == 0 && lane == 0) {
+                // every activation copy issued lands before teardown
+                for (int i = 0; i < kW8ConvStages; ++i) {
+                    if (!a_issued[i]) continue;
+                    const uint64_t t0 = ptx::globaltimer_ns();
+                    while (!ptx::mbar_try_wait(&ctl->afull[i], a_phase[i]) &&
+                           ptx::globaltimer_ns() - t0 < p.timeout_ns) {
+                    }
+                }
+            }
         }
     }
 
@@ -586,6 +791,23 @@ bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int 
     return r == CUDA_SUCCESS;
 }
 
+// 2-D map over a row-major [rows][cols] matrix of E4M3 codes, box = 128 codes
+// x box_rows rows, 128-byte swizzle (cols a multiple of 128).
+bool make_map_u8(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    if (rows <= 0) rows = 1;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)cols};
+    const cuuint32_t box[2] = {128u, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // the four activation maps of one matrix (box heights 16, 32, 64, 128 rows)
 bool make_amaps(CUtensorMap (&m)[kABoxes], const void* base, int64_t rows, int64_t cols) {
     bool ok = true;
@@ -614,11 +836,14 @@ int test_stall() {
 }
 
 constexpr size_t kSmemBytes = 1024 + kRingBytes + sizeof(SmemCtl) + 64;
+constexpr size_t kSmemBytesW8 = 1024 + kW8RingBytes + sizeof(SmemCtl) + 64;
+static_assert(kSmemBytesW8 <= 232448, "W8 shared memory exceeds the per-CTA limit");
 
-template <int EPI, bool PAIR>
+template <int EPI, bool PAIR, bool W8 = false>
 cudaError_t launch_tc(const TcParams& p, cudaStream_t st) {
-    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<EPI, PAIR>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    constexpr size_t smem = W8 ? kSmemBytesW8 : kSmemBytes;
+    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<EPI, PAIR, W8>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int sms = device_sm_count();
     int units = PAIR ? sms / 2 : sms;
@@ -643,7 +868,7 @@ cudaError_t launch_tc(const TcParams& p, cudaStream_t st) {
         e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel<EPI, PAIR>, p);
         if (e != cudaSuccess) return e;
     } else {
-        tc_gemm_kernel<EPI, PAIR><<<units, kThreadsTc, kSmemBytes, st>>>(p);
+        tc_gemm_kernel<EPI, PAIR, W8><<<units, W8 ? kThreadsW8 : kThreadsTc, smem, st>>>(p);
     }
     return cudaGetLastError();
 }
@@ -775,6 +1000,89 @@ cudaError_t launch_ffn_tc(const FfnGroups& g, const FfnPlanHeader* hdr, const in
     }
     q.mtiles = single_list;
     return launch_tc<EPI_STORE_BF16, false>(q, st);
+}
+
+// The expert FFN with E4M3 weights: the same two GEMMs on single-SM tiles
+// (every plan entry in the single list), routed rows from the permuted copy.
+cudaError_t launch_ffn_tc_fp8(const FfnGroups& g, const FfnPlanHeader* hdr, const int4* mtile_list,
+                              int max_mtiles, DevError* err, cudaStream_t st) {
+    const int64_t R = g.n_routed_rows;
+    // ---- gate/up: h = SiLU(s_g * (x Q_gate^T)) * (s_u * (x Q_up^T))
+    TcParams p{};
+    bool ok = true;
+    ok &= make_amaps(p.a[0], g.a_perm, R, g.d);
+    p.ag = p.a[0][0];
+    p.row_src = nullptr;
+    p.gather_max = 0;
+    ok &= make_map_u8(&p.q0[0], g.w_gate, (int64_t)g.E * g.I, g.d, 128);
+    ok &= make_map_u8(&p.q1[0], g.w_up, (int64_t)g.E * g.I, g.d, 128);
+    p.sc0[0] = g.s_gate;
+    p.sc1[0] = g.s_up;
+    if (g.has_shared) {
+        ok &= make_amaps(p.a[1], g.a_shared, g.T, g.d);
+        ok &= make_map_u8(&p.q0[1], g.ws_gate, g.Is, g.d, 128);
+        ok &= make_map_u8(&p.q1[1], g.ws_up, g.Is, g.d, 128);
+        p.sc0[1] = g.ss_gate;
+        p.sc1[1] = g.ss_up;
+    } else {
+        for (int b = 0; b < kABoxes; ++b) p.a[1][b] = p.a[0][b];
+        p.q0[1] = p.q0[0]; p.q1[1] = p.q1[0];
+        p.sc0[1] = p.sc0[0]; p.sc1[1] = p.sc1[0];
+    }
+    p.qw[0] = p.q0[0]; p.qw[1] = p.q0[1];  // unused by the SWIGLU epilogue
+    if (!ok) return cudaErrorInvalidValue;
+    p.hdr = hdr;
+    p.mtiles = mtile_list;
+    p.E = g.E;
+    p.max_mtiles = max_mtiles;
+    p.dense_rows = 0;
+    const int max_inter = g.has_shared && g.Is > g.I ? g.Is : g.I;
+    p.NB = (max_inter + BN / 2 - 1) / (BN / 2);
+    p.n_out[0] = g.I; p.n_out[1] = g.has_shared ? g.Is : 0;
+    p.kdim[0] = g.d; p.kdim[1] = g.d;
+    p.wrows[0] = g.I; p.wrows[1] = 0;
+    p.out[0] = g.h; p.out[1] = g.h_s;
+    p.ld_out[0] = g.I; p.ld_out[1] = g.Is;
+    p.err = err;
+    p.timeout_ns = timeout_ns();
+    p.test_stall = test_stall();
+    cudaError_t e = launch_tc<EPI_SWIGLU, false, true>(p, st);
+    if (e != cudaSuccess) return e;
+
+    // ---- down: y = s_d * (h Q_down^T)
+    TcParams q{};
+    ok = true;
+    ok &= make_amaps(q.a[0], g.h, R, g.I);
+    ok &= make_map_u8(&q.qw[0], g.w_down, (int64_t)g.E * g.d, g.I, 256);
+    q.sc0[0] = g.s_down;
+    if (g.has_shared) {
+        ok &= make_amaps(q.a[1], g.h_s, g.T, g.Is);
+        ok &= make_map_u8(&q.qw[1], g.ws_down, g.d, g.Is, 256);
+        q.sc0[1] = g.ss_down;
+    } else {
+        for (int b = 0; b < kABoxes; ++b) q.a[1][b] = q.a[0][b];
+        q.qw[1] = q.qw[0];
+        q.sc0[1] = q.sc0[0];
+    }
+    q.ag = q.a[0][0];
+    q.q0[0] = q.qw[0]; q.q0[1] = q.qw[1]; q.q1[0] = q.qw[0]; q.q1[1] = q.qw[1];
+    q.sc1[0] = q.sc0[0]; q.sc1[1] = q.sc0[1];
+    if (!ok) return cudaErrorInvalidValue;
+    q.hdr = hdr;
+    q.mtiles = mtile_list;
+    q.E = g.E;
+    q.max_mtiles = max_mtiles;
+    q.dense_rows = 0;
+    q.NB = (g.d + BN - 1) / BN;
+    q.n_out[0] = g.d; q.n_out[1] = g.has_shared ? g.d : 0;
+    q.kdim[0] = g.I; q.kdim[1] = g.has_shared ? g.Is : g.I;
+    q.wrows[0] = g.d; q.wrows[1] = 0;
+    q.out[0] = g.y; q.out[1] = g.y_s;
+    q.ld_out[0] = g.d; q.ld_out[1] = g.d;
+    q.err = err;
+    q.timeout_ns = timeout_ns();
+    q.test_stall = test_stall();
+    return launch_tc<EPI_STORE_BF16, false, true>(q, st);
 }
 
 // scores[T][E] (fp32) = x w_g^T on the tensor cores (single tiles)

@@ -44,6 +44,14 @@ struct FfnGroups {
     const void* ws_gate;     // [Is][d]
     const void* ws_up;
     const void* ws_down;     // [d][Is]
+    // 8-bit weights (launch_ffn_tc_fp8 only): the w_* / ws_* pointers above
+    // hold E4M3 codes and these the fp32 scale of each weight row
+    const float* s_gate;     // [E][I]
+    const float* s_up;       // [E][I]
+    const float* s_down;     // [E][d]
+    const float* ss_gate;    // [Is]
+    const float* ss_up;      // [Is]
+    const float* ss_down;    // [d]
     void* h;                 // [n_routed_rows][I]
     void* h_s;               // [T][Is]
     void* y;                 // [n_routed_rows][d]
@@ -76,10 +84,11 @@ cudaError_t launch_gather_rows(const moe_shape& s, const void* x, const int32_t*
 
 // ---- ffn_plan + ffn_gemv.cu ----
 int gemv_max_rows();  // groups with at most this many rows take the GEMV path
-// mtile_list holds 2 * max_mtiles entries: single-SM tiles, then pair tiles.
+// mtile_list holds 2 * max_mtiles entries: single-SM tiles, then pair tiles
+// (none when allow_pair is false).
 cudaError_t launch_ffn_plan(const FfnGroups& g, int dtype, FfnPlanHeader* hdr,
                             int32_t* gemv_list, int4* mtile_list, int max_mtiles,
-                            int gemv_limit, cudaStream_t st);
+                            int gemv_limit, bool allow_pair, cudaStream_t st);
 cudaError_t launch_ffn_gemv(const FfnGroups& g, int dtype, const FfnPlanHeader* hdr,
                             const int32_t* gemv_list, cudaStream_t st);
 
@@ -95,6 +104,14 @@ cudaError_t launch_ffn_tc(const FfnGroups& g, const FfnPlanHeader* hdr, const in
                           int max_mtiles, bool may_pair, DevError* err, cudaStream_t st);
 cudaError_t launch_router_tc(const moe_shape& s, const void* x, const void* w_g, float* scores,
                              DevError* err, cudaStream_t st);
+// E4M3 expert weights with row scales (g.s_* set); bf16 activations; every
+// group on single-SM tiles (the plan must have been built with allow_pair false)
+cudaError_t launch_ffn_tc_fp8(const FfnGroups& g, const FfnPlanHeader* hdr, const int4* mtile_list,
+                              int max_mtiles, DevError* err, cudaStream_t st);
+
+// ---- quant.cu ----
+cudaError_t launch_quantize_fp8_rows(int64_t rows, int64_t cols, int dtype, const void* w,
+                                     uint8_t* codes, float* scales, cudaStream_t st);
 
 // ---- combine.cu ----
 cudaError_t launch_combine(const moe_shape& s, const void* y_perm, const int32_t* inv_perm,

@@ -62,6 +62,26 @@ bool use_tc_router(const moe_shape& s) {
     return s.dtype == MOE_BF16 && s.T >= 128 && s.E >= 64;
 }
 
+// 8-bit weights: bf16 activations, K extents that whole 128-code boxes tile
+moe_status check_fp8_shape(const moe_shape& s) {
+    if (s.dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+    if (s.d % 128 || s.inter % 128 || s.inter_shared % 128) return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+
+// routed code and scale pointers present and aligned; shared ones iff wanted
+moe_status check_fp8_weights(const moe_fp8_experts* w, bool shared) {
+    if (!w) return MOE_ERR_INVALID_ARG;
+    const void* routed[] = {w->w_gate, w->w_up, w->w_down, w->s_gate, w->s_up, w->s_down};
+    for (const void* p : routed)
+        if (!p || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+    if (!shared) return MOE_OK;
+    const void* sh[] = {w->ws_gate, w->ws_up, w->ws_down, w->ss_gate, w->ss_up, w->ss_down};
+    for (const void* p : sh)
+        if (!p || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
+}
+
 }  // namespace
 
 int device_sm_count() {
@@ -245,7 +265,7 @@ moe_status moe_expert_ffn(const moe_shape* shape, const void* x_perm, const int3
     FfnPlanHeader* hdr = at<FfnPlanHeader>(workspace, L.plan);
     int32_t* glist = at<int32_t>(workspace, L.gemv_list);
     int4* mtiles = at<int4>(workspace, L.mtile_list);
-    e = launch_ffn_plan(g, s.dtype, hdr, glist, mtiles, L.max_mtiles, gemv_limit(), cs);
+    e = launch_ffn_plan(g, s.dtype, hdr, glist, mtiles, L.max_mtiles, gemv_limit(), true, cs);
     if (e == cudaSuccess && gemv_possible(s)) e = launch_ffn_gemv(g, s.dtype, hdr, glist, cs);
     if (e == cudaSuccess && need_tc)
         e = launch_ffn_tc(g, hdr, mtiles, L.max_mtiles, tc_pair_possible(rows), err, cs);
@@ -353,11 +373,156 @@ moe_status moe_forward(const moe_shape* shape, const void* x, const void* w_g, c
     FfnPlanHeader* hdr = at<FfnPlanHeader>(workspace, L.plan);
     int32_t* glist = at<int32_t>(workspace, L.gemv_list);
     int4* mtiles = at<int4>(workspace, L.mtile_list);
-    e = launch_ffn_plan(g, s.dtype, hdr, glist, mtiles, L.max_mtiles, gemv_limit(), cs);
+    e = launch_ffn_plan(g, s.dtype, hdr, glist, mtiles, L.max_mtiles, gemv_limit(), true, cs);
     if (e == cudaSuccess && gemv_possible(s)) e = launch_ffn_gemv(g, s.dtype, hdr, glist, cs);
     // a group has at most T rows (a token picks an expert once)
     if (e == cudaSuccess && need_tc)
         e = launch_ffn_tc(g, hdr, mtiles, L.max_mtiles, tc_pair_possible(s.T), err, cs);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+
+    // 4. combine
+    return cuda_status(launch_combine(s, g.y, inv, topk_w, shared ? g.y_s : nullptr, y, cs));
+}
+
+moe_status moe_quantize_fp8_rows(int64_t rows, int64_t cols, int32_t dtype, const void* w,
+                                 uint8_t* codes, float* scales, void* stream) {
+    if (rows < 0 || cols <= 0) return MOE_ERR_INVALID_ARG;
+    if (dtype != MOE_F32 && dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+    if (rows >= ((int64_t)1 << 31) || cols % 16) return MOE_ERR_UNSUPPORTED;
+    if (rows == 0) return MOE_OK;
+    if (!w || !codes || !scales || !aligned16(w) || !aligned16(codes)) return MOE_ERR_INVALID_ARG;
+    return cuda_status(launch_quantize_fp8_rows(rows, cols, dtype, w, codes, scales,
+                                                (cudaStream_t)stream));
+}
+
+moe_status moe_expert_ffn_fp8(const moe_shape* shape, const void* x_perm, const int32_t* offsets,
+                              const moe_fp8_experts* w, void* y_perm, void* workspace,
+                              size_t ws_bytes, void* stream) {
+    moe_status st = check_shape(shape);
+    if (st != MOE_OK) return st;
+    const moe_shape& s = *shape;
+    if ((st = check_fp8_shape(s)) != MOE_OK) return st;
+    if (s.T == 0) return MOE_OK;
+    if (!x_perm || !offsets || !y_perm || !aligned16(x_perm) || !aligned16(y_perm))
+        return MOE_ERR_INVALID_ARG;
+    if ((st = check_fp8_weights(w, false)) != MOE_OK) return st;
+    if ((st = check_ws(s, workspace, ws_bytes)) != MOE_OK) return st;
+    if (!tc_available()) return MOE_ERR_UNSUPPORTED;
+    cudaStream_t cs = (cudaStream_t)stream;
+    const WsLayout L = ws_layout(s);
+    DevError* err = at<DevError>(workspace, L.err);
+    cudaError_t e = cudaMemsetAsync(err, 0, sizeof(DevError), cs);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    FfnGroups g{};
+    g.E = s.E;
+    g.has_shared = 0;
+    g.d = s.d;
+    g.I = s.inter;
+    g.Is = 0;
+    g.n_routed_rows = s.T * s.K;
+    g.T = s.T;
+    g.offsets = offsets;
+    g.row_src = nullptr;
+    g.a_routed = x_perm;
+    g.a_perm = x_perm;
+    g.a_shared = x_perm;
+    g.w_gate = w->w_gate;
+    g.w_up = w->w_up;
+    g.w_down = w->w_down;
+    g.s_gate = w->s_gate;
+    g.s_up = w->s_up;
+    g.s_down = w->s_down;
+    g.h = at<void>(workspace, L.h);
+    g.y = y_perm;
+    FfnPlanHeader* hdr = at<FfnPlanHeader>(workspace, L.plan);
+    int4* mtiles = at<int4>(workspace, L.mtile_list);
+    e = launch_ffn_plan(g, s.dtype, hdr, at<int32_t>(workspace, L.gemv_list), mtiles, L.max_mtiles,
+                        0, false, cs);
+    if (e == cudaSuccess) e = launch_ffn_tc_fp8(g, hdr, mtiles, L.max_mtiles, err, cs);
+    return cuda_status(e);
+}
+
+moe_status moe_forward_fp8(const moe_shape* shape, const void* x, const void* w_g, const float* bias,
+                           const moe_fp8_experts* w, void* y, void* workspace, size_t ws_bytes,
+                           void* stream) {
+    moe_status st = check_shape(shape);
+    if (st != MOE_OK) return st;
+    const moe_shape& s = *shape;
+    if ((st = check_fp8_shape(s)) != MOE_OK) return st;
+    const bool shared = s.inter_shared > 0;
+    if (s.T == 0) return MOE_OK;
+    if (!x || !w_g || !y || !aligned16(x) || !aligned16(w_g) || !aligned16(y))
+        return MOE_ERR_INVALID_ARG;
+    if ((st = check_fp8_weights(w, shared)) != MOE_OK) return st;
+    if (!shared && w->ws_gate) return MOE_ERR_INVALID_ARG;
+    if ((st = check_ws(s, workspace, ws_bytes)) != MOE_OK) return st;
+    if (!tc_available()) return MOE_ERR_UNSUPPORTED;
+    cudaStream_t cs = (cudaStream_t)stream;
+    const WsLayout L = ws_layout(s);
+    DevError* err = at<DevError>(workspace, L.err);
+    cudaError_t e = cudaMemsetAsync(err, 0, sizeof(DevError), cs);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+
+    // 1. router (bf16 weights), top-K and weights
+    float* part = at<float>(workspace, L.router_part);
+    int32_t* topk_idx = at<int32_t>(workspace, L.topk_idx);
+    float* topk_w = at<float>(workspace, L.topk_w);
+    int splits = L.router_splits;
+    if (use_tc_router(s)) {
+        e = launch_router_tc(s, x, w_g, part, err, cs);
+        splits = 1;
+    } else {
+        e = launch_router_gemv(s, x, w_g, part, splits, cs);
+    }
+    if (e == cudaSuccess) e = launch_topk_softmax(s, part, splits, bias, nullptr, topk_idx, topk_w, cs);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+
+    // 2. dispatch and the permuted copy of the routed rows
+    int32_t* offsets = at<int32_t>(workspace, L.offsets);
+    int32_t* inv = at<int32_t>(workspace, L.inv_perm);
+    int32_t* tok = at<int32_t>(workspace, L.tok_of);
+    e = launch_dispatch(s, topk_idx, at<int32_t>(workspace, L.counts), offsets,
+                        at<int32_t>(workspace, L.perm), inv, tok, at<int32_t>(workspace, L.blk_hist),
+                        err, cs);
+    void* x_perm = at<void>(workspace, L.x_perm);
+    if (e == cudaSuccess) e = launch_gather_rows(s, x, inv, x_perm, cs);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+
+    // 3. routed and shared experts, 8-bit weights, single-SM tensor-core tiles
+    FfnGroups g{};
+    g.E = s.E;
+    g.has_shared = shared ? 1 : 0;
+    g.d = s.d;
+    g.I = s.inter;
+    g.Is = s.inter_shared;
+    g.n_routed_rows = s.T * s.K;
+    g.T = s.T;
+    g.offsets = offsets;
+    g.row_src = nullptr;
+    g.a_routed = x_perm;
+    g.a_perm = x_perm;
+    g.a_shared = x;
+    g.w_gate = w->w_gate;
+    g.w_up = w->w_up;
+    g.w_down = w->w_down;
+    g.s_gate = w->s_gate;
+    g.s_up = w->s_up;
+    g.s_down = w->s_down;
+    g.ws_gate = w->ws_gate;
+    g.ws_up = w->ws_up;
+    g.ws_down = w->ws_down;
+    g.ss_gate = w->ss_gate;
+    g.ss_up = w->ss_up;
+    g.ss_down = w->ss_down;
+    g.h = at<void>(workspace, L.h);
+    g.h_s = at<void>(workspace, L.h_s);
+    g.y = at<void>(workspace, L.y_perm);
+    g.y_s = at<void>(workspace, L.y_s);
+    FfnPlanHeader* hdr = at<FfnPlanHeader>(workspace, L.plan);
+    int4* mtiles = at<int4>(workspace, L.mtile_list);
+    e = launch_ffn_plan(g, s.dtype, hdr, at<int32_t>(workspace, L.gemv_list), mtiles, L.max_mtiles,
+                        0, false, cs);
+    if (e == cudaSuccess) e = launch_ffn_tc_fp8(g, hdr, mtiles, L.max_mtiles, err, cs);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
 
     // 4. combine

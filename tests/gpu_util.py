@@ -74,6 +74,18 @@ class Layer:
     def bias_host(self):
         return None if self.bias is None else self.bias.double().cpu().numpy()
 
+    def oracle_tokens(self, tokens, x=None):
+        """The oracle's per-token layer for these tokens (either weight format)."""
+        import oracle
+        c = self.cfg
+        xh = host(self.x if x is None else x)
+        if c.weights == "e4m3":
+            return oracle.forward_tokens_fp8(tokens, xh, self.hp["w_g"], self.hp, c.K,
+                                             dtype=c.dtype, bias=self.bias_host(),
+                                             router=c.router)
+        return oracle.forward_tokens(tokens, xh, self.hp, c.K, dtype=c.dtype,
+                                     bias=self.bias_host(), router=c.router)
+
     def shape(self, moe, T=None):
         c = self.cfg
         return moe.make_shape(c.T if T is None else T, c.d, c.E, c.K, c.I, c.Is, c.dtype, c.router)
@@ -84,8 +96,11 @@ class Layer:
         y = torch.empty_like(x)
         ws = moe.alloc_workspace(s) if ws is None else ws
         p = self.p
-        moe.moe_forward(s, x, p["w_g"], self.bias, p["w_gate"], p["w_up"], p["w_down"],
-                        p.get("ws_gate"), p.get("ws_up"), p.get("ws_down"), y, ws)
+        if self.cfg.weights == "e4m3":
+            moe.moe_forward_fp8(s, x, p["w_g"], self.bias, moe.make_fp8_experts(p), y, ws)
+        else:
+            moe.moe_forward(s, x, p["w_g"], self.bias, p["w_gate"], p["w_up"], p["w_down"],
+                            p.get("ws_gate"), p.get("ws_up"), p.get("ws_down"), y, ws)
         torch.cuda.synchronize()
         assert moe.moe_get_device_error(ws) == 0
         return y

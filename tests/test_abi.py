@@ -26,7 +26,7 @@ def moe(lib):
 def _declared_functions():
     text = open(os.path.join(ROOT, "include", "moe.h")).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(moe_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_header_declares_the_stage_entry_points():
@@ -131,3 +131,62 @@ def test_binding_refuses_host_tensors(moe):
     x = torch.zeros(2, 64)
     with pytest.raises(ValueError):
         moe.moe_combine(s, x, x, x, None, x, stream=0)
+
+
+def test_fp8_argument_errors_return_before_any_launch(lib, moe):
+    """The 8-bit entry points refuse bad shapes and pointers on the host."""
+    vp, z = ctypes.c_void_p, ctypes.c_size_t
+    fake = (1 << 20)
+    odd = (1 << 20) + 4
+    for f in ("moe_quantize_fp8_rows", "moe_expert_ffn_fp8", "moe_forward_fp8"):
+        getattr(lib, f).restype = ctypes.c_int32
+    lib.moe_quantize_fp8_rows.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,
+                                          vp, vp, vp, vp]
+    q = lib.moe_quantize_fp8_rows
+    assert q(-1, 64, moe.MOE_BF16, vp(fake), vp(fake), vp(fake), None) == moe.MOE_ERR_INVALID_ARG
+    assert q(4, 0, moe.MOE_BF16, vp(fake), vp(fake), vp(fake), None) == moe.MOE_ERR_INVALID_ARG
+    assert q(4, 64, 5, vp(fake), vp(fake), vp(fake), None) == moe.MOE_ERR_INVALID_ARG
+    assert q(4, 40, moe.MOE_BF16, vp(fake), vp(fake), vp(fake), None) == moe.MOE_ERR_UNSUPPORTED
+    assert q(4, 64, moe.MOE_BF16, None, vp(fake), vp(fake), None) == moe.MOE_ERR_INVALID_ARG
+    assert q(4, 64, moe.MOE_BF16, vp(fake), vp(odd), vp(fake), None) == moe.MOE_ERR_INVALID_ARG
+    assert q(0, 64, moe.MOE_BF16, None, None, None, None) == moe.MOE_OK
+
+    full = {n: fake for n, _ in moe.moe_fp8_experts._fields_}
+    routed = dict(full, ws_gate=None, ws_up=None, ws_down=None, ss_gate=None, ss_up=None,
+                  ss_down=None)
+    W = moe.moe_fp8_experts(*[routed[n] for n, _ in moe.moe_fp8_experts._fields_])
+    s = moe.make_shape(4, 128, 8, 2, 256, 0, "bf16")
+    big = z(1 << 30)
+
+    def fwd(shape, w, **kw):
+        a = dict(x=vp(fake), w_g=vp(fake), y=vp(fake), ws=vp(fake), n=big)
+        a.update(kw)
+        return lib.moe_forward_fp8(ctypes.byref(shape), a["x"], a["w_g"], None,
+                                   ctypes.byref(w) if w is not None else None, a["y"], a["ws"],
+                                   a["n"], None)
+
+    # activations must be bf16; K extents multiples of 128
+    assert fwd(moe.make_shape(4, 128, 8, 2, 256, 0, "f32"), W) == moe.MOE_ERR_UNSUPPORTED
+    assert fwd(moe.make_shape(4, 192, 8, 2, 256, 0, "bf16"), W) == moe.MOE_ERR_UNSUPPORTED
+    assert fwd(moe.make_shape(4, 128, 8, 2, 320, 0, "bf16"), W) == moe.MOE_ERR_UNSUPPORTED
+    assert fwd(moe.make_shape(4, 128, 8, 2, 256, 64, "bf16"), W) == moe.MOE_ERR_UNSUPPORTED
+    # null / misaligned pointers, missing or unwanted shared weights, short workspace
+    assert fwd(s, None) == moe.MOE_ERR_INVALID_ARG
+    assert fwd(s, W, x=None) == moe.MOE_ERR_INVALID_ARG
+    assert fwd(s, W, y=vp(odd)) == moe.MOE_ERR_INVALID_ARG
+    bad = moe.moe_fp8_experts(*[(odd if n == "s_down" else routed[n])
+                                for n, _ in moe.moe_fp8_experts._fields_])
+    assert fwd(s, bad) == moe.MOE_ERR_INVALID_ARG
+    W_full = moe.moe_fp8_experts(*[full[n] for n, _ in moe.moe_fp8_experts._fields_])
+    assert fwd(s, W_full) == moe.MOE_ERR_INVALID_ARG
+    assert fwd(moe.make_shape(4, 128, 8, 2, 256, 128, "bf16"), W) == moe.MOE_ERR_INVALID_ARG
+    assert fwd(s, W, n=z(16)) == moe.MOE_ERR_WORKSPACE
+    assert fwd(moe.make_shape(0, 128, 8, 2, 256, 0, "bf16"), None) == moe.MOE_OK
+
+    e = lib.moe_expert_ffn_fp8
+    assert e(ctypes.byref(s), vp(fake), None, ctypes.byref(W), vp(fake), vp(fake), big,
+             None) == moe.MOE_ERR_INVALID_ARG
+    assert e(ctypes.byref(s), vp(fake), vp(fake), None, vp(fake), vp(fake), big,
+             None) == moe.MOE_ERR_INVALID_ARG
+    assert e(ctypes.byref(s), vp(fake), vp(fake), ctypes.byref(W), vp(fake), vp(fake), z(16),
+             None) == moe.MOE_ERR_WORKSPACE

@@ -1,0 +1,202 @@
+"""8-bit (E4M3) expert weights on the GPU against the oracle.
+
+The row quantiser is integer work decided by fp32 arithmetic that both sides
+do in the same precision (amax / 448 and w / scale as IEEE fp32 divisions,
+round to nearest even): codes and scales must match bit for bit.  The fp8
+expert FFN and the fp8 layer are compared like the bf16 ones (relative L2
+against the fp64 oracle on the same codes and scales)."""
+import numpy as np
+import pytest
+import torch
+from dataclasses import replace
+
+import moe_inputs as mi
+import oracle
+from tests.gpu_util import (BF16_REL_L2, MARGIN, Layer, boundary_margin, host, rel_l2, to_f64)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def moe():
+    import sparse_expert_ffn_moe_gb300 as m
+    return m
+
+
+# ---------------------------------------------------------------- quantiser
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("rows,cols", [(600, 2048), (1, 16), (37, 7168)])
+def test_quantize_rows_bit_exact(moe, dtype, rows, cols):
+    g = torch.Generator().manual_seed(rows * 7 + cols)
+    w = torch.randn(rows, cols, generator=g) * torch.exp2(torch.rand(rows, 1, generator=g) * 16 - 8)
+    if rows > 2:
+        w[1] = 0.0                         # a row of zeros
+        w[2, 3] = -w[2].abs().max() * 3    # a negative extreme
+    w = w.to(mi.torch_dtype(dtype))
+    wd = w.cuda()
+    codes = torch.empty(rows, cols, dtype=torch.uint8, device="cuda")
+    scales = torch.empty(rows, dtype=torch.float32, device="cuda")
+    moe.moe_quantize_fp8_rows(wd, codes, scales)
+    torch.cuda.synchronize()
+    rc, rs = oracle.quantize_fp8_rows(mi.to_host_array(w), dtype)
+    assert np.array_equal(scales.cpu().numpy(), rs)
+    assert np.array_equal(codes.cpu().numpy(), rc)
+
+
+def test_quantize_rows_of_a_3d_weight_stack(moe):
+    cfg = replace(mi.CONFIGS["dsv3_decode"], E=3, I=256)
+    w = mi.make_weights(cfg, "cuda", only={"w_down"})["w_down"]     # [3][7168][256] bf16
+    codes = torch.empty(w.shape, dtype=torch.uint8, device="cuda")
+    scales = torch.empty(w.shape[:-1], dtype=torch.float32, device="cuda")
+    moe.moe_quantize_fp8_rows(w, codes, scales)
+    torch.cuda.synchronize()
+    rc, rs = oracle.quantize_fp8_rows(host(w), "bf16")
+    assert np.array_equal(codes.cpu().numpy(), rc)
+    assert np.array_equal(scales.cpu().numpy(), rs)
+
+
+# ---------------------------------------------------------------- expert FFN
+
+def _expert_ffn_case(moe, counts, d, I, seed=0):
+    E = len(counts)
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    rows = int(offsets[-1])
+    cfg = mi.LayerConfig("fp8_ffn", T=max(rows, 1), d=d, E=E, K=1, I=I, weights="e4m3", seed=seed)
+    q = mi.make_weights(cfg, "cuda", only={"w_gate", "w_up", "w_down", "s_gate", "s_up",
+                                           "s_down"})
+    x_perm = mi.normal((max(rows, 1), d), 1.0, "bf16", "cuda", seed, "x_perm")[:rows]
+    s = moe.make_shape(rows, d, E, 1, I, 0, "bf16")
+    ws = moe.alloc_workspace(s)
+    y = torch.full((rows, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    W = moe.make_fp8_experts(q)
+    moe.moe_expert_ffn_fp8(s, x_perm, torch.from_numpy(offsets).cuda(), W, y, ws)
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_error(ws) == 0
+    qh = {k: host(v) for k, v in q.items()}
+    ref = oracle.expert_ffn_fp8(host(x_perm), offsets, qh, dtype="bf16")
+    return to_f64(y), ref
+
+
+@pytest.mark.parametrize("counts,d,I", [
+    ([75, 0, 140, 3, 1, 260, 77, 44], 256, 384),     # ragged groups, one empty
+    ([600, 257, 1, 129], 384, 640),                  # several m-tiles per group, 5 n-blocks
+    ([1, 2, 1, 1, 3, 1, 1, 2], 1024, 256),           # decode-like: a few rows per expert
+])
+def test_expert_ffn_fp8_matches_oracle(moe, counts, d, I):
+    y, ref = _expert_ffn_case(moe, counts, d, I)
+    assert rel_l2(y, ref) <= BF16_REL_L2
+    for r in range(y.shape[0]):
+        assert rel_l2(y[r], ref[r]) <= 2 * BF16_REL_L2, r
+
+
+# ---------------------------------------------------------------- the layer
+
+def _clean_x(L: Layer):
+    cfg = L.cfg
+    x = L.x
+    for attempt in range(1, 20):
+        _, _, logits = oracle.route(host(x), L.hp["w_g"], cfg.K, dtype=cfg.dtype,
+                                    bias=L.bias_host(), router=cfg.router)
+        bad = np.nonzero(boundary_margin(logits, cfg.K) < MARGIN)[0]
+        if bad.size == 0:
+            return x
+        x = mi.redraw_rows(x, bad, cfg, attempt)
+    raise AssertionError("could not draw well-separated router scores")
+
+
+def _check_rows(y, ref):
+    assert rel_l2(y, ref) <= BF16_REL_L2
+    for r in range(y.shape[0]):
+        assert rel_l2(y[r], ref[r]) <= 2 * BF16_REL_L2, r
+
+
+@pytest.mark.parametrize("router", ["softmax", "sigmoid"])
+def test_forward_fp8_small_layer_all_tokens(moe, router):
+    cfg = mi.LayerConfig("fp8_small", T=45, d=256, E=12, K=3, I=384, Is=256, router=router,
+                         weights="e4m3")
+    L = Layer(cfg)
+    L.x = _clean_x(L)
+    y = to_f64(L.forward(moe))
+    ref = L.oracle_tokens(np.arange(cfg.T))
+    _check_rows(y, ref["y"])
+
+
+def test_forward_fp8_without_shared_expert(moe):
+    cfg = mi.LayerConfig("fp8_noshared", T=300, d=512, E=8, K=2, I=256, weights="e4m3")
+    L = Layer(cfg)
+    L.x = _clean_x(L)
+    y = to_f64(L.forward(moe))
+    ref = L.oracle_tokens(np.arange(cfg.T))
+    _check_rows(y, ref["y"])
+
+
+def test_forward_fp8_decode_full_size(moe):
+    cfg = mi.CONFIGS["dsv3_decode_fp8"]
+    L = Layer(cfg)
+    L.x = _clean_x(L)
+    y = to_f64(L.forward(moe))
+    ref = L.oracle_tokens(np.arange(cfg.T))
+    _check_rows(y, ref["y"])
+
+
+def test_forward_fp8_prefill_sampled_tokens(moe):
+    cfg = mi.CONFIGS["mixtral_prefill_fp8"]
+    L = Layer(cfg)
+    y = L.forward(moe)
+    tokens = mi.sample_tokens(cfg.T, 96, seed=cfg.seed).numpy()
+    ref = L.oracle_tokens(tokens)
+    ok = boundary_margin(ref["logits"], cfg.K) >= MARGIN
+    assert ok.mean() >= 0.9
+    _check_rows(to_f64(y[torch.from_numpy(tokens[ok]).long().cuda()]), ref["y"][ok])
+
+
+def test_forward_fp8_matches_bf16_layer_on_exact_weights(moe):
+    """Power-of-two row scales make every dequantised weight a bf16 value: the
+    fp8 layer and the bf16 layer on those weights compute the same products,
+    so their outputs agree to accumulation order."""
+    cfg = mi.LayerConfig("fp8_exact", T=200, d=256, E=8, K=2, I=256, Is=128, weights="e4m3")
+    L = Layer(cfg)
+    for k in list(L.p):
+        if k.startswith("s") and L.p[k].dtype == torch.float32:
+            L.p[k] = torch.exp2(torch.round(torch.log2(L.p[k])))
+    y8 = to_f64(L.forward(moe))
+    deq = {}
+    for n in ("w_gate", "w_up", "w_down", "ws_gate", "ws_up", "ws_down"):
+        sn = "s" + n[1:] if n.startswith("w_") else "ss" + n[2:]
+        v = torch.from_numpy(oracle.e4m3_decode(host(L.p[n]))).cuda()
+        deq[n] = (v * L.p[sn].double()[..., None]).to(torch.bfloat16)
+    s = L.shape(moe)
+    ybf = torch.empty_like(L.x)
+    ws = moe.alloc_workspace(s)
+    moe.moe_forward(s, L.x, L.p["w_g"], L.bias, deq["w_gate"], deq["w_up"], deq["w_down"],
+                    deq["ws_gate"], deq["ws_up"], deq["ws_down"], ybf, ws)
+    torch.cuda.synchronize()
+    assert rel_l2(y8, to_f64(ybf)) <= 2e-3
+
+
+def test_forward_fp8_zero_tokens_is_a_no_op(moe):
+    cfg = mi.LayerConfig("fp8_empty", T=4, d=128, E=4, K=2, I=128, weights="e4m3")
+    L = Layer(cfg)
+    s = moe.make_shape(0, 128, 4, 2, 128, 0, "bf16")
+    moe.moe_forward_fp8(s, None, L.p["w_g"], None, moe.make_fp8_experts(L.p), None, None)
+
+
+def test_fp8_stalled_copy_times_out_and_the_context_survives(moe, monkeypatch):
+    """No raw weight tile is ever requested: the converters' and the MMA's
+    bounded waits run out, the kernel records MOE_ERR_TIMEOUT and returns."""
+    cfg = mi.LayerConfig("fp8_stall", T=64, d=256, E=4, K=2, I=256, Is=128, weights="e4m3")
+    L = Layer(cfg)
+    monkeypatch.setenv("MOE_TC_TIMEOUT_MS", "50")
+    monkeypatch.setenv("MOE_TC_TEST_STALL", "1")
+    s = L.shape(moe)
+    ws = moe.alloc_workspace(s)
+    y = torch.empty_like(L.x)
+    moe.moe_forward_fp8(s, L.x, L.p["w_g"], L.bias, moe.make_fp8_experts(L.p), y, ws)
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_error(ws) == moe.MOE_ERR_TIMEOUT
+    monkeypatch.delenv("MOE_TC_TEST_STALL")
+    monkeypatch.delenv("MOE_TC_TIMEOUT_MS")
+    L.x = _clean_x(L)
+    y = to_f64(L.forward(moe))
+    _check_rows(y, L.oracle_tokens(np.arange(cfg.T))["y"])
