@@ -39,9 +39,9 @@
  *   shared ws_gate/ws_up [Is][d], ws_down [d][Is].
  * dtype 0 = fp32 (float), 1 = bf16 (uint16_t bit patterns).
  *
- * 8-bit expert weights ("LLM inference optimisation" page, section "make
- * every byte cheaper": x_q = round(x / s) + z, x_hat = (x_q - z) s, with the
- * scale per tensor, per channel or per group): codes are OCP E4M3 floats
+ * 8-bit expert weights ("LLM from scratch, ch. 6", section "second route:
+ * make every byte cheaper": x_q = round(x / s) + z, x_hat = (x_q - z) s, with
+ * the scale per tensor, per channel or per group): codes are OCP E4M3 floats
  * (1 sign bit, 4 exponent bits with bias 7, 3 mantissa bits; largest finite
  * magnitude 448; S.1111.111 is NaN; no infinities), zero point 0, one fp32
  * scale per weight row (output channel).  The dequantised weight is
@@ -796,7 +796,7 @@ int oracle_e4m3_encode(int64_t n, const float *v, uint8_t *codes)
 /*
  * oracle_quantize_fp8_rows: per-channel quantisation of a row-major
  * [rows][cols] weight matrix (fp32 or bf16) to E4M3 codes with one fp32
- * scale per row (the x_q = round(x / s) + z form of the quantisation section
+ * scale per row (the x_q = round(x / s) + z form of the "make every byte cheaper" section
  * with z = 0): scale[r] = amax_r / 448 (1 when the row is all zeros), computed
  * in fp32; code = nearest E4M3 to (w / scale[r]) computed as an fp32 division.
  */
