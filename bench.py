@@ -57,13 +57,58 @@ def elem_bytes(cfg) -> int:
     return 2 if cfg.dtype == "bf16" else 4
 
 
+def expert_bytes(cfg, inter: int) -> int:
+    """Bytes of one expert's three matrices (E4M3: one byte per weight plus an
+    fp32 scale per weight row)."""
+    if cfg.weights == "e4m3":
+        return 3 * cfg.d * inter + 4 * (2 * inter + cfg.d)
+    return elem_bytes(cfg) * 3 * cfg.d * inter
+
+
 def layer_bytes(cfg, n_active: int) -> int:
     """Algorithmic HBM bytes of one call: router weights, the weights of every
     expert that got at least one token, the shared expert, x in and y out.
     Permuted copies and intermediates are implementation traffic, not counted."""
     s = elem_bytes(cfg)
-    return s * (cfg.E * cfg.d + n_active * 3 * cfg.d * cfg.I + 3 * cfg.d * cfg.Is
-                + 2 * cfg.T * cfg.d)
+    shared = expert_bytes(cfg, cfg.Is) if cfg.Is else 0
+    return (s * (cfg.E * cfg.d + 2 * cfg.T * cfg.d) + n_active * expert_bytes(cfg, cfg.I)
+            + shared)
+
+
+def ffn_stage_bytes(cfg, n_active: int) -> int:
+    """Algorithmic bytes of the routed expert-FFN stage: the active experts'
+    weights, the permuted rows in and the expert outputs out."""
+    return n_active * expert_bytes(cfg, cfg.I) + 2 * elem_bytes(cfg) * cfg.T * cfg.K * cfg.d
+
+
+class Forward:
+    """One moe_forward (or moe_forward_fp8 for 8-bit expert weights) on fixed
+    buffers; the argument structs are built once."""
+
+    def __init__(self, moe, cfg, s, p, bias, ws, stream):
+        self.moe, self.cfg, self.s, self.p, self.bias, self.ws, self.stream = (
+            moe, cfg, s, p, bias, ws, stream)
+        self.fp8 = moe.make_fp8_experts(p) if cfg.weights == "e4m3" else None
+
+    def __call__(self, x, y):
+        m, p = self.moe, self.p
+        if self.fp8 is not None:
+            m.moe_forward_fp8(self.s, x, p["w_g"], self.bias, self.fp8, y, self.ws,
+                              stream=self.stream)
+        else:
+            m.moe_forward(self.s, x, p["w_g"], self.bias, p["w_gate"], p["w_up"], p["w_down"],
+                          p.get("ws_gate"), p.get("ws_up"), p.get("ws_down"), y, self.ws,
+                          stream=self.stream)
+
+
+def oracle_tokens(cfg, tokens, x_host, p_host, bias_host):
+    """The oracle's per-token layer in the workload's weight format."""
+    import oracle
+    if cfg.weights == "e4m3":
+        return oracle.forward_tokens_fp8(tokens, x_host, p_host["w_g"], p_host, cfg.K,
+                                         dtype=cfg.dtype, bias=bias_host, router=cfg.router)
+    return oracle.forward_tokens(tokens, x_host, p_host, cfg.K, dtype=cfg.dtype, bias=bias_host,
+                                 router=cfg.router)
 
 
 def launches_per_forward(cfg, gemv_limit: int = 0) -> int:
@@ -74,6 +119,9 @@ def launches_per_forward(cfg, gemv_limit: int = 0) -> int:
     single-SM tcgen05 gate/up and down GEMMs when needed, and the CTA-pair
     ones too when a group can hold more rows than one 128-row tile (or, with
     MOE_PAIR_MIN_ROWS set, at least that many rows), combine."""
+    if cfg.weights == "e4m3":
+        # router + top-K, 3 dispatch kernels, row gather, plan, gate/up, down, combine
+        return 2 + 3 + 1 + 1 + 2 + 1
     need_tc = cfg.dtype == "bf16" and cfg.T > gemv_limit
     gather = need_tc and cfg.T > int(os.environ.get("MOE_GATHER_MAX_ROWS", "0"))
     gemv = cfg.dtype == "f32" or gemv_limit > 0
@@ -198,7 +246,7 @@ def oracle_tokens_per_s(cfg, x_host, p_host, bias_host, budget_s: float = 15.0,
     while True:
         tokens = mi.sample_tokens(cfg.T, n, seed=cfg.seed, name=f"{seed_name}/{n}").numpy()
         t0 = time.perf_counter()
-        oracle.forward_tokens(tokens, x_host, p_host, cfg.K, dtype=cfg.dtype, bias=bias_host)
+        oracle_tokens(cfg, tokens, x_host, p_host, bias_host)
         dt = time.perf_counter() - t0
         spent += dt
         done = len(tokens)
@@ -236,9 +284,10 @@ def run_ours(args):
     stream = torch.cuda.Stream()
     torch.cuda.synchronize()  # every input is written before the side stream reads it
 
+    call = Forward(moe, cfg, s, p, bias, ws, stream)
+
     def fwd(xx=x, yy=y):
-        moe.moe_forward(s, xx, p["w_g"], bias, p["w_gate"], p["w_up"], p["w_down"],
-                        p.get("ws_gate"), p.get("ws_up"), p.get("ws_down"), yy, ws, stream=stream)
+        call(xx, yy)
 
     # active experts of this batch (for the byte count), from the library's own routing
     n_active = count_active(moe, cfg, x, p, bias, stream)
@@ -263,7 +312,7 @@ def run_ours(args):
         barrier(ws_n)
         # dominant stage, timed alone on the same stream: the expert FFN (tcgen05
         # gate/up GEMM with fused SiLU*mul, then the down GEMM) of this batch
-        stage = time_expert_ffn(moe, cfg, x, p, bias, stream, args.steps)
+        stage = time_expert_ffn(moe, cfg, x, p, bias, stream, args.steps, n_active)
     t_ms = ev0.elapsed_time(ev1) / args.steps
     t_ms_max = max_over_ranks(t_ms, ws_n)
     code = moe.moe_get_device_error(ws)
@@ -271,7 +320,7 @@ def run_ours(args):
         raise RuntimeError(f"device error in the timed region: {moe.status_string(code)}")
 
     tokens_per_s = cfg.T * ws_n / (t_ms_max / 1e3)
-    e2e = time_e2e(moe, cfg, s, p, bias, ws, stream, args.steps, x)
+    e2e = time_e2e(call, stream, args.steps, x)
     e2e_ms = max_over_ranks(e2e["ms"], ws_n)
 
     result = {
@@ -286,11 +335,16 @@ def run_ours(args):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": cfg.dtype,
-        "data": "synthetic (seeded N(0,1) tokens, N(0,1/d) weights; no trained weights)",
+        "data": ("synthetic (seeded N(0,1) tokens, N(0,1/d) weights; no trained weights)"
+                 if cfg.weights != "e4m3" else
+                 "synthetic (seeded N(0,1) tokens; random E4M3 expert codes with fp32 row "
+                 "scales; no trained weights)"),
         "config": {"workload": cfg.name, "T": cfg.T, "d": cfg.d, "E": cfg.E, "K": cfg.K,
                    "inter": cfg.I, "inter_shared": cfg.Is, "active_experts": n_active,
+                   "expert_weights": "e4m3 + fp32 row scales" if cfg.weights == "e4m3"
+                                     else cfg.dtype,
                    "l2": "inputs larger than L2 (expert weights "
-                         f"{3 * cfg.E * cfg.d * cfg.I * elem_bytes(cfg) / 1e9:.2f} GB), no flush",
+                         f"{cfg.E * expert_bytes(cfg, cfg.I) / 1e9:.2f} GB), no flush",
                    "parallelism": f"replicas x{ws_n} (independent batches, no collective)"},
         "layer": {"tflops": layer_flops(cfg) / (t_ms_max / 1e3) / 1e12,
                   "gbs": layer_bytes(cfg, n_active) / (t_ms_max / 1e3) / 1e9,
@@ -336,8 +390,9 @@ def count_active(moe, cfg, x, p, bias, stream) -> int:
     return int(torch.unique(idx).numel())
 
 
-def time_expert_ffn(moe, cfg, x, p, bias, stream, steps: int) -> dict:
-    """Events around moe_expert_ffn alone (routed experts of this batch)."""
+def time_expert_ffn(moe, cfg, x, p, bias, stream, steps: int, n_active: int) -> dict:
+    """Events around moe_expert_ffn (or moe_expert_ffn_fp8) alone: the routed
+    experts of this batch."""
     import torch
     s = moe.make_shape(cfg.T, cfg.d, cfg.E, cfg.K, cfg.I, 0, cfg.dtype, cfg.router)
     ws = moe.alloc_workspace(s)
@@ -352,9 +407,14 @@ def time_expert_ffn(moe, cfg, x, p, bias, stream, steps: int) -> dict:
     moe.moe_route(s, x, p["w_g"], bias, None, None, idx, w, ws, stream=stream)
     moe.moe_permute(s, idx, x, counts, offsets, None, None, x_perm, ws, stream=stream)
 
+    fp8 = moe.make_fp8_experts(p) if cfg.weights == "e4m3" else None
+
     def run():
-        moe.moe_expert_ffn(s, x_perm, offsets, p["w_gate"], p["w_up"], p["w_down"], y_perm, ws,
-                           stream=stream)
+        if fp8 is not None:
+            moe.moe_expert_ffn_fp8(s, x_perm, offsets, fp8, y_perm, ws, stream=stream)
+        else:
+            moe.moe_expert_ffn(s, x_perm, offsets, p["w_gate"], p["w_up"], p["w_down"], y_perm,
+                               ws, stream=stream)
     for _ in range(3):
         run()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -365,7 +425,7 @@ def time_expert_ffn(moe, cfg, x, p, bias, stream, steps: int) -> dict:
     e1.record(stream)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
-    return {"ms": ms, "flops": 6 * n * cfg.d * cfg.I}
+    return {"ms": ms, "flops": 6 * n * cfg.d * cfg.I, "bytes": ffn_stage_bytes(cfg, n_active)}
 
 
 # DRAM bytes (read + write) of one expert-FFN stage (both tcgen05 launches), from one
@@ -388,19 +448,35 @@ def stage_traffic(workload: str):
 
 
 def stage_roofline(cfg, stage, peaks) -> dict:
-    achieved = stage["flops"] / (stage["ms"] / 1e3) / 1e12
-    peak = peaks["bf16_tflops"]
-    return {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-            "frac": achieved / peak, "traffic": stage_traffic(cfg.name),
-            "traffic_unit": "bytes per launch pair (DRAM read + write, ncu)",
-            "kernel": "expert FFN stage: tcgen05 gate/up GEMM (SiLU*mul epilogue) + tcgen05 "
-                      "down GEMM (+ plan, empty GEMV launches)",
-            "per_launch_flops": stage["flops"], "ms_per_launch": stage["ms"],
-            "peak_kind": f"bf16 dense, burst, {peaks['source']}"}
+    """The expert-FFN stage against the roofline that binds it: the tensor
+    pipe (bf16 dense) or HBM, whichever the stage comes closer to."""
+    sec = stage["ms"] / 1e3
+    tflops = stage["flops"] / sec / 1e12
+    gbs = stage["bytes"] / sec / 1e9
+    t_frac, h_frac = tflops / peaks["bf16_tflops"], gbs / peaks["hbm_gbs"]
+    kernel = ("expert FFN stage: tcgen05 gate/up GEMM (SiLU*mul epilogue) + tcgen05 down GEMM "
+              + ("on E4M3 weights widened in-kernel" if cfg.weights == "e4m3" else
+                 "(+ plan, empty GEMV launches)"))
+    common = {"traffic": stage_traffic(cfg.name),
+              "traffic_unit": "bytes per launch pair (DRAM read + write, ncu)",
+              "kernel": kernel, "per_launch_flops": stage["flops"],
+              "per_launch_bytes": stage["bytes"], "ms_per_launch": stage["ms"],
+              "other_frac": None}
+    if t_frac >= h_frac:
+        out = {"bound": "tensor", "achieved": tflops, "peak": peaks["bf16_tflops"],
+               "unit": "TFLOP/s", "frac": t_frac,
+               "peak_kind": f"bf16 dense, burst, {peaks['source']}"}
+        common["other_frac"] = {"hbm": h_frac}
+    else:
+        out = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+               "frac": h_frac, "peak_kind": f"HBM copy, {peaks['source']}"}
+        common["other_frac"] = {"tensor": t_frac}
+    out.update(common)
+    return out
 
 
-def time_e2e(moe, cfg, s, p, bias, ws, stream, steps, x_dev) -> dict:
-    """Through the C ABI with host buffers: pinned x -> device, moe_forward,
+def time_e2e(call, stream, steps, x_dev) -> dict:
+    """Through the C ABI with host buffers: pinned x -> device, the forward call,
     y -> pinned host, every step inside the timed region."""
     import torch
     xh = x_dev.cpu().pin_memory()
@@ -411,9 +487,7 @@ def time_e2e(moe, cfg, s, p, bias, ws, stream, steps, x_dev) -> dict:
     def step():
         with torch.cuda.stream(stream):
             xd.copy_(xh, non_blocking=True)
-            moe.moe_forward(s, xd, p["w_g"], bias, p["w_gate"], p["w_up"], p["w_down"],
-                            p.get("ws_gate"), p.get("ws_up"), p.get("ws_down"), yd, ws,
-                            stream=stream)
+            call(xd, yd)
             yh.copy_(yd, non_blocking=True)
     for _ in range(3):
         step()
@@ -448,10 +522,10 @@ def bench_workload(moe, cfg, peaks, steps: int, graph: bool = False) -> dict:
     st = torch.cuda.Stream()
     torch.cuda.synchronize()  # every input is written before the side stream reads it
     n_active = count_active(moe, cfg, x, p, bias, st)
+    call = Forward(moe, cfg, s, p, bias, ws, st)
 
     def fwd():
-        moe.moe_forward(s, x, p["w_g"], bias, p["w_gate"], p["w_up"], p["w_down"],
-                        p.get("ws_gate"), p.get("ws_up"), p.get("ws_down"), y, ws, stream=st)
+        call(x, y)
     for _ in range(5):
         fwd()
     torch.cuda.synchronize()
@@ -498,7 +572,8 @@ def bench_workload(moe, cfg, peaks, steps: int, graph: bool = False) -> dict:
 def bench_all(moe, peaks, args) -> list:
     res = []
     for name in ("tiny_f32", "mixtral_prefill", "dsv3_decode", "dsv3_prefill_zipf",
-                 *[f"dsv3_sweep_T{t}" for t in mi.SWEEP_T], "dsv3_decode_sigmoid"):
+                 *[f"dsv3_sweep_T{t}" for t in mi.SWEEP_T], "dsv3_decode_sigmoid",
+                 "dsv3_decode_fp8", "mixtral_prefill_fp8"):
         cfg = mi.CONFIGS[name]
         res.append(bench_workload(moe, cfg, peaks, steps=max(10, args.steps),
                                   graph=cfg.T <= 64))
@@ -529,7 +604,7 @@ def run_reference(args):
     for i in range(args.warmup + args.steps):
         tokens = mi.sample_tokens(cfg.T, per_step, seed=cfg.seed, name=f"ref_step/{i}").numpy()
         t0 = time.perf_counter()
-        oracle.forward_tokens(tokens, xh, hp, cfg.K, dtype=cfg.dtype, bias=bh)
+        oracle_tokens(cfg, tokens, xh, hp, bh)
         dt = time.perf_counter() - t0
         if i >= args.warmup:
             times.append(dt)

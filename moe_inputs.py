@@ -21,7 +21,8 @@ Workloads (shapes and distributions; names by what they are):
   dsv3_decode_sigmoid dsv3_decode with the DeepSeek-V3 router (sigmoid affinities,
                       weights a / (sum a + 1e-6)).
   dsv3_decode_fp8     dsv3_decode with 8-bit expert weights (routed and shared):
-  mixtral_prefill_fp8 mixtral_prefill likewise.  Each weight is an E4M3 code drawn
+  mixtral_prefill_fp8 mixtral_prefill likewise (dsv3_decode_fp8_E32: the decode
+                      layer with a pool of 32 experts).  Each weight is an E4M3 code drawn
                       as random bits -- sign uniform, exponent field uniform in
                       9..15, mantissa uniform, the NaN pattern S.1111.111 redrawn
                       as S.1111.110 -- so magnitudes are log-uniform over [4, 448]
@@ -87,6 +88,10 @@ CONFIGS["dsv3_decode_fp8"] = replace(CONFIGS["dsv3_decode"], name="dsv3_decode_f
                                      weights="e4m3")
 CONFIGS["mixtral_prefill_fp8"] = replace(CONFIGS["mixtral_prefill"], name="mixtral_prefill_fp8",
                                          weights="e4m3")
+# the same decode layer over a pool of 32 experts (1.4 GB of codes): small enough
+# for multi-pass counter captures, still far larger than L2
+CONFIGS["dsv3_decode_fp8_E32"] = replace(CONFIGS["dsv3_decode_fp8"], name="dsv3_decode_fp8_E32",
+                                         E=32)
 SWEEP_T = (1, 8, 64, 512, 4096)
 for _t in SWEEP_T:
     CONFIGS[f"dsv3_sweep_T{_t}"] = LayerConfig(f"dsv3_sweep_T{_t}", T=_t, d=7168, E=256, K=8,

@@ -247,15 +247,16 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two) {
 // W8 converter warp cw (0..3): rows 64*cw .. 64*cw+63 of K half h (codes
 // 64h .. 64h+63 of each 128-code row) of a raw tile -> the bf16 weight tile of
 // an MMA stage.  Both tiles use the 128-byte swizzle (16-byte chunk c of row r
-// at chunk c ^ (r & 7)); lane (r % 8, q) reads code chunk 4h+q of row r and
-// writes bf16 chunks 2q and 2q+1, so every shared-memory access of a warp
-// spreads evenly over the banks.
+// at chunk c ^ (r & 7)).  Lane 8j + 4s + q takes row 8*it + j + 4s: it reads
+// code chunk 4h+q and writes bf16 chunks 2q and 2q+1, the odd one first when
+// s = 1.  Each quarter-warp (8 lanes, one shared-memory wavefront of 16-byte
+// accesses) then touches 8 distinct chunk positions on every load and store.
 __device__ __forceinline__ void convert_rows_w8(const uint8_t* raw, uint8_t* dst, int h, int cw,
                                                 int lane) {
-    const int q = lane & 3, rsub = lane >> 2;
+    const int q = lane & 3, s = (lane >> 2) & 1, j = lane >> 3;
 #pragma unroll
     for (int it = 0; it < 8; ++it) {
-        const int r = cw * 64 + it * 8 + rsub;
+        const int r = cw * 64 + it * 8 + j + 4 * s;
         const int x = r & 7;
         const uint4 v = *reinterpret_cast<const uint4*>(raw + r * 128 + (((h * 4 + q) ^ x) << 4));
         uint4 lo, hi;
@@ -267,8 +268,10 @@ __device__ __forceinline__ void convert_rows_w8(const uint8_t* raw, uint8_t* dst
         hi.y = e4m3x2_to_bf16x2(v.z >> 16);
         hi.z = e4m3x2_to_bf16x2(v.w);
         hi.w = e4m3x2_to_bf16x2(v.w >> 16);
-        *reinterpret_cast<uint4*>(dst + r * 128 + (((2 * q) ^ x) << 4)) = lo;
-        *reinterpret_cast<uint4*>(dst + r * 128 + (((2 * q + 1) ^ x) << 4)) = hi;
+        const uint4 first = s ? hi : lo, second = s ? lo : hi;
+        const int c_first = 2 * q + s, c_second = 2 * q + 1 - s;
+        *reinterpret_cast<uint4*>(dst + r * 128 + ((c_first ^ x) << 4)) = first;
+        *reinterpret_cast<uint4*>(dst + r * 128 + ((c_second ^ x) << 4)) = second;
     }
 }
 

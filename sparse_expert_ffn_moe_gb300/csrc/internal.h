@@ -109,6 +109,14 @@ cudaError_t launch_router_tc(const moe_shape& s, const void* x, const void* w_g,
 cudaError_t launch_ffn_tc_fp8(const FfnGroups& g, const FfnPlanHeader* hdr, const int4* mtile_list,
                               int max_mtiles, DevError* err, cudaStream_t st);
 
+// ---- ffn_gemv_fp8.cu (E4M3 weights, small groups) ----
+int gemv8_max_rows();  // groups with at most this many rows take the 8-bit GEMV
+bool gemv8_fits(int widest);  // its staged activation rows of this width fit in shared memory
+constexpr int kGemv8Rows = 8;  // activation rows per pass of the 8-bit GEMV
+constexpr size_t kGemv8SmemLimit = 232448;
+cudaError_t launch_ffn_gemv_fp8(const FfnGroups& g, const FfnPlanHeader* hdr, const int32_t* list,
+                                cudaStream_t st);
+
 // ---- quant.cu ----
 cudaError_t launch_quantize_fp8_rows(int64_t rows, int64_t cols, int dtype, const void* w,
                                      uint8_t* codes, float* scales, cudaStream_t st);

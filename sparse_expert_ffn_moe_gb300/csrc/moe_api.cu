@@ -6,6 +6,7 @@
 #include <stdint.h>
 #include <stdlib.h>
 
+#include <algorithm>
 #include <atomic>
 
 #include "common.cuh"
@@ -67,6 +68,13 @@ moe_status check_fp8_shape(const moe_shape& s) {
     if (s.dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
     if (s.d % 128 || s.inter % 128 || s.inter_shared % 128) return MOE_ERR_UNSUPPORTED;
     return MOE_OK;
+}
+
+// Groups with at most this many rows take the 8-bit GEMV (0 when its staged
+// activation rows would not fit in shared memory).
+int gemv8_limit(const moe_shape& s) {
+    const int widest = std::max(s.d, std::max(s.inter, s.inter_shared));
+    return gemv8_fits(widest) ? gemv8_max_rows() : 0;
 }
 
 // routed code and scale pointers present and aligned; shared ones iff wanted
@@ -435,10 +443,14 @@ moe_status moe_expert_ffn_fp8(const moe_shape* shape, const void* x_perm, const 
     g.h = at<void>(workspace, L.h);
     g.y = y_perm;
     FfnPlanHeader* hdr = at<FfnPlanHeader>(workspace, L.plan);
+    int32_t* glist = at<int32_t>(workspace, L.gemv_list);
     int4* mtiles = at<int4>(workspace, L.mtile_list);
-    e = launch_ffn_plan(g, s.dtype, hdr, at<int32_t>(workspace, L.gemv_list), mtiles, L.max_mtiles,
-                        0, false, cs);
-    if (e == cudaSuccess) e = launch_ffn_tc_fp8(g, hdr, mtiles, L.max_mtiles, err, cs);
+    const int lim = gemv8_limit(s);
+    e = launch_ffn_plan(g, s.dtype, hdr, glist, mtiles, L.max_mtiles, lim, false, cs);
+    if (e == cudaSuccess && lim > 0) e = launch_ffn_gemv_fp8(g, hdr, glist, cs);
+    // a group has at most T*K rows here (the offsets are the caller's)
+    if (e == cudaSuccess && (int64_t)s.T * s.K > lim)
+        e = launch_ffn_tc_fp8(g, hdr, mtiles, L.max_mtiles, err, cs);
     return cuda_status(e);
 }
 
@@ -519,10 +531,13 @@ moe_status moe_forward_fp8(const moe_shape* shape, const void* x, const void* w_
     g.y = at<void>(workspace, L.y_perm);
     g.y_s = at<void>(workspace, L.y_s);
     FfnPlanHeader* hdr = at<FfnPlanHeader>(workspace, L.plan);
+    int32_t* glist = at<int32_t>(workspace, L.gemv_list);
     int4* mtiles = at<int4>(workspace, L.mtile_list);
-    e = launch_ffn_plan(g, s.dtype, hdr, at<int32_t>(workspace, L.gemv_list), mtiles, L.max_mtiles,
-                        0, false, cs);
-    if (e == cudaSuccess) e = launch_ffn_tc_fp8(g, hdr, mtiles, L.max_mtiles, err, cs);
+    const int lim = gemv8_limit(s);
+    e = launch_ffn_plan(g, s.dtype, hdr, glist, mtiles, L.max_mtiles, lim, false, cs);
+    if (e == cudaSuccess && lim > 0) e = launch_ffn_gemv_fp8(g, hdr, glist, cs);
+    // a group has at most T rows (a token picks an expert once; the shared group has T)
+    if (e == cudaSuccess && s.T > lim) e = launch_ffn_tc_fp8(g, hdr, mtiles, L.max_mtiles, err, cs);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
 
     // 4. combine

@@ -79,9 +79,10 @@ def _expert_ffn_case(moe, counts, d, I, seed=0):
 
 
 @pytest.mark.parametrize("counts,d,I", [
-    ([75, 0, 140, 3, 1, 260, 77, 44], 256, 384),     # ragged groups, one empty
+    ([75, 0, 140, 3, 1, 260, 77, 44], 256, 384),     # ragged groups, one empty; GEMV + tiles
     ([600, 257, 1, 129], 384, 640),                  # several m-tiles per group, 5 n-blocks
-    ([1, 2, 1, 1, 3, 1, 1, 2], 1024, 256),           # decode-like: a few rows per expert
+    ([1, 2, 1, 1, 3, 1, 1, 2], 1024, 256),           # decode-like: a few rows per expert (GEMV)
+    ([8, 9, 0, 7, 16, 17], 128, 128),                # around the GEMV limit, narrowest shapes
 ])
 def test_expert_ffn_fp8_matches_oracle(moe, counts, d, I):
     y, ref = _expert_ffn_case(moe, counts, d, I)
@@ -112,7 +113,12 @@ def _check_rows(y, ref):
 
 
 @pytest.mark.parametrize("router", ["softmax", "sigmoid"])
-def test_forward_fp8_small_layer_all_tokens(moe, router):
+@pytest.mark.parametrize("gemv8", ["0", "8", "16"])
+def test_forward_fp8_small_layer_all_tokens(moe, router, gemv8, monkeypatch):
+    """Groups of ~11 rows and a 45-row shared group: all on the tensor cores
+    (limit 0), small groups on the 8-bit GEMV (default 8), or every routed
+    group on the GEMV in two passes of at most 8 rows (limit 16)."""
+    monkeypatch.setenv("MOE_GEMV8_MAX_ROWS", gemv8)
     cfg = mi.LayerConfig("fp8_small", T=45, d=256, E=12, K=3, I=384, Is=256, router=router,
                          weights="e4m3")
     L = Layer(cfg)
@@ -131,7 +137,11 @@ def test_forward_fp8_without_shared_expert(moe):
     _check_rows(y, ref["y"])
 
 
-def test_forward_fp8_decode_full_size(moe):
+@pytest.mark.parametrize("gemv8", ["0", "8"])
+def test_forward_fp8_decode_full_size(moe, gemv8, monkeypatch):
+    """DeepSeek-V3 decode shapes: every group on the 8-bit GEMV (default) or on
+    the tensor cores (limit 0)."""
+    monkeypatch.setenv("MOE_GEMV8_MAX_ROWS", gemv8)
     cfg = mi.CONFIGS["dsv3_decode_fp8"]
     L = Layer(cfg)
     L.x = _clean_x(L)
