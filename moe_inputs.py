@@ -88,6 +88,9 @@ CONFIGS["dsv3_decode_fp8"] = replace(CONFIGS["dsv3_decode"], name="dsv3_decode_f
                                      weights="e4m3")
 CONFIGS["mixtral_prefill_fp8"] = replace(CONFIGS["mixtral_prefill"], name="mixtral_prefill_fp8",
                                          weights="e4m3")
+for _t in (64, 512):
+    CONFIGS[f"dsv3_sweep_fp8_T{_t}"] = replace(CONFIGS["dsv3_decode_fp8"],
+                                               name=f"dsv3_sweep_fp8_T{_t}", T=_t)
 # the same decode layer over a pool of 32 experts (1.4 GB of codes): small enough
 # for multi-pass counter captures, still far larger than L2
 CONFIGS["dsv3_decode_fp8_E32"] = replace(CONFIGS["dsv3_decode_fp8"], name="dsv3_decode_fp8_E32",

@@ -58,18 +58,20 @@ __device__ int32_t scan_1024(int32_t v, int32_t* sh, int32_t* total) {
 }
 
 // groups: E routed (+1 shared), up to 1024 per pass of one 1024-thread block.
-// A group goes to the GEMV list (1..limit rows), to the pair-tile list (at
+// A group goes to a GEMV list (1..limit rows: the first list up to `small`
+// rows when small > 0, the second list above), to the pair-tile list (at
 // least pair_min rows, tiles of pair_m rows) or to the single-tile list
-// (tiles of single_m rows).  Entries are (group, first row of the group, rows
-// of the group, index of the m-tile within the group).
+// (tiles of single_m rows).  Tile entries are (group, first row of the group,
+// rows of the group, index of the m-tile within the group).
 __global__ void __launch_bounds__(1024)
 ffn_plan_kernel(const int32_t* __restrict__ offsets, int E, int has_shared, int T, int limit,
-                int single_m, int pair_min, int pair_m, FfnPlanHeader* __restrict__ hdr,
+                int small, int single_m, int pair_min, int pair_m, FfnPlanHeader* __restrict__ hdr,
                 int32_t* __restrict__ gemv_list, int4* __restrict__ mtile_list, int max_mtiles) {
     __shared__ int32_t sh[32];
-    __shared__ int32_t tot_g, tot_s, tot_p, base_g, base_s, base_p;
-    if (threadIdx.x == 0) { base_g = 0; base_s = 0; base_p = 0; }
+    __shared__ int32_t tot_g, tot_g2, tot_s, tot_p, base_g, base_g2, base_s, base_p;
+    if (threadIdx.x == 0) { base_g = 0; base_g2 = 0; base_s = 0; base_p = 0; }
     __syncthreads();
+    int32_t* gemv_list2 = gemv_list + (E + 1);
     int4* pair_list = mtile_list + max_mtiles;
     const int G = E + (has_shared ? 1 : 0);
     for (int g0 = 0; g0 < G; g0 += blockDim.x) {
@@ -77,7 +79,9 @@ ffn_plan_kernel(const int32_t* __restrict__ offsets, int E, int has_shared, int 
         int32_t rows = 0, row0 = 0;
         if (g < E) { row0 = offsets[g]; rows = offsets[g + 1] - row0; }
         else if (g < G) { row0 = 0; rows = T; }
-        const bool to_gemv = rows > 0 && rows <= limit;
+        const bool gemv_any = rows > 0 && rows <= limit;
+        const bool to_gemv = gemv_any && (small <= 0 || rows <= small);
+        const bool to_gemv2 = gemv_any && !to_gemv;
         // pair_min > 0: fixed threshold.  0: the cheaper shape by padded rows
         // over the measured tensor-pipe activity of each shape (pair ~85%,
         // single ~70% on GB300): pair if ceil(r/256)*256/85 < ceil(r/128)*128/70.
@@ -87,9 +91,11 @@ ffn_plan_kernel(const int32_t* __restrict__ offsets, int E, int has_shared, int 
         const int32_t st = (rows > limit && !to_pair) ? (rows + single_m - 1) / single_m : 0;
         const int32_t pt = to_pair ? (rows + pair_m - 1) / pair_m : 0;
         const int32_t pg = scan_1024(to_gemv ? 1 : 0, sh, &tot_g);
+        const int32_t pg2 = scan_1024(to_gemv2 ? 1 : 0, sh, &tot_g2);
         const int32_t ps = scan_1024(st, sh, &tot_s);
         const int32_t pp = scan_1024(pt, sh, &tot_p);
         if (to_gemv) gemv_list[base_g + pg] = g;
+        if (to_gemv2) gemv_list2[base_g2 + pg2] = g;
         for (int32_t i = 0; i < st; ++i) {
             const int32_t slot = base_s + ps + i;
             if (slot < max_mtiles) mtile_list[slot] = make_int4(g, row0, rows, i);
@@ -99,11 +105,12 @@ ffn_plan_kernel(const int32_t* __restrict__ offsets, int E, int has_shared, int 
             if (slot < max_mtiles) pair_list[slot] = make_int4(g, row0, rows, i);
         }
         __syncthreads();
-        if (threadIdx.x == 0) { base_g += tot_g; base_s += tot_s; base_p += tot_p; }
+        if (threadIdx.x == 0) { base_g += tot_g; base_g2 += tot_g2; base_s += tot_s; base_p += tot_p; }
         __syncthreads();
     }
     if (threadIdx.x == 0) {
         hdr->n_gemv = base_g;
+        hdr->n_gemv2 = base_g2;
         hdr->n_mtiles = min(base_s, max_mtiles);
         hdr->n_ptiles = min(base_p, max_mtiles);
     }
@@ -340,12 +347,13 @@ int gemv_max_rows() {
 
 cudaError_t launch_ffn_plan(const FfnGroups& g, int dtype, FfnPlanHeader* hdr, int32_t* gemv_list,
                             int4* mtile_list, int max_mtiles, int gemv_limit, bool allow_pair,
-                            cudaStream_t st) {
+                            int small_rows, cudaStream_t st) {
     // fp32 layers never use the tensor cores (no TF32): every group streams
     const int limit = dtype == MOE_F32 ? 0x7fffffff : gemv_limit;
     // a pair threshold no group can reach keeps every group on single tiles
     const int pair_min = allow_pair ? tc_pair_min_rows() : 0x7fffffff;
-    ffn_plan_kernel<<<1, 1024, 0, st>>>(g.offsets, g.E, g.has_shared, g.T, limit, tc_tile_rows(false),
+    ffn_plan_kernel<<<1, 1024, 0, st>>>(g.offsets, g.E, g.has_shared, g.T, limit, small_rows,
+                                        tc_tile_rows(false),
                                         pair_min, tc_tile_rows(true), hdr, gemv_list,
                                         mtile_list, max_mtiles);
     return cudaGetLastError();

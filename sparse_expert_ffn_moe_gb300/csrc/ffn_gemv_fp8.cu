@@ -12,8 +12,8 @@
 // widening and FMAs; both stay far below the HBM rate.  Here each code goes
 // HBM -> register once and is widened with one cvt per two codes (E4M3 ->
 // f16, exact); the products run on the warp-level tensor-core instruction
-// mma.m16n8k16 (f16 x f16 -> f32), whose N = 8 columns hold up to 8 token
-// rows of the group.
+// mma.m16n8k16 (f16 x f16 -> f32); one or two MMAs per A fragment (8 or 16
+// token rows of the group per pass, by what fits in shared memory).
 //
 // A warp owns 16 weight rows (gate/up: 8 gate rows and the 8 up rows of the
 // same intermediate indices, so SiLU(g) * u is formed in the accumulator
@@ -31,7 +31,9 @@
 // scaled by an exact power of two 2^-e so that its largest magnitude lies in
 // [2^14, 2^15): every bf16 value within 2^29 of the row maximum is exact in
 // f16 and nothing overflows.  The fp32 sums are multiplied by 2^e and by the
-// weight row's scale.
+// weight row's scale.  Row m stores its 8-byte slot s (4 values) at slot
+// s ^ (m % 16) of the same 128-byte segment, so the B loads of a half-warp
+// (4 token rows x 4 lanes) hit 16 distinct bank pairs.
 //
 // Work: warp tasks (group, 16 weight rows); each block takes a contiguous
 // range of tasks and walks it group by group, staging each group's activation
@@ -49,10 +51,9 @@ namespace {
 
 constexpr int kG8Warps = 16;
 constexpr int kG8Threads = kG8Warps * 32;
-constexpr int kG8Tok = kGemv8Rows;  // activation rows per pass = MMA N (8)
+constexpr int kG8Tok = 8;           // token rows per MMA (its N)
+constexpr int kG8MaxTiles = 2;      // MMAs per A fragment: up to 16 token rows per pass
 constexpr int kG8U = 8;             // 64-code K blocks in flight per lane
-constexpr int kG8Pad = 4;           // f16 padding per staged row (conflict-free B loads)
-static_assert(kG8Tok == 8, "the MMA has 8 columns");
 
 struct Group8 {
     int rows;
@@ -109,16 +110,18 @@ __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// 8-byte slot s of staged row m (swizzled within its 128-byte segment)
+__device__ __forceinline__ int sw_slot(int s, int m) { return (s & ~15) | ((s & 15) ^ (m & 15)); }
+
 // Stage token rows c0 .. c0+nt-1 of group v (n values each) into act as f16
-// scaled by 2^-e_m (rows nt..7 zero), with rs[m] = 2^e_m.  Routed rows come
-// from the permuted copy (row0 + c0 + m), shared rows from the token rows.
-// One warp per row.
+// scaled by 2^-e_m (rows nt .. rows-1 zero), with rs[m] = 2^e_m.  Routed rows
+// come from the permuted copy (row0 + c0 + m), shared rows from the token
+// rows.  One warp per row.
 __device__ __forceinline__ void stage_f16(__half* act, float* rs, const bf16* routed,
                                           const bf16* shared, const Group8& v, int c0, int nt,
-                                          int n, int warp, int lane) {
-    const int ld = n + kG8Pad;
-    for (int m = warp; m < kG8Tok; m += kG8Warps) {
-        uint2* dst = reinterpret_cast<uint2*>(act + (int64_t)m * ld);
+                                          int rows, int n, int warp, int lane) {
+    for (int m = warp; m < rows; m += kG8Warps) {
+        uint2* dst = reinterpret_cast<uint2*>(act + (int64_t)m * n);
         if (m >= nt) {
             for (int c = lane; c < n / 4; c += 32) dst[c] = make_uint2(0u, 0u);
             if (lane == 0) rs[m] = 0.0f;
@@ -152,19 +155,23 @@ __device__ __forceinline__ void stage_f16(__half* act, float* rs, const bf16* ro
                 const __half2 h2 = __floats2half2_rn(f[2 * k] * down, f[2 * k + 1] * down);
                 hw[k] = *reinterpret_cast<const uint32_t*>(&h2);
             }
-            dst[2 * c] = make_uint2(hw[0], hw[1]);
-            dst[2 * c + 1] = make_uint2(hw[2], hw[3]);
+            dst[sw_slot(2 * c, m)] = make_uint2(hw[0], hw[1]);
+            dst[sw_slot(2 * c + 1, m)] = make_uint2(hw[2], hw[3]);
         }
     }
 }
 
-// c += weight rows (p0: M rows 0-7 via lane group g, p1: M rows 8-15) of n
-// codes times the staged activations (8 token columns)
+// c[nt] += weight rows (p0: MMA rows 0-7 via the lane's group g, p1: rows
+// 8-15) of n codes times staged token rows 8 nt .. 8 nt + 7
+template <int NTILE, int R>
 __device__ __forceinline__ void mma_rows(const uint8_t* p0, const uint8_t* p1, int n,
-                                         const __half* act, int lane, float (&c)[4]) {
+                                         const __half* act, int lane, float (&c)[NTILE][4]) {
     const int g = lane >> 2, t = lane & 3;
     const int nkb = n / 64;
-    const __half* brow = act + (int64_t)g * (n + kG8Pad) + 16 * t;
+    const uint2* arow[NTILE];
+#pragma unroll
+    for (int j = 0; j < NTILE; ++j)  // (rows past R are never read)
+        arow[j] = reinterpret_cast<const uint2*>(act + (int64_t)min(8 * j + g, R - 1) * n);
     p0 += 16 * t;
     p1 += 16 * t;
     for (int kb0 = 0; kb0 < nkb; kb0 += kG8U) {
@@ -182,9 +189,16 @@ __device__ __forceinline__ void mma_rows(const uint8_t* p0, const uint8_t* p1, i
             const uint32_t r1[4] = {w1[u].x, w1[u].y, w1[u].z, w1[u].w};
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
-                const uint2 b = *reinterpret_cast<const uint2*>(brow + (kb0 + u) * 64 + 4 * kk);
-                mma16816(c, e4m3x2_to_f16x2(r0[kk]), e4m3x2_to_f16x2(r1[kk]),
-                         e4m3x2_to_f16x2(r0[kk] >> 16), e4m3x2_to_f16x2(r1[kk] >> 16), b.x, b.y);
+                const uint32_t a0 = e4m3x2_to_f16x2(r0[kk]), a1 = e4m3x2_to_f16x2(r1[kk]);
+                const uint32_t a2 = e4m3x2_to_f16x2(r0[kk] >> 16), a3 = e4m3x2_to_f16x2(r1[kk] >> 16);
+                const int slot = 16 * (kb0 + u) + 4 * t + kk;
+#pragma unroll
+                for (int j = 0; j < NTILE; ++j) {
+                    // token rows past the R staged ones are zero columns
+                    const uint2 b = (R >= 8 * (j + 1) || 8 * j + g < R) ? arow[j][sw_slot(slot, 8 * j + g)]
+                                                                       : make_uint2(0u, 0u);
+                    mma16816(c[j], a0, a1, a2, a3, b.x, b.y);
+                }
             }
         }
     }
@@ -196,125 +210,195 @@ __device__ __forceinline__ void task_range(int64_t tasks, int64_t& u0, int64_t& 
     u1 = tasks * (blockIdx.x + 1) / gridDim.x;
 }
 
-// h = SiLU(s_g * (Q_gate x)) * (s_u * (Q_up x)) for the GEMV groups.
-// Warp task: intermediate rows i0 .. i0+7 (MMA rows 0-7 gate, 8-15 up).
+// One warp, gate/up: intermediate rows i0 .. i0+7 (MMA rows 0-7 gate, 8-15 up)
+// for staged token rows 0 .. nt-1 (nt <= 8 NTILE).
+template <int NTILE, int R>
+__device__ __forceinline__ void gate_up_task(const FfnGroups& g, const Group8& v, int i0, int c0,
+                                             int nt, const __half* act, const float* rs, int lane) {
+    const int t = lane & 3;
+    const int i = i0 + (lane >> 2);
+    float c[NTILE][4];
+#pragma unroll
+    for (int j = 0; j < NTILE; ++j) c[j][0] = c[j][1] = c[j][2] = c[j][3] = 0.0f;
+    mma_rows<NTILE, R>(v.wg + (int64_t)i * g.d, v.wu + (int64_t)i * g.d, g.d, act, lane, c);
+    const float sg = v.sg[i], su = v.su[i];
+#pragma unroll
+    for (int j = 0; j < NTILE; ++j)
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const int tok = 8 * j + 2 * t + q;
+            if (tok < nt) {
+                const float gv = c[j][q] * rs[tok] * sg, uv = c[j][2 + q] * rs[tok] * su;
+                bf16* h = v.shared ? (bf16*)g.h_s + (int64_t)(c0 + tok) * v.inter
+                                   : (bf16*)g.h + (v.row0 + c0 + tok) * v.inter;
+                h[i] = __float2bfloat16_rn(silu_mul(gv, uv));
+            }
+        }
+}
+
+// One warp, down: output rows j0 .. j0+15 for staged token rows 0 .. nt-1.
+template <int NTILE, int R>
+__device__ __forceinline__ void down_task(const FfnGroups& g, const Group8& v, int j0, int c0,
+                                          int nt, const __half* act, const float* rs, int lane) {
+    const int t = lane & 3;
+    const int jr = j0 + (lane >> 2);
+    float c[NTILE][4];
+#pragma unroll
+    for (int j = 0; j < NTILE; ++j) c[j][0] = c[j][1] = c[j][2] = c[j][3] = 0.0f;
+    mma_rows<NTILE, R>(v.wd + (int64_t)jr * v.inter, v.wd + (int64_t)(jr + 8) * v.inter, v.inter,
+                       act, lane, c);
+    const float s0 = v.sd[jr], s1 = v.sd[jr + 8];
+#pragma unroll
+    for (int j = 0; j < NTILE; ++j)
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const int tok = 8 * j + 2 * t + q;
+            if (tok < nt) {
+                bf16* y = v.shared ? (bf16*)g.y_s + (int64_t)(c0 + tok) * g.d
+                                   : (bf16*)g.y + (v.row0 + c0 + tok) * g.d;
+                y[jr] = __float2bfloat16_rn(c[j][q] * rs[tok] * s0);
+                y[jr + 8] = __float2bfloat16_rn(c[j][2 + q] * rs[tok] * s1);
+            }
+        }
+}
+
+// h = SiLU(s_g * (Q_gate x)) * (s_u * (Q_up x)) for the groups of one GEMV
+// list (which = 0: first list, 1: second), up to R token rows per pass; a pass
+// of at most 8 rows runs one MMA per A fragment.
+template <int R>
 __global__ void __launch_bounds__(kG8Threads, 1)
 gemv8_gate_up_kernel(FfnGroups g, const FfnPlanHeader* __restrict__ hdr,
-                     const int32_t* __restrict__ gemv_list) {
+                     const int32_t* __restrict__ list, int which) {
+    constexpr int NT = (R + kG8Tok - 1) / kG8Tok;
     extern __shared__ __align__(16) unsigned char smem8[];
-    float* rs = reinterpret_cast<float*>(smem8);               // [8] 2^e of each token row
-    __half* act = reinterpret_cast<__half*>(smem8 + 64);       // [8][d + pad]
+    float* rs = reinterpret_cast<float*>(smem8);          // [R] 2^e of each token row
+    __half* act = reinterpret_cast<__half*>(smem8 + 64);  // [R][d], swizzled slots
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int gq = lane >> 2, t = lane & 3;
     const int max_inter = g.has_shared && g.Is > g.I ? g.Is : g.I;
     const int tpg = max_inter / 8;  // tasks per group
     int64_t u, u1;
-    task_range((int64_t)hdr->n_gemv * tpg, u, u1);
+    task_range((int64_t)(which ? hdr->n_gemv2 : hdr->n_gemv) * tpg, u, u1);
     while (u < u1) {
         const int a = (int)(u / tpg);
-        const Group8 v = group8(g, gemv_list[a]);
+        const Group8 v = group8(g, list[a]);
         const int64_t seg_end = min(u1, (int64_t)(a + 1) * tpg);
-        for (int c0 = 0; c0 < v.rows; c0 += kG8Tok) {
-            const int nt = min(kG8Tok, v.rows - c0);
+        for (int c0 = 0; c0 < v.rows; c0 += R) {
+            const int nt = min(R, v.rows - c0);
+            const int rows = (NT == 1 || nt <= kG8Tok) ? min(R, kG8Tok) : R;
             __syncthreads();  // earlier readers of act are done
-            stage_f16(act, rs, (const bf16*)g.a_routed, (const bf16*)g.a_shared, v, c0, nt, g.d,
-                      warp, lane);
+            stage_f16(act, rs, (const bf16*)g.a_routed, (const bf16*)g.a_shared, v, c0, nt, rows,
+                      g.d, warp, lane);
             __syncthreads();
             for (int64_t k = u + warp; k < seg_end; k += kG8Warps) {
                 const int i0 = (int)(k - (int64_t)a * tpg) * 8;
                 if (i0 >= v.inter) continue;  // warp-uniform
-                const int i = i0 + gq;
-                float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-                mma_rows(v.wg + (int64_t)i * g.d, v.wu + (int64_t)i * g.d, g.d, act, lane, c);
-                const float sg = v.sg[i], su = v.su[i];
-#pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    const int tok = 2 * t + q;
-                    if (tok < nt) {
-                        const float gv = c[q] * rs[tok] * sg, uv = c[2 + q] * rs[tok] * su;
-                        bf16* h = v.shared ? (bf16*)g.h_s + (int64_t)(c0 + tok) * v.inter
-                                           : (bf16*)g.h + (v.row0 + c0 + tok) * v.inter;
-                        h[i] = __float2bfloat16_rn(silu_mul(gv, uv));
-                    }
-                }
+                if (NT == 1 || nt <= kG8Tok) gate_up_task<1, (R < kG8Tok ? R : kG8Tok)>(g, v, i0, c0, nt, act, rs, lane);
+                else gate_up_task<NT, R>(g, v, i0, c0, nt, act, rs, lane);
             }
         }
         u = seg_end;
     }
 }
 
-// y = s_d * (Q_down h) for the GEMV groups.  Warp task: output rows j0 .. j0+15.
+// y = s_d * (Q_down h) for the groups of one GEMV list, up to R token rows per pass.
+template <int R>
 __global__ void __launch_bounds__(kG8Threads, 1)
 gemv8_down_kernel(FfnGroups g, const FfnPlanHeader* __restrict__ hdr,
-                  const int32_t* __restrict__ gemv_list) {
+                  const int32_t* __restrict__ list, int which) {
+    constexpr int NT = (R + kG8Tok - 1) / kG8Tok;
     extern __shared__ __align__(16) unsigned char smem8[];
     float* rs = reinterpret_cast<float*>(smem8);
-    __half* act = reinterpret_cast<__half*>(smem8 + 64);       // [8][inter + pad]
+    __half* act = reinterpret_cast<__half*>(smem8 + 64);  // [R][inter], swizzled slots
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int gq = lane >> 2, t = lane & 3;
     const int tpg = g.d / 16;
     int64_t u, u1;
-    task_range((int64_t)hdr->n_gemv * tpg, u, u1);
+    task_range((int64_t)(which ? hdr->n_gemv2 : hdr->n_gemv) * tpg, u, u1);
     while (u < u1) {
         const int a = (int)(u / tpg);
-        const Group8 v = group8(g, gemv_list[a]);
+        const Group8 v = group8(g, list[a]);
         const int64_t seg_end = min(u1, (int64_t)(a + 1) * tpg);
-        for (int c0 = 0; c0 < v.rows; c0 += kG8Tok) {
-            const int nt = min(kG8Tok, v.rows - c0);
+        for (int c0 = 0; c0 < v.rows; c0 += R) {
+            const int nt = min(R, v.rows - c0);
+            const int rows = (NT == 1 || nt <= kG8Tok) ? min(R, kG8Tok) : R;
             __syncthreads();
-            stage_f16(act, rs, (const bf16*)g.h, (const bf16*)g.h_s, v, c0, nt, v.inter, warp, lane);
+            stage_f16(act, rs, (const bf16*)g.h, (const bf16*)g.h_s, v, c0, nt, rows, v.inter, warp,
+                      lane);
             __syncthreads();
             for (int64_t k = u + warp; k < seg_end; k += kG8Warps) {
                 const int j0 = (int)(k - (int64_t)a * tpg) * 16;
-                const int j = j0 + gq;
-                float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-                mma_rows(v.wd + (int64_t)j * v.inter, v.wd + (int64_t)(j + 8) * v.inter, v.inter,
-                         act, lane, c);
-                const float s0 = v.sd[j], s1 = v.sd[j + 8];
-#pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    const int tok = 2 * t + q;
-                    if (tok < nt) {
-                        bf16* y = v.shared ? (bf16*)g.y_s + (int64_t)(c0 + tok) * g.d
-                                           : (bf16*)g.y + (v.row0 + c0 + tok) * g.d;
-                        y[j] = __float2bfloat16_rn(c[q] * rs[tok] * s0);
-                        y[j + 8] = __float2bfloat16_rn(c[2 + q] * rs[tok] * s1);
-                    }
-                }
+                if (NT == 1 || nt <= kG8Tok) down_task<1, (R < kG8Tok ? R : kG8Tok)>(g, v, j0, c0, nt, act, rs, lane);
+                else down_task<NT, R>(g, v, j0, c0, nt, act, rs, lane);
             }
         }
         u = seg_end;
     }
 }
 
-size_t gemv8_smem(int n) { return 64 + (size_t)kG8Tok * (n + kG8Pad) * sizeof(__half); }
+size_t gemv8_smem(int n, int rows) { return 64 + (size_t)rows * n * sizeof(__half); }
+
+constexpr int kG8Small = 8;  // rows of the first GEMV list's groups (one MMA column tile)
+
+// Shared memory a launch may use and still leave L1 room for the weight loads
+// in flight (measured: the same kernel streams at ~50% of HBM with a 229 KB
+// carve-out and ~85% with 115 KB).
+constexpr size_t kG8FastSmem = 120 * 1024;
+
+template <int R>
+cudaError_t launch_gu(const FfnGroups& g, const FfnPlanHeader* hdr, const int32_t* list, int which,
+                      cudaStream_t st) {
+    const size_t sm = gemv8_smem(g.d, R);
+    cudaError_t e = cudaFuncSetAttribute(gemv8_gate_up_kernel<R>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    if (e != cudaSuccess) return e;
+    gemv8_gate_up_kernel<R><<<device_sm_count(), kG8Threads, sm, st>>>(g, hdr, list, which);
+    return cudaGetLastError();
+}
+
+template <int R>
+cudaError_t launch_dn(const FfnGroups& g, const FfnPlanHeader* hdr, const int32_t* list, int which,
+                      int max_inter, cudaStream_t st) {
+    const size_t sm = gemv8_smem(max_inter, R);
+    cudaError_t e = cudaFuncSetAttribute(gemv8_down_kernel<R>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    if (e != cudaSuccess) return e;
+    gemv8_down_kernel<R><<<device_sm_count(), kG8Threads, sm, st>>>(g, hdr, list, which);
+    return cudaGetLastError();
+}
 
 }  // namespace
 
 // Groups of at most this many rows take the 8-bit GEMV path (MOE_GEMV8_MAX_ROWS,
-// read on every call; default 8 -- one MMA column per row; 0 sends every group
-// to the tcgen05 path; larger values take several passes of 8 rows).
+// read on every call; default 16 -- two MMA column tiles; 0 sends every group
+// to the tcgen05 path; larger groups take several passes).
 int gemv8_max_rows() {
     const char* s = getenv("MOE_GEMV8_MAX_ROWS");
-    const int x = s ? atoi(s) : kG8Tok;
+    const int x = s ? atoi(s) : kG8Tok * kG8MaxTiles;
     return x < 0 ? 0 : x;
 }
 
-bool gemv8_fits(int widest) { return gemv8_smem(widest) <= kGemv8SmemLimit; }
+bool gemv8_fits(int widest) { return gemv8_smem(widest, kG8Tok) <= kGemv8SmemLimit; }
 
+int gemv8_small_rows() { return kG8Small; }
+
+// First list (groups of 1..8 rows): 8 staged rows, one MMA per A fragment.
+// Second list (9..limit rows): 16 rows per pass where they fit in
+// kG8FastSmem, else passes of 8.  Both lists' gate/up kernels run before the
+// down kernels that read their h.
 cudaError_t launch_ffn_gemv_fp8(const FfnGroups& g, const FfnPlanHeader* hdr, const int32_t* list,
-                                cudaStream_t st) {
+                                int limit, cudaStream_t st) {
     const int max_inter = g.has_shared && g.Is > g.I ? g.Is : g.I;
-    const size_t smem_gu = gemv8_smem(g.d), smem_dn = gemv8_smem(max_inter);
-    cudaError_t e = cudaFuncSetAttribute(gemv8_gate_up_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem_gu);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(gemv8_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_dn);
-    if (e != cudaSuccess) return e;
-    const int sms = device_sm_count();
-    gemv8_gate_up_kernel<<<sms, kG8Threads, smem_gu, st>>>(g, hdr, list);
-    gemv8_down_kernel<<<sms, kG8Threads, smem_dn, st>>>(g, hdr, list);
-    return cudaGetLastError();
+    const int32_t* list2 = list + (g.E + 1);
+    const bool second = limit > kG8Small;
+    const bool gu16 = gemv8_smem(g.d, 2 * kG8Tok) <= kG8FastSmem;
+    const bool dn16 = gemv8_smem(max_inter, 2 * kG8Tok) <= kG8FastSmem;
+    cudaError_t e = launch_gu<kG8Small>(g, hdr, list, 0, st);
+    if (e == cudaSuccess && second)
+        e = gu16 ? launch_gu<2 * kG8Tok>(g, hdr, list2, 1, st) : launch_gu<kG8Tok>(g, hdr, list2, 1, st);
+    if (e == cudaSuccess) e = launch_dn<kG8Small>(g, hdr, list, 0, max_inter, st);
+    if (e == cudaSuccess && second)
+        e = dn16 ? launch_dn<2 * kG8Tok>(g, hdr, list2, 1, max_inter, st)
+                 : launch_dn<kG8Tok>(g, hdr, list2, 1, max_inter, st);
+    return e;
 }
 
 }  // namespace moe

@@ -16,10 +16,10 @@ struct DevError;
 // expert g with rows [offsets[g], offsets[g+1]) of the permuted row space;
 // group E (when present) is the shared expert, whose rows are the T tokens.
 struct FfnPlanHeader {
-    int32_t n_gemv;    // groups handled by the streaming GEMV kernels
+    int32_t n_gemv;    // groups handled by the streaming GEMV kernels (first list)
     int32_t n_mtiles;  // 128-row tiles of the single-SM tensor-core GEMM
     int32_t n_ptiles;  // 256-row tiles of the CTA-pair tensor-core GEMM
-    int32_t pad;
+    int32_t n_gemv2;   // second GEMV list (groups above the small-row split), or 0
 };
 
 // One routed/shared expert group as the FFN kernels see it.
@@ -84,11 +84,13 @@ cudaError_t launch_gather_rows(const moe_shape& s, const void* x, const int32_t*
 
 // ---- ffn_plan + ffn_gemv.cu ----
 int gemv_max_rows();  // groups with at most this many rows take the GEMV path
-// mtile_list holds 2 * max_mtiles entries: single-SM tiles, then pair tiles
-// (none when allow_pair is false).
+// gemv_list holds 2 * (E + 1) entries: groups of 1..small_rows rows (all GEMV
+// groups when small_rows is 0), then from entry E + 1 on the groups of
+// small_rows + 1 .. gemv_limit rows.  mtile_list holds 2 * max_mtiles
+// entries: single-SM tiles, then pair tiles (none when allow_pair is false).
 cudaError_t launch_ffn_plan(const FfnGroups& g, int dtype, FfnPlanHeader* hdr,
                             int32_t* gemv_list, int4* mtile_list, int max_mtiles,
-                            int gemv_limit, bool allow_pair, cudaStream_t st);
+                            int gemv_limit, bool allow_pair, int small_rows, cudaStream_t st);
 cudaError_t launch_ffn_gemv(const FfnGroups& g, int dtype, const FfnPlanHeader* hdr,
                             const int32_t* gemv_list, cudaStream_t st);
 
@@ -112,10 +114,11 @@ cudaError_t launch_ffn_tc_fp8(const FfnGroups& g, const FfnPlanHeader* hdr, cons
 // ---- ffn_gemv_fp8.cu (E4M3 weights, small groups) ----
 int gemv8_max_rows();  // groups with at most this many rows take the 8-bit GEMV
 bool gemv8_fits(int widest);  // its staged activation rows of this width fit in shared memory
-constexpr int kGemv8Rows = 8;  // activation rows per pass of the 8-bit GEMV
+int gemv8_small_rows();       // groups up to this size go to the first GEMV list
 constexpr size_t kGemv8SmemLimit = 232448;
+// both GEMV lists of the plan (limit: the plan's GEMV row limit)
 cudaError_t launch_ffn_gemv_fp8(const FfnGroups& g, const FfnPlanHeader* hdr, const int32_t* list,
-                                cudaStream_t st);
+                                int limit, cudaStream_t st);
 
 // ---- quant.cu ----
 cudaError_t launch_quantize_fp8_rows(int64_t rows, int64_t cols, int dtype, const void* w,

@@ -135,7 +135,7 @@ WsLayout ws_layout(const moe_shape& s) {
     L.tok_of = take(sizeof(int32_t) * n);
     L.blk_hist = take(sizeof(int32_t) * (size_t)L.dispatch_blocks * E);
     L.plan = take(sizeof(FfnPlanHeader));
-    L.gemv_list = take(sizeof(int32_t) * (E + 1));
+    L.gemv_list = take(sizeof(int32_t) * 2 * (E + 1));  // two GEMV lists
     L.mtile_list = take(sizeof(int4) * 2 * (size_t)L.max_mtiles);  // single, then pair tiles
     L.x_perm = take(es * n * d);
     L.h = take(es * n * I);
@@ -273,7 +273,7 @@ moe_status moe_expert_ffn(const moe_shape* shape, const void* x_perm, const int3
     FfnPlanHeader* hdr = at<FfnPlanHeader>(workspace, L.plan);
     int32_t* glist = at<int32_t>(workspace, L.gemv_list);
     int4* mtiles = at<int4>(workspace, L.mtile_list);
-    e = launch_ffn_plan(g, s.dtype, hdr, glist, mtiles, L.max_mtiles, gemv_limit(), true, cs);
+    e = launch_ffn_plan(g, s.dtype, hdr, glist, mtiles, L.max_mtiles, gemv_limit(), true, 0, cs);
     if (e == cudaSuccess && gemv_possible(s)) e = launch_ffn_gemv(g, s.dtype, hdr, glist, cs);
     if (e == cudaSuccess && need_tc)
         e = launch_ffn_tc(g, hdr, mtiles, L.max_mtiles, tc_pair_possible(rows), err, cs);
@@ -381,7 +381,7 @@ moe_status moe_forward(const moe_shape* shape, const void* x, const void* w_g, c
     FfnPlanHeader* hdr = at<FfnPlanHeader>(workspace, L.plan);
     int32_t* glist = at<int32_t>(workspace, L.gemv_list);
     int4* mtiles = at<int4>(workspace, L.mtile_list);
-    e = launch_ffn_plan(g, s.dtype, hdr, glist, mtiles, L.max_mtiles, gemv_limit(), true, cs);
+    e = launch_ffn_plan(g, s.dtype, hdr, glist, mtiles, L.max_mtiles, gemv_limit(), true, 0, cs);
     if (e == cudaSuccess && gemv_possible(s)) e = launch_ffn_gemv(g, s.dtype, hdr, glist, cs);
     // a group has at most T rows (a token picks an expert once)
     if (e == cudaSuccess && need_tc)
@@ -446,8 +446,9 @@ moe_status moe_expert_ffn_fp8(const moe_shape* shape, const void* x_perm, const 
     int32_t* glist = at<int32_t>(workspace, L.gemv_list);
     int4* mtiles = at<int4>(workspace, L.mtile_list);
     const int lim = gemv8_limit(s);
-    e = launch_ffn_plan(g, s.dtype, hdr, glist, mtiles, L.max_mtiles, lim, false, cs);
-    if (e == cudaSuccess && lim > 0) e = launch_ffn_gemv_fp8(g, hdr, glist, cs);
+    e = launch_ffn_plan(g, s.dtype, hdr, glist, mtiles, L.max_mtiles, lim, false,
+                        gemv8_small_rows(), cs);
+    if (e == cudaSuccess && lim > 0) e = launch_ffn_gemv_fp8(g, hdr, glist, lim, cs);
     // a group has at most T*K rows here (the offsets are the caller's)
     if (e == cudaSuccess && (int64_t)s.T * s.K > lim)
         e = launch_ffn_tc_fp8(g, hdr, mtiles, L.max_mtiles, err, cs);
@@ -534,8 +535,9 @@ moe_status moe_forward_fp8(const moe_shape* shape, const void* x, const void* w_
     int32_t* glist = at<int32_t>(workspace, L.gemv_list);
     int4* mtiles = at<int4>(workspace, L.mtile_list);
     const int lim = gemv8_limit(s);
-    e = launch_ffn_plan(g, s.dtype, hdr, glist, mtiles, L.max_mtiles, lim, false, cs);
-    if (e == cudaSuccess && lim > 0) e = launch_ffn_gemv_fp8(g, hdr, glist, cs);
+    e = launch_ffn_plan(g, s.dtype, hdr, glist, mtiles, L.max_mtiles, lim, false,
+                        gemv8_small_rows(), cs);
+    if (e == cudaSuccess && lim > 0) e = launch_ffn_gemv_fp8(g, hdr, glist, lim, cs);
     // a group has at most T rows (a token picks an expert once; the shared group has T)
     if (e == cudaSuccess && s.T > lim) e = launch_ffn_tc_fp8(g, hdr, mtiles, L.max_mtiles, err, cs);
     if (e != cudaSuccess) return MOE_ERR_CUDA;

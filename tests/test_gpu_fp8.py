@@ -83,6 +83,7 @@ def _expert_ffn_case(moe, counts, d, I, seed=0):
     ([600, 257, 1, 129], 384, 640),                  # several m-tiles per group, 5 n-blocks
     ([1, 2, 1, 1, 3, 1, 1, 2], 1024, 256),           # decode-like: a few rows per expert (GEMV)
     ([8, 9, 0, 7, 16, 17], 128, 128),                # around the GEMV limit, narrowest shapes
+    ([16, 15, 1, 33], 7168, 256),                    # DeepSeek-width rows, 16-row passes
 ])
 def test_expert_ffn_fp8_matches_oracle(moe, counts, d, I):
     y, ref = _expert_ffn_case(moe, counts, d, I)
@@ -113,11 +114,12 @@ def _check_rows(y, ref):
 
 
 @pytest.mark.parametrize("router", ["softmax", "sigmoid"])
-@pytest.mark.parametrize("gemv8", ["0", "8", "16"])
+@pytest.mark.parametrize("gemv8", ["0", "8", "16", "40"])
 def test_forward_fp8_small_layer_all_tokens(moe, router, gemv8, monkeypatch):
     """Groups of ~11 rows and a 45-row shared group: all on the tensor cores
-    (limit 0), small groups on the 8-bit GEMV (default 8), or every routed
-    group on the GEMV in two passes of at most 8 rows (limit 16)."""
+    (limit 0), part of the routed groups on the 8-bit GEMV (8), every routed
+    group in one 16-row pass (16, the default), or everything including the
+    shared group in passes of 16 rows (40)."""
     monkeypatch.setenv("MOE_GEMV8_MAX_ROWS", gemv8)
     cfg = mi.LayerConfig("fp8_small", T=45, d=256, E=12, K=3, I=384, Is=256, router=router,
                          weights="e4m3")
