@@ -71,6 +71,70 @@ router_gemv_kernel(const T* __restrict__ x, const T* __restrict__ w_g, float* __
     }
 }
 
+// Few experts, many tokens: part[t][e] = sum_k x[t][k] * w_g[e][k] with one
+// warp per TT tokens and all E <= EM experts, so x is streamed from HBM once
+// and the small W_g (E rows) is served from L1.  (The split-K kernel above
+// reads x once per expert, which for E = 8 and thousands of tokens costs
+// ~8x the x traffic.)
+constexpr int kRouterTokWarps = 4;
+template <typename T, int EM, int TT>
+__global__ void __launch_bounds__(kRouterTokWarps * 32)
+router_tokens_kernel(const T* __restrict__ x, const T* __restrict__ w_g, float* __restrict__ part,
+                     int Tn, int d, int E) {
+    constexpr int V = Elem<T>::kPerVec;
+    constexpr int kUnroll = EM <= 8 ? 2 : 1;  // steps whose loads are in flight together
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int nvec = d / V;
+    const int64_t units = (Tn + TT - 1) / TT;
+    for (int64_t u = (int64_t)blockIdx.x * kRouterTokWarps + warp; u < units;
+         u += (int64_t)gridDim.x * kRouterTokWarps) {
+        const int t0 = (int)(u * TT);
+        const int nt = min(TT, Tn - t0);
+        float acc[TT][EM];
+#pragma unroll
+        for (int t = 0; t < TT; ++t)
+#pragma unroll
+            for (int e = 0; e < EM; ++e) acc[t][e] = 0.f;
+#pragma unroll kUnroll
+        for (int v = lane; v < nvec; v += 32) {
+            // every load of the step first (x from HBM, W_g from L1), then the FMAs
+            uint4 xv[TT], wv[EM];
+#pragma unroll
+            for (int t = 0; t < TT; ++t)
+                xv[t] = t < nt ? ld_stream(x + (int64_t)(t0 + t) * d + (int64_t)v * V)
+                               : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int e = 0; e < EM; ++e)
+                wv[e] = e < E ? ld_ro(w_g + (int64_t)e * d + (int64_t)v * V) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int t = 0; t < TT; ++t) {
+                float xf[V];
+                unpack(xv[t], xf, (const T*)nullptr);
+#pragma unroll
+                for (int e = 0; e < EM; ++e) {
+                    float wf[V];
+                    unpack(wv[e], wf, (const T*)nullptr);
+#pragma unroll
+                    for (int q = 0; q < V; ++q) acc[t][e] = fmaf(wf[q], xf[q], acc[t][e]);
+                }
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < TT; ++t)
+#pragma unroll
+            for (int e = 0; e < EM; ++e) {
+                if (e < E) {
+                    const float r = warp_sum(acc[t][e]);
+                    if (lane == 0 && t < nt) part[(int64_t)(t0 + t) * E + e] = r;
+                }
+            }
+    }
+}
+
+// the token-major kernel serves E <= 32 from this many tokens on
+constexpr int kRouterTokMinT = 256;
+
 struct Cand {
     float key;  // what the selection compares
     float val;  // what the weights are formed from
@@ -160,15 +224,37 @@ topk_route_kernel(const float* __restrict__ part, int splits, const float* __res
 
 }  // namespace
 
-// about 224 16-byte vectors (7 per lane) of a W_g row per split
+// about 224 16-byte vectors (7 per lane) of a W_g row per split; one split
+// (full sums) on the token-major path
 int router_splits_for(const moe_shape& s) {
+    if (s.E <= 32 && s.T >= kRouterTokMinT) return 1;
     const int V = s.dtype == MOE_BF16 ? 8 : 4;
     int splits = (s.d / V) / 224;
     return splits < 1 ? 1 : (splits > kMaxSplits ? kMaxSplits : splits);
 }
 
+template <typename T>
+cudaError_t launch_router_tokens(const moe_shape& s, const void* x, const void* w_g, float* part,
+                                 cudaStream_t st) {
+    const int tt = 2;
+    int64_t blocks = ceil_div(ceil_div(s.T, tt), kRouterTokWarps);
+    const int64_t cap = (int64_t)device_sm_count() * 16;
+    if (blocks > cap) blocks = cap;
+    const dim3 grid((unsigned)blocks), block(kRouterTokWarps * 32);
+    if (s.E <= 8)
+        router_tokens_kernel<T, 8, 2><<<grid, block, 0, st>>>((const T*)x, (const T*)w_g, part, s.T, s.d, s.E);
+    else if (s.E <= 16)
+        router_tokens_kernel<T, 16, 2><<<grid, block, 0, st>>>((const T*)x, (const T*)w_g, part, s.T, s.d, s.E);
+    else
+        router_tokens_kernel<T, 32, 2><<<grid, block, 0, st>>>((const T*)x, (const T*)w_g, part, s.T, s.d, s.E);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_router_gemv(const moe_shape& s, const void* x, const void* w_g, float* part,
                                int splits, cudaStream_t st) {
+    if (splits == 1 && s.E <= 32 && s.T >= kRouterTokMinT)
+        return s.dtype == MOE_BF16 ? launch_router_tokens<bf16>(s, x, w_g, part, st)
+                                   : launch_router_tokens<float>(s, x, w_g, part, st);
     const int64_t units = ceil_div(s.T, kRouterTok) * (int64_t)s.E * splits;
     int64_t blocks = ceil_div(units, kRouterWarps);
     const int64_t cap = (int64_t)device_sm_count() * 8;

@@ -63,12 +63,20 @@ def test_route_bit_exact_with_zipf_bias_and_all_ties(moe):
     assert np.allclose(w, 1 / 8, rtol=1e-7)
 
 
+SMALL_E = {f"smallE{E}_{dt}_T{T}": mi.LayerConfig(f"smallE{E}_{dt}", T=T, d=192, E=E, K=min(E, 4),
+                                                     I=64, dtype=dt)
+           for E, dt, T in [(3, "bf16", 257), (8, "f32", 300), (12, "bf16", 300),
+                            (20, "f32", 511), (32, "bf16", 256)]}
+
+
 @pytest.mark.parametrize("name,T", [("tiny_f32", None), ("dsv3_decode", None),
                                     ("dsv3_prefill_zipf", 512), ("dsv3_sweep_T4096", None),
-                                    ("mixtral_prefill", 256)])
+                                    ("mixtral_prefill", 256), ("mixtral_prefill", 4096),
+                                    *[(n, None) for n in SMALL_E]])
 def test_route_from_x(moe, name, T):
-    """Scores from x . w_g (GEMV router, or the tensor-core router for large bf16 batches)."""
-    cfg = mi.CONFIGS[name]
+    """Scores from x . w_g: split-K GEMV router (few tokens), token-major router
+    (E <= 32, T >= 256), or the tensor-core router (large bf16 batches, E >= 64)."""
+    cfg = SMALL_E[name] if name in SMALL_E else mi.CONFIGS[name]
     if T is not None:
         cfg = cfg.with_T(T)
     L = Layer(cfg, only={"w_g"})
