@@ -120,8 +120,13 @@ def launches_per_forward(cfg, gemv_limit: int = 0) -> int:
     ones too when a group can hold more rows than one 128-row tile (or, with
     MOE_PAIR_MIN_ROWS set, at least that many rows), combine."""
     if cfg.weights == "e4m3":
-        # router + top-K, 3 dispatch kernels, row gather, plan, gate/up, down, combine
-        return 2 + 3 + 1 + 1 + 2 + 1
+        # router + top-K, 3 dispatch kernels, row gather, plan, the 8-bit GEMV
+        # (gate/up and down for each of its two group lists), the tcgen05
+        # gate/up and down when a group can exceed the GEMV limit, combine
+        limit = int(os.environ.get("MOE_GEMV8_MAX_ROWS", "16"))
+        gemv = (2 if limit > 0 else 0) + (2 if limit > 8 else 0)
+        tc = 2 if cfg.T > limit else 0
+        return 2 + 3 + 1 + 1 + gemv + tc + 1
     need_tc = cfg.dtype == "bf16" and cfg.T > gemv_limit
     gather = need_tc and cfg.T > int(os.environ.get("MOE_GATHER_MAX_ROWS", "0"))
     gemv = cfg.dtype == "f32" or gemv_limit > 0
@@ -432,7 +437,7 @@ def time_expert_ffn(moe, cfg, x, p, bias, stream, steps: int, n_active: int) -> 
 # ncu capture per workload (profiles/ffn_stage_traffic_<workload>.md), valid only for
 # the ffn_tc.cu source it was taken on (sha256 prefix).
 STAGE_TRAFFIC = {
-    "mixtral_prefill": {"bytes": 4507861760, "ffn_tc_sha256": "50a74337d372d7dc"},
+    "mixtral_prefill": {"bytes": 6252355072, "ffn_tc_sha256": "2f38323651d02d0c"},
 }
 
 
@@ -573,7 +578,8 @@ def bench_all(moe, peaks, args) -> list:
     res = []
     for name in ("tiny_f32", "mixtral_prefill", "dsv3_decode", "dsv3_prefill_zipf",
                  *[f"dsv3_sweep_T{t}" for t in mi.SWEEP_T], "dsv3_decode_sigmoid",
-                 "dsv3_decode_fp8", "mixtral_prefill_fp8"):
+                 "dsv3_decode_fp8", "dsv3_sweep_fp8_T64", "dsv3_sweep_fp8_T512",
+                 "mixtral_prefill_fp8"):
         cfg = mi.CONFIGS[name]
         res.append(bench_workload(moe, cfg, peaks, steps=max(10, args.steps),
                                   graph=cfg.T <= 64))
