@@ -22,6 +22,8 @@ __global__ void __launch_bounds__(256)
 combine_kernel(const T* __restrict__ y_perm, const int32_t* __restrict__ inv_perm,
                const float* __restrict__ topk_w, const T* __restrict__ y_shared, T* __restrict__ y,
                int d, int K, int64_t n_rows) {
+    pdl_wait();
+    pdl_trigger();
     constexpr int V = Elem<T>::kPerVec;
     const int nvec = d / V;
     const int t = blockIdx.x;
@@ -68,12 +70,10 @@ cudaError_t launch_combine(const moe_shape& s, const void* y_perm, const int32_t
     const dim3 grid((unsigned)s.T, (unsigned)ceil_div(nvec, 256));
     const int64_t rows = (int64_t)s.T * s.K;
     if (s.dtype == MOE_BF16)
-        combine_kernel<bf16><<<grid, 256, 0, st>>>((const bf16*)y_perm, inv_perm, topk_w,
-                                                   (const bf16*)y_shared, (bf16*)y, s.d, s.K, rows);
-    else
-        combine_kernel<float><<<grid, 256, 0, st>>>((const float*)y_perm, inv_perm, topk_w,
-                                                    (const float*)y_shared, (float*)y, s.d, s.K, rows);
-    return cudaGetLastError();
+        return launch_pdl(combine_kernel<bf16>, grid, dim3(256), 0, st, (const bf16*)y_perm,
+                          inv_perm, topk_w, (const bf16*)y_shared, (bf16*)y, s.d, s.K, rows);
+    return launch_pdl(combine_kernel<float>, grid, dim3(256), 0, st, (const float*)y_perm, inv_perm,
+                      topk_w, (const float*)y_shared, (float*)y, s.d, s.K, rows);
 }
 
 }  // namespace moe

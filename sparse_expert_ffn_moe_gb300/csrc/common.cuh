@@ -78,4 +78,13 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
 
 __host__ __device__ __forceinline__ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// Programmatic dependent launch.  Every kernel calls pdl_wait() before it
+// touches global memory that an earlier kernel of the stream writes or reads
+// (the wait returns once the preceding grid has completed and its writes are
+// visible; without a programmatic dependency it returns at once), and
+// pdl_trigger() to let the next kernel of the stream be scheduled onto SMs as
+// they free up, so its launch and prologue overlap this kernel's tail.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
 }  // namespace moe

@@ -33,6 +33,8 @@ __device__ __forceinline__ bool valid_expert(int e, int E) { return e >= 0 && e 
 __global__ void __launch_bounds__(kChunk)
 dispatch_hist_kernel(const int32_t* __restrict__ idx, int64_t n, int E,
                      int32_t* __restrict__ blk_hist, DevError* err) {
+    pdl_wait();
+    pdl_trigger();
     extern __shared__ int32_t hist[];
     for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
     __syncthreads();
@@ -79,6 +81,8 @@ __device__ int32_t block_exclusive_scan(int32_t v, int32_t* warp_tot, int32_t* t
 __global__ void __launch_bounds__(1024)
 dispatch_scan_kernel(int32_t* __restrict__ blk_hist, int nb, int E, int32_t* __restrict__ counts,
                      int32_t* __restrict__ offsets) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ int32_t warp_tot[32];
     __shared__ int32_t total;
     const int e = threadIdx.x;
@@ -103,6 +107,8 @@ __global__ void __launch_bounds__(kChunk)
 dispatch_scatter_kernel(const int32_t* __restrict__ idx, int64_t n, int E, int K,
                         const int32_t* __restrict__ blk_base, int32_t* __restrict__ perm,
                         int32_t* __restrict__ inv_perm, int32_t* __restrict__ tok_of) {
+    pdl_wait();
+    pdl_trigger();
     extern __shared__ int32_t wcnt[];  // [32 warps][E]: counts, then exclusive prefix over warps
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     for (int i = threadIdx.x; i < 32 * E; i += blockDim.x) wcnt[i] = 0;
@@ -141,6 +147,8 @@ dispatch_scatter_kernel(const int32_t* __restrict__ idx, int64_t n, int E, int K
 __global__ void __launch_bounds__(256)
 gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ inv_perm,
                    uint4* __restrict__ x_perm, int Tn, int K, int vec_per_row, int64_t n_rows) {
+    pdl_wait();
+    pdl_trigger();
     const int lane = threadIdx.x & 31;
     for (int64_t t = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); t < Tn;
          t += (int64_t)gridDim.x * 8) {
@@ -177,15 +185,19 @@ cudaError_t launch_dispatch(const moe_shape& s, const int32_t* topk_idx, int32_t
     const size_t hist_smem = (size_t)s.E * sizeof(int32_t);
     const size_t scat_smem = (size_t)32 * s.E * sizeof(int32_t);
     // the scatter kernel's per-warp table needs up to 128 KB of shared memory
-    cudaError_t ae = cudaFuncSetAttribute(dispatch_scatter_kernel,
-                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          (int)(32 * 1024 * sizeof(int32_t)));
-    if (ae != cudaSuccess) return ae;
-    dispatch_hist_kernel<<<nb, kChunk, hist_smem, st>>>(topk_idx, n, s.E, blk_hist, err);
-    dispatch_scan_kernel<<<1, 1024, 0, st>>>(blk_hist, nb, s.E, counts, offsets);
-    dispatch_scatter_kernel<<<nb, kChunk, scat_smem, st>>>(topk_idx, n, s.E, s.K, blk_hist, perm,
-                                                           inv_perm, tok_of);
-    return cudaGetLastError();
+    cudaError_t e = cudaFuncSetAttribute(dispatch_scatter_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)(32 * 1024 * sizeof(int32_t)));
+    if (e == cudaSuccess)
+        e = launch_pdl(dispatch_hist_kernel, dim3(nb), dim3(kChunk), hist_smem, st, topk_idx, n,
+                       s.E, blk_hist, err);
+    if (e == cudaSuccess)
+        e = launch_pdl(dispatch_scan_kernel, dim3(1), dim3(1024), 0, st, blk_hist, nb, s.E, counts,
+                       offsets);
+    if (e == cudaSuccess)
+        e = launch_pdl(dispatch_scatter_kernel, dim3(nb), dim3(kChunk), scat_smem, st, topk_idx, n,
+                       s.E, s.K, blk_hist, perm, inv_perm, tok_of);
+    return e;
 }
 
 cudaError_t launch_gather_rows(const moe_shape& s, const void* x, const int32_t* inv_perm,
@@ -197,9 +209,8 @@ cudaError_t launch_gather_rows(const moe_shape& s, const void* x, const int32_t*
     const int64_t cap = (int64_t)device_sm_count() * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    gather_rows_kernel<<<(unsigned)blocks, 256, 0, st>>>((const uint4*)x, inv_perm, (uint4*)x_perm,
-                                                         s.T, s.K, vpr, rows);
-    return cudaGetLastError();
+    return launch_pdl(gather_rows_kernel, dim3((unsigned)blocks), dim3(256), 0, st, (const uint4*)x,
+                      inv_perm, (uint4*)x_perm, s.T, s.K, vpr, rows);
 }
 
 }  // namespace moe

@@ -67,6 +67,8 @@ __global__ void __launch_bounds__(1024)
 ffn_plan_kernel(const int32_t* __restrict__ offsets, int E, int has_shared, int T, int limit,
                 int small, int single_m, int pair_min, int pair_m, FfnPlanHeader* __restrict__ hdr,
                 int32_t* __restrict__ gemv_list, int4* __restrict__ mtile_list, int max_mtiles) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ int32_t sh[32];
     __shared__ int32_t tot_g, tot_g2, tot_s, tot_p, base_g, base_g2, base_s, base_p;
     if (threadIdx.x == 0) { base_g = 0; base_g2 = 0; base_s = 0; base_p = 0; }
@@ -154,6 +156,8 @@ template <typename T, int MT, int U>
 __global__ void __launch_bounds__(kThreads)
 gemv_gate_up_kernel(FfnGroups g, const FfnPlanHeader* __restrict__ hdr,
                     const int32_t* __restrict__ gemv_list) {
+    pdl_wait();
+    pdl_trigger();
     constexpr int V = Elem<T>::kPerVec;
     extern __shared__ uint4 xs[];  // [MT][d / V]
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -242,6 +246,8 @@ template <typename T, int MT, int U>
 __global__ void __launch_bounds__(kThreads)
 gemv_down_kernel(FfnGroups g, const FfnPlanHeader* __restrict__ hdr,
                  const int32_t* __restrict__ gemv_list) {
+    pdl_wait();
+    pdl_trigger();
     constexpr int V = Elem<T>::kPerVec;
     extern __shared__ uint4 hs[];  // [MT][inter / V]
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -327,9 +333,11 @@ cudaError_t launch_gemv_t(const FfnGroups& g, const FfnPlanHeader* hdr, const in
     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_dn, gemv_down_kernel<T, MT, U>, kThreads,
                                                   smem_dn);
     const int sms = device_sm_count();
-    gemv_gate_up_kernel<T, MT, U><<<sms * (occ_gu > 0 ? occ_gu : 1), kThreads, smem_gu, st>>>(g, hdr, list);
-    gemv_down_kernel<T, MT, U><<<sms * (occ_dn > 0 ? occ_dn : 1), kThreads, smem_dn, st>>>(g, hdr, list);
-    return cudaGetLastError();
+    e = launch_pdl(gemv_gate_up_kernel<T, MT, U>, dim3(sms * (occ_gu > 0 ? occ_gu : 1)),
+                   dim3(kThreads), smem_gu, st, g, hdr, list);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(gemv_down_kernel<T, MT, U>, dim3(sms * (occ_dn > 0 ? occ_dn : 1)),
+                      dim3(kThreads), smem_dn, st, g, hdr, list);
 }
 
 }  // namespace
@@ -352,11 +360,9 @@ cudaError_t launch_ffn_plan(const FfnGroups& g, int dtype, FfnPlanHeader* hdr, i
     const int limit = dtype == MOE_F32 ? 0x7fffffff : gemv_limit;
     // a pair threshold no group can reach keeps every group on single tiles
     const int pair_min = allow_pair ? tc_pair_min_rows() : 0x7fffffff;
-    ffn_plan_kernel<<<1, 1024, 0, st>>>(g.offsets, g.E, g.has_shared, g.T, limit, small_rows,
-                                        tc_tile_rows(false),
-                                        pair_min, tc_tile_rows(true), hdr, gemv_list,
-                                        mtile_list, max_mtiles);
-    return cudaGetLastError();
+    return launch_pdl(ffn_plan_kernel, dim3(1), dim3(1024), 0, st, g.offsets, g.E, g.has_shared, g.T,
+                      limit, small_rows, tc_tile_rows(false), pair_min, tc_tile_rows(true), hdr,
+                      gemv_list, mtile_list, max_mtiles);
 }
 
 cudaError_t launch_ffn_gemv(const FfnGroups& g, int dtype, const FfnPlanHeader* hdr,

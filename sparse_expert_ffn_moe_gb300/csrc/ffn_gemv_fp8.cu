@@ -269,6 +269,8 @@ template <int R>
 __global__ void __launch_bounds__(kG8Threads, 1)
 gemv8_gate_up_kernel(FfnGroups g, const FfnPlanHeader* __restrict__ hdr,
                      const int32_t* __restrict__ list, int which) {
+    pdl_wait();
+    pdl_trigger();
     constexpr int NT = (R + kG8Tok - 1) / kG8Tok;
     extern __shared__ __align__(16) unsigned char smem8[];
     float* rs = reinterpret_cast<float*>(smem8);          // [R] 2^e of each token row
@@ -305,6 +307,8 @@ template <int R>
 __global__ void __launch_bounds__(kG8Threads, 1)
 gemv8_down_kernel(FfnGroups g, const FfnPlanHeader* __restrict__ hdr,
                   const int32_t* __restrict__ list, int which) {
+    pdl_wait();
+    pdl_trigger();
     constexpr int NT = (R + kG8Tok - 1) / kG8Tok;
     extern __shared__ __align__(16) unsigned char smem8[];
     float* rs = reinterpret_cast<float*>(smem8);
@@ -350,8 +354,8 @@ cudaError_t launch_gu(const FfnGroups& g, const FfnPlanHeader* hdr, const int32_
     cudaError_t e = cudaFuncSetAttribute(gemv8_gate_up_kernel<R>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (e != cudaSuccess) return e;
-    gemv8_gate_up_kernel<R><<<device_sm_count(), kG8Threads, sm, st>>>(g, hdr, list, which);
-    return cudaGetLastError();
+    return launch_pdl(gemv8_gate_up_kernel<R>, dim3(device_sm_count()), dim3(kG8Threads), sm, st, g, hdr, list,
+                      which);
 }
 
 template <int R>
@@ -361,8 +365,8 @@ cudaError_t launch_dn(const FfnGroups& g, const FfnPlanHeader* hdr, const int32_
     cudaError_t e = cudaFuncSetAttribute(gemv8_down_kernel<R>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (e != cudaSuccess) return e;
-    gemv8_down_kernel<R><<<device_sm_count(), kG8Threads, sm, st>>>(g, hdr, list, which);
-    return cudaGetLastError();
+    return launch_pdl(gemv8_down_kernel<R>, dim3(device_sm_count()), dim3(kG8Threads), sm, st, g, hdr, list,
+                      which);
 }
 
 }  // namespace

@@ -303,10 +303,7 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
     const uint32_t rank = PAIR ? ptx::cluster_ctarank() : 0u;  // 0 issues the MMAs
     const int unit = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
     const int n_units = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
-    const int list_len = p.dense_rows > 0
-        ? (p.dense_rows + S::kTileRows - 1) / S::kTileRows
-        : min(PAIR ? p.hdr->n_ptiles : p.hdr->n_mtiles, p.max_mtiles);
-    const int n_tiles = list_len * p.NB;
+    pdl_trigger();
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -362,6 +359,12 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
     cta_sync_all<PAIR>();  // barriers initialised (in both CTAs of a pair), tensor memory allocated
     ptx::tc_fence_after();
     const uint32_t tmem = ctl->tmem_base;
+    // the prologue above overlaps the previous kernel; its outputs (plan, operands) are read below
+    pdl_wait();
+    const int list_len = p.dense_rows > 0
+        ? (p.dense_rows + S::kTileRows - 1) / S::kTileRows
+        : min(PAIR ? p.hdr->n_ptiles : p.hdr->n_mtiles, p.max_mtiles);
+    const int n_tiles = list_len * p.NB;
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer (warp 0)
@@ -861,17 +864,21 @@ cudaError_t launch_tc(const TcParams& p, cudaStream_t st) {
         cfg.blockDim = dim3(kThreadsTc);
         cfg.dynamicSmemBytes = kSmemBytes;
         cfg.stream = st;
-        cudaLaunchAttribute attr[1];
+        cudaLaunchAttribute attr[2];
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = 2;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
         cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        cfg.numAttrs = 2;
         e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel<EPI, PAIR>, p);
         if (e != cudaSuccess) return e;
     } else {
-        tc_gemm_kernel<EPI, PAIR, W8><<<units, W8 ? kThreadsW8 : kThreadsTc, smem, st>>>(p);
+        e = launch_pdl(tc_gemm_kernel<EPI, PAIR, W8>, dim3(units), dim3(W8 ? kThreadsW8 : kThreadsTc),
+                       smem, st, p);
+        if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
 }

@@ -92,6 +92,11 @@ moe_status check_fp8_weights(const moe_fp8_experts* w, bool shared) {
 
 }  // namespace
 
+bool pdl_enabled() {
+    const char* e = getenv("MOE_PDL");
+    return !(e && e[0] == '0');
+}
+
 int device_sm_count() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 1;

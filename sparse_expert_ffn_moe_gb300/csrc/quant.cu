@@ -48,6 +48,8 @@ template <typename T>
 __global__ void __launch_bounds__(kQuantThreads)
 quantize_rows_kernel(const T* __restrict__ w, uint8_t* __restrict__ codes,
                      float* __restrict__ scales, int64_t cols) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ float red[kQuantThreads / 32];
     const int64_t r = blockIdx.x;
     const T* row = w + r * cols;
@@ -93,10 +95,10 @@ cudaError_t launch_quantize_fp8_rows(int64_t rows, int64_t cols, int dtype, cons
                                      uint8_t* codes, float* scales, cudaStream_t st) {
     if (rows <= 0) return cudaSuccess;
     if (dtype == MOE_BF16)
-        quantize_rows_kernel<bf16><<<(unsigned)rows, kQuantThreads, 0, st>>>((const bf16*)w, codes, scales, cols);
-    else
-        quantize_rows_kernel<float><<<(unsigned)rows, kQuantThreads, 0, st>>>((const float*)w, codes, scales, cols);
-    return cudaGetLastError();
+        return launch_pdl(quantize_rows_kernel<bf16>, dim3((unsigned)rows), dim3(kQuantThreads), 0,
+                          st, (const bf16*)w, codes, scales, cols);
+    return launch_pdl(quantize_rows_kernel<float>, dim3((unsigned)rows), dim3(kQuantThreads), 0, st,
+                      (const float*)w, codes, scales, cols);
 }
 
 }  // namespace moe

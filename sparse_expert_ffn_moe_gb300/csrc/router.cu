@@ -29,6 +29,8 @@ template <typename T>
 __global__ void __launch_bounds__(kRouterWarps * 32)
 router_gemv_kernel(const T* __restrict__ x, const T* __restrict__ w_g, float* __restrict__ part,
                    int Tn, int d, int E, int splits) {
+    pdl_wait();
+    pdl_trigger();
     constexpr int V = Elem<T>::kPerVec;
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -81,6 +83,8 @@ template <typename T, int EM, int TT>
 __global__ void __launch_bounds__(kRouterTokWarps * 32)
 router_tokens_kernel(const T* __restrict__ x, const T* __restrict__ w_g, float* __restrict__ part,
                      int Tn, int d, int E) {
+    pdl_wait();
+    pdl_trigger();
     constexpr int V = Elem<T>::kPerVec;
     constexpr int kUnroll = EM <= 8 ? 2 : 1;  // steps whose loads are in flight together
     const int lane = threadIdx.x & 31;
@@ -157,6 +161,8 @@ __global__ void __launch_bounds__(256)
 topk_route_kernel(const float* __restrict__ part, int splits, const float* __restrict__ bias,
                   float* __restrict__ logits_out, int32_t* __restrict__ topk_idx,
                   float* __restrict__ topk_w, int Tn, int E, int K) {
+    pdl_wait();
+    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (t >= Tn) return;
@@ -242,12 +248,13 @@ cudaError_t launch_router_tokens(const moe_shape& s, const void* x, const void* 
     if (blocks > cap) blocks = cap;
     const dim3 grid((unsigned)blocks), block(kRouterTokWarps * 32);
     if (s.E <= 8)
-        router_tokens_kernel<T, 8, 2><<<grid, block, 0, st>>>((const T*)x, (const T*)w_g, part, s.T, s.d, s.E);
-    else if (s.E <= 16)
-        router_tokens_kernel<T, 16, 2><<<grid, block, 0, st>>>((const T*)x, (const T*)w_g, part, s.T, s.d, s.E);
-    else
-        router_tokens_kernel<T, 32, 2><<<grid, block, 0, st>>>((const T*)x, (const T*)w_g, part, s.T, s.d, s.E);
-    return cudaGetLastError();
+        return launch_pdl(router_tokens_kernel<T, 8, 2>, grid, block, 0, st, (const T*)x,
+                          (const T*)w_g, part, s.T, s.d, s.E);
+    if (s.E <= 16)
+        return launch_pdl(router_tokens_kernel<T, 16, 2>, grid, block, 0, st, (const T*)x,
+                          (const T*)w_g, part, s.T, s.d, s.E);
+    return launch_pdl(router_tokens_kernel<T, 32, 2>, grid, block, 0, st, (const T*)x,
+                      (const T*)w_g, part, s.T, s.d, s.E);
 }
 
 cudaError_t launch_router_gemv(const moe_shape& s, const void* x, const void* w_g, float* part,
@@ -260,13 +267,12 @@ cudaError_t launch_router_gemv(const moe_shape& s, const void* x, const void* w_
     const int64_t cap = (int64_t)device_sm_count() * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
+    const dim3 grid((unsigned)blocks), block(kRouterWarps * 32);
     if (s.dtype == MOE_BF16)
-        router_gemv_kernel<bf16><<<(unsigned)blocks, kRouterWarps * 32, 0, st>>>(
-            (const bf16*)x, (const bf16*)w_g, part, s.T, s.d, s.E, splits);
-    else
-        router_gemv_kernel<float><<<(unsigned)blocks, kRouterWarps * 32, 0, st>>>(
-            (const float*)x, (const float*)w_g, part, s.T, s.d, s.E, splits);
-    return cudaGetLastError();
+        return launch_pdl(router_gemv_kernel<bf16>, grid, block, 0, st, (const bf16*)x,
+                          (const bf16*)w_g, part, s.T, s.d, s.E, splits);
+    return launch_pdl(router_gemv_kernel<float>, grid, block, 0, st, (const float*)x,
+                      (const float*)w_g, part, s.T, s.d, s.E, splits);
 }
 
 cudaError_t launch_topk_softmax(const moe_shape& s, const float* part, int splits,
@@ -274,9 +280,9 @@ cudaError_t launch_topk_softmax(const moe_shape& s, const float* part, int split
                                 float* topk_w, cudaStream_t st) {
     const unsigned blocks = (unsigned)ceil_div(s.T, 8);
     const int m = (int)ceil_div(s.E, 32);
-#define MOE_TOPK(M, MODE)                                                                      \
-    topk_route_kernel<M, MODE><<<blocks, 256, 0, st>>>(part, splits, bias, logits_out, topk_idx, \
-                                                       topk_w, s.T, s.E, s.K)
+#define MOE_TOPK(M, MODE)                                                                     \
+    e = launch_pdl(topk_route_kernel<M, MODE>, dim3(blocks), dim3(256), 0, st, part, splits, bias, \
+                   logits_out, topk_idx, topk_w, s.T, s.E, s.K)
 #define MOE_TOPK_M(MODE)                    \
     if (m <= 1) MOE_TOPK(1, MODE);          \
     else if (m <= 2) MOE_TOPK(2, MODE);     \
@@ -284,6 +290,7 @@ cudaError_t launch_topk_softmax(const moe_shape& s, const float* part, int split
     else if (m <= 8) MOE_TOPK(8, MODE);     \
     else if (m <= 16) MOE_TOPK(16, MODE);   \
     else MOE_TOPK(32, MODE)
+    cudaError_t e;
     if (s.router == MOE_ROUTER_SIGMOID) {
         MOE_TOPK_M(1);
     } else {
@@ -291,6 +298,7 @@ cudaError_t launch_topk_softmax(const moe_shape& s, const float* part, int split
     }
 #undef MOE_TOPK_M
 #undef MOE_TOPK
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
