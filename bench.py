@@ -123,7 +123,7 @@ def launches_per_forward(cfg, gemv_limit: int = 0) -> int:
         # router + top-K, 3 dispatch kernels, row gather, plan, the 8-bit GEMV
         # (gate/up and down for each of its two group lists), the tcgen05
         # gate/up and down when a group can exceed the GEMV limit, combine
-        limit = int(os.environ.get("MOE_GEMV8_MAX_ROWS", "16"))
+        limit = int(os.environ.get("MOE_GEMV8_MAX_ROWS", "8"))
         gemv = (2 if limit > 0 else 0) + (2 if limit > 8 else 0)
         tc = 2 if cfg.T > limit else 0
         return 2 + 3 + 1 + 1 + gemv + tc + 1

@@ -52,7 +52,6 @@ namespace {
 constexpr int kG8Warps = 16;
 constexpr int kG8Threads = kG8Warps * 32;
 constexpr int kG8Tok = 8;           // token rows per MMA (its N)
-constexpr int kG8MaxTiles = 2;      // MMAs per A fragment: up to 16 token rows per pass
 constexpr int kG8U = 8;             // 64-code K blocks in flight per lane
 
 struct Group8 {
@@ -372,11 +371,13 @@ cudaError_t launch_dn(const FfnGroups& g, const FfnPlanHeader* hdr, const int32_
 }  // namespace
 
 // Groups of at most this many rows take the 8-bit GEMV path (MOE_GEMV8_MAX_ROWS,
-// read on every call; default 16 -- two MMA column tiles; 0 sends every group
-// to the tcgen05 path; larger groups take several passes).
+// read on every call; default 8 -- one MMA column tile; 0 sends every group to
+// the tcgen05 path; larger values use the second list, 16 rows per pass).
+// Measured on GB300 (DeepSeek-V3 shapes): 8 and 16 tie at T = 8, 8 is 3% faster
+// at T = 64 and 16 is 0.8% faster at T = 512.
 int gemv8_max_rows() {
     const char* s = getenv("MOE_GEMV8_MAX_ROWS");
-    const int x = s ? atoi(s) : kG8Tok * kG8MaxTiles;
+    const int x = s ? atoi(s) : kG8Tok;
     return x < 0 ? 0 : x;
 }
 

@@ -87,18 +87,37 @@ template <bool PAIR> struct Shape {
 
 enum Epi { EPI_SWIGLU = 0, EPI_STORE_BF16 = 1, EPI_STORE_F32 = 2 };
 
-// 8-bit weights (W8, single-SM tiles only).  TMA streams E4M3 weight tiles of
-// 256 rows x 128 codes (32 KB, two 64-deep K steps) into a 4-stage raw ring;
-// four converter warps widen each K step to bf16 (exact: every E4M3 value is
-// a bf16 value) into a 2-stage ring of 48 KB MMA stages, whose activation
-// tile the first converter warp requests by TMA.  The per-row weight scale
-// factors out of the K sum and is applied in the epilogue.
-constexpr int kW8ConvStages = 2;
-constexpr int kW8RawStages = 4;
-constexpr uint32_t kW8RawBytes = 256 * 128;  // 32 KB
-constexpr int kThreadsW8 = 320;              // + warps 6..9: converters
-constexpr uint32_t kW8RingBytes =
-    kW8ConvStages * (kABytes + Shape<false>::kBBytes) + kW8RawStages * kW8RawBytes;  // 224 KB
+// 8-bit weights (W8).  TMA streams a CTA's E4M3 weight rows (256 for a
+// single-SM tile, 128 per CTA of a pair) x 128 codes (two 64-deep K steps)
+// into a raw ring; eight converter warps widen each K step to bf16 (exact:
+// every E4M3 value is a bf16 value) into a ring of bf16 weight stages; the
+// producer requests the activation tiles into their own ring.  The per-row
+// weight scale factors out of the K sum and is applied in the epilogue.  In a
+// pair each CTA widens only its own 128 weight rows.  Measured on GB300
+// (Mixtral-shaped prefill): moving the activation loads from the converters
+// to the producer and doubling the converter warps took the single-SM
+// variant from 4.85 to 3.65 ms; the pair variant stays slower (5.3 ms), its
+// stage handoffs crossing the cluster, so 8-bit groups use single-SM tiles
+// unless MOE_W8_PAIR=1.
+// Three rings: activation tiles (TMA, requested by the producer several K
+// steps ahead), raw code tiles (TMA), and widened bf16 weight tiles (written
+// by the converter warps); the MMA waits for one stage of each A and B ring.
+constexpr int kW8ConvWarps = 8;  // converter warps per CTA (warps 6..13)
+template <bool PAIR> struct W8Shape {
+    static constexpr int kA = PAIR ? 4 : 3;                          // activation stages
+    static constexpr int kConv = PAIR ? 5 : 3;                       // bf16 weight stages
+    static constexpr int kRaw = PAIR ? 4 : 2;                        // raw code tiles
+    static constexpr uint32_t kRawBytes = Shape<PAIR>::kBRows * 128;  // 16 / 32 KB
+    static constexpr uint32_t kRingBytes =
+        kA * kABytes + kConv * Shape<PAIR>::kBBytes + kRaw * kRawBytes;  // 208 KB
+    // converter warps that fill a stage (of both CTAs in a pair)
+    static constexpr int kConvArrivals = PAIR ? 2 * kW8ConvWarps : kW8ConvWarps;
+};
+static_assert(W8Shape<false>::kRingBytes == W8Shape<true>::kRingBytes, "one W8 ring size");
+constexpr int kW8MaxA = 4;
+constexpr int kW8MaxRaw = 4;
+constexpr uint32_t kW8RingBytes = W8Shape<false>::kRingBytes;
+constexpr int kThreadsW8 = (6 + kW8ConvWarps) * 32;  // + the converter warps
 
 // Activation maps come in four box heights; a CTA loads the smallest box that
 // covers its valid rows.  The MMA still reads all 128 rows of the stage: rows
@@ -200,9 +219,10 @@ struct SmemCtl {
     uint64_t tfull[2];           // accumulator a is ready (each CTA)
     uint64_t tempty[2];          // the epilogue warps drained accumulator a (a pair: even CTA, 8 warps)
     uint64_t drain;
-    uint64_t afull[kW8ConvStages];   // W8: the activation tile of MMA stage s landed
-    uint64_t rfull[kW8RawStages];    // W8: raw code tile r landed
-    uint64_t rempty[kW8RawStages];   // W8: the 4 converter warps are done with raw tile r
+    uint64_t afull[kW8MaxA];      // W8: activation stage a landed (a pair: both CTAs' tiles, even CTA)
+    uint64_t aempty[kW8MaxA];     // W8: the MMAs reading activation stage a completed (each CTA)
+    uint64_t rfull[kW8MaxRaw];    // W8: this CTA's raw code tile r landed
+    uint64_t rempty[kW8MaxRaw];   // W8: this CTA's 4 converter warps are done with raw tile r
     uint32_t tmem_base;
     volatile int abort_flag;
 };
@@ -244,19 +264,20 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two) {
     return *reinterpret_cast<const uint32_t*>(&b);
 }
 
-// W8 converter warp cw (0..3): rows 64*cw .. 64*cw+63 of K half h (codes
+// W8 converter warp cw (0..3): rows RPW*cw .. RPW*cw+RPW-1 of K half h (codes
 // 64h .. 64h+63 of each 128-code row) of a raw tile -> the bf16 weight tile of
 // an MMA stage.  Both tiles use the 128-byte swizzle (16-byte chunk c of row r
 // at chunk c ^ (r & 7)).  Lane 8j + 4s + q takes row 8*it + j + 4s: it reads
 // code chunk 4h+q and writes bf16 chunks 2q and 2q+1, the odd one first when
 // s = 1.  Each quarter-warp (8 lanes, one shared-memory wavefront of 16-byte
 // accesses) then touches 8 distinct chunk positions on every load and store.
+template <int RPW>  // weight rows per converter warp (64 single-SM, 32 in a pair)
 __device__ __forceinline__ void convert_rows_w8(const uint8_t* raw, uint8_t* dst, int h, int cw,
                                                 int lane) {
     const int q = lane & 3, s = (lane >> 2) & 1, j = lane >> 3;
 #pragma unroll
-    for (int it = 0; it < 8; ++it) {
-        const int r = cw * 64 + it * 8 + j + 4 * s;
+    for (int it = 0; it < RPW / 8; ++it) {
+        const int r = cw * RPW + it * 8 + j + 4 * s;
         const int x = r & 7;
         const uint4 v = *reinterpret_cast<const uint4*>(raw + r * 128 + (((h * 4 + q) ^ x) << 4));
         uint4 lo, hi;
@@ -287,16 +308,17 @@ __device__ __forceinline__ void ld_scale16(const float* src, float (&s)[16]) {
 template <int EPI, bool PAIR, bool W8 = false>
 __global__ void __launch_bounds__(W8 ? kThreadsW8 : kThreadsTc, 1)
 tc_gemm_kernel(const __grid_constant__ TcParams p) {
-    static_assert(!(W8 && PAIR), "8-bit weights run on single-SM tiles");
     static_assert(!(W8 && EPI == EPI_STORE_F32), "8-bit weights feed the expert GEMMs only");
     using S = Shape<PAIR>;
-    constexpr int kStages = W8 ? kW8ConvStages : S::kStages;  // MMA stages
+    using W = W8Shape<PAIR>;
+    constexpr int kStages = W8 ? W::kConv : S::kStages;  // B stages (and A stages without W8)
+    constexpr int kAStages = W8 ? W::kA : S::kStages;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte alignment for the 128-byte-swizzle atoms (the same offset in both CTAs of a pair)
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t* sA = smem;
-    uint8_t* sB = smem + kStages * kABytes;
-    uint8_t* sRaw = smem + kStages * (kABytes + S::kBBytes);  // W8 only
+    uint8_t* sB = smem + kAStages * kABytes;
+    uint8_t* sRaw = sB + kStages * S::kBBytes;  // W8 only
     SmemCtl* ctl = (SmemCtl*)(smem + (W8 ? kW8RingBytes : kRingBytes));
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -307,15 +329,18 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            // W8: full = the 4 converter warps wrote the bf16 weight tile
-            ptx::mbar_init(&ctl->full[s], W8 ? 4 : 1);
+            // W8: full = the converter warps (of both CTAs of a pair) wrote the bf16 weight tile
+            ptx::mbar_init(&ctl->full[s], W8 ? W::kConvArrivals : 1);
             ptx::mbar_init(&ctl->empty[s], 1);
         }
         if constexpr (W8) {
-            for (int s = 0; s < kW8ConvStages; ++s) ptx::mbar_init(&ctl->afull[s], 1);
-            for (int r = 0; r < kW8RawStages; ++r) {
+            for (int a = 0; a < W::kA; ++a) {
+                ptx::mbar_init(&ctl->afull[a], 1);
+                ptx::mbar_init(&ctl->aempty[a], 1);
+            }
+            for (int r = 0; r < W::kRaw; ++r) {
                 ptx::mbar_init(&ctl->rfull[r], 1);
-                ptx::mbar_init(&ctl->rempty[r], 4);
+                ptx::mbar_init(&ctl->rempty[r], kW8ConvWarps);
             }
         }
         for (int a = 0; a < 2; ++a) {
@@ -374,43 +399,88 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
         // lane l loads rows 4l..4l+3 of this CTA's block, so one stage takes up
         // to 32 gather instructions issued in parallel.
         if constexpr (W8) {
-            // W8: lane 0 streams the raw code tiles, two K steps per tile
+            // W8: lane 0 streams this CTA's raw code tiles (two K steps each; a
+            // pair: the even CTA the gate rows or weight rows 0-127 of the
+            // n-block, the odd CTA the up rows or rows 128-255) and its
+            // activation tiles, each ring as far ahead as it has free stages.
             if (lane == 0) {
-                int rs = 0;
-                uint32_t rph = 0;
-                bool issued[kW8RawStages];
-                uint32_t issued_phase[kW8RawStages];
-                for (int r = 0; r < kW8RawStages; ++r) { issued[r] = false; issued_phase[r] = 0; }
+                int rs = 0, as = 0;
+                uint32_t rph = 0, aph = 0;
+                bool r_issued[W::kRaw], a_issued[W::kA];
+                uint32_t r_phase[W::kRaw], a_phase[W::kA];
+                for (int r = 0; r < W::kRaw; ++r) { r_issued[r] = false; r_phase[r] = 0; }
+                for (int a = 0; a < W::kA; ++a) { a_issued[a] = false; a_phase[a] = 0; }
+                const uint32_t afull0 = PAIR ? ptx::map_to_rank(&ctl->afull[0], 0) : 0u;
                 bool ok = p.test_stall == 0;
                 for (int t = unit; t < n_tiles && ok; t += n_units) {
                     const Tile tl = decode_tile<EPI, PAIR>(p, list_len, t);
                     if (!tl.valid) continue;
-                    const int nraw = (tl.kblocks + 1) / 2;
-                    for (int kr = 0; kr < nraw; ++kr) {
-                        if (!wait_bounded(&ctl->rempty[rs], rph ^ 1u, ctl, p, 110)) { ok = false; break; }
-                        uint8_t* dst = sRaw + rs * kW8RawBytes;
-                        // a box past the end of K or of the weight rows is zero-filled
-                        // and still counts its full size
-                        ptx::mbar_arrive_expect_tx(&ctl->rfull[rs], kW8RawBytes);
-                        if (EPI == EPI_SWIGLU) {
-                            ptx::tma_load_2d(dst, &p.q0[tl.kind], &ctl->rfull[rs], kr * 128, tl.wrow0);
-                            ptx::tma_load_2d(dst + kW8RawBytes / 2, &p.q1[tl.kind], &ctl->rfull[rs],
-                                             kr * 128, tl.wrow0);
-                        } else {
-                            ptx::tma_load_2d(dst, &p.qw[tl.kind], &ctl->rfull[rs], kr * 128, tl.wrow0);
+                    const int rows_me = max(0, min(BMC, tl.rows - (int)rank * BMC));
+                    const CUtensorMap* ma = &p.a[tl.kind][abox_for(rows_me)];
+                    const int arow = tl.row0 + (int)rank * BMC;
+                    // bytes of one activation stage (both CTAs' tiles in a pair)
+                    const uint32_t abytes = PAIR ? abytes_for(min(BMC, tl.rows)) + abytes_for(tl.rows - BMC)
+                                                 : abytes_for(rows_me);
+                    for (int kb = 0; kb < tl.kblocks; ++kb) {
+                        if ((kb & 1) == 0) {
+                            if (!wait_bounded(&ctl->rempty[rs], rph ^ 1u, ctl, p, 110)) { ok = false; break; }
+                            uint8_t* dst = sRaw + rs * W::kRawBytes;
+                            // a box past the end of K or of the weight rows is zero-filled
+                            // and still counts its full size
+                            ptx::mbar_arrive_expect_tx(&ctl->rfull[rs], W::kRawBytes);
+                            const int kr = kb >> 1;
+                            if constexpr (PAIR) {
+                                const CUtensorMap* mq = (EPI == EPI_SWIGLU && rank == 1) ? &p.q1[tl.kind]
+                                                                                         : &p.q0[tl.kind];
+                                const int qrow = tl.wrow0 + (EPI == EPI_SWIGLU ? 0 : (int)rank * S::kBRows);
+                                ptx::tma_load_2d(dst, mq, &ctl->rfull[rs], kr * 128, qrow);
+                            } else if (EPI == EPI_SWIGLU) {
+                                ptx::tma_load_2d(dst, &p.q0[tl.kind], &ctl->rfull[rs], kr * 128, tl.wrow0);
+                                ptx::tma_load_2d(dst + W::kRawBytes / 2, &p.q1[tl.kind], &ctl->rfull[rs],
+                                                 kr * 128, tl.wrow0);
+                            } else {
+                                ptx::tma_load_2d(dst, &p.qw[tl.kind], &ctl->rfull[rs], kr * 128, tl.wrow0);
+                            }
+                            r_issued[rs] = true;
+                            r_phase[rs] = rph;
+                            if (++rs == W::kRaw) { rs = 0; rph ^= 1u; }
                         }
-                        issued[rs] = true;
-                        issued_phase[rs] = rph;
-                        if (++rs == kW8RawStages) { rs = 0; rph ^= 1u; }
+                        if (!wait_bounded(&ctl->aempty[as], aph ^ 1u, ctl, p, 111)) { ok = false; break; }
+                        if constexpr (PAIR) {
+                            const uint32_t ab = afull0 + (uint32_t)(as * sizeof(uint64_t));
+                            if (rank == 0) ptx::mbar_arrive_expect_tx(&ctl->afull[as], abytes);
+                            if (rows_me > 0) ptx::tma_load_2d_pair(sA + as * kABytes, ma, ab, kb * BK, arow);
+                        } else {
+                            ptx::mbar_arrive_expect_tx(&ctl->afull[as], abytes);
+                            ptx::tma_load_2d(sA + as * kABytes, ma, &ctl->afull[as], kb * BK, arow);
+                        }
+                        a_issued[as] = true;
+                        a_phase[as] = aph;
+                        if (++as == W::kA) { as = 0; aph ^= 1u; }
                     }
                 }
                 if (!ok || ctl->abort_flag) {
-                    // every raw copy issued lands before teardown
-                    for (int r = 0; r < kW8RawStages; ++r) {
-                        if (!issued[r]) continue;
+                    // every copy issued lands before teardown: raw tiles on this CTA's
+                    // barriers; activation tiles on the even CTA's (the odd CTA cannot
+                    // observe those, so it gives its copies a bounded time)
+                    for (int r = 0; r < W::kRaw; ++r) {
+                        if (!r_issued[r]) continue;
                         const uint64_t t0 = ptx::globaltimer_ns();
-                        while (!ptx::mbar_try_wait(&ctl->rfull[r], issued_phase[r]) &&
+                        while (!ptx::mbar_try_wait(&ctl->rfull[r], r_phase[r]) &&
                                ptx::globaltimer_ns() - t0 < p.timeout_ns) {
+                        }
+                    }
+                    if (rank == 0) {
+                        for (int a = 0; a < W::kA; ++a) {
+                            if (!a_issued[a]) continue;
+                            const uint64_t t0 = ptx::globaltimer_ns();
+                            while (!ptx::mbar_try_wait(&ctl->afull[a], a_phase[a]) &&
+                                   ptx::globaltimer_ns() - t0 < p.timeout_ns) {
+                            }
+                        }
+                    } else {
+                        const uint64_t t0 = ptx::globaltimer_ns();
+                        while (ptx::globaltimer_ns() - t0 < 2000000ull) {
                         }
                     }
                 }
@@ -542,8 +612,10 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
         // ------------------------------------------------ MMA issuer (rank 0)
         if (lane == 0 && rank == 0) {
             constexpr uint32_t idesc = ptx::idesc_bf16_f32(S::kTileRows, BN);
-            int stage = 0;
+            int stage = 0;       // B stage (and A stage without W8)
             uint32_t phase = 0;
+            int ast = 0;         // W8: A stage
+            uint32_t aphase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
@@ -556,9 +628,9 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
                 const uint32_t d_tmem = tmem + (uint32_t)(acc * BN);
                 for (int kb = 0; kb < tl.kblocks; ++kb) {
                     if (!wait_bounded(&ctl->full[stage], phase, ctl, p, 201)) { ok = false; break; }
-                    if (W8 && !wait_bounded(&ctl->afull[stage], phase, ctl, p, 202)) { ok = false; break; }
+                    if (W8 && !wait_bounded(&ctl->afull[ast], aphase, ctl, p, 202)) { ok = false; break; }
                     ptx::tc_fence_after();
-                    const uint32_t a_base = ptx::smem_u32(sA + stage * kABytes);
+                    const uint32_t a_base = ptx::smem_u32(sA + (W8 ? ast : stage) * kABytes);
                     const uint32_t b_base = ptx::smem_u32(sB + stage * S::kBBytes);
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk) {
@@ -571,6 +643,11 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
                     any = true;
                     if constexpr (PAIR) ptx::tc_commit_pair(&ctl->empty[stage], 0x3);
                     else ptx::tc_commit(&ctl->empty[stage]);
+                    if constexpr (W8) {
+                        if constexpr (PAIR) ptx::tc_commit_pair(&ctl->aempty[ast], 0x3);
+                        else ptx::tc_commit(&ctl->aempty[ast]);
+                        if (++ast == W::kA) { ast = 0; aphase ^= 1u; }
+                    }
                     if (++stage == kStages) { stage = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
@@ -691,24 +768,19 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
     } else {
         if constexpr (W8) {
             // -------------------------------------------- W8 converters (warps 6..9)
-            // Per K step: wait for the raw tile (first half) and a free MMA
-            // stage; warp 6 requests the activation tile; every warp widens its
-            // 64 weight rows to bf16, makes the writes visible to the tensor
-            // core (async proxy) and arrives on full; after the second half
-            // the raw tile is released.
+            // Per K step: wait for the raw tile (first half) and a free bf16
+            // stage; every warp widens its weight rows to bf16, makes the writes
+            // visible to the tensor core (async proxy) and arrives on full (a
+            // pair: on the even CTA, whose MMA reads both CTAs' stages); after
+            // the second half the raw tile is released.
             const int cw = warp - 6;
+            const uint32_t full0 = PAIR ? ptx::map_to_rank(&ctl->full[0], 0) : 0u;
             int rs = 0, cs = 0;
             uint32_t rph = 0, cph = 0;
-            bool a_issued[kW8ConvStages];
-            uint32_t a_phase[kW8ConvStages];
-            for (int i = 0; i < kW8ConvStages; ++i) { a_issued[i] = false; a_phase[i] = 0; }
             bool ok = true;
             for (int t = unit; t < n_tiles && ok; t += n_units) {
                 const Tile tl = decode_tile<EPI, PAIR>(p, list_len, t);
                 if (!tl.valid) continue;
-                const int rows_me = min(BMC, tl.rows);
-                const CUtensorMap* ma = &p.a[tl.kind][abox_for(rows_me)];
-                const uint32_t abytes = abytes_for(rows_me);
                 for (int kb = 0; kb < tl.kblocks; ++kb) {
                     const int h = kb & 1;
                     if (h == 0) {
@@ -717,30 +789,18 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
                     }
                     const int oke = lane == 0 ? (int)wait_bounded(&ctl->empty[cs], cph ^ 1u, ctl, p, 401) : 0;
                     if (!__shfl_sync(0xffffffffu, oke, 0)) { ok = false; break; }
-                    if (cw == 0 && lane == 0) {
-                        ptx::mbar_arrive_expect_tx(&ctl->afull[cs], abytes);
-                        ptx::tma_load_2d(sA + cs * kABytes, ma, &ctl->afull[cs], kb * BK, tl.row0);
-                        a_issued[cs] = true;
-                        a_phase[cs] = cph;
-                    }
-                    convert_rows_w8(sRaw + rs * kW8RawBytes, sB + cs * S::kBBytes, h, cw, lane);
+                    convert_rows_w8<S::kBRows / kW8ConvWarps>(sRaw + rs * W::kRawBytes,
+                                                              sB + cs * S::kBBytes, h, cw, lane);
                     ptx::fence_proxy_async_smem();
                     __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive(&ctl->full[cs]);
-                    if (++cs == kW8ConvStages) { cs = 0; cph ^= 1u; }
+                    if (lane == 0) {
+                        if constexpr (PAIR) ptx::mbar_arrive_cluster(full0 + (uint32_t)(cs * sizeof(uint64_t)));
+                        else ptx::mbar_arrive(&ctl->full[cs]);
+                    }
+                    if (++cs == W::kConv) { cs = 0; cph ^= 1u; }
                     if (h == 1 || kb == tl.kblocks - 1) {
                         if (lane == 0) ptx::mbar_arrive(&ctl->rempty[rs]);
-                        if (++rs == kW8RawStages) { rs = 0; rph ^= 1u; }
-                    }
-                }
-            }
-            if ((!ok || ctl->abort_flag) && cw == 0 && lane == 0) {
-                // every activation copy issued lands before teardown
-                for (int i = 0; i < kW8ConvStages; ++i) {
-                    if (!a_issued[i]) continue;
-                    const uint64_t t0 = ptx::globaltimer_ns();
-                    while (!ptx::mbar_try_wait(&ctl->afull[i], a_phase[i]) &&
-                           ptx::globaltimer_ns() - t0 < p.timeout_ns) {
+                        if (++rs == W::kRaw) { rs = 0; rph ^= 1u; }
                     }
                 }
             }
@@ -861,8 +921,8 @@ cudaError_t launch_tc(const TcParams& p, cudaStream_t st) {
     if constexpr (PAIR) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(2 * units);
-        cfg.blockDim = dim3(kThreadsTc);
-        cfg.dynamicSmemBytes = kSmemBytes;
+        cfg.blockDim = dim3(W8 ? kThreadsW8 : kThreadsTc);
+        cfg.dynamicSmemBytes = smem;
         cfg.stream = st;
         cudaLaunchAttribute attr[2];
         attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -873,7 +933,7 @@ cudaError_t launch_tc(const TcParams& p, cudaStream_t st) {
         attr[1].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
         cfg.attrs = attr;
         cfg.numAttrs = 2;
-        e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel<EPI, PAIR>, p);
+        e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel<EPI, PAIR, W8>, p);
         if (e != cudaSuccess) return e;
     } else {
         e = launch_pdl(tc_gemm_kernel<EPI, PAIR, W8>, dim3(units), dim3(W8 ? kThreadsW8 : kThreadsTc),
@@ -1015,7 +1075,9 @@ cudaError_t launch_ffn_tc(const FfnGroups& g, const FfnPlanHeader* hdr, const in
 // The expert FFN with E4M3 weights: the same two GEMMs on single-SM tiles
 // (every plan entry in the single list), routed rows from the permuted copy.
 cudaError_t launch_ffn_tc_fp8(const FfnGroups& g, const FfnPlanHeader* hdr, const int4* mtile_list,
-                              int max_mtiles, DevError* err, cudaStream_t st) {
+                              int max_mtiles, bool may_pair, DevError* err, cudaStream_t st) {
+    const int4* single_list = mtile_list;
+    const int4* pair_list = mtile_list + max_mtiles;
     const int64_t R = g.n_routed_rows;
     // ---- gate/up: h = SiLU(s_g * (x Q_gate^T)) * (s_u * (x Q_up^T))
     TcParams p{};
@@ -1042,7 +1104,6 @@ cudaError_t launch_ffn_tc_fp8(const FfnGroups& g, const FfnPlanHeader* hdr, cons
     p.qw[0] = p.q0[0]; p.qw[1] = p.q0[1];  // unused by the SWIGLU epilogue
     if (!ok) return cudaErrorInvalidValue;
     p.hdr = hdr;
-    p.mtiles = mtile_list;
     p.E = g.E;
     p.max_mtiles = max_mtiles;
     p.dense_rows = 0;
@@ -1056,7 +1117,14 @@ cudaError_t launch_ffn_tc_fp8(const FfnGroups& g, const FfnPlanHeader* hdr, cons
     p.err = err;
     p.timeout_ns = timeout_ns();
     p.test_stall = test_stall();
-    cudaError_t e = launch_tc<EPI_SWIGLU, false, true>(p, st);
+    cudaError_t e = cudaSuccess;
+    if (may_pair) {
+        p.mtiles = pair_list;
+        e = launch_tc<EPI_SWIGLU, true, true>(p, st);
+        if (e != cudaSuccess) return e;
+    }
+    p.mtiles = single_list;
+    e = launch_tc<EPI_SWIGLU, false, true>(p, st);
     if (e != cudaSuccess) return e;
 
     // ---- down: y = s_d * (h Q_down^T)
@@ -1075,11 +1143,14 @@ cudaError_t launch_ffn_tc_fp8(const FfnGroups& g, const FfnPlanHeader* hdr, cons
         q.sc0[1] = q.sc0[0];
     }
     q.ag = q.a[0][0];
-    q.q0[0] = q.qw[0]; q.q0[1] = q.qw[1]; q.q1[0] = q.qw[0]; q.q1[1] = q.qw[1];
+    // pair tiles load 128 of the n-block's 256 weight rows per CTA (box 128 rows)
+    ok &= make_map_u8(&q.q0[0], g.w_down, (int64_t)g.E * g.d, g.I, 128);
+    if (g.has_shared) ok &= make_map_u8(&q.q0[1], g.ws_down, g.d, g.Is, 128);
+    else q.q0[1] = q.q0[0];
+    q.q1[0] = q.q0[0]; q.q1[1] = q.q0[1];
     q.sc1[0] = q.sc0[0]; q.sc1[1] = q.sc0[1];
     if (!ok) return cudaErrorInvalidValue;
     q.hdr = hdr;
-    q.mtiles = mtile_list;
     q.E = g.E;
     q.max_mtiles = max_mtiles;
     q.dense_rows = 0;
@@ -1092,6 +1163,12 @@ cudaError_t launch_ffn_tc_fp8(const FfnGroups& g, const FfnPlanHeader* hdr, cons
     q.err = err;
     q.timeout_ns = timeout_ns();
     q.test_stall = test_stall();
+    if (may_pair) {
+        q.mtiles = pair_list;
+        e = launch_tc<EPI_STORE_BF16, true, true>(q, st);
+        if (e != cudaSuccess) return e;
+    }
+    q.mtiles = single_list;
     return launch_tc<EPI_STORE_BF16, false, true>(q, st);
 }
 

@@ -106,10 +106,10 @@ cudaError_t launch_ffn_tc(const FfnGroups& g, const FfnPlanHeader* hdr, const in
                           int max_mtiles, bool may_pair, DevError* err, cudaStream_t st);
 cudaError_t launch_router_tc(const moe_shape& s, const void* x, const void* w_g, float* scores,
                              DevError* err, cudaStream_t st);
-// E4M3 expert weights with row scales (g.s_* set); bf16 activations; every
-// group on single-SM tiles (the plan must have been built with allow_pair false)
+// E4M3 expert weights with row scales (g.s_* set); bf16 activations; the
+// plan's pair tiles (launched only when may_pair) and single-SM tiles
 cudaError_t launch_ffn_tc_fp8(const FfnGroups& g, const FfnPlanHeader* hdr, const int4* mtile_list,
-                              int max_mtiles, DevError* err, cudaStream_t st);
+                              int max_mtiles, bool may_pair, DevError* err, cudaStream_t st);
 
 // ---- ffn_gemv_fp8.cu (E4M3 weights, small groups) ----
 int gemv8_max_rows();  // groups with at most this many rows take the 8-bit GEMV

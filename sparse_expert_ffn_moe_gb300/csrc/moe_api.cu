@@ -77,6 +77,16 @@ int gemv8_limit(const moe_shape& s) {
     return gemv8_fits(widest) ? gemv8_max_rows() : 0;
 }
 
+// 8-bit weights on CTA-pair tiles (MOE_W8_PAIR=1, read per call; default off).
+// Measured on GB300: the pair variant (each CTA widens half of the n-block's
+// weight rows) is slower than single-SM tiles on prefill shapes (Mixtral:
+// 5.3 ms vs 3.65 ms), its handoffs crossing the cluster; it stays selectable
+// and parity-tested.
+bool w8_pair() {
+    const char* e = getenv("MOE_W8_PAIR");
+    return e && e[0] == '1';
+}
+
 // routed code and scale pointers present and aligned; shared ones iff wanted
 moe_status check_fp8_weights(const moe_fp8_experts* w, bool shared) {
     if (!w) return MOE_ERR_INVALID_ARG;
@@ -451,12 +461,14 @@ moe_status moe_expert_ffn_fp8(const moe_shape* shape, const void* x_perm, const 
     int32_t* glist = at<int32_t>(workspace, L.gemv_list);
     int4* mtiles = at<int4>(workspace, L.mtile_list);
     const int lim = gemv8_limit(s);
-    e = launch_ffn_plan(g, s.dtype, hdr, glist, mtiles, L.max_mtiles, lim, false,
+    const bool pair = w8_pair();
+    e = launch_ffn_plan(g, s.dtype, hdr, glist, mtiles, L.max_mtiles, lim, pair,
                         gemv8_small_rows(), cs);
     if (e == cudaSuccess && lim > 0) e = launch_ffn_gemv_fp8(g, hdr, glist, lim, cs);
     // a group has at most T*K rows here (the offsets are the caller's)
     if (e == cudaSuccess && (int64_t)s.T * s.K > lim)
-        e = launch_ffn_tc_fp8(g, hdr, mtiles, L.max_mtiles, err, cs);
+        e = launch_ffn_tc_fp8(g, hdr, mtiles, L.max_mtiles,
+                              pair && tc_pair_possible((int64_t)s.T * s.K), err, cs);
     return cuda_status(e);
 }
 
@@ -540,11 +552,13 @@ moe_status moe_forward_fp8(const moe_shape* shape, const void* x, const void* w_
     int32_t* glist = at<int32_t>(workspace, L.gemv_list);
     int4* mtiles = at<int4>(workspace, L.mtile_list);
     const int lim = gemv8_limit(s);
-    e = launch_ffn_plan(g, s.dtype, hdr, glist, mtiles, L.max_mtiles, lim, false,
+    const bool pair = w8_pair();
+    e = launch_ffn_plan(g, s.dtype, hdr, glist, mtiles, L.max_mtiles, lim, pair,
                         gemv8_small_rows(), cs);
     if (e == cudaSuccess && lim > 0) e = launch_ffn_gemv_fp8(g, hdr, glist, lim, cs);
     // a group has at most T rows (a token picks an expert once; the shared group has T)
-    if (e == cudaSuccess && s.T > lim) e = launch_ffn_tc_fp8(g, hdr, mtiles, L.max_mtiles, err, cs);
+    if (e == cudaSuccess && s.T > lim)
+        e = launch_ffn_tc_fp8(g, hdr, mtiles, L.max_mtiles, pair && tc_pair_possible(s.T), err, cs);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
 
     // 4. combine

@@ -85,7 +85,9 @@ def _expert_ffn_case(moe, counts, d, I, seed=0):
     ([8, 9, 0, 7, 16, 17], 128, 128),                # around the GEMV limit, narrowest shapes
     ([16, 15, 1, 33], 7168, 256),                    # DeepSeek-width rows, 16-row passes
 ])
-def test_expert_ffn_fp8_matches_oracle(moe, counts, d, I):
+@pytest.mark.parametrize("w8_pair", ["0", "1"])
+def test_expert_ffn_fp8_matches_oracle(moe, counts, d, I, w8_pair, monkeypatch):
+    monkeypatch.setenv("MOE_W8_PAIR", w8_pair)
     y, ref = _expert_ffn_case(moe, counts, d, I)
     assert rel_l2(y, ref) <= BF16_REL_L2
     for r in range(y.shape[0]):
@@ -117,9 +119,9 @@ def _check_rows(y, ref):
 @pytest.mark.parametrize("gemv8", ["0", "8", "16", "40"])
 def test_forward_fp8_small_layer_all_tokens(moe, router, gemv8, monkeypatch):
     """Groups of ~11 rows and a 45-row shared group: all on the tensor cores
-    (limit 0), part of the routed groups on the 8-bit GEMV (8), every routed
-    group in one 16-row pass (16, the default), or everything including the
-    shared group in passes of 16 rows (40)."""
+    (limit 0), part of the routed groups on the 8-bit GEMV (8, the default),
+    every routed group in one 16-row pass of the second list (16), or
+    everything including the shared group in passes of 16 rows (40)."""
     monkeypatch.setenv("MOE_GEMV8_MAX_ROWS", gemv8)
     cfg = mi.LayerConfig("fp8_small", T=45, d=256, E=12, K=3, I=384, Is=256, router=router,
                          weights="e4m3")
@@ -152,7 +154,11 @@ def test_forward_fp8_decode_full_size(moe, gemv8, monkeypatch):
     _check_rows(y, ref["y"])
 
 
-def test_forward_fp8_prefill_sampled_tokens(moe):
+@pytest.mark.parametrize("w8_pair", ["0", "1"])
+def test_forward_fp8_prefill_sampled_tokens(moe, w8_pair, monkeypatch):
+    """Mixtral-shaped prefill: ~1024-row groups on single-SM 8-bit tiles (default)
+    or on CTA-pair 8-bit tiles (MOE_W8_PAIR=1)."""
+    monkeypatch.setenv("MOE_W8_PAIR", w8_pair)
     cfg = mi.CONFIGS["mixtral_prefill_fp8"]
     L = Layer(cfg)
     y = L.forward(moe)
