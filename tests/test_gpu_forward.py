@@ -128,6 +128,32 @@ def test_forward_is_deterministic_and_graph_capturable(moe):
     assert torch.equal(y3, y1)
 
 
+@pytest.mark.parametrize("name", ["dsv3_decode", "mixtral_prefill", "dsv3_decode_fp8", "tiny_f32"])
+def test_programmatic_dependent_launch_changes_no_bit(moe, name, monkeypatch):
+    """Every kernel orders itself after its predecessor with griddepcontrol.wait;
+    the same call with programmatic launch off (MOE_PDL=0) gives identical bits,
+    back to back on one stream (repeated calls overlap only their launch)."""
+    cfg = mi.CONFIGS[name]
+    L = Layer(cfg)
+    s = L.shape(moe)
+    ws = moe.alloc_workspace(s)
+    monkeypatch.setenv("MOE_PDL", "0")
+    ref = L.forward(moe, ws=ws)
+    monkeypatch.setenv("MOE_PDL", "1")
+    outs = [torch.empty_like(ref) for _ in range(3)]
+    for y in outs:  # three calls in a row, no host synchronisation in between
+        if cfg.weights == "e4m3":
+            moe.moe_forward_fp8(s, L.x, L.p["w_g"], L.bias, moe.make_fp8_experts(L.p), y, ws)
+        else:
+            p = L.p
+            moe.moe_forward(s, L.x, p["w_g"], L.bias, p["w_gate"], p["w_up"], p["w_down"],
+                            p.get("ws_gate"), p.get("ws_up"), p.get("ws_down"), y, ws)
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_error(ws) == 0
+    for y in outs:
+        assert torch.equal(y, ref)
+
+
 def test_combine_matches_oracle(moe):
     for dtype in ("f32", "bf16"):
         T, d, K = 50, 256, 3
