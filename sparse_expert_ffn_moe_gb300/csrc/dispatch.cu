@@ -141,34 +141,38 @@ dispatch_scatter_kernel(const int32_t* __restrict__ idx, int64_t n, int E, int K
     }
 }
 
-// One warp per token: the token's row of x is read once (four 16-byte loads in
-// flight per lane) and written to the K permuted positions inv_perm[t*K + j],
-// so x crosses HBM once even when it does not fit in L2.
+// One warp per (token, 128 16-byte vectors of its row): the slice of x is read
+// once (four loads in flight per lane) and written to the token's K permuted
+// positions inv_perm[t*K + j], so x crosses HBM once even when it does not fit
+// in L2, and a few tokens still spread over many warps.
+constexpr int kGatherVecs = 32 * 4;  // vectors per warp item
+
 __global__ void __launch_bounds__(256)
 gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ inv_perm,
                    uint4* __restrict__ x_perm, int Tn, int K, int vec_per_row, int64_t n_rows) {
     pdl_wait();
     pdl_trigger();
     const int lane = threadIdx.x & 31;
-    for (int64_t t = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); t < Tn;
-         t += (int64_t)gridDim.x * 8) {
+    const int nchunks = (vec_per_row + kGatherVecs - 1) / kGatherVecs;
+    const int64_t items = (int64_t)Tn * nchunks;
+    for (int64_t w = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); w < items;
+         w += (int64_t)gridDim.x * 8) {
+        const int64_t t = w / nchunks;
+        const int v0 = (int)(w - t * nchunks) * kGatherVecs + lane;
         const int32_t my_p = lane < K ? inv_perm[t * K + lane] : -1;
         const uint4* src = x + t * vec_per_row;
-        // warp-uniform trip count: every lane reaches the shuffles below
-        for (int b = 0; b < vec_per_row; b += 32 * 4) {
-            const int v0 = b + lane;
-            uint4 tmp[4];
+        uint4 tmp[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            if (v0 + 32 * q < vec_per_row) tmp[q] = __ldg(src + v0 + 32 * q);
+        // warp-uniform trip count: every lane reaches the shuffles
+        for (int j = 0; j < K; ++j) {
+            const int32_t p = __shfl_sync(0xffffffffu, my_p, j);
+            if (p < 0 || p >= n_rows) continue;  // dropped slot
+            uint4* dst = x_perm + (int64_t)p * vec_per_row;
 #pragma unroll
             for (int q = 0; q < 4; ++q)
-                if (v0 + 32 * q < vec_per_row) tmp[q] = __ldg(src + v0 + 32 * q);
-            for (int j = 0; j < K; ++j) {
-                const int32_t p = __shfl_sync(0xffffffffu, my_p, j);
-                if (p < 0 || p >= n_rows) continue;  // dropped slot
-                uint4* dst = x_perm + (int64_t)p * vec_per_row;
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    if (v0 + 32 * q < vec_per_row) dst[v0 + 32 * q] = tmp[q];
-            }
+                if (v0 + 32 * q < vec_per_row) dst[v0 + 32 * q] = tmp[q];
         }
     }
 }
@@ -205,7 +209,7 @@ cudaError_t launch_gather_rows(const moe_shape& s, const void* x, const int32_t*
     const int64_t rows = (int64_t)s.T * s.K;
     const int esz = s.dtype == MOE_BF16 ? 2 : 4;
     const int vpr = s.d * esz / 16;
-    int64_t blocks = ceil_div(s.T, 8);
+    int64_t blocks = ceil_div((int64_t)s.T * ceil_div(vpr, kGatherVecs), 8);
     const int64_t cap = (int64_t)device_sm_count() * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
