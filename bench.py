@@ -437,7 +437,7 @@ def time_expert_ffn(moe, cfg, x, p, bias, stream, steps: int, n_active: int) -> 
 # ncu capture per workload (profiles/ffn_stage_traffic_<workload>.md), valid only for
 # the ffn_tc.cu source it was taken on (sha256 prefix).
 STAGE_TRAFFIC = {
-    "mixtral_prefill": {"bytes": 6252355072, "ffn_tc_sha256": "2f38323651d02d0c"},
+    "mixtral_prefill": {"bytes": 4670973952, "ffn_tc_sha256": "6945fa05a70cf73b"},
 }
 
 
