@@ -14,7 +14,8 @@ SwiGLU expert FFN and the weighted combine plus the shared expert.
 Inputs: ``dtype`` is ``"f32"`` (numpy float32 arrays) or ``"bf16"`` (numpy
 uint16 arrays holding bf16 bit patterns).  Outputs are float64 / int32 numpy
 arrays.  8-bit expert weights are numpy uint8 arrays of E4M3 codes with one
-float32 scale per weight row (``*_fp8`` functions).
+float32 scale per weight row (``*_fp8`` functions); the ``*_w8a8`` functions
+also quantise the experts' input and hidden rows to E4M3, one scale per row.
 """
 from __future__ import annotations
 
@@ -74,10 +75,15 @@ def bind(lib):
     lib.oracle_e4m3_decode.argtypes = [i64, vp, vp]
     lib.oracle_e4m3_encode.argtypes = [i64, vp, vp]
     lib.oracle_quantize_fp8_rows.argtypes = [i64, i64, i32, vp, vp, vp]
+    lib.oracle_round_bf16.argtypes = [i64, vp, vp]
+    lib.oracle_expert_ffn_w8a8.argtypes = [i64, i64, i64, i32] + [vp] * 11 + [i32]
+    lib.oracle_forward_tokens_w8a8.argtypes = ([i64, vp] + [i64] * 6 + [i32, i32] + [vp] * 19
+                                               + [i32])
     for f in ("oracle_route", "oracle_permute", "oracle_expert_ffn", "oracle_combine",
               "oracle_shared_ffn", "oracle_forward", "oracle_forward_tokens",
               "oracle_expert_ffn_fp8", "oracle_forward_tokens_fp8", "oracle_e4m3_decode",
-              "oracle_e4m3_encode", "oracle_quantize_fp8_rows"):
+              "oracle_e4m3_encode", "oracle_quantize_fp8_rows", "oracle_expert_ffn_w8a8",
+              "oracle_forward_tokens_w8a8", "oracle_round_bf16"):
         getattr(lib, f).restype = i32
     return lib
 
@@ -333,11 +339,45 @@ def expert_ffn_fp8(x_perm, offsets, q: dict, dtype: str = "bf16", threads: int =
     return y
 
 
+def round_bf16(v):
+    """float32 -> bf16 (round to nearest even) as the W8A8 experts round h;
+    returns float32."""
+    lib = _load()
+    v = _arr(v, np.float32)
+    out = np.zeros(v.shape, np.float32)
+    _check(lib.oracle_round_bf16(v.size, _ptr(v), _ptr(out)), "oracle_round_bf16")
+    return out
+
+
+def expert_ffn_w8a8(x_perm, offsets, q: dict, dtype: str = "bf16", threads: int = 0,
+                    taps: bool = False):
+    """expert_ffn_fp8 with 8-bit activations: each x_perm row and each hidden row
+    (after fp32 -> bf16 rounding) quantised to E4M3 with one scale per row.
+    Returns y_perm [rows, d] f64, or (y_perm, h_pre, h_hat) with taps: h before
+    rounding and the dequantised quantised h, both [rows, I] f64."""
+    lib = _load()
+    x_perm = _in(x_perm, dtype)
+    offsets = _arr(offsets, np.int32)
+    w = _fp8_weights(q)
+    E, I, d = w["w_gate"].shape
+    rows = max(int(offsets[E]), 0)
+    y = np.zeros((rows, d), np.float64)
+    h_pre = np.zeros((rows, I), np.float64) if taps else None
+    h_hat = np.zeros((rows, I), np.float64) if taps else None
+    _check(lib.oracle_expert_ffn_w8a8(
+        d, E, I, _DT[dtype], _ptr(x_perm), _ptr(offsets), _ptr(w["w_gate"]), _ptr(w["w_up"]),
+        _ptr(w["w_down"]), _ptr(w["s_gate"]), _ptr(w["s_up"]), _ptr(w["s_down"]), _ptr(y),
+        _ptr(h_pre), _ptr(h_hat), threads), "oracle_expert_ffn_w8a8")
+    return (y, h_pre, h_hat) if taps else y
+
+
 def forward_tokens_fp8(tokens, x, w_g, q: dict, K: int, dtype: str = "bf16", bias=None,
-                       threads: int = 0, router: str = "softmax"):
+                       threads: int = 0, router: str = "softmax", act8: bool = False):
     """forward_tokens with E4M3 expert weights (routed and, when present, shared):
     q holds w_gate/w_up/w_down (+ ws_*) codes and s_gate/s_up/s_down (+ ss_*)
-    row scales; x and w_g are in dtype.  Returns the same dict as forward_tokens."""
+    row scales; x and w_g are in dtype.  Returns the same dict as forward_tokens.
+    act8: every expert runs W8A8 (its input and hidden rows quantised per row;
+    see oracle_forward_tokens_w8a8)."""
     lib = _load()
     tokens = _arr(tokens, np.int32)
     x, w_g = _in(x, dtype), _in(w_g, dtype)
@@ -353,11 +393,12 @@ def forward_tokens_fp8(tokens, x, w_g, q: dict, K: int, dtype: str = "bf16", bia
         "topk_w": np.zeros((n, K), np.float64),
         "logits": np.zeros((n, E), np.float64),
     }
-    _check(lib.oracle_forward_tokens_fp8(
+    fn = lib.oracle_forward_tokens_w8a8 if act8 else lib.oracle_forward_tokens_fp8
+    _check(fn(
         n, _ptr(tokens), T, d, E, K, I, Is, _DT[dtype], _ROUTER[router], _ptr(x), _ptr(w_g),
         _ptr(bias), _ptr(w["w_gate"]), _ptr(w["w_up"]), _ptr(w["w_down"]), _ptr(w["s_gate"]),
         _ptr(w["s_up"]), _ptr(w["s_down"]), _ptr(w["ws_gate"]), _ptr(w["ws_up"]),
         _ptr(w["ws_down"]), _ptr(w["ss_gate"]), _ptr(w["ss_up"]), _ptr(w["ss_down"]),
         _ptr(out["y"]), _ptr(out["topk_idx"]), _ptr(out["topk_w"]), _ptr(out["logits"]),
-        threads), "oracle_forward_tokens_fp8")
+        threads), "oracle_forward_tokens_w8a8" if act8 else "oracle_forward_tokens_fp8")
     return out

@@ -52,6 +52,11 @@
  * row's largest magnitude to 448 (scale = amax / 448 in fp32, 1 for a row of
  * zeros).
  *
+ * 8-bit activations (W8A8, the *_w8a8 entry points at the end): the same
+ * per-row quantisation applied to x and to the expert's hidden row h, which
+ * is first rounded to fp32 and then to bf16; these roundings are part of
+ * that method's definition and the only intermediate roundings in the file.
+ *
  * Every entry point returns 0 on success and a negative number on a bad
  * argument; nothing is allocated that is not freed before return.
  */
@@ -793,6 +798,22 @@ int oracle_e4m3_encode(int64_t n, const float *v, uint8_t *codes)
     return 0;
 }
 
+/* One scale for n fp32 values (amax / 448 in fp32, 1 when all are zero) and
+ * the code of each value / scale (fp32 division); returns the scale. */
+static float quantize_vec(const float *v, int64_t n, uint8_t *codes)
+{
+    float amax = 0.0f;
+    for (int64_t c = 0; c < n; ++c) {
+        const float a = fabsf(v[c]);
+        if (a > amax)
+            amax = a;
+    }
+    const float s = amax > 0.0f ? amax / 448.0f : 1.0f;
+    for (int64_t c = 0; c < n; ++c)
+        codes[c] = e4m3_code(v[c] / s);
+    return s;
+}
+
 /*
  * oracle_quantize_fp8_rows: per-channel quantisation of a row-major
  * [rows][cols] weight matrix (fp32 or bf16) to E4M3 codes with one fp32
@@ -805,19 +826,250 @@ int oracle_quantize_fp8_rows(int64_t rows, int64_t cols, int dtype, const void *
 {
     if (rows < 0 || cols < 1 || (rows > 0 && (!w || !codes || !scale)))
         return -1;
+    float *row = (float *)malloc(sizeof(float) * (size_t)cols);
     for (int64_t r = 0; r < rows; ++r) {
-        float amax = 0.0f;
-        for (int64_t c = 0; c < cols; ++c) {
-            const float a = fabsf((float)load_elem(w, dtype, r * cols + c));
-            if (a > amax)
-                amax = a;
-        }
-        const float s = amax > 0.0f ? amax / 448.0f : 1.0f;
-        scale[r] = s;
-        for (int64_t c = 0; c < cols; ++c) {
-            const float q = (float)load_elem(w, dtype, r * cols + c) / s;
-            codes[r * cols + c] = e4m3_code(q);
-        }
+        for (int64_t c = 0; c < cols; ++c)
+            row[c] = (float)load_elem(w, dtype, r * cols + c);
+        scale[r] = quantize_vec(row, cols, codes + r * cols);
     }
+    free(row);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* 8-bit activations (W8A8)                                                 */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * The same x_q = round(x / s) + z rule ("LLM from scratch, ch. 6", section
+ * "second route: make every byte cheaper"; the section notes that a method
+ * may quantise weights, activations or the KV cache) applied to the two
+ * activations that enter an expert's matrix products, each with one scale
+ * per row, exactly as a weight row is quantised:
+ *   x_hat = value(quant(x)) * s_x         (the token's row, bf16 input)
+ *   h     = SiLU(W_gate x_hat) * (W_up x_hat)
+ *   h_b   = bf16(fp32(h))                  (h held in fp32, stored in bf16,
+ *                                           the layer's activation type)
+ *   h_hat = value(quant(h_b)) * s_h
+ *   y     = W_down h_hat
+ * with the E4M3 expert weights above.  Reading: the pages name activation
+ * quantisation without fixing its granularity or where h is rounded; one
+ * scale per row (per token for x, per routed row for h) and a bf16 h are
+ * taken here.
+ */
+
+/* fp32 -> bf16, round to nearest even (NaN stays NaN, overflow gives inf) */
+static float round_bf16(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7f800000u) == 0x7f800000u) {
+        u = (u & 0xffff0000u) | ((u & 0x007fffffu) ? 0x00400000u : 0u);
+    } else {
+        u += 0x7fffu + ((u >> 16) & 1u);
+        u &= 0xffff0000u;
+    }
+    float r;
+    memcpy(&r, &u, sizeof r);
+    return r;
+}
+
+/* out[i] = round_bf16(v[i]) (exposed for its pin) */
+int oracle_round_bf16(int64_t n, const float *v, float *out)
+{
+    if (n < 0 || (n > 0 && (!v || !out)))
+        return -1;
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = round_bf16(v[i]);
+    return 0;
+}
+
+/* Scratch of one W8A8 expert row: n = max(d, I). */
+typedef struct {
+    float *f;    /* [n] fp32 row being quantised */
+    uint8_t *c;  /* [n] its codes               */
+    double *xh;  /* [d] x_hat                   */
+    double *h;   /* [I] h, then h_hat           */
+} a8_scratch;
+
+static int a8_alloc(a8_scratch *s, int64_t d, int64_t I)
+{
+    const int64_t n = d > I ? d : I;
+    s->f = (float *)malloc(sizeof(float) * (size_t)n);
+    s->c = (uint8_t *)malloc((size_t)n);
+    s->xh = (double *)malloc(sizeof(double) * (size_t)d);
+    s->h = (double *)malloc(sizeof(double) * (size_t)I);
+    return s->f && s->c && s->xh && s->h;
+}
+
+static void a8_free(a8_scratch *s)
+{
+    free(s->f); free(s->c); free(s->xh); free(s->h);
+}
+
+/* One row through a W8A8 expert (see above).  h_pre (optional, [I]) gets h
+ * before rounding, h_hat_out (optional, [I]) gets h_hat. */
+static void swiglu_row_a8(int64_t d, int64_t I, int dtype, const void *xrow_base,
+                          int64_t xrow_off, const orc_weight *w_gate, const orc_weight *w_up,
+                          const orc_weight *w_down, int64_t wg_off, int64_t wu_off,
+                          int64_t wd_off, a8_scratch *s, double *y, double *h_pre,
+                          double *h_hat_out)
+{
+    for (int64_t k = 0; k < d; ++k)
+        s->f[k] = (float)load_elem(xrow_base, dtype, xrow_off + k);
+    const float sx = quantize_vec(s->f, d, s->c);
+    for (int64_t k = 0; k < d; ++k)
+        s->xh[k] = e4m3_value(s->c[k]) * (double)sx;
+    for (int64_t i = 0; i < I; ++i) {
+        double g = 0.0, u = 0.0;
+        for (int64_t k = 0; k < d; ++k) {
+            g += load_weight(w_gate, wg_off + i * d + k) * s->xh[k];
+            u += load_weight(w_up, wu_off + i * d + k) * s->xh[k];
+        }
+        s->h[i] = g / (1.0 + exp(-g)) * u;
+    }
+    if (h_pre)
+        memcpy(h_pre, s->h, sizeof(double) * (size_t)I);
+    for (int64_t i = 0; i < I; ++i)
+        s->f[i] = round_bf16((float)s->h[i]);
+    const float sh = quantize_vec(s->f, I, s->c);
+    for (int64_t i = 0; i < I; ++i)
+        s->h[i] = e4m3_value(s->c[i]) * (double)sh;
+    if (h_hat_out)
+        memcpy(h_hat_out, s->h, sizeof(double) * (size_t)I);
+    for (int64_t j = 0; j < d; ++j) {
+        double acc = 0.0;
+        for (int64_t i = 0; i < I; ++i)
+            acc += load_weight(w_down, wd_off + j * I + i) * s->h[i];
+        y[j] = acc;
+    }
+}
+
+typedef struct {
+    int64_t d, E, I;
+    int dtype;
+    const void *x_perm;
+    const int32_t *offsets;
+    orc_weight w_gate, w_up, w_down;
+    double *y_perm, *h_pre, *h_hat;
+} ffn_a8_ctx;
+
+static void ffn_row_a8(void *vctx, int64_t p)
+{
+    ffn_a8_ctx *c = (ffn_a8_ctx *)vctx;
+    const int64_t e = expert_of_row(c->offsets, c->E, p);
+    const int64_t wgu = e * c->I * c->d, wd = e * c->d * c->I;
+    a8_scratch s;
+    if (a8_alloc(&s, c->d, c->I))
+        swiglu_row_a8(c->d, c->I, c->dtype, c->x_perm, p * c->d, &c->w_gate, &c->w_up,
+                      &c->w_down, wgu, wgu, wd, &s, c->y_perm + p * c->d,
+                      c->h_pre ? c->h_pre + p * c->I : NULL,
+                      c->h_hat ? c->h_hat + p * c->I : NULL);
+    a8_free(&s);
+}
+
+/*
+ * oracle_expert_ffn_w8a8: oracle_expert_ffn_fp8 with 8-bit activations: each
+ * row of x_perm (dtype) is quantised per row, h per row after its bf16
+ * rounding.  Optional taps [rows][I] (fp64): h_pre = h before rounding,
+ * h_hat = the dequantised quantised h.
+ */
+int oracle_expert_ffn_w8a8(int64_t d, int64_t E, int64_t I, int dtype,
+                           const void *x_perm, const int32_t *offsets,
+                           const uint8_t *w_gate, const uint8_t *w_up,
+                           const uint8_t *w_down, const float *s_gate,
+                           const float *s_up, const float *s_down, double *y_perm,
+                           double *h_pre, double *h_hat, int nthreads)
+{
+    if (d < 1 || E < 1 || I < 1 || !offsets || !y_perm || !w_gate || !w_up || !w_down ||
+        !s_gate || !s_up || !s_down || offsets[0] != 0)
+        return -1;
+    for (int64_t e = 0; e < E; ++e)
+        if (offsets[e + 1] < offsets[e])
+            return -1;
+    ffn_a8_ctx c = {d, E, I, dtype, x_perm, offsets, fp8_weight(w_gate, s_gate, d),
+                    fp8_weight(w_up, s_up, d), fp8_weight(w_down, s_down, I), y_perm,
+                    h_pre, h_hat};
+    par_for(offsets[E], nthreads, ffn_row_a8, &c);
+    return 0;
+}
+
+static void token_row_a8(void *vctx, int64_t r)
+{
+    tok_ctx *c = (tok_ctx *)vctx;
+    const int64_t t = c->tokens[r];
+    const int64_t d = c->d;
+    const int64_t hmax = c->I > c->Is ? c->I : c->Is;
+    double *sc = (double *)malloc(sizeof(double) * (size_t)c->E * 3);
+    double *key = sc + c->E, *aff = sc + 2 * c->E;
+    unsigned char *taken = (unsigned char *)malloc((size_t)c->E);
+    double *ye = (double *)malloc(sizeof(double) * (size_t)d);
+    int32_t *idx = c->idx + r * c->K;
+    double *w = c->w + r * c->K;
+    double *y = c->y + r * d;
+    a8_scratch s;
+    a8_alloc(&s, d, hmax);
+
+    router_scores(d, c->E, c->dtype, c->x, t, c->w_g, sc);
+    select_and_weigh(c->mode, c->E, c->K, sc, c->bias, key, aff, taken, idx, w);
+    if (c->logits)
+        memcpy(c->logits + r * c->E, key, sizeof(double) * (size_t)c->E);
+
+    /* y = SharedExpert(x_t) + sum_j w_j * Expert_{i_j}(x_t), every expert W8A8 */
+    if (c->Is) {
+        swiglu_row_a8(d, c->Is, c->dtype, c->x, t * d, &c->ws_gate, &c->ws_up, &c->ws_down,
+                      0, 0, 0, &s, y, NULL, NULL);
+    } else {
+        for (int64_t k = 0; k < d; ++k)
+            y[k] = 0.0;
+    }
+    for (int64_t j = 0; j < c->K; ++j) {
+        const int64_t e = idx[j];
+        const int64_t wgu = e * c->I * d, wd = e * d * c->I;
+        swiglu_row_a8(d, c->I, c->dtype, c->x, t * d, &c->w_gate, &c->w_up, &c->w_down, wgu,
+                      wgu, wd, &s, ye, NULL, NULL);
+        for (int64_t k = 0; k < d; ++k)
+            y[k] += w[j] * ye[k];
+    }
+    free(sc); free(taken); free(ye);
+    a8_free(&s);
+}
+
+/*
+ * oracle_forward_tokens_w8a8: oracle_forward_tokens_fp8 with every expert
+ * (routed and shared) run W8A8 as above; the router still reads the
+ * unquantised x.  Same arguments and outputs as oracle_forward_tokens_fp8.
+ */
+int oracle_forward_tokens_w8a8(int64_t n, const int32_t *tokens, int64_t T,
+                               int64_t d, int64_t E, int64_t K, int64_t I,
+                               int64_t Is, int dtype, int mode, const void *x,
+                               const void *w_g, const double *bias,
+                               const uint8_t *w_gate, const uint8_t *w_up,
+                               const uint8_t *w_down, const float *s_gate,
+                               const float *s_up, const float *s_down,
+                               const uint8_t *ws_gate, const uint8_t *ws_up,
+                               const uint8_t *ws_down, const float *ss_gate,
+                               const float *ss_up, const float *ss_down,
+                               double *y, int32_t *topk_idx, double *topk_w,
+                               double *logits, int nthreads)
+{
+    if (!w_gate || !w_up || !w_down || !s_gate || !s_up || !s_down)
+        return -1;
+    if (Is > 0 && (!ws_gate || !ws_up || !ws_down || !ss_gate || !ss_up || !ss_down))
+        return -1;
+    if (n < 0 || d < 1 || E < 1 || K < 1 || K > E || I < 1 || Is < 0 || !y ||
+        !topk_idx || !topk_w || (n > 0 && !tokens) ||
+        (mode != ORC_ROUTER_SOFTMAX && mode != ORC_ROUTER_SIGMOID))
+        return -1;
+    for (int64_t r = 0; r < n; ++r)
+        if (tokens[r] < 0 || tokens[r] >= T)
+            return -1;
+    tok_ctx c = {d, E, K, I, Is, dtype, mode, x, w_g, bias,
+                 fp8_weight(w_gate, s_gate, d), fp8_weight(w_up, s_up, d),
+                 fp8_weight(w_down, s_down, I),
+                 fp8_weight(ws_gate, ss_gate, d), fp8_weight(ws_up, ss_up, d),
+                 fp8_weight(ws_down, ss_down, Is),
+                 tokens, y, logits, topk_idx, topk_w};
+    par_for(n, nthreads, token_row_a8, &c);
     return 0;
 }

@@ -1,5 +1,6 @@
 """Plant plausible mistakes in a copy of the oracle (on the CPU) and check that
-the pins in test_oracle_pins.py catch every one of them."""
+the pins in test_oracle_pins.py, test_oracle_fp8.py and test_oracle_w8a8.py
+catch every one of them."""
 import ctypes
 import os
 
@@ -8,6 +9,7 @@ import pytest
 import oracle
 from tests import test_oracle_fp8 as pins8
 from tests import test_oracle_pins as pins
+from tests import test_oracle_w8a8 as pins_a8
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "moe_oracle.c")
 
@@ -17,8 +19,8 @@ MUTATIONS = [
     ("softmax_sign", "w[j] = exp(key[idx[j]] - kmax);", "w[j] = exp(kmax - key[idx[j]]);"),
     ("silu_sign", "double silu = g / (1.0 + exp(-g));", "double silu = g / (1.0 + exp(g));"),
     ("dropped_up_projection", "h[i] = silu * u;", "h[i] = silu;"),
-    ("transposed_down_projection", "load_weight(w_down, wd_off + j * I + i)",
-     "load_weight(w_down, wd_off + i * d + j)"),
+    ("transposed_down_projection", "load_weight(w_down, wd_off + j * I + i) * h[i]",
+     "load_weight(w_down, wd_off + i * d + j) * h[i]"),
     ("swapped_gate_and_up", "double silu = g / (1.0 + exp(-g));\n        h[i] = silu * u;",
      "double silu = u / (1.0 + exp(-u));\n        h[i] = silu * g;"),
     ("dropped_bias", "const double b = bias ? bias[e] : 0.0;", "const double b = 0.0;"),
@@ -40,6 +42,19 @@ MUTATIONS = [
     ("fp8_down_scale_row_length", "fp8_weight(w_down, s_down, I), fp8_weight(ws_gate",
      "fp8_weight(w_down, s_down, d), fp8_weight(ws_gate"),
     ("quant_scale_not_amax", "amax / 448.0f", "amax / 240.0f"),
+    ("a8_x_not_quantised", "s->xh[k] = e4m3_value(s->c[k]) * (double)sx;",
+     "s->xh[k] = (double)s->f[k];"),
+    ("a8_h_not_rounded_to_bf16", "s->f[i] = round_bf16((float)s->h[i]);",
+     "s->f[i] = (float)s->h[i];"),
+    ("a8_h_not_quantised", "s->h[i] = e4m3_value(s->c[i]) * (double)sh;",
+     "s->h[i] = (double)s->f[i];"),
+    ("a8_h_takes_the_input_scale", "s->h[i] = e4m3_value(s->c[i]) * (double)sh;",
+     "s->h[i] = e4m3_value(s->c[i]) * (double)sx;"),
+    ("a8_bf16_rounds_half_up", "u += 0x7fffu + ((u >> 16) & 1u);", "u += 0x8000u;"),
+    ("a8_down_scale_row_length", "fp8_weight(w_down, s_down, I), y_perm,\n                    h_pre",
+     "fp8_weight(w_down, s_down, d), y_perm,\n                    h_pre"),
+    ("a8_shared_expert_skipped", "swiglu_row_a8(d, c->Is, c->dtype, c->x, t * d, &c->ws_gate",
+     "if (0) swiglu_row_a8(d, c->Is, c->dtype, c->x, t * d, &c->ws_gate"),
 ]
 
 PIN_TESTS = [
@@ -62,6 +77,10 @@ PIN_TESTS = [
     lambda: pins8.test_encode_saturates_and_keeps_nan(),
     lambda: pins8.test_quantised_rows_meet_the_format_error_bound("f32"),
     lambda: pins8.test_fp8_layer_equals_the_layer_on_dequantised_weights("bf16", 0),
+    lambda: pins_a8.test_bf16_rounding_matches_torch_including_ties(),
+    lambda: pins_a8.test_w8a8_expert_matches_library_quantisation_at_every_step(1, [3, 0, 5, 1]),
+    lambda: pins_a8.test_w8a8_layer_equals_the_8bit_weight_layer_when_activations_are_exact(
+        "softmax", 32),
 ]
 
 
