@@ -82,17 +82,22 @@ def ffn_stage_bytes(cfg, n_active: int) -> int:
 
 
 class Forward:
-    """One moe_forward (or moe_forward_fp8 for 8-bit expert weights) on fixed
-    buffers; the argument structs are built once."""
+    """One moe_forward (moe_forward_fp8 for 8-bit expert weights,
+    moe_forward_w8a8 for 8-bit weights and activations) on fixed buffers; the
+    argument structs are built once."""
 
     def __init__(self, moe, cfg, s, p, bias, ws, stream):
         self.moe, self.cfg, self.s, self.p, self.bias, self.ws, self.stream = (
             moe, cfg, s, p, bias, ws, stream)
         self.fp8 = moe.make_fp8_experts(p) if cfg.weights == "e4m3" else None
+        self.a8 = cfg.acts == "e4m3"
 
     def __call__(self, x, y):
         m, p = self.moe, self.p
-        if self.fp8 is not None:
+        if self.a8:
+            m.moe_forward_w8a8(self.s, x, p["w_g"], self.bias, self.fp8, y, self.ws,
+                               stream=self.stream)
+        elif self.fp8 is not None:
             m.moe_forward_fp8(self.s, x, p["w_g"], self.bias, self.fp8, y, self.ws,
                               stream=self.stream)
         else:
@@ -106,7 +111,8 @@ def oracle_tokens(cfg, tokens, x_host, p_host, bias_host):
     import oracle
     if cfg.weights == "e4m3":
         return oracle.forward_tokens_fp8(tokens, x_host, p_host["w_g"], p_host, cfg.K,
-                                         dtype=cfg.dtype, bias=bias_host, router=cfg.router)
+                                         dtype=cfg.dtype, bias=bias_host, router=cfg.router,
+                                         act8=cfg.acts == "e4m3")
     return oracle.forward_tokens(tokens, x_host, p_host, cfg.K, dtype=cfg.dtype, bias=bias_host,
                                  router=cfg.router)
 
@@ -119,6 +125,13 @@ def launches_per_forward(cfg, gemv_limit: int = 0) -> int:
     single-SM tcgen05 gate/up and down GEMMs when needed, and the CTA-pair
     ones too when a group can hold more rows than one 128-row tile (or, with
     MOE_PAIR_MIN_ROWS set, at least that many rows), combine."""
+    if cfg.acts == "e4m3":
+        # router + top-K, 3 dispatch kernels, x quantiser, code gather, plan,
+        # tcgen05 gate/up, h quantiser (+ h_s), tcgen05 down -- the gate/up and
+        # down twice when a group can take pair tiles -- combine
+        pair = cfg.T > 128
+        return 2 + 3 + 1 + 1 + 1 + (2 if pair else 1) + (2 if cfg.Is else 1) \
+            + (2 if pair else 1) + 1
     if cfg.weights == "e4m3":
         # router + top-K, 3 dispatch kernels, row gather, plan, the 8-bit GEMV
         # (gate/up and down for each of its two group lists), the tcgen05
@@ -339,7 +352,7 @@ def run_ours(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": cfg.dtype,
+        "dtype": "e4m3" if cfg.acts == "e4m3" else cfg.dtype,
         "data": ("synthetic (seeded N(0,1) tokens, N(0,1/d) weights; no trained weights)"
                  if cfg.weights != "e4m3" else
                  "synthetic (seeded N(0,1) tokens; random E4M3 expert codes with fp32 row "
@@ -348,6 +361,8 @@ def run_ours(args):
                    "inter": cfg.I, "inter_shared": cfg.Is, "active_experts": n_active,
                    "expert_weights": "e4m3 + fp32 row scales" if cfg.weights == "e4m3"
                                      else cfg.dtype,
+                   "expert_activations": ("e4m3 + fp32 row scales (x and h quantised per row)"
+                                          if cfg.acts == "e4m3" else cfg.dtype),
                    "l2": "inputs larger than L2 (expert weights "
                          f"{cfg.E * expert_bytes(cfg, cfg.I) / 1e9:.2f} GB), no flush",
                    "parallelism": f"replicas x{ws_n} (independent batches, no collective)"},
@@ -415,7 +430,9 @@ def time_expert_ffn(moe, cfg, x, p, bias, stream, steps: int, n_active: int) -> 
     fp8 = moe.make_fp8_experts(p) if cfg.weights == "e4m3" else None
 
     def run():
-        if fp8 is not None:
+        if cfg.acts == "e4m3":
+            moe.moe_expert_ffn_w8a8(s, x_perm, offsets, fp8, y_perm, ws, stream=stream)
+        elif fp8 is not None:
             moe.moe_expert_ffn_fp8(s, x_perm, offsets, fp8, y_perm, ws, stream=stream)
         else:
             moe.moe_expert_ffn(s, x_perm, offsets, p["w_gate"], p["w_up"], p["w_down"], y_perm,
@@ -452,15 +469,29 @@ def stage_traffic(workload: str):
     return rec["bytes"] if sha == rec["ffn_tc_sha256"] else None
 
 
+def tensor_peak(cfg, peaks) -> tuple:
+    """Dense tensor peak for the dtype the expert GEMMs multiply in: bf16 as
+    measured, or (8-bit activations: E4M3 x E4M3) the measured bf16 peak times
+    the nominal fp8 / bf16 ratio 4.5 / 2.25 = 2."""
+    if cfg.acts == "e4m3":
+        return 2.0 * peaks["bf16_tflops"], (f"fp8 dense = 2 x measured bf16 burst "
+                                            f"(nominal ratio), {peaks['source']}")
+    return peaks["bf16_tflops"], f"bf16 dense, burst, {peaks['source']}"
+
+
 def stage_roofline(cfg, stage, peaks) -> dict:
     """The expert-FFN stage against the roofline that binds it: the tensor
-    pipe (bf16 dense) or HBM, whichever the stage comes closer to."""
+    pipe (dense, in the GEMMs' operand type) or HBM, whichever the stage comes
+    closer to."""
     sec = stage["ms"] / 1e3
     tflops = stage["flops"] / sec / 1e12
     gbs = stage["bytes"] / sec / 1e9
-    t_frac, h_frac = tflops / peaks["bf16_tflops"], gbs / peaks["hbm_gbs"]
+    t_peak, t_kind = tensor_peak(cfg, peaks)
+    t_frac, h_frac = tflops / t_peak, gbs / peaks["hbm_gbs"]
     kernel = ("expert FFN stage: tcgen05 gate/up GEMM (SiLU*mul epilogue) + tcgen05 down GEMM "
-              + ("on E4M3 weights widened in-kernel" if cfg.weights == "e4m3" else
+              + ("on E4M3 weights and E4M3 activations (kind::f8f6f4, + x and h quantisers)"
+                 if cfg.acts == "e4m3" else
+                 "on E4M3 weights widened in-kernel" if cfg.weights == "e4m3" else
                  "(+ plan, empty GEMV launches)"))
     common = {"traffic": stage_traffic(cfg.name),
               "traffic_unit": "bytes per launch pair (DRAM read + write, ncu)",
@@ -468,9 +499,8 @@ def stage_roofline(cfg, stage, peaks) -> dict:
               "per_launch_bytes": stage["bytes"], "ms_per_launch": stage["ms"],
               "other_frac": None}
     if t_frac >= h_frac:
-        out = {"bound": "tensor", "achieved": tflops, "peak": peaks["bf16_tflops"],
-               "unit": "TFLOP/s", "frac": t_frac,
-               "peak_kind": f"bf16 dense, burst, {peaks['source']}"}
+        out = {"bound": "tensor", "achieved": tflops, "peak": t_peak,
+               "unit": "TFLOP/s", "frac": t_frac, "peak_kind": t_kind}
         common["other_frac"] = {"hbm": h_frac}
     else:
         out = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -565,7 +595,7 @@ def bench_workload(moe, cfg, peaks, steps: int, graph: bool = False) -> dict:
     out["hbm_gbs"] = gbs
     out["hbm_frac"] = gbs / peaks["hbm_gbs"]
     out["tensor_tflops"] = tfs
-    out["tensor_frac"] = tfs / peaks["bf16_tflops"]
+    out["tensor_frac"] = tfs / tensor_peak(cfg, peaks)[0]
     code = moe.moe_get_device_error(ws)
     if code:
         raise RuntimeError(f"device error in {cfg.name}: {moe.status_string(code)}")
@@ -579,7 +609,8 @@ def bench_all(moe, peaks, args) -> list:
     for name in ("tiny_f32", "mixtral_prefill", "dsv3_decode", "dsv3_prefill_zipf",
                  *[f"dsv3_sweep_T{t}" for t in mi.SWEEP_T], "dsv3_decode_sigmoid",
                  "dsv3_decode_fp8", "dsv3_sweep_fp8_T64", "dsv3_sweep_fp8_T512",
-                 "mixtral_prefill_fp8"):
+                 "mixtral_prefill_fp8", "dsv3_sweep_w8a8_T512", "dsv3_sweep_w8a8_T4096",
+                 "mixtral_prefill_w8a8"):
         cfg = mi.CONFIGS[name]
         res.append(bench_workload(moe, cfg, peaks, steps=max(10, args.steps),
                                   graph=cfg.T <= 64))

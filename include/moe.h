@@ -274,6 +274,38 @@ moe_status moe_forward_fp8(const moe_shape *shape, const void *x, const void *w_
                            void *workspace, size_t ws_bytes, void *stream);
 
 /*
+ * ---- 8-bit weights AND 8-bit activations (W8A8) ----------------------------
+ * [Q] names weights, activations and the KV cache as things a quantisation
+ * method may act on.  Here the same per-row rule quantises the two
+ * activations that enter an expert's matrix products:
+ *     x_hat = e4m3_value(code(x row)) * s_x,      s_x = amax(x row) / 448
+ *     h     = SiLU(W_gate_hat x_hat) * (W_up_hat x_hat)  (fp32, stored bf16)
+ *     h_hat = e4m3_value(code(h row)) * s_h,      s_h = amax(h row) / 448
+ *     y     = W_down_hat h_hat
+ * (scales and codes decided exactly as in moe_quantize_fp8_rows: fp32
+ * divisions, round to nearest even, saturation at 448), with the 8-bit
+ * weights of moe_fp8_experts.  Both operands of every expert GEMM are E4M3,
+ * multiplied on tcgen05 kind::f8f6f4 with fp32 accumulation; both row scales
+ * are applied to the fp32 sums.  Every group runs on the tensor cores, so
+ * this is the prefill path; for decode moe_forward_fp8 streams the same
+ * weights with bf16 activations.  The router reads the unquantised x.
+ * Limits and workspace as moe_forward_fp8 / moe_expert_ffn_fp8.
+ */
+
+/* moe_expert_ffn_fp8 with 8-bit activations: each x_perm row is quantised
+ * (per row) before the gate/up GEMM, each h row after it. */
+moe_status moe_expert_ffn_w8a8(const moe_shape *shape, const void *x_perm,
+                               const int32_t *offsets, const moe_fp8_experts *w,
+                               void *y_perm, void *workspace, size_t ws_bytes,
+                               void *stream);
+
+/* moe_forward_fp8 with every expert (routed and shared) run W8A8; each token's
+ * row of x is quantised once and its codes gathered into expert order. */
+moe_status moe_forward_w8a8(const moe_shape *shape, const void *x, const void *w_g,
+                            const float *bias, const moe_fp8_experts *w, void *y,
+                            void *workspace, size_t ws_bytes, void *stream);
+
+/*
  * Reads the device error word of `workspace` (a device pointer passed to a
  * previous call) into *code_out (a HOST pointer): MOE_OK, MOE_ERR_TIMEOUT or
  * MOE_ERR_BOUNDS.  Synchronous (a 4-byte device-to-host copy); call it after

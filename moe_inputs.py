@@ -29,6 +29,9 @@ Workloads (shapes and distributions; names by what they are):
                       with an RMS of about 162; each weight row has its own fp32
                       scale std / 162 * U(0.8, 1.2), std being the bf16 workload's
                       weight std.  The router weights stay bf16.
+  mixtral_prefill_w8a8, dsv3_sweep_w8a8_T{512,4096}
+                      the 8-bit-weight workloads run with 8-bit activations too
+                      (the library quantises x and the hidden rows per row).
 
 Every tensor has its own sub-seed, splitmix64(seed ^ fnv1a64(name)), so adding
 or resizing one tensor never changes another.  Large weights are drawn one
@@ -65,6 +68,7 @@ class LayerConfig:
     zipf_bias: bool = False
     router: str = "softmax"   # "softmax" or "sigmoid" (DeepSeek-V3 affinities)
     weights: str = "act"      # "act": experts in dtype; "e4m3": 8-bit codes + row scales
+    acts: str = "act"         # "e4m3": the experts' input and hidden rows quantised (W8A8)
     seed: int = 0
     extra: dict = field(default_factory=dict, compare=False)
 
@@ -95,6 +99,13 @@ for _t in (64, 512):
 # for multi-pass counter captures, still far larger than L2
 CONFIGS["dsv3_decode_fp8_E32"] = replace(CONFIGS["dsv3_decode_fp8"], name="dsv3_decode_fp8_E32",
                                          E=32)
+# 8-bit weights and 8-bit activations (W8A8): the same weights; the library
+# quantises x and h itself, so no extra tensor is drawn
+CONFIGS["mixtral_prefill_w8a8"] = replace(CONFIGS["mixtral_prefill_fp8"],
+                                          name="mixtral_prefill_w8a8", acts="e4m3")
+for _t in (512, 4096):
+    CONFIGS[f"dsv3_sweep_w8a8_T{_t}"] = replace(CONFIGS["dsv3_decode_fp8"],
+                                                name=f"dsv3_sweep_w8a8_T{_t}", T=_t, acts="e4m3")
 SWEEP_T = (1, 8, 64, 512, 4096)
 for _t in SWEEP_T:
     CONFIGS[f"dsv3_sweep_T{_t}"] = LayerConfig(f"dsv3_sweep_T{_t}", T=_t, d=7168, E=256, K=8,

@@ -25,7 +25,7 @@ MOE_ROUTER_SOFTMAX, MOE_ROUTER_SIGMOID = 0, 1
 EXPORTED = ("moe_status_string", "moe_workspace_bytes", "moe_route", "moe_permute",
             "moe_permute_noalloc", "moe_expert_ffn", "moe_combine", "moe_forward",
             "moe_quantize_fp8_rows", "moe_expert_ffn_fp8", "moe_forward_fp8",
-            "moe_get_device_error")
+            "moe_expert_ffn_w8a8", "moe_forward_w8a8", "moe_get_device_error")
 
 
 class MoeError(RuntimeError):
@@ -70,10 +70,12 @@ def _load_lib() -> ctypes.CDLL:
     lib.moe_quantize_fp8_rows.argtypes = [ctypes.c_int64, ctypes.c_int64, i32, vp, vp, vp, vp]
     lib.moe_expert_ffn_fp8.argtypes = [sp, vp, vp, fp, vp, vp, sz, vp]
     lib.moe_forward_fp8.argtypes = [sp, vp, vp, vp, fp, vp, vp, sz, vp]
+    lib.moe_expert_ffn_w8a8.argtypes = [sp, vp, vp, fp, vp, vp, sz, vp]
+    lib.moe_forward_w8a8.argtypes = [sp, vp, vp, vp, fp, vp, vp, sz, vp]
     lib.moe_get_device_error.argtypes = [vp, ctypes.POINTER(i32)]
     for f in ("moe_route", "moe_permute", "moe_permute_noalloc", "moe_expert_ffn", "moe_combine",
               "moe_forward", "moe_quantize_fp8_rows", "moe_expert_ffn_fp8", "moe_forward_fp8",
-              "moe_get_device_error"):
+              "moe_expert_ffn_w8a8", "moe_forward_w8a8", "moe_get_device_error"):
         getattr(lib, f).restype = i32
     return lib
 
@@ -212,6 +214,20 @@ def moe_forward_fp8(shape, x, w_g, bias, w: moe_fp8_experts, y, workspace, strea
     ws, nws = _ws(workspace)
     _check(_lib.moe_forward_fp8(ctypes.byref(shape), _p(x), _p(w_g), _p(bias), ctypes.byref(w),
                                 _p(y), ws, nws, _stream(stream)), "moe_forward_fp8")
+
+
+def moe_expert_ffn_w8a8(shape, x_perm, offsets, w: moe_fp8_experts, y_perm, workspace,
+                        stream=None):
+    ws, nws = _ws(workspace)
+    _check(_lib.moe_expert_ffn_w8a8(ctypes.byref(shape), _p(x_perm), _p(offsets),
+                                    ctypes.byref(w), _p(y_perm), ws, nws, _stream(stream)),
+           "moe_expert_ffn_w8a8")
+
+
+def moe_forward_w8a8(shape, x, w_g, bias, w: moe_fp8_experts, y, workspace, stream=None):
+    ws, nws = _ws(workspace)
+    _check(_lib.moe_forward_w8a8(ctypes.byref(shape), _p(x), _p(w_g), _p(bias), ctypes.byref(w),
+                                 _p(y), ws, nws, _stream(stream)), "moe_forward_w8a8")
 
 
 def moe_get_device_error(workspace) -> int:

@@ -144,12 +144,15 @@ dispatch_scatter_kernel(const int32_t* __restrict__ idx, int64_t n, int E, int K
 // One warp per (token, 128 16-byte vectors of its row): the slice of x is read
 // once (four loads in flight per lane) and written to the token's K permuted
 // positions inv_perm[t*K + j], so x crosses HBM once even when it does not fit
-// in L2, and a few tokens still spread over many warps.
+// in L2, and a few tokens still spread over many warps.  Rows are opaque
+// bytes (bf16, fp32 or E4M3 codes); with s_src set, the warp that copies the
+// first slice of a row also copies the row's scale s_src[t] to s_dst[p].
 constexpr int kGatherVecs = 32 * 4;  // vectors per warp item
 
 __global__ void __launch_bounds__(256)
 gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ inv_perm,
-                   uint4* __restrict__ x_perm, int Tn, int K, int vec_per_row, int64_t n_rows) {
+                   uint4* __restrict__ x_perm, int Tn, int K, int vec_per_row, int64_t n_rows,
+                   const float* __restrict__ s_src, float* __restrict__ s_dst) {
     pdl_wait();
     pdl_trigger();
     const int lane = threadIdx.x & 31;
@@ -160,6 +163,7 @@ gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ inv_
         const int64_t t = w / nchunks;
         const int v0 = (int)(w - t * nchunks) * kGatherVecs + lane;
         const int32_t my_p = lane < K ? inv_perm[t * K + lane] : -1;
+        if (s_src != nullptr && v0 < 32 && my_p >= 0 && my_p < n_rows) s_dst[my_p] = s_src[t];
         const uint4* src = x + t * vec_per_row;
         uint4 tmp[4];
 #pragma unroll
@@ -214,7 +218,21 @@ cudaError_t launch_gather_rows(const moe_shape& s, const void* x, const int32_t*
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     return launch_pdl(gather_rows_kernel, dim3((unsigned)blocks), dim3(256), 0, st, (const uint4*)x,
-                      inv_perm, (uint4*)x_perm, s.T, s.K, vpr, rows);
+                      inv_perm, (uint4*)x_perm, s.T, s.K, vpr, rows, (const float*)nullptr,
+                      (float*)nullptr);
+}
+
+cudaError_t launch_gather_codes(const moe_shape& s, const uint8_t* xq, const float* sx,
+                                const int32_t* inv_perm, uint8_t* xq_perm, float* s_perm,
+                                cudaStream_t st) {
+    const int64_t rows = (int64_t)s.T * s.K;
+    const int vpr = s.d / 16;
+    int64_t blocks = ceil_div((int64_t)s.T * ceil_div(vpr, kGatherVecs), 8);
+    const int64_t cap = (int64_t)device_sm_count() * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    return launch_pdl(gather_rows_kernel, dim3((unsigned)blocks), dim3(256), 0, st,
+                      (const uint4*)xq, inv_perm, (uint4*)xq_perm, s.T, s.K, vpr, rows, sx, s_perm);
 }
 
 }  // namespace moe

@@ -68,21 +68,22 @@ namespace {
 constexpr int BMC = 128;  // accumulator rows per CTA
 constexpr int BN = 256;   // MMA N
 constexpr int BK = 64;
-constexpr int kMaxStages = 6;
+constexpr int kMaxStages = 7;
 constexpr uint32_t kABytes = BMC * BK * 2;  // 16 KB
-constexpr uint32_t kRingBytes = 192 * 1024; // 4 x 48 KB (single) = 6 x 32 KB (pair)
 constexpr int kThreadsTc = 192;
 constexpr uint32_t kTmemCols = 512;
 
 template <bool PAIR> struct Shape {
     static constexpr int kTileRows = PAIR ? 256 : 128;  // rows per tile
     static constexpr int kBRows = PAIR ? 128 : 256;     // weight rows per CTA per K step
-    static constexpr int kStages = PAIR ? 6 : 4;
+    static constexpr int kStages = PAIR ? 7 : 4;
     static constexpr int kBand = PAIR ? 4 : 8;          // m-tiles per band (1024 rows)
     static constexpr uint32_t kBBytes = kBRows * BK * 2;
     static constexpr uint32_t kStageBytes = kABytes + kBBytes;
+    // 4 x 48 KB (single) or 7 x 32 KB (pair)
+    static constexpr uint32_t kRingBytes = kStages * kStageBytes;
     static constexpr uint32_t kEpiArrivals = PAIR ? 8 : 4;  // epilogue warps per tile
-    static_assert(kStages * kStageBytes == kRingBytes, "ring size");
+    static_assert(kStages <= kMaxStages, "stage barriers");
 };
 
 enum Epi { EPI_SWIGLU = 0, EPI_STORE_BF16 = 1, EPI_STORE_F32 = 2 };
@@ -150,8 +151,9 @@ struct TcParams {
     CUtensorMap q0[2];          // W8: E4M3 gate / down codes, box 128 rows x 128 codes
     CUtensorMap q1[2];          // W8: E4M3 up codes (SWIGLU only)
     CUtensorMap qw[2];          // W8: E4M3 codes, box 256 rows x 128 codes (non-SWIGLU)
-    const float* sc0[2];        // W8: scale of each gate / down weight row
-    const float* sc1[2];        // W8: scale of each up weight row
+    const float* sc0[2];        // W8, A8: scale of each gate / down weight row
+    const float* sc1[2];        // W8, A8: scale of each up weight row
+    const float* sa[2];         // A8: scale of each activation row (routed, shared)
     const int32_t* row_src;     // token of each routed row (gather from x), or null
     int gather_max;             // gather a CTA's routed rows when it has at most this many
     const FfnPlanHeader* hdr;
@@ -180,7 +182,9 @@ struct Tile {
     bool valid;
 };
 
-template <int EPI, bool PAIR>
+// KSTEP: elements of the reduction per K block (64 bf16 or 128 8-bit values,
+// 128 bytes either way)
+template <int EPI, bool PAIR, int KSTEP>
 __device__ __forceinline__ Tile decode_tile(const TcParams& p, int n_tiles_in_list, int t) {
     using S = Shape<PAIR>;
     constexpr int kNCols = EPI == EPI_SWIGLU ? BN / 2 : BN;  // output columns per n-block
@@ -208,7 +212,7 @@ __device__ __forceinline__ Tile decode_tile(const TcParams& p, int n_tiles_in_li
     tl.rows = min(S::kTileRows, Mg - mi * S::kTileRows);
     tl.n0 = nb * kNCols;
     tl.wrow0 = (tl.kind == 0 ? g * p.wrows[0] : 0) + tl.n0;
-    tl.kblocks = (p.kdim[tl.kind] + BK - 1) / BK;
+    tl.kblocks = (p.kdim[tl.kind] + KSTEP - 1) / KSTEP;
     tl.valid = tl.n0 < p.n_out[tl.kind] && tl.rows > 0;
     return tl;
 }
@@ -305,12 +309,15 @@ __device__ __forceinline__ void ld_scale16(const float* src, float (&s)[16]) {
     }
 }
 
-template <int EPI, bool PAIR, bool W8 = false>
+template <int EPI, bool PAIR, bool W8 = false, bool A8 = false>
 __global__ void __launch_bounds__(W8 ? kThreadsW8 : kThreadsTc, 1)
 tc_gemm_kernel(const __grid_constant__ TcParams p) {
     static_assert(!(W8 && EPI == EPI_STORE_F32), "8-bit weights feed the expert GEMMs only");
+    static_assert(!(A8 && (W8 || EPI == EPI_STORE_F32)), "A8: 8-bit operands, expert GEMMs only");
     using S = Shape<PAIR>;
     using W = W8Shape<PAIR>;
+    // A8: both operands E4M3 (kind::f8f6f4); a 128-byte K block holds 128 values
+    constexpr int kKStep = A8 ? 2 * BK : BK;
     constexpr int kStages = W8 ? W::kConv : S::kStages;  // B stages (and A stages without W8)
     constexpr int kAStages = W8 ? W::kA : S::kStages;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -319,7 +326,7 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
     uint8_t* sA = smem;
     uint8_t* sB = smem + kAStages * kABytes;
     uint8_t* sRaw = sB + kStages * S::kBBytes;  // W8 only
-    SmemCtl* ctl = (SmemCtl*)(smem + (W8 ? kW8RingBytes : kRingBytes));
+    SmemCtl* ctl = (SmemCtl*)(smem + (W8 ? kW8RingBytes : S::kRingBytes));
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = PAIR ? ptx::cluster_ctarank() : 0u;  // 0 issues the MMAs
@@ -413,7 +420,7 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
                 const uint32_t afull0 = PAIR ? ptx::map_to_rank(&ctl->afull[0], 0) : 0u;
                 bool ok = p.test_stall == 0;
                 for (int t = unit; t < n_tiles && ok; t += n_units) {
-                    const Tile tl = decode_tile<EPI, PAIR>(p, list_len, t);
+                    const Tile tl = decode_tile<EPI, PAIR, kKStep>(p, list_len, t);
                     if (!tl.valid) continue;
                     const int rows_me = max(0, min(BMC, tl.rows - (int)rank * BMC));
                     const CUtensorMap* ma = &p.a[tl.kind][abox_for(rows_me)];
@@ -494,7 +501,7 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
             const uint32_t full0 = PAIR ? ptx::map_to_rank(&ctl->full[0], 0) : 0u;
             bool ok = p.test_stall == 0;
             for (int t = unit; t < n_tiles && ok; t += n_units) {
-                const Tile tl = decode_tile<EPI, PAIR>(p, list_len, t);
+                const Tile tl = decode_tile<EPI, PAIR, kKStep>(p, list_len, t);
                 if (!tl.valid) continue;
                 const int rows_me = max(0, min(BMC, tl.rows - (int)rank * BMC));
                 const CUtensorMap* ma = &p.a[tl.kind][abox_for(rows_me)];
@@ -533,7 +540,7 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
                     if (lane == 0) {
                         for (int kb = 0; kb < tl.kblocks; ++kb) {
                             if (!wait_bounded(&ctl->empty[stage], phase ^ 1u, ctl, p, 100)) { ok = false; break; }
-                            const int k0 = kb * BK;
+                            const int k0 = kb * kKStep;
                             uint8_t* a_dst = sA + stage * kABytes;
                             uint8_t* b_dst = sB + stage * S::kBBytes;
                             if constexpr (PAIR) {
@@ -561,7 +568,7 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
                     for (int kb = 0; kb < tl.kblocks; ++kb) {
                         const int okw = lane == 0 ? (int)wait_bounded(&ctl->empty[stage], phase ^ 1u, ctl, p, 100) : 0;
                         if (!__shfl_sync(0xffffffffu, okw, 0)) { ok = false; break; }
-                        const int k0 = kb * BK;
+                        const int k0 = kb * kKStep;
                         uint8_t* a_dst = sA + stage * kABytes;
                         uint8_t* b_dst = sB + stage * S::kBBytes;
                         if constexpr (PAIR) {
@@ -611,7 +618,8 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer (rank 0)
         if (lane == 0 && rank == 0) {
-            constexpr uint32_t idesc = ptx::idesc_bf16_f32(S::kTileRows, BN);
+            constexpr uint32_t idesc = A8 ? ptx::idesc_e4m3_f32(S::kTileRows, BN)
+                                          : ptx::idesc_bf16_f32(S::kTileRows, BN);
             int stage = 0;       // B stage (and A stage without W8)
             uint32_t phase = 0;
             int ast = 0;         // W8: A stage
@@ -621,7 +629,7 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
             bool ok = true;
             bool any = false;
             for (int t = unit; t < n_tiles && ok; t += n_units) {
-                const Tile tl = decode_tile<EPI, PAIR>(p, list_len, t);
+                const Tile tl = decode_tile<EPI, PAIR, kKStep>(p, list_len, t);
                 if (!tl.valid) continue;
                 if (!wait_bounded(&ctl->tempty[acc], acc_phase ^ 1u, ctl, p, 200)) { ok = false; break; }
                 ptx::tc_fence_after();
@@ -633,12 +641,18 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
                     const uint32_t a_base = ptx::smem_u32(sA + (W8 ? ast : stage) * kABytes);
                     const uint32_t b_base = ptx::smem_u32(sB + stage * S::kBBytes);
 #pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk) {
+                    // four MMAs per 128-byte K block: K = 16 bf16 or 32 E4M3 values each
+                    for (int kk = 0; kk < 4; ++kk) {
                         const uint64_t ad = ptx::sw128_kmajor_desc(a_base + kk * 32);
                         const uint64_t bd = ptx::sw128_kmajor_desc(b_base + kk * 32);
                         const uint32_t accum = (kb | kk) != 0 ? 1u : 0u;
-                        if constexpr (PAIR) ptx::tc_mma_f16_pair(d_tmem, ad, bd, idesc, accum);
-                        else ptx::tc_mma_f16(d_tmem, ad, bd, idesc, accum);
+                        if constexpr (A8) {
+                            if constexpr (PAIR) ptx::tc_mma_f8_pair(d_tmem, ad, bd, idesc, accum);
+                            else ptx::tc_mma_f8(d_tmem, ad, bd, idesc, accum);
+                        } else {
+                            if constexpr (PAIR) ptx::tc_mma_f16_pair(d_tmem, ad, bd, idesc, accum);
+                            else ptx::tc_mma_f16(d_tmem, ad, bd, idesc, accum);
+                        }
                     }
                     any = true;
                     if constexpr (PAIR) ptx::tc_commit_pair(&ctl->empty[stage], 0x3);
@@ -673,7 +687,7 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int t = unit; t < n_tiles; t += n_units) {
-            const Tile tl = decode_tile<EPI, PAIR>(p, list_len, t);
+            const Tile tl = decode_tile<EPI, PAIR, kKStep>(p, list_len, t);
             if (!tl.valid) continue;
             // one lane waits, the warp follows its verdict (tcgen05.ld needs the whole warp)
             const int ok = lane == 0 ? (int)wait_bounded(&ctl->tfull[acc], acc_phase, ctl, p, 300) : 0;
@@ -684,6 +698,8 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
             const bool row_ok = r < rows_me;
             const int64_t orow = (int64_t)tl.row0 + (int64_t)rank * BMC + r;
             const int nvalid = p.n_out[tl.kind];
+            // A8: the activation row's scale factors out of every output of the row
+            const float sa = (A8 && row_ok) ? __ldg(p.sa[tl.kind] + (tl.row0 + (int)rank * BMC + r)) : 1.0f;
             if (EPI == EPI_SWIGLU) {
                 bf16* out = (bf16*)p.out[tl.kind] + orow * p.ld_out[tl.kind] + tl.n0;
 #pragma unroll 1
@@ -694,9 +710,13 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
                     ptx::tmem_ld_wait();
                     if (row_ok && tl.n0 + c < nvalid) {
                         float gs[16], us[16];
-                        if constexpr (W8) {
+                        if constexpr (W8 || A8) {
                             ld_scale16(p.sc0[tl.kind] + tl.wrow0 + c, gs);
                             ld_scale16(p.sc1[tl.kind] + tl.wrow0 + c, us);
+                            if constexpr (A8) {
+#pragma unroll
+                                for (int k = 0; k < 16; ++k) { gs[k] *= sa; us[k] *= sa; }
+                            }
                         } else {
 #pragma unroll
                             for (int k = 0; k < 16; ++k) { gs[k] = 1.0f; us[k] = 1.0f; }
@@ -725,8 +745,12 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
                     ptx::tmem_ld_wait();
                     if (row_ok && tl.n0 + c < nvalid) {
                         float ds[16];
-                        if constexpr (W8) {
+                        if constexpr (W8 || A8) {
                             ld_scale16(p.sc0[tl.kind] + tl.wrow0 + c, ds);
+                            if constexpr (A8) {
+#pragma unroll
+                                for (int k = 0; k < 16; ++k) ds[k] *= sa;
+                            }
                         } else {
 #pragma unroll
                             for (int k = 0; k < 16; ++k) ds[k] = 1.0f;
@@ -779,7 +803,7 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
             uint32_t rph = 0, cph = 0;
             bool ok = true;
             for (int t = unit; t < n_tiles && ok; t += n_units) {
-                const Tile tl = decode_tile<EPI, PAIR>(p, list_len, t);
+                const Tile tl = decode_tile<EPI, PAIR, kKStep>(p, list_len, t);
                 if (!tl.valid) continue;
                 for (int kb = 0; kb < tl.kblocks; ++kb) {
                     const int h = kb & 1;
@@ -857,14 +881,16 @@ bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int 
     return r == CUDA_SUCCESS;
 }
 
-// 2-D map over a row-major [rows][cols] matrix of E4M3 codes, box = 128 codes
-// x box_rows rows, 128-byte swizzle (cols a multiple of 128).
-bool make_map_u8(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int box_rows) {
+// 2-D map over a row-major [rows][cols] matrix of E4M3 codes with rows ld
+// bytes apart (0: cols), box = 128 codes x box_rows rows, 128-byte swizzle
+// (cols a multiple of 128, ld a multiple of 16).
+bool make_map_u8(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int box_rows,
+                 int64_t ld = 0) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     if (rows <= 0) rows = 1;
     const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)cols};
+    const cuuint64_t strides[1] = {(cuuint64_t)(ld > 0 ? ld : cols)};
     const cuuint32_t box[2] = {128u, (cuuint32_t)box_rows};
     const cuuint32_t estr[2] = {1, 1};
     const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
@@ -878,6 +904,14 @@ bool make_map_u8(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, i
 bool make_amaps(CUtensorMap (&m)[kABoxes], const void* base, int64_t rows, int64_t cols) {
     bool ok = true;
     for (int b = 0; b < kABoxes; ++b) ok &= make_map(&m[b], base, rows, cols, abox_rows(b));
+    return ok;
+}
+
+// the four activation maps of a matrix of E4M3 codes (rows ld bytes apart)
+bool make_amaps_u8(CUtensorMap (&m)[kABoxes], const void* base, int64_t rows, int64_t cols,
+                   int64_t ld) {
+    bool ok = true;
+    for (int b = 0; b < kABoxes; ++b) ok &= make_map_u8(&m[b], base, rows, cols, abox_rows(b), ld);
     return ok;
 }
 
@@ -901,14 +935,16 @@ int test_stall() {
     return (s && atoi(s) != 0) ? 1 : 0;
 }
 
-constexpr size_t kSmemBytes = 1024 + kRingBytes + sizeof(SmemCtl) + 64;
+template <bool PAIR> constexpr size_t kSmemBytes = 1024 + Shape<PAIR>::kRingBytes + sizeof(SmemCtl) + 64;
 constexpr size_t kSmemBytesW8 = 1024 + kW8RingBytes + sizeof(SmemCtl) + 64;
+static_assert(kSmemBytes<true> <= 232448 && kSmemBytes<false> <= 232448,
+              "shared memory exceeds the per-CTA limit");
 static_assert(kSmemBytesW8 <= 232448, "W8 shared memory exceeds the per-CTA limit");
 
-template <int EPI, bool PAIR, bool W8 = false>
+template <int EPI, bool PAIR, bool W8 = false, bool A8 = false>
 cudaError_t launch_tc(const TcParams& p, cudaStream_t st) {
-    constexpr size_t smem = W8 ? kSmemBytesW8 : kSmemBytes;
-    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<EPI, PAIR, W8>,
+    constexpr size_t smem = W8 ? kSmemBytesW8 : kSmemBytes<PAIR>;
+    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<EPI, PAIR, W8, A8>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int sms = device_sm_count();
@@ -933,10 +969,10 @@ cudaError_t launch_tc(const TcParams& p, cudaStream_t st) {
         attr[1].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
         cfg.attrs = attr;
         cfg.numAttrs = 2;
-        e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel<EPI, PAIR, W8>, p);
+        e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel<EPI, PAIR, W8, A8>, p);
         if (e != cudaSuccess) return e;
     } else {
-        e = launch_pdl(tc_gemm_kernel<EPI, PAIR, W8>, dim3(units), dim3(W8 ? kThreadsW8 : kThreadsTc),
+        e = launch_pdl(tc_gemm_kernel<EPI, PAIR, W8, A8>, dim3(units), dim3(W8 ? kThreadsW8 : kThreadsTc),
                        smem, st, p);
         if (e != cudaSuccess) return e;
     }
@@ -1170,6 +1206,118 @@ cudaError_t launch_ffn_tc_fp8(const FfnGroups& g, const FfnPlanHeader* hdr, cons
     }
     q.mtiles = single_list;
     return launch_tc<EPI_STORE_BF16, false, true>(q, st);
+}
+
+// The expert FFN with E4M3 weights AND E4M3 activations (kind::f8f6f4): the
+// gate/up GEMM on the quantised rows g.a_perm / g.a_shared (scales
+// g.sa_routed / g.sa_shared) writes bf16 h / h_s; the caller quantises those
+// in place (codes at the start of each row, 2 * I bytes apart) and runs the
+// down GEMM on them (scales g.sa_h / g.sa_hs).  The plan's tiles as in
+// launch_ffn_tc: pair tiles (when may_pair) and single-SM tiles.
+cudaError_t launch_ffn_tc_a8_gate_up(const FfnGroups& g, const FfnPlanHeader* hdr,
+                                     const int4* mtile_list, int max_mtiles, bool may_pair,
+                                     DevError* err, cudaStream_t st) {
+    const int64_t R = g.n_routed_rows;
+    TcParams p{};
+    bool ok = true;
+    ok &= make_amaps_u8(p.a[0], g.a_perm, R, g.d, g.d);
+    p.ag = p.a[0][0];
+    p.row_src = nullptr;
+    p.gather_max = 0;
+    ok &= make_map_u8(&p.b0[0], g.w_gate, (int64_t)g.E * g.I, g.d, 128);
+    ok &= make_map_u8(&p.b1[0], g.w_up, (int64_t)g.E * g.I, g.d, 128);
+    p.sc0[0] = g.s_gate;
+    p.sc1[0] = g.s_up;
+    p.sa[0] = g.sa_routed;
+    if (g.has_shared) {
+        ok &= make_amaps_u8(p.a[1], g.a_shared, g.T, g.d, g.d);
+        ok &= make_map_u8(&p.b0[1], g.ws_gate, g.Is, g.d, 128);
+        ok &= make_map_u8(&p.b1[1], g.ws_up, g.Is, g.d, 128);
+        p.sc0[1] = g.ss_gate;
+        p.sc1[1] = g.ss_up;
+        p.sa[1] = g.sa_shared;
+    } else {
+        for (int b = 0; b < kABoxes; ++b) p.a[1][b] = p.a[0][b];
+        p.b0[1] = p.b0[0]; p.b1[1] = p.b1[0];
+        p.sc0[1] = p.sc0[0]; p.sc1[1] = p.sc1[0];
+        p.sa[1] = p.sa[0];
+    }
+    p.bw[0] = p.b0[0]; p.bw[1] = p.b0[1];  // unused by the SWIGLU epilogue
+    if (!ok) return cudaErrorInvalidValue;
+    p.hdr = hdr;
+    p.E = g.E;
+    p.max_mtiles = max_mtiles;
+    p.dense_rows = 0;
+    const int max_inter = g.has_shared && g.Is > g.I ? g.Is : g.I;
+    p.NB = (max_inter + BN / 2 - 1) / (BN / 2);
+    p.n_out[0] = g.I; p.n_out[1] = g.has_shared ? g.Is : 0;
+    p.kdim[0] = g.d; p.kdim[1] = g.d;
+    p.wrows[0] = g.I; p.wrows[1] = 0;
+    p.out[0] = g.h; p.out[1] = g.h_s;
+    p.ld_out[0] = g.I; p.ld_out[1] = g.Is;
+    p.err = err;
+    p.timeout_ns = timeout_ns();
+    p.test_stall = test_stall();
+    cudaError_t e = cudaSuccess;
+    if (may_pair) {
+        p.mtiles = mtile_list + max_mtiles;
+        e = launch_tc<EPI_SWIGLU, true, false, true>(p, st);
+        if (e != cudaSuccess) return e;
+    }
+    p.mtiles = mtile_list;
+    return launch_tc<EPI_SWIGLU, false, false, true>(p, st);
+}
+
+cudaError_t launch_ffn_tc_a8_down(const FfnGroups& g, const FfnPlanHeader* hdr,
+                                  const int4* mtile_list, int max_mtiles, bool may_pair,
+                                  DevError* err, cudaStream_t st) {
+    const int64_t R = g.n_routed_rows;
+    TcParams q{};
+    bool ok = true;
+    // h codes in place: row r at h + r * 2I bytes
+    ok &= make_amaps_u8(q.a[0], g.h, R, g.I, 2 * (int64_t)g.I);
+    ok &= make_map_u8(&q.bw[0], g.w_down, (int64_t)g.E * g.d, g.I, 256);
+    ok &= make_map_u8(&q.b0[0], g.w_down, (int64_t)g.E * g.d, g.I, 128);
+    q.sc0[0] = g.s_down;
+    q.sa[0] = g.sa_h;
+    if (g.has_shared) {
+        ok &= make_amaps_u8(q.a[1], g.h_s, g.T, g.Is, 2 * (int64_t)g.Is);
+        ok &= make_map_u8(&q.bw[1], g.ws_down, g.d, g.Is, 256);
+        ok &= make_map_u8(&q.b0[1], g.ws_down, g.d, g.Is, 128);
+        q.sc0[1] = g.ss_down;
+        q.sa[1] = g.sa_hs;
+    } else {
+        for (int b = 0; b < kABoxes; ++b) q.a[1][b] = q.a[0][b];
+        q.bw[1] = q.bw[0]; q.b0[1] = q.b0[0];
+        q.sc0[1] = q.sc0[0];
+        q.sa[1] = q.sa[0];
+    }
+    q.b1[0] = q.b0[0]; q.b1[1] = q.b0[1];
+    q.sc1[0] = q.sc0[0]; q.sc1[1] = q.sc0[1];
+    q.ag = q.a[0][0];
+    q.row_src = nullptr;
+    if (!ok) return cudaErrorInvalidValue;
+    q.hdr = hdr;
+    q.E = g.E;
+    q.max_mtiles = max_mtiles;
+    q.dense_rows = 0;
+    q.NB = (g.d + BN - 1) / BN;
+    q.n_out[0] = g.d; q.n_out[1] = g.has_shared ? g.d : 0;
+    q.kdim[0] = g.I; q.kdim[1] = g.has_shared ? g.Is : g.I;
+    q.wrows[0] = g.d; q.wrows[1] = 0;
+    q.out[0] = g.y; q.out[1] = g.y_s;
+    q.ld_out[0] = g.d; q.ld_out[1] = g.d;
+    q.err = err;
+    q.timeout_ns = timeout_ns();
+    q.test_stall = test_stall();
+    cudaError_t e = cudaSuccess;
+    if (may_pair) {
+        q.mtiles = mtile_list + max_mtiles;
+        e = launch_tc<EPI_STORE_BF16, true, false, true>(q, st);
+        if (e != cudaSuccess) return e;
+    }
+    q.mtiles = mtile_list;
+    return launch_tc<EPI_STORE_BF16, false, false, true>(q, st);
 }
 
 // scores[T][E] (fp32) = x w_g^T on the tensor cores (single tiles)

@@ -52,6 +52,13 @@ struct FfnGroups {
     const float* ss_gate;    // [Is]
     const float* ss_up;      // [Is]
     const float* ss_down;    // [d]
+    // 8-bit activations (launch_ffn_tc_a8_*): a_perm / a_shared hold E4M3 codes
+    // and these the fp32 scale of each row; h / h_s hold codes in place after
+    // the gate/up GEMM (rows 2 * I / 2 * Is bytes apart)
+    const float* sa_routed;  // [n_routed_rows]
+    const float* sa_shared;  // [T]
+    const float* sa_h;       // [n_routed_rows]
+    const float* sa_hs;      // [T]
     void* h;                 // [n_routed_rows][I]
     void* h_s;               // [T][Is]
     void* y;                 // [n_routed_rows][d]
@@ -61,7 +68,7 @@ struct FfnGroups {
 // Workspace carving (all offsets 256-byte aligned).
 struct WsLayout {
     size_t err, router_part, logits, topk_idx, topk_w, counts, offsets, perm, inv_perm,
-        tok_of, blk_hist, plan, gemv_list, mtile_list, x_perm, h, h_s, y_perm, y_s, total;
+        tok_of, blk_hist, plan, gemv_list, mtile_list, x_perm, h, h_s, y_perm, y_s, ascale, total;
     int router_splits, dispatch_blocks, max_mtiles;
 };
 WsLayout ws_layout(const moe_shape& s);
@@ -81,6 +88,10 @@ cudaError_t launch_dispatch(const moe_shape& s, const int32_t* topk_idx, int32_t
                             int32_t* blk_hist, DevError* err, cudaStream_t st);
 cudaError_t launch_gather_rows(const moe_shape& s, const void* x, const int32_t* inv_perm,
                                void* x_perm, cudaStream_t st);
+// E4M3 rows xq [T][d] and their scales sx [T] into expert order (d bytes per row)
+cudaError_t launch_gather_codes(const moe_shape& s, const uint8_t* xq, const float* sx,
+                                const int32_t* inv_perm, uint8_t* xq_perm, float* s_perm,
+                                cudaStream_t st);
 
 // ---- ffn_plan + ffn_gemv.cu ----
 int gemv_max_rows();  // groups with at most this many rows take the GEMV path
@@ -111,6 +122,15 @@ cudaError_t launch_router_tc(const moe_shape& s, const void* x, const void* w_g,
 cudaError_t launch_ffn_tc_fp8(const FfnGroups& g, const FfnPlanHeader* hdr, const int4* mtile_list,
                               int max_mtiles, bool may_pair, DevError* err, cudaStream_t st);
 
+// E4M3 weights and activations (kind::f8f6f4), the two GEMMs launched
+// separately so the caller can quantise h in between
+cudaError_t launch_ffn_tc_a8_gate_up(const FfnGroups& g, const FfnPlanHeader* hdr,
+                                     const int4* mtile_list, int max_mtiles, bool may_pair,
+                                     DevError* err, cudaStream_t st);
+cudaError_t launch_ffn_tc_a8_down(const FfnGroups& g, const FfnPlanHeader* hdr,
+                                  const int4* mtile_list, int max_mtiles, bool may_pair,
+                                  DevError* err, cudaStream_t st);
+
 // ---- ffn_gemv_fp8.cu (E4M3 weights, small groups) ----
 int gemv8_max_rows();  // groups with at most this many rows take the 8-bit GEMV
 bool gemv8_fits(int widest);  // its staged activation rows of this width fit in shared memory
@@ -123,6 +143,11 @@ cudaError_t launch_ffn_gemv_fp8(const FfnGroups& g, const FfnPlanHeader* hdr, co
 // ---- quant.cu ----
 cudaError_t launch_quantize_fp8_rows(int64_t rows, int64_t cols, int dtype, const void* w,
                                      uint8_t* codes, float* scales, cudaStream_t st);
+// bf16 activation rows (cols <= 16384): row r read at w + r * ld_in elements,
+// its codes written at codes + r * ld_out bytes (may be the row's own storage)
+cudaError_t launch_quantize_act_rows(int64_t rows, int cols, const void* w, int64_t ld_in,
+                                     uint8_t* codes, int64_t ld_out, float* scales,
+                                     cudaStream_t st);
 
 // ---- combine.cu ----
 cudaError_t launch_combine(const moe_shape& s, const void* y_perm, const int32_t* inv_perm,

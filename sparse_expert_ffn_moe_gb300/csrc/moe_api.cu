@@ -157,6 +157,8 @@ WsLayout ws_layout(const moe_shape& s) {
     L.h_s = take(es * T * Is);
     L.y_perm = take(es * n * d);
     L.y_s = take(es * T * d);
+    // 8-bit activations: row scales of x [T], x_perm [T*K], h [T*K], h_s [T]
+    L.ascale = take(sizeof(float) * (size_t)(2 * T + 2 * n));
     L.total = o;
     return L;
 }
@@ -559,6 +561,176 @@ moe_status moe_forward_fp8(const moe_shape* shape, const void* x, const void* w_
     // a group has at most T rows (a token picks an expert once; the shared group has T)
     if (e == cudaSuccess && s.T > lim)
         e = launch_ffn_tc_fp8(g, hdr, mtiles, L.max_mtiles, pair && tc_pair_possible(s.T), err, cs);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+
+    // 4. combine
+    return cuda_status(launch_combine(s, g.y, inv, topk_w, shared ? g.y_s : nullptr, y, cs));
+}
+
+// W8A8 expert stage on groups g whose a_perm / a_shared already hold E4M3 rows
+// and sa_routed / sa_shared their scales: gate/up GEMM (bf16 h), h quantised in
+// place, down GEMM.  Every group runs on the tensor cores (no GEMV list);
+// max_rows bounds the rows of any group (pair launches are skipped when no
+// group can take pair tiles).
+static cudaError_t run_ffn_w8a8(const moe_shape& s, FfnGroups& g, const WsLayout& L, void* ws,
+                                int64_t max_rows, DevError* err, cudaStream_t cs) {
+    FfnPlanHeader* hdr = at<FfnPlanHeader>(ws, L.plan);
+    int32_t* glist = at<int32_t>(ws, L.gemv_list);
+    int4* mtiles = at<int4>(ws, L.mtile_list);
+    const int64_t R = (int64_t)s.T * s.K;
+    const bool may_pair = tc_pair_possible(max_rows);
+    cudaError_t e = launch_ffn_plan(g, s.dtype, hdr, glist, mtiles, L.max_mtiles, 0, true, 0, cs);
+    if (e == cudaSuccess)
+        e = launch_ffn_tc_a8_gate_up(g, hdr, mtiles, L.max_mtiles, may_pair, err, cs);
+    if (e == cudaSuccess)
+        e = launch_quantize_act_rows(R, s.inter, g.h, s.inter, (uint8_t*)g.h, 2 * (int64_t)s.inter,
+                                     const_cast<float*>(g.sa_h), cs);
+    if (e == cudaSuccess && g.has_shared)
+        e = launch_quantize_act_rows(s.T, s.inter_shared, g.h_s, s.inter_shared, (uint8_t*)g.h_s,
+                                     2 * (int64_t)s.inter_shared, const_cast<float*>(g.sa_hs), cs);
+    if (e == cudaSuccess) e = launch_ffn_tc_a8_down(g, hdr, mtiles, L.max_mtiles, may_pair, err, cs);
+    return e;
+}
+
+moe_status moe_expert_ffn_w8a8(const moe_shape* shape, const void* x_perm, const int32_t* offsets,
+                               const moe_fp8_experts* w, void* y_perm, void* workspace,
+                               size_t ws_bytes, void* stream) {
+    moe_status st = check_shape(shape);
+    if (st != MOE_OK) return st;
+    const moe_shape& s = *shape;
+    if ((st = check_fp8_shape(s)) != MOE_OK) return st;
+    if (s.T == 0) return MOE_OK;
+    if (!x_perm || !offsets || !y_perm || !aligned16(x_perm) || !aligned16(y_perm))
+        return MOE_ERR_INVALID_ARG;
+    if ((st = check_fp8_weights(w, false)) != MOE_OK) return st;
+    if ((st = check_ws(s, workspace, ws_bytes)) != MOE_OK) return st;
+    if (!tc_available()) return MOE_ERR_UNSUPPORTED;
+    cudaStream_t cs = (cudaStream_t)stream;
+    const WsLayout L = ws_layout(s);
+    DevError* err = at<DevError>(workspace, L.err);
+    cudaError_t e = cudaMemsetAsync(err, 0, sizeof(DevError), cs);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    const int64_t R = (int64_t)s.T * s.K;
+    float* sc = at<float>(workspace, L.ascale);
+    uint8_t* xq = at<uint8_t>(workspace, L.x_perm);
+    e = launch_quantize_act_rows(R, s.d, x_perm, s.d, xq, s.d, sc + s.T, cs);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    FfnGroups g{};
+    g.E = s.E;
+    g.has_shared = 0;
+    g.d = s.d;
+    g.I = s.inter;
+    g.Is = 0;
+    g.n_routed_rows = (int)R;
+    g.T = s.T;
+    g.offsets = offsets;
+    g.row_src = nullptr;
+    g.a_routed = xq;
+    g.a_perm = xq;
+    g.a_shared = xq;
+    g.w_gate = w->w_gate;
+    g.w_up = w->w_up;
+    g.w_down = w->w_down;
+    g.s_gate = w->s_gate;
+    g.s_up = w->s_up;
+    g.s_down = w->s_down;
+    g.sa_routed = sc + s.T;
+    g.sa_shared = sc + s.T;
+    g.sa_h = sc + s.T + R;
+    g.sa_hs = sc + s.T + R;
+    g.h = at<void>(workspace, L.h);
+    g.y = y_perm;
+    // a group has at most T*K rows here (the offsets are the caller's)
+    return cuda_status(run_ffn_w8a8(s, g, L, workspace, R, err, cs));
+}
+
+moe_status moe_forward_w8a8(const moe_shape* shape, const void* x, const void* w_g,
+                            const float* bias, const moe_fp8_experts* w, void* y, void* workspace,
+                            size_t ws_bytes, void* stream) {
+    moe_status st = check_shape(shape);
+    if (st != MOE_OK) return st;
+    const moe_shape& s = *shape;
+    if ((st = check_fp8_shape(s)) != MOE_OK) return st;
+    const bool shared = s.inter_shared > 0;
+    if (s.T == 0) return MOE_OK;
+    if (!x || !w_g || !y || !aligned16(x) || !aligned16(w_g) || !aligned16(y))
+        return MOE_ERR_INVALID_ARG;
+    if ((st = check_fp8_weights(w, shared)) != MOE_OK) return st;
+    if (!shared && w->ws_gate) return MOE_ERR_INVALID_ARG;
+    if ((st = check_ws(s, workspace, ws_bytes)) != MOE_OK) return st;
+    if (!tc_available()) return MOE_ERR_UNSUPPORTED;
+    cudaStream_t cs = (cudaStream_t)stream;
+    const WsLayout L = ws_layout(s);
+    DevError* err = at<DevError>(workspace, L.err);
+    cudaError_t e = cudaMemsetAsync(err, 0, sizeof(DevError), cs);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+
+    // 1. router (bf16 x and weights), top-K and weights
+    float* part = at<float>(workspace, L.router_part);
+    int32_t* topk_idx = at<int32_t>(workspace, L.topk_idx);
+    float* topk_w = at<float>(workspace, L.topk_w);
+    int splits = L.router_splits;
+    if (use_tc_router(s)) {
+        e = launch_router_tc(s, x, w_g, part, err, cs);
+        splits = 1;
+    } else {
+        e = launch_router_gemv(s, x, w_g, part, splits, cs);
+    }
+    if (e == cudaSuccess) e = launch_topk_softmax(s, part, splits, bias, nullptr, topk_idx, topk_w, cs);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+
+    // 2. dispatch; x quantised per token row, codes and scales gathered into
+    //    expert order (x_perm region: permuted codes [T*K][d], then x codes [T][d])
+    int32_t* offsets = at<int32_t>(workspace, L.offsets);
+    int32_t* inv = at<int32_t>(workspace, L.inv_perm);
+    int32_t* tok = at<int32_t>(workspace, L.tok_of);
+    e = launch_dispatch(s, topk_idx, at<int32_t>(workspace, L.counts), offsets,
+                        at<int32_t>(workspace, L.perm), inv, tok, at<int32_t>(workspace, L.blk_hist),
+                        err, cs);
+    const int64_t R = (int64_t)s.T * s.K;
+    float* sc = at<float>(workspace, L.ascale);
+    uint8_t* xq_perm = at<uint8_t>(workspace, L.x_perm);
+    uint8_t* xq = xq_perm + R * s.d;
+    if (e == cudaSuccess) e = launch_quantize_act_rows(s.T, s.d, x, s.d, xq, s.d, sc, cs);
+    if (e == cudaSuccess) e = launch_gather_codes(s, xq, sc, inv, xq_perm, sc + s.T, cs);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+
+    // 3. routed and shared experts, W8A8 on the tensor cores
+    FfnGroups g{};
+    g.E = s.E;
+    g.has_shared = shared ? 1 : 0;
+    g.d = s.d;
+    g.I = s.inter;
+    g.Is = s.inter_shared;
+    g.n_routed_rows = (int)R;
+    g.T = s.T;
+    g.offsets = offsets;
+    g.row_src = nullptr;
+    g.a_routed = xq_perm;
+    g.a_perm = xq_perm;
+    g.a_shared = xq;
+    g.w_gate = w->w_gate;
+    g.w_up = w->w_up;
+    g.w_down = w->w_down;
+    g.s_gate = w->s_gate;
+    g.s_up = w->s_up;
+    g.s_down = w->s_down;
+    g.ws_gate = w->ws_gate;
+    g.ws_up = w->ws_up;
+    g.ws_down = w->ws_down;
+    g.ss_gate = w->ss_gate;
+    g.ss_up = w->ss_up;
+    g.ss_down = w->ss_down;
+    g.sa_routed = sc + s.T;
+    g.sa_shared = sc;
+    g.sa_h = sc + s.T + R;
+    g.sa_hs = sc + s.T + 2 * R;
+    g.h = at<void>(workspace, L.h);
+    g.h_s = at<void>(workspace, L.h_s);
+    g.y = at<void>(workspace, L.y_perm);
+    g.y_s = at<void>(workspace, L.y_s);
+    // a group has at most T rows (a token picks an expert once; the shared group has T)
+    e = run_ffn_w8a8(s, g, L, workspace, s.T, err, cs);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
 
     // 4. combine

@@ -1,4 +1,5 @@
-// quant.cu -- per-row E4M3 quantisation of expert weights (moe_quantize_fp8_rows).
+// quant.cu -- per-row E4M3 quantisation of expert weights (moe_quantize_fp8_rows)
+// and of the activation rows of 8-bit-activation experts.
 //
 // "LLM from scratch, ch. 6", section "second route: make every byte
 // cheaper": x_q = round(x / s) + z with a per-channel scale.  Here z = 0, the
@@ -7,9 +8,10 @@
 // +-448.  Both divisions are IEEE fp32 divisions, so a code is the same
 // integer whatever machine computes it from the same fp32 quotient.
 //
-// One 256-thread block per row, two passes over the row (the second reads it
-// from L1/L2): a max-reduction of |w|, then 16 codes per thread and step
-// (one 16-byte store).  An offline conversion step, HBM bound.
+// Weights: one 256-thread block per row, two passes over the row (the second
+// reads it from L1/L2): a max-reduction of |w|, then 16 codes per thread and
+// step (one 16-byte store).  An offline conversion step, HBM bound.
+// Activations (8-bit-activation experts): quantize_act_rows_kernel below.
 #include <cuda_fp8.h>
 
 #include "common.cuh"
@@ -89,7 +91,84 @@ quantize_rows_kernel(const T* __restrict__ w, uint8_t* __restrict__ codes,
     }
 }
 
+// Activation rows (bf16, cols a multiple of 16 and at most 16384): one
+// 256-thread block per row loads the whole row into registers (at most four
+// 16-value vectors per thread) before any code is written, so the codes may
+// overwrite the row's own storage.  Row r is read at w + r * ld_in (elements)
+// and its codes written at codes + r * ld_out (bytes).  The same decisions as
+// quantize_rows_kernel: scale = amax / 448, code = E4M3 nearest to v / scale.
+constexpr int kActVecs = 4;
+
+__device__ __forceinline__ void unpack16(const uint4& a, const uint4& b, float (&f)[16]) {
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        f[2 * j] = __uint_as_float(w[j] << 16);
+        f[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+    }
+}
+
+__global__ void __launch_bounds__(kQuantThreads)
+quantize_act_rows_kernel(const bf16* w, int64_t ld_in, uint8_t* codes, int64_t ld_out,
+                         float* __restrict__ scales, int cols) {
+    pdl_wait();
+    pdl_trigger();
+    __shared__ float red[kQuantThreads / 32];
+    const int64_t r = blockIdx.x;
+    const uint4* row = reinterpret_cast<const uint4*>(w + r * ld_in);
+    const int nvec = cols / 16;
+    uint4 v[kActVecs][2];
+    float amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < kActVecs; ++j) {
+        const int vi = (int)threadIdx.x + j * kQuantThreads;
+        if (vi < nvec) {
+            v[j][0] = row[2 * vi];
+            v[j][1] = row[2 * vi + 1];
+            float f[16];
+            unpack16(v[j][0], v[j][1], f);
+#pragma unroll
+            for (int k = 0; k < 16; ++k) amax = fmaxf(amax, fabsf(f[k]));
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+    __syncthreads();  // every load of the row has completed past this point
+    float m = 0.0f;
+#pragma unroll
+    for (int i = 0; i < kQuantThreads / 32; ++i) m = fmaxf(m, red[i]);
+    const float s = m > 0.0f ? m / 448.0f : 1.0f;
+    if (threadIdx.x == 0) scales[r] = s;
+    uint8_t* out = codes + r * ld_out;
+#pragma unroll
+    for (int j = 0; j < kActVecs; ++j) {
+        const int vi = (int)threadIdx.x + j * kQuantThreads;
+        if (vi < nvec) {
+            float f[16];
+            unpack16(v[j][0], v[j][1], f);
+            uint32_t packed[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const __nv_fp8_storage_t c = __nv_cvt_float_to_fp8(f[k] / s, __NV_SATFINITE, __NV_E4M3);
+                packed[k >> 2] |= (uint32_t)c << (8 * (k & 3));
+            }
+            *reinterpret_cast<uint4*>(out + (int64_t)vi * 16) =
+                make_uint4(packed[0], packed[1], packed[2], packed[3]);
+        }
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_quantize_act_rows(int64_t rows, int cols, const void* w, int64_t ld_in,
+                                     uint8_t* codes, int64_t ld_out, float* scales,
+                                     cudaStream_t st) {
+    if (rows <= 0) return cudaSuccess;
+    if (cols % 16 || cols > kActVecs * kQuantThreads * 16) return cudaErrorInvalidValue;
+    return launch_pdl(quantize_act_rows_kernel, dim3((unsigned)rows), dim3(kQuantThreads), 0, st,
+                      (const bf16*)w, ld_in, codes, ld_out, scales, cols);
+}
 
 cudaError_t launch_quantize_fp8_rows(int64_t rows, int64_t cols, int dtype, const void* w,
                                      uint8_t* codes, float* scales, cudaStream_t st) {

@@ -82,7 +82,7 @@ class Layer:
         if c.weights == "e4m3":
             return oracle.forward_tokens_fp8(tokens, xh, self.hp["w_g"], self.hp, c.K,
                                              dtype=c.dtype, bias=self.bias_host(),
-                                             router=c.router)
+                                             router=c.router, act8=c.acts == "e4m3")
         return oracle.forward_tokens(tokens, xh, self.hp, c.K, dtype=c.dtype,
                                      bias=self.bias_host(), router=c.router)
 
@@ -96,7 +96,9 @@ class Layer:
         y = torch.empty_like(x)
         ws = moe.alloc_workspace(s) if ws is None else ws
         p = self.p
-        if self.cfg.weights == "e4m3":
+        if self.cfg.acts == "e4m3":
+            moe.moe_forward_w8a8(s, x, p["w_g"], self.bias, moe.make_fp8_experts(p), y, ws)
+        elif self.cfg.weights == "e4m3":
             moe.moe_forward_fp8(s, x, p["w_g"], self.bias, moe.make_fp8_experts(p), y, ws)
         else:
             moe.moe_forward(s, x, p["w_g"], self.bias, p["w_gate"], p["w_up"], p["w_down"],

@@ -133,12 +133,15 @@ def test_binding_refuses_host_tensors(moe):
         moe.moe_combine(s, x, x, x, None, x, stream=0)
 
 
-def test_fp8_argument_errors_return_before_any_launch(lib, moe):
-    """The 8-bit entry points refuse bad shapes and pointers on the host."""
+@pytest.mark.parametrize("a8", [False, True])
+def test_fp8_argument_errors_return_before_any_launch(lib, moe, a8):
+    """The 8-bit entry points (8-bit weights, and 8-bit weights and
+    activations) refuse bad shapes and pointers on the host."""
     vp, z = ctypes.c_void_p, ctypes.c_size_t
     fake = (1 << 20)
     odd = (1 << 20) + 4
-    for f in ("moe_quantize_fp8_rows", "moe_expert_ffn_fp8", "moe_forward_fp8"):
+    for f in ("moe_quantize_fp8_rows", "moe_expert_ffn_fp8", "moe_forward_fp8",
+              "moe_expert_ffn_w8a8", "moe_forward_w8a8"):
         getattr(lib, f).restype = ctypes.c_int32
     lib.moe_quantize_fp8_rows.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,
                                           vp, vp, vp, vp]
@@ -161,9 +164,9 @@ def test_fp8_argument_errors_return_before_any_launch(lib, moe):
     def fwd(shape, w, **kw):
         a = dict(x=vp(fake), w_g=vp(fake), y=vp(fake), ws=vp(fake), n=big)
         a.update(kw)
-        return lib.moe_forward_fp8(ctypes.byref(shape), a["x"], a["w_g"], None,
-                                   ctypes.byref(w) if w is not None else None, a["y"], a["ws"],
-                                   a["n"], None)
+        f = lib.moe_forward_w8a8 if a8 else lib.moe_forward_fp8
+        return f(ctypes.byref(shape), a["x"], a["w_g"], None,
+                 ctypes.byref(w) if w is not None else None, a["y"], a["ws"], a["n"], None)
 
     # activations must be bf16; K extents multiples of 128
     assert fwd(moe.make_shape(4, 128, 8, 2, 256, 0, "f32"), W) == moe.MOE_ERR_UNSUPPORTED
@@ -183,7 +186,7 @@ def test_fp8_argument_errors_return_before_any_launch(lib, moe):
     assert fwd(s, W, n=z(16)) == moe.MOE_ERR_WORKSPACE
     assert fwd(moe.make_shape(0, 128, 8, 2, 256, 0, "bf16"), None) == moe.MOE_OK
 
-    e = lib.moe_expert_ffn_fp8
+    e = lib.moe_expert_ffn_w8a8 if a8 else lib.moe_expert_ffn_fp8
     assert e(ctypes.byref(s), vp(fake), None, ctypes.byref(W), vp(fake), vp(fake), big,
              None) == moe.MOE_ERR_INVALID_ARG
     assert e(ctypes.byref(s), vp(fake), vp(fake), None, vp(fake), vp(fake), big,

@@ -1,0 +1,128 @@
+"""8-bit weights and 8-bit activations (W8A8) on the GPU against the oracle.
+
+Both sides quantise the same rows with the same fp32 decisions; x is the
+same bf16 input on both, so its codes agree bit for bit.  h is computed by
+each side in its own precision (fp32 tensor-core sums, fp64 in the oracle) and
+rounded to bf16 before it is quantised, so its codes agree except where the
+two h values straddle a bf16 rounding boundary: then one element moves by at
+most one E4M3 step, or -- when it is the row's largest magnitude -- the row's
+scale moves by one bf16 step (2^-8 relative) and ~3% of the row's codes by one
+step, about 1% relative on that row's output.  The bf16 tolerances of the
+other layer tests (1e-2 relative L2 overall, 2e-2 per row) cover both.
+"""
+import numpy as np
+import pytest
+import torch
+
+import moe_inputs as mi
+import oracle
+from tests.gpu_util import BF16_REL_L2, Layer, host, rel_l2, to_f64, pair_min_rows
+from tests.test_gpu_fp8 import _check_rows, _clean_x
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def moe():
+    import sparse_expert_ffn_moe_gb300 as m
+    return m
+
+
+# ---------------------------------------------------------------- expert stage
+
+def _expert_ffn_case(moe, counts, d, I, seed=0):
+    E = len(counts)
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    rows = int(offsets[-1])
+    cfg = mi.LayerConfig("w8a8_ffn", T=max(rows, 1), d=d, E=E, K=1, I=I, weights="e4m3",
+                         acts="e4m3", seed=seed)
+    q = mi.make_weights(cfg, "cuda", only={"w_gate", "w_up", "w_down", "s_gate", "s_up",
+                                           "s_down"})
+    x_perm = mi.normal((max(rows, 1), d), 1.0, "bf16", "cuda", seed, "x_perm")[:rows]
+    s = moe.make_shape(rows, d, E, 1, I, 0, "bf16")
+    ws = moe.alloc_workspace(s)
+    y = torch.full((rows, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    moe.moe_expert_ffn_w8a8(s, x_perm, torch.from_numpy(offsets).cuda(),
+                            moe.make_fp8_experts(q), y, ws)
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_error(ws) == 0
+    qh = {k: host(v) for k, v in q.items()}
+    ref = oracle.expert_ffn_w8a8(host(x_perm), offsets, qh, dtype="bf16")
+    return to_f64(y), ref
+
+
+@pytest.mark.parametrize("counts,d,I", [
+    ([75, 0, 140, 3, 1, 260, 77, 44], 256, 384),     # ragged groups, one empty
+    ([600, 257, 1, 129], 384, 640),                  # several m-tiles per group, 5 n-blocks
+    ([1, 2, 1, 1, 3, 1, 1, 2], 1024, 256),           # a few rows per expert
+    ([16, 15, 1, 33], 7168, 256),                    # DeepSeek-width rows
+])
+@pytest.mark.parametrize("pair_rows", [0, 100000])
+def test_expert_ffn_w8a8_matches_oracle(moe, counts, d, I, pair_rows):
+    """pair_rows 0: the plan's cost rule picks CTA-pair or single-SM tiles per
+    group; 100000: single-SM tiles only."""
+    with pair_min_rows(pair_rows):
+        y, ref = _expert_ffn_case(moe, counts, d, I)
+    _check_rows(y, ref)
+
+
+# ---------------------------------------------------------------- the layer
+
+@pytest.mark.parametrize("router", ["softmax", "sigmoid"])
+def test_forward_w8a8_small_layer_all_tokens(moe, router):
+    cfg = mi.LayerConfig("w8a8_small", T=45, d=256, E=12, K=3, I=384, Is=256, router=router,
+                         weights="e4m3", acts="e4m3")
+    L = Layer(cfg)
+    L.x = _clean_x(L)
+    y = to_f64(L.forward(moe))
+    ref = L.oracle_tokens(np.arange(cfg.T))
+    _check_rows(y, ref["y"])
+
+
+def test_forward_w8a8_without_shared_expert_and_pair_tiles(moe):
+    cfg = mi.LayerConfig("w8a8_noshared", T=600, d=512, E=4, K=2, I=256, weights="e4m3",
+                         acts="e4m3")
+    L = Layer(cfg)
+    L.x = _clean_x(L)
+    y = to_f64(L.forward(moe))
+    ref = L.oracle_tokens(np.arange(cfg.T))
+    _check_rows(y, ref["y"])
+
+
+def test_forward_w8a8_differs_from_the_8bit_weight_layer(moe):
+    """The activations really are quantised: the W8A8 output moves away from
+    the W8A16 output of the same weights by the E4M3 noise of x and h (a few
+    percent), far more than the parity tolerance of either path."""
+    cfg = mi.LayerConfig("w8a8_vs_a16", T=64, d=512, E=8, K=2, I=512, Is=256, weights="e4m3",
+                         acts="e4m3")
+    L = Layer(cfg)
+    L.x = _clean_x(L)
+    y8 = to_f64(L.forward(moe))
+    s = L.shape(moe)
+    ws = moe.alloc_workspace(s)
+    y16 = torch.empty_like(L.x)
+    moe.moe_forward_fp8(s, L.x, L.p["w_g"], L.bias, moe.make_fp8_experts(L.p), y16, ws)
+    torch.cuda.synchronize()
+    d = rel_l2(y8, to_f64(y16))
+    assert 2e-2 < d < 0.2, d
+
+
+@pytest.mark.parametrize("name", ["mixtral_prefill_w8a8", "dsv3_sweep_w8a8_T512"])
+def test_forward_w8a8_full_size_sampled_tokens(moe, name):
+    cfg = mi.CONFIGS[name]
+    L = Layer(cfg)
+    y = L.forward(moe)
+    tokens = mi.sample_tokens(cfg.T, 64, seed=cfg.seed).numpy()
+    ref = L.oracle_tokens(tokens)
+    from tests.gpu_util import MARGIN, boundary_margin
+    ok = boundary_margin(ref["logits"], cfg.K) >= MARGIN
+    assert ok.mean() >= 0.9
+    _check_rows(to_f64(y[torch.from_numpy(tokens[ok]).long().cuda()]), ref["y"][ok])
+
+
+def test_forward_w8a8_zero_tokens_is_a_no_op(moe):
+    cfg = mi.LayerConfig("w8a8_empty", T=4, d=128, E=4, K=2, I=128, weights="e4m3",
+                         acts="e4m3")
+    L = Layer(cfg)
+    s = moe.make_shape(0, 128, 4, 2, 128, 0, "bf16")
+    moe.moe_forward_w8a8(s, None, L.p["w_g"], None, moe.make_fp8_experts(L.p), None, None)
