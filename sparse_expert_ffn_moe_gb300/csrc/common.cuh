@@ -71,9 +71,12 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-// SiLU(g) * u in fp32: g / (1 + e^-g) * u, with the CUDA fast exponential.
+// SiLU(g) * u in fp32: g / (1 + e^-g) * u, with the CUDA fast exponential and
+// fast division (a few ulp; for g < -87 the denominator overflows and the
+// result is 0).  Measured on the tcgen05 gate/up epilogue: the IEEE division
+// cost 6 % of an 8-bit prefill layer call.
 __device__ __forceinline__ float silu_mul(float g, float u) {
-    return g / (1.0f + __expf(-g)) * u;
+    return __fdividef(g, 1.0f + __expf(-g)) * u;
 }
 
 __host__ __device__ __forceinline__ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }

@@ -57,8 +57,9 @@ struct FfnGroups {
     // the gate/up GEMM (rows 2 * I / 2 * Is bytes apart)
     const float* sa_routed;  // [n_routed_rows]
     const float* sa_shared;  // [T]
-    const float* sa_h;       // [n_routed_rows]
-    const float* sa_hs;      // [T]
+    const float* sa_h;       // [n_routed_rows]: zero before the gate/up GEMM, which
+    const float* sa_hs;      // [T]              raises it to max |h| (fp32 bits); the
+                             // h quantiser turns it into the row scale
     void* h;                 // [n_routed_rows][I]
     void* h_s;               // [T][Is]
     void* y;                 // [n_routed_rows][d]
@@ -148,6 +149,12 @@ cudaError_t launch_quantize_fp8_rows(int64_t rows, int64_t cols, int dtype, cons
 cudaError_t launch_quantize_act_rows(int64_t rows, int cols, const void* w, int64_t ld_in,
                                      uint8_t* codes, int64_t ld_out, float* scales,
                                      cudaStream_t st);
+// The same quantisation with each row's max |value| already known: amax_scale[r]
+// holds it as fp32 bits on entry and the row's scale on return.  One warp per
+// row, walking it from low to high addresses, so codes may overwrite the row.
+cudaError_t launch_quantize_rows_known_amax(int64_t rows, int cols, const void* w, int64_t ld_in,
+                                            uint8_t* codes, int64_t ld_out, float* amax_scale,
+                                            cudaStream_t st);
 
 // ---- combine.cu ----
 cudaError_t launch_combine(const moe_shape& s, const void* y_perm, const int32_t* inv_perm,

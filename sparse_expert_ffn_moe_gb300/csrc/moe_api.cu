@@ -579,15 +579,21 @@ static cudaError_t run_ffn_w8a8(const moe_shape& s, FfnGroups& g, const WsLayout
     int4* mtiles = at<int4>(ws, L.mtile_list);
     const int64_t R = (int64_t)s.T * s.K;
     const bool may_pair = tc_pair_possible(max_rows);
-    cudaError_t e = launch_ffn_plan(g, s.dtype, hdr, glist, mtiles, L.max_mtiles, 0, true, 0, cs);
+    // the gate/up epilogue raises each h row's max |h| from zero
+    cudaError_t e = cudaMemsetAsync(const_cast<float*>(g.sa_h), 0, sizeof(float) * R, cs);
+    if (e == cudaSuccess && g.has_shared)
+        e = cudaMemsetAsync(const_cast<float*>(g.sa_hs), 0, sizeof(float) * s.T, cs);
+    if (e == cudaSuccess)
+        e = launch_ffn_plan(g, s.dtype, hdr, glist, mtiles, L.max_mtiles, 0, true, 0, cs);
     if (e == cudaSuccess)
         e = launch_ffn_tc_a8_gate_up(g, hdr, mtiles, L.max_mtiles, may_pair, err, cs);
     if (e == cudaSuccess)
-        e = launch_quantize_act_rows(R, s.inter, g.h, s.inter, (uint8_t*)g.h, 2 * (int64_t)s.inter,
-                                     const_cast<float*>(g.sa_h), cs);
+        e = launch_quantize_rows_known_amax(R, s.inter, g.h, s.inter, (uint8_t*)g.h,
+                                            2 * (int64_t)s.inter, const_cast<float*>(g.sa_h), cs);
     if (e == cudaSuccess && g.has_shared)
-        e = launch_quantize_act_rows(s.T, s.inter_shared, g.h_s, s.inter_shared, (uint8_t*)g.h_s,
-                                     2 * (int64_t)s.inter_shared, const_cast<float*>(g.sa_hs), cs);
+        e = launch_quantize_rows_known_amax(s.T, s.inter_shared, g.h_s, s.inter_shared,
+                                            (uint8_t*)g.h_s, 2 * (int64_t)s.inter_shared,
+                                            const_cast<float*>(g.sa_hs), cs);
     if (e == cudaSuccess) e = launch_ffn_tc_a8_down(g, hdr, mtiles, L.max_mtiles, may_pair, err, cs);
     return e;
 }

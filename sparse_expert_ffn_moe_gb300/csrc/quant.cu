@@ -159,7 +159,71 @@ quantize_act_rows_kernel(const bf16* w, int64_t ld_in, uint8_t* codes, int64_t l
     }
 }
 
+// Rows whose max |value| is known (raised by the producing GEMM): no block
+// reduction, one warp per row.  The warp walks its row from low to high
+// addresses, 1024 values per step (16 per lane, two 512-value halves), and
+// orders each step's loads before its stores with __syncwarp.  Codes of
+// values [a, a + 1024) land on bytes [a, a + 1024), which hold bf16 values
+// [a / 2, a / 2 + 512) -- all loaded at this step or an earlier one -- and
+// every later load reads bytes past every earlier store, so the codes may
+// overwrite the row in place.
+constexpr int kRowsPerBlock = kQuantThreads / 32;
+
+__global__ void __launch_bounds__(kQuantThreads)
+quantize_rows_known_amax_kernel(const bf16* w, int64_t ld_in, uint8_t* codes, int64_t ld_out,
+                                float* amax_scale, int cols, int64_t rows) {
+    pdl_wait();
+    pdl_trigger();
+    const int lane = threadIdx.x & 31;
+    const int64_t r = (int64_t)blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5);
+    if (r >= rows) return;
+    const float m = __uint_as_float(reinterpret_cast<const uint32_t*>(amax_scale)[r]);
+    const float s = m > 0.0f ? m / 448.0f : 1.0f;
+    const uint4* row = reinterpret_cast<const uint4*>(w + r * ld_in);
+    uint8_t* out = codes + r * ld_out;
+    for (int c0 = 0; c0 < cols; c0 += 1024) {
+        uint4 v[2][2];
+        bool ok[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int e = c0 + j * 512 + lane * 16;
+            ok[j] = e < cols;
+            if (ok[j]) {
+                v[j][0] = row[e / 8];
+                v[j][1] = row[e / 8 + 1];
+            }
+        }
+        __syncwarp();  // every lane's loads of this step precede any store of it
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            if (!ok[j]) continue;
+            float f[16];
+            unpack16(v[j][0], v[j][1], f);
+            uint32_t packed[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const __nv_fp8_storage_t c = __nv_cvt_float_to_fp8(f[k] / s, __NV_SATFINITE, __NV_E4M3);
+                packed[k >> 2] |= (uint32_t)c << (8 * (k & 3));
+            }
+            *reinterpret_cast<uint4*>(out + c0 + j * 512 + lane * 16) =
+                make_uint4(packed[0], packed[1], packed[2], packed[3]);
+        }
+    }
+    __syncwarp();  // every lane has read the max before it is replaced by the scale
+    if (lane == 0) amax_scale[r] = s;
+}
+
 }  // namespace
+
+cudaError_t launch_quantize_rows_known_amax(int64_t rows, int cols, const void* w, int64_t ld_in,
+                                            uint8_t* codes, int64_t ld_out, float* amax_scale,
+                                            cudaStream_t st) {
+    if (rows <= 0) return cudaSuccess;
+    if (cols % 16) return cudaErrorInvalidValue;
+    const int64_t blocks = (rows + kRowsPerBlock - 1) / kRowsPerBlock;
+    return launch_pdl(quantize_rows_known_amax_kernel, dim3((unsigned)blocks), dim3(kQuantThreads),
+                      0, st, (const bf16*)w, ld_in, codes, ld_out, amax_scale, cols, rows);
+}
 
 cudaError_t launch_quantize_act_rows(int64_t rows, int cols, const void* w, int64_t ld_in,
                                      uint8_t* codes, int64_t ld_out, float* scales,
