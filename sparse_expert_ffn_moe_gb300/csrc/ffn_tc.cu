@@ -189,20 +189,19 @@ struct Tile {
 
 // KSTEP: elements of the reduction per K block (64 bf16 or 128 8-bit values,
 // 128 bytes either way)
+// The plan entry of tile t (group, first row, rows, m-tile index); a load
+// whose result decode_tile_entry uses, so a role can issue it one tile ahead.
+__device__ __forceinline__ int4 fetch_tile_entry(const TcParams& p, int t) {
+    return p.dense_rows > 0 ? make_int4(-1, 0, p.dense_rows, t / p.NB) : p.mtiles[t / p.NB];
+}
+
 template <int EPI, bool PAIR, int KSTEP>
-__device__ __forceinline__ Tile decode_tile(const TcParams& p, int n_tiles_in_list, int t) {
+__device__ __forceinline__ Tile decode_tile_entry(const TcParams& p, int4 e, int t) {
     using S = Shape<PAIR>;
     constexpr int kNCols = EPI == EPI_SWIGLU ? BN / 2 : BN;  // output columns per n-block
     Tile tl;
     const int NB = p.NB;
-    int g, gr0, Mg, i;
-    if (p.dense_rows > 0) {
-        g = -1; gr0 = 0; Mg = p.dense_rows; i = t / NB;
-    } else {
-        const int4 e = p.mtiles[t / NB];
-        g = e.x; gr0 = e.y; Mg = e.z; i = e.w;
-    }
-    (void)n_tiles_in_list;
+    const int g = e.x, gr0 = e.y, Mg = e.z, i = e.w;
     const int q = t / NB;
     const int cnt = (Mg + S::kTileRows - 1) / S::kTileRows;
     const int tt = t - (q - i) * NB;  // index inside this group's tiles
@@ -220,6 +219,12 @@ __device__ __forceinline__ Tile decode_tile(const TcParams& p, int n_tiles_in_li
     tl.kblocks = (p.kdim[tl.kind] + KSTEP - 1) / KSTEP;
     tl.valid = tl.n0 < p.n_out[tl.kind] && tl.rows > 0;
     return tl;
+}
+
+template <int EPI, bool PAIR, int KSTEP>
+__device__ __forceinline__ Tile decode_tile(const TcParams& p, int n_tiles_in_list, int t) {
+    (void)n_tiles_in_list;
+    return decode_tile_entry<EPI, PAIR, KSTEP>(p, fetch_tile_entry(p, t), t);
 }
 
 struct SmemCtl {
@@ -634,8 +639,14 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
             uint32_t acc_phase = 0;
             bool ok = true;
             bool any = false;
+            // the next tile's plan entry is loaded while this tile's MMAs run (its load
+            // took ~700 cycles per tile of this warp's time; measured 0.5 % faster on
+            // the bf16 prefill layers, neutral elsewhere)
+            int4 entry_next = unit < n_tiles ? fetch_tile_entry(p, unit) : make_int4(0, 0, 0, 0);
             for (int t = unit; t < n_tiles && ok; t += n_units) {
-                const Tile tl = decode_tile<EPI, PAIR, kKStep>(p, list_len, t);
+                const int4 entry = entry_next;
+                if (t + n_units < n_tiles) entry_next = fetch_tile_entry(p, t + n_units);
+                const Tile tl = decode_tile_entry<EPI, PAIR, kKStep>(p, entry, t);
                 if (!tl.valid) continue;
                 if (!wait_bounded(&ctl->tempty[acc], acc_phase ^ 1u, ctl, p, 200)) { ok = false; break; }
                 ptx::tc_fence_after();

@@ -126,3 +126,54 @@ def test_forward_w8a8_zero_tokens_is_a_no_op(moe):
     L = Layer(cfg)
     s = moe.make_shape(0, 128, 4, 2, 128, 0, "bf16")
     moe.moe_forward_w8a8(s, None, L.p["w_g"], None, moe.make_fp8_experts(L.p), None, None)
+
+
+def test_forward_w8a8_is_deterministic_graph_capturable_and_pdl_neutral(moe, monkeypatch):
+    """Repeated calls give identical bits (the row maxima of h are raised with
+    integer atomics, whose order does not matter); the call replays from a CUDA
+    graph (its memsets and launches are all stream work); programmatic launch
+    off gives the same bits."""
+    cfg = mi.CONFIGS["dsv3_sweep_w8a8_T512"]
+    L = Layer(cfg)
+    s = L.shape(moe)
+    ws = moe.alloc_workspace(s)
+    y1 = L.forward(moe, ws=ws)
+    y2 = L.forward(moe, ws=ws)
+    assert torch.equal(y1, y2)
+    monkeypatch.setenv("MOE_PDL", "0")
+    assert torch.equal(L.forward(moe, ws=ws), y1)
+    monkeypatch.delenv("MOE_PDL")
+    W = moe.make_fp8_experts(L.p)
+    y3 = torch.empty_like(y1)
+    st = torch.cuda.Stream()
+    with torch.cuda.stream(st):
+        moe.moe_forward_w8a8(s, L.x, L.p["w_g"], L.bias, W, y3, ws, stream=st)
+    st.synchronize()
+    g = torch.cuda.CUDAGraph()
+    y3.zero_()
+    with torch.cuda.graph(g, stream=st):
+        moe.moe_forward_w8a8(s, L.x, L.p["w_g"], L.bias, W, y3, ws, stream=st)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(y3, y1)
+
+
+def test_w8a8_stalled_copy_times_out_and_the_context_survives(moe, monkeypatch):
+    """No operand tile is ever requested: the MMA's bounded waits run out, the
+    kernel records MOE_ERR_TIMEOUT and returns; the next call is correct."""
+    cfg = mi.LayerConfig("w8a8_stall", T=300, d=256, E=4, K=2, I=256, Is=128, weights="e4m3",
+                         acts="e4m3")
+    L = Layer(cfg)
+    monkeypatch.setenv("MOE_TC_TIMEOUT_MS", "50")
+    monkeypatch.setenv("MOE_TC_TEST_STALL", "1")
+    s = L.shape(moe)
+    ws = moe.alloc_workspace(s)
+    y = torch.empty_like(L.x)
+    moe.moe_forward_w8a8(s, L.x, L.p["w_g"], L.bias, moe.make_fp8_experts(L.p), y, ws)
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_error(ws) == moe.MOE_ERR_TIMEOUT
+    monkeypatch.delenv("MOE_TC_TEST_STALL")
+    monkeypatch.delenv("MOE_TC_TIMEOUT_MS")
+    L.x = _clean_x(L)
+    y = to_f64(L.forward(moe))
+    _check_rows(y, L.oracle_tokens(np.arange(cfg.T))["y"])
