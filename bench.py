@@ -450,11 +450,12 @@ def time_expert_ffn(moe, cfg, x, p, bias, stream, steps: int, n_active: int) -> 
     return {"ms": ms, "flops": 6 * n * cfg.d * cfg.I, "bytes": ffn_stage_bytes(cfg, n_active)}
 
 
-# DRAM bytes (read + write) of one expert-FFN stage (both tcgen05 launches), from one
+# DRAM bytes (read + write) of one expert-FFN stage (its tcgen05 launches), from one
 # ncu capture per workload (profiles/ffn_stage_traffic_<workload>.md), valid only for
 # the ffn_tc.cu source it was taken on (sha256 prefix).
 STAGE_TRAFFIC = {
-    "mixtral_prefill": {"bytes": 4670973952, "ffn_tc_sha256": "6945fa05a70cf73b"},
+    "mixtral_prefill": {"bytes": 5309651712, "ffn_tc_sha256": "b2183592a4f6db63"},
+    "mixtral_prefill_w8a8": {"bytes": 2299095808, "ffn_tc_sha256": "b2183592a4f6db63"},
 }
 
 
@@ -511,26 +512,51 @@ def stage_roofline(cfg, stage, peaks) -> dict:
 
 
 def time_e2e(call, stream, steps, x_dev) -> dict:
-    """Through the C ABI with host buffers: pinned x -> device, the forward call,
-    y -> pinned host, every step inside the timed region."""
+    """Through the C ABI with host buffers: every step copies its x from pinned
+    host memory to the device, runs the forward call and copies y back to pinned
+    host memory, all inside the timed region.  The copies run on a second stream
+    with two device buffers each way, so step i's upload and step i-1's download
+    overlap step i-1's / step i's compute (the usual serving pipeline); the
+    events keep every buffer's reuse ordered."""
     import torch
     xh = x_dev.cpu().pin_memory()
-    yh = torch.empty_like(xh).pin_memory()
-    xd = torch.empty_like(x_dev)
-    yd = torch.empty_like(x_dev)
+    yh = [torch.empty_like(xh).pin_memory() for _ in range(2)]
+    xd = [torch.empty_like(x_dev) for _ in range(2)]
+    yd = [torch.empty_like(x_dev) for _ in range(2)]
+    cp = torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event()  # noqa: E731
+    up = [ev(), ev()]        # x copied in
+    done = [ev(), ev()]      # compute finished with xd[b] / wrote yd[b]
+    down = [ev(), ev()]      # y copied out of yd[b]
+    for b in range(2):       # every buffer starts free
+        done[b].record(stream)
+        down[b].record(cp)
 
-    def step():
+    def step(i):
+        b = i & 1
+        with torch.cuda.stream(cp):
+            cp.wait_event(done[b])            # compute of step i-2 released xd[b]
+            xd[b].copy_(xh, non_blocking=True)
+            up[b].record(cp)
+        stream.wait_event(up[b])
+        stream.wait_event(down[b])            # y of step i-2 copied out of yd[b]
         with torch.cuda.stream(stream):
-            xd.copy_(xh, non_blocking=True)
-            call(xd, yd)
-            yh.copy_(yd, non_blocking=True)
-    for _ in range(3):
-        step()
+            call(xd[b], yd[b])
+            done[b].record(stream)
+        with torch.cuda.stream(cp):
+            cp.wait_event(done[b])
+            yh[b].copy_(yd[b], non_blocking=True)
+            down[b].record(cp)
+
+    for i in range(4):
+        step(i)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(steps):
-        step()
+    cp.wait_event(e0)                         # no timed copy starts before the clock does
+    for i in range(steps):
+        step(i)
+    stream.wait_stream(cp)                    # the last download is inside the timed region
     e1.record(stream)
     torch.cuda.synchronize()
     nbytes = xh.numel() * xh.element_size()
