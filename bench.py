@@ -514,49 +514,50 @@ def stage_roofline(cfg, stage, peaks) -> dict:
 def time_e2e(call, stream, steps, x_dev) -> dict:
     """Through the C ABI with host buffers: every step copies its x from pinned
     host memory to the device, runs the forward call and copies y back to pinned
-    host memory, all inside the timed region.  The copies run on a second stream
-    with two device buffers each way, so step i's upload and step i-1's download
-    overlap step i-1's / step i's compute (the usual serving pipeline); the
+    host memory, all inside the timed region.  Uploads and downloads run on two
+    more streams with two device buffers each way, so step i+1's upload and step
+    i-1's download overlap step i's compute (the usual serving pipeline); the
     events keep every buffer's reuse ordered."""
     import torch
     xh = x_dev.cpu().pin_memory()
     yh = [torch.empty_like(xh).pin_memory() for _ in range(2)]
     xd = [torch.empty_like(x_dev) for _ in range(2)]
     yd = [torch.empty_like(x_dev) for _ in range(2)]
-    cp = torch.cuda.Stream()
+    h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
     ev = lambda: torch.cuda.Event()  # noqa: E731
-    up = [ev(), ev()]        # x copied in
-    done = [ev(), ev()]      # compute finished with xd[b] / wrote yd[b]
+    up = [ev(), ev()]        # x copied into xd[b]
+    done = [ev(), ev()]      # compute finished with xd[b] and wrote yd[b]
     down = [ev(), ev()]      # y copied out of yd[b]
     for b in range(2):       # every buffer starts free
         done[b].record(stream)
-        down[b].record(cp)
+        down[b].record(d2h)
 
     def step(i):
         b = i & 1
-        with torch.cuda.stream(cp):
-            cp.wait_event(done[b])            # compute of step i-2 released xd[b]
+        with torch.cuda.stream(h2d):
+            h2d.wait_event(done[b])           # compute of step i-2 released xd[b]
             xd[b].copy_(xh, non_blocking=True)
-            up[b].record(cp)
+            up[b].record(h2d)
         stream.wait_event(up[b])
         stream.wait_event(down[b])            # y of step i-2 copied out of yd[b]
         with torch.cuda.stream(stream):
             call(xd[b], yd[b])
             done[b].record(stream)
-        with torch.cuda.stream(cp):
-            cp.wait_event(done[b])
+        with torch.cuda.stream(d2h):
+            d2h.wait_event(done[b])
             yh[b].copy_(yd[b], non_blocking=True)
-            down[b].record(cp)
+            down[b].record(d2h)
 
     for i in range(4):
         step(i)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    cp.wait_event(e0)                         # no timed copy starts before the clock does
+    h2d.wait_event(e0)                        # no timed copy starts before the clock does
+    d2h.wait_event(e0)
     for i in range(steps):
         step(i)
-    stream.wait_stream(cp)                    # the last download is inside the timed region
+    stream.wait_stream(d2h)                   # the last download is inside the timed region
     e1.record(stream)
     torch.cuda.synchronize()
     nbytes = xh.numel() * xh.element_size()
