@@ -63,12 +63,22 @@ __device__ int32_t scan_1024(int32_t v, int32_t* sh, int32_t* total) {
 // least pair_min rows, tiles of pair_m rows) or to the single-tile list
 // (tiles of single_m rows).  Tile entries are (group, first row of the group,
 // rows of the group, index of the m-tile within the group).
-__global__ void __launch_bounds__(1024)
-ffn_plan_kernel(const int32_t* __restrict__ offsets, int E, int has_shared, int T, int limit,
-                int small, int single_m, int pair_min, int pair_m, FfnPlanHeader* __restrict__ hdr,
-                int32_t* __restrict__ gemv_list, int4* __restrict__ mtile_list, int max_mtiles) {
-    pdl_wait();
-    pdl_trigger();
+struct PlanArgs {
+    int E, has_shared, T, limit, small, single_m, pair_min, pair_m, max_mtiles;
+    FfnPlanHeader* hdr;
+    int32_t* gemv_list;
+    int4* mtile_list;
+};
+
+// The plan, run by one 1024-thread block; offsets may point to global or
+// shared memory.
+__device__ void plan_groups(const int32_t* offsets, const PlanArgs& a) {
+    const int E = a.E, has_shared = a.has_shared, T = a.T, limit = a.limit, small = a.small;
+    const int single_m = a.single_m, pair_min = a.pair_min, pair_m = a.pair_m;
+    const int max_mtiles = a.max_mtiles;
+    FfnPlanHeader* hdr = a.hdr;
+    int32_t* gemv_list = a.gemv_list;
+    int4* mtile_list = a.mtile_list;
     __shared__ int32_t sh[32];
     __shared__ int32_t tot_g, tot_g2, tot_s, tot_p, base_g, base_g2, base_s, base_p;
     if (threadIdx.x == 0) { base_g = 0; base_g2 = 0; base_s = 0; base_p = 0; }
@@ -116,6 +126,99 @@ ffn_plan_kernel(const int32_t* __restrict__ offsets, int E, int has_shared, int 
         hdr->n_mtiles = min(base_s, max_mtiles);
         hdr->n_ptiles = min(base_p, max_mtiles);
     }
+}
+
+__global__ void __launch_bounds__(1024)
+ffn_plan_kernel(const int32_t* __restrict__ offsets, PlanArgs a) {
+    pdl_wait();
+    pdl_trigger();
+    plan_groups(offsets, a);
+}
+
+// Dispatch and plan for a small batch (n = T*K <= 1024 slots, E <= 1024) in
+// one block of 1024 threads: thread f holds slot f.  The same results as the
+// three dispatch kernels and the plan kernel -- counts, exclusive offsets,
+// the permutation stable by flat slot (rank inside the warp from
+// __match_any_sync plus the exclusive sum over earlier warps), the token of
+// every row, and the plan -- in one launch instead of four.
+__global__ void __launch_bounds__(1024)
+dispatch_plan_small_kernel(const int32_t* __restrict__ idx, int n, int K, int32_t* __restrict__ counts,
+                           int32_t* __restrict__ offsets, int32_t* __restrict__ perm,
+                           int32_t* __restrict__ inv_perm, int32_t* __restrict__ tok_of,
+                           DevError* err, PlanArgs a) {
+    pdl_wait();
+    pdl_trigger();
+    extern __shared__ int32_t dyn[];
+    const int E = a.E;
+    int32_t* wcnt = dyn;                // [32 warps][E]: counts, then exclusive prefix over warps
+    int32_t* off_sh = dyn + 32 * E;     // [E + 1]
+    __shared__ int32_t sh[32];
+    __shared__ int32_t total;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int i = threadIdx.x; i < 32 * E; i += blockDim.x) wcnt[i] = 0;
+    __syncthreads();
+    const int f = threadIdx.x;
+    int e = f < n ? idx[f] : -1;
+    if (f < n && !(e >= 0 && e < E)) {
+        record_error(err, MOE_ERR_BOUNDS, 200);
+        e = -1;
+    }
+    if (!(e >= 0 && e < E)) e = -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    if (e >= 0 && rank == 0) wcnt[warp * E + e] = __popc(peers);
+    __syncthreads();
+    int32_t c = 0;  // thread x < E: the count of expert x
+    if (threadIdx.x < E) {
+        for (int w = 0; w < 32; ++w) {
+            const int32_t t = wcnt[w * E + threadIdx.x];
+            wcnt[w * E + threadIdx.x] = c;
+            c += t;
+        }
+    }
+    const int32_t off = scan_1024(threadIdx.x < E ? c : 0, sh, &total);
+    if (threadIdx.x < E) {
+        counts[threadIdx.x] = c;
+        offsets[threadIdx.x] = off;
+        off_sh[threadIdx.x] = off;
+    }
+    if (threadIdx.x == 0) {
+        offsets[E] = total;
+        off_sh[E] = total;
+    }
+    __syncthreads();
+    if (f < n) {
+        if (e >= 0) {
+            const int32_t p = off_sh[e] + wcnt[warp * E + e] + rank;
+            if (perm) perm[p] = f;
+            inv_perm[f] = p;
+            tok_of[p] = f / K;
+        } else {
+            inv_perm[f] = -1;  // dropped slot (out-of-range expert id)
+        }
+    }
+    plan_groups(off_sh, a);
+}
+
+PlanArgs plan_args(const FfnGroups& g, int dtype, FfnPlanHeader* hdr, int32_t* gemv_list,
+                   int4* mtile_list, int max_mtiles, int gemv_limit, bool allow_pair,
+                   int small_rows) {
+    PlanArgs a;
+    a.E = g.E;
+    a.has_shared = g.has_shared;
+    a.T = g.T;
+    // fp32 layers never use the tensor cores (no TF32): every group streams
+    a.limit = dtype == MOE_F32 ? 0x7fffffff : gemv_limit;
+    a.small = small_rows;
+    a.single_m = tc_tile_rows(false);
+    // a pair threshold no group can reach keeps every group on single tiles
+    a.pair_min = allow_pair ? tc_pair_min_rows() : 0x7fffffff;
+    a.pair_m = tc_tile_rows(true);
+    a.max_mtiles = max_mtiles;
+    a.hdr = hdr;
+    a.gemv_list = gemv_list;
+    a.mtile_list = mtile_list;
+    return a;
 }
 
 struct GroupView {
@@ -356,13 +459,32 @@ int gemv_max_rows() {
 cudaError_t launch_ffn_plan(const FfnGroups& g, int dtype, FfnPlanHeader* hdr, int32_t* gemv_list,
                             int4* mtile_list, int max_mtiles, int gemv_limit, bool allow_pair,
                             int small_rows, cudaStream_t st) {
-    // fp32 layers never use the tensor cores (no TF32): every group streams
-    const int limit = dtype == MOE_F32 ? 0x7fffffff : gemv_limit;
-    // a pair threshold no group can reach keeps every group on single tiles
-    const int pair_min = allow_pair ? tc_pair_min_rows() : 0x7fffffff;
-    return launch_pdl(ffn_plan_kernel, dim3(1), dim3(1024), 0, st, g.offsets, g.E, g.has_shared, g.T,
-                      limit, small_rows, tc_tile_rows(false), pair_min, tc_tile_rows(true), hdr,
-                      gemv_list, mtile_list, max_mtiles);
+    return launch_pdl(ffn_plan_kernel, dim3(1), dim3(1024), 0, st, g.offsets,
+                      plan_args(g, dtype, hdr, gemv_list, mtile_list, max_mtiles, gemv_limit,
+                                allow_pair, small_rows));
+}
+
+// Read on every call: MOE_FUSED_DISPATCH=0 keeps the four-launch path.
+bool dispatch_plan_fusable(const moe_shape& s) {
+    const char* v = getenv("MOE_FUSED_DISPATCH");
+    if (v && v[0] == '0') return false;
+    return (int64_t)s.T * s.K <= 1024 && s.E <= 1024;
+}
+
+cudaError_t launch_dispatch_plan_small(const moe_shape& s, const int32_t* topk_idx, int32_t* counts,
+                                       int32_t* offsets, int32_t* perm, int32_t* inv_perm,
+                                       int32_t* tok_of, DevError* err, const FfnGroups& g,
+                                       FfnPlanHeader* hdr, int32_t* gemv_list, int4* mtile_list,
+                                       int max_mtiles, int gemv_limit, bool allow_pair,
+                                       int small_rows, cudaStream_t st) {
+    const size_t smem = sizeof(int32_t) * (32 * (size_t)s.E + s.E + 1);
+    cudaError_t e = cudaFuncSetAttribute(dispatch_plan_small_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(dispatch_plan_small_kernel, dim3(1), dim3(1024), smem, st, topk_idx,
+                      s.T * s.K, s.K, counts, offsets, perm, inv_perm, tok_of, err,
+                      plan_args(g, s.dtype, hdr, gemv_list, mtile_list, max_mtiles, gemv_limit,
+                                allow_pair, small_rows));
 }
 
 cudaError_t launch_ffn_gemv(const FfnGroups& g, int dtype, const FfnPlanHeader* hdr,

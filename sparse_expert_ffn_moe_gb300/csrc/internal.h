@@ -105,6 +105,16 @@ cudaError_t launch_ffn_plan(const FfnGroups& g, int dtype, FfnPlanHeader* hdr,
                             int gemv_limit, bool allow_pair, int small_rows, cudaStream_t st);
 cudaError_t launch_ffn_gemv(const FfnGroups& g, int dtype, const FfnPlanHeader* hdr,
                             const int32_t* gemv_list, cudaStream_t st);
+// Small batches (T*K <= 1024 slots, E <= 1024): the three dispatch kernels
+// and the plan as one single-block launch with identical results
+// (MOE_FUSED_DISPATCH=0, read per call, keeps the separate launches).
+bool dispatch_plan_fusable(const moe_shape& s);
+cudaError_t launch_dispatch_plan_small(const moe_shape& s, const int32_t* topk_idx, int32_t* counts,
+                                       int32_t* offsets, int32_t* perm, int32_t* inv_perm,
+                                       int32_t* tok_of, DevError* err, const FfnGroups& g,
+                                       FfnPlanHeader* hdr, int32_t* gemv_list, int4* mtile_list,
+                                       int max_mtiles, int gemv_limit, bool allow_pair,
+                                       int small_rows, cudaStream_t st);
 
 // ---- ffn_tc.cu (tcgen05 grouped GEMM) ----
 bool tc_available();

@@ -351,27 +351,17 @@ moe_status moe_forward(const moe_shape* shape, const void* x, const void* w_g, c
     if (e == cudaSuccess) e = launch_topk_softmax(s, part, splits, bias, nullptr, topk_idx, topk_w, cs);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
 
-    // 2. dispatch
+    // 2. dispatch (and, for small batches, the expert plan in the same launch)
     int32_t* counts = at<int32_t>(workspace, L.counts);
     int32_t* offsets = at<int32_t>(workspace, L.offsets);
     int32_t* inv = at<int32_t>(workspace, L.inv_perm);
     int32_t* tok = at<int32_t>(workspace, L.tok_of);
-    e = launch_dispatch(s, topk_idx, counts, offsets, at<int32_t>(workspace, L.perm), inv, tok,
-                        at<int32_t>(workspace, L.blk_hist), err, cs);
-    if (e != cudaSuccess) return MOE_ERR_CUDA;
     // Both expert paths read routed rows from x through the row -> token map
     // (the tensor-core path with TMA gather4 for row blocks of at most
     // tc_gather_max_rows() rows).  Larger blocks need the contiguous permuted
     // copy, which is only built when a group can be that large (a group has at
     // most T rows: a token picks an expert once).
-    void* x_perm = nullptr;
-    if (need_tc && s.T > tc_gather_max_rows()) {
-        x_perm = at<void>(workspace, L.x_perm);
-        e = launch_gather_rows(s, x, inv, x_perm, cs);
-        if (e != cudaSuccess) return MOE_ERR_CUDA;
-    }
-
-    // 3. routed experts and the shared expert
+    void* x_perm = (need_tc && s.T > tc_gather_max_rows()) ? at<void>(workspace, L.x_perm) : nullptr;
     FfnGroups g{};
     g.E = s.E;
     g.has_shared = shared ? 1 : 0;
@@ -398,7 +388,20 @@ moe_status moe_forward(const moe_shape* shape, const void* x, const void* w_g, c
     FfnPlanHeader* hdr = at<FfnPlanHeader>(workspace, L.plan);
     int32_t* glist = at<int32_t>(workspace, L.gemv_list);
     int4* mtiles = at<int4>(workspace, L.mtile_list);
-    e = launch_ffn_plan(g, s.dtype, hdr, glist, mtiles, L.max_mtiles, gemv_limit(), true, 0, cs);
+    int32_t* perm = at<int32_t>(workspace, L.perm);
+    const bool fused = dispatch_plan_fusable(s);
+    if (fused)
+        e = launch_dispatch_plan_small(s, topk_idx, counts, offsets, perm, inv, tok, err, g, hdr,
+                                       glist, mtiles, L.max_mtiles, gemv_limit(), true, 0, cs);
+    else
+        e = launch_dispatch(s, topk_idx, counts, offsets, perm, inv, tok,
+                            at<int32_t>(workspace, L.blk_hist), err, cs);
+    if (e == cudaSuccess && x_perm) e = launch_gather_rows(s, x, inv, x_perm, cs);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+
+    // 3. routed experts and the shared expert
+    if (!fused)
+        e = launch_ffn_plan(g, s.dtype, hdr, glist, mtiles, L.max_mtiles, gemv_limit(), true, 0, cs);
     if (e == cudaSuccess && gemv_possible(s)) e = launch_ffn_gemv(g, s.dtype, hdr, glist, cs);
     // a group has at most T rows (a token picks an expert once)
     if (e == cudaSuccess && need_tc)
@@ -509,18 +512,12 @@ moe_status moe_forward_fp8(const moe_shape* shape, const void* x, const void* w_
     if (e == cudaSuccess) e = launch_topk_softmax(s, part, splits, bias, nullptr, topk_idx, topk_w, cs);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
 
-    // 2. dispatch and the permuted copy of the routed rows
+    // 2. dispatch (for small batches with the expert plan) and the permuted
+    //    copy of the routed rows
     int32_t* offsets = at<int32_t>(workspace, L.offsets);
     int32_t* inv = at<int32_t>(workspace, L.inv_perm);
     int32_t* tok = at<int32_t>(workspace, L.tok_of);
-    e = launch_dispatch(s, topk_idx, at<int32_t>(workspace, L.counts), offsets,
-                        at<int32_t>(workspace, L.perm), inv, tok, at<int32_t>(workspace, L.blk_hist),
-                        err, cs);
     void* x_perm = at<void>(workspace, L.x_perm);
-    if (e == cudaSuccess) e = launch_gather_rows(s, x, inv, x_perm, cs);
-    if (e != cudaSuccess) return MOE_ERR_CUDA;
-
-    // 3. routed and shared experts, 8-bit weights, single-SM tensor-core tiles
     FfnGroups g{};
     g.E = s.E;
     g.has_shared = shared ? 1 : 0;
@@ -555,8 +552,24 @@ moe_status moe_forward_fp8(const moe_shape* shape, const void* x, const void* w_
     int4* mtiles = at<int4>(workspace, L.mtile_list);
     const int lim = gemv8_limit(s);
     const bool pair = w8_pair();
-    e = launch_ffn_plan(g, s.dtype, hdr, glist, mtiles, L.max_mtiles, lim, pair,
-                        gemv8_small_rows(), cs);
+    int32_t* counts = at<int32_t>(workspace, L.counts);
+    int32_t* perm = at<int32_t>(workspace, L.perm);
+    const bool fused = dispatch_plan_fusable(s);
+    if (fused)
+        e = launch_dispatch_plan_small(s, topk_idx, counts, offsets, perm, inv, tok, err, g, hdr,
+                                       glist, mtiles, L.max_mtiles, lim, pair, gemv8_small_rows(),
+                                       cs);
+    else
+        e = launch_dispatch(s, topk_idx, counts, offsets, perm, inv, tok,
+                            at<int32_t>(workspace, L.blk_hist), err, cs);
+    if (e == cudaSuccess) e = launch_gather_rows(s, x, inv, x_perm, cs);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+
+    // 3. routed and shared experts, 8-bit weights: the 8-bit GEMV for small
+    //    groups, tensor-core tiles for the rest
+    if (!fused)
+        e = launch_ffn_plan(g, s.dtype, hdr, glist, mtiles, L.max_mtiles, lim, pair,
+                            gemv8_small_rows(), cs);
     if (e == cudaSuccess && lim > 0) e = launch_ffn_gemv_fp8(g, hdr, glist, lim, cs);
     // a group has at most T rows (a token picks an expert once; the shared group has T)
     if (e == cudaSuccess && s.T > lim)
@@ -573,7 +586,7 @@ moe_status moe_forward_fp8(const moe_shape* shape, const void* x, const void* w_
 // max_rows bounds the rows of any group (pair launches are skipped when no
 // group can take pair tiles).
 static cudaError_t run_ffn_w8a8(const moe_shape& s, FfnGroups& g, const WsLayout& L, void* ws,
-                                int64_t max_rows, DevError* err, cudaStream_t cs) {
+                                int64_t max_rows, bool planned, DevError* err, cudaStream_t cs) {
     FfnPlanHeader* hdr = at<FfnPlanHeader>(ws, L.plan);
     int32_t* glist = at<int32_t>(ws, L.gemv_list);
     int4* mtiles = at<int4>(ws, L.mtile_list);
@@ -583,7 +596,7 @@ static cudaError_t run_ffn_w8a8(const moe_shape& s, FfnGroups& g, const WsLayout
     cudaError_t e = cudaMemsetAsync(const_cast<float*>(g.sa_h), 0, sizeof(float) * R, cs);
     if (e == cudaSuccess && g.has_shared)
         e = cudaMemsetAsync(const_cast<float*>(g.sa_hs), 0, sizeof(float) * s.T, cs);
-    if (e == cudaSuccess)
+    if (e == cudaSuccess && !planned)
         e = launch_ffn_plan(g, s.dtype, hdr, glist, mtiles, L.max_mtiles, 0, true, 0, cs);
     if (e == cudaSuccess)
         e = launch_ffn_tc_a8_gate_up(g, hdr, mtiles, L.max_mtiles, may_pair, err, cs);
@@ -647,7 +660,7 @@ moe_status moe_expert_ffn_w8a8(const moe_shape* shape, const void* x_perm, const
     g.h = at<void>(workspace, L.h);
     g.y = y_perm;
     // a group has at most T*K rows here (the offsets are the caller's)
-    return cuda_status(run_ffn_w8a8(s, g, L, workspace, R, err, cs));
+    return cuda_status(run_ffn_w8a8(s, g, L, workspace, R, false, err, cs));
 }
 
 moe_status moe_forward_w8a8(const moe_shape* shape, const void* x, const void* w_g,
@@ -685,23 +698,16 @@ moe_status moe_forward_w8a8(const moe_shape* shape, const void* x, const void* w
     if (e == cudaSuccess) e = launch_topk_softmax(s, part, splits, bias, nullptr, topk_idx, topk_w, cs);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
 
-    // 2. dispatch; x quantised per token row, codes and scales gathered into
-    //    expert order (x_perm region: permuted codes [T*K][d], then x codes [T][d])
+    // 2. dispatch (for small batches with the expert plan); x quantised per
+    //    token row, codes and scales gathered into expert order (x_perm region:
+    //    permuted codes [T*K][d], then x codes [T][d])
     int32_t* offsets = at<int32_t>(workspace, L.offsets);
     int32_t* inv = at<int32_t>(workspace, L.inv_perm);
     int32_t* tok = at<int32_t>(workspace, L.tok_of);
-    e = launch_dispatch(s, topk_idx, at<int32_t>(workspace, L.counts), offsets,
-                        at<int32_t>(workspace, L.perm), inv, tok, at<int32_t>(workspace, L.blk_hist),
-                        err, cs);
     const int64_t R = (int64_t)s.T * s.K;
     float* sc = at<float>(workspace, L.ascale);
     uint8_t* xq_perm = at<uint8_t>(workspace, L.x_perm);
     uint8_t* xq = xq_perm + R * s.d;
-    if (e == cudaSuccess) e = launch_quantize_act_rows(s.T, s.d, x, s.d, xq, s.d, sc, cs);
-    if (e == cudaSuccess) e = launch_gather_codes(s, xq, sc, inv, xq_perm, sc + s.T, cs);
-    if (e != cudaSuccess) return MOE_ERR_CUDA;
-
-    // 3. routed and shared experts, W8A8 on the tensor cores
     FfnGroups g{};
     g.E = s.E;
     g.has_shared = shared ? 1 : 0;
@@ -735,8 +741,25 @@ moe_status moe_forward_w8a8(const moe_shape* shape, const void* x, const void* w
     g.h_s = at<void>(workspace, L.h_s);
     g.y = at<void>(workspace, L.y_perm);
     g.y_s = at<void>(workspace, L.y_s);
+    int32_t* counts = at<int32_t>(workspace, L.counts);
+    int32_t* perm = at<int32_t>(workspace, L.perm);
+    const bool fused = dispatch_plan_fusable(s);
+    if (fused)
+        e = launch_dispatch_plan_small(s, topk_idx, counts, offsets, perm, inv, tok, err, g,
+                                       at<FfnPlanHeader>(workspace, L.plan),
+                                       at<int32_t>(workspace, L.gemv_list),
+                                       at<int4>(workspace, L.mtile_list), L.max_mtiles, 0, true, 0,
+                                       cs);
+    else
+        e = launch_dispatch(s, topk_idx, counts, offsets, perm, inv, tok,
+                            at<int32_t>(workspace, L.blk_hist), err, cs);
+    if (e == cudaSuccess) e = launch_quantize_act_rows(s.T, s.d, x, s.d, xq, s.d, sc, cs);
+    if (e == cudaSuccess) e = launch_gather_codes(s, xq, sc, inv, xq_perm, sc + s.T, cs);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+
+    // 3. routed and shared experts, W8A8 on the tensor cores
     // a group has at most T rows (a token picks an expert once; the shared group has T)
-    e = run_ffn_w8a8(s, g, L, workspace, s.T, err, cs);
+    e = run_ffn_w8a8(s, g, L, workspace, s.T, fused, err, cs);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
 
     // 4. combine

@@ -209,3 +209,23 @@ def test_forward_skewed_groups_cover_every_activation_path(moe, monkeypatch, gat
     assert counts.max() >= 512 and counts.min() <= 32 and ((counts > 32) & (counts < 512)).any()
     ref = oracle.forward(host(L.x), L.hp, cfg.K, dtype=cfg.dtype, bias=L.bias_host())["y"]
     _check(cfg, to_f64(L.forward(moe)), ref)
+
+
+@pytest.mark.parametrize("name", ["dsv3_decode", "dsv3_sweep_T64", "dsv3_decode_fp8", "tiny_f32",
+                                  "w8a8_T64"])
+def test_fused_small_dispatch_changes_no_bit(moe, name, monkeypatch):
+    """Small batches (T*K <= 1024) run the dispatch and the expert plan as one
+    single-block launch; the separate kernels (MOE_FUSED_DISPATCH=0) give the
+    same bits."""
+    from dataclasses import replace
+    cfg = (replace(mi.CONFIGS["dsv3_sweep_fp8_T64"], name="w8a8_T64", acts="e4m3")
+           if name == "w8a8_T64" else mi.CONFIGS[name])
+    assert cfg.T * cfg.K <= 1024
+    L = Layer(cfg)
+    s = L.shape(moe)
+    ws = moe.alloc_workspace(s)
+    monkeypatch.setenv("MOE_FUSED_DISPATCH", "0")
+    ref = L.forward(moe, ws=ws)
+    monkeypatch.setenv("MOE_FUSED_DISPATCH", "1")
+    out = L.forward(moe, ws=ws)
+    assert torch.equal(out, ref)
