@@ -336,6 +336,7 @@ def run_ours(args):
         # dominant stage, timed alone on the same stream: the expert FFN (tcgen05
         # gate/up GEMM with fused SiLU*mul, then the down GEMM) of this batch
         stage = time_expert_ffn(moe, cfg, x, p, bias, stream, args.steps, n_active)
+        spread = step_stats(fwd, stream, args.steps)
     t_ms = ev0.elapsed_time(ev1) / args.steps
     t_ms_max = max_over_ranks(t_ms, ws_n)
     code = moe.moe_get_device_error(ws)
@@ -379,6 +380,8 @@ def run_ours(args):
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": e2e["h2d"],
                 "d2h_bytes_per_step": e2e["d2h"]},
         "gpu_launches": launches_per_forward(cfg) * args.steps,
+        # per-call spread, from a separate pass with an event between calls
+        "step_ms": spread,
         "clocks": clk.summary(),
         "peaks": peaks,
     }
@@ -516,6 +519,25 @@ def stage_roofline(cfg, stage, peaks) -> dict:
     return out
 
 
+def step_stats(fn, stream, steps: int) -> dict:
+    """Per-call durations from an event between consecutive calls (a separate
+    pass after the timed region, so the events cannot disturb it): median,
+    standard deviation, min and max in ms."""
+    import statistics
+    import torch
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        ev[0].record(stream)
+        for i in range(steps):
+            fn()
+            ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    d = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
+    return {"median": statistics.median(d), "std": statistics.pstdev(d), "min": min(d),
+            "max": max(d), "n": steps}
+
+
 def time_e2e(call, stream, steps, x_dev) -> dict:
     """Through the C ABI with host buffers: every step copies its x from pinned
     host memory to the device, runs the forward call and copies y back to pinned
@@ -607,7 +629,9 @@ def bench_workload(moe, cfg, peaks, steps: int, graph: bool = False) -> dict:
         return e0.elapsed_time(e1) / steps
 
     ms = timed(fwd)
+    spread = step_stats(fwd, st, steps)
     out = {"workload": cfg.name, "T": cfg.T, "us_per_call": ms * 1e3,
+           "us_per_call_median": spread["median"] * 1e3, "us_per_call_std": spread["std"] * 1e3,
            "tokens_per_s": cfg.T / (ms / 1e3), "active_experts": n_active,
            "alg_bytes": layer_bytes(cfg, n_active), "flops": layer_flops(cfg)}
     if graph:
