@@ -218,8 +218,10 @@ moe_status moe_forward(const moe_shape *shape, const void *x, const void *w_g,
  *     w_hat[r][c] = e4m3_value(code[r][c]) * scale[r].
  * The layer is the bf16 layer above with every expert matrix (routed and
  * shared) replaced by w_hat; x, w_g, y and the intermediates stay bf16.
- * The kernels widen codes to bf16 (exact), multiply on the tensor cores
- * with fp32 accumulation and apply the row scale to the fp32 sums.
+ * Groups of at most 8 rows (decode) stream their codes through a GEMV that
+ * widens them to f16 (exact) for mma.sync; larger groups widen them to bf16
+ * (exact) for the tcgen05 tensor cores.  Both accumulate in fp32 and apply
+ * the row scale to the fp32 sums.
  */
 typedef struct moe_fp8_experts {
     const uint8_t *w_gate;  /* [E][I][d] codes                       */
@@ -254,8 +256,8 @@ moe_status moe_quantize_fp8_rows(int64_t rows, int64_t cols, int32_t dtype,
  * moe_expert_ffn with 8-bit expert weights: *w is a HOST struct of device
  * pointers (the ws_* / ss_* members are ignored here).  shape->dtype must be
  * MOE_BF16 and d, inter multiples of 128 (else MOE_ERR_UNSUPPORTED); scale
- * arrays 16-byte aligned.  Every group runs on the tensor cores (128-row
- * tiles).  Same workspace size as moe_expert_ffn.
+ * arrays 16-byte aligned.  Groups of at most 8 rows take the 8-bit GEMV,
+ * larger ones the tensor cores.  Same workspace size as moe_expert_ffn.
  */
 moe_status moe_expert_ffn_fp8(const moe_shape *shape, const void *x_perm,
                               const int32_t *offsets, const moe_fp8_experts *w,

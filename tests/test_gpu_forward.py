@@ -229,3 +229,23 @@ def test_fused_small_dispatch_changes_no_bit(moe, name, monkeypatch):
     monkeypatch.setenv("MOE_FUSED_DISPATCH", "1")
     out = L.forward(moe, ws=ws)
     assert torch.equal(out, ref)
+
+
+def test_fused_small_dispatch_at_its_limits(moe, monkeypatch):
+    """The largest fused case: 1024 slots over 1024 experts (the block's
+    per-warp table is 128 KB of shared memory), with a shared expert; the
+    outputs match the four-launch path bit for bit and the oracle."""
+    cfg = mi.LayerConfig("fused_limits", T=256, d=128, E=1024, K=4, I=128, Is=128)
+    L = Layer(cfg)
+    s = L.shape(moe)
+    ws = moe.alloc_workspace(s)
+    monkeypatch.setenv("MOE_FUSED_DISPATCH", "0")
+    ref = L.forward(moe, ws=ws)
+    monkeypatch.setenv("MOE_FUSED_DISPATCH", "1")
+    out = L.forward(moe, ws=ws)
+    assert torch.equal(out, ref)
+    toks = np.arange(0, cfg.T, 8)
+    want = L.oracle_tokens(toks)
+    ok = boundary_margin(want["logits"], cfg.K) >= MARGIN
+    got = to_f64(out[torch.from_numpy(toks[ok]).long().cuda()])
+    assert rel_l2(got, want["y"][ok]) <= BF16_REL_L2
