@@ -159,6 +159,9 @@ struct TcParams {
     const float* sc1[2];        // W8, A8: scale of each up weight row
     const float* sa[2];         // A8: scale of each activation row (routed, shared)
     unsigned int* hmax[2];      // A8 gate/up: per-row max |h| as fp32 bits, raised atomically
+    CUtensorMap g64[2];         // half pair tiles, gate/up: gate rows, box 64 rows
+    CUtensorMap u64[2];         // half pair tiles, gate/up: up rows, box 64 rows
+    int half_tiles;             // pair tiles of <= 128 rows run as M = 128 (64 rows per CTA)
     const int32_t* row_src;     // token of each routed row (gather from x), or null
     int gather_max;             // gather a CTA's routed rows when it has at most this many
     const FfnPlanHeader* hdr;
@@ -185,6 +188,7 @@ struct Tile {
     int n0;     // first output column
     int kblocks;
     bool valid;
+    bool half;  // a pair tile of at most 128 rows, run with M = 128: 64 rows per CTA
 };
 
 // KSTEP: elements of the reduction per K block (64 bf16 or 128 8-bit values,
@@ -218,6 +222,7 @@ __device__ __forceinline__ Tile decode_tile_entry(const TcParams& p, int4 e, int
     tl.wrow0 = (tl.kind == 0 ? g * p.wrows[0] : 0) + tl.n0;
     tl.kblocks = (p.kdim[tl.kind] + KSTEP - 1) / KSTEP;
     tl.valid = tl.n0 < p.n_out[tl.kind] && tl.rows > 0;
+    tl.half = PAIR && p.half_tiles != 0 && tl.rows <= BMC;
     return tl;
 }
 
@@ -514,9 +519,10 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
             for (int t = unit; t < n_tiles && ok; t += n_units) {
                 const Tile tl = decode_tile<EPI, PAIR, kKStep>(p, list_len, t);
                 if (!tl.valid) continue;
-                const int rows_me = max(0, min(BMC, tl.rows - (int)rank * BMC));
+                const int crows = tl.half ? BMC / 2 : BMC;  // activation rows per CTA
+                const int rows_me = max(0, min(crows, tl.rows - (int)rank * crows));
                 const CUtensorMap* ma = &p.a[tl.kind][abox_for(rows_me)];
-                const int arow = tl.row0 + (int)rank * BMC;
+                const int arow = tl.row0 + (int)rank * crows;
                 const bool gather = tl.kind == 0 && p.row_src != nullptr && rows_me <= p.gather_max;
                 const int n4 = gather ? (rows_me + 3) / 4 : 0;
                 int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
@@ -537,8 +543,23 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
                 uint32_t tx;
                 const CUtensorMap* mb;
                 int brow;
+                // Half gate/up pair tiles: each CTA loads the gate rows (smem rows 0-63)
+                // and the up rows (64-127) of its 64 intermediate indices, so that with
+                // M = 128 the gate and up sums of one index land in the same thread's
+                // tensor-memory columns (c and 64 + c).
+                const bool split64 = EPI == EPI_SWIGLU && tl.half;
+                const int j64 = tl.wrow0 + (int)rank * (BMC / 2);
+                const auto load_b_pair = [&](uint8_t* b_dst, uint32_t fb, int k0, const CUtensorMap* mbp,
+                                             int browp) {
+                    if (split64) {
+                        ptx::tma_load_2d_pair(b_dst, &p.g64[tl.kind], fb, k0, j64);
+                        ptx::tma_load_2d_pair(b_dst + 64 * 128, &p.u64[tl.kind], fb, k0, j64);
+                    } else {
+                        ptx::tma_load_2d_pair(b_dst, mbp, fb, k0, browp);
+                    }
+                };
                 if constexpr (PAIR) {
-                    tx = a_bytes(min(BMC, tl.rows)) + a_bytes(max(0, tl.rows - BMC)) + 2 * S::kBBytes;
+                    tx = a_bytes(min(crows, tl.rows)) + a_bytes(max(0, tl.rows - crows)) + 2 * S::kBBytes;
                     mb = (EPI == EPI_SWIGLU && rank == 1) ? &p.b1[tl.kind] : &p.b0[tl.kind];
                     brow = tl.wrow0 + ((EPI == EPI_SWIGLU) ? 0 : (int)rank * S::kBRows);
                 } else {
@@ -558,7 +579,7 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
                                 const uint32_t fb = full0 + (uint32_t)(stage * sizeof(uint64_t));
                                 if (rank == 0) ptx::mbar_arrive_expect_tx(&ctl->full[stage], tx);
                                 if (rows_me > 0) ptx::tma_load_2d_pair(a_dst, ma, fb, k0, arow);
-                                ptx::tma_load_2d_pair(b_dst, mb, fb, k0, brow);
+                                load_b_pair(b_dst, fb, k0, mb, brow);
                             } else {
                                 ptx::mbar_arrive_expect_tx(&ctl->full[stage], tx);
                                 ptx::tma_load_2d(a_dst, ma, &ctl->full[stage], k0, arow);
@@ -587,7 +608,7 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
                             if (lane == 0 && rank == 0) ptx::mbar_arrive_expect_tx(&ctl->full[stage], tx);
                             __syncwarp();
                             if (lane < n4) ptx::tma_gather4_pair(a_dst + lane * 512, &p.ag, fb, k0, r0, r1, r2, r3);
-                            if (lane == 0) ptx::tma_load_2d_pair(b_dst, mb, fb, k0, brow);
+                            if (lane == 0) load_b_pair(b_dst, fb, k0, mb, brow);
                         } else {
                             if (lane == 0) ptx::mbar_arrive_expect_tx(&ctl->full[stage], tx);
                             __syncwarp();  // the byte count is posted before any gathered row lands
@@ -631,6 +652,9 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
         if (lane == 0 && rank == 0) {
             constexpr uint32_t idesc = A8 ? ptx::idesc_e4m3_f32(S::kTileRows, BN)
                                           : ptx::idesc_bf16_f32(S::kTileRows, BN);
+            // half pair tiles: M = 128, 64 rows of A from each CTA
+            constexpr uint32_t idesc_half = A8 ? ptx::idesc_e4m3_f32(BMC, BN)
+                                               : ptx::idesc_bf16_f32(BMC, BN);
             int stage = 0;       // B stage (and A stage without W8)
             uint32_t phase = 0;
             int ast = 0;         // W8: A stage
@@ -651,6 +675,7 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
                 if (!wait_bounded(&ctl->tempty[acc], acc_phase ^ 1u, ctl, p, 200)) { ok = false; break; }
                 ptx::tc_fence_after();
                 const uint32_t d_tmem = tmem + (uint32_t)(acc * BN);
+                const uint32_t id_t = tl.half ? idesc_half : idesc;
                 for (int kb = 0; kb < tl.kblocks; ++kb) {
                     if (!wait_bounded(&ctl->full[stage], phase, ctl, p, 201)) { ok = false; break; }
                     if (W8 && !wait_bounded(&ctl->afull[ast], aphase, ctl, p, 202)) { ok = false; break; }
@@ -664,10 +689,10 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
                         const uint64_t bd = ptx::sw128_kmajor_desc(b_base + kk * 32);
                         const uint32_t accum = (kb | kk) != 0 ? 1u : 0u;
                         if constexpr (A8) {
-                            if constexpr (PAIR) ptx::tc_mma_f8_pair(d_tmem, ad, bd, idesc, accum);
+                            if constexpr (PAIR) ptx::tc_mma_f8_pair(d_tmem, ad, bd, id_t, accum);
                             else ptx::tc_mma_f8(d_tmem, ad, bd, idesc, accum);
                         } else {
-                            if constexpr (PAIR) ptx::tc_mma_f16_pair(d_tmem, ad, bd, idesc, accum);
+                            if constexpr (PAIR) ptx::tc_mma_f16_pair(d_tmem, ad, bd, id_t, accum);
                             else ptx::tc_mma_f16(d_tmem, ad, bd, idesc, accum);
                         }
                     }
@@ -711,13 +736,71 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
             if (!__shfl_sync(0xffffffffu, ok, 0)) break;
             ptx::tc_fence_after();
             const uint32_t tbase = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * BN);
-            const int rows_me = max(0, min(BMC, tl.rows - (int)rank * BMC));
-            const bool row_ok = r < rows_me;
-            const int64_t orow = (int64_t)tl.row0 + (int64_t)rank * BMC + r;
+            // Half pair tiles (M = 128) leave each CTA 64 rows: tensor-memory lane L
+            // holds row L & 63; lanes 0-63 hold output columns 0-127 of the n-block
+            // and lanes 64-127 columns 128-255, in tensor-memory columns 0-127.
+            const int crows = tl.half ? BMC / 2 : BMC;
+            const int hi = tl.half ? (r >> 6) : 0;
+            const int rr = tl.half ? (r & 63) : r;
+            const int rows_me = max(0, min(crows, tl.rows - (int)rank * crows));
+            const bool row_ok = rr < rows_me;
+            const int arow_me = tl.row0 + (int)rank * crows + rr;  // activation row of this thread
+            const int64_t orow = arow_me;
             const int nvalid = p.n_out[tl.kind];
             // A8: the activation row's scale factors out of every output of the row
-            const float sa = (A8 && row_ok) ? __ldg(p.sa[tl.kind] + (tl.row0 + (int)rank * BMC + r)) : 1.0f;
-            if (EPI == EPI_SWIGLU) {
+            const float sa = (A8 && row_ok) ? __ldg(p.sa[tl.kind] + arow_me) : 1.0f;
+            if (EPI == EPI_SWIGLU && tl.half) {
+                // tensor-memory columns 0-63: gate sums, 64-127: up sums of the same 64
+                // intermediate indices (n0 + 64 hi ..) of this thread's row
+                bf16* out = (bf16*)p.out[tl.kind] + orow * p.ld_out[tl.kind] + tl.n0 + 64 * hi;
+                uint32_t hmax_bits = 0;
+#pragma unroll 1
+                for (int c = 0; c < 64; c += 16) {
+                    uint32_t g[16], u[16];
+                    ptx::tmem_ld16(tbase + c, g);
+                    ptx::tmem_ld16(tbase + 64 + c, u);
+                    const int hc = 64 * hi + c;  // first h column, relative to n0
+                    const bool col_ok = tl.n0 + hc < nvalid;
+                    float gs[16], us[16];
+                    if constexpr (W8 || A8) {
+                        if (col_ok) {
+                            ld_scale16(p.sc0[tl.kind] + tl.wrow0 + hc, gs);
+                            ld_scale16(p.sc1[tl.kind] + tl.wrow0 + hc, us);
+                        }
+                    }
+                    ptx::tmem_ld_wait();
+                    if (row_ok && col_ok) {
+                        if constexpr (W8 || A8) {
+                            if constexpr (A8) {
+#pragma unroll
+                                for (int k = 0; k < 16; ++k) { gs[k] *= sa; us[k] *= sa; }
+                            }
+                        } else {
+#pragma unroll
+                            for (int k = 0; k < 16; ++k) { gs[k] = 1.0f; us[k] = 1.0f; }
+                        }
+                        uint32_t w[8];
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            const float h0 = silu_mul(__uint_as_float(g[2 * k]) * gs[2 * k],
+                                                      __uint_as_float(u[2 * k]) * us[2 * k]);
+                            const float h1 = silu_mul(__uint_as_float(g[2 * k + 1]) * gs[2 * k + 1],
+                                                      __uint_as_float(u[2 * k + 1]) * us[2 * k + 1]);
+                            const __nv_bfloat162 b2 = __floats2bfloat162_rn(h0, h1);
+                            w[k] = *reinterpret_cast<const uint32_t*>(&b2);
+                        }
+                        if constexpr (A8) {
+#pragma unroll
+                            for (int k = 0; k < 8; ++k)
+                                hmax_bits = max(hmax_bits, max(w[k] & 0x7FFFu, (w[k] >> 16) & 0x7FFFu));
+                        }
+                        uint4* dst = reinterpret_cast<uint4*>(out + c);
+                        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                    }
+                }
+                if (A8 && row_ok && hmax_bits != 0) atomicMax(p.hmax[tl.kind] + arow_me, hmax_bits << 16);
+            } else if (EPI == EPI_SWIGLU) {
                 bf16* out = (bf16*)p.out[tl.kind] + orow * p.ld_out[tl.kind] + tl.n0;
                 uint32_t hmax_bits = 0;  // A8: largest |h| this thread stored (bf16 bits)
 #pragma unroll 1
@@ -767,14 +850,15 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
                     }
                 }
                 // A8: the row's max |h| over every tile of the row, for its quantiser
-                if (A8 && row_ok && hmax_bits != 0)
-                    atomicMax(p.hmax[tl.kind] + (tl.row0 + (int)rank * BMC + r), hmax_bits << 16);
+                if (A8 && row_ok && hmax_bits != 0) atomicMax(p.hmax[tl.kind] + arow_me, hmax_bits << 16);
             } else if (EPI == EPI_STORE_BF16) {
                 bf16* out = (bf16*)p.out[tl.kind] + orow * p.ld_out[tl.kind] + tl.n0;
+                const int ncol = tl.half ? BN / 2 : BN;  // tensor-memory columns of this thread's row
 #pragma unroll 1
-                for (int c = 0; c < BN; c += 16) {
+                for (int tc = 0; tc < ncol; tc += 16) {
                     uint32_t v[16];
-                    ptx::tmem_ld16(tbase + c, v);
+                    ptx::tmem_ld16(tbase + tc, v);
+                    const int c = tc + (BN / 2) * hi;  // output column, relative to n0
                     const bool col_ok = tl.n0 + c < nvalid;
                     float ds[16];
                     if constexpr (W8 || A8) {
@@ -1035,6 +1119,18 @@ int tc_gather_max_rows() {
     return x < 0 ? 0 : (x > BMC ? BMC : x);
 }
 
+// Pair tiles of at most 128 rows (a group's last m-tile) run as M = 128 MMAs
+// (MOE_HALF_TILES=0, read per call, keeps them at M = 256).  Measured on GB300
+// (interleaved A/B): Mixtral-shaped prefill 1.0 % faster in bf16 and 1.6 % with
+// 8-bit operands, other workloads unchanged -- less than the 6.8 % of MMA rows
+// the half tiles drop there, so an M = 128 pair MMA costs more than half of an
+// M = 256 one.  (Loading the gate/up rows of a half tile in alternating 8-row
+// blocks instead of two 64-row boxes made it 7 % slower: small TMA boxes.)
+int half_tiles() {
+    const char* s = getenv("MOE_HALF_TILES");
+    return (s && s[0] == '0') ? 0 : 1;
+}
+
 // Groups with at least this many rows take 256-row pair tiles.
 // MOE_PAIR_MIN_ROWS > 0 sets a fixed threshold; unset or 0 lets the plan pick
 // the cheaper tile shape per group (padding over measured efficiency).
@@ -1074,14 +1170,20 @@ cudaError_t launch_ffn_tc(const FfnGroups& g, const FfnPlanHeader* hdr, const in
     }
     ok &= make_map(&p.b0[0], g.w_gate, (int64_t)g.E * g.I, g.d, 128);
     ok &= make_map(&p.b1[0], g.w_up, (int64_t)g.E * g.I, g.d, 128);
+    ok &= make_map(&p.g64[0], g.w_gate, (int64_t)g.E * g.I, g.d, 64);
+    ok &= make_map(&p.u64[0], g.w_up, (int64_t)g.E * g.I, g.d, 64);
     if (g.has_shared) {
         ok &= make_amaps(p.a[1], g.a_shared, g.T, g.d);
         ok &= make_map(&p.b0[1], g.ws_gate, g.Is, g.d, 128);
         ok &= make_map(&p.b1[1], g.ws_up, g.Is, g.d, 128);
+        ok &= make_map(&p.g64[1], g.ws_gate, g.Is, g.d, 64);
+        ok &= make_map(&p.u64[1], g.ws_up, g.Is, g.d, 64);
     } else {
         for (int b = 0; b < kABoxes; ++b) p.a[1][b] = p.a[0][b];
         p.b0[1] = p.b0[0]; p.b1[1] = p.b1[0];
+        p.g64[1] = p.g64[0]; p.u64[1] = p.u64[0];
     }
+    p.half_tiles = half_tiles();
     p.bw[0] = p.b0[0]; p.bw[1] = p.b0[1];  // unused by the SWIGLU epilogue
     if (!ok) return cudaErrorInvalidValue;
     p.hdr = hdr;
@@ -1122,6 +1224,7 @@ cudaError_t launch_ffn_tc(const FfnGroups& g, const FfnPlanHeader* hdr, const in
     }
     q.b1[0] = q.b0[0]; q.b1[1] = q.b0[1];
     if (!ok) return cudaErrorInvalidValue;
+    q.half_tiles = half_tiles();
     q.hdr = hdr;
     q.E = g.E;
     q.max_mtiles = max_mtiles;
@@ -1262,6 +1365,9 @@ cudaError_t launch_ffn_tc_a8_gate_up(const FfnGroups& g, const FfnPlanHeader* hd
     p.gather_max = 0;
     ok &= make_map_u8(&p.b0[0], g.w_gate, (int64_t)g.E * g.I, g.d, 128);
     ok &= make_map_u8(&p.b1[0], g.w_up, (int64_t)g.E * g.I, g.d, 128);
+    ok &= make_map_u8(&p.g64[0], g.w_gate, (int64_t)g.E * g.I, g.d, 64);
+    ok &= make_map_u8(&p.u64[0], g.w_up, (int64_t)g.E * g.I, g.d, 64);
+    p.half_tiles = half_tiles();
     p.sc0[0] = g.s_gate;
     p.sc1[0] = g.s_up;
     p.sa[0] = g.sa_routed;
@@ -1271,12 +1377,15 @@ cudaError_t launch_ffn_tc_a8_gate_up(const FfnGroups& g, const FfnPlanHeader* hd
         ok &= make_amaps_u8(p.a[1], g.a_shared, g.T, g.d, g.d);
         ok &= make_map_u8(&p.b0[1], g.ws_gate, g.Is, g.d, 128);
         ok &= make_map_u8(&p.b1[1], g.ws_up, g.Is, g.d, 128);
+        ok &= make_map_u8(&p.g64[1], g.ws_gate, g.Is, g.d, 64);
+        ok &= make_map_u8(&p.u64[1], g.ws_up, g.Is, g.d, 64);
         p.sc0[1] = g.ss_gate;
         p.sc1[1] = g.ss_up;
         p.sa[1] = g.sa_shared;
     } else {
         for (int b = 0; b < kABoxes; ++b) p.a[1][b] = p.a[0][b];
         p.b0[1] = p.b0[0]; p.b1[1] = p.b1[0];
+        p.g64[1] = p.g64[0]; p.u64[1] = p.u64[0];
         p.sc0[1] = p.sc0[0]; p.sc1[1] = p.sc1[0];
         p.sa[1] = p.sa[0];
     }
@@ -1334,6 +1443,7 @@ cudaError_t launch_ffn_tc_a8_down(const FfnGroups& g, const FfnPlanHeader* hdr,
     q.sc1[0] = q.sc0[0]; q.sc1[1] = q.sc0[1];
     q.ag = q.a[0][0];
     q.row_src = nullptr;
+    q.half_tiles = half_tiles();
     if (!ok) return cudaErrorInvalidValue;
     q.hdr = hdr;
     q.E = g.E;

@@ -125,3 +125,23 @@ def test_bounded_wait_reports_timeout_and_the_context_survives(moe, monkeypatch)
         monkeypatch.delenv("MOE_TC_TIMEOUT_MS")
         y_ok, ref = _run(moe, counts, 256, 256, "bf16", limit=0)
     assert rel_l2(y_ok, ref) <= BF16_REL_L2
+
+
+@pytest.mark.parametrize("counts,d,I", [([1100, 0, 257, 640, 1, 128, 0, 900], 512, 256),
+                                        ([300, 2, 130, 60], 1024, 384)])
+def test_half_pair_tiles_match_full_pair_tiles(moe, counts, d, I, monkeypatch):
+    """Every group on CTA-pair tiles; a group's last tile with at most 128 rows
+    runs as an M = 128 MMA (64 rows per CTA; gate/up weight rows loaded in
+    alternating 8-row blocks) or, with MOE_HALF_TILES=0, as a full M = 256 tile.
+    Both agree with the oracle and with each other."""
+    from tests.gpu_util import pair_min_rows
+    out = {}
+    for half in ("0", "1"):
+        monkeypatch.setenv("MOE_HALF_TILES", half)
+        with pair_min_rows(1):
+            y, ref = _run(moe, counts, d, I, "bf16", limit=0, seed=9)
+        assert rel_l2(y, ref) <= BF16_REL_L2
+        for r in range(y.shape[0]):
+            assert rel_l2(y[r], ref[r]) <= 2 * BF16_REL_L2, r
+        out[half] = y
+    assert rel_l2(out["1"], out["0"]) <= 1e-3

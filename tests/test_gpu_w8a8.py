@@ -177,3 +177,16 @@ def test_w8a8_stalled_copy_times_out_and_the_context_survives(moe, monkeypatch):
     L.x = _clean_x(L)
     y = to_f64(L.forward(moe))
     _check_rows(y, L.oracle_tokens(np.arange(cfg.T))["y"])
+
+
+def test_expert_ffn_w8a8_half_pair_tiles_match_full_pair_tiles(moe, monkeypatch):
+    """8-bit operands on pair tiles whose last tile has at most 128 rows: M = 128
+    (default) or M = 256 (MOE_HALF_TILES=0); both match the oracle."""
+    out = {}
+    for half in ("0", "1"):
+        monkeypatch.setenv("MOE_HALF_TILES", half)
+        with pair_min_rows(1):
+            y, ref = _expert_ffn_case(moe, [300, 2, 130, 60, 640], 512, 384)
+        _check_rows(y, ref)
+        out[half] = y
+    assert rel_l2(out["1"], out["0"]) <= 1e-3
