@@ -1120,12 +1120,7 @@ int tc_gather_max_rows() {
 }
 
 // Pair tiles of at most 128 rows (a group's last m-tile) run as M = 128 MMAs
-// (MOE_HALF_TILES=0, read per call, keeps them at M = 256).  Measured on GB300
-// (interleaved A/B): Mixtral-shaped prefill 1.0 % faster in bf16 and 1.6 % with
-// 8-bit operands, other workloads unchanged -- less than the 6.8 % of MMA rows
-// the half tiles drop there, so an M = 128 pair MMA costs more than half of an
-// M = 256 one.  (Loading the gate/up rows of a half tile in alternating 8-row
-// blocks instead of two 64-row boxes made it 7 % slower: small TMA boxes.)
+// (MOE_HALF_TILES=0, read per call, keeps them at M = 256).
 int half_tiles() {
     const char* s = getenv("MOE_HALF_TILES");
     return (s && s[0] == '0') ? 0 : 1;
