@@ -665,8 +665,8 @@ def bench_all(moe, peaks, args) -> list:
     for name in ("tiny_f32", "mixtral_prefill", "dsv3_decode", "dsv3_prefill_zipf",
                  *[f"dsv3_sweep_T{t}" for t in mi.SWEEP_T], "dsv3_decode_sigmoid",
                  "dsv3_decode_fp8", "dsv3_sweep_fp8_T64", "dsv3_sweep_fp8_T512",
-                 "mixtral_prefill_fp8", "dsv3_sweep_w8a8_T512", "dsv3_sweep_w8a8_T4096",
-                 "mixtral_prefill_w8a8"):
+                 "mixtral_prefill_fp8", "dsv3_decode_w8a8", "dsv3_sweep_w8a8_T512",
+                 "dsv3_sweep_w8a8_T4096", "mixtral_prefill_w8a8", "dsv3_prefill_zipf_w8a8"):
         cfg = mi.CONFIGS[name]
         res.append(bench_workload(moe, cfg, peaks, steps=max(10, args.steps),
                                   graph=cfg.T <= 64))

@@ -29,7 +29,8 @@ Workloads (shapes and distributions; names by what they are):
                       with an RMS of about 162; each weight row has its own fp32
                       scale std / 162 * U(0.8, 1.2), std being the bf16 workload's
                       weight std.  The router weights stay bf16.
-  mixtral_prefill_w8a8, dsv3_sweep_w8a8_T{512,4096}
+  mixtral_prefill_w8a8, dsv3_sweep_w8a8_T{512,4096}, dsv3_decode_w8a8,
+  dsv3_prefill_zipf_w8a8
                       the 8-bit-weight workloads run with 8-bit activations too
                       (the library quantises x and the hidden rows per row).
 
@@ -106,6 +107,11 @@ CONFIGS["mixtral_prefill_w8a8"] = replace(CONFIGS["mixtral_prefill_fp8"],
 for _t in (512, 4096):
     CONFIGS[f"dsv3_sweep_w8a8_T{_t}"] = replace(CONFIGS["dsv3_decode_fp8"],
                                                 name=f"dsv3_sweep_w8a8_T{_t}", T=_t, acts="e4m3")
+CONFIGS["dsv3_decode_w8a8"] = replace(CONFIGS["dsv3_decode_fp8"], name="dsv3_decode_w8a8",
+                                      acts="e4m3")
+CONFIGS["dsv3_prefill_zipf_w8a8"] = replace(CONFIGS["dsv3_prefill_zipf"],
+                                            name="dsv3_prefill_zipf_w8a8", weights="e4m3",
+                                            acts="e4m3")
 SWEEP_T = (1, 8, 64, 512, 4096)
 for _t in SWEEP_T:
     CONFIGS[f"dsv3_sweep_T{_t}"] = LayerConfig(f"dsv3_sweep_T{_t}", T=_t, d=7168, E=256, K=8,

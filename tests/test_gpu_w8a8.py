@@ -107,7 +107,7 @@ def test_forward_w8a8_differs_from_the_8bit_weight_layer(moe):
     assert 2e-2 < d < 0.2, d
 
 
-@pytest.mark.parametrize("name", ["mixtral_prefill_w8a8", "dsv3_sweep_w8a8_T512"])
+@pytest.mark.parametrize("name", ["mixtral_prefill_w8a8", "dsv3_sweep_w8a8_T512", "dsv3_decode_w8a8"])
 def test_forward_w8a8_full_size_sampled_tokens(moe, name):
     cfg = mi.CONFIGS[name]
     L = Layer(cfg)
