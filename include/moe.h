@@ -32,8 +32,13 @@
  *    no TF32) or MOE_BF16 (bf16 storage, fp32 accumulation).  Router scores
  *    and routing weights are always fp32; indices are int32.
  *  - Ownership: the caller allocates every buffer, including `workspace`
- *    (size from moe_workspace_bytes).  The library never allocates, frees or
- *    synchronises; all work is enqueued on `stream` in order.
+ *    (size from moe_workspace_bytes).  The library never allocates device
+ *    memory, frees or synchronises; all work is ordered on `stream`.  When
+ *    one call's tensor-core stage has both 256-row (CTA-pair) and 128-row
+ *    tiles, the 128-row grids run on a second stream of the library's own,
+ *    forked from `stream` with an event and joined back before the call's
+ *    next kernel (so the call stays ordered on `stream` and graph capturable);
+ *    MOE_CONCURRENT=0 keeps everything on `stream`.
  *  - Errors: argument errors return a non-zero moe_status immediately and
  *    enqueue nothing.  A failed launch returns MOE_ERR_CUDA.  Errors found
  *    on the device (index out of range, a bounded wait that ran out) are
@@ -48,7 +53,9 @@
  *    index (scores compared as floats, so -0.0 == +0.0); slot j of a token
  *    holds its j-th pick (descending score).  Flat slot f = t*K + j.
  *  - Threading: entry points are reentrant and keep no mutable global state
- *    beyond per-device attributes cached on first use.
+ *    beyond per-device attributes cached on first use and, per host thread
+ *    and device, that second stream and its two events (made on first use
+ *    outside stream capture, kept for the thread's lifetime).
  */
 #ifndef MOE_H
 #define MOE_H

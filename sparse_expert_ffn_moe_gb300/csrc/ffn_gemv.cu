@@ -63,8 +63,16 @@ __device__ int32_t scan_1024(int32_t v, int32_t* sh, int32_t* total) {
 // least pair_min rows, tiles of pair_m rows) or to the single-tile list
 // (tiles of single_m rows).  Tile entries are (group, first row of the group,
 // rows of the group, index of the m-tile within the group).
+//
+// SM split (split_rho > 0): the pair-tile and single-tile GEMMs then run side
+// by side, and the plan divides the sms between them in proportion to their
+// estimated work, in units of one MMA K step of one tile on one SM: a pair
+// tile costs 2 (two SMs), a single-tile group max(tiles, split_rho / 100) --
+// its few rows leave it bound by streaming the expert's weights, which costs
+// about split_rho / 100 MMA steps per weight K step on one SM.
 struct PlanArgs {
     int E, has_shared, T, limit, small, single_m, pair_min, pair_m, max_mtiles;
+    int sms, split_rho;
     FfnPlanHeader* hdr;
     int32_t* gemv_list;
     int4* mtile_list;
@@ -80,8 +88,8 @@ __device__ void plan_groups(const int32_t* offsets, const PlanArgs& a) {
     int32_t* gemv_list = a.gemv_list;
     int4* mtile_list = a.mtile_list;
     __shared__ int32_t sh[32];
-    __shared__ int32_t tot_g, tot_g2, tot_s, tot_p, base_g, base_g2, base_s, base_p;
-    if (threadIdx.x == 0) { base_g = 0; base_g2 = 0; base_s = 0; base_p = 0; }
+    __shared__ int32_t tot_g, tot_g2, tot_s, tot_p, tot_c, base_g, base_g2, base_s, base_p, base_c;
+    if (threadIdx.x == 0) { base_g = 0; base_g2 = 0; base_s = 0; base_p = 0; base_c = 0; }
     __syncthreads();
     int32_t* gemv_list2 = gemv_list + (E + 1);
     int4* pair_list = mtile_list + max_mtiles;
@@ -106,6 +114,7 @@ __device__ void plan_groups(const int32_t* offsets, const PlanArgs& a) {
         const int32_t pg2 = scan_1024(to_gemv2 ? 1 : 0, sh, &tot_g2);
         const int32_t ps = scan_1024(st, sh, &tot_s);
         const int32_t pp = scan_1024(pt, sh, &tot_p);
+        (void)scan_1024(st > 0 ? max(st * 100, a.split_rho) : 0, sh, &tot_c);
         if (to_gemv) gemv_list[base_g + pg] = g;
         if (to_gemv2) gemv_list2[base_g2 + pg2] = g;
         for (int32_t i = 0; i < st; ++i) {
@@ -117,7 +126,9 @@ __device__ void plan_groups(const int32_t* offsets, const PlanArgs& a) {
             if (slot < max_mtiles) pair_list[slot] = make_int4(g, row0, rows, i);
         }
         __syncthreads();
-        if (threadIdx.x == 0) { base_g += tot_g; base_g2 += tot_g2; base_s += tot_s; base_p += tot_p; }
+        if (threadIdx.x == 0) {
+            base_g += tot_g; base_g2 += tot_g2; base_s += tot_s; base_p += tot_p; base_c += tot_c;
+        }
         __syncthreads();
     }
     if (threadIdx.x == 0) {
@@ -125,6 +136,23 @@ __device__ void plan_groups(const int32_t* offsets, const PlanArgs& a) {
         hdr->n_gemv2 = base_g2;
         hdr->n_mtiles = min(base_s, max_mtiles);
         hdr->n_ptiles = min(base_p, max_mtiles);
+        const int sms = a.sms;
+        int up = sms / 2, us = sms;
+        if (a.split_rho > 0) {
+            const int64_t cp = 200ll * base_p, cs = base_c;
+            if (cp == 0) {
+                up = 0;
+            } else if (cs == 0) {
+                us = 0;
+            } else {
+                int ss = (int)(((int64_t)sms * cs + (cp + cs) / 2) / (cp + cs));
+                ss = max(2, min(sms - 2, ss));
+                up = (sms - ss) / 2;
+                us = sms - 2 * up;
+            }
+        }
+        hdr->units_pair = up;
+        hdr->units_single = us;
     }
 }
 
@@ -215,6 +243,8 @@ PlanArgs plan_args(const FfnGroups& g, int dtype, FfnPlanHeader* hdr, int32_t* g
     a.pair_min = allow_pair ? tc_pair_min_rows() : 0x7fffffff;
     a.pair_m = tc_tile_rows(true);
     a.max_mtiles = max_mtiles;
+    a.sms = device_sm_count();
+    a.split_rho = allow_pair ? tc_split_rho() : 0;
     a.hdr = hdr;
     a.gemv_list = gemv_list;
     a.mtile_list = mtile_list;

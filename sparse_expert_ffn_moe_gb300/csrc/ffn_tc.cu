@@ -145,6 +145,9 @@ __device__ __forceinline__ uint32_t abytes_for(int rows) {
 // took ~2.5x the MMA time per stage) -- so the default is 0 (off); the path
 // stays selectable and parity-tested.
 constexpr int kGatherMaxRows = 0;
+// Weight-streaming cost of a single-tile group, in hundredths of an MMA step
+// per weight K step (the plan's SM split between the two tile shapes).
+constexpr int kSplitRho = 150;
 
 struct TcParams {
     CUtensorMap a[2][kABoxes];  // activations: [0] routed rows, [1] shared / dense rows
@@ -162,6 +165,7 @@ struct TcParams {
     CUtensorMap g64[2];         // half pair tiles, gate/up: gate rows, box 64 rows
     CUtensorMap u64[2];         // half pair tiles, gate/up: up rows, box 64 rows
     int half_tiles;             // pair tiles of <= 128 rows run as M = 128 (64 rows per CTA)
+    int split;                  // take only the first hdr->units_pair / units_single units
     const int32_t* row_src;     // token of each routed row (gather from x), or null
     int gather_max;             // gather a CTA's routed rows when it has at most this many
     const FfnPlanHeader* hdr;
@@ -347,7 +351,7 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = PAIR ? ptx::cluster_ctarank() : 0u;  // 0 issues the MMAs
     const int unit = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
-    const int n_units = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+    const int n_units_grid = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
     pdl_trigger();
 
     if (threadIdx.x == 0) {
@@ -412,7 +416,11 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
     const int list_len = p.dense_rows > 0
         ? (p.dense_rows + S::kTileRows - 1) / S::kTileRows
         : min(PAIR ? p.hdr->n_ptiles : p.hdr->n_mtiles, p.max_mtiles);
-    const int n_tiles = list_len * p.NB;
+    // Side by side with the other tile shape, this grid keeps the plan's share
+    // of the SMs; its other units take no tile and leave through the teardown.
+    const int n_units = p.split ? min(n_units_grid, PAIR ? p.hdr->units_pair : p.hdr->units_single)
+                                : n_units_grid;
+    const int n_tiles = unit < n_units ? list_len * p.NB : 0;
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer (warp 0)
@@ -1061,8 +1069,10 @@ static_assert(kSmemBytes<true> <= 232448 && kSmemBytes<false> <= 232448,
               "shared memory exceeds the per-CTA limit");
 static_assert(kSmemBytesW8 <= 232448, "W8 shared memory exceeds the per-CTA limit");
 
+// allow_pdl = false: the grid starts only when the previous kernel of the
+// stream has finished (so units that take no tile do not hold SMs meanwhile).
 template <int EPI, bool PAIR, bool W8 = false, bool A8 = false>
-cudaError_t launch_tc(const TcParams& p, cudaStream_t st) {
+cudaError_t launch_tc(const TcParams& p, cudaStream_t st, bool allow_pdl = true) {
     constexpr size_t smem = W8 ? kSmemBytesW8 : kSmemBytes<PAIR>;
     cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<EPI, PAIR, W8, A8>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -1086,15 +1096,17 @@ cudaError_t launch_tc(const TcParams& p, cudaStream_t st) {
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
         attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[1].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+        attr[1].val.programmaticStreamSerializationAllowed = allow_pdl && pdl_enabled() ? 1 : 0;
         cfg.attrs = attr;
         cfg.numAttrs = 2;
         e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel<EPI, PAIR, W8, A8>, p);
         if (e != cudaSuccess) return e;
-    } else {
+    } else if (allow_pdl) {
         e = launch_pdl(tc_gemm_kernel<EPI, PAIR, W8, A8>, dim3(units), dim3(W8 ? kThreadsW8 : kThreadsTc),
                        smem, st, p);
         if (e != cudaSuccess) return e;
+    } else {
+        tc_gemm_kernel<EPI, PAIR, W8, A8><<<units, W8 ? kThreadsW8 : kThreadsTc, smem, st>>>(p);
     }
     return cudaGetLastError();
 }
@@ -1126,6 +1138,47 @@ int half_tiles() {
     return (s && s[0] == '0') ? 0 : 1;
 }
 
+// A second stream and its fork/join events, one set per host thread and
+// device, made on first use (not while the caller's stream is being captured:
+// that call runs the two tile shapes one after the other instead).  Kept for
+// the thread's lifetime, like a library handle.
+struct SideStream {
+    cudaStream_t s = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+
+SideStream* side_stream(cudaStream_t st) {
+    constexpr int kMaxDevices = 64;
+    static thread_local SideStream cache[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    SideStream& c = cache[dev];
+    if (c.s && c.fork && c.join) return &c;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    if (!c.s && cudaStreamCreateWithFlags(&c.s, cudaStreamNonBlocking) != cudaSuccess) c.s = nullptr;
+    if (!c.fork && cudaEventCreateWithFlags(&c.fork, cudaEventDisableTiming) != cudaSuccess) c.fork = nullptr;
+    if (!c.join && cudaEventCreateWithFlags(&c.join, cudaEventDisableTiming) != cudaSuccess) c.join = nullptr;
+    if (c.s && c.fork && c.join) return &c;
+    cudaGetLastError();
+    return nullptr;
+}
+
+// Fork the side stream off st (it waits for everything enqueued on st so far);
+// join() makes st wait for everything enqueued on the side stream.
+cudaError_t fork_side(SideStream* side, cudaStream_t st) {
+    cudaError_t e = cudaEventRecord(side->fork, st);
+    return e != cudaSuccess ? e : cudaStreamWaitEvent(side->s, side->fork, 0);
+}
+
+cudaError_t join_side(SideStream* side, cudaStream_t st) {
+    cudaError_t e = cudaEventRecord(side->join, side->s);
+    return e != cudaSuccess ? e : cudaStreamWaitEvent(st, side->join, 0);
+}
+
 // Groups with at least this many rows take 256-row pair tiles.
 // MOE_PAIR_MIN_ROWS > 0 sets a fixed threshold; unset or 0 lets the plan pick
 // the cheaper tile shape per group (padding over measured efficiency).
@@ -1133,6 +1186,18 @@ int tc_pair_min_rows() {
     const char* s = getenv("MOE_PAIR_MIN_ROWS");
     const int x = s ? atoi(s) : 0;
     return x < 0 ? 0 : x;
+}
+
+// Pair-tile and single-tile GEMMs of one call run side by side on two streams,
+// with the SMs split by the plan; the value is the plan's weight-streaming cost
+// of a single-tile group in hundredths of an MMA step (MOE_SPLIT_RHO, read per
+// call).  MOE_CONCURRENT=0 runs them one after the other on the caller's stream.
+int tc_split_rho() {
+    const char* c = getenv("MOE_CONCURRENT");
+    if (c && c[0] == '0') return 0;
+    const char* s = getenv("MOE_SPLIT_RHO");
+    const int r = s ? atoi(s) : kSplitRho;
+    return r < 1 ? 1 : r;
 }
 
 // Some group with at most max_rows rows could take pair tiles.
@@ -1195,15 +1260,24 @@ cudaError_t launch_ffn_tc(const FfnGroups& g, const FfnPlanHeader* hdr, const in
     p.err = err;
     p.timeout_ns = timeout_ns();
     p.test_stall = test_stall();
-    cudaError_t e = cudaSuccess;
+    // pair tiles on st, single tiles on the side stream, each on its share of the SMs
+    SideStream* side = may_pair && tc_split_rho() > 0 ? side_stream(st) : nullptr;
+    cudaStream_t st2 = side ? side->s : st;
+    p.split = side ? 1 : 0;
+    cudaError_t e = side ? fork_side(side, st) : cudaSuccess;
+    if (e != cudaSuccess) return e;
     if (may_pair) {
         p.mtiles = pair_list;
         e = launch_tc<EPI_SWIGLU, true>(p, st);
-        if (e != cudaSuccess) return e;
     }
-    p.mtiles = single_list;
-    e = launch_tc<EPI_SWIGLU, false>(p, st);
-    if (e != cudaSuccess) return e;
+    if (e == cudaSuccess) {
+        p.mtiles = single_list;
+        e = launch_tc<EPI_SWIGLU, false>(p, st2);
+    }
+    if (e != cudaSuccess) {
+        if (side) join_side(side, st);
+        return e;
+    }
 
     // ---- down: y = h W_down^T
     TcParams q{};
@@ -1218,7 +1292,10 @@ cudaError_t launch_ffn_tc(const FfnGroups& g, const FfnPlanHeader* hdr, const in
         q.b0[1] = q.b0[0]; q.bw[1] = q.bw[0];
     }
     q.b1[0] = q.b0[0]; q.b1[1] = q.b0[1];
-    if (!ok) return cudaErrorInvalidValue;
+    if (!ok) {
+        if (side) join_side(side, st);
+        return cudaErrorInvalidValue;
+    }
     q.half_tiles = half_tiles();
     q.hdr = hdr;
     q.E = g.E;
@@ -1233,13 +1310,20 @@ cudaError_t launch_ffn_tc(const FfnGroups& g, const FfnPlanHeader* hdr, const in
     q.err = err;
     q.timeout_ns = timeout_ns();
     q.test_stall = test_stall();
+    q.split = p.split;
     if (may_pair) {
         q.mtiles = pair_list;
-        e = launch_tc<EPI_STORE_BF16, true>(q, st);
-        if (e != cudaSuccess) return e;
+        e = launch_tc<EPI_STORE_BF16, true>(q, st, side == nullptr);
     }
-    q.mtiles = single_list;
-    return launch_tc<EPI_STORE_BF16, false>(q, st);
+    if (e == cudaSuccess) {
+        q.mtiles = single_list;
+        e = launch_tc<EPI_STORE_BF16, false>(q, st2, side == nullptr);
+    }
+    if (side) {
+        const cudaError_t j = join_side(side, st);
+        if (e == cudaSuccess) e = j;
+    }
+    return e;
 }
 
 // The expert FFN with E4M3 weights: the same two GEMMs on single-SM tiles

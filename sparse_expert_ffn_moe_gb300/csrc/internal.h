@@ -20,6 +20,12 @@ struct FfnPlanHeader {
     int32_t n_mtiles;  // 128-row tiles of the single-SM tensor-core GEMM
     int32_t n_ptiles;  // 256-row tiles of the CTA-pair tensor-core GEMM
     int32_t n_gemv2;   // second GEMV list (groups above the small-row split), or 0
+    // SM split when the pair-tile and single-tile GEMMs run side by side on two
+    // streams: CTA pairs of the pair-tile grid and CTAs of the single-tile grid
+    // that take tiles (the rest of each grid exits at once)
+    int32_t units_pair;
+    int32_t units_single;
+    int32_t pad_[2];
 };
 
 // One routed/shared expert group as the FFN kernels see it.
@@ -120,6 +126,7 @@ cudaError_t launch_dispatch_plan_small(const moe_shape& s, const int32_t* topk_i
 bool tc_available();
 int tc_tile_rows(bool pair);  // rows per tensor-core m-tile (single-SM or CTA pair)
 int tc_pair_min_rows();       // fixed pair threshold (0: the plan picks the cheaper shape)
+int tc_split_rho();          // > 0: the two tile shapes run side by side (plan's SM split cost)
 bool tc_pair_possible(int64_t max_rows);  // a group of at most max_rows rows may take pair tiles
 int tc_gather_max_rows();     // per-CTA routed row blocks up to this size are gathered from x
 // may_pair: some group can reach tc_pair_min_rows() rows (else the pair

@@ -145,3 +145,65 @@ def test_half_pair_tiles_match_full_pair_tiles(moe, counts, d, I, monkeypatch):
             assert rel_l2(y[r], ref[r]) <= 2 * BF16_REL_L2, r
         out[half] = y
     assert rel_l2(out["1"], out["0"]) <= 1e-3
+
+
+# groups the plan sends to CTA-pair tiles next to groups it sends to single-SM tiles
+MIXED = [([1100, 0, 257, 640, 1, 128, 0, 900], 512, 256),
+         ([300, 2, 130, 60, 700], 1024, 384)]
+
+
+@pytest.mark.parametrize("counts,d,I", MIXED)
+def test_side_by_side_tile_shapes_change_no_bit(moe, counts, d, I, monkeypatch):
+    """The pair-tile and single-tile GEMMs of one call run on two streams at
+    once, each grid on the plan's share of the SMs (shares pushed to both
+    extremes through MOE_SPLIT_RHO), or one after the other on the caller's
+    stream (MOE_CONCURRENT=0).  Every tile is computed the same way whichever
+    unit takes it: identical bits, and parity with the oracle."""
+    outs = []
+    for conc, rho in (("0", None), ("1", None), ("1", "1"), ("1", "1000000")):
+        monkeypatch.setenv("MOE_CONCURRENT", conc)
+        if rho is None:
+            monkeypatch.delenv("MOE_SPLIT_RHO", raising=False)
+        else:
+            monkeypatch.setenv("MOE_SPLIT_RHO", rho)
+        y, ref = _run(moe, counts, d, I, "bf16", limit=0, seed=11)
+        outs.append(y)
+    assert rel_l2(outs[0], ref) <= BF16_REL_L2
+    for r in range(ref.shape[0]):
+        assert rel_l2(outs[0][r], ref[r]) <= 2 * BF16_REL_L2, r
+    for y in outs[1:]:
+        assert np.array_equal(y, outs[0])
+
+
+def test_side_by_side_tile_shapes_in_a_cuda_graph(moe):
+    """The fork onto the second stream and the join back are captured into a
+    CUDA graph with the kernels; the replay gives the eager call's bits."""
+    counts, d, I = MIXED[0]
+    E = len(counts)
+    offsets = _counts_to_offsets(counts)
+    rows = int(offsets[-1])
+    cfg = mi.LayerConfig("ffn_graph", T=rows, d=d, E=E, K=1, I=I, seed=3)
+    p = mi.make_weights(cfg, "cuda", only={"w_gate", "w_up", "w_down"})
+    x_perm = mi.normal((rows, d), 1.0, "bf16", "cuda", 3, "x_perm")
+    s = moe.make_shape(rows, d, E, 1, I, 0, "bf16")
+    ws = moe.alloc_workspace(s)
+    off_d = torch.from_numpy(offsets).cuda()
+    y1 = torch.zeros((rows, d), dtype=torch.bfloat16, device="cuda")
+    y2 = torch.zeros_like(y1)
+    st = torch.cuda.Stream()
+    with gemv_limit(0):
+        with torch.cuda.stream(st):
+            moe.moe_expert_ffn(s, x_perm, off_d, p["w_gate"], p["w_up"], p["w_down"], y1, ws,
+                               stream=st)
+        st.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=st):
+            moe.moe_expert_ffn(s, x_perm, off_d, p["w_gate"], p["w_up"], p["w_down"], y2, ws,
+                               stream=st)
+        g.replay()
+        torch.cuda.synchronize()
+    assert moe.moe_get_device_error(ws) == 0
+    assert torch.equal(y1, y2)
+    ref = oracle.expert_ffn(host(x_perm), offsets, host(p["w_gate"]), host(p["w_up"]),
+                            host(p["w_down"]), dtype="bf16")
+    assert rel_l2(to_f64(y1), ref) <= BF16_REL_L2
