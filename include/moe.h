@@ -37,8 +37,9 @@
  *    one call's tensor-core stage has both 256-row (CTA-pair) and 128-row
  *    tiles, the 128-row grids run on a second stream of the library's own,
  *    forked from `stream` with an event and joined back before the call's
- *    next kernel (so the call stays ordered on `stream` and graph capturable);
- *    MOE_CONCURRENT=0 keeps everything on `stream`.
+ *    next kernel (so the call stays ordered on `stream` and graph capturable).
+ *    MOE_CONCURRENT=0 keeps everything on `stream`; the 8-bit entry points
+ *    use the second stream only with MOE_CONCURRENT=1.
  *  - Errors: argument errors return a non-zero moe_status immediately and
  *    enqueue nothing.  A failed launch returns MOE_ERR_CUDA.  Errors found
  *    on the device (index out of range, a bounded wait that ran out) are

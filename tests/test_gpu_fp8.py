@@ -94,6 +94,24 @@ def test_expert_ffn_fp8_matches_oracle(moe, counts, d, I, w8_pair, monkeypatch):
         assert rel_l2(y[r], ref[r]) <= 2 * BF16_REL_L2, r
 
 
+@pytest.mark.parametrize("rho", [None, "1", "1000000"])
+def test_expert_ffn_fp8_side_by_side_changes_no_bit(moe, rho, monkeypatch):
+    """Groups on CTA-pair tiles and groups on single-SM tiles: the two tile
+    shapes run on two streams at once, on the plan's split of the SMs (pushed
+    to both extremes through MOE_SPLIT_RHO), with the same bits as one after
+    the other (MOE_CONCURRENT=0)."""
+    counts, d, I = [600, 257, 1, 129, 300, 140], 384, 640
+    monkeypatch.setenv("MOE_W8_PAIR", "1")
+    monkeypatch.setenv("MOE_CONCURRENT", "0")
+    y0, ref = _expert_ffn_case(moe, counts, d, I, seed=4)
+    monkeypatch.setenv("MOE_CONCURRENT", "1")
+    if rho is not None:
+        monkeypatch.setenv("MOE_SPLIT_RHO", rho)
+    y1, _ = _expert_ffn_case(moe, counts, d, I, seed=4)
+    assert np.array_equal(y0, y1)
+    assert rel_l2(y0, ref) <= BF16_REL_L2
+
+
 # ---------------------------------------------------------------- the layer
 
 def _clean_x(L: Layer):

@@ -66,6 +66,23 @@ def test_expert_ffn_w8a8_matches_oracle(moe, counts, d, I, pair_rows):
     _check_rows(y, ref)
 
 
+@pytest.mark.parametrize("rho", [None, "1", "1000000"])
+def test_expert_ffn_w8a8_side_by_side_changes_no_bit(moe, rho, monkeypatch):
+    """Groups on CTA-pair tiles and groups on single-SM tiles: both GEMMs run
+    their two tile shapes on two streams at once, on the plan's split of the
+    SMs (pushed to both extremes through MOE_SPLIT_RHO), with the same bits as
+    one after the other (MOE_CONCURRENT=0)."""
+    counts, d, I = [600, 257, 1, 129, 300, 140], 384, 640
+    monkeypatch.setenv("MOE_CONCURRENT", "0")
+    y0, ref = _expert_ffn_case(moe, counts, d, I, seed=4)
+    monkeypatch.setenv("MOE_CONCURRENT", "1")
+    if rho is not None:
+        monkeypatch.setenv("MOE_SPLIT_RHO", rho)
+    y1, _ = _expert_ffn_case(moe, counts, d, I, seed=4)
+    assert np.array_equal(y0, y1)
+    _check_rows(y0, ref)
+
+
 # ---------------------------------------------------------------- the layer
 
 @pytest.mark.parametrize("router", ["softmax", "sigmoid"])
