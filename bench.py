@@ -511,6 +511,10 @@ def stage_roofline(cfg, stage, peaks) -> dict:
         out = {"bound": "tensor", "achieved": tflops, "peak": t_peak,
                "unit": "TFLOP/s", "frac": t_frac, "peak_kind": t_kind}
         common["other_frac"] = {"hbm": h_frac}
+        # the same against the measured back-to-back (power-capped) GEMM rate,
+        # the ceiling that applies when the timed loop runs under sw_power_cap
+        sus = peaks["bf16_tflops_sustained"] * (2.0 if cfg.acts == "e4m3" else 1.0)
+        common["frac_of_sustained_peak"] = {"peak": sus, "frac": tflops / sus}
     else:
         out = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                "frac": h_frac, "peak_kind": f"HBM copy, {peaks['source']}"}
