@@ -57,6 +57,26 @@ def test_forward_all_tokens(moe, name):
     _check(cfg, y, ref["y"])
 
 
+@pytest.mark.parametrize("d,I", [(16384, 128), (128, 16384)])
+@pytest.mark.parametrize("kind", ["f32", "bf16", "fp8", "w8a8"])
+def test_forward_at_the_widest_rows(moe, d, I, kind):
+    """d and I (and Is) at their limit, 16384: the widest rows every kernel
+    stages -- the fp32 GEMV's shared-memory rows, the 8-bit GEMV's fit check
+    (rows this wide go to the tcgen05 path), the per-row activation quantiser
+    holding a whole row in registers, the in-place h quantiser -- with a
+    160-row shared group on CTA-pair tiles next to routed groups on single
+    tiles.  All tokens against the oracle."""
+    cfg = mi.LayerConfig(f"wide_{kind}", T=160, d=d, E=4, K=2, I=I, Is=I,
+                         dtype="f32" if kind == "f32" else "bf16",
+                         weights="e4m3" if kind in ("fp8", "w8a8") else "act",
+                         acts="e4m3" if kind == "w8a8" else "act", seed=21)
+    L = Layer(cfg)
+    L.x = _clean_x(L)
+    y = to_f64(L.forward(moe))
+    ref = L.oracle_tokens(np.arange(cfg.T))
+    _check(cfg, y, ref["y"])
+
+
 @pytest.mark.parametrize("name", ["mixtral_prefill", "dsv3_prefill_zipf", "dsv3_sweep_T512",
                                   "dsv3_sweep_T4096"])
 def test_forward_sampled_tokens(moe, name):
