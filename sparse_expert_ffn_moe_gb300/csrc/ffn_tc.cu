@@ -78,16 +78,27 @@ constexpr uint32_t kABytes = BMC * BK * 2;  // 16 KB
 constexpr int kThreadsTc = 192;
 constexpr uint32_t kTmemCols = 512;
 
-template <bool PAIR> struct Shape {
+// Small-row ring (SMA, single-SM bf16 or W8A8 tiles whose groups all have at most kSmaRows
+// rows, e.g. every group of a decode batch of <= 32 tokens): an activation
+// stage holds 32 rows (4 KB) instead of 128, so the ring carries 6 weight
+// stages instead of 4 -- 50 % more weight bytes in flight per SM for the
+// weight-streaming GEMMs of small batches.  The MMA still reads 128 activation
+// rows; rows past the 32 loaded ones are whatever lies beyond the stage (never
+// stored, like the unloaded rows of a short box in the full-size ring).
+constexpr int kSmaRows = 32;
+
+template <bool PAIR, bool SMA = false> struct Shape {
     static constexpr int kTileRows = PAIR ? 256 : 128;  // rows per tile
     static constexpr int kBRows = PAIR ? 128 : 256;     // weight rows per CTA per K step
-    static constexpr int kStages = PAIR ? 7 : 4;
+    static constexpr int kStages = SMA ? 6 : (PAIR ? 7 : 4);
     static constexpr int kBand = PAIR ? 4 : 8;          // m-tiles per band (1024 rows)
+    static constexpr uint32_t kAStride = SMA ? kSmaRows * BK * 2 : kABytes;  // bytes per A stage
     static constexpr uint32_t kBBytes = kBRows * BK * 2;
-    static constexpr uint32_t kStageBytes = kABytes + kBBytes;
-    // 4 x 48 KB (single) or 7 x 32 KB (pair)
+    static constexpr uint32_t kStageBytes = kAStride + kBBytes;
+    // 4 x 48 KB (single), 7 x 32 KB (pair) or 6 x 36 KB (single, small rows)
     static constexpr uint32_t kRingBytes = kStages * kStageBytes;
     static_assert(kStages <= kMaxStages, "stage barriers");
+    static_assert(kAStride % 1024 == 0, "128-byte-swizzle atoms need 1 KB aligned stages");
 };
 
 enum Epi { EPI_SWIGLU = 0, EPI_STORE_BF16 = 1, EPI_STORE_F32 = 2 };
@@ -328,13 +339,15 @@ __device__ __forceinline__ void ld_scale16(const float* src, float (&s)[16]) {
     }
 }
 
-template <int EPI, bool PAIR, bool W8 = false, bool A8 = false>
+template <int EPI, bool PAIR, bool W8 = false, bool A8 = false, bool SMA = false>
 __global__ void __launch_bounds__(W8 ? kThreadsW8 : kThreadsTc, 1)
 tc_gemm_kernel(const __grid_constant__ TcParams p) {
     static_assert(!(W8 && EPI == EPI_STORE_F32), "8-bit weights feed the expert GEMMs only");
+    static_assert(!(SMA && (PAIR || W8)), "small-row ring: single-SM tiles without the W8 rings");
     static_assert(!(A8 && (W8 || EPI == EPI_STORE_F32)), "A8: 8-bit operands, expert GEMMs only");
-    using S = Shape<PAIR>;
+    using S = Shape<PAIR, SMA>;
     using W = W8Shape<PAIR>;
+    constexpr uint32_t kAStride = S::kAStride;  // bytes per activation stage (W8: kABytes)
     // A8: both operands E4M3 (kind::f8f6f4); a 128-byte K block holds 128 values
     constexpr int kKStep = A8 ? 2 * BK : BK;
     constexpr int kEpiWarps = 4;  // warps 2..5
@@ -344,7 +357,7 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
     // 1024-byte alignment for the 128-byte-swizzle atoms (the same offset in both CTAs of a pair)
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t* sA = smem;
-    uint8_t* sB = smem + kAStages * kABytes;
+    uint8_t* sB = smem + kAStages * kAStride;
     uint8_t* sRaw = sB + kStages * S::kBBytes;  // W8 only
     SmemCtl* ctl = (SmemCtl*)(smem + (W8 ? kW8RingBytes : S::kRingBytes));
 
@@ -528,7 +541,15 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
                 const Tile tl = decode_tile<EPI, PAIR, kKStep>(p, list_len, t);
                 if (!tl.valid) continue;
                 const int crows = tl.half ? BMC / 2 : BMC;  // activation rows per CTA
-                const int rows_me = max(0, min(crows, tl.rows - (int)rank * crows));
+                int rows_me = max(0, min(crows, tl.rows - (int)rank * crows));
+                if constexpr (SMA) {
+                    // the host sends only groups of <= kSmaRows rows here; anything
+                    // longer is reported, and no copy spills past its 4 KB stage
+                    if (rows_me > kSmaRows) {
+                        if (lane == 0) record_error(p.err, MOE_ERR_BOUNDS, 60);
+                        rows_me = kSmaRows;
+                    }
+                }
                 const CUtensorMap* ma = &p.a[tl.kind][abox_for(rows_me)];
                 const int arow = tl.row0 + (int)rank * crows;
                 const bool gather = tl.kind == 0 && p.row_src != nullptr && rows_me <= p.gather_max;
@@ -581,7 +602,7 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
                         for (int kb = 0; kb < tl.kblocks; ++kb) {
                             if (!wait_bounded(&ctl->empty[stage], phase ^ 1u, ctl, p, 100)) { ok = false; break; }
                             const int k0 = kb * kKStep;
-                            uint8_t* a_dst = sA + stage * kABytes;
+                            uint8_t* a_dst = sA + stage * kAStride;
                             uint8_t* b_dst = sB + stage * S::kBBytes;
                             if constexpr (PAIR) {
                                 const uint32_t fb = full0 + (uint32_t)(stage * sizeof(uint64_t));
@@ -609,7 +630,7 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
                         const int okw = lane == 0 ? (int)wait_bounded(&ctl->empty[stage], phase ^ 1u, ctl, p, 100) : 0;
                         if (!__shfl_sync(0xffffffffu, okw, 0)) { ok = false; break; }
                         const int k0 = kb * kKStep;
-                        uint8_t* a_dst = sA + stage * kABytes;
+                        uint8_t* a_dst = sA + stage * kAStride;
                         uint8_t* b_dst = sB + stage * S::kBBytes;
                         if constexpr (PAIR) {
                             const uint32_t fb = full0 + (uint32_t)(stage * sizeof(uint64_t));
@@ -688,7 +709,7 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
                     if (!wait_bounded(&ctl->full[stage], phase, ctl, p, 201)) { ok = false; break; }
                     if (W8 && !wait_bounded(&ctl->afull[ast], aphase, ctl, p, 202)) { ok = false; break; }
                     ptx::tc_fence_after();
-                    const uint32_t a_base = ptx::smem_u32(sA + (W8 ? ast : stage) * kABytes);
+                    const uint32_t a_base = ptx::smem_u32(sA + (W8 ? ast : stage) * kAStride);
                     const uint32_t b_base = ptx::smem_u32(sB + stage * S::kBBytes);
 #pragma unroll
                     // four MMAs per 128-byte K block: K = 16 bf16 or 32 E4M3 values each
@@ -1063,18 +1084,19 @@ int test_stall() {
     return (s && atoi(s) != 0) ? 1 : 0;
 }
 
-template <bool PAIR> constexpr size_t kSmemBytes = 1024 + Shape<PAIR>::kRingBytes + sizeof(SmemCtl) + 64;
+template <bool PAIR, bool SMA = false>
+constexpr size_t kSmemBytes = 1024 + Shape<PAIR, SMA>::kRingBytes + sizeof(SmemCtl) + 64;
 constexpr size_t kSmemBytesW8 = 1024 + kW8RingBytes + sizeof(SmemCtl) + 64;
-static_assert(kSmemBytes<true> <= 232448 && kSmemBytes<false> <= 232448,
+static_assert(kSmemBytes<true> <= 232448 && kSmemBytes<false> <= 232448 && kSmemBytes<false, true> <= 232448,
               "shared memory exceeds the per-CTA limit");
 static_assert(kSmemBytesW8 <= 232448, "W8 shared memory exceeds the per-CTA limit");
 
 // allow_pdl = false: the grid starts only when the previous kernel of the
 // stream has finished (so units that take no tile do not hold SMs meanwhile).
-template <int EPI, bool PAIR, bool W8 = false, bool A8 = false>
+template <int EPI, bool PAIR, bool W8 = false, bool A8 = false, bool SMA = false>
 cudaError_t launch_tc(const TcParams& p, cudaStream_t st, bool allow_pdl = true) {
-    constexpr size_t smem = W8 ? kSmemBytesW8 : kSmemBytes<PAIR>;
-    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<EPI, PAIR, W8, A8>,
+    constexpr size_t smem = W8 ? kSmemBytesW8 : kSmemBytes<PAIR, SMA>;
+    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<EPI, PAIR, W8, A8, SMA>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int sms = device_sm_count();
@@ -1099,14 +1121,14 @@ cudaError_t launch_tc(const TcParams& p, cudaStream_t st, bool allow_pdl = true)
         attr[1].val.programmaticStreamSerializationAllowed = allow_pdl && pdl_enabled() ? 1 : 0;
         cfg.attrs = attr;
         cfg.numAttrs = 2;
-        e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel<EPI, PAIR, W8, A8>, p);
+        e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel<EPI, PAIR, W8, A8, SMA>, p);
         if (e != cudaSuccess) return e;
     } else if (allow_pdl) {
-        e = launch_pdl(tc_gemm_kernel<EPI, PAIR, W8, A8>, dim3(units), dim3(W8 ? kThreadsW8 : kThreadsTc),
-                       smem, st, p);
+        e = launch_pdl(tc_gemm_kernel<EPI, PAIR, W8, A8, SMA>, dim3(units),
+                       dim3(W8 ? kThreadsW8 : kThreadsTc), smem, st, p);
         if (e != cudaSuccess) return e;
     } else {
-        tc_gemm_kernel<EPI, PAIR, W8, A8><<<units, W8 ? kThreadsW8 : kThreadsTc, smem, st>>>(p);
+        tc_gemm_kernel<EPI, PAIR, W8, A8, SMA><<<units, W8 ? kThreadsW8 : kThreadsTc, smem, st>>>(p);
     }
     return cudaGetLastError();
 }
@@ -1136,6 +1158,13 @@ int tc_gather_max_rows() {
 int half_tiles() {
     const char* s = getenv("MOE_HALF_TILES");
     return (s && s[0] == '0') ? 0 : 1;
+}
+
+// Groups of at most 32 rows take the small-row ring (MOE_SMALL_RING=0, read
+// per call, keeps the full-size one).
+bool small_ring() {
+    const char* s = getenv("MOE_SMALL_RING");
+    return !(s && s[0] == '0');
 }
 
 // A second stream and its fork/join events, one set per host thread and
@@ -1215,10 +1244,12 @@ struct TwoShapes {
     ~TwoShapes() { finish(cudaSuccess); }
 };
 
-// One GEMM over both tile lists; pdl as launch_tc's allow_pdl.
+// One GEMM over both tile lists; pdl as launch_tc's allow_pdl; small_rows:
+// every group has at most kSmaRows rows (single tiles then take the small-row
+// ring; not with W8's rings).
 template <int EPI, bool W8 = false, bool A8 = false>
 cudaError_t launch_shapes(TcParams& p, const int4* pair_list, const int4* single_list, bool may_pair,
-                          const TwoShapes& sh, bool pdl) {
+                          const TwoShapes& sh, bool pdl, bool small_rows = false) {
     p.split = sh.split();
     cudaError_t e = cudaSuccess;
     if (may_pair) {
@@ -1227,6 +1258,9 @@ cudaError_t launch_shapes(TcParams& p, const int4* pair_list, const int4* single
     }
     if (e == cudaSuccess) {
         p.mtiles = single_list;
+        if constexpr (!W8) {
+            if (small_rows && small_ring()) return launch_tc<EPI, false, false, A8, true>(p, sh.st2, pdl);
+        }
         e = launch_tc<EPI, false, W8, A8>(p, sh.st2, pdl);
     }
     return e;
@@ -1316,7 +1350,8 @@ cudaError_t launch_ffn_tc(const FfnGroups& g, const FfnPlanHeader* hdr, const in
     // pair tiles on st, single tiles on the side stream, each on its share of
     // the SMs; the down GEMMs follow on the same streams, joined at the end
     TwoShapes sh(may_pair, st, false);
-    cudaError_t e = launch_shapes<EPI_SWIGLU>(p, pair_list, single_list, may_pair, sh, true);
+    const bool small = g.max_group_rows > 0 && g.max_group_rows <= kSmaRows;
+    cudaError_t e = launch_shapes<EPI_SWIGLU>(p, pair_list, single_list, may_pair, sh, true, small);
     if (e != cudaSuccess) return sh.finish(e);
 
     // ---- down: y = h W_down^T
@@ -1348,7 +1383,7 @@ cudaError_t launch_ffn_tc(const FfnGroups& g, const FfnPlanHeader* hdr, const in
     q.timeout_ns = timeout_ns();
     q.test_stall = test_stall();
     // side by side, the down grids start only when their stream's gate/up grid ended
-    e = launch_shapes<EPI_STORE_BF16>(q, pair_list, single_list, may_pair, sh, sh.side == nullptr);
+    e = launch_shapes<EPI_STORE_BF16>(q, pair_list, single_list, may_pair, sh, sh.side == nullptr, small);
     return sh.finish(e);
 }
 
@@ -1500,8 +1535,9 @@ cudaError_t launch_ffn_tc_a8_gate_up(const FfnGroups& g, const FfnPlanHeader* hd
     p.timeout_ns = timeout_ns();
     p.test_stall = test_stall();
     TwoShapes sh(may_pair, st, true);
+    const bool small = g.max_group_rows > 0 && g.max_group_rows <= kSmaRows;
     return sh.finish(launch_shapes<EPI_SWIGLU, false, true>(p, mtile_list + max_mtiles, mtile_list,
-                                                            may_pair, sh, true));
+                                                            may_pair, sh, true, small));
 }
 
 cudaError_t launch_ffn_tc_a8_down(const FfnGroups& g, const FfnPlanHeader* hdr,
@@ -1548,8 +1584,9 @@ cudaError_t launch_ffn_tc_a8_down(const FfnGroups& g, const FfnPlanHeader* hdr,
     q.timeout_ns = timeout_ns();
     q.test_stall = test_stall();
     TwoShapes sh(may_pair, st, true);
+    const bool small = g.max_group_rows > 0 && g.max_group_rows <= kSmaRows;
     return sh.finish(launch_shapes<EPI_STORE_BF16, false, true>(q, mtile_list + max_mtiles, mtile_list,
-                                                                may_pair, sh, sh.side == nullptr));
+                                                                may_pair, sh, sh.side == nullptr, small));
 }
 
 // scores[T][E] (fp32) = x w_g^T on the tensor cores (single tiles)

@@ -35,6 +35,7 @@ struct FfnGroups {
     int d;             // hidden size
     int I, Is;         // intermediate sizes (routed, shared)
     int n_routed_rows; // T*K (rows of x_perm / h / y_perm)
+    int max_group_rows; // bound on any group's rows (0: unknown); <= 32 selects the small-row ring
     int T;             // tokens (rows of the shared group)
     const int32_t* offsets;  // [E+1] device
     const int32_t* row_src;  // [n_routed_rows] token of each routed row, or

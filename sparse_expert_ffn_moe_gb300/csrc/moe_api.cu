@@ -275,6 +275,7 @@ moe_status moe_expert_ffn(const moe_shape* shape, const void* x_perm, const int3
     g.Is = 0;
     g.n_routed_rows = (int)rows;
     g.T = s.T;
+    g.max_group_rows = (int)rows;
     g.offsets = offsets;
     g.row_src = nullptr;
     g.a_routed = x_perm;
@@ -370,6 +371,7 @@ moe_status moe_forward(const moe_shape* shape, const void* x, const void* w_g, c
     g.Is = s.inter_shared;
     g.n_routed_rows = s.T * s.K;
     g.T = s.T;
+    g.max_group_rows = s.T;  // a token picks an expert once; the shared group has T rows
     g.offsets = offsets;
     g.row_src = tok;
     g.a_routed = x;
@@ -642,6 +644,7 @@ moe_status moe_expert_ffn_w8a8(const moe_shape* shape, const void* x_perm, const
     g.Is = 0;
     g.n_routed_rows = (int)R;
     g.T = s.T;
+    g.max_group_rows = (int)R;
     g.offsets = offsets;
     g.row_src = nullptr;
     g.a_routed = xq;
@@ -716,6 +719,7 @@ moe_status moe_forward_w8a8(const moe_shape* shape, const void* x, const void* w
     g.Is = s.inter_shared;
     g.n_routed_rows = (int)R;
     g.T = s.T;
+    g.max_group_rows = s.T;  // a token picks an expert once; the shared group has T rows
     g.offsets = offsets;
     g.row_src = nullptr;
     g.a_routed = xq_perm;

@@ -207,3 +207,17 @@ def test_side_by_side_tile_shapes_in_a_cuda_graph(moe):
     ref = oracle.expert_ffn(host(x_perm), offsets, host(p["w_gate"]), host(p["w_up"]),
                             host(p["w_down"]), dtype="bf16")
     assert rel_l2(to_f64(y1), ref) <= BF16_REL_L2
+
+
+@pytest.mark.parametrize("counts", [[1, 0, 7, 32, 3], [32, 0], [5, 0, 0, 1]])
+def test_small_row_ring_expert_stage(moe, counts, monkeypatch):
+    """moe_expert_ffn with at most 32 rows in all takes the small-row ring for
+    its single-SM tiles: oracle parity and the full-size ring's bits."""
+    monkeypatch.setenv("MOE_SMALL_RING", "0")
+    y0, ref = _run(moe, counts, 7168 if len(counts) == 4 else 512, 256, "bf16", limit=0, seed=13)
+    monkeypatch.setenv("MOE_SMALL_RING", "1")
+    y1, _ = _run(moe, counts, 7168 if len(counts) == 4 else 512, 256, "bf16", limit=0, seed=13)
+    assert np.array_equal(y0, y1)
+    assert rel_l2(y1, ref) <= BF16_REL_L2
+    for r in range(ref.shape[0]):
+        assert rel_l2(y1[r], ref[r]) <= 2 * BF16_REL_L2, r

@@ -269,3 +269,22 @@ def test_fused_small_dispatch_at_its_limits(moe, monkeypatch):
     ok = boundary_margin(want["logits"], cfg.K) >= MARGIN
     got = to_f64(out[torch.from_numpy(toks[ok]).long().cuda()])
     assert rel_l2(got, want["y"][ok]) <= BF16_REL_L2
+
+
+@pytest.mark.parametrize("T", [1, 8, 32, 33])
+def test_small_row_ring_changes_no_bit(moe, T, monkeypatch):
+    """Batches of at most 32 tokens run their single-SM tiles on the small-row
+    ring (6 weight stages of 4 KB activations + 32 KB weights instead of 4 of
+    16 + 32 KB); MOE_SMALL_RING=0 keeps the full-size ring.  Same bits, and
+    parity with the oracle (T = 33 is past the bound and takes the full ring
+    either way)."""
+    cfg = mi.LayerConfig(f"small_ring_T{T}", T=T, d=1024, E=64, K=8, I=256, Is=256, seed=31)
+    L = Layer(cfg)
+    L.x = _clean_x(L)
+    monkeypatch.setenv("MOE_SMALL_RING", "0")
+    y0 = L.forward(moe)
+    monkeypatch.setenv("MOE_SMALL_RING", "1")
+    y1 = L.forward(moe)
+    assert torch.equal(y0, y1)
+    ref = oracle.forward(host(L.x), L.hp, cfg.K, dtype=cfg.dtype, bias=L.bias_host())
+    _check(cfg, to_f64(y1), ref["y"])

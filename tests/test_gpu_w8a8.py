@@ -207,3 +207,22 @@ def test_expert_ffn_w8a8_half_pair_tiles_match_full_pair_tiles(moe, monkeypatch)
         _check_rows(y, ref)
         out[half] = y
     assert rel_l2(out["1"], out["0"]) <= 1e-3
+
+
+@pytest.mark.parametrize("T", [1, 8, 32])
+def test_forward_w8a8_small_row_ring_changes_no_bit(moe, T, monkeypatch):
+    """Batches of at most 32 tokens run their single-SM kind::f8f6f4 tiles on
+    the small-row ring (6 stages of 4 KB activation codes + 32 KB weight
+    codes); MOE_SMALL_RING=0 keeps the full-size ring: same bits, and parity
+    with the oracle."""
+    cfg = mi.LayerConfig(f"w8a8_small_ring_T{T}", T=T, d=1024, E=64, K=8, I=256, Is=256,
+                         weights="e4m3", acts="e4m3", seed=33)
+    L = Layer(cfg)
+    L.x = _clean_x(L)
+    monkeypatch.setenv("MOE_SMALL_RING", "0")
+    y0 = L.forward(moe)
+    monkeypatch.setenv("MOE_SMALL_RING", "1")
+    y1 = L.forward(moe)
+    assert torch.equal(y0, y1)
+    ref = L.oracle_tokens(np.arange(cfg.T))
+    _check_rows(to_f64(y1), ref["y"])
