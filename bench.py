@@ -462,8 +462,8 @@ def time_expert_ffn(moe, cfg, x, p, bias, stream, steps: int, n_active: int) -> 
 # ncu capture per workload (profiles/ffn_stage_traffic_<workload>.md), valid only for
 # the ffn_tc.cu source it was taken on (sha256 prefix).
 STAGE_TRAFFIC = {
-    "mixtral_prefill": {"bytes": 4922273792, "ffn_tc_sha256": "1fc46f9fb70cd1ba"},
-    "mixtral_prefill_w8a8": {"bytes": 2298236416, "ffn_tc_sha256": "1fc46f9fb70cd1ba"},
+    "mixtral_prefill": {"bytes": 4630342400, "ffn_tc_sha256": "0fb4e005abf25f74"},
+    "mixtral_prefill_w8a8": {"bytes": 2283144960, "ffn_tc_sha256": "0fb4e005abf25f74"},
 }
 
 
