@@ -100,6 +100,9 @@ for _t in (64, 512):
 # for multi-pass counter captures, still far larger than L2
 CONFIGS["dsv3_decode_fp8_E32"] = replace(CONFIGS["dsv3_decode_fp8"], name="dsv3_decode_fp8_E32",
                                          E=32)
+# the bf16 decode layer with a pool of 32 experts (2.8 GB of expert weights,
+# still larger than L2): small enough for counter captures of the decode GEMMs
+CONFIGS["dsv3_decode_E32"] = replace(CONFIGS["dsv3_decode"], name="dsv3_decode_E32", E=32)
 # 8-bit weights and 8-bit activations (W8A8): the same weights; the library
 # quantises x and h itself, so no extra tensor is drawn
 CONFIGS["mixtral_prefill_w8a8"] = replace(CONFIGS["mixtral_prefill_fp8"],
