@@ -160,13 +160,24 @@ __device__ __forceinline__ void stage_f16(__half* act, float* rs, const bf16* ro
     }
 }
 
+__device__ __forceinline__ void prefetch_l2(const void* a) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
+}
+
 // c[nt] += weight rows (p0: MMA rows 0-7 via the lane's group g, p1: rows
-// 8-15) of n codes times staged token rows 8 nt .. 8 nt + 7
+// 8-15) of n codes times staged token rows 8 nt .. 8 nt + 7.  pf: while a
+// step's kG8U blocks are in flight, the four lanes of each row ask L2 for the
+// row's next kG8U blocks (512 bytes, one 128-byte line per lane), so the next
+// step's loads find them in L2 -- twice the weight bytes in flight per SM
+// without holding more registers.
 template <int NTILE, int R>
 __device__ __forceinline__ void mma_rows(const uint8_t* p0, const uint8_t* p1, int n,
-                                         const __half* act, int lane, float (&c)[NTILE][4]) {
+                                         const __half* act, int lane, float (&c)[NTILE][4],
+                                         int pf) {
     const int g = lane >> 2, t = lane & 3;
     const int nkb = n / 64;
+    const uint8_t* const row0 = p0;
+    const uint8_t* const row1 = p1;
     const uint2* arow[NTILE];
 #pragma unroll
     for (int j = 0; j < NTILE; ++j)  // (rows past R are never read)
@@ -174,6 +185,13 @@ __device__ __forceinline__ void mma_rows(const uint8_t* p0, const uint8_t* p1, i
     p0 += 16 * t;
     p1 += 16 * t;
     for (int kb0 = 0; kb0 < nkb; kb0 += kG8U) {
+        if (pf) {
+            const int off = (kb0 + pf * kG8U) * 64 + 128 * t;  // inside the row: off < n
+            if (off < n) {
+                prefetch_l2(row0 + off);
+                prefetch_l2(row1 + off);
+            }
+        }
         uint4 w0[kG8U], w1[kG8U];
 #pragma unroll
         for (int u = 0; u < kG8U; ++u) {
@@ -219,7 +237,8 @@ __device__ __forceinline__ void gate_up_task(const FfnGroups& g, const Group8& v
     float c[NTILE][4];
 #pragma unroll
     for (int j = 0; j < NTILE; ++j) c[j][0] = c[j][1] = c[j][2] = c[j][3] = 0.0f;
-    mma_rows<NTILE, R>(v.wg + (int64_t)i * g.d, v.wu + (int64_t)i * g.d, g.d, act, lane, c);
+    mma_rows<NTILE, R>(v.wg + (int64_t)i * g.d, v.wu + (int64_t)i * g.d, g.d, act, lane, c,
+                       g.g8_prefetch);
     const float sg = v.sg[i], su = v.su[i];
 #pragma unroll
     for (int j = 0; j < NTILE; ++j)
@@ -245,7 +264,7 @@ __device__ __forceinline__ void down_task(const FfnGroups& g, const Group8& v, i
 #pragma unroll
     for (int j = 0; j < NTILE; ++j) c[j][0] = c[j][1] = c[j][2] = c[j][3] = 0.0f;
     mma_rows<NTILE, R>(v.wd + (int64_t)jr * v.inter, v.wd + (int64_t)(jr + 8) * v.inter, v.inter,
-                       act, lane, c);
+                       act, lane, c, g.g8_prefetch);
     const float s0 = v.sd[jr], s1 = v.sd[jr + 8];
 #pragma unroll
     for (int j = 0; j < NTILE; ++j)
@@ -389,8 +408,13 @@ int gemv8_small_rows() { return kG8Small; }
 // Second list (9..limit rows): 16 rows per pass where they fit in
 // kG8FastSmem, else passes of 8.  Both lists' gate/up kernels run before the
 // down kernels that read their h.
-cudaError_t launch_ffn_gemv_fp8(const FfnGroups& g, const FfnPlanHeader* hdr, const int32_t* list,
+cudaError_t launch_ffn_gemv_fp8(const FfnGroups& g0, const FfnPlanHeader* hdr, const int32_t* list,
                                 int limit, cudaStream_t st) {
+    FfnGroups g = g0;
+    // read per call: how many steps ahead the L2 prefetch runs (0: off)
+    const char* pfe = getenv("MOE_G8_PREFETCH");
+    g.g8_prefetch = pfe ? atoi(pfe) : 1;
+    if (g.g8_prefetch < 0 || g.g8_prefetch > 4) g.g8_prefetch = 1;
     const int max_inter = g.has_shared && g.Is > g.I ? g.Is : g.I;
     const int32_t* list2 = list + (g.E + 1);
     const bool second = limit > kG8Small;

@@ -36,6 +36,7 @@ struct FfnGroups {
     int I, Is;         // intermediate sizes (routed, shared)
     int n_routed_rows; // T*K (rows of x_perm / h / y_perm)
     int max_group_rows; // bound on any group's rows (0: unknown); <= 32 selects the small-row ring
+    int g8_prefetch;    // 8-bit GEMV: prefetch each warp's next weight blocks into L2
     int T;             // tokens (rows of the shared group)
     const int32_t* offsets;  // [E+1] device
     const int32_t* row_src;  // [n_routed_rows] token of each routed row, or
