@@ -112,6 +112,10 @@ for _t in (512, 4096):
                                                 name=f"dsv3_sweep_w8a8_T{_t}", T=_t, acts="e4m3")
 CONFIGS["dsv3_decode_w8a8"] = replace(CONFIGS["dsv3_decode_fp8"], name="dsv3_decode_w8a8",
                                       acts="e4m3")
+# the T=4096 W8A8 per-expert shape (~128 rows per expert) over a pool of 64
+# experts (2.8 GB of codes): small enough for counter captures
+CONFIGS["dsv3_sweep_w8a8_T1024_E64"] = replace(CONFIGS["dsv3_sweep_w8a8_T4096"],
+                                               name="dsv3_sweep_w8a8_T1024_E64", T=1024, E=64)
 CONFIGS["dsv3_prefill_zipf_w8a8"] = replace(CONFIGS["dsv3_prefill_zipf"],
                                             name="dsv3_prefill_zipf_w8a8", weights="e4m3",
                                             acts="e4m3")

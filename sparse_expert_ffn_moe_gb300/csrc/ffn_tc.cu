@@ -330,13 +330,49 @@ __device__ __forceinline__ void convert_rows_w8(const uint8_t* raw, uint8_t* dst
     }
 }
 
-// 16 consecutive row scales (64-byte aligned), the same for every lane
-__device__ __forceinline__ void ld_scale16(const float* src, float (&s)[16]) {
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const float4 v = __ldg(reinterpret_cast<const float4*>(src) + k);
-        s[4 * k] = v.x; s[4 * k + 1] = v.y; s[4 * k + 2] = v.z; s[4 * k + 3] = v.w;
+// 8-bit weights: the weight-row scales one epilogue warp needs for a tile,
+// 8 per lane, requested before the warp waits for the tile's accumulator so the
+// loads overlap the K loop (a short K loop -- 16 steps for a 2048-long 8-bit
+// reduction -- would otherwise wait on one global load per 16 columns).  Lane l
+// holds the scales of columns col0 + 8 l' .. + 7 of one vector: SWIGLU, gate
+// scales in the first lanes and up scales in the next (16 + 16 lanes for a full
+// tile's 128 h columns, 8 + 8 for a half tile's 64); STORE, the 256 (or 128)
+// output columns.  Columns past n_out read as 0 (never stored).
+template <int EPI>
+__device__ __forceinline__ void load_tile_scales(const TcParams& p, const Tile& tl, int hi, int lane,
+                                                 int nvalid, float (&s)[8]) {
+    const float* src = nullptr;
+    int col = 0;  // first output (h or y) column of this lane's scales, relative to n0
+    bool active;
+    if (EPI == EPI_SWIGLU) {
+        const int nl = (tl.half ? 64 : BN / 2) / 8;  // lanes per vector
+        const bool up = lane >= nl;
+        const int l = up ? lane - nl : lane;
+        active = lane < 2 * nl;
+        col = (tl.half ? 64 * hi : 0) + 8 * l;
+        src = (up ? p.sc1[tl.kind] : p.sc0[tl.kind]) + tl.wrow0 + col;
+    } else {
+        active = 8 * lane < (tl.half ? BN / 2 : BN);
+        col = (tl.half ? (BN / 2) * hi : 0) + 8 * lane;
+        src = p.sc0[tl.kind] + tl.wrow0 + col;
     }
+    if (active && tl.n0 + col < nvalid) {  // n_out is a multiple of 8: all 8 valid or none
+        const float4 a = __ldg(reinterpret_cast<const float4*>(src));
+        const float4 b = __ldg(reinterpret_cast<const float4*>(src) + 1);
+        s[0] = a.x; s[1] = a.y; s[2] = a.z; s[3] = a.w;
+        s[4] = b.x; s[5] = b.y; s[6] = b.z; s[7] = b.w;
+    } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) s[k] = 0.0f;
+    }
+}
+
+// 16 consecutive scales of load_tile_scales' layout, starting at vector lane
+// `lane0` (the first of the 16 columns is a multiple of 8): every lane of the
+// warp must call it.
+__device__ __forceinline__ void tile_scales16(const float (&s)[8], int lane0, float (&out)[16]) {
+#pragma unroll
+    for (int k = 0; k < 16; ++k) out[k] = __shfl_sync(0xffffffffu, s[k & 7], lane0 + (k >> 3));
 }
 
 template <int EPI, bool PAIR, bool W8 = false, bool A8 = false, bool SMA = false>
@@ -760,24 +796,28 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
         for (int t = unit; t < n_tiles; t += n_units) {
             const Tile tl = decode_tile<EPI, PAIR, kKStep>(p, list_len, t);
             if (!tl.valid) continue;
-            // one lane waits, the warp follows its verdict (tcgen05.ld needs the whole warp)
-            const int ok = lane == 0 ? (int)wait_bounded(&ctl->tfull[acc], acc_phase, ctl, p, 300) : 0;
-            if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-            ptx::tc_fence_after();
-            const uint32_t tbase = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * BN);
             // Half pair tiles (M = 128) leave each CTA 64 rows: tensor-memory lane L
             // holds row L & 63; lanes 0-63 hold output columns 0-127 of the n-block
             // and lanes 64-127 columns 128-255, in tensor-memory columns 0-127.
             const int crows = tl.half ? BMC / 2 : BMC;
-            const int hi = tl.half ? (r >> 6) : 0;
+            const int hi = tl.half ? (r >> 6) : 0;  // the same for the whole warp
             const int rr = tl.half ? (r & 63) : r;
             const int rows_me = max(0, min(crows, tl.rows - (int)rank * crows));
             const bool row_ok = rr < rows_me;
             const int arow_me = tl.row0 + (int)rank * crows + rr;  // activation row of this thread
             const int64_t orow = arow_me;
             const int nvalid = p.n_out[tl.kind];
-            // A8: the activation row's scale factors out of every output of the row
+            // scales are requested before the accumulator wait, so they arrive during
+            // the K loop: A8, the activation row's scale (it factors out of every
+            // output of the row); 8-bit weights, the tile's weight-row scales
             const float sa = (A8 && row_ok) ? __ldg(p.sa[tl.kind] + arow_me) : 1.0f;
+            float sreg[8];
+            if constexpr (W8 || A8) load_tile_scales<EPI>(p, tl, hi, lane, nvalid, sreg);
+            // one lane waits, the warp follows its verdict (tcgen05.ld needs the whole warp)
+            const int ok = lane == 0 ? (int)wait_bounded(&ctl->tfull[acc], acc_phase, ctl, p, 300) : 0;
+            if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+            ptx::tc_fence_after();
+            const uint32_t tbase = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * BN);
             if (EPI == EPI_SWIGLU && tl.half) {
                 // tensor-memory columns 0-63: gate sums, 64-127: up sums of the same 64
                 // intermediate indices (n0 + 64 hi ..) of this thread's row
@@ -791,11 +831,9 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
                     const int hc = 64 * hi + c;  // first h column, relative to n0
                     const bool col_ok = tl.n0 + hc < nvalid;
                     float gs[16], us[16];
-                    if constexpr (W8 || A8) {
-                        if (col_ok) {
-                            ld_scale16(p.sc0[tl.kind] + tl.wrow0 + hc, gs);
-                            ld_scale16(p.sc1[tl.kind] + tl.wrow0 + hc, us);
-                        }
+                    if constexpr (W8 || A8) {  // gate scales in lanes 0-7, up in 8-15
+                        tile_scales16(sreg, c >> 3, gs);
+                        tile_scales16(sreg, 8 + (c >> 3), us);
                     }
                     ptx::tmem_ld_wait();
                     if (row_ok && col_ok) {
@@ -838,13 +876,10 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
                     ptx::tmem_ld16(tbase + c, g);
                     ptx::tmem_ld16(tbase + BN / 2 + c, u);
                     const bool col_ok = tl.n0 + c < nvalid;
-                    // the scale loads overlap the tensor-memory loads
                     float gs[16], us[16];
-                    if constexpr (W8 || A8) {
-                        if (col_ok) {
-                            ld_scale16(p.sc0[tl.kind] + tl.wrow0 + c, gs);
-                            ld_scale16(p.sc1[tl.kind] + tl.wrow0 + c, us);
-                        }
+                    if constexpr (W8 || A8) {  // gate scales in lanes 0-15, up in 16-31
+                        tile_scales16(sreg, c >> 3, gs);
+                        tile_scales16(sreg, 16 + (c >> 3), us);
                     }
                     ptx::tmem_ld_wait();
                     if (row_ok && col_ok) {
@@ -890,9 +925,7 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
                     const int c = tc + (BN / 2) * hi;  // output column, relative to n0
                     const bool col_ok = tl.n0 + c < nvalid;
                     float ds[16];
-                    if constexpr (W8 || A8) {
-                        if (col_ok) ld_scale16(p.sc0[tl.kind] + tl.wrow0 + c, ds);
-                    }
+                    if constexpr (W8 || A8) tile_scales16(sreg, tc >> 3, ds);
                     ptx::tmem_ld_wait();
                     if (row_ok && col_ok) {
                         if constexpr (W8 || A8) {
