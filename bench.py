@@ -462,8 +462,8 @@ def time_expert_ffn(moe, cfg, x, p, bias, stream, steps: int, n_active: int) -> 
 # ncu capture per workload (profiles/ffn_stage_traffic_<workload>.md), valid only for
 # the ffn_tc.cu source it was taken on (sha256 prefix).
 STAGE_TRAFFIC = {
-    "mixtral_prefill": {"bytes": 4581865984, "ffn_tc_sha256": "36bf38ec5c336267"},
-    "mixtral_prefill_w8a8": {"bytes": 2285430016, "ffn_tc_sha256": "36bf38ec5c336267"},
+    "mixtral_prefill": {"bytes": 4581865984, "ffn_tc_sha256": "68710359d65ad885"},
+    "mixtral_prefill_w8a8": {"bytes": 2285430016, "ffn_tc_sha256": "68710359d65ad885"},
 }
 
 

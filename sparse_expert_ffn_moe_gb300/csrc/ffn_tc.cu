@@ -333,10 +333,10 @@ __device__ __forceinline__ void convert_rows_w8(const uint8_t* raw, uint8_t* dst
 // 8-bit weights: the weight-row scales one epilogue warp needs for a tile,
 // 8 per lane, requested before the warp waits for the tile's accumulator so the
 // loads overlap the K loop (a short K loop -- 16 steps for a 2048-long 8-bit
-// reduction -- would otherwise wait on one global load per 16 columns).  Lane l
-// holds the scales of columns col0 + 8 l' .. + 7 of one vector: SWIGLU, gate
-// scales in the first lanes and up scales in the next (16 + 16 lanes for a full
-// tile's 128 h columns, 8 + 8 for a half tile's 64); STORE, the 256 (or 128)
+// reduction -- would otherwise wait on one global load per 16 columns).  Each
+// lane holds 8 consecutive scales: SWIGLU, lanes 0..n-1 the gate scales and
+// lanes n..2n-1 the up scales (n = 16 for a full tile's 128 h columns, 8 for a
+// half tile's 64); STORE, lanes 0..31 (or 0..15) the tile's 256 (or 128)
 // output columns.  Columns past n_out read as 0 (never stored).
 template <int EPI>
 __device__ __forceinline__ void load_tile_scales(const TcParams& p, const Tile& tl, int hi, int lane,
