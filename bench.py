@@ -459,8 +459,8 @@ def time_expert_ffn(moe, cfg, x, p, bias, stream, steps: int, n_active: int) -> 
 
 
 # DRAM bytes (read + write) of one expert-FFN stage (its tcgen05 launches), from one
-# ncu capture per workload (profiles/ffn_stage_traffic_<workload>.md), valid only for
-# the ffn_tc.cu source it was taken on (sha256 prefix).
+# ncu capture per workload, valid only for the ffn_tc.cu source it was taken on
+# (sha256 prefix).
 STAGE_TRAFFIC = {
     "mixtral_prefill": {"bytes": 4581865984, "ffn_tc_sha256": "68710359d65ad885"},
     "mixtral_prefill_w8a8": {"bytes": 2285430016, "ffn_tc_sha256": "68710359d65ad885"},

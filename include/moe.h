@@ -156,12 +156,15 @@ moe_status moe_permute(const moe_shape *shape, const int32_t *topk_idx,
  * array inside the library, which every GPU that loads the library holds
  * until the process exits.  Shapes whose scratch would exceed it -- about
  * (T*K + T*K/1024*E) * 4 bytes, doubled for T*K when inv_perm is NULL -- are
- * refused with MOE_ERR_UNSUPPORTED.  Nothing is allocated: no cudaMalloc,
- * cudaFree or allocating library call.  The first call on a device looks up
- * the array's device address (once per device, with that device current);
- * make that first call before any stream capture.  All calls share the
- * array, and calls whose work overlaps on the GPU race on it.  Device-side
- * errors are not reported: a dropped slot (expert id outside [0, E)) shows as
+ * refused with MOE_ERR_UNSUPPORTED; other shapes are checked exactly as
+ * moe_permute checks them.  Nothing is allocated: no cudaMalloc, cudaFree or
+ * allocating library call.  The first call on a device looks up the array's
+ * device address (with that device current) and later calls in the same CUDA
+ * context reuse it; make that first call before any stream capture.  A
+ * context torn down and made again (cudaDeviceReset) counts as a new one: its
+ * first call looks the address up again.  All calls share the array, and
+ * calls whose work overlaps on the GPU race on it.  Device-side errors are
+ * not reported: a dropped slot (expert id outside [0, E)) shows as
  * offsets[E] < T*K and inv_perm[f] == -1.
  */
 moe_status moe_permute_noalloc(const moe_shape *shape, const int32_t *topk_idx,
@@ -318,8 +321,9 @@ moe_status moe_forward_w8a8(const moe_shape *shape, const void *x, const void *w
 /*
  * Reads the device error word of `workspace` (a device pointer passed to a
  * previous call) into *code_out (a HOST pointer): MOE_OK, MOE_ERR_TIMEOUT or
- * MOE_ERR_BOUNDS.  Synchronous (a 4-byte device-to-host copy); call it after
- * the stream that ran the work has been synchronised.
+ * MOE_ERR_BOUNDS.  Synchronous (one 16-byte device-to-host copy of the error
+ * record: code, where, padding); call it after the stream that ran the work
+ * has been synchronised.
  */
 moe_status moe_get_device_error(const void *workspace, int32_t *code_out);
 

@@ -288,6 +288,13 @@ def sample_tokens(T: int, n: int, seed: int, name: str = "sample") -> torch.Tens
     return torch.sort(torch.randperm(T, generator=g)[:n]).values.to(torch.int32)
 
 
+def token_order(T: int, seed: int, name: str = "sample_order") -> torch.Tensor:
+    """A seeded permutation of the token ids [0, T) (int64, CPU): the order in
+    which a sampler that skips some tokens considers them."""
+    g = _gen("cpu", seed, name)
+    return torch.randperm(T, generator=g)
+
+
 def to_host_array(t: torch.Tensor):
     """Host numpy view of a tensor for the oracle: bf16 -> uint16 bit patterns,
     fp32 -> float32, anything else as is."""

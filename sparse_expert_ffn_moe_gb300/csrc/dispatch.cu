@@ -252,14 +252,21 @@ cudaError_t launch_gather_codes(const moe_shape& s, const uint8_t* xq, const flo
 // The array (kNoAllocScratchBytes, 4 MiB) is held by every GPU that loads the
 // library until the process exits.  In host code its name is a host-side
 // stand-in, not a device address: the address the kernels get comes from
-// cudaGetSymbolAddress, looked up once per device, with that device current,
-// on the first call made on that device (make that first call before any
-// stream capture).  Every call shares the array and it keeps the last call's
-// contents, so the error word is cleared at the start of every call; calls
-// whose work overlaps on the GPU (other streams, other threads) race on it.
+// cudaGetSymbolAddress, called with the device current.  The first call made
+// on a device (in a given CUDA context) does that lookup and keeps the result
+// for later calls in the same context, so make that first call before any
+// stream capture.  The result is keyed on the context's unique id: after a
+// cudaDeviceReset, or any other teardown and re-creation of the context, the
+// module is loaded again, the array may sit elsewhere, and the next call
+// looks it up again instead of handing the kernels a stale address.  Every
+// call shares the array and it keeps the last call's contents, so the error
+// word is cleared at the start of every call; calls whose work overlaps on the
+// GPU (other streams, other threads) race on it.
 // ---------------------------------------------------------------------------
 static constexpr size_t kNoAllocScratchBytes = (size_t)4 << 20;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+#include <cuda.h>
 
 #include <mutex>
 
@@ -267,23 +274,66 @@ namespace moe {
 namespace {
 
 constexpr int kNoAllocMaxDevices = 64;
+struct NoAllocEntry {
+    unsigned long long ctx_id = 0;  // unique id of the context the address belongs to (0: none)
+    void* addr = nullptr;
+};
 std::mutex g_noalloc_mu;
-void* g_noalloc_addr[kNoAllocMaxDevices] = {};
+NoAllocEntry g_noalloc[kNoAllocMaxDevices];
 
-// Device address of g_noalloc_scratch on the current device (looked up once per device).
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// the driver's cuCtxGetCurrent / cuCtxGetId, found through the runtime (no -lcuda)
+template <typename F>
+F driver_fn(const char* name) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+        return nullptr;
+    return reinterpret_cast<F>(f);
+}
+
+// Unique id of the calling thread's current context (0 when none is current or
+// the driver cannot say).
+unsigned long long current_ctx_id() {
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        get_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+        get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+    if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+
+// Device address of g_noalloc_scratch in the current device's current context.
 cudaError_t noalloc_scratch(void** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kNoAllocMaxDevices) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (g_noalloc_addr[dev] == nullptr) {
-        void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess) return e;
-        g_noalloc_addr[dev] = p;
+    NoAllocEntry& c = g_noalloc[dev];
+    unsigned long long id = current_ctx_id();
+    if (id != 0 && id == c.ctx_id && c.addr != nullptr) {
+        *out = c.addr;
+        return cudaSuccess;
     }
-    *out = g_noalloc_addr[dev];
+    // first call in this context (the lookup also makes the runtime's context
+    // current when no runtime call on this thread has done so yet)
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    if (id == 0) id = current_ctx_id();
+    c.ctx_id = id;  // 0 (unknown context) is never matched: the next call looks up again
+    c.addr = p;
+    *out = p;
     return cudaSuccess;
 }
 
@@ -297,13 +347,10 @@ extern "C" moe_status moe_permute_noalloc(const moe_shape* shape, const int32_t*
                                           int32_t* perm, int32_t* inv_perm, void* x_perm,
                                           void* stream) {
     using namespace moe;
-    if (!shape) return MOE_ERR_INVALID_ARG;
+    // the shapes moe_permute accepts, no more
+    const moe_status st = check_shape(shape);
+    if (st != MOE_OK) return st;
     const moe_shape& s = *shape;
-    if (s.T < 0 || s.d <= 0 || s.E <= 0 || s.K <= 0 || s.K > s.E ||
-        (s.dtype != MOE_F32 && s.dtype != MOE_BF16))
-        return MOE_ERR_INVALID_ARG;
-    if (s.K > 32 || s.E > 1024 || s.d % 64 || s.d > 16384 || (int64_t)s.T * s.K >= ((int64_t)1 << 31))
-        return MOE_ERR_UNSUPPORTED;
     if (!counts || !offsets || (s.T > 0 && !topk_idx)) return MOE_ERR_INVALID_ARG;
     if (((uintptr_t)x & 15u) || ((uintptr_t)x_perm & 15u)) return MOE_ERR_INVALID_ARG;
     // scratch carving: error word | per-chunk histogram | token of each row | inverse permutation

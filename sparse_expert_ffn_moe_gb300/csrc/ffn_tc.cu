@@ -20,9 +20,12 @@
 //                          CTA's 128 accumulator rows in its own tensor memory.
 // A pair tile needs 32 KB per SM per K step instead of 48 KB, so the ring
 // hides ~1.5x more memory latency and large groups run faster; but it pads
-// ragged groups to 256 rows.  The plan kernel therefore sends groups of at
-// least MOE_PAIR_MIN_ROWS rows (default 512) to pair tiles and the rest to
-// single tiles; each GEMM is two launches (pair list, then single list).
+// ragged groups to 256 rows.  The plan kernel picks the shape per group by
+// its padded rows over each shape's measured tensor-pipe activity (or, with
+// MOE_PAIR_MIN_ROWS > 0, by a fixed row threshold) and writes one tile list
+// per shape; each GEMM is one launch per list, and when a call has both, the
+// pair-tile launch runs on the caller's stream and the single-tile launch on
+// a second stream beside it, each on the share of the SMs the plan gives it.
 //
 // Both shapes keep two 128x256 fp32 accumulators per CTA in tensor memory
 // (all 512 columns), double-buffered so the epilogue of one tile overlaps the

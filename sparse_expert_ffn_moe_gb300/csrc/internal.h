@@ -82,6 +82,11 @@ struct WsLayout {
 };
 WsLayout ws_layout(const moe_shape& s);
 
+// ---- moe_api.cu ----
+// The shape rules every entry point applies (MOE_ERR_INVALID_ARG or
+// MOE_ERR_UNSUPPORTED before anything is enqueued).
+moe_status check_shape(const moe_shape* s);
+
 // ---- router.cu ----
 int router_splits_for(const moe_shape& s);
 cudaError_t launch_router_gemv(const moe_shape& s, const void* x, const void* w_g, float* part,

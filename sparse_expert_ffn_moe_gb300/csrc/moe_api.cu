@@ -14,16 +14,7 @@
 
 namespace moe {
 
-namespace {
-
-constexpr size_t kAlign = 256;
-size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
-
-constexpr int kMaxDevices = 64;
-std::atomic<int> g_sm_count[kMaxDevices];
-
-bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
-
+// The shape rules every entry point applies before it enqueues anything.
 moe_status check_shape(const moe_shape* s) {
     if (!s) return MOE_ERR_INVALID_ARG;
     if (s->T < 0 || s->d <= 0 || s->E <= 0 || s->K <= 0 || s->inter <= 0 || s->inter_shared < 0)
@@ -37,6 +28,16 @@ moe_status check_shape(const moe_shape* s) {
     if ((int64_t)s->T * s->K >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
     return MOE_OK;
 }
+
+namespace {
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sm_count[kMaxDevices];
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 size_t esize(const moe_shape& s) { return s.dtype == MOE_BF16 ? 2 : 4; }
 

@@ -2,15 +2,17 @@
 
 Bit-exact routing: both sides get the same fp32 scores on a 1/512 grid (distinct
 values differ by >= 1.95e-3, equal values are decided only by the tie rule).
-Scores computed from x . w_g: compared within the fp32 accumulation error, and
-the selection compared on tokens whose top-K boundary gap is >= 1e-3."""
+Scores computed from x . w_g: compared within the fp32 accumulation error; the
+picks, in slot order, compared on every token whose fp64 keys leave gaps of at
+least 1e-3 among its K picks and at the top-K boundary; the weights within the
+bound the score error sets."""
 import numpy as np
 import pytest
 import torch
 
 import moe_inputs as mi
 import oracle
-from tests.gpu_util import MARGIN, W_RTOL, Layer, boundary_margin, host
+from tests.gpu_util import MARGIN, W_RTOL, Layer, host, order_margin
 
 pytestmark = pytest.mark.gpu
 
@@ -93,17 +95,15 @@ def test_route_from_x(moe, name, T):
     got = out.cpu().numpy().astype(np.float64)
     # fp32 accumulation of exact products: error well under 1e-4 of the score scale
     assert np.max(np.abs(got - ref_logits)) <= 1e-4 * max(1.0, np.max(np.abs(ref_logits)))
-    ok = boundary_margin(ref_logits, cfg.K) >= MARGIN
+    # tokens whose picks and slot order are unique at fp32 precision
+    ok = order_margin(ref_logits, cfg.K) >= MARGIN
     assert ok.mean() > 0.9
     gi = idx.cpu().numpy()
-    assert np.array_equal(np.sort(gi[ok], axis=1), np.sort(ref_idx[ok], axis=1))
-    # the selected set decides the weights; compare per expert id
+    assert np.array_equal(gi[ok], ref_idx[ok])  # slot j = the j-th pick
+    # a score error delta moves ln w_j by at most 2 max|delta| (softmax over the K)
     gw = w.cpu().numpy().astype(np.float64)
-    for t in np.nonzero(ok)[0][:200]:
-        a = dict(zip(gi[t].tolist(), gw[t].tolist()))
-        b = dict(zip(ref_idx[t].tolist(), ref_w[t].tolist()))
-        for e in b:
-            assert abs(a[e] - b[e]) <= 1e-4 * b[e] + 1e-6
+    delta = np.abs(got - ref_logits).max(axis=1, keepdims=True)
+    assert np.all(np.abs(gw[ok] - ref_w[ok]) <= (2.0 * delta[ok] + 2e-6) * ref_w[ok])
 
 
 # ---------------------------------------------------------------- sigmoid router (DeepSeek-V3)
@@ -128,14 +128,15 @@ def test_sigmoid_route_matches_oracle(moe, T, E, K, with_bias):
     """Same fp32 scores on both sides.  Without a bias the sigmoid keeps the
     order of the scores, so the selection is bit-exact including ties; with a
     bias (1/32 grid) keys of different experts can nearly coincide, so tokens
-    whose fp64 boundary gap is below 1e-5 are left out (and counted)."""
+    whose fp64 keys leave a gap below 1e-5 among the picks or at the boundary
+    are left out."""
     logits = mi.grid_logits(T, E, seed=111, scale=512)
     bias = (np.round(np.random.default_rng(5).standard_normal(E) * 8) / 32) if with_bias else None
     idx, w, keys = _route_logits_mode(moe, logits, K, "sigmoid", bias)
     ref_idx, ref_w, ref_keys = oracle.route(None, None, K, logits_in=logits.numpy(), bias=bias,
                                             router="sigmoid")
     assert np.max(np.abs(keys - ref_keys)) <= 1e-6
-    ok = boundary_margin(ref_keys, K) >= (1e-5 if with_bias else 0.0)
+    ok = order_margin(ref_keys, K) >= (1e-5 if with_bias else 0.0)
     if with_bias:
         assert ok.mean() >= 0.95
     assert np.array_equal(idx[ok], ref_idx[ok])
@@ -162,11 +163,17 @@ def test_sigmoid_route_from_x(moe, name, T):
                                             bias=None if bias is None else bias.double().cpu().numpy(),
                                             router="sigmoid")
     assert np.max(np.abs(keys.cpu().numpy() - ref_keys)) <= 1e-5
-    ok = boundary_margin(ref_keys, cfg.K) >= 1e-4
+    ok = order_margin(ref_keys, cfg.K) >= 1e-4
     assert ok.mean() > 0.9
     gi, gw = idx.cpu().numpy(), w.cpu().numpy().astype(np.float64)
-    assert np.array_equal(np.sort(gi[ok], axis=1), np.sort(ref_idx[ok], axis=1))
-    for t in np.nonzero(ok)[0][:200]:
-        a = dict(zip(gi[t].tolist(), gw[t].tolist()))
-        for e, wr in zip(ref_idx[t].tolist(), ref_w[t].tolist()):
-            assert abs(a[e] - wr) <= 1e-4 * wr + 1e-6
+    assert np.array_equal(gi[ok], ref_idx[ok])  # slot j = the j-th pick
+    # the raw scores' error bounds the weights' (d ln sigmoid(s) / ds = 1 - sigmoid(s) <= 1,
+    # so |dw| / w <= 2 max|delta|); the raw scores come from the softmax router without bias
+    s0 = moe.make_shape(cfg.T, cfg.d, cfg.E, cfg.K, cfg.I, cfg.Is, cfg.dtype, "softmax")
+    raw = torch.empty((cfg.T, cfg.E), dtype=torch.float32, device="cuda")
+    moe.moe_route(s0, L.x, L.p["w_g"], None, None, raw, idx.clone(), w.clone(),
+                  moe.alloc_workspace(s0))
+    torch.cuda.synchronize()
+    _, _, raw_ref = oracle.route(host(L.x), L.hp["w_g"], cfg.K, dtype=cfg.dtype)
+    delta = np.abs(raw.cpu().numpy() - raw_ref).max(axis=1, keepdims=True)
+    assert np.all(np.abs(gw[ok] - ref_w[ok]) <= (2.0 * delta[ok] + 2e-6) * ref_w[ok])
