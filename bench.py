@@ -5,14 +5,18 @@
 
 One step = one moe_forward (router + top-K + softmax, dispatch, routed and
 shared expert FFN, combine) over one batch of the workload's synthetic tokens,
-inputs resident in HBM.  Default workload: the Mixtral-shaped prefill layer
-(T=4096, d=4096, E=8, K=2, I=14336, bf16).  Every weight set is larger than the
-129 MB L2, so no flush is needed between steps.  Also reported: the
-DeepSeek-V3-shaped decode layer (T=8) in microseconds per call against the HBM
-roofline, the end-to-end number through the C ABI with host buffers, the
-dominant stage against its roofline, and the fp64 CPU oracle on a bounded
-sample of the same workload.  Under torchrun every rank runs an independent
-replica on its own tokens (weak scaling, no collective on the data path).
+inputs resident in HBM.  Default workload: the largest single-GPU layer, the
+DeepSeek-V3-shaped prefill chunk with Zipf load imbalance (T=16384, d=7168,
+E=256, K=8, I=2048, one shared expert, bf16).  Every weight set is larger than
+the 129 MB L2, so no flush is needed between steps.  Also reported: the
+dominant stage (the expert FFN) against its roofline, timed over at least 100
+repeats with its own clock record; the end-to-end number through the C ABI
+with host buffers; the Mixtral-shaped prefill layer; the DeepSeek-V3-shaped
+decode layer (T=8) in microseconds per call against the HBM roofline; the
+token-count sweep on the DeepSeek-V3 shape (T = 1, 8, 64, 512, 4096) with its
+HBM and tensor fractions; and the fp64 CPU oracle on a bounded sample of the
+same workload.  Under torchrun every rank runs an independent replica on its
+own tokens (weak scaling, no collective on the data path).
 
 ``--impl reference`` times the CPU oracle (the only reference this layer has)
 on the host cores for the same workload and metric.
@@ -37,8 +41,26 @@ import numpy as np  # noqa: E402
 
 import moe_inputs as mi  # noqa: E402
 
-DEFAULT_WORKLOAD = "mixtral_prefill"
+DEFAULT_WORKLOAD = "dsv3_prefill_zipf"
 DECODE_WORKLOAD = "dsv3_decode"
+MIXTRAL_WORKLOAD = "mixtral_prefill"
+SWEEP_T = "1,8,64,512,4096"
+STAGE_REPEATS = 100   # the dominant stage's timed loop (>= 1 s of clock samples at prefill sizes)
+
+
+def source_sha256() -> str:
+    """sha256 (first 16 hex digits) over the library's sources and public
+    header, in name order: the build a result or a profile was taken on."""
+    import glob
+    import hashlib
+    h = hashlib.sha256()
+    files = sorted(glob.glob(os.path.join(ROOT, "sparse_expert_ffn_moe_gb300", "csrc", "*"))) + \
+        [os.path.join(ROOT, "include", "moe.h")]
+    for f in files:
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
 
 
 # --------------------------------------------------------------------------- work accounting
@@ -175,8 +197,9 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index: int):
+    def __init__(self, index: int, interval_ms: int = 25):
         self.index = index
+        self.interval_ms = interval_ms
         self.proc = None
         self.lines: list[str] = []
         self.reader = None
@@ -185,7 +208,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "50"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.interval_ms)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.reader = threading.Thread(target=self._read, daemon=True)
             self.reader.start()
@@ -212,7 +235,7 @@ class ClockSampler:
                 self.reader.join(timeout=2)
 
     def summary(self) -> dict:
-        sm, mx, reasons = [], [], set()
+        sm, mx, pw, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in self.lines:
             parts = [p.strip() for p in ln.split(",")]
@@ -223,13 +246,21 @@ class ClockSampler:
                 mx.append(float(parts[1]))
             except ValueError:
                 continue
+            try:
+                pw.append(float(parts[2]))
+            except ValueError:
+                pass
             for n, v in zip(names, parts[4:8]):
                 if v.lower() == "active":
                     reasons.add(n)
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
-                "reasons": sorted(reasons), "samples": len(sm)}
+        out = {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+               "reasons": sorted(reasons), "samples": len(sm), "interval_ms": self.interval_ms}
+        if pw:
+            out["power_w_median"] = statistics.median(pw)
+            out["power_w_max"] = max(pw)
+        return out
 
 
 def dist_env():
@@ -333,10 +364,14 @@ def run_ours(args):
         ev1.record(stream)
         torch.cuda.synchronize()
         barrier(ws_n)
-        # dominant stage, timed alone on the same stream: the expert FFN (tcgen05
-        # gate/up GEMM with fused SiLU*mul, then the down GEMM) of this batch
-        stage = time_expert_ffn(moe, cfg, x, p, bias, stream, args.steps, n_active)
-        spread = step_stats(fwd, stream, args.steps)
+    spread = step_stats(fwd, stream, args.steps)
+    # dominant stage, timed alone on the same stream over >= STAGE_REPEATS calls, with
+    # its own clock record: the expert FFN (tcgen05 gate/up GEMM with fused SiLU*mul,
+    # then the down GEMM) of this batch
+    with ClockSampler(torch.cuda.current_device()) as stage_clk:
+        stage = time_expert_ffn(moe, cfg, x, p, bias, stream, max(STAGE_REPEATS, args.steps),
+                                n_active)
+    stage["clocks"] = stage_clk.summary()
     t_ms = ev0.elapsed_time(ev1) / args.steps
     t_ms_max = max_over_ranks(t_ms, ws_n)
     code = moe.moe_get_device_error(ws)
@@ -380,19 +415,35 @@ def run_ours(args):
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": e2e["h2d"],
                 "d2h_bytes_per_step": e2e["d2h"]},
         "gpu_launches": launches_per_forward(cfg) * args.steps,
-        # per-call spread, from a separate pass with an event between calls
+        # per-call spread, from a separate pass with an event between calls; the
+        # back-to-back timed region lets each call's first kernels start while the
+        # previous call's last ones finish (programmatic dependent launch), so
+        # ms_per_step can sit below step_ms.median
         "step_ms": spread,
         "clocks": clk.summary(),
         "peaks": peaks,
+        "source_sha256": source_sha256(),
     }
-    if not args.no_decode and rank == 0:
-        result["decode"] = bench_decode(moe, peaks, args)
-    if args.all and rank == 0:
-        result["workloads"] = bench_all(moe, peaks, args)
-    if args.sweep_T and rank == 0:
-        result["sweep"] = [bench_workload(moe, cfg.with_T(int(t)), peaks, steps=max(10, args.steps),
-                                          graph=False)
-                           for t in args.sweep_T.split(",")]
+    if rank == 0:
+        # the other workloads go last, so that they cannot disturb the lines above
+        del call, ws, y
+        torch.cuda.empty_cache()
+        if not args.no_decode:
+            result["decode"] = bench_decode(moe, peaks, args)
+        if not args.no_extra and args.workload != MIXTRAL_WORKLOAD:
+            result[MIXTRAL_WORKLOAD] = bench_workload(
+                moe, mi.CONFIGS[MIXTRAL_WORKLOAD], peaks, steps=max(20, args.steps),
+                graph=False, stage_repeats=max(STAGE_REPEATS, args.steps))
+        if args.sweep_T:
+            # the token-count sweep on the DeepSeek-V3 shape (uniform routing): the GEMV-like
+            # to GEMM crossover against the HBM and tensor roofs
+            base = mi.CONFIGS["dsv3_sweep_T8"]
+            result["sweep"] = [
+                bench_workload(moe, mi.CONFIGS.get(f"dsv3_sweep_T{t}", base.with_T(int(t))), peaks,
+                               steps=max(20, args.steps), graph=int(t) <= 64)
+                for t in args.sweep_T.split(",")]
+        if args.all:
+            result["workloads"] = bench_all(moe, peaks, args)
     if not args.no_cpu_baseline and rank == 0:
         torch.cuda.synchronize()
         hp = {k: mi.to_host_array(v) for k, v in p.items()}
@@ -455,7 +506,8 @@ def time_expert_ffn(moe, cfg, x, p, bias, stream, steps: int, n_active: int) -> 
     e1.record(stream)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
-    return {"ms": ms, "flops": 6 * n * cfg.d * cfg.I, "bytes": ffn_stage_bytes(cfg, n_active)}
+    return {"ms": ms, "flops": 6 * n * cfg.d * cfg.I, "bytes": ffn_stage_bytes(cfg, n_active),
+            "repeats": steps}
 
 
 # DRAM bytes (read + write) of one expert-FFN stage (its tcgen05 launches), from one
@@ -506,7 +558,19 @@ def stage_roofline(cfg, stage, peaks) -> dict:
               "traffic_unit": "bytes per launch pair (DRAM read + write, ncu)",
               "kernel": kernel, "per_launch_flops": stage["flops"],
               "per_launch_bytes": stage["bytes"], "ms_per_launch": stage["ms"],
-              "other_frac": None}
+              "repeats": stage.get("repeats"), "other_frac": None}
+    clk = stage.get("clocks")
+    if clk and clk.get("sm_mhz"):
+        # the clock behind the number: work per SM clock cycle of the whole GPU, and the
+        # fraction of the peak scaled to the median SM clock sampled during the loop
+        # (the measured peaks are taken as holding at the maximum SM clock)
+        mhz, mx = clk["sm_mhz"], clk["sm_max_mhz"] or clk["sm_mhz"]
+        common["clocks"] = clk
+        common["per_cycle"] = {
+            "flop_per_cycle": stage["flops"] / (sec * mhz * 1e6),
+            "bytes_per_cycle": stage["bytes"] / (sec * mhz * 1e6),
+            "tensor_frac_at_sampled_clock": t_frac * mx / mhz,
+            "hbm_frac_at_sampled_clock": h_frac * mx / mhz}
     if t_frac >= h_frac:
         out = {"bound": "tensor", "achieved": tflops, "peak": t_peak,
                "unit": "TFLOP/s", "frac": t_frac, "peak_kind": t_kind}
@@ -604,7 +668,8 @@ def bench_decode(moe, peaks, args) -> dict:
     return r
 
 
-def bench_workload(moe, cfg, peaks, steps: int, graph: bool = False) -> dict:
+def bench_workload(moe, cfg, peaks, steps: int, graph: bool = False,
+                   stage_repeats: int = 0) -> dict:
     import torch
     p = mi.make_weights(cfg, "cuda")
     x = mi.make_x(cfg, "cuda")
@@ -659,6 +724,12 @@ def bench_workload(moe, cfg, peaks, steps: int, graph: bool = False) -> dict:
     code = moe.moe_get_device_error(ws)
     if code:
         raise RuntimeError(f"device error in {cfg.name}: {moe.status_string(code)}")
+    if stage_repeats:
+        # the expert-FFN stage of this batch against its roofline, with its clock record
+        with ClockSampler(torch.cuda.current_device()) as clk:
+            stage = time_expert_ffn(moe, cfg, x, p, bias, st, stage_repeats, n_active)
+        stage["clocks"] = clk.summary()
+        out["roofline"] = stage_roofline(cfg, stage, peaks)
     del p, x, y, ws
     torch.cuda.empty_cache()
     return out
@@ -687,13 +758,18 @@ def run_reference(args):
     import torch
     cfg = mi.CONFIGS[args.workload]
     import oracle
-    p = mi.make_weights(cfg, "cpu")
-    x = mi.make_x(cfg, "cpu")
-    bias = mi.make_bias(cfg, "cpu")
+    # the seeded inputs are drawn where it is quick (22.6 GB of weights at the DeepSeek-V3
+    # shape), then copied to host memory; the timed oracle runs on the host cores only
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    p = mi.make_weights(cfg, dev)
+    x = mi.make_x(cfg, dev)
+    bias = mi.make_bias(cfg, dev)
     hp = {k: mi.to_host_array(v) for k, v in p.items()}
     xh = mi.to_host_array(x)
-    bh = None if bias is None else bias.double().numpy()
-    del p
+    bh = None if bias is None else bias.double().cpu().numpy()
+    del p, x
+    if dev == "cuda":
+        torch.cuda.empty_cache()
     threads = oracle.default_threads()
     # per-step sample sized so that warm-up + steps end within a few minutes
     per_step = max(threads, 16)
@@ -733,8 +809,11 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--all", action="store_true", help="also time every workload")
-    ap.add_argument("--sweep-T", default="", help="comma-separated token counts: time the "
-                    "workload's shapes at each T (one JSON object per T under 'sweep')")
+    ap.add_argument("--sweep-T", default=SWEEP_T, help="comma-separated token counts: time the "
+                    "DeepSeek-V3 shape at each T (one JSON object per T under 'sweep'); "
+                    "empty to skip")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the Mixtral prefill block")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3

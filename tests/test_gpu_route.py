@@ -12,7 +12,7 @@ import torch
 
 import moe_inputs as mi
 import oracle
-from tests.gpu_util import MARGIN, W_RTOL, Layer, host, order_margin
+from tests.gpu_util import MARGIN, W_RTOL, Layer, clean_rows, host, order_margin
 
 pytestmark = pytest.mark.gpu
 
@@ -82,6 +82,8 @@ def test_route_from_x(moe, name, T):
     if T is not None:
         cfg = cfg.with_T(T)
     L = Layer(cfg, only={"w_g"})
+    if cfg.T <= 256:
+        L.x = clean_rows(L)  # small batches: every token's routing made unique, all checked
     s = L.shape(moe)
     ws = moe.alloc_workspace(s)
     idx = torch.empty((cfg.T, cfg.K), dtype=torch.int32, device="cuda")
@@ -97,7 +99,7 @@ def test_route_from_x(moe, name, T):
     assert np.max(np.abs(got - ref_logits)) <= 1e-4 * max(1.0, np.max(np.abs(ref_logits)))
     # tokens whose picks and slot order are unique at fp32 precision
     ok = order_margin(ref_logits, cfg.K) >= MARGIN
-    assert ok.mean() > 0.9
+    assert ok.mean() > 0.9 and (cfg.T > 256 or ok.all())
     gi = idx.cpu().numpy()
     assert np.array_equal(gi[ok], ref_idx[ok])  # slot j = the j-th pick
     # a score error delta moves ln w_j by at most 2 max|delta| (softmax over the K)
@@ -152,6 +154,9 @@ def test_sigmoid_route_from_x(moe, name, T):
     cfg = dataclasses.replace(cfg, router="sigmoid")
     L = Layer(cfg, only={"w_g"})
     bias = None if L.bias is None else (L.bias / 8).contiguous()  # keys live in (0, 1)
+    L.bias = bias
+    if cfg.T <= 256:
+        L.x = clean_rows(L)  # small batches: every token's routing made unique, all checked
     s = L.shape(moe)
     ws = moe.alloc_workspace(s)
     idx = torch.empty((cfg.T, cfg.K), dtype=torch.int32, device="cuda")
@@ -164,7 +169,7 @@ def test_sigmoid_route_from_x(moe, name, T):
                                             router="sigmoid")
     assert np.max(np.abs(keys.cpu().numpy() - ref_keys)) <= 1e-5
     ok = order_margin(ref_keys, cfg.K) >= 1e-4
-    assert ok.mean() > 0.9
+    assert ok.mean() > 0.9 and (cfg.T > 256 or ok.all())
     gi, gw = idx.cpu().numpy(), w.cpu().numpy().astype(np.float64)
     assert np.array_equal(gi[ok], ref_idx[ok])  # slot j = the j-th pick
     # the raw scores' error bounds the weights' (d ln sigmoid(s) / ds = 1 - sigmoid(s) <= 1,
