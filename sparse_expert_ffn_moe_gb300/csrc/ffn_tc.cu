@@ -151,6 +151,22 @@ __device__ __forceinline__ uint32_t abytes_for(int rows) {
     return rows <= 0 ? 0u : (uint32_t)abox_rows(abox_for(rows)) * BK * 2;
 }
 
+// Swapped single tiles.  A single-SM tile of few rows (at most
+// MOE_SWAP_MAX_ROWS, default 64: the tail experts of a skewed routing, every
+// group of a decode batch) would spend an M = 128 MMA on each K step although
+// most of its rows are padding.  Such a tile runs with the operands swapped:
+// the stage's 256 weight rows are the A operand, as two M = 128 halves (gate
+// and up rows, or the n-block's first and second 128 output columns), and the
+// activation box (16, 32 or 64 rows) is the B operand, N = the box height, so
+// each K step costs 2 x 128 x N instead of 128 x 256 multiply-adds -- a
+// quarter or less of the tensor work and energy for groups of <= 32 rows.
+// The products land transposed in tensor memory (lane = weight row, column =
+// activation row): the first half at columns 0..N-1, the second at
+// 128..128+N-1 of the tile's accumulator.  The ring and the copies are
+// unchanged; only the MMA issue and the epilogue differ (bf16 operands, no
+// 8-bit rings or scales).
+constexpr int kSwapMaxRows = 64;
+
 // Routed rows of at most MOE_GATHER_MAX_ROWS per CTA can be gathered from x
 // with tile::gather4 inside the GEMM instead of being copied into expert order
 // first; larger row blocks load the contiguous permuted copy.  Measured on
@@ -179,6 +195,7 @@ struct TcParams {
     CUtensorMap g64[2];         // half pair tiles, gate/up: gate rows, box 64 rows
     CUtensorMap u64[2];         // half pair tiles, gate/up: up rows, box 64 rows
     int half_tiles;             // pair tiles of <= 128 rows run as M = 128 (64 rows per CTA)
+    int swap_max_rows;          // single tiles of at most this many rows (<= 64) run swapped
     int split;                  // take only the first hdr->units_pair / units_single units
     const int32_t* row_src;     // token of each routed row (gather from x), or null
     int gather_max;             // gather a CTA's routed rows when it has at most this many
@@ -207,6 +224,8 @@ struct Tile {
     int kblocks;
     bool valid;
     bool half;  // a pair tile of at most 128 rows, run with M = 128: 64 rows per CTA
+    bool swap;  // a single tile of few rows, run with the operands swapped (see kSwap below)
+    int nsw;    // swap: MMA N = the activation box height (16, 32 or 64 rows)
 };
 
 // KSTEP: elements of the reduction per K block (64 bf16 or 128 8-bit values,
@@ -241,6 +260,8 @@ __device__ __forceinline__ Tile decode_tile_entry(const TcParams& p, int4 e, int
     tl.kblocks = (p.kdim[tl.kind] + KSTEP - 1) / KSTEP;
     tl.valid = tl.n0 < p.n_out[tl.kind] && tl.rows > 0;
     tl.half = PAIR && p.half_tiles != 0 && tl.rows <= BMC;
+    tl.swap = !PAIR && EPI != EPI_STORE_F32 && tl.rows <= p.swap_max_rows;
+    tl.nsw = abox_rows(abox_for(tl.rows));
     return tl;
 }
 
@@ -392,6 +413,8 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
     constexpr int kEpiWarps = 4;  // warps 2..5
     constexpr int kStages = W8 ? W::kConv : S::kStages;  // B stages (and A stages without W8)
     constexpr int kAStages = W8 ? W::kA : S::kStages;
+    // swapped tiles (few rows): bf16 single-SM expert GEMMs only
+    constexpr bool kSwap = !PAIR && !W8 && !A8 && EPI != EPI_STORE_F32;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte alignment for the 128-byte-swizzle atoms (the same offset in both CTAs of a pair)
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -744,12 +767,32 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
                 ptx::tc_fence_after();
                 const uint32_t d_tmem = tmem + (uint32_t)(acc * BN);
                 const uint32_t id_t = tl.half ? idesc_half : idesc;
+                const bool swp = kSwap && tl.swap;
+                // swapped: M = 128, N = the box rows (within the small-row ring's 32-row stage)
+                const uint32_t id_sw = ptx::idesc_bf16_f32(BMC, SMA ? min(tl.nsw, kSmaRows) : tl.nsw);
                 for (int kb = 0; kb < tl.kblocks; ++kb) {
                     if (!wait_bounded(&ctl->full[stage], phase, ctl, p, 201)) { ok = false; break; }
                     if (W8 && !wait_bounded(&ctl->afull[ast], aphase, ctl, p, 202)) { ok = false; break; }
                     ptx::tc_fence_after();
                     const uint32_t a_base = ptx::smem_u32(sA + (W8 ? ast : stage) * kAStride);
                     const uint32_t b_base = ptx::smem_u32(sB + stage * S::kBBytes);
+                    if (kSwap && swp) {
+                        // weight halves (rows 0-127 and 128-255 of the stage) times the
+                        // activation rows: two M = 128, N = nsw products per 16-deep slice
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint64_t xd = ptx::sw128_kmajor_desc(a_base + kk * 32);
+                            const uint64_t w0 = ptx::sw128_kmajor_desc(b_base + kk * 32);
+                            const uint64_t w1 = ptx::sw128_kmajor_desc(b_base + S::kBBytes / 2 + kk * 32);
+                            const uint32_t accum = (kb | kk) != 0 ? 1u : 0u;
+                            ptx::tc_mma_f16(d_tmem, w0, xd, id_sw, accum);
+                            ptx::tc_mma_f16(d_tmem + BN / 2, w1, xd, id_sw, accum);
+                        }
+                        any = true;
+                        ptx::tc_commit(&ctl->empty[stage]);
+                        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                        continue;
+                    }
 #pragma unroll
                     // four MMAs per 128-byte K block: K = 16 bf16 or 32 E4M3 values each
                     for (int kk = 0; kk < 4; ++kk) {
@@ -821,7 +864,42 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
             if (!__shfl_sync(0xffffffffu, ok, 0)) break;
             ptx::tc_fence_after();
             const uint32_t tbase = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * BN);
-            if (EPI == EPI_SWIGLU && tl.half) {
+            if (kSwap && tl.swap) {
+                // Swapped tile: tensor-memory lane r is weight row r of the n-block --
+                // h column n0 + r (gate sums in columns t, up sums in 128 + t), or y
+                // columns n0 + r and n0 + 128 + r -- and column t is the tile's
+                // activation row t.  A warp's 32 lanes store 32 adjacent columns of a row.
+                const int col = tl.n0 + r;
+                const int64_t ld = p.ld_out[tl.kind];
+                bf16* base = (bf16*)p.out[tl.kind] + (int64_t)tl.row0 * ld;
+                const int nsw = SMA ? min(tl.nsw, kSmaRows) : tl.nsw;
+#pragma unroll 1
+                for (int t0 = 0; t0 < nsw; t0 += 16) {
+                    uint32_t a[16], b[16];
+                    ptx::tmem_ld16(tbase + t0, a);
+                    ptx::tmem_ld16(tbase + BN / 2 + t0, b);
+                    ptx::tmem_ld_wait();
+                    const int nt = min(16, tl.rows - t0);  // valid activation rows in this batch
+                    if (EPI == EPI_SWIGLU) {
+                        if (col < nvalid) {
+#pragma unroll
+                            for (int k = 0; k < 16; ++k)
+                                if (k < nt)
+                                    base[(int64_t)(t0 + k) * ld + col] = __float2bfloat16_rn(
+                                        silu_mul(__uint_as_float(a[k]), __uint_as_float(b[k])));
+                        }
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) {
+                            if (k < nt) {
+                                bf16* dst = base + (int64_t)(t0 + k) * ld + col;
+                                if (col < nvalid) dst[0] = __float2bfloat16_rn(__uint_as_float(a[k]));
+                                if (col + BN / 2 < nvalid) dst[BN / 2] = __float2bfloat16_rn(__uint_as_float(b[k]));
+                            }
+                        }
+                    }
+                }
+            } else if (EPI == EPI_SWIGLU && tl.half) {
                 // tensor-memory columns 0-63: gate sums, 64-127: up sums of the same 64
                 // intermediate indices (n0 + 64 hi ..) of this thread's row
                 bf16* out = (bf16*)p.out[tl.kind] + orow * p.ld_out[tl.kind] + tl.n0 + 64 * hi;
@@ -1196,6 +1274,14 @@ int half_tiles() {
     return (s && s[0] == '0') ? 0 : 1;
 }
 
+// Single tiles of at most this many rows run swapped (MOE_SWAP_MAX_ROWS, read
+// per call; 0 turns it off; capped at 64, the largest swapped N).
+int swap_max_rows() {
+    const char* s = getenv("MOE_SWAP_MAX_ROWS");
+    const int x = s ? atoi(s) : kSwapMaxRows;
+    return x < 0 ? 0 : (x > kSwapMaxRows ? kSwapMaxRows : x);
+}
+
 // Groups of at most 32 rows take the small-row ring (MOE_SMALL_RING=0, read
 // per call, keeps the full-size one).
 bool small_ring() {
@@ -1367,6 +1453,7 @@ cudaError_t launch_ffn_tc(const FfnGroups& g, const FfnPlanHeader* hdr, const in
         p.g64[1] = p.g64[0]; p.u64[1] = p.u64[0];
     }
     p.half_tiles = half_tiles();
+    p.swap_max_rows = swap_max_rows();
     p.bw[0] = p.b0[0]; p.bw[1] = p.b0[1];  // unused by the SWIGLU epilogue
     if (!ok) return cudaErrorInvalidValue;
     p.hdr = hdr;
@@ -1405,6 +1492,7 @@ cudaError_t launch_ffn_tc(const FfnGroups& g, const FfnPlanHeader* hdr, const in
     q.b1[0] = q.b0[0]; q.b1[1] = q.b0[1];
     if (!ok) return sh.finish(cudaErrorInvalidValue);
     q.half_tiles = half_tiles();
+    q.swap_max_rows = swap_max_rows();
     q.hdr = hdr;
     q.E = g.E;
     q.max_mtiles = max_mtiles;

@@ -221,3 +221,24 @@ def test_small_row_ring_expert_stage(moe, counts, monkeypatch):
     assert rel_l2(y1, ref) <= BF16_REL_L2
     for r in range(ref.shape[0]):
         assert rel_l2(y1[r], ref[r]) <= 2 * BF16_REL_L2, r
+
+
+# groups of 1 to 64 rows in every activation box height (16, 32, 64), ragged,
+# next to single tiles of more rows and a pair-tile group; d = 1088 and I = 320
+# leave partial n-blocks (the last gate/up block has 64 of 128 columns, the
+# last down block 64 of 256)
+SWAP_COUNTS = [1, 15, 16, 17, 31, 32, 33, 63, 64, 65, 0, 100, 300]
+
+
+@pytest.mark.parametrize("swap", ["0", "16", "32", "64"])
+def test_swapped_small_tiles(moe, swap, monkeypatch):
+    """Single tiles of at most MOE_SWAP_MAX_ROWS rows run with the operands
+    swapped (the weight rows as the M = 128 operand, the activation rows as
+    N = the box height), their products transposed in tensor memory: every
+    setting against the oracle, row by row."""
+    monkeypatch.setenv("MOE_SWAP_MAX_ROWS", swap)
+    y, ref = _run(moe, SWAP_COUNTS, 1088, 320, "bf16", limit=0, seed=17)
+    assert np.all(np.isfinite(y))
+    assert rel_l2(y, ref) <= BF16_REL_L2
+    for r in range(ref.shape[0]):
+        assert rel_l2(y[r], ref[r]) <= 2 * BF16_REL_L2, r

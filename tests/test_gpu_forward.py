@@ -215,13 +215,14 @@ def test_forward_sigmoid_router(moe, name, T):
     _check(cfg, to_f64(y[torch.from_numpy(tokens).long().cuda()]), ref["y"])
 
 
-@pytest.mark.parametrize("gather_max", [0, 32, 128])
-def test_forward_skewed_groups_cover_every_activation_path(moe, monkeypatch, gather_max):
+@pytest.mark.parametrize("gather_max,swap", [(0, 64), (0, 0), (32, 64), (128, 64)])
+def test_forward_skewed_groups_cover_every_activation_path(moe, monkeypatch, gather_max, swap):
     """Expert groups from a few rows to >1000 rows in one call, on single-SM and
-    CTA-pair tiles (pair remainders included); with the in-GEMM gather enabled,
-    row blocks of <= gather_max rows come straight from x (tile::gather4) and
-    larger ones from the permuted copy."""
+    CTA-pair tiles (pair remainders included), small single tiles swapped or
+    not; with the in-GEMM gather enabled, row blocks of <= gather_max rows come
+    straight from x (tile::gather4) and larger ones from the permuted copy."""
     monkeypatch.setenv("MOE_GATHER_MAX_ROWS", str(gather_max))
+    monkeypatch.setenv("MOE_SWAP_MAX_ROWS", str(swap))
     cfg = mi.LayerConfig("skewed", T=2048, d=256, E=16, K=2, I=256, Is=128, seed=4)
     L = Layer(cfg)
     L.bias = (torch.linspace(2.5, -2.5, cfg.E)).float().cuda()   # expert 0 hot, 15 cold
