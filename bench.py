@@ -141,7 +141,8 @@ def oracle_tokens(cfg, tokens, x_host, p_host, bias_host):
 
 def launches_per_forward(cfg, gemv_limit: int = 0) -> int:
     """Kernels libmoe launches for one moe_forward (mirrors the host logic in
-    moe_api.cu): router (GEMV or tcgen05) + top-K, 3 dispatch kernels and the FFN
+    moe_api.cu): router (GEMV or tcgen05) + top-K (one fused launch for at most
+    16 tokens with MOE_FUSED_ROUTER=1), 3 dispatch kernels and the FFN
     plan (one fused launch when T*K <= 1024 and E <= 1024), the row gather when
     the tensor-core path may run,
     (2 GEMV kernels only for fp32 layers or a non-zero GEMV row limit), the
@@ -152,12 +153,14 @@ def launches_per_forward(cfg, gemv_limit: int = 0) -> int:
     fused = cfg.T * cfg.K <= 1024 and cfg.E <= 1024 and \
         os.environ.get("MOE_FUSED_DISPATCH", "1") != "0"
     disp_plan = 1 if fused else 3 + 1
+    # router + top-K: one fused launch for at most 16 tokens when MOE_FUSED_ROUTER=1
+    router = 1 if 0 < cfg.T <= 16 and os.environ.get("MOE_FUSED_ROUTER", "0") == "1" else 2
     if cfg.acts == "e4m3":
         # router + top-K, dispatch + plan, x quantiser, code gather,
         # tcgen05 gate/up, h quantiser (+ h_s), tcgen05 down -- the gate/up and
         # down twice when a group can take pair tiles -- combine
         pair = cfg.T > 128
-        return 2 + disp_plan + 1 + 1 + (2 if pair else 1) + (2 if cfg.Is else 1) \
+        return router + disp_plan + 1 + 1 + (2 if pair else 1) + (2 if cfg.Is else 1) \
             + (2 if pair else 1) + 1
     if cfg.weights == "e4m3":
         # router + top-K, 3 dispatch kernels, row gather, plan, the 8-bit GEMV
@@ -166,13 +169,13 @@ def launches_per_forward(cfg, gemv_limit: int = 0) -> int:
         limit = int(os.environ.get("MOE_GEMV8_MAX_ROWS", "8"))
         gemv = (2 if limit > 0 else 0) + (2 if limit > 8 else 0)
         tc = 2 if cfg.T > limit else 0
-        return 2 + disp_plan + 1 + gemv + tc + 1
+        return router + disp_plan + 1 + gemv + tc + 1
     need_tc = cfg.dtype == "bf16" and cfg.T > gemv_limit
     gather = need_tc and cfg.T > int(os.environ.get("MOE_GATHER_MAX_ROWS", "0"))
     gemv = cfg.dtype == "f32" or gemv_limit > 0
     pair_min = int(os.environ.get("MOE_PAIR_MIN_ROWS", "0"))
     pair = need_tc and (cfg.T >= pair_min if pair_min > 0 else cfg.T > 128)
-    return (2 + disp_plan + (1 if gather else 0) + (2 if gemv else 0) + (2 if need_tc else 0)
+    return (router + disp_plan + (1 if gather else 0) + (2 if gemv else 0) + (2 if need_tc else 0)
             + (2 if pair else 0) + 1)
 
 

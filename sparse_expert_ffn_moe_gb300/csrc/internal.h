@@ -91,6 +91,13 @@ moe_status check_shape(const moe_shape* s);
 int router_splits_for(const moe_shape& s);
 cudaError_t launch_router_gemv(const moe_shape& s, const void* x, const void* w_g, float* part,
                                int splits, cudaStream_t st);
+// a few tokens: GEMV and top-K in one launch (ticket: a zeroed counter)
+bool fused_router_enabled();
+bool router_fused_possible(const moe_shape& s);
+cudaError_t launch_router_fused(const moe_shape& s, const void* x, const void* w_g, float* part,
+                                int splits, const float* bias, float* logits_out,
+                                int32_t* topk_idx, float* topk_w, unsigned int* ticket,
+                                cudaStream_t st);
 cudaError_t launch_topk_softmax(const moe_shape& s, const float* part, int splits,
                                 const float* bias, float* logits_out, int32_t* topk_idx,
                                 float* topk_w, cudaStream_t st);

@@ -64,6 +64,40 @@ bool use_tc_router(const moe_shape& s) {
     return s.dtype == MOE_BF16 && s.T >= 128 && s.E >= 64;
 }
 
+// The workspace's error block: the device error record at its start, the fused
+// router's ticket counter at kRouteTicket; every entry point clears the whole
+// block before it enqueues work.
+constexpr size_t kErrBlockBytes = 256;
+constexpr size_t kRouteTicket = 128;
+static_assert(sizeof(DevError) <= kRouteTicket, "error record and ticket overlap");
+
+unsigned int* route_ticket(void* workspace, const WsLayout& L) {
+    return reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(workspace) + L.err + kRouteTicket);
+}
+
+// Stage 1 from x into topk_idx / topk_w (and the selection keys into
+// logits_out when given): the tensor-core GEMM for large bf16 batches, one
+// fused GEMV + top-K launch for a few tokens, else the split-K GEMV and then
+// the top-K.  The error block must have been cleared on the stream.
+cudaError_t launch_route(const moe_shape& s, const WsLayout& L, void* workspace, const void* x,
+                         const void* w_g, const float* bias, float* logits_out, int32_t* topk_idx,
+                         float* topk_w, DevError* err, cudaStream_t cs) {
+    float* part = at<float>(workspace, L.router_part);
+    int splits = L.router_splits;
+    cudaError_t e;
+    if (use_tc_router(s) && tc_available()) {
+        e = launch_router_tc(s, x, w_g, part, err, cs);
+        splits = 1;
+    } else if (router_fused_possible(s)) {
+        return launch_router_fused(s, x, w_g, part, splits, bias, logits_out, topk_idx, topk_w,
+                                   route_ticket(workspace, L), cs);
+    } else {
+        e = launch_router_gemv(s, x, w_g, part, splits, cs);
+    }
+    if (e != cudaSuccess) return e;
+    return launch_topk_softmax(s, part, splits, bias, logits_out, topk_idx, topk_w, cs);
+}
+
 // 8-bit weights: bf16 activations, K extents that whole 128-code boxes tile
 moe_status check_fp8_shape(const moe_shape& s) {
     if (s.dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
@@ -139,7 +173,7 @@ WsLayout ws_layout(const moe_shape& s) {
         o = align_up(o + (bytes ? bytes : 1));
         return at_;
     };
-    L.err = take(sizeof(DevError));
+    L.err = take(kErrBlockBytes);
     L.router_part = take(sizeof(float) * (size_t)(L.router_splits > 1 ? L.router_splits : 1) * T * E);
     L.logits = 0;
     L.topk_idx = take(sizeof(int32_t) * n);
@@ -202,20 +236,12 @@ moe_status moe_route(const moe_shape* shape, const void* x, const void* w_g, con
     cudaStream_t cs = (cudaStream_t)stream;
     const WsLayout L = ws_layout(s);
     DevError* err = at<DevError>(workspace, L.err);
-    cudaError_t e = cudaMemsetAsync(err, 0, sizeof(DevError), cs);
+    cudaError_t e = cudaMemsetAsync(err, 0, kErrBlockBytes, cs);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     if (logits_in)
         return cuda_status(launch_topk_softmax(s, logits_in, 1, bias, logits_out, topk_idx, topk_w, cs));
-    float* part = at<float>(workspace, L.router_part);
-    int splits = L.router_splits;
-    if (use_tc_router(s) && tc_available()) {
-        e = launch_router_tc(s, x, w_g, part, err, cs);
-        splits = 1;
-    } else {
-        e = launch_router_gemv(s, x, w_g, part, splits, cs);
-    }
-    if (e != cudaSuccess) return MOE_ERR_CUDA;
-    return cuda_status(launch_topk_softmax(s, part, splits, bias, logits_out, topk_idx, topk_w, cs));
+    return cuda_status(launch_route(s, L, workspace, x, w_g, bias, logits_out, topk_idx, topk_w,
+                                    err, cs));
 }
 
 moe_status moe_permute(const moe_shape* shape, const int32_t* topk_idx, const void* x,
@@ -230,7 +256,7 @@ moe_status moe_permute(const moe_shape* shape, const int32_t* topk_idx, const vo
     cudaStream_t cs = (cudaStream_t)stream;
     const WsLayout L = ws_layout(s);
     DevError* err = at<DevError>(workspace, L.err);
-    cudaError_t e = cudaMemsetAsync(err, 0, sizeof(DevError), cs);
+    cudaError_t e = cudaMemsetAsync(err, 0, kErrBlockBytes, cs);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     if (s.T == 0) {
         // no slots: every count is zero and every offset is zero
@@ -266,7 +292,7 @@ moe_status moe_expert_ffn(const moe_shape* shape, const void* x_perm, const int3
     cudaStream_t cs = (cudaStream_t)stream;
     const WsLayout L = ws_layout(s);
     DevError* err = at<DevError>(workspace, L.err);
-    cudaError_t e = cudaMemsetAsync(err, 0, sizeof(DevError), cs);
+    cudaError_t e = cudaMemsetAsync(err, 0, kErrBlockBytes, cs);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     FfnGroups g{};
     g.E = s.E;
@@ -336,21 +362,13 @@ moe_status moe_forward(const moe_shape* shape, const void* x, const void* w_g, c
     cudaStream_t cs = (cudaStream_t)stream;
     const WsLayout L = ws_layout(s);
     DevError* err = at<DevError>(workspace, L.err);
-    cudaError_t e = cudaMemsetAsync(err, 0, sizeof(DevError), cs);
+    cudaError_t e = cudaMemsetAsync(err, 0, kErrBlockBytes, cs);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
 
     // 1. router scores, top-K, softmax over the K
-    float* part = at<float>(workspace, L.router_part);
     int32_t* topk_idx = at<int32_t>(workspace, L.topk_idx);
     float* topk_w = at<float>(workspace, L.topk_w);
-    int splits = L.router_splits;
-    if (use_tc_router(s) && tc_available()) {
-        e = launch_router_tc(s, x, w_g, part, err, cs);
-        splits = 1;
-    } else {
-        e = launch_router_gemv(s, x, w_g, part, splits, cs);
-    }
-    if (e == cudaSuccess) e = launch_topk_softmax(s, part, splits, bias, nullptr, topk_idx, topk_w, cs);
+    e = launch_route(s, L, workspace, x, w_g, bias, nullptr, topk_idx, topk_w, err, cs);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
 
     // 2. dispatch (and, for small batches, the expert plan in the same launch)
@@ -442,7 +460,7 @@ moe_status moe_expert_ffn_fp8(const moe_shape* shape, const void* x_perm, const 
     cudaStream_t cs = (cudaStream_t)stream;
     const WsLayout L = ws_layout(s);
     DevError* err = at<DevError>(workspace, L.err);
-    cudaError_t e = cudaMemsetAsync(err, 0, sizeof(DevError), cs);
+    cudaError_t e = cudaMemsetAsync(err, 0, kErrBlockBytes, cs);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     FfnGroups g{};
     g.E = s.E;
@@ -498,21 +516,13 @@ moe_status moe_forward_fp8(const moe_shape* shape, const void* x, const void* w_
     cudaStream_t cs = (cudaStream_t)stream;
     const WsLayout L = ws_layout(s);
     DevError* err = at<DevError>(workspace, L.err);
-    cudaError_t e = cudaMemsetAsync(err, 0, sizeof(DevError), cs);
+    cudaError_t e = cudaMemsetAsync(err, 0, kErrBlockBytes, cs);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
 
     // 1. router (bf16 weights), top-K and weights
-    float* part = at<float>(workspace, L.router_part);
     int32_t* topk_idx = at<int32_t>(workspace, L.topk_idx);
     float* topk_w = at<float>(workspace, L.topk_w);
-    int splits = L.router_splits;
-    if (use_tc_router(s)) {
-        e = launch_router_tc(s, x, w_g, part, err, cs);
-        splits = 1;
-    } else {
-        e = launch_router_gemv(s, x, w_g, part, splits, cs);
-    }
-    if (e == cudaSuccess) e = launch_topk_softmax(s, part, splits, bias, nullptr, topk_idx, topk_w, cs);
+    e = launch_route(s, L, workspace, x, w_g, bias, nullptr, topk_idx, topk_w, err, cs);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
 
     // 2. dispatch (for small batches with the expert plan) and the permuted
@@ -630,7 +640,7 @@ moe_status moe_expert_ffn_w8a8(const moe_shape* shape, const void* x_perm, const
     cudaStream_t cs = (cudaStream_t)stream;
     const WsLayout L = ws_layout(s);
     DevError* err = at<DevError>(workspace, L.err);
-    cudaError_t e = cudaMemsetAsync(err, 0, sizeof(DevError), cs);
+    cudaError_t e = cudaMemsetAsync(err, 0, kErrBlockBytes, cs);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     const int64_t R = (int64_t)s.T * s.K;
     float* sc = at<float>(workspace, L.ascale);
@@ -685,21 +695,13 @@ moe_status moe_forward_w8a8(const moe_shape* shape, const void* x, const void* w
     cudaStream_t cs = (cudaStream_t)stream;
     const WsLayout L = ws_layout(s);
     DevError* err = at<DevError>(workspace, L.err);
-    cudaError_t e = cudaMemsetAsync(err, 0, sizeof(DevError), cs);
+    cudaError_t e = cudaMemsetAsync(err, 0, kErrBlockBytes, cs);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
 
     // 1. router (bf16 x and weights), top-K and weights
-    float* part = at<float>(workspace, L.router_part);
     int32_t* topk_idx = at<int32_t>(workspace, L.topk_idx);
     float* topk_w = at<float>(workspace, L.topk_w);
-    int splits = L.router_splits;
-    if (use_tc_router(s)) {
-        e = launch_router_tc(s, x, w_g, part, err, cs);
-        splits = 1;
-    } else {
-        e = launch_router_gemv(s, x, w_g, part, splits, cs);
-    }
-    if (e == cudaSuccess) e = launch_topk_softmax(s, part, splits, bias, nullptr, topk_idx, topk_w, cs);
+    e = launch_route(s, L, workspace, x, w_g, bias, nullptr, topk_idx, topk_w, err, cs);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
 
     // 2. dispatch (for small batches with the expert plan); x quantised per

@@ -24,13 +24,12 @@ constexpr int kRouterWarps = 8;
 constexpr int kRouterTok = 8;  // tokens per pass
 constexpr int kMaxSplits = 8;  // split-K partials per score
 
-// part[s][t][e] = sum_{k in split s} x[t][k] * w_g[e][k]
+// part[s][t][e] = sum_{k in split s} x[t][k] * w_g[e][k], for the units
+// (token chunk, expert, split) this block's warps take
 template <typename T>
-__global__ void __launch_bounds__(kRouterWarps * 32)
-router_gemv_kernel(const T* __restrict__ x, const T* __restrict__ w_g, float* __restrict__ part,
-                   int Tn, int d, int E, int splits) {
-    pdl_wait();
-    pdl_trigger();
+__device__ __forceinline__ void router_gemv_units(const T* __restrict__ x, const T* __restrict__ w_g,
+                                                  float* __restrict__ part, int Tn, int d, int E,
+                                                  int splits) {
     constexpr int V = Elem<T>::kPerVec;
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -71,6 +70,15 @@ router_gemv_kernel(const T* __restrict__ x, const T* __restrict__ w_g, float* __
             if (lane == 0 && m < nt) part[((int64_t)s * Tn + t0 + m) * E + e] = r;
         }
     }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kRouterWarps * 32)
+router_gemv_kernel(const T* __restrict__ x, const T* __restrict__ w_g, float* __restrict__ part,
+                   int Tn, int d, int E, int splits) {
+    pdl_wait();
+    pdl_trigger();
+    router_gemv_units<T>(x, w_g, part, Tn, d, E, splits);
 }
 
 // Few experts, many tokens: part[t][e] = sum_k x[t][k] * w_g[e][k] with one
@@ -138,6 +146,9 @@ router_tokens_kernel(const T* __restrict__ x, const T* __restrict__ w_g, float* 
 
 // the token-major kernel serves E <= 32 from this many tokens on
 constexpr int kRouterTokMinT = 256;
+// the fused GEMV + top-K launch serves batches of at most this many tokens
+// (its last block routes them all, two per warp at most)
+constexpr int kFusedRouteMaxT = 16;
 
 struct Cand {
     float key;  // what the selection compares
@@ -156,16 +167,15 @@ __device__ __forceinline__ bool beats(const Cand& a, const Cand& b) {
 //          section 4.3): a = sigmoid(score), key = a + bias (the bias only
 //          steers the selection), w = a / (sum of the selected a + 1e-6).
 // logits_out receives the keys.
-template <int MAXM, int MODE>
-__global__ void __launch_bounds__(256)
-topk_route_kernel(const float* __restrict__ part, int splits, const float* __restrict__ bias,
-                  float* __restrict__ logits_out, int32_t* __restrict__ topk_idx,
-                  float* __restrict__ topk_w, int Tn, int E, int K) {
-    pdl_wait();
-    pdl_trigger();
-    const int lane = threadIdx.x & 31;
-    const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    if (t >= Tn) return;
+// The whole warp routes token t.  CG: read the partials through L2 only (they
+// were written by other blocks of the same launch).
+template <int MAXM, int MODE, bool CG>
+__device__ __forceinline__ void topk_token(const float* __restrict__ part, int splits,
+                                           const float* __restrict__ bias,
+                                           float* __restrict__ logits_out,
+                                           int32_t* __restrict__ topk_idx,
+                                           float* __restrict__ topk_w, int Tn, int E, int K, int t,
+                                           int lane) {
     float key[MAXM], val[MAXM];
 #pragma unroll
     for (int m = 0; m < MAXM; ++m) {
@@ -175,8 +185,10 @@ topk_route_kernel(const float* __restrict__ part, int splits, const float* __res
             // fixed summation order over the split-K partials (deterministic)
             float pq[kMaxSplits];
 #pragma unroll
-            for (int q = 0; q < kMaxSplits; ++q)
-                pq[q] = q < splits ? part[((int64_t)q * Tn + t) * E + e] : 0.f;
+            for (int q = 0; q < kMaxSplits; ++q) {
+                const float* src = part + ((int64_t)q * Tn + t) * E + e;
+                pq[q] = q < splits ? (CG ? __ldcg(src) : *src) : 0.f;
+            }
             float s = pq[0];
 #pragma unroll
             for (int q = 1; q < kMaxSplits; ++q)
@@ -228,6 +240,53 @@ topk_route_kernel(const float* __restrict__ part, int splits, const float* __res
     }
 }
 
+template <int MAXM, int MODE>
+__global__ void __launch_bounds__(256)
+topk_route_kernel(const float* __restrict__ part, int splits, const float* __restrict__ bias,
+                  float* __restrict__ logits_out, int32_t* __restrict__ topk_idx,
+                  float* __restrict__ topk_w, int Tn, int E, int K) {
+    pdl_wait();
+    pdl_trigger();
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (t >= Tn) return;
+    topk_token<MAXM, MODE, false>(part, splits, bias, logits_out, topk_idx, topk_w, Tn, E, K, t,
+                                  lane);
+}
+
+// A few tokens (T <= kFusedRouteMaxT): the split-K GEMV and the top-K in one
+// launch.  Every block computes its (chunk, expert, split) partials as
+// router_gemv_kernel does, makes them visible device-wide and takes a ticket;
+// the block that takes the last ticket finds every partial written and routes
+// the tokens, one warp per token (the same fixed-order sum of the partials and
+// the same warp top-K as the two-launch path, so the same bits).  No block
+// waits for another.  The ticket counter lives in the workspace's error block,
+// which the entry point clears before the launch; the last block also puts it
+// back to zero.
+template <typename T, int MAXM, int MODE>
+__global__ void __launch_bounds__(kRouterWarps * 32)
+router_fused_kernel(const T* __restrict__ x, const T* __restrict__ w_g, float* __restrict__ part,
+                    int Tn, int d, int E, int splits, const float* __restrict__ bias,
+                    float* __restrict__ logits_out, int32_t* __restrict__ topk_idx,
+                    float* __restrict__ topk_w, int K, unsigned int* __restrict__ ticket) {
+    pdl_wait();
+    pdl_trigger();
+    __shared__ int last;
+    router_gemv_units<T>(x, w_g, part, Tn, d, E, splits);
+    // the lanes that wrote partials make them visible device-wide before the ticket
+    if ((threadIdx.x & 31) == 0) __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) last = atomicAdd(ticket, 1u) == gridDim.x - 1;
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int t = warp; t < Tn; t += kRouterWarps)
+        topk_token<MAXM, MODE, true>(part, splits, bias, logits_out, topk_idx, topk_w, Tn, E, K, t,
+                                     lane);
+    if (threadIdx.x == 0) *ticket = 0u;
+}
+
 }  // namespace
 
 // about 224 16-byte vectors (7 per lane) of a W_g row per split; one split
@@ -273,6 +332,55 @@ cudaError_t launch_router_gemv(const moe_shape& s, const void* x, const void* w_
                           (const bf16*)w_g, part, s.T, s.d, s.E, splits);
     return launch_pdl(router_gemv_kernel<float>, grid, block, 0, st, (const float*)x,
                       (const float*)w_g, part, s.T, s.d, s.E, splits);
+}
+
+bool router_fused_possible(const moe_shape& s) {
+    return s.T > 0 && s.T <= kFusedRouteMaxT && fused_router_enabled();
+}
+
+// MOE_FUSED_ROUTER=1 (read per call) routes batches of at most 16 tokens in
+// one launch.  Off by default: measured on GB300 (interleaved, 4 x 300 calls
+// each) the fused launch was slower than the two launches -- DeepSeek-V3 decode
+// 827.6 vs 818.3 us, T = 1 164.3 vs 163.2 us -- the last block's top-K starting
+// only after every block's fence and ticket, where the separate top-K kernel
+// is already resident and waiting.
+bool fused_router_enabled() {
+    const char* e = getenv("MOE_FUSED_ROUTER");
+    return e && e[0] == '1';
+}
+
+cudaError_t launch_router_fused(const moe_shape& s, const void* x, const void* w_g, float* part,
+                                int splits, const float* bias, float* logits_out,
+                                int32_t* topk_idx, float* topk_w, unsigned int* ticket,
+                                cudaStream_t st) {
+    const int64_t units = ceil_div(s.T, kRouterTok) * (int64_t)s.E * splits;
+    int64_t blocks = ceil_div(units, kRouterWarps);
+    const int64_t cap = (int64_t)device_sm_count() * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    const dim3 grid((unsigned)blocks), block(kRouterWarps * 32);
+    const int m = (int)ceil_div(s.E, 32);
+    cudaError_t e;
+#define MOE_FUSED(TT, M, MODE)                                                                    \
+    e = launch_pdl(router_fused_kernel<TT, M, MODE>, grid, block, 0, st, (const TT*)x,            \
+                   (const TT*)w_g, part, s.T, s.d, s.E, splits, bias, logits_out, topk_idx,       \
+                   topk_w, s.K, ticket)
+#define MOE_FUSED_M(TT, MODE)                    \
+    if (m <= 1) MOE_FUSED(TT, 1, MODE);          \
+    else if (m <= 2) MOE_FUSED(TT, 2, MODE);     \
+    else if (m <= 4) MOE_FUSED(TT, 4, MODE);     \
+    else if (m <= 8) MOE_FUSED(TT, 8, MODE);     \
+    else if (m <= 16) MOE_FUSED(TT, 16, MODE);   \
+    else MOE_FUSED(TT, 32, MODE)
+    if (s.dtype == MOE_BF16) {
+        if (s.router == MOE_ROUTER_SIGMOID) { MOE_FUSED_M(bf16, 1); } else { MOE_FUSED_M(bf16, 0); }
+    } else {
+        if (s.router == MOE_ROUTER_SIGMOID) { MOE_FUSED_M(float, 1); } else { MOE_FUSED_M(float, 0); }
+    }
+#undef MOE_FUSED_M
+#undef MOE_FUSED
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
 }
 
 cudaError_t launch_topk_softmax(const moe_shape& s, const float* part, int splits,

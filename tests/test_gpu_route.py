@@ -182,3 +182,51 @@ def test_sigmoid_route_from_x(moe, name, T):
     _, _, raw_ref = oracle.route(host(L.x), L.hp["w_g"], cfg.K, dtype=cfg.dtype)
     delta = np.abs(raw.cpu().numpy() - raw_ref).max(axis=1, keepdims=True)
     assert np.all(np.abs(gw[ok] - ref_w[ok]) <= (2.0 * delta[ok] + 2e-6) * ref_w[ok])
+
+
+@pytest.mark.parametrize("T,d,E,K,dtype,router", [
+    (1, 7168, 256, 8, "bf16", "softmax"), (8, 7168, 256, 8, "bf16", "sigmoid"),
+    (16, 7168, 256, 8, "bf16", "softmax"), (5, 256, 8, 2, "f32", "softmax"),
+    (16, 512, 1024, 32, "bf16", "softmax"), (3, 192, 33, 5, "f32", "sigmoid"),
+    (17, 7168, 256, 8, "bf16", "softmax")])
+def test_fused_router_changes_no_bit(moe, T, d, E, K, dtype, router, monkeypatch):
+    """With MOE_FUSED_ROUTER=1 batches of at most 16 tokens score and route in one
+    launch (the block that finishes last runs the top-K): the same expert ids,
+    weights and keys, bit for bit, as the two launches (the default), on three
+    calls in a row on one workspace (the ticket counter must start from zero each
+    time) and from a replayed CUDA graph.  T = 17 is past the bound (two launches
+    either way)."""
+    cfg = mi.LayerConfig("fused_route", T=T, d=d, E=E, K=K, I=64, dtype=dtype, router=router,
+                         seed=23)
+    L = Layer(cfg, only={"w_g"})
+    bias = torch.from_numpy(np.random.default_rng(3).standard_normal(E) / 16).float().cuda()
+    s = L.shape(moe)
+    ws = moe.alloc_workspace(s)
+
+    def route():
+        idx = torch.full((T, K), -7, dtype=torch.int32, device="cuda")
+        w = torch.full((T, K), -1.0, dtype=torch.float32, device="cuda")
+        keys = torch.empty((T, E), dtype=torch.float32, device="cuda")
+        moe.moe_route(s, L.x, L.p["w_g"], bias, None, keys, idx, w, ws)
+        return idx, w, keys
+
+    monkeypatch.setenv("MOE_FUSED_ROUTER", "0")
+    ref = route()
+    torch.cuda.synchronize()
+    monkeypatch.setenv("MOE_FUSED_ROUTER", "1")
+    outs = [route() for _ in range(3)]
+    st = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    idx = torch.full((T, K), -7, dtype=torch.int32, device="cuda")
+    w = torch.full((T, K), -1.0, dtype=torch.float32, device="cuda")
+    keys = torch.empty((T, E), dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g, stream=st):
+        moe.moe_route(s, L.x, L.p["w_g"], bias, None, keys, idx, w, ws, stream=st)
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_error(ws) == 0
+    for o in outs + [(idx, w, keys)]:
+        for a, b in zip(o, ref):
+            assert torch.equal(a, b)
