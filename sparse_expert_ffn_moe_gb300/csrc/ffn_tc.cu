@@ -47,6 +47,13 @@
 //              up for the same intermediate indices: h = SiLU(g) * u -> bf16.
 //   STORE_BF16 plain product -> bf16 (down projection).
 //   STORE_F32  plain product -> fp32 (router scores).
+//   COMBINE    the shared expert's down projection fused with the combine:
+//              a dense launch over the T tokens whose epilogue adds, to each
+//              fp32 product y_s[t][c], w[t][j] * y_perm[inv_perm[t*K+j]][c]
+//              for j = 0..K-1 (shared term first, then j ascending, one fp32
+//              fma each -- the combine kernel's order), rounds once and
+//              stores the layer output y.  The routed down launches skip the
+//              shared group and have finished (stream order) before it starts.
 //
 // Every wait on an mbarrier is bounded (MOE_TC_TIMEOUT_MS, default 1000 ms
 // of wall time); when one runs out the CTA records MOE_ERR_TIMEOUT in the
@@ -104,7 +111,7 @@ template <bool PAIR, bool SMA = false> struct Shape {
     static_assert(kAStride % 1024 == 0, "128-byte-swizzle atoms need 1 KB aligned stages");
 };
 
-enum Epi { EPI_SWIGLU = 0, EPI_STORE_BF16 = 1, EPI_STORE_F32 = 2 };
+enum Epi { EPI_SWIGLU = 0, EPI_STORE_BF16 = 1, EPI_STORE_F32 = 2, EPI_COMBINE = 3 };
 
 // 8-bit weights (W8).  TMA streams a CTA's E4M3 weight rows (256 for a
 // single-SM tile, 128 per CTA of a pair) x 128 codes (two 64-deep K steps)
@@ -196,6 +203,13 @@ struct TcParams {
     CUtensorMap u64[2];         // half pair tiles, gate/up: up rows, box 64 rows
     int half_tiles;             // pair tiles of <= 128 rows run as M = 128 (64 rows per CTA)
     int swap_max_rows;          // single tiles of at most this many rows (<= 64) run swapped
+    int skip_shared;            // tiles of the shared group (kind 1) take no work here
+    // COMBINE epilogue: the routed outputs and how to sum them into each token's row
+    const bf16* cmb_yperm;      // y_perm [T*K][d]
+    const int32_t* cmb_inv;     // inv_perm [T*K]: routed row of slot t*K + j (< 0: dropped)
+    const float* cmb_w;         // topk_w [T*K]
+    int cmb_K;
+    int64_t cmb_rows;           // T*K (slots outside [0, cmb_rows) are dropped)
     int split;                  // take only the first hdr->units_pair / units_single units
     const int32_t* row_src;     // token of each routed row (gather from x), or null
     int gather_max;             // gather a CTA's routed rows when it has at most this many
@@ -258,9 +272,9 @@ __device__ __forceinline__ Tile decode_tile_entry(const TcParams& p, int4 e, int
     tl.n0 = nb * kNCols;
     tl.wrow0 = (tl.kind == 0 ? g * p.wrows[0] : 0) + tl.n0;
     tl.kblocks = (p.kdim[tl.kind] + KSTEP - 1) / KSTEP;
-    tl.valid = tl.n0 < p.n_out[tl.kind] && tl.rows > 0;
+    tl.valid = tl.n0 < p.n_out[tl.kind] && tl.rows > 0 && !(p.skip_shared && tl.kind == 1);
     tl.half = PAIR && p.half_tiles != 0 && tl.rows <= BMC;
-    tl.swap = !PAIR && EPI != EPI_STORE_F32 && tl.rows <= p.swap_max_rows;
+    tl.swap = !PAIR && (EPI == EPI_SWIGLU || EPI == EPI_STORE_BF16) && tl.rows <= p.swap_max_rows;
     tl.nsw = abox_rows(abox_for(tl.rows));
     return tl;
 }
@@ -414,7 +428,8 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
     constexpr int kStages = W8 ? W::kConv : S::kStages;  // B stages (and A stages without W8)
     constexpr int kAStages = W8 ? W::kA : S::kStages;
     // swapped tiles (few rows): bf16 single-SM expert GEMMs only
-    constexpr bool kSwap = !PAIR && !W8 && !A8 && EPI != EPI_STORE_F32;
+    constexpr bool kSwap = !PAIR && !W8 && !A8 && (EPI == EPI_SWIGLU || EPI == EPI_STORE_BF16);
+    static_assert(!(EPI == EPI_COMBINE && (W8 || A8 || SMA)), "COMBINE: the bf16 shared down GEMM");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte alignment for the 128-byte-swizzle atoms (the same offset in both CTAs of a pair)
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -996,9 +1011,27 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
                 }
                 // A8: the row's max |h| over every tile of the row, for its quantiser
                 if (A8 && row_ok && hmax_bits != 0) atomicMax(p.hmax[tl.kind] + arow_me, hmax_bits << 16);
-            } else if (EPI == EPI_STORE_BF16) {
+            } else if (EPI == EPI_STORE_BF16 || EPI == EPI_COMBINE) {
                 bf16* out = (bf16*)p.out[tl.kind] + orow * p.ld_out[tl.kind] + tl.n0;
                 const int ncol = tl.half ? BN / 2 : BN;  // tensor-memory columns of this thread's row
+                // COMBINE: the routed rows and weights of this row's token (the first 8
+                // slots kept in registers for every column chunk)
+                constexpr int kCmbSlots = 8;
+                int32_t crow[kCmbSlots];
+                float cw[kCmbSlots];
+                if constexpr (EPI == EPI_COMBINE) {
+#pragma unroll
+                    for (int q = 0; q < kCmbSlots; ++q) {
+                        crow[q] = -1;
+                        cw[q] = 0.0f;
+                        if (row_ok && q < p.cmb_K) {
+                            const int64_t f = (int64_t)arow_me * p.cmb_K + q;
+                            const int32_t r = __ldg(p.cmb_inv + f);
+                            crow[q] = (r >= 0 && r < p.cmb_rows) ? r : -1;
+                            cw[q] = __ldg(p.cmb_w + f);
+                        }
+                    }
+                }
 #pragma unroll 1
                 for (int tc = 0; tc < ncol; tc += 16) {
                     uint32_t v[16];
@@ -1019,11 +1052,69 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
                             for (int k = 0; k < 16; ++k) ds[k] = 1.0f;
                         }
                         uint32_t w[8];
+                        if constexpr (EPI == EPI_COMBINE) {
+                            // y = y_s + sum_j w_j * y_perm[row_j], in fp32, j ascending
+                            float acc[16];
 #pragma unroll
-                        for (int k = 0; k < 8; ++k) {
-                            const __nv_bfloat162 b2 = __floats2bfloat162_rn(
-                                __uint_as_float(v[2 * k]) * ds[2 * k], __uint_as_float(v[2 * k + 1]) * ds[2 * k + 1]);
-                            w[k] = *reinterpret_cast<const uint32_t*>(&b2);
+                            for (int k = 0; k < 16; ++k) acc[k] = __uint_as_float(v[k]);
+                            const int64_t ldy = p.ld_out[tl.kind];
+                            const int64_t col = tl.n0 + c;
+                            for (int j0 = 0; j0 < p.cmb_K; j0 += kCmbSlots) {
+                                int32_t rr[kCmbSlots];
+                                float ww[kCmbSlots];
+#pragma unroll
+                                for (int q = 0; q < kCmbSlots; ++q) {
+                                    if (j0 == 0) {
+                                        rr[q] = crow[q];
+                                        ww[q] = cw[q];
+                                    } else {
+                                        rr[q] = -1;
+                                        ww[q] = 0.0f;
+                                        if (j0 + q < p.cmb_K) {
+                                            const int64_t f = (int64_t)arow_me * p.cmb_K + j0 + q;
+                                            const int32_t r = __ldg(p.cmb_inv + f);
+                                            rr[q] = (r >= 0 && r < p.cmb_rows) ? r : -1;
+                                            ww[q] = __ldg(p.cmb_w + f);
+                                        }
+                                    }
+                                }
+                                // every slot's 16 columns requested before any is summed
+                                uint4 yv[kCmbSlots][2];
+#pragma unroll
+                                for (int q = 0; q < kCmbSlots; ++q) {
+                                    if (rr[q] >= 0) {
+                                        const uint4* src = reinterpret_cast<const uint4*>(
+                                            p.cmb_yperm + (int64_t)rr[q] * ldy + col);
+                                        yv[q][0] = __ldg(src);
+                                        yv[q][1] = __ldg(src + 1);
+                                    }
+                                }
+#pragma unroll
+                                for (int q = 0; q < kCmbSlots; ++q) {
+                                    if (rr[q] < 0) continue;
+                                    const uint32_t u[8] = {yv[q][0].x, yv[q][0].y, yv[q][0].z, yv[q][0].w,
+                                                           yv[q][1].x, yv[q][1].y, yv[q][1].z, yv[q][1].w};
+#pragma unroll
+                                    for (int k = 0; k < 8; ++k) {
+                                        const float lo = __uint_as_float(u[k] << 16);
+                                        const float hi2 = __uint_as_float(u[k] & 0xFFFF0000u);
+                                        acc[2 * k] = fmaf(ww[q], lo, acc[2 * k]);
+                                        acc[2 * k + 1] = fmaf(ww[q], hi2, acc[2 * k + 1]);
+                                    }
+                                }
+                            }
+#pragma unroll
+                            for (int k = 0; k < 8; ++k) {
+                                const __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[2 * k], acc[2 * k + 1]);
+                                w[k] = *reinterpret_cast<const uint32_t*>(&b2);
+                            }
+                        } else {
+#pragma unroll
+                            for (int k = 0; k < 8; ++k) {
+                                const __nv_bfloat162 b2 = __floats2bfloat162_rn(
+                                    __uint_as_float(v[2 * k]) * ds[2 * k], __uint_as_float(v[2 * k + 1]) * ds[2 * k + 1]);
+                                w[k] = *reinterpret_cast<const uint32_t*>(&b2);
+                            }
                         }
                         uint4* dst = reinterpret_cast<uint4*>(out + c);
                         dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
@@ -1415,8 +1506,21 @@ bool tc_pair_possible(int64_t max_rows) {
     return pm > 0 ? max_rows >= pm : max_rows > Shape<false>::kTileRows;
 }
 
+// The combine fused into the shared expert's down projection (MOE_FUSED_COMBINE=1,
+// read per call).  Off by default: measured on GB300 (interleaved A/B, the same
+// box) it is slower on every workload -- Zipf prefill 10.97 vs 10.44 ms,
+// DeepSeek-V3 T=4096 4.08 vs 3.87 ms, decode 823 vs 800 us, T=1 185 vs 161 us:
+// the shared expert's down tiles no longer fill the SMs the routed down tiles
+// leave idle, and its launch waits for every routed row, while the combine it
+// replaces is a short bandwidth-bound pass.
+bool fused_combine_enabled() {
+    const char* e = getenv("MOE_FUSED_COMBINE");
+    return e && e[0] == '1';
+}
+
 cudaError_t launch_ffn_tc(const FfnGroups& g, const FfnPlanHeader* hdr, const int4* mtile_list,
-                          int max_mtiles, bool may_pair, DevError* err, cudaStream_t st) {
+                          int max_mtiles, bool may_pair, DevError* err, cudaStream_t st,
+                          const CombineArgs* cmb) {
     const int64_t R = g.n_routed_rows;
     const int4* single_list = mtile_list;
     const int4* pair_list = mtile_list + max_mtiles;
@@ -1506,9 +1610,42 @@ cudaError_t launch_ffn_tc(const FfnGroups& g, const FfnPlanHeader* hdr, const in
     q.err = err;
     q.timeout_ns = timeout_ns();
     q.test_stall = test_stall();
+    const bool fuse = cmb != nullptr && g.has_shared;
+    q.skip_shared = fuse ? 1 : 0;
     // side by side, the down grids start only when their stream's gate/up grid ended
     e = launch_shapes<EPI_STORE_BF16>(q, pair_list, single_list, may_pair, sh, sh.side == nullptr, small);
-    return sh.finish(e);
+    e = sh.finish(e);
+    if (!fuse || e != cudaSuccess) return e;
+
+    // ---- shared down + combine: y[t] = h_s[t] Ws_down^T + sum_j w[t][j] y_perm[inv[t*K+j]]
+    // (a dense launch over the T token rows, after every routed row is written)
+    TcParams r{};
+    ok = make_amaps(r.a[1], g.h_s, g.T, g.Is);
+    ok &= make_wmaps(r, 1, g.ws_down, g.d, g.Is);
+    if (!ok) return cudaErrorInvalidValue;
+    for (int b = 0; b < kABoxes; ++b) r.a[0][b] = r.a[1][b];
+    r.b0[0] = r.b0[1]; r.bw[0] = r.bw[1]; r.b1[0] = r.b0[1]; r.b1[1] = r.b0[1];
+    r.ag = r.a[1][0];
+    r.half_tiles = half_tiles();
+    r.hdr = nullptr;
+    r.mtiles = nullptr;
+    r.dense_rows = g.T;
+    r.NB = (g.d + BN - 1) / BN;
+    r.n_out[0] = r.n_out[1] = g.d;
+    r.kdim[0] = r.kdim[1] = g.Is;
+    r.wrows[0] = r.wrows[1] = 0;
+    r.out[0] = r.out[1] = cmb->y;
+    r.ld_out[0] = r.ld_out[1] = g.d;
+    r.err = err;
+    r.timeout_ns = timeout_ns();
+    r.test_stall = test_stall();
+    r.cmb_yperm = (const bf16*)g.y;
+    r.cmb_inv = cmb->inv_perm;
+    r.cmb_w = cmb->topk_w;
+    r.cmb_K = cmb->K;
+    r.cmb_rows = g.n_routed_rows;
+    return g.T > Shape<false>::kTileRows ? launch_tc<EPI_COMBINE, true>(r, st)
+                                         : launch_tc<EPI_COMBINE, false>(r, st);
 }
 
 // The expert FFN with E4M3 weights: the same two GEMMs on single-SM tiles

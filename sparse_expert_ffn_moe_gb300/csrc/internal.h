@@ -143,10 +143,22 @@ int tc_pair_min_rows();       // fixed pair threshold (0: the plan picks the che
 int tc_split_rho();          // > 0: the two tile shapes run side by side (plan's SM split cost)
 bool tc_pair_possible(int64_t max_rows);  // a group of at most max_rows rows may take pair tiles
 int tc_gather_max_rows();     // per-CTA routed row blocks up to this size are gathered from x
+// The combine fused into the shared expert's down projection (launch_ffn_tc
+// with a shared group): each token's routed rows and weights, and the output.
+struct CombineArgs {
+    const int32_t* inv_perm;  // [T*K] routed row of each slot (< 0: dropped)
+    const float* topk_w;      // [T*K]
+    int K;
+    void* y;                  // [T][d] layer output (bf16)
+};
+bool fused_combine_enabled();  // MOE_FUSED_COMBINE (read per call)
 // may_pair: some group can reach tc_pair_min_rows() rows (else the pair
-// launches are skipped)
+// launches are skipped).  cmb (with a shared group): the routed down launches
+// skip the shared group, whose down projection then runs as one dense launch
+// that also sums the routed rows into y -- no separate combine.
 cudaError_t launch_ffn_tc(const FfnGroups& g, const FfnPlanHeader* hdr, const int4* mtile_list,
-                          int max_mtiles, bool may_pair, DevError* err, cudaStream_t st);
+                          int max_mtiles, bool may_pair, DevError* err, cudaStream_t st,
+                          const CombineArgs* cmb = nullptr);
 cudaError_t launch_router_tc(const moe_shape& s, const void* x, const void* w_g, float* scores,
                              DevError* err, cudaStream_t st);
 // E4M3 expert weights with row scales (g.s_* set); bf16 activations; the

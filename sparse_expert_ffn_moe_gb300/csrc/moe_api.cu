@@ -424,12 +424,16 @@ moe_status moe_forward(const moe_shape* shape, const void* x, const void* w_g, c
     if (!fused)
         e = launch_ffn_plan(g, s.dtype, hdr, glist, mtiles, L.max_mtiles, gemv_limit(), true, 0, cs);
     if (e == cudaSuccess && gemv_possible(s)) e = launch_ffn_gemv(g, s.dtype, hdr, glist, cs);
+    // 4. combine: with a shared expert on the tensor-core path, fused into the
+    //    shared expert's down projection (its epilogue sums the routed rows)
+    const bool fuse = need_tc && shared && !gemv_possible(s) && fused_combine_enabled();
+    const CombineArgs cmb{inv, topk_w, s.K, y};
     // a group has at most T rows (a token picks an expert once)
     if (e == cudaSuccess && need_tc)
-        e = launch_ffn_tc(g, hdr, mtiles, L.max_mtiles, tc_pair_possible(s.T), err, cs);
+        e = launch_ffn_tc(g, hdr, mtiles, L.max_mtiles, tc_pair_possible(s.T), err, cs,
+                          fuse ? &cmb : nullptr);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
-
-    // 4. combine
+    if (fuse) return MOE_OK;
     return cuda_status(launch_combine(s, g.y, inv, topk_w, shared ? g.y_s : nullptr, y, cs));
 }
 

@@ -292,3 +292,24 @@ def test_small_row_ring_changes_no_bit(moe, T, monkeypatch):
     assert torch.equal(y0, y1)
     ref = oracle.forward(host(L.x), L.hp, cfg.K, dtype=cfg.dtype, bias=L.bias_host())
     _check(cfg, to_f64(y1), ref["y"])
+
+
+@pytest.mark.parametrize("T,K", [(8, 4), (300, 10), (1030, 4)])
+def test_fused_combine(moe, T, K, monkeypatch):
+    """With a shared expert the combine runs in the epilogue of the shared
+    expert's down projection (one dense launch after the routed down GEMMs:
+    single tiles at T = 8, pair tiles with a 6-row half tile at T = 1030; K = 10
+    takes the slot loop past its first 8 slots).  Both ways against the oracle,
+    and within bf16 rounding of each other (the separate combine adds the shared
+    term after rounding it to bf16; the fused one adds its fp32 sum)."""
+    cfg = mi.LayerConfig(f"fused_combine_T{T}", T=T, d=512, E=16, K=K, I=256, Is=384, seed=29)
+    L = Layer(cfg)
+    L.x = _clean_x(L)
+    ref = oracle.forward(host(L.x), L.hp, cfg.K, dtype=cfg.dtype, bias=L.bias_host())["y"]
+    monkeypatch.setenv("MOE_FUSED_COMBINE", "0")
+    y0 = to_f64(L.forward(moe))
+    monkeypatch.setenv("MOE_FUSED_COMBINE", "1")
+    y1 = to_f64(L.forward(moe))
+    _check(cfg, y0, ref)
+    _check(cfg, y1, ref)
+    assert rel_l2(y1, y0) <= 4e-3
