@@ -751,6 +751,75 @@ def bench_all(moe, peaks, args) -> list:
     return res
 
 
+# --------------------------------------------------------------------------- reduced expert pools
+
+def pool_counts(moe, cfg, n_pool: int) -> list:
+    """Per-expert row counts of a reduced pool with the workload's routing
+    profile: the workload's per-expert counts (its own routing on the GPU),
+    sorted, taken at every (E / n_pool)-th rank -- the hottest expert, and so on
+    down to the coldest kept one."""
+    import torch
+    p = mi.make_weights(cfg, "cuda", only={"w_g"})
+    x = mi.make_x(cfg, "cuda")
+    bias = mi.make_bias(cfg, "cuda")
+    s = moe.make_shape(cfg.T, cfg.d, cfg.E, cfg.K, cfg.I, cfg.Is, cfg.dtype, cfg.router)
+    ws = moe.alloc_workspace(s)
+    idx = torch.empty((cfg.T, cfg.K), dtype=torch.int32, device="cuda")
+    w = torch.empty((cfg.T, cfg.K), dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()
+    moe.moe_route(s, x, p["w_g"], bias, None, None, idx, w, ws)
+    counts = torch.bincount(idx.flatten().long(), minlength=cfg.E).cpu()
+    ranked = torch.sort(counts, descending=True).values.tolist()
+    step = max(1, cfg.E // n_pool)
+    del p, x, ws, idx, w
+    torch.cuda.empty_cache()
+    return [int(c) for c in ranked[::step][:n_pool]]
+
+
+def run_stage_pool(args):
+    """The expert-FFN stage alone (moe_expert_ffn) on a reduced pool of
+    args.stage_pool experts with the workload's routing profile (pool_counts):
+    a few GB on the device, for counter captures of the stage's GEMMs."""
+    import torch
+    import sparse_expert_ffn_moe_gb300 as moe
+    torch.cuda.set_device(0)
+    cfg = mi.CONFIGS[args.workload]
+    counts = pool_counts(moe, cfg, args.stage_pool)
+    E, rows = len(counts), sum(counts)
+    pcfg = mi.LayerConfig(f"{cfg.name}_pool{E}", T=rows, d=cfg.d, E=E, K=1, I=cfg.I,
+                          dtype=cfg.dtype, seed=cfg.seed)
+    p = mi.make_weights(pcfg, "cuda", only={"w_gate", "w_up", "w_down"})
+    x_perm = mi.normal((rows, cfg.d), 1.0, cfg.dtype, "cuda", cfg.seed, "x_perm")
+    y_perm = torch.empty_like(x_perm)
+    offsets = torch.tensor([0] + list(np.cumsum(counts)), dtype=torch.int32, device="cuda")
+    s = moe.make_shape(rows, cfg.d, E, 1, cfg.I, 0, cfg.dtype)
+    ws = moe.alloc_workspace(s)
+    st = torch.cuda.Stream()
+    torch.cuda.synchronize()
+
+    def run():
+        moe.moe_expert_ffn(s, x_perm, offsets, p["w_gate"], p["w_up"], p["w_down"], y_perm, ws,
+                           stream=st)
+    for _ in range(max(3, args.warmup)):
+        run()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(st)
+    for _ in range(args.steps):
+        run()
+    e1.record(st)
+    torch.cuda.synchronize()
+    if moe.moe_get_device_error(ws):
+        raise RuntimeError("device error in the expert stage")
+    ms = e0.elapsed_time(e1) / args.steps
+    flops = 6 * rows * cfg.d * cfg.I
+    wbytes = E * expert_bytes(cfg, cfg.I)
+    print(json.dumps({"workload": pcfg.name, "counts": counts, "rows": rows, "ms_per_stage": ms,
+                      "tflops": flops / ms / 1e9, "weight_bytes": wbytes,
+                      "alg_bytes": wbytes + 2 * elem_bytes(cfg) * rows * cfg.d,
+                      "source_sha256": source_sha256()}), flush=True)
+
+
 # --------------------------------------------------------------------------- reference arm
 
 def run_reference(args):
@@ -817,11 +886,16 @@ def main(argv=None):
                     "empty to skip")
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the Mixtral prefill block")
+    ap.add_argument("--stage-pool", type=int, default=0,
+                    help="time only the expert stage on a pool of this many experts with the "
+                         "workload's routing profile (for counter captures)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.stage_pool:
+        run_stage_pool(args)
     else:
         run_ours(args)
 
