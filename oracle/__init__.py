@@ -79,11 +79,15 @@ def bind(lib):
     lib.oracle_expert_ffn_w8a8.argtypes = [i64, i64, i64, i32] + [vp] * 11 + [i32]
     lib.oracle_forward_tokens_w8a8.argtypes = ([i64, vp] + [i64] * 6 + [i32, i32] + [vp] * 19
                                                + [i32])
+    lib.oracle_forward_tokens_a2.argtypes = lib.oracle_forward_tokens_w8a8.argtypes
+    lib.oracle_expert_ffn_a2.argtypes = lib.oracle_expert_ffn_w8a8.argtypes
+    lib.oracle_split_e4m3_rows.argtypes = [i64, i64, i32, vp, vp, vp, vp]
     for f in ("oracle_route", "oracle_permute", "oracle_expert_ffn", "oracle_combine",
               "oracle_shared_ffn", "oracle_forward", "oracle_forward_tokens",
               "oracle_expert_ffn_fp8", "oracle_forward_tokens_fp8", "oracle_e4m3_decode",
               "oracle_e4m3_encode", "oracle_quantize_fp8_rows", "oracle_expert_ffn_w8a8",
-              "oracle_forward_tokens_w8a8", "oracle_round_bf16"):
+              "oracle_forward_tokens_w8a8", "oracle_round_bf16", "oracle_forward_tokens_a2",
+              "oracle_expert_ffn_a2", "oracle_split_e4m3_rows"):
         getattr(lib, f).restype = i32
     return lib
 
@@ -349,12 +353,39 @@ def round_bf16(v):
     return out
 
 
+def split_e4m3_rows(x, dtype: str = "bf16"):
+    """Two E4M3 planes per row: (hi, lo) uint8 codes [rows, cols] and the fp32
+    row scale [rows], with x ~ scale * (value(hi) + value(lo)) (see
+    split_vec in moe_oracle.c)."""
+    lib = _load()
+    x = _in(x, dtype)
+    rows, cols = x.shape
+    hi = np.zeros((rows, cols), np.uint8)
+    lo = np.zeros((rows, cols), np.uint8)
+    sc = np.zeros(rows, np.float32)
+    _check(lib.oracle_split_e4m3_rows(rows, cols, _DT[dtype], _ptr(x), _ptr(hi), _ptr(lo),
+                                      _ptr(sc)), "oracle_split_e4m3_rows")
+    return hi, lo, sc
+
+
+def expert_ffn_a2(x_perm, offsets, q: dict, dtype: str = "bf16", threads: int = 0,
+                  taps: bool = False):
+    """expert_ffn_fp8 with every x_perm row and every hidden row (after its bf16
+    rounding) carried as two E4M3 planes (split_e4m3_rows).  Returns as
+    expert_ffn_w8a8."""
+    return _expert_ffn_a8(x_perm, offsets, q, dtype, threads, taps, "oracle_expert_ffn_a2")
+
+
 def expert_ffn_w8a8(x_perm, offsets, q: dict, dtype: str = "bf16", threads: int = 0,
                     taps: bool = False):
     """expert_ffn_fp8 with 8-bit activations: each x_perm row and each hidden row
     (after fp32 -> bf16 rounding) quantised to E4M3 with one scale per row.
     Returns y_perm [rows, d] f64, or (y_perm, h_pre, h_hat) with taps: h before
     rounding and the dequantised quantised h, both [rows, I] f64."""
+    return _expert_ffn_a8(x_perm, offsets, q, dtype, threads, taps, "oracle_expert_ffn_w8a8")
+
+
+def _expert_ffn_a8(x_perm, offsets, q, dtype, threads, taps, fname):
     lib = _load()
     x_perm = _in(x_perm, dtype)
     offsets = _arr(offsets, np.int32)
@@ -364,20 +395,22 @@ def expert_ffn_w8a8(x_perm, offsets, q: dict, dtype: str = "bf16", threads: int 
     y = np.zeros((rows, d), np.float64)
     h_pre = np.zeros((rows, I), np.float64) if taps else None
     h_hat = np.zeros((rows, I), np.float64) if taps else None
-    _check(lib.oracle_expert_ffn_w8a8(
+    _check(getattr(lib, fname)(
         d, E, I, _DT[dtype], _ptr(x_perm), _ptr(offsets), _ptr(w["w_gate"]), _ptr(w["w_up"]),
         _ptr(w["w_down"]), _ptr(w["s_gate"]), _ptr(w["s_up"]), _ptr(w["s_down"]), _ptr(y),
-        _ptr(h_pre), _ptr(h_hat), threads), "oracle_expert_ffn_w8a8")
+        _ptr(h_pre), _ptr(h_hat), threads), fname)
     return (y, h_pre, h_hat) if taps else y
 
 
 def forward_tokens_fp8(tokens, x, w_g, q: dict, K: int, dtype: str = "bf16", bias=None,
-                       threads: int = 0, router: str = "softmax", act8: bool = False):
+                       threads: int = 0, router: str = "softmax", act8=False):
     """forward_tokens with E4M3 expert weights (routed and, when present, shared):
     q holds w_gate/w_up/w_down (+ ws_*) codes and s_gate/s_up/s_down (+ ss_*)
     row scales; x and w_g are in dtype.  Returns the same dict as forward_tokens.
-    act8: every expert runs W8A8 (its input and hidden rows quantised per row;
-    see oracle_forward_tokens_w8a8)."""
+    act8: True (or "w8a8") -- every expert runs W8A8 (its input and hidden rows
+    quantised per row; see oracle_forward_tokens_w8a8); "planes" -- every
+    expert's input and hidden rows carried as two E4M3 planes
+    (oracle_forward_tokens_a2)."""
     lib = _load()
     tokens = _arr(tokens, np.int32)
     x, w_g = _in(x, dtype), _in(w_g, dtype)
@@ -393,12 +426,14 @@ def forward_tokens_fp8(tokens, x, w_g, q: dict, K: int, dtype: str = "bf16", bia
         "topk_w": np.zeros((n, K), np.float64),
         "logits": np.zeros((n, E), np.float64),
     }
-    fn = lib.oracle_forward_tokens_w8a8 if act8 else lib.oracle_forward_tokens_fp8
+    fname = ("oracle_forward_tokens_a2" if act8 == "planes" else
+             "oracle_forward_tokens_w8a8" if act8 else "oracle_forward_tokens_fp8")
+    fn = getattr(lib, fname)
     _check(fn(
         n, _ptr(tokens), T, d, E, K, I, Is, _DT[dtype], _ROUTER[router], _ptr(x), _ptr(w_g),
         _ptr(bias), _ptr(w["w_gate"]), _ptr(w["w_up"]), _ptr(w["w_down"]), _ptr(w["s_gate"]),
         _ptr(w["s_up"]), _ptr(w["s_down"]), _ptr(w["ws_gate"]), _ptr(w["ws_up"]),
         _ptr(w["ws_down"]), _ptr(w["ss_gate"]), _ptr(w["ss_up"]), _ptr(w["ss_down"]),
         _ptr(out["y"]), _ptr(out["topk_idx"]), _ptr(out["topk_w"]), _ptr(out["logits"]),
-        threads), "oracle_forward_tokens_w8a8" if act8 else "oracle_forward_tokens_fp8")
+        threads), fname)
     return out

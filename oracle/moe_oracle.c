@@ -56,6 +56,9 @@
  * per-row quantisation applied to x and to the expert's hidden row h, which
  * is first rounded to fp32 and then to bf16; these roundings are part of
  * that method's definition and the only intermediate roundings in the file.
+ * The *_a2 entry points carry x and h as two E4M3 planes each (a code and
+ * the code of its remainder, one scale per row): the library's form of the
+ * 8-bit-weight layer on its 8-bit-by-8-bit tensor-core path.
  *
  * Every entry point returns 0 on success and a negative number on a bad
  * argument; nothing is allocated that is not freed before return.
@@ -657,6 +660,7 @@ typedef struct {
     double *y, *logits;
     int32_t *idx;
     double *w;
+    int planes;  /* 8-bit-activation experts: 1 or 2 E4M3 planes per row */
 } tok_ctx;
 
 static void token_row(void *vctx, int64_t r)
@@ -723,7 +727,7 @@ static int forward_tokens(int64_t n, const int32_t *tokens, int64_t T, int64_t d
         if (tokens[r] < 0 || tokens[r] >= T)
             return -1;
     tok_ctx c = {d, E, K, I, Is, dtype, mode, x, w_g, bias, w[0], w[1], w[2],
-                 w[3], w[4], w[5], tokens, y, logits, topk_idx, topk_w};
+                 w[3], w[4], w[5], tokens, y, logits, topk_idx, topk_w, 0};
     par_for(n, nthreads, token_row, &c);
     return 0;
 }
@@ -884,12 +888,71 @@ int oracle_round_bf16(int64_t n, const float *v, float *out)
     return 0;
 }
 
+/* ------------------------------------------------------------------------ */
+/* activations as two E4M3 planes                                           */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * A bf16 activation row carried by two E4M3 codes per element and one fp32
+ * scale per row (the same "make every byte cheaper" rule, x_q = round(x / s),
+ * applied twice): s = amax / 448 as for one plane, q = v / s (fp32 division),
+ * hi = round(q) onto the E4M3 grid, r = q - value(hi) (an fp32 subtraction,
+ * exact: r is a multiple of q's unit in the last place and smaller than half
+ * of hi's grid step), lo = round(r).  The row is then read as
+ *   x_tilde = s * (value(hi) + value(lo)),
+ * within 2^-8 of |x| relative plus 2^-10 s absolute (lo's subnormal step),
+ * and exactly x when s is a power of two and |x| >= s / 4 (a bf16 value has
+ * 8 significant bits; hi keeps the top 4 after rounding, r needs at most 3
+ * more, none finer than the 2^-9 step).  Reading:
+ * the page names 8-bit activations without a second plane; this split is
+ * how the library feeds bf16 activations to an 8-bit-by-8-bit tensor-core
+ * product, an approximation of the exact W8A16 layer defined here so that it
+ * can be checked on its own.
+ */
+static float split_vec(const float *v, int64_t n, uint8_t *hi, uint8_t *lo)
+{
+    float amax = 0.0f;
+    for (int64_t c = 0; c < n; ++c) {
+        const float a = fabsf(v[c]);
+        if (a > amax)
+            amax = a;
+    }
+    const float s = amax > 0.0f ? amax / 448.0f : 1.0f;
+    for (int64_t c = 0; c < n; ++c) {
+        const float q = v[c] / s;
+        hi[c] = e4m3_code(q);
+        const float r = q - (float)e4m3_value(hi[c]);
+        lo[c] = e4m3_code(r);
+    }
+    return s;
+}
+
+/*
+ * oracle_split_e4m3_rows: the two-plane codes of a row-major [rows][cols]
+ * matrix (fp32 or bf16): hi[r][c], lo[r][c] and scale[r] as in split_vec.
+ */
+int oracle_split_e4m3_rows(int64_t rows, int64_t cols, int dtype, const void *x, uint8_t *hi,
+                           uint8_t *lo, float *scale)
+{
+    if (rows < 0 || cols < 1 || (rows > 0 && (!x || !hi || !lo || !scale)))
+        return -1;
+    float *row = (float *)malloc(sizeof(float) * (size_t)cols);
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t c = 0; c < cols; ++c)
+            row[c] = (float)load_elem(x, dtype, r * cols + c);
+        scale[r] = split_vec(row, cols, hi + r * cols, lo + r * cols);
+    }
+    free(row);
+    return 0;
+}
+
 /* Scratch of one W8A8 expert row: n = max(d, I). */
 typedef struct {
-    float *f;    /* [n] fp32 row being quantised */
-    uint8_t *c;  /* [n] its codes               */
-    double *xh;  /* [d] x_hat                   */
-    double *h;   /* [I] h, then h_hat           */
+    float *f;    /* [n] fp32 row being quantised  */
+    uint8_t *c;  /* [n] its codes (hi plane)      */
+    uint8_t *c2; /* [n] lo plane (two planes)     */
+    double *xh;  /* [d] x_hat                     */
+    double *h;   /* [I] h, then h_hat             */
 } a8_scratch;
 
 static int a8_alloc(a8_scratch *s, int64_t d, int64_t I)
@@ -897,29 +960,44 @@ static int a8_alloc(a8_scratch *s, int64_t d, int64_t I)
     const int64_t n = d > I ? d : I;
     s->f = (float *)malloc(sizeof(float) * (size_t)n);
     s->c = (uint8_t *)malloc((size_t)n);
+    s->c2 = (uint8_t *)malloc((size_t)n);
     s->xh = (double *)malloc(sizeof(double) * (size_t)d);
     s->h = (double *)malloc(sizeof(double) * (size_t)I);
-    return s->f && s->c && s->xh && s->h;
+    return s->f && s->c && s->c2 && s->xh && s->h;
 }
 
 static void a8_free(a8_scratch *s)
 {
-    free(s->f); free(s->c); free(s->xh); free(s->h);
+    free(s->f); free(s->c); free(s->c2); free(s->xh); free(s->h);
 }
 
-/* One row through a W8A8 expert (see above).  h_pre (optional, [I]) gets h
+/* The row s->f[0..n) as the expert reads it: one plane (planes = 1:
+ * value(code) * s) or two (planes = 2: (value(hi) + value(lo)) * s). */
+static void act_hat(a8_scratch *s, int64_t n, int planes, double *out)
+{
+    if (planes == 2) {
+        const float sc = split_vec(s->f, n, s->c, s->c2);
+        for (int64_t k = 0; k < n; ++k)
+            out[k] = (e4m3_value(s->c[k]) + e4m3_value(s->c2[k])) * (double)sc;
+    } else {
+        const float sc = quantize_vec(s->f, n, s->c);
+        for (int64_t k = 0; k < n; ++k)
+            out[k] = e4m3_value(s->c[k]) * (double)sc;
+    }
+}
+
+/* One row through a W8A8 expert (see above); planes = 2: x and h each as two
+ * E4M3 planes (split_vec) instead of one.  h_pre (optional, [I]) gets h
  * before rounding, h_hat_out (optional, [I]) gets h_hat. */
 static void swiglu_row_a8(int64_t d, int64_t I, int dtype, const void *xrow_base,
                           int64_t xrow_off, const orc_weight *w_gate, const orc_weight *w_up,
                           const orc_weight *w_down, int64_t wg_off, int64_t wu_off,
                           int64_t wd_off, a8_scratch *s, double *y, double *h_pre,
-                          double *h_hat_out)
+                          double *h_hat_out, int planes)
 {
     for (int64_t k = 0; k < d; ++k)
         s->f[k] = (float)load_elem(xrow_base, dtype, xrow_off + k);
-    const float sx = quantize_vec(s->f, d, s->c);
-    for (int64_t k = 0; k < d; ++k)
-        s->xh[k] = e4m3_value(s->c[k]) * (double)sx;
+    act_hat(s, d, planes, s->xh);
     for (int64_t i = 0; i < I; ++i) {
         double g = 0.0, u = 0.0;
         for (int64_t k = 0; k < d; ++k) {
@@ -932,9 +1010,7 @@ static void swiglu_row_a8(int64_t d, int64_t I, int dtype, const void *xrow_base
         memcpy(h_pre, s->h, sizeof(double) * (size_t)I);
     for (int64_t i = 0; i < I; ++i)
         s->f[i] = round_bf16((float)s->h[i]);
-    const float sh = quantize_vec(s->f, I, s->c);
-    for (int64_t i = 0; i < I; ++i)
-        s->h[i] = e4m3_value(s->c[i]) * (double)sh;
+    act_hat(s, I, planes, s->h);
     if (h_hat_out)
         memcpy(h_hat_out, s->h, sizeof(double) * (size_t)I);
     for (int64_t j = 0; j < d; ++j) {
@@ -952,6 +1028,7 @@ typedef struct {
     const int32_t *offsets;
     orc_weight w_gate, w_up, w_down;
     double *y_perm, *h_pre, *h_hat;
+    int planes;
 } ffn_a8_ctx;
 
 static void ffn_row_a8(void *vctx, int64_t p)
@@ -964,7 +1041,7 @@ static void ffn_row_a8(void *vctx, int64_t p)
         swiglu_row_a8(c->d, c->I, c->dtype, c->x_perm, p * c->d, &c->w_gate, &c->w_up,
                       &c->w_down, wgu, wgu, wd, &s, c->y_perm + p * c->d,
                       c->h_pre ? c->h_pre + p * c->I : NULL,
-                      c->h_hat ? c->h_hat + p * c->I : NULL);
+                      c->h_hat ? c->h_hat + p * c->I : NULL, c->planes);
     a8_free(&s);
 }
 
@@ -974,12 +1051,43 @@ static void ffn_row_a8(void *vctx, int64_t p)
  * rounding.  Optional taps [rows][I] (fp64): h_pre = h before rounding,
  * h_hat = the dequantised quantised h.
  */
+static int expert_ffn_a8(int64_t d, int64_t E, int64_t I, int dtype, const void *x_perm,
+                         const int32_t *offsets, const uint8_t *w_gate, const uint8_t *w_up,
+                         const uint8_t *w_down, const float *s_gate, const float *s_up,
+                         const float *s_down, double *y_perm, double *h_pre, double *h_hat,
+                         int nthreads, int planes);
+
 int oracle_expert_ffn_w8a8(int64_t d, int64_t E, int64_t I, int dtype,
                            const void *x_perm, const int32_t *offsets,
                            const uint8_t *w_gate, const uint8_t *w_up,
                            const uint8_t *w_down, const float *s_gate,
                            const float *s_up, const float *s_down, double *y_perm,
                            double *h_pre, double *h_hat, int nthreads)
+{
+    return expert_ffn_a8(d, E, I, dtype, x_perm, offsets, w_gate, w_up, w_down, s_gate, s_up,
+                         s_down, y_perm, h_pre, h_hat, nthreads, 1);
+}
+
+/*
+ * oracle_expert_ffn_a2: oracle_expert_ffn_fp8 with each row of x_perm and
+ * each hidden row h (after its bf16 rounding) carried as two E4M3 planes
+ * (split_vec).  Same arguments and taps as oracle_expert_ffn_w8a8.
+ */
+int oracle_expert_ffn_a2(int64_t d, int64_t E, int64_t I, int dtype, const void *x_perm,
+                         const int32_t *offsets, const uint8_t *w_gate, const uint8_t *w_up,
+                         const uint8_t *w_down, const float *s_gate, const float *s_up,
+                         const float *s_down, double *y_perm, double *h_pre, double *h_hat,
+                         int nthreads)
+{
+    return expert_ffn_a8(d, E, I, dtype, x_perm, offsets, w_gate, w_up, w_down, s_gate, s_up,
+                         s_down, y_perm, h_pre, h_hat, nthreads, 2);
+}
+
+static int expert_ffn_a8(int64_t d, int64_t E, int64_t I, int dtype, const void *x_perm,
+                         const int32_t *offsets, const uint8_t *w_gate, const uint8_t *w_up,
+                         const uint8_t *w_down, const float *s_gate, const float *s_up,
+                         const float *s_down, double *y_perm, double *h_pre, double *h_hat,
+                         int nthreads, int planes)
 {
     if (d < 1 || E < 1 || I < 1 || !offsets || !y_perm || !w_gate || !w_up || !w_down ||
         !s_gate || !s_up || !s_down || offsets[0] != 0)
@@ -989,7 +1097,7 @@ int oracle_expert_ffn_w8a8(int64_t d, int64_t E, int64_t I, int dtype,
             return -1;
     ffn_a8_ctx c = {d, E, I, dtype, x_perm, offsets, fp8_weight(w_gate, s_gate, d),
                     fp8_weight(w_up, s_up, d), fp8_weight(w_down, s_down, I), y_perm,
-                    h_pre, h_hat};
+                    h_pre, h_hat, planes};
     par_for(offsets[E], nthreads, ffn_row_a8, &c);
     return 0;
 }
@@ -1018,7 +1126,7 @@ static void token_row_a8(void *vctx, int64_t r)
     /* y = SharedExpert(x_t) + sum_j w_j * Expert_{i_j}(x_t), every expert W8A8 */
     if (c->Is) {
         swiglu_row_a8(d, c->Is, c->dtype, c->x, t * d, &c->ws_gate, &c->ws_up, &c->ws_down,
-                      0, 0, 0, &s, y, NULL, NULL);
+                      0, 0, 0, &s, y, NULL, NULL, c->planes);
     } else {
         for (int64_t k = 0; k < d; ++k)
             y[k] = 0.0;
@@ -1027,13 +1135,23 @@ static void token_row_a8(void *vctx, int64_t r)
         const int64_t e = idx[j];
         const int64_t wgu = e * c->I * d, wd = e * d * c->I;
         swiglu_row_a8(d, c->I, c->dtype, c->x, t * d, &c->w_gate, &c->w_up, &c->w_down, wgu,
-                      wgu, wd, &s, ye, NULL, NULL);
+                      wgu, wd, &s, ye, NULL, NULL, c->planes);
         for (int64_t k = 0; k < d; ++k)
             y[k] += w[j] * ye[k];
     }
     free(sc); free(taken); free(ye);
     a8_free(&s);
 }
+
+static int forward_tokens_a8(int64_t n, const int32_t *tokens, int64_t T, int64_t d, int64_t E,
+                             int64_t K, int64_t I, int64_t Is, int dtype, int mode,
+                             const void *x, const void *w_g, const double *bias,
+                             const uint8_t *w_gate, const uint8_t *w_up, const uint8_t *w_down,
+                             const float *s_gate, const float *s_up, const float *s_down,
+                             const uint8_t *ws_gate, const uint8_t *ws_up,
+                             const uint8_t *ws_down, const float *ss_gate, const float *ss_up,
+                             const float *ss_down, double *y, int32_t *topk_idx,
+                             double *topk_w, double *logits, int nthreads, int planes);
 
 /*
  * oracle_forward_tokens_w8a8: oracle_forward_tokens_fp8 with every expert
@@ -1053,6 +1171,48 @@ int oracle_forward_tokens_w8a8(int64_t n, const int32_t *tokens, int64_t T,
                                double *y, int32_t *topk_idx, double *topk_w,
                                double *logits, int nthreads)
 {
+    return forward_tokens_a8(n, tokens, T, d, E, K, I, Is, dtype, mode, x, w_g, bias, w_gate,
+                             w_up, w_down, s_gate, s_up, s_down, ws_gate, ws_up, ws_down,
+                             ss_gate, ss_up, ss_down, y, topk_idx, topk_w, logits, nthreads, 1);
+}
+
+/*
+ * oracle_forward_tokens_a2: oracle_forward_tokens_fp8 with every expert's
+ * input row and hidden row carried as two E4M3 planes (split_vec): the
+ * library's form of the 8-bit-weight layer for expert groups on its
+ * 8-bit-by-8-bit tensor-core path.  Same arguments and outputs.
+ */
+int oracle_forward_tokens_a2(int64_t n, const int32_t *tokens, int64_t T,
+                             int64_t d, int64_t E, int64_t K, int64_t I,
+                             int64_t Is, int dtype, int mode, const void *x,
+                             const void *w_g, const double *bias,
+                             const uint8_t *w_gate, const uint8_t *w_up,
+                             const uint8_t *w_down, const float *s_gate,
+                             const float *s_up, const float *s_down,
+                             const uint8_t *ws_gate, const uint8_t *ws_up,
+                             const uint8_t *ws_down, const float *ss_gate,
+                             const float *ss_up, const float *ss_down,
+                             double *y, int32_t *topk_idx, double *topk_w,
+                             double *logits, int nthreads)
+{
+    return forward_tokens_a8(n, tokens, T, d, E, K, I, Is, dtype, mode, x, w_g, bias, w_gate,
+                             w_up, w_down, s_gate, s_up, s_down, ws_gate, ws_up, ws_down,
+                             ss_gate, ss_up, ss_down, y, topk_idx, topk_w, logits, nthreads, 2);
+}
+
+static int forward_tokens_a8(int64_t n, const int32_t *tokens, int64_t T,
+                               int64_t d, int64_t E, int64_t K, int64_t I,
+                               int64_t Is, int dtype, int mode, const void *x,
+                               const void *w_g, const double *bias,
+                               const uint8_t *w_gate, const uint8_t *w_up,
+                               const uint8_t *w_down, const float *s_gate,
+                               const float *s_up, const float *s_down,
+                               const uint8_t *ws_gate, const uint8_t *ws_up,
+                               const uint8_t *ws_down, const float *ss_gate,
+                               const float *ss_up, const float *ss_down,
+                               double *y, int32_t *topk_idx, double *topk_w,
+                               double *logits, int nthreads, int planes)
+{
     if (!w_gate || !w_up || !w_down || !s_gate || !s_up || !s_down)
         return -1;
     if (Is > 0 && (!ws_gate || !ws_up || !ws_down || !ss_gate || !ss_up || !ss_down))
@@ -1069,7 +1229,7 @@ int oracle_forward_tokens_w8a8(int64_t n, const int32_t *tokens, int64_t T,
                  fp8_weight(w_down, s_down, I),
                  fp8_weight(ws_gate, ss_gate, d), fp8_weight(ws_up, ss_up, d),
                  fp8_weight(ws_down, ss_down, Is),
-                 tokens, y, logits, topk_idx, topk_w};
+                 tokens, y, logits, topk_idx, topk_w, planes};
     par_for(n, nthreads, token_row_a8, &c);
     return 0;
 }

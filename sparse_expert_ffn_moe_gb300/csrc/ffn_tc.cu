@@ -203,6 +203,7 @@ struct TcParams {
     CUtensorMap u64[2];         // half pair tiles, gate/up: up rows, box 64 rows
     int half_tiles;             // pair tiles of <= 128 rows run as M = 128 (64 rows per CTA)
     int swap_max_rows;          // single tiles of at most this many rows (<= 64) run swapped
+    int band;                   // m-tiles per band (0: the shape's default, Shape::kBand)
     int skip_shared;            // tiles of the shared group (kind 1) take no work here
     // COMBINE epilogue: the routed outputs and how to sum them into each token's row
     const bf16* cmb_yperm;      // y_perm [T*K][d]
@@ -260,10 +261,11 @@ __device__ __forceinline__ Tile decode_tile_entry(const TcParams& p, int4 e, int
     const int q = t / NB;
     const int cnt = (Mg + S::kTileRows - 1) / S::kTileRows;
     const int tt = t - (q - i) * NB;  // index inside this group's tiles
-    const int band = tt / (S::kBand * NB);
-    const int bstart = band * S::kBand;
-    const int bcnt = min(S::kBand, cnt - bstart);
-    const int r = tt - band * S::kBand * NB;
+    const int kb = p.band > 0 ? p.band : S::kBand;
+    const int band = tt / (kb * NB);
+    const int bstart = band * kb;
+    const int bcnt = min(kb, cnt - bstart);
+    const int r = tt - band * kb * NB;
     const int nb = r / bcnt;
     const int mi = bstart + r % bcnt;
     tl.kind = (p.dense_rows > 0 || g >= p.E) ? 1 : 0;
@@ -1365,6 +1367,15 @@ int half_tiles() {
     return (s && s[0] == '0') ? 0 : 1;
 }
 
+// m-tiles per band of the CTA-pair tiles (MOE_BAND_PAIR, read per call; 0 or
+// unset: Shape<true>::kBand).  A band's weight n-blocks are swept once per band,
+// so wider bands re-read a large group's weights fewer times.
+int band_pair() {
+    const char* s = getenv("MOE_BAND_PAIR");
+    const int x = s ? atoi(s) : 0;
+    return x < 0 ? 0 : (x > 64 ? 64 : x);
+}
+
 // Single tiles of at most this many rows run swapped (MOE_SWAP_MAX_ROWS, read
 // per call; 0 turns it off; capped at 64, the largest swapped N).
 int swap_max_rows() {
@@ -1467,10 +1478,12 @@ cudaError_t launch_shapes(TcParams& p, const int4* pair_list, const int4* single
     cudaError_t e = cudaSuccess;
     if (may_pair) {
         p.mtiles = pair_list;
+        p.band = band_pair();
         e = launch_tc<EPI, true, W8, A8>(p, sh.st, pdl);
     }
     if (e == cudaSuccess) {
         p.mtiles = single_list;
+        p.band = 0;
         if constexpr (!W8) {
             if (small_rows && small_ring()) return launch_tc<EPI, false, false, A8, true>(p, sh.st2, pdl);
         }

@@ -1,6 +1,6 @@
 """Plant plausible mistakes in a copy of the oracle (on the CPU) and check that
-the pins in test_oracle_pins.py, test_oracle_fp8.py and test_oracle_w8a8.py
-catch every one of them."""
+the pins in test_oracle_pins.py, test_oracle_fp8.py, test_oracle_w8a8.py and
+test_oracle_a2.py catch every one of them."""
 import ctypes
 import os
 
@@ -9,6 +9,7 @@ import pytest
 import oracle
 from tests import test_oracle_fp8 as pins8
 from tests import test_oracle_pins as pins
+from tests import test_oracle_a2 as pins_a2
 from tests import test_oracle_w8a8 as pins_a8
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "moe_oracle.c")
@@ -41,20 +42,33 @@ MUTATIONS = [
     ("fp8_scale_by_column", "(double)w->scale[i / w->row_len]", "(double)w->scale[i % w->row_len]"),
     ("fp8_down_scale_row_length", "fp8_weight(w_down, s_down, I), fp8_weight(ws_gate",
      "fp8_weight(w_down, s_down, d), fp8_weight(ws_gate"),
-    ("quant_scale_not_amax", "amax / 448.0f", "amax / 240.0f"),
-    ("a8_x_not_quantised", "s->xh[k] = e4m3_value(s->c[k]) * (double)sx;",
-     "s->xh[k] = (double)s->f[k];"),
+    ("quant_scale_not_amax", "amax / 448.0f : 1.0f;\n    for (int64_t c = 0; c < n; ++c)\n        codes[c]",
+     "amax / 240.0f : 1.0f;\n    for (int64_t c = 0; c < n; ++c)\n        codes[c]"),
+    ("a2_scale_not_amax", "amax / 448.0f : 1.0f;\n    for (int64_t c = 0; c < n; ++c) {\n        const float q",
+     "amax / 240.0f : 1.0f;\n    for (int64_t c = 0; c < n; ++c) {\n        const float q"),
+    ("a8_x_not_quantised", "act_hat(s, d, planes, s->xh);",
+     "for (int64_t k = 0; k < d; ++k) s->xh[k] = (double)s->f[k];"),
     ("a8_h_not_rounded_to_bf16", "s->f[i] = round_bf16((float)s->h[i]);",
      "s->f[i] = (float)s->h[i];"),
-    ("a8_h_not_quantised", "s->h[i] = e4m3_value(s->c[i]) * (double)sh;",
-     "s->h[i] = (double)s->f[i];"),
-    ("a8_h_takes_the_input_scale", "s->h[i] = e4m3_value(s->c[i]) * (double)sh;",
-     "s->h[i] = e4m3_value(s->c[i]) * (double)sx;"),
+    ("a8_h_not_quantised", "act_hat(s, I, planes, s->h);",
+     "for (int64_t i = 0; i < I; ++i) s->h[i] = (double)s->f[i];"),
+    ("a8_h_read_as_two_planes", "act_hat(s, I, planes, s->h);", "act_hat(s, I, 2, s->h);"),
     ("a8_bf16_rounds_half_up", "u += 0x7fffu + ((u >> 16) & 1u);", "u += 0x8000u;"),
     ("a8_down_scale_row_length", "fp8_weight(w_down, s_down, I), y_perm,\n                    h_pre",
      "fp8_weight(w_down, s_down, d), y_perm,\n                    h_pre"),
     ("a8_shared_expert_skipped", "swiglu_row_a8(d, c->Is, c->dtype, c->x, t * d, &c->ws_gate",
      "if (0) swiglu_row_a8(d, c->Is, c->dtype, c->x, t * d, &c->ws_gate"),
+    ("a2_lo_plane_dropped",
+     "out[k] = (e4m3_value(s->c[k]) + e4m3_value(s->c2[k])) * (double)sc;",
+     "out[k] = e4m3_value(s->c[k]) * (double)sc;"),
+    ("a2_remainder_of_the_unscaled_value", "const float r = q - (float)e4m3_value(hi[c]);",
+     "const float r = v[c] - (float)e4m3_value(hi[c]);"),
+    ("a2_remainder_plane_scaled_twice",
+     "out[k] = (e4m3_value(s->c[k]) + e4m3_value(s->c2[k])) * (double)sc;",
+     "out[k] = (e4m3_value(s->c[k]) + e4m3_value(s->c2[k]) * (double)sc) * (double)sc;"),
+    ("a2_one_plane_in_the_token_layer",
+     "ss_gate, ss_up, ss_down, y, topk_idx, topk_w, logits, nthreads, 2);",
+     "ss_gate, ss_up, ss_down, y, topk_idx, topk_w, logits, nthreads, 1);"),
 ]
 
 PIN_TESTS = [
@@ -81,6 +95,10 @@ PIN_TESTS = [
     lambda: pins_a8.test_w8a8_expert_matches_library_quantisation_at_every_step(1, [3, 0, 5, 1]),
     lambda: pins_a8.test_w8a8_layer_equals_the_8bit_weight_layer_when_activations_are_exact(
         "softmax", 32),
+    lambda: pins_a2.test_planes_match_torch_float8_casts(),
+    lambda: pins_a2.test_planes_meet_the_two_step_error_bound_and_are_not_one_plane(),
+    lambda: pins_a2.test_a2_expert_matches_library_casts_at_every_step(1, [3, 0, 5, 1]),
+    lambda: pins_a2.test_a2_token_forward_matches_the_expert_stage(),
 ]
 
 
