@@ -118,7 +118,8 @@ __device__ __forceinline__ int sw_slot(int s, int m) { return (s & ~15) | ((s & 
 // rows.  One warp per row.
 __device__ __forceinline__ void stage_f16(__half* act, float* rs, const bf16* routed,
                                           const bf16* shared, const Group8& v, int c0, int nt,
-                                          int rows, int n, int warp, int lane) {
+                                          int rows, int n, int warp, int lane,
+                                          const int32_t* row_src = nullptr) {
     for (int m = warp; m < rows; m += kG8Warps) {
         uint2* dst = reinterpret_cast<uint2*>(act + (int64_t)m * n);
         if (m >= nt) {
@@ -126,7 +127,9 @@ __device__ __forceinline__ void stage_f16(__half* act, float* rs, const bf16* ro
             if (lane == 0) rs[m] = 0.0f;
             continue;
         }
-        const int64_t row = v.shared ? (int64_t)(c0 + m) : v.row0 + c0 + m;
+        // a routed row: its permuted copy, or (row_src) the token's row of x
+        const int64_t prow = v.row0 + c0 + m;
+        const int64_t row = v.shared ? (int64_t)(c0 + m) : (row_src ? (int64_t)row_src[prow] : prow);
         const uint4* src = reinterpret_cast<const uint4*>((v.shared ? shared : routed) + row * n);
         float amax = 0.0f;
 #pragma unroll 4
@@ -307,7 +310,7 @@ gemv8_gate_up_kernel(FfnGroups g, const FfnPlanHeader* __restrict__ hdr,
             const int rows = (NT == 1 || nt <= kG8Tok) ? min(R, kG8Tok) : R;
             __syncthreads();  // earlier readers of act are done
             stage_f16(act, rs, (const bf16*)g.a_routed, (const bf16*)g.a_shared, v, c0, nt, rows,
-                      g.d, warp, lane);
+                      g.d, warp, lane, g.row_src);
             __syncthreads();
             for (int64_t k = u + warp; k < seg_end; k += kG8Warps) {
                 const int i0 = (int)(k - (int64_t)a * tpg) * 8;

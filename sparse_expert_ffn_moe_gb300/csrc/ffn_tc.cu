@@ -111,6 +111,26 @@ template <bool PAIR, bool SMA = false> struct Shape {
     static_assert(kAStride % 1024 == 0, "128-byte-swizzle atoms need 1 KB aligned stages");
 };
 
+// 8-bit activations carried as two E4M3 planes (A8 == 2): each 128-code K
+// block of an activation row is [128 hi codes | 128 lo codes] (the row's value
+// is scale * (hi + lo)), so a stage holds two activation tiles, one per plane,
+// and every K slice issues two kind::f8f6f4 MMAs into the same accumulator --
+// the tensor time of one bf16 MMA, on 1-byte weights with no widening.  The
+// ring: 4 stages of 48 KB (pair) or 3 of 64 KB (single).
+template <bool PAIR> struct A2Shape {
+    static constexpr int kTileRows = Shape<PAIR>::kTileRows;
+    static constexpr int kBRows = Shape<PAIR>::kBRows;
+    static constexpr int kStages = PAIR ? 4 : 3;
+    static constexpr int kBand = Shape<PAIR>::kBand;
+    static constexpr uint32_t kAStride = 2 * kABytes;  // hi and lo planes
+    static constexpr uint32_t kBBytes = Shape<PAIR>::kBBytes;
+    static constexpr uint32_t kStageBytes = kAStride + kBBytes;
+    static constexpr uint32_t kRingBytes = kStages * kStageBytes;
+    static_assert(kStages <= kMaxStages, "stage barriers");
+};
+template <bool PAIR, bool SMA, int A8> struct RingOf { using type = Shape<PAIR, SMA>; };
+template <bool PAIR, bool SMA> struct RingOf<PAIR, SMA, 2> { using type = A2Shape<PAIR>; };
+
 enum Epi { EPI_SWIGLU = 0, EPI_STORE_BF16 = 1, EPI_STORE_F32 = 2, EPI_COMBINE = 3 };
 
 // 8-bit weights (W8).  TMA streams a CTA's E4M3 weight rows (256 for a
@@ -415,13 +435,15 @@ __device__ __forceinline__ void tile_scales16(const float (&s)[8], int lane0, fl
     for (int k = 0; k < 16; ++k) out[k] = __shfl_sync(0xffffffffu, s[k & 7], lane0 + (k >> 3));
 }
 
-template <int EPI, bool PAIR, bool W8 = false, bool A8 = false, bool SMA = false>
+template <int EPI, bool PAIR, bool W8 = false, int A8 = 0, bool SMA = false>
 __global__ void __launch_bounds__(W8 ? kThreadsW8 : kThreadsTc, 1)
 tc_gemm_kernel(const __grid_constant__ TcParams p) {
     static_assert(!(W8 && EPI == EPI_STORE_F32), "8-bit weights feed the expert GEMMs only");
     static_assert(!(SMA && (PAIR || W8)), "small-row ring: single-SM tiles without the W8 rings");
     static_assert(!(A8 && (W8 || EPI == EPI_STORE_F32)), "A8: 8-bit operands, expert GEMMs only");
-    using S = Shape<PAIR, SMA>;
+    static_assert(!(A8 == 2 && SMA), "two activation planes: the full-size rings");
+    using S = typename RingOf<PAIR, SMA, A8>::type;
+    constexpr uint32_t kAPlanes = A8 == 2 ? 2u : 1u;  // activation tiles per stage
     using W = W8Shape<PAIR>;
     constexpr uint32_t kAStride = S::kAStride;  // bytes per activation stage (W8: kABytes)
     // A8: both operands E4M3 (kind::f8f6f4); a 128-byte K block holds 128 values
@@ -667,11 +689,12 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
                     }
                 };
                 if constexpr (PAIR) {
-                    tx = a_bytes(min(crows, tl.rows)) + a_bytes(max(0, tl.rows - crows)) + 2 * S::kBBytes;
+                    tx = kAPlanes * (a_bytes(min(crows, tl.rows)) + a_bytes(max(0, tl.rows - crows))) +
+                         2 * S::kBBytes;
                     mb = (EPI == EPI_SWIGLU && rank == 1) ? &p.b1[tl.kind] : &p.b0[tl.kind];
                     brow = tl.wrow0 + ((EPI == EPI_SWIGLU) ? 0 : (int)rank * S::kBRows);
                 } else {
-                    tx = a_bytes(rows_me) + S::kBBytes;
+                    tx = kAPlanes * a_bytes(rows_me) + S::kBBytes;
                     mb = EPI == EPI_SWIGLU ? &p.b0[tl.kind] : &p.bw[tl.kind];
                     brow = tl.wrow0;
                 }
@@ -686,11 +709,23 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
                             if constexpr (PAIR) {
                                 const uint32_t fb = full0 + (uint32_t)(stage * sizeof(uint64_t));
                                 if (rank == 0) ptx::mbar_arrive_expect_tx(&ctl->full[stage], tx);
-                                if (rows_me > 0) ptx::tma_load_2d_pair(a_dst, ma, fb, k0, arow);
+                                if (rows_me > 0) {
+                                    if constexpr (A8 == 2) {  // hi and lo codes of K block kb
+                                        ptx::tma_load_2d_pair(a_dst, ma, fb, 2 * k0, arow);
+                                        ptx::tma_load_2d_pair(a_dst + kABytes, ma, fb, 2 * k0 + 128, arow);
+                                    } else {
+                                        ptx::tma_load_2d_pair(a_dst, ma, fb, k0, arow);
+                                    }
+                                }
                                 load_b_pair(b_dst, fb, k0, mb, brow);
                             } else {
                                 ptx::mbar_arrive_expect_tx(&ctl->full[stage], tx);
-                                ptx::tma_load_2d(a_dst, ma, &ctl->full[stage], k0, arow);
+                                if constexpr (A8 == 2) {
+                                    ptx::tma_load_2d(a_dst, ma, &ctl->full[stage], 2 * k0, arow);
+                                    ptx::tma_load_2d(a_dst + kABytes, ma, &ctl->full[stage], 2 * k0 + 128, arow);
+                                } else {
+                                    ptx::tma_load_2d(a_dst, ma, &ctl->full[stage], k0, arow);
+                                }
                                 ptx::tma_load_2d(b_dst, mb, &ctl->full[stage], k0, brow);
                                 if (EPI == EPI_SWIGLU)
                                     ptx::tma_load_2d(b_dst + S::kBBytes / 2, &p.b1[tl.kind], &ctl->full[stage], k0, brow);
@@ -819,6 +854,11 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
                         if constexpr (A8) {
                             if constexpr (PAIR) ptx::tc_mma_f8_pair(d_tmem, ad, bd, id_t, accum);
                             else ptx::tc_mma_f8(d_tmem, ad, bd, idesc, accum);
+                            if constexpr (A8 == 2) {  // the lo plane times the same weights
+                                const uint64_t ad2 = ptx::sw128_kmajor_desc(a_base + kABytes + kk * 32);
+                                if constexpr (PAIR) ptx::tc_mma_f8_pair(d_tmem, ad2, bd, id_t, 1u);
+                                else ptx::tc_mma_f8(d_tmem, ad2, bd, idesc, 1u);
+                            }
                         } else {
                             if constexpr (PAIR) ptx::tc_mma_f16_pair(d_tmem, ad, bd, id_t, accum);
                             else ptx::tc_mma_f16(d_tmem, ad, bd, idesc, accum);
@@ -1291,18 +1331,20 @@ int test_stall() {
     return (s && atoi(s) != 0) ? 1 : 0;
 }
 
-template <bool PAIR, bool SMA = false>
-constexpr size_t kSmemBytes = 1024 + Shape<PAIR, SMA>::kRingBytes + sizeof(SmemCtl) + 64;
+template <bool PAIR, bool SMA = false, int A8 = 0>
+constexpr size_t kSmemBytes = 1024 + RingOf<PAIR, SMA, A8>::type::kRingBytes + sizeof(SmemCtl) + 64;
 constexpr size_t kSmemBytesW8 = 1024 + kW8RingBytes + sizeof(SmemCtl) + 64;
 static_assert(kSmemBytes<true> <= 232448 && kSmemBytes<false> <= 232448 && kSmemBytes<false, true> <= 232448,
               "shared memory exceeds the per-CTA limit");
+static_assert(kSmemBytes<true, false, 2> <= 232448 && kSmemBytes<false, false, 2> <= 232448,
+              "two-plane shared memory exceeds the per-CTA limit");
 static_assert(kSmemBytesW8 <= 232448, "W8 shared memory exceeds the per-CTA limit");
 
 // allow_pdl = false: the grid starts only when the previous kernel of the
 // stream has finished (so units that take no tile do not hold SMs meanwhile).
-template <int EPI, bool PAIR, bool W8 = false, bool A8 = false, bool SMA = false>
+template <int EPI, bool PAIR, bool W8 = false, int A8 = 0, bool SMA = false>
 cudaError_t launch_tc(const TcParams& p, cudaStream_t st, bool allow_pdl = true) {
-    constexpr size_t smem = W8 ? kSmemBytesW8 : kSmemBytes<PAIR, SMA>;
+    constexpr size_t smem = W8 ? kSmemBytesW8 : kSmemBytes<PAIR, SMA, A8>;
     cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<EPI, PAIR, W8, A8, SMA>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -1367,12 +1409,18 @@ int half_tiles() {
     return (s && s[0] == '0') ? 0 : 1;
 }
 
-// m-tiles per band of the CTA-pair tiles (MOE_BAND_PAIR, read per call; 0 or
-// unset: Shape<true>::kBand).  A band's weight n-blocks are swept once per band,
-// so wider bands re-read a large group's weights fewer times.
+// m-tiles per band of the CTA-pair tiles (MOE_BAND_PAIR, read per call; 0:
+// Shape<true>::kBand = 4).  A band's weight n-blocks are swept once per band,
+// so wider bands re-read a large group's weights fewer times (the Zipf
+// prefill's hottest expert, 14016 rows, sweeps its weights 14 times at 4 pair
+// m-tiles per band); its activation rows (8 x 256 rows x d) stay in L2 across
+// the band's n-blocks.  Measured (ABBA, Zipf prefill): expert stage 9.63 ms at
+// 4, 9.44 ms at 8, 9.45 ms at 16; Mixtral (one band per expert either way)
+// unchanged.
+constexpr int kBandPair = 8;
 int band_pair() {
     const char* s = getenv("MOE_BAND_PAIR");
-    const int x = s ? atoi(s) : 0;
+    const int x = s ? atoi(s) : kBandPair;
     return x < 0 ? 0 : (x > 64 ? 64 : x);
 }
 
@@ -1471,7 +1519,7 @@ struct TwoShapes {
 // One GEMM over both tile lists; pdl as launch_tc's allow_pdl; small_rows:
 // every group has at most kSmaRows rows (single tiles then take the small-row
 // ring; not with W8's rings).
-template <int EPI, bool W8 = false, bool A8 = false>
+template <int EPI, bool W8 = false, int A8 = 0>
 cudaError_t launch_shapes(TcParams& p, const int4* pair_list, const int4* single_list, bool may_pair,
                           const TwoShapes& sh, bool pdl, bool small_rows = false) {
     p.split = sh.split();
@@ -1484,7 +1532,7 @@ cudaError_t launch_shapes(TcParams& p, const int4* pair_list, const int4* single
     if (e == cudaSuccess) {
         p.mtiles = single_list;
         p.band = 0;
-        if constexpr (!W8) {
+        if constexpr (!W8 && A8 != 2) {
             if (small_rows && small_ring()) return launch_tc<EPI, false, false, A8, true>(p, sh.st2, pdl);
         }
         e = launch_tc<EPI, false, W8, A8>(p, sh.st2, pdl);
@@ -1758,11 +1806,12 @@ cudaError_t launch_ffn_tc_fp8(const FfnGroups& g, const FfnPlanHeader* hdr, cons
 // launch_ffn_tc: pair tiles (when may_pair) and single-SM tiles.
 cudaError_t launch_ffn_tc_a8_gate_up(const FfnGroups& g, const FfnPlanHeader* hdr,
                                      const int4* mtile_list, int max_mtiles, bool may_pair,
-                                     DevError* err, cudaStream_t st) {
+                                     DevError* err, cudaStream_t st, int planes) {
     const int64_t R = g.n_routed_rows;
     TcParams p{};
     bool ok = true;
-    ok &= make_amaps_u8(p.a[0], g.a_perm, R, g.d, g.d);
+    // activation rows: planes * d codes each (two planes interleaved per 128-code block)
+    ok &= make_amaps_u8(p.a[0], g.a_perm, R, planes * g.d, planes * g.d);
     p.ag = p.a[0][0];
     p.row_src = nullptr;
     p.gather_max = 0;
@@ -1777,7 +1826,7 @@ cudaError_t launch_ffn_tc_a8_gate_up(const FfnGroups& g, const FfnPlanHeader* hd
     p.hmax[0] = reinterpret_cast<unsigned int*>(const_cast<float*>(g.sa_h));
     p.hmax[1] = reinterpret_cast<unsigned int*>(const_cast<float*>(g.sa_hs));
     if (g.has_shared) {
-        ok &= make_amaps_u8(p.a[1], g.a_shared, g.T, g.d, g.d);
+        ok &= make_amaps_u8(p.a[1], g.a_shared, g.T, planes * g.d, planes * g.d);
         ok &= make_map_u8(&p.b0[1], g.ws_gate, g.Is, g.d, 128);
         ok &= make_map_u8(&p.b1[1], g.ws_up, g.Is, g.d, 128);
         ok &= make_map_u8(&p.g64[1], g.ws_gate, g.Is, g.d, 64);
@@ -1810,24 +1859,27 @@ cudaError_t launch_ffn_tc_a8_gate_up(const FfnGroups& g, const FfnPlanHeader* hd
     p.test_stall = test_stall();
     TwoShapes sh(may_pair, st, true);
     const bool small = g.max_group_rows > 0 && g.max_group_rows <= kSmaRows;
-    return sh.finish(launch_shapes<EPI_SWIGLU, false, true>(p, mtile_list + max_mtiles, mtile_list,
-                                                            may_pair, sh, true, small));
+    if (planes == 2)
+        return sh.finish(launch_shapes<EPI_SWIGLU, false, 2>(p, mtile_list + max_mtiles, mtile_list,
+                                                             may_pair, sh, true));
+    return sh.finish(launch_shapes<EPI_SWIGLU, false, 1>(p, mtile_list + max_mtiles, mtile_list,
+                                                         may_pair, sh, true, small));
 }
 
 cudaError_t launch_ffn_tc_a8_down(const FfnGroups& g, const FfnPlanHeader* hdr,
                                   const int4* mtile_list, int max_mtiles, bool may_pair,
-                                  DevError* err, cudaStream_t st) {
+                                  DevError* err, cudaStream_t st, int planes) {
     const int64_t R = g.n_routed_rows;
     TcParams q{};
     bool ok = true;
-    // h codes in place: row r at h + r * 2I bytes
-    ok &= make_amaps_u8(q.a[0], g.h, R, g.I, 2 * (int64_t)g.I);
+    // h codes in place: row r at h + r * 2I bytes (I codes, or 2I with two planes)
+    ok &= make_amaps_u8(q.a[0], g.h, R, planes * (int64_t)g.I, 2 * (int64_t)g.I);
     ok &= make_map_u8(&q.bw[0], g.w_down, (int64_t)g.E * g.d, g.I, 256);
     ok &= make_map_u8(&q.b0[0], g.w_down, (int64_t)g.E * g.d, g.I, 128);
     q.sc0[0] = g.s_down;
     q.sa[0] = g.sa_h;
     if (g.has_shared) {
-        ok &= make_amaps_u8(q.a[1], g.h_s, g.T, g.Is, 2 * (int64_t)g.Is);
+        ok &= make_amaps_u8(q.a[1], g.h_s, g.T, planes * (int64_t)g.Is, 2 * (int64_t)g.Is);
         ok &= make_map_u8(&q.bw[1], g.ws_down, g.d, g.Is, 256);
         ok &= make_map_u8(&q.b0[1], g.ws_down, g.d, g.Is, 128);
         q.sc0[1] = g.ss_down;
@@ -1859,8 +1911,11 @@ cudaError_t launch_ffn_tc_a8_down(const FfnGroups& g, const FfnPlanHeader* hdr,
     q.test_stall = test_stall();
     TwoShapes sh(may_pair, st, true);
     const bool small = g.max_group_rows > 0 && g.max_group_rows <= kSmaRows;
-    return sh.finish(launch_shapes<EPI_STORE_BF16, false, true>(q, mtile_list + max_mtiles, mtile_list,
-                                                                may_pair, sh, sh.side == nullptr, small));
+    if (planes == 2)
+        return sh.finish(launch_shapes<EPI_STORE_BF16, false, 2>(q, mtile_list + max_mtiles, mtile_list,
+                                                                 may_pair, sh, sh.side == nullptr));
+    return sh.finish(launch_shapes<EPI_STORE_BF16, false, 1>(q, mtile_list + max_mtiles, mtile_list,
+                                                             may_pair, sh, sh.side == nullptr, small));
 }
 
 // scores[T][E] (fp32) = x w_g^T on the tensor cores (single tiles)

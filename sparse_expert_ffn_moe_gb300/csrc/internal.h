@@ -170,10 +170,10 @@ cudaError_t launch_ffn_tc_fp8(const FfnGroups& g, const FfnPlanHeader* hdr, cons
 // separately so the caller can quantise h in between
 cudaError_t launch_ffn_tc_a8_gate_up(const FfnGroups& g, const FfnPlanHeader* hdr,
                                      const int4* mtile_list, int max_mtiles, bool may_pair,
-                                     DevError* err, cudaStream_t st);
+                                     DevError* err, cudaStream_t st, int planes = 1);
 cudaError_t launch_ffn_tc_a8_down(const FfnGroups& g, const FfnPlanHeader* hdr,
                                   const int4* mtile_list, int max_mtiles, bool may_pair,
-                                  DevError* err, cudaStream_t st);
+                                  DevError* err, cudaStream_t st, int planes = 1);
 
 // ---- ffn_gemv_fp8.cu (E4M3 weights, small groups) ----
 int gemv8_max_rows();  // groups with at most this many rows take the 8-bit GEMV
@@ -195,6 +195,15 @@ cudaError_t launch_quantize_act_rows(int64_t rows, int cols, const void* w, int6
 // The same quantisation with each row's max |value| already known: amax_scale[r]
 // holds it as fp32 bits on entry and the row's scale on return.  One warp per
 // row, walking it from low to high addresses, so codes may overwrite the row.
+// Two E4M3 planes per value (a code and the code of its fp32 remainder),
+// interleaved per 128-value block: [128 hi | 128 lo] bytes; cols a multiple
+// of 128.  x rows to a separate buffer (ld_out bytes apart, 2 * cols used), or
+// rows whose max |value| is known split in place (amax_scale: the max as fp32
+// bits in, the row scale out).
+cudaError_t launch_split_act_rows(int64_t rows, int cols, const void* w, int64_t ld_in,
+                                  uint8_t* codes, int64_t ld_out, float* scales, cudaStream_t st);
+cudaError_t launch_split_rows_known_amax(int64_t rows, int cols, void* w, int64_t ld,
+                                         float* amax_scale, cudaStream_t st);
 cudaError_t launch_quantize_rows_known_amax(int64_t rows, int cols, const void* w, int64_t ld_in,
                                             uint8_t* codes, int64_t ld_out, float* amax_scale,
                                             cudaStream_t st);

@@ -122,6 +122,14 @@ bool w8_pair() {
     return e && e[0] == '1';
 }
 
+// Tensor-core groups of the 8-bit-weight entry points carry their bf16
+// activations as two E4M3 planes on the 8-bit-by-8-bit MMA (MOE_W8_PLANES,
+// read per call; 0 widens the codes to bf16 inside the GEMM instead).
+bool w8_planes() {
+    const char* e = getenv("MOE_W8_PLANES");
+    return !(e && e[0] == '0');
+}
+
 // routed code and scale pointers present and aligned; shared ones iff wanted
 moe_status check_fp8_weights(const moe_fp8_experts* w, bool shared) {
     if (!w) return MOE_ERR_INVALID_ARG;
@@ -448,6 +456,33 @@ moe_status moe_quantize_fp8_rows(int64_t rows, int64_t cols, int32_t dtype, cons
                                                 (cudaStream_t)stream));
 }
 
+// The tensor-core groups of an 8-bit-weight call with two-plane activations:
+// g.a_perm / g.a_shared hold the planes of the routed / shared rows and
+// g.sa_routed / g.sa_shared their scales; the plan is built.  Gate/up GEMM
+// (bf16 h, each row's max |h| raised from zero), h split into two planes in
+// place, down GEMM.  Groups on the 8-bit GEMV have run before (their bf16 h
+// rows, already consumed, are split along with the rest and never read).
+static cudaError_t run_tc_planes(const moe_shape& s, FfnGroups& g, const WsLayout& L, void* ws,
+                                 int64_t max_rows, DevError* err, cudaStream_t cs) {
+    FfnPlanHeader* hdr = at<FfnPlanHeader>(ws, L.plan);
+    int4* mtiles = at<int4>(ws, L.mtile_list);
+    const int64_t R = (int64_t)s.T * s.K;
+    const bool may_pair = tc_pair_possible(max_rows);
+    cudaError_t e = cudaMemsetAsync(const_cast<float*>(g.sa_h), 0, sizeof(float) * R, cs);
+    if (e == cudaSuccess && g.has_shared)
+        e = cudaMemsetAsync(const_cast<float*>(g.sa_hs), 0, sizeof(float) * s.T, cs);
+    if (e == cudaSuccess)
+        e = launch_ffn_tc_a8_gate_up(g, hdr, mtiles, L.max_mtiles, may_pair, err, cs, 2);
+    if (e == cudaSuccess)
+        e = launch_split_rows_known_amax(R, s.inter, g.h, s.inter, const_cast<float*>(g.sa_h), cs);
+    if (e == cudaSuccess && g.has_shared)
+        e = launch_split_rows_known_amax(s.T, s.inter_shared, g.h_s, s.inter_shared,
+                                         const_cast<float*>(g.sa_hs), cs);
+    if (e == cudaSuccess)
+        e = launch_ffn_tc_a8_down(g, hdr, mtiles, L.max_mtiles, may_pair, err, cs, 2);
+    return e;
+}
+
 moe_status moe_expert_ffn_fp8(const moe_shape* shape, const void* x_perm, const int32_t* offsets,
                               const moe_fp8_experts* w, void* y_perm, void* workspace,
                               size_t ws_bytes, void* stream) {
@@ -491,14 +526,27 @@ moe_status moe_expert_ffn_fp8(const moe_shape* shape, const void* x_perm, const 
     int32_t* glist = at<int32_t>(workspace, L.gemv_list);
     int4* mtiles = at<int4>(workspace, L.mtile_list);
     const int lim = gemv8_limit(s);
-    const bool pair = w8_pair();
-    e = launch_ffn_plan(g, s.dtype, hdr, glist, mtiles, L.max_mtiles, lim, pair,
-                        gemv8_small_rows(), cs);
-    if (e == cudaSuccess && lim > 0) e = launch_ffn_gemv_fp8(g, hdr, glist, lim, cs);
+    const int64_t R = (int64_t)s.T * s.K;
     // a group has at most T*K rows here (the offsets are the caller's)
-    if (e == cudaSuccess && (int64_t)s.T * s.K > lim)
-        e = launch_ffn_tc_fp8(g, hdr, mtiles, L.max_mtiles,
-                              pair && tc_pair_possible((int64_t)s.T * s.K), err, cs);
+    const bool planes = R > lim && w8_planes();
+    const bool pair = planes || w8_pair();
+    if (planes) {
+        // the rows' two planes (2d codes per row) and their scales
+        float* sc = at<float>(workspace, L.ascale);
+        g.a_perm = at<uint8_t>(workspace, L.x_perm);
+        g.sa_routed = sc + s.T;
+        g.sa_h = sc + s.T + R;
+        e = launch_split_act_rows(R, s.d, x_perm, s.d, at<uint8_t>(workspace, L.x_perm),
+                                  2 * (int64_t)s.d, sc + s.T, cs);
+    }
+    if (e == cudaSuccess)
+        e = launch_ffn_plan(g, s.dtype, hdr, glist, mtiles, L.max_mtiles, lim, pair,
+                            gemv8_small_rows(), cs);
+    if (e == cudaSuccess && lim > 0) e = launch_ffn_gemv_fp8(g, hdr, glist, lim, cs);
+    if (e == cudaSuccess && R > lim) {
+        if (planes) e = run_tc_planes(s, g, L, workspace, R, err, cs);
+        else e = launch_ffn_tc_fp8(g, hdr, mtiles, L.max_mtiles, pair && tc_pair_possible(R), err, cs);
+    }
     return cuda_status(e);
 }
 
@@ -568,7 +616,24 @@ moe_status moe_forward_fp8(const moe_shape* shape, const void* x, const void* w_
     int32_t* glist = at<int32_t>(workspace, L.gemv_list);
     int4* mtiles = at<int4>(workspace, L.mtile_list);
     const int lim = gemv8_limit(s);
-    const bool pair = w8_pair();
+    // a group has at most T rows (a token picks an expert once; the shared group has T)
+    const bool planes = s.T > lim && w8_planes();
+    const bool pair = planes || w8_pair();
+    const int64_t R = (int64_t)s.T * s.K;
+    float* sc = at<float>(workspace, L.ascale);
+    uint8_t* xq = at<uint8_t>(workspace, L.y_s);  // x planes [T][2d], read before y_s is written
+    if (planes) {
+        // tensor-core groups read two-plane rows (routed: gathered into expert
+        // order; shared: the x planes); GEMV groups read x through the row map
+        g.row_src = tok;
+        g.a_routed = x;
+        g.a_perm = x_perm;
+        g.a_shared = xq;
+        g.sa_routed = sc + s.T;
+        g.sa_shared = sc;
+        g.sa_h = sc + s.T + R;
+        g.sa_hs = sc + s.T + 2 * R;
+    }
     int32_t* counts = at<int32_t>(workspace, L.counts);
     int32_t* perm = at<int32_t>(workspace, L.perm);
     const bool fused = dispatch_plan_fusable(s);
@@ -579,7 +644,14 @@ moe_status moe_forward_fp8(const moe_shape* shape, const void* x, const void* w_
     else
         e = launch_dispatch(s, topk_idx, counts, offsets, perm, inv, tok,
                             at<int32_t>(workspace, L.blk_hist), err, cs);
-    if (e == cudaSuccess) e = launch_gather_rows(s, x, inv, x_perm, cs);
+    if (e == cudaSuccess && !planes) e = launch_gather_rows(s, x, inv, x_perm, cs);
+    if (e == cudaSuccess && planes) {
+        moe_shape s2 = s;  // rows of 2d bytes: the two planes
+        s2.d = 2 * s.d;
+        e = launch_split_act_rows(s.T, s.d, x, s.d, xq, 2 * (int64_t)s.d, sc, cs);
+        if (e == cudaSuccess)
+            e = launch_gather_codes(s2, xq, sc, inv, (uint8_t*)x_perm, sc + s.T, cs);
+    }
     if (e != cudaSuccess) return MOE_ERR_CUDA;
 
     // 3. routed and shared experts, 8-bit weights: the 8-bit GEMV for small
@@ -588,9 +660,10 @@ moe_status moe_forward_fp8(const moe_shape* shape, const void* x, const void* w_
         e = launch_ffn_plan(g, s.dtype, hdr, glist, mtiles, L.max_mtiles, lim, pair,
                             gemv8_small_rows(), cs);
     if (e == cudaSuccess && lim > 0) e = launch_ffn_gemv_fp8(g, hdr, glist, lim, cs);
-    // a group has at most T rows (a token picks an expert once; the shared group has T)
-    if (e == cudaSuccess && s.T > lim)
-        e = launch_ffn_tc_fp8(g, hdr, mtiles, L.max_mtiles, pair && tc_pair_possible(s.T), err, cs);
+    if (e == cudaSuccess && s.T > lim) {
+        if (planes) e = run_tc_planes(s, g, L, workspace, s.T, err, cs);
+        else e = launch_ffn_tc_fp8(g, hdr, mtiles, L.max_mtiles, pair && tc_pair_possible(s.T), err, cs);
+    }
     if (e != cudaSuccess) return MOE_ERR_CUDA;
 
     // 4. combine

@@ -11,7 +11,9 @@
 // Weights: one 256-thread block per row, two passes over the row (the second
 // reads it from L1/L2): a max-reduction of |w|, then 16 codes per thread and
 // step (one 16-byte store).  An offline conversion step, HBM bound.
-// Activations (8-bit-activation experts): quantize_act_rows_kernel below.
+// Activations (8-bit-activation experts): quantize_act_rows_kernel below; and
+// bf16 activations as two E4M3 planes (a code and the code of its remainder)
+// for the 8-bit-weight tensor-core path: split_*_kernel below.
 #include <cuda_fp8.h>
 
 #include "common.cuh"
@@ -213,7 +215,137 @@ quantize_rows_known_amax_kernel(const bf16* w, int64_t ld_in, uint8_t* codes, in
     if (lane == 0) amax_scale[r] = s;
 }
 
+// Two E4M3 planes per value (bf16 rows carried to the 8-bit-by-8-bit tensor
+// cores): q = v / s, hi = E4M3(q), lo = E4M3(q - value(hi)); the fp32
+// subtraction is exact.  The planes are interleaved per 128-value block --
+// [128 hi codes | 128 lo codes] -- so a block's codes take exactly the 256
+// bytes its bf16 values took, and one TMA box of 128 codes loads either plane.
+__device__ __forceinline__ void split16(const float (&f)[16], float s, uint4& hi, uint4& lo) {
+    uint32_t ph[4] = {0u, 0u, 0u, 0u}, pl[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+        const float q = f[k] / s;
+        const __nv_fp8_storage_t c = __nv_cvt_float_to_fp8(q, __NV_SATFINITE, __NV_E4M3);
+        const float vc = __half2float(__half(__nv_cvt_fp8_to_halfraw(c, __NV_E4M3)));
+        const __nv_fp8_storage_t c2 = __nv_cvt_float_to_fp8(q - vc, __NV_SATFINITE, __NV_E4M3);
+        ph[k >> 2] |= (uint32_t)c << (8 * (k & 3));
+        pl[k >> 2] |= (uint32_t)c2 << (8 * (k & 3));
+    }
+    hi = make_uint4(ph[0], ph[1], ph[2], ph[3]);
+    lo = make_uint4(pl[0], pl[1], pl[2], pl[3]);
+}
+
+// Activation rows (bf16, cols a multiple of 128 and at most 16384) to two
+// planes: quantize_act_rows_kernel's block per row with its whole row in
+// registers, the scale amax / 448, and values [16 v, 16 v + 16) of block
+// b = v / 8 written at bytes 256 b + 16 (v % 8) (hi) and 256 b + 128 + 16 (v % 8)
+// (lo) of the row's 2 * cols bytes at codes + r * ld_out.
+__global__ void __launch_bounds__(kQuantThreads)
+split_act_rows_kernel(const bf16* w, int64_t ld_in, uint8_t* codes, int64_t ld_out,
+                      float* __restrict__ scales, int cols) {
+    pdl_wait();
+    pdl_trigger();
+    __shared__ float red[kQuantThreads / 32];
+    const int64_t r = blockIdx.x;
+    const uint4* row = reinterpret_cast<const uint4*>(w + r * ld_in);
+    const int nvec = cols / 16;
+    uint4 v[kActVecs][2];
+    float amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < kActVecs; ++j) {
+        const int vi = (int)threadIdx.x + j * kQuantThreads;
+        if (vi < nvec) {
+            v[j][0] = row[2 * vi];
+            v[j][1] = row[2 * vi + 1];
+            float f[16];
+            unpack16(v[j][0], v[j][1], f);
+#pragma unroll
+            for (int k = 0; k < 16; ++k) amax = fmaxf(amax, fabsf(f[k]));
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+    __syncthreads();  // every load of the row has completed past this point
+    float m = 0.0f;
+#pragma unroll
+    for (int i = 0; i < kQuantThreads / 32; ++i) m = fmaxf(m, red[i]);
+    const float s = m > 0.0f ? m / 448.0f : 1.0f;
+    if (threadIdx.x == 0) scales[r] = s;
+    uint8_t* out = codes + r * ld_out;
+#pragma unroll
+    for (int j = 0; j < kActVecs; ++j) {
+        const int vi = (int)threadIdx.x + j * kQuantThreads;
+        if (vi < nvec) {
+            float f[16];
+            unpack16(v[j][0], v[j][1], f);
+            uint4 hi, lo;
+            split16(f, s, hi, lo);
+            uint8_t* blk = out + (int64_t)(vi >> 3) * 256 + (vi & 7) * 16;
+            *reinterpret_cast<uint4*>(blk) = hi;
+            *reinterpret_cast<uint4*>(blk + 128) = lo;
+        }
+    }
+}
+
+// Rows whose max |value| is known (raised by the producing GEMM), split into
+// two planes in place: one warp per row, four 128-value blocks per step (lane
+// l takes values 16 (l % 8) .. of block l / 8), every load of a step before
+// any store of it (__syncwarp).  A block's planes land on exactly the 256
+// bytes of its bf16 values, all loaded at this step, and later steps read
+// only later blocks, so the codes may overwrite the row.
+__global__ void __launch_bounds__(kQuantThreads)
+split_rows_known_amax_kernel(bf16* w, int64_t ld, float* amax_scale, int cols, int64_t rows) {
+    pdl_wait();
+    pdl_trigger();
+    const int lane = threadIdx.x & 31;
+    const int64_t r = (int64_t)blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5);
+    if (r >= rows) return;
+    const float m = __uint_as_float(reinterpret_cast<const uint32_t*>(amax_scale)[r]);
+    const float s = m > 0.0f ? m / 448.0f : 1.0f;
+    bf16* row = w + r * ld;
+    for (int c0 = 0; c0 < cols; c0 += 512) {
+        const int blk = c0 + (lane >> 3) * 128;    // first value of this lane's block
+        const int e = blk + (lane & 7) * 16;       // first of its 16 values
+        const bool ok = e < cols;
+        uint4 a, b;
+        if (ok) {
+            a = reinterpret_cast<const uint4*>(row + e)[0];
+            b = reinterpret_cast<const uint4*>(row + e)[1];
+        }
+        __syncwarp();  // every lane's loads of this step precede any store of it
+        if (ok) {
+            float f[16];
+            unpack16(a, b, f);
+            uint4 hi, lo;
+            split16(f, s, hi, lo);
+            uint8_t* dst = reinterpret_cast<uint8_t*>(row + blk) + (lane & 7) * 16;
+            *reinterpret_cast<uint4*>(dst) = hi;
+            *reinterpret_cast<uint4*>(dst + 128) = lo;
+        }
+    }
+    __syncwarp();  // every lane has read the max before it is replaced by the scale
+    if (lane == 0) amax_scale[r] = s;
+}
+
 }  // namespace
+
+cudaError_t launch_split_act_rows(int64_t rows, int cols, const void* w, int64_t ld_in,
+                                  uint8_t* codes, int64_t ld_out, float* scales, cudaStream_t st) {
+    if (rows <= 0) return cudaSuccess;
+    if (cols % 128 || cols > kActVecs * kQuantThreads * 16) return cudaErrorInvalidValue;
+    return launch_pdl(split_act_rows_kernel, dim3((unsigned)rows), dim3(kQuantThreads), 0, st,
+                      (const bf16*)w, ld_in, codes, ld_out, scales, cols);
+}
+
+cudaError_t launch_split_rows_known_amax(int64_t rows, int cols, void* w, int64_t ld,
+                                         float* amax_scale, cudaStream_t st) {
+    if (rows <= 0) return cudaSuccess;
+    if (cols % 128) return cudaErrorInvalidValue;
+    const int64_t blocks = (rows + kRowsPerBlock - 1) / kRowsPerBlock;
+    return launch_pdl(split_rows_known_amax_kernel, dim3((unsigned)blocks), dim3(kQuantThreads), 0,
+                      st, (bf16*)w, ld, amax_scale, cols, rows);
+}
 
 cudaError_t launch_quantize_rows_known_amax(int64_t rows, int cols, const void* w, int64_t ld_in,
                                             uint8_t* codes, int64_t ld_out, float* amax_scale,

@@ -59,7 +59,7 @@ def test_quantize_rows_of_a_3d_weight_stack(moe):
 
 # ---------------------------------------------------------------- expert FFN
 
-def _expert_ffn_case(moe, counts, d, I, seed=0):
+def _expert_ffn_case(moe, counts, d, I, seed=0, with_planes=False):
     E = len(counts)
     offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
     rows = int(offsets[-1])
@@ -76,7 +76,16 @@ def _expert_ffn_case(moe, counts, d, I, seed=0):
     assert moe.moe_get_device_error(ws) == 0
     qh = {k: host(v) for k, v in q.items()}
     ref = oracle.expert_ffn_fp8(host(x_perm), offsets, qh, dtype="bf16")
+    if with_planes:
+        return to_f64(y), ref, oracle.expert_ffn_a2(host(x_perm), offsets, qh, dtype="bf16")
     return to_f64(y), ref
+
+
+# the tensor-core groups' activation path: two E4M3 planes on the 8-bit MMA (the
+# default), or the codes widened to bf16 in the GEMM on single-SM or pair tiles
+PATHS = {"planes": {"MOE_W8_PLANES": "1"},
+         "widen": {"MOE_W8_PLANES": "0", "MOE_W8_PAIR": "0"},
+         "widen_pair": {"MOE_W8_PLANES": "0", "MOE_W8_PAIR": "1"}}
 
 
 @pytest.mark.parametrize("counts,d,I", [
@@ -86,23 +95,33 @@ def _expert_ffn_case(moe, counts, d, I, seed=0):
     ([8, 9, 0, 7, 16, 17], 128, 128),                # around the GEMV limit, narrowest shapes
     ([16, 15, 1, 33], 7168, 256),                    # DeepSeek-width rows, 16-row passes
 ])
-@pytest.mark.parametrize("w8_pair", ["0", "1"])
-def test_expert_ffn_fp8_matches_oracle(moe, counts, d, I, w8_pair, monkeypatch):
-    monkeypatch.setenv("MOE_W8_PAIR", w8_pair)
-    y, ref = _expert_ffn_case(moe, counts, d, I)
+@pytest.mark.parametrize("path", sorted(PATHS))
+def test_expert_ffn_fp8_matches_oracle(moe, counts, d, I, path, monkeypatch):
+    """Every path against the exact 8-bit-weight stage (fp64, bf16 activations);
+    the two-plane path also against the oracle's two-plane stage, which it
+    computes up to fp32 accumulation and the bf16 storage of h and y."""
+    for k, v in PATHS[path].items():
+        monkeypatch.setenv(k, v)
+    y, ref, ref2 = _expert_ffn_case(moe, counts, d, I, with_planes=True)
     assert rel_l2(y, ref) <= BF16_REL_L2
     for r in range(y.shape[0]):
         assert rel_l2(y[r], ref[r]) <= 2 * BF16_REL_L2, r
+    if path == "planes":
+        assert rel_l2(y, ref2) <= BF16_REL_L2
+        for r in range(y.shape[0]):
+            assert rel_l2(y[r], ref2[r]) <= 2 * BF16_REL_L2, r
 
 
+@pytest.mark.parametrize("planes", ["1", "0"])
 @pytest.mark.parametrize("rho", [None, "1", "1000000"])
-def test_expert_ffn_fp8_side_by_side_changes_no_bit(moe, rho, monkeypatch):
+def test_expert_ffn_fp8_side_by_side_changes_no_bit(moe, rho, planes, monkeypatch):
     """Groups on CTA-pair tiles and groups on single-SM tiles: the two tile
     shapes run on two streams at once, on the plan's split of the SMs (pushed
     to both extremes through MOE_SPLIT_RHO), with the same bits as one after
     the other (MOE_CONCURRENT=0)."""
     counts, d, I = [600, 257, 1, 129, 300, 140], 384, 640
     monkeypatch.setenv("MOE_W8_PAIR", "1")
+    monkeypatch.setenv("MOE_W8_PLANES", planes)
     monkeypatch.setenv("MOE_CONCURRENT", "0")
     y0, ref = _expert_ffn_case(moe, counts, d, I, seed=4)
     monkeypatch.setenv("MOE_CONCURRENT", "1")
@@ -164,11 +183,13 @@ def test_forward_fp8_decode_full_size(moe, gemv8, monkeypatch):
     _check_rows(y, ref["y"])
 
 
-@pytest.mark.parametrize("w8_pair", ["0", "1"])
-def test_forward_fp8_prefill_sampled_tokens(moe, w8_pair, monkeypatch):
-    """Mixtral-shaped prefill: ~1024-row groups on single-SM 8-bit tiles (default)
-    or on CTA-pair 8-bit tiles (MOE_W8_PAIR=1)."""
-    monkeypatch.setenv("MOE_W8_PAIR", w8_pair)
+@pytest.mark.parametrize("path", sorted(PATHS))
+def test_forward_fp8_prefill_sampled_tokens(moe, path, monkeypatch):
+    """Mixtral-shaped prefill: ~1024-row groups with two-plane activations on the
+    8-bit MMA (default), or widened to bf16 in the GEMM on single-SM or CTA-pair
+    tiles."""
+    for k, v in PATHS[path].items():
+        monkeypatch.setenv(k, v)
     cfg = mi.CONFIGS["mixtral_prefill_fp8"]
     L = Layer(cfg)
     y = L.forward(moe)
@@ -179,10 +200,14 @@ def test_forward_fp8_prefill_sampled_tokens(moe, w8_pair, monkeypatch):
     _check_rows(to_f64(y[torch.from_numpy(tokens).long().cuda()]), ref["y"])
 
 
-def test_forward_fp8_matches_bf16_layer_on_exact_weights(moe):
-    """Power-of-two row scales make every dequantised weight a bf16 value: the
-    fp8 layer and the bf16 layer on those weights compute the same products,
-    so their outputs agree to accumulation order."""
+@pytest.mark.parametrize("planes,tol", [("0", 2e-3), ("1", BF16_REL_L2)])
+def test_forward_fp8_matches_bf16_layer_on_exact_weights(moe, planes, tol, monkeypatch):
+    """Power-of-two row scales make every dequantised weight a bf16 value: with
+    the codes widened in the GEMM the fp8 layer and the bf16 layer on those
+    weights compute the same products, so their outputs agree to accumulation
+    order; with two-plane activations, within the planes' 2^-8 reading of x and
+    h (the bf16 layer budget)."""
+    monkeypatch.setenv("MOE_W8_PLANES", planes)
     cfg = mi.LayerConfig("fp8_exact", T=200, d=256, E=8, K=2, I=256, Is=128, weights="e4m3")
     L = Layer(cfg)
     for k in list(L.p):
@@ -200,7 +225,7 @@ def test_forward_fp8_matches_bf16_layer_on_exact_weights(moe):
     moe.moe_forward(s, L.x, L.p["w_g"], L.bias, deq["w_gate"], deq["w_up"], deq["w_down"],
                     deq["ws_gate"], deq["ws_up"], deq["ws_down"], ybf, ws)
     torch.cuda.synchronize()
-    assert rel_l2(y8, to_f64(ybf)) <= 2e-3
+    assert rel_l2(y8, to_f64(ybf)) <= tol
 
 
 def test_forward_fp8_zero_tokens_is_a_no_op(moe):
@@ -210,9 +235,12 @@ def test_forward_fp8_zero_tokens_is_a_no_op(moe):
     moe.moe_forward_fp8(s, None, L.p["w_g"], None, moe.make_fp8_experts(L.p), None, None)
 
 
-def test_fp8_stalled_copy_times_out_and_the_context_survives(moe, monkeypatch):
-    """No raw weight tile is ever requested: the converters' and the MMA's
-    bounded waits run out, the kernel records MOE_ERR_TIMEOUT and returns."""
+@pytest.mark.parametrize("planes", ["1", "0"])
+def test_fp8_stalled_copy_times_out_and_the_context_survives(moe, planes, monkeypatch):
+    """No tile is ever requested: the MMA's bounded waits (and, with the codes
+    widened in the GEMM, the converters') run out, the kernel records
+    MOE_ERR_TIMEOUT and returns."""
+    monkeypatch.setenv("MOE_W8_PLANES", planes)
     cfg = mi.LayerConfig("fp8_stall", T=64, d=256, E=4, K=2, I=256, Is=128, weights="e4m3")
     L = Layer(cfg)
     monkeypatch.setenv("MOE_TC_TIMEOUT_MS", "50")
