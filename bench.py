@@ -163,11 +163,19 @@ def launches_per_forward(cfg, gemv_limit: int = 0) -> int:
         return router + disp_plan + 1 + 1 + (2 if pair else 1) + (2 if cfg.Is else 1) \
             + (2 if pair else 1) + 1
     if cfg.weights == "e4m3":
-        # router + top-K, 3 dispatch kernels, row gather, plan, the 8-bit GEMV
-        # (gate/up and down for each of its two group lists), the tcgen05
-        # gate/up and down when a group can exceed the GEMV limit, combine
+        # router + top-K, 3 dispatch kernels and the plan, the 8-bit GEMV
+        # (gate/up and down for each of its two group lists), and when a group
+        # can exceed the GEMV limit: with two-plane activations (the default)
+        # the x split and the plane gather, the tcgen05 gate/up, the h split
+        # (+ h_s), the tcgen05 down -- gate/up and down twice when a group can
+        # take pair tiles; with the codes widened in the GEMM, the row gather
+        # and one gate/up and one down; combine
         limit = int(os.environ.get("MOE_GEMV8_MAX_ROWS", "8"))
         gemv = (2 if limit > 0 else 0) + (2 if limit > 8 else 0)
+        if cfg.T > limit and os.environ.get("MOE_W8_PLANES", "1") != "0":
+            pair = cfg.T > 128
+            tc = 2 * (2 if pair else 1) + (2 if cfg.Is else 1)
+            return router + disp_plan + 2 + gemv + tc + 1
         tc = 2 if cfg.T > limit else 0
         return router + disp_plan + 1 + gemv + tc + 1
     need_tc = cfg.dtype == "bf16" and cfg.T > gemv_limit
@@ -536,7 +544,8 @@ def stage_traffic(workload: str):
 def tensor_peak(cfg, peaks) -> tuple:
     """Dense tensor peak for the dtype the expert GEMMs multiply in: bf16 as
     measured, or (8-bit activations: E4M3 x E4M3) the measured bf16 peak times
-    the nominal fp8 / bf16 ratio 4.5 / 2.25 = 2."""
+    the nominal fp8 / bf16 ratio 4.5 / 2.25 = 2.  Two-plane activations run two
+    E4M3 MMAs per bf16 one, the same tensor time: the bf16 peak."""
     if cfg.acts == "e4m3":
         return 2.0 * peaks["bf16_tflops"], (f"fp8 dense = 2 x measured bf16 burst "
                                             f"(nominal ratio), {peaks['source']}")
@@ -552,10 +561,13 @@ def stage_roofline(cfg, stage, peaks) -> dict:
     gbs = stage["bytes"] / sec / 1e9
     t_peak, t_kind = tensor_peak(cfg, peaks)
     t_frac, h_frac = tflops / t_peak, gbs / peaks["hbm_gbs"]
+    planes = os.environ.get("MOE_W8_PLANES", "1") != "0"
     kernel = ("expert FFN stage: tcgen05 gate/up GEMM (SiLU*mul epilogue) + tcgen05 down GEMM "
               + ("on E4M3 weights and E4M3 activations (kind::f8f6f4, + x and h quantisers)"
                  if cfg.acts == "e4m3" else
-                 "on E4M3 weights widened in-kernel" if cfg.weights == "e4m3" else
+                 ("on E4M3 weights with bf16 activations as two E4M3 planes (kind::f8f6f4, "
+                  "+ x and h splits)" if planes else "on E4M3 weights widened in-kernel")
+                 if cfg.weights == "e4m3" else
                  "(+ plan, empty GEMV launches)"))
     common = {"traffic": stage_traffic(cfg.name),
               "traffic_unit": "bytes per launch pair (DRAM read + write, ncu)",
