@@ -183,8 +183,12 @@ def launches_per_forward(cfg, gemv_limit: int = 0) -> int:
     gemv = cfg.dtype == "f32" or gemv_limit > 0
     pair_min = int(os.environ.get("MOE_PAIR_MIN_ROWS", "0"))
     pair = need_tc and (cfg.T >= pair_min if pair_min > 0 else cfg.T > 128)
+    # small batches with a shared expert: its gate/up and down in two launches of
+    # their own (beside the routing, on a side stream)
+    apart = (2 if need_tc and not gemv and cfg.Is and not pair
+             and cfg.T <= int(os.environ.get("MOE_SHARED_APART", "0")) else 0)
     return (router + disp_plan + (1 if gather else 0) + (2 if gemv else 0) + (2 if need_tc else 0)
-            + (2 if pair else 0) + 1)
+            + (2 if pair else 0) + apart + 1)
 
 
 # --------------------------------------------------------------------------- helpers

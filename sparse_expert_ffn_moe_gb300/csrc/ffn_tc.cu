@@ -1425,8 +1425,15 @@ int band_pair() {
 }
 
 // Single tiles of at most this many rows run swapped (MOE_SWAP_MAX_ROWS, read
-// per call; 0 turns it off; capped at 64, the largest swapped N).
-int swap_max_rows() {
+// per call; 0 turns it off; capped at 64, the largest swapped N) -- in calls
+// where some group can have more rows (max_group_rows > 64, or unknown).  When
+// every group is small the GEMMs stream weights, HBM bound, and two narrow
+// MMAs per 16-deep slice cost more issue latency than one wide one: measured
+// on DeepSeek-V3 decode, expert stage 0.771 ms swapped vs 0.758 ms not, T=64
+// 2.810 vs 2.792 ms layer.  With large groups beside them (skewed prefill) the
+// tail's saved tensor energy buys clock under the power cap instead.
+int swap_max_rows(int max_group_rows = 0) {
+    if (max_group_rows > 0 && max_group_rows <= kSwapMaxRows) return 0;
     const char* s = getenv("MOE_SWAP_MAX_ROWS");
     const int x = s ? atoi(s) : kSwapMaxRows;
     return x < 0 ? 0 : (x > kSwapMaxRows ? kSwapMaxRows : x);
@@ -1567,6 +1574,81 @@ bool tc_pair_possible(int64_t max_rows) {
     return pm > 0 ? max_rows >= pm : max_rows > Shape<false>::kTileRows;
 }
 
+// Batches of at most this many tokens run the shared expert apart
+// (MOE_SHARED_APART, read per call).  Off (0) by default: measured on GB300
+// (interleaved, 4 x 100 calls each) it is slower -- T=1 197 vs 160 us,
+// DeepSeek-V3 decode 806 vs 800 us, T=64 unchanged: the shared expert's SMs
+// hold back some units of the persistent routed grid, whose tiles are
+// assigned by unit, so the routed GEMM ends later than the routing it hid.
+constexpr int kSharedApartMaxT = 0;
+int shared_apart_max_tokens() {
+    const char* s = getenv("MOE_SHARED_APART");
+    const int x = s ? atoi(s) : kSharedApartMaxT;
+    return x < 0 ? 0 : (x > Shape<false>::kTileRows ? Shape<false>::kTileRows : x);
+}
+
+// The shared expert of a small batch in two dense launches (single-SM tiles,
+// swapped for <= 64 rows) on the side stream, forked off st: it reads only x
+// and its own weights, so it runs while the router, the dispatch and the
+// gather of the routed rows run on st -- on a handful of SMs, streaming its
+// weights while HBM would otherwise sit idle behind those latency-bound
+// kernels.  The grouped launches then skip the shared group (shared_apart),
+// and join_shared_apart() makes st wait for y_s before the combine.  Returns
+// false (nothing enqueued) when no side stream can be had (first use inside a
+// stream capture): the caller keeps the shared group in the grouped launches.
+bool launch_shared_apart(const FfnGroups& g, DevError* err, cudaStream_t st, cudaError_t* status) {
+    *status = cudaSuccess;
+    if (!g.has_shared || g.T > Shape<false>::kTileRows) return false;
+    SideStream* side = side_stream(st);
+    if (!side) return false;
+    cudaError_t e = fork_side(side, st);
+    if (e != cudaSuccess) { *status = e; return true; }
+    TcParams p{};
+    bool ok = make_amaps(p.a[1], g.a_shared, g.T, g.d);
+    ok &= make_map(&p.b0[1], g.ws_gate, g.Is, g.d, 128);
+    ok &= make_map(&p.b1[1], g.ws_up, g.Is, g.d, 128);
+    TcParams q{};
+    ok &= make_amaps(q.a[1], g.h_s, g.T, g.Is);
+    ok &= make_wmaps(q, 1, g.ws_down, g.d, g.Is);
+    if (!ok) { *status = cudaErrorInvalidValue; return true; }
+    for (TcParams* t : {&p, &q}) {
+        for (int b = 0; b < kABoxes; ++b) t->a[0][b] = t->a[1][b];
+        t->ag = t->a[1][0];
+        t->half_tiles = half_tiles();
+        t->swap_max_rows = swap_max_rows(g.T);
+        t->hdr = nullptr;
+        t->mtiles = nullptr;
+        t->dense_rows = g.T;
+        t->err = err;
+        t->timeout_ns = timeout_ns();
+        t->test_stall = test_stall();
+    }
+    // gate/up: h_s = SiLU(x Ws_gate^T) * (x Ws_up^T)
+    p.b0[0] = p.b0[1]; p.b1[0] = p.b1[1]; p.bw[0] = p.bw[1] = p.b0[1];
+    p.g64[0] = p.g64[1] = p.b0[1]; p.u64[0] = p.u64[1] = p.b1[1];
+    p.NB = (g.Is + BN / 2 - 1) / (BN / 2);
+    p.n_out[0] = p.n_out[1] = g.Is;
+    p.kdim[0] = p.kdim[1] = g.d;
+    p.out[0] = p.out[1] = g.h_s;
+    p.ld_out[0] = p.ld_out[1] = g.Is;
+    // down: y_s = h_s Ws_down^T
+    q.b0[0] = q.b0[1]; q.bw[0] = q.bw[1]; q.b1[0] = q.b1[1] = q.b0[1];
+    q.NB = (g.d + BN - 1) / BN;
+    q.n_out[0] = q.n_out[1] = g.d;
+    q.kdim[0] = q.kdim[1] = g.Is;
+    q.out[0] = q.out[1] = g.y_s;
+    q.ld_out[0] = q.ld_out[1] = g.d;
+    e = launch_tc<EPI_SWIGLU, false>(p, side->s);
+    if (e == cudaSuccess) e = launch_tc<EPI_STORE_BF16, false>(q, side->s);
+    *status = e;
+    return true;
+}
+
+cudaError_t join_shared_apart(cudaStream_t st) {
+    SideStream* side = side_stream(st);
+    return side ? join_side(side, st) : cudaErrorInvalidResourceHandle;
+}
+
 // The combine fused into the shared expert's down projection (MOE_FUSED_COMBINE=1,
 // read per call).  Off by default: measured on GB300 (interleaved A/B, the same
 // box) it is slower on every workload -- Zipf prefill 10.97 vs 10.44 ms,
@@ -1581,7 +1663,7 @@ bool fused_combine_enabled() {
 
 cudaError_t launch_ffn_tc(const FfnGroups& g, const FfnPlanHeader* hdr, const int4* mtile_list,
                           int max_mtiles, bool may_pair, DevError* err, cudaStream_t st,
-                          const CombineArgs* cmb) {
+                          const CombineArgs* cmb, bool shared_apart) {
     const int64_t R = g.n_routed_rows;
     const int4* single_list = mtile_list;
     const int4* pair_list = mtile_list + max_mtiles;
@@ -1618,7 +1700,8 @@ cudaError_t launch_ffn_tc(const FfnGroups& g, const FfnPlanHeader* hdr, const in
         p.g64[1] = p.g64[0]; p.u64[1] = p.u64[0];
     }
     p.half_tiles = half_tiles();
-    p.swap_max_rows = swap_max_rows();
+    p.swap_max_rows = swap_max_rows(g.max_group_rows);
+    p.skip_shared = shared_apart ? 1 : 0;  // the shared expert runs in its own launches
     p.bw[0] = p.b0[0]; p.bw[1] = p.b0[1];  // unused by the SWIGLU epilogue
     if (!ok) return cudaErrorInvalidValue;
     p.hdr = hdr;
@@ -1657,7 +1740,7 @@ cudaError_t launch_ffn_tc(const FfnGroups& g, const FfnPlanHeader* hdr, const in
     q.b1[0] = q.b0[0]; q.b1[1] = q.b0[1];
     if (!ok) return sh.finish(cudaErrorInvalidValue);
     q.half_tiles = half_tiles();
-    q.swap_max_rows = swap_max_rows();
+    q.swap_max_rows = swap_max_rows(g.max_group_rows);
     q.hdr = hdr;
     q.E = g.E;
     q.max_mtiles = max_mtiles;
@@ -1671,8 +1754,8 @@ cudaError_t launch_ffn_tc(const FfnGroups& g, const FfnPlanHeader* hdr, const in
     q.err = err;
     q.timeout_ns = timeout_ns();
     q.test_stall = test_stall();
-    const bool fuse = cmb != nullptr && g.has_shared;
-    q.skip_shared = fuse ? 1 : 0;
+    const bool fuse = cmb != nullptr && g.has_shared && !shared_apart;
+    q.skip_shared = (fuse || shared_apart) ? 1 : 0;
     // side by side, the down grids start only when their stream's gate/up grid ended
     e = launch_shapes<EPI_STORE_BF16>(q, pair_list, single_list, may_pair, sh, sh.side == nullptr, small);
     e = sh.finish(e);

@@ -156,9 +156,18 @@ bool fused_combine_enabled();  // MOE_FUSED_COMBINE (read per call)
 // launches are skipped).  cmb (with a shared group): the routed down launches
 // skip the shared group, whose down projection then runs as one dense launch
 // that also sums the routed rows into y -- no separate combine.
+// shared_apart: the shared expert ran in launch_shared_apart's launches, and
+// the grouped launches skip its group.
 cudaError_t launch_ffn_tc(const FfnGroups& g, const FfnPlanHeader* hdr, const int4* mtile_list,
                           int max_mtiles, bool may_pair, DevError* err, cudaStream_t st,
-                          const CombineArgs* cmb = nullptr);
+                          const CombineArgs* cmb = nullptr, bool shared_apart = false);
+// The shared expert of a batch of at most shared_apart_max_tokens() tokens in
+// its own two launches on a side stream forked off st (true: enqueued, *status
+// tells whether it worked; false: nothing enqueued); join_shared_apart makes
+// st wait for it.
+int shared_apart_max_tokens();
+bool launch_shared_apart(const FfnGroups& g, DevError* err, cudaStream_t st, cudaError_t* status);
+cudaError_t join_shared_apart(cudaStream_t st);
 cudaError_t launch_router_tc(const moe_shape& s, const void* x, const void* w_g, float* scores,
                              DevError* err, cudaStream_t st);
 // E4M3 expert weights with row scales (g.s_* set); bf16 activations; the

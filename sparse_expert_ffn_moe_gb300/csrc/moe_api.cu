@@ -373,6 +373,28 @@ moe_status moe_forward(const moe_shape* shape, const void* x, const void* w_g, c
     cudaError_t e = cudaMemsetAsync(err, 0, kErrBlockBytes, cs);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
 
+    // 0. small batches: the shared expert (it reads only x) starts on a side
+    //    stream, beside the routing and dispatch below
+    FfnGroups g{};
+    g.E = s.E;
+    g.has_shared = shared ? 1 : 0;
+    g.d = s.d;
+    g.I = s.inter;
+    g.Is = s.inter_shared;
+    g.T = s.T;
+    g.a_shared = x;
+    g.ws_gate = ws_gate;
+    g.ws_up = ws_up;
+    g.ws_down = ws_down;
+    g.h_s = at<void>(workspace, L.h_s);
+    g.y_s = at<void>(workspace, L.y_s);
+    bool apart = false;
+    if (need_tc && shared && !gemv_possible(s) && s.T <= shared_apart_max_tokens() &&
+        !tc_pair_possible(s.T)) {
+        apart = launch_shared_apart(g, err, cs, &e);
+        if (e != cudaSuccess) return MOE_ERR_CUDA;
+    }
+
     // 1. router scores, top-K, softmax over the K
     int32_t* topk_idx = at<int32_t>(workspace, L.topk_idx);
     float* topk_w = at<float>(workspace, L.topk_w);
@@ -390,30 +412,17 @@ moe_status moe_forward(const moe_shape* shape, const void* x, const void* w_g, c
     // copy, which is only built when a group can be that large (a group has at
     // most T rows: a token picks an expert once).
     void* x_perm = (need_tc && s.T > tc_gather_max_rows()) ? at<void>(workspace, L.x_perm) : nullptr;
-    FfnGroups g{};
-    g.E = s.E;
-    g.has_shared = shared ? 1 : 0;
-    g.d = s.d;
-    g.I = s.inter;
-    g.Is = s.inter_shared;
     g.n_routed_rows = s.T * s.K;
-    g.T = s.T;
     g.max_group_rows = s.T;  // a token picks an expert once; the shared group has T rows
     g.offsets = offsets;
     g.row_src = tok;
     g.a_routed = x;
     g.a_perm = x_perm;
-    g.a_shared = x;
     g.w_gate = w_gate;
     g.w_up = w_up;
     g.w_down = w_down;
-    g.ws_gate = ws_gate;
-    g.ws_up = ws_up;
-    g.ws_down = ws_down;
     g.h = at<void>(workspace, L.h);
-    g.h_s = at<void>(workspace, L.h_s);
     g.y = at<void>(workspace, L.y_perm);
-    g.y_s = at<void>(workspace, L.y_s);
     FfnPlanHeader* hdr = at<FfnPlanHeader>(workspace, L.plan);
     int32_t* glist = at<int32_t>(workspace, L.gemv_list);
     int4* mtiles = at<int4>(workspace, L.mtile_list);
@@ -439,9 +448,10 @@ moe_status moe_forward(const moe_shape* shape, const void* x, const void* w_g, c
     // a group has at most T rows (a token picks an expert once)
     if (e == cudaSuccess && need_tc)
         e = launch_ffn_tc(g, hdr, mtiles, L.max_mtiles, tc_pair_possible(s.T), err, cs,
-                          fuse ? &cmb : nullptr);
+                          fuse && !apart ? &cmb : nullptr, apart);
+    if (e == cudaSuccess && apart) e = join_shared_apart(cs);  // y_s is ready
     if (e != cudaSuccess) return MOE_ERR_CUDA;
-    if (fuse) return MOE_OK;
+    if (fuse && !apart) return MOE_OK;
     return cuda_status(launch_combine(s, g.y, inv, topk_w, shared ? g.y_s : nullptr, y, cs));
 }
 

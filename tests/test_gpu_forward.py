@@ -313,3 +313,36 @@ def test_fused_combine(moe, T, K, monkeypatch):
     _check(cfg, y0, ref)
     _check(cfg, y1, ref)
     assert rel_l2(y1, y0) <= 4e-3
+
+
+@pytest.mark.parametrize("T", [1, 8, 33, 64])
+def test_shared_expert_apart_changes_no_bit(moe, T, monkeypatch):
+    """Batches of at most 64 tokens run the shared expert in two launches of its
+    own on a side stream, beside the routing and dispatch; MOE_SHARED_APART=0
+    keeps it in the grouped launches.  Each of its tiles is computed the same
+    way either way: identical bits, eager and replayed from a CUDA graph, and
+    parity with the oracle."""
+    cfg = mi.LayerConfig(f"apart_T{T}", T=T, d=1024, E=64, K=8, I=256, Is=384, seed=37)
+    L = Layer(cfg)
+    L.x = _clean_x(L)
+    s = L.shape(moe)
+    ws = moe.alloc_workspace(s)
+    monkeypatch.setenv("MOE_SHARED_APART", "0")
+    y0 = L.forward(moe, ws=ws)
+    monkeypatch.setenv("MOE_SHARED_APART", "64")
+    y1 = L.forward(moe, ws=ws)
+    assert torch.equal(y0, y1)
+    p = L.p
+    y2 = torch.zeros_like(y1)
+    st = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g, stream=st):
+        moe.moe_forward(s, L.x, p["w_g"], None, p["w_gate"], p["w_up"], p["w_down"],
+                        p["ws_gate"], p["ws_up"], p["ws_down"], y2, ws, stream=st)
+    g.replay()
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_error(ws) == 0
+    assert torch.equal(y2, y1)
+    ref = oracle.forward(host(L.x), L.hp, cfg.K, dtype=cfg.dtype)["y"]
+    _check(cfg, to_f64(y1), ref)
