@@ -179,7 +179,10 @@ def launches_per_forward(cfg, gemv_limit: int = 0) -> int:
         tc = 2 if cfg.T > limit else 0
         return router + disp_plan + 1 + gemv + tc + 1
     need_tc = cfg.dtype == "bf16" and cfg.T > gemv_limit
-    gather = need_tc and cfg.T > int(os.environ.get("MOE_GATHER_MAX_ROWS", "0"))
+    # the permuted copy of the routed rows: not made when every row of the batch is
+    # gathered inside the GEMM (by default, batches of at most 16 tokens)
+    gather_max = int(os.environ.get("MOE_GATHER_MAX_ROWS", "16" if cfg.T <= 16 else "0"))
+    gather = need_tc and cfg.T > gather_max
     gemv = cfg.dtype == "f32" or gemv_limit > 0
     pair_min = int(os.environ.get("MOE_PAIR_MIN_ROWS", "0"))
     pair = need_tc and (cfg.T >= pair_min if pair_min > 0 else cfg.T > 128)

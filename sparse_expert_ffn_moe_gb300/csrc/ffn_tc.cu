@@ -197,11 +197,15 @@ constexpr int kSwapMaxRows = 64;
 // Routed rows of at most MOE_GATHER_MAX_ROWS per CTA can be gathered from x
 // with tile::gather4 inside the GEMM instead of being copied into expert order
 // first; larger row blocks load the contiguous permuted copy.  Measured on
-// GB300 (interleaved A/B, every workload): gathering is never faster -- 4-7%
-// slower on prefill shapes, even at <= 32 rows per CTA (128 rows per CTA
-// took ~2.5x the MMA time per stage) -- so the default is 0 (off); the path
-// stays selectable and parity-tested.
+// GB300 (interleaved A/B): on prefill shapes gathering is 4-7% slower, even at
+// <= 32 rows per CTA (128 rows per CTA took ~2.5x the MMA time per stage), and
+// 1% slower at T=64; for batches of a few tokens, where it also spares the
+// separate copy launch, it is faster (T=1 161.0 -> 157.6 us, DeepSeek-V3
+// decode 801.3 -> 795.3 us).  Default: every routed row of a batch of at most
+// kGatherSmallT tokens is gathered in the GEMM (no permuted copy is made);
+// larger batches use the copy.
 constexpr int kGatherMaxRows = 0;
+constexpr int kGatherSmallT = 16;
 // Weight-streaming cost of a single-tile group, in hundredths of an MMA step
 // per weight K step (the plan's SM split between the two tile shapes).
 constexpr int kSplitRho = 150;
@@ -1395,10 +1399,11 @@ bool tc_available() {
 int tc_tile_rows(bool pair) { return pair ? Shape<true>::kTileRows : Shape<false>::kTileRows; }
 
 // Read on every call: MOE_GATHER_MAX_ROWS (0 disables the in-GEMM gather;
-// capped at 128, the rows of one CTA's block).
-int tc_gather_max_rows() {
+// capped at 128, the rows of one CTA's block); unset, kGatherSmallT for a
+// batch of at most that many tokens T (a group has at most T rows) and 0 above.
+int tc_gather_max_rows(int64_t T) {
     const char* s = getenv("MOE_GATHER_MAX_ROWS");
-    const int x = s ? atoi(s) : kGatherMaxRows;
+    const int x = s ? atoi(s) : (T <= kGatherSmallT ? kGatherSmallT : kGatherMaxRows);
     return x < 0 ? 0 : (x > BMC ? BMC : x);
 }
 
@@ -1678,7 +1683,7 @@ cudaError_t launch_ffn_tc(const FfnGroups& g, const FfnPlanHeader* hdr, const in
         if (g.a_perm) ok &= make_amaps(p.a[0], g.a_perm, R, g.d);
         else ok &= make_amaps(p.a[0], g.a_routed, g.T, g.d);
         p.row_src = g.row_src;
-        p.gather_max = tc_gather_max_rows();
+        p.gather_max = tc_gather_max_rows(g.T);
     } else {
         ok &= make_amaps(p.a[0], g.a_routed, R, g.d);
         p.ag = p.a[0][0];

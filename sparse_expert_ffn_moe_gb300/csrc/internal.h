@@ -44,7 +44,7 @@ struct FfnGroups {
     const void* a_routed;    // rows of x_perm (or x when row_src is set)
     const void* a_perm;      // contiguous permuted rows for the tensor-core path's
                              // large row blocks when row_src is set (or null when
-                             // no group can exceed tc_gather_max_rows())
+                             // no group can exceed tc_gather_max_rows(T))
     const void* a_shared;    // x [T][d] (shared group input)
     const void* w_gate;      // [E][I][d]
     const void* w_up;
@@ -142,7 +142,8 @@ int tc_tile_rows(bool pair);  // rows per tensor-core m-tile (single-SM or CTA p
 int tc_pair_min_rows();       // fixed pair threshold (0: the plan picks the cheaper shape)
 int tc_split_rho();          // > 0: the two tile shapes run side by side (plan's SM split cost)
 bool tc_pair_possible(int64_t max_rows);  // a group of at most max_rows rows may take pair tiles
-int tc_gather_max_rows();     // per-CTA routed row blocks up to this size are gathered from x
+// per-CTA routed row blocks up to this size are gathered from x (batch of T tokens)
+int tc_gather_max_rows(int64_t T);
 // The combine fused into the shared expert's down projection (launch_ffn_tc
 // with a shared group): each token's routed rows and weights, and the output.
 struct CombineArgs {

@@ -408,10 +408,10 @@ moe_status moe_forward(const moe_shape* shape, const void* x, const void* w_g, c
     int32_t* tok = at<int32_t>(workspace, L.tok_of);
     // Both expert paths read routed rows from x through the row -> token map
     // (the tensor-core path with TMA gather4 for row blocks of at most
-    // tc_gather_max_rows() rows).  Larger blocks need the contiguous permuted
+    // tc_gather_max_rows(T) rows).  Larger blocks need the contiguous permuted
     // copy, which is only built when a group can be that large (a group has at
     // most T rows: a token picks an expert once).
-    void* x_perm = (need_tc && s.T > tc_gather_max_rows()) ? at<void>(workspace, L.x_perm) : nullptr;
+    void* x_perm = (need_tc && s.T > tc_gather_max_rows(s.T)) ? at<void>(workspace, L.x_perm) : nullptr;
     g.n_routed_rows = s.T * s.K;
     g.max_group_rows = s.T;  // a token picks an expert once; the shared group has T rows
     g.offsets = offsets;

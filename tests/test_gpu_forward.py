@@ -346,3 +346,22 @@ def test_shared_expert_apart_changes_no_bit(moe, T, monkeypatch):
     assert torch.equal(y2, y1)
     ref = oracle.forward(host(L.x), L.hp, cfg.K, dtype=cfg.dtype)["y"]
     _check(cfg, to_f64(y1), ref)
+
+
+@pytest.mark.parametrize("T", [1, 8, 16, 17])
+def test_small_batches_gather_inside_the_gemm_with_the_same_bits(moe, T, monkeypatch):
+    """Batches of at most 16 tokens load their routed rows straight from x inside
+    the GEMM (tile::gather4 through the row -> token map) and make no permuted
+    copy; MOE_GATHER_MAX_ROWS=0 forces the copy.  The MMA sees the same rows:
+    identical bits, and parity with the oracle (T = 17 takes the copy by
+    default)."""
+    cfg = mi.LayerConfig(f"gather_T{T}", T=T, d=1024, E=64, K=8, I=256, Is=256, seed=41)
+    L = Layer(cfg)
+    L.x = _clean_x(L)
+    monkeypatch.setenv("MOE_GATHER_MAX_ROWS", "0")
+    y0 = L.forward(moe)
+    monkeypatch.delenv("MOE_GATHER_MAX_ROWS")
+    y1 = L.forward(moe)
+    assert torch.equal(y0, y1)
+    ref = oracle.forward(host(L.x), L.hp, cfg.K, dtype=cfg.dtype)["y"]
+    _check(cfg, to_f64(y1), ref)
