@@ -806,8 +806,10 @@ def run_stage_pool(args):
     counts = pool_counts(moe, cfg, args.stage_pool)
     E, rows = len(counts), sum(counts)
     pcfg = mi.LayerConfig(f"{cfg.name}_pool{E}", T=rows, d=cfg.d, E=E, K=1, I=cfg.I,
-                          dtype=cfg.dtype, seed=cfg.seed)
-    p = mi.make_weights(pcfg, "cuda", only={"w_gate", "w_up", "w_down"})
+                          dtype=cfg.dtype, weights=cfg.weights, acts=cfg.acts, seed=cfg.seed)
+    p = mi.make_weights(pcfg, "cuda", only={"w_gate", "w_up", "w_down", "s_gate", "s_up",
+                                            "s_down"})
+    fp8 = moe.make_fp8_experts(p) if cfg.weights == "e4m3" else None
     x_perm = mi.normal((rows, cfg.d), 1.0, cfg.dtype, "cuda", cfg.seed, "x_perm")
     y_perm = torch.empty_like(x_perm)
     offsets = torch.tensor([0] + list(np.cumsum(counts)), dtype=torch.int32, device="cuda")
@@ -817,8 +819,13 @@ def run_stage_pool(args):
     torch.cuda.synchronize()
 
     def run():
-        moe.moe_expert_ffn(s, x_perm, offsets, p["w_gate"], p["w_up"], p["w_down"], y_perm, ws,
-                           stream=st)
+        if cfg.acts == "e4m3":
+            moe.moe_expert_ffn_w8a8(s, x_perm, offsets, fp8, y_perm, ws, stream=st)
+        elif fp8 is not None:
+            moe.moe_expert_ffn_fp8(s, x_perm, offsets, fp8, y_perm, ws, stream=st)
+        else:
+            moe.moe_expert_ffn(s, x_perm, offsets, p["w_gate"], p["w_up"], p["w_down"], y_perm,
+                               ws, stream=st)
     for _ in range(max(3, args.warmup)):
         run()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
