@@ -532,8 +532,12 @@ def time_expert_ffn(moe, cfg, x, p, bias, stream, steps: int, n_active: int) -> 
 # ncu capture per workload, valid only for the ffn_tc.cu source it was taken on
 # (sha256 prefix).
 STAGE_TRAFFIC = {
-    "mixtral_prefill": {"bytes": 4581865984, "ffn_tc_sha256": "68710359d65ad885"},
-    "mixtral_prefill_w8a8": {"bytes": 2285430016, "ffn_tc_sha256": "68710359d65ad885"},
+    # the four GEMM launches of one stage call (pair and single gate/up, pair and single down)
+    "dsv3_prefill_zipf": {"bytes": 9988049664 + 491900928 + 11163724288 + 44581888
+                          + 2670783744 + 1703299072 + 5510320384 + 154845696,
+                          "ffn_tc_sha256": "756cd63a7aadaa33"},
+    "mixtral_prefill": {"bytes": 2406684160 + 229825280 + 45312 + 1476628480 + 62856704 + 40704,
+                        "ffn_tc_sha256": "756cd63a7aadaa33"},
 }
 
 
