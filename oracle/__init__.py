@@ -82,6 +82,11 @@ def bind(lib):
     lib.oracle_forward_tokens_a2.argtypes = lib.oracle_forward_tokens_w8a8.argtypes
     lib.oracle_expert_ffn_a2.argtypes = lib.oracle_expert_ffn_w8a8.argtypes
     lib.oracle_split_e4m3_rows.argtypes = [i64, i64, i32, vp, vp, vp, vp]
+    lib.oracle_quantize_fp8_blocks.argtypes = lib.oracle_quantize_fp8_rows.argtypes
+    lib.oracle_expert_ffn_fp8_blocks.argtypes = lib.oracle_expert_ffn_fp8.argtypes
+    lib.oracle_expert_ffn_a2_blocks.argtypes = lib.oracle_expert_ffn_w8a8.argtypes
+    lib.oracle_forward_tokens_fp8_blocks.argtypes = lib.oracle_forward_tokens_fp8.argtypes
+    lib.oracle_forward_tokens_a2_blocks.argtypes = lib.oracle_forward_tokens_w8a8.argtypes
     for f in ("oracle_route", "oracle_permute", "oracle_expert_ffn", "oracle_combine",
               "oracle_shared_ffn", "oracle_forward", "oracle_forward_tokens",
               "oracle_expert_ffn_fp8", "oracle_forward_tokens_fp8", "oracle_e4m3_decode",
@@ -312,6 +317,26 @@ def quantize_fp8_rows(w, dtype: str = "f32"):
     return codes, scales
 
 
+FP8_BLOCK = 128  # side of a square weight-scale block
+
+
+def quantize_fp8_blocks(w, dtype: str = "f32"):
+    """Block-scaled E4M3 quantisation of a [..., cols] matrix taken as one
+    stacked [rows][cols] matrix (rows = the product of the leading sizes): one
+    scale per 128 x 128 block.  Returns (codes uint8 of w's shape, scales
+    float32 [ceil(rows/128)][ceil(cols/128)])."""
+    lib = _load()
+    w = _in(w, dtype)
+    cols = w.shape[-1]
+    rows = w.size // cols
+    B = FP8_BLOCK
+    codes = np.zeros(w.shape, np.uint8)
+    scales = np.zeros(((rows + B - 1) // B, (cols + B - 1) // B), np.float32)
+    _check(lib.oracle_quantize_fp8_blocks(rows, cols, _DT[dtype], _ptr(w), _ptr(codes),
+                                          _ptr(scales)), "oracle_quantize_fp8_blocks")
+    return codes, scales
+
+
 _FP8_NAMES = ("w_gate", "w_up", "w_down", "ws_gate", "ws_up", "ws_down")
 
 
@@ -326,20 +351,23 @@ def _fp8_weights(q: dict):
     return out
 
 
-def expert_ffn_fp8(x_perm, offsets, q: dict, dtype: str = "bf16", threads: int = 0):
+def expert_ffn_fp8(x_perm, offsets, q: dict, dtype: str = "bf16", threads: int = 0,
+                   blocks: bool = False):
     """SwiGLU per expert with E4M3 weights (q: w_gate, w_up, w_down codes and
-    s_gate, s_up, s_down row scales).  Returns y_perm [rows, d] f64."""
+    s_gate, s_up, s_down row scales, or with blocks=True the 128 x 128 block
+    scales of quantize_fp8_blocks).  Returns y_perm [rows, d] f64."""
     lib = _load()
+    fname = "oracle_expert_ffn_fp8_blocks" if blocks else "oracle_expert_ffn_fp8"
     x_perm = _in(x_perm, dtype)
     offsets = _arr(offsets, np.int32)
     w = _fp8_weights(q)
     E, I, d = w["w_gate"].shape
     rows = int(offsets[E])
     y = np.zeros((max(rows, 0), d), np.float64)
-    _check(lib.oracle_expert_ffn_fp8(
+    _check(getattr(lib, fname)(
         d, E, I, _DT[dtype], _ptr(x_perm), _ptr(offsets), _ptr(w["w_gate"]), _ptr(w["w_up"]),
         _ptr(w["w_down"]), _ptr(w["s_gate"]), _ptr(w["s_up"]), _ptr(w["s_down"]), _ptr(y),
-        threads), "oracle_expert_ffn_fp8")
+        threads), fname)
     return y
 
 
@@ -369,11 +397,12 @@ def split_e4m3_rows(x, dtype: str = "bf16"):
 
 
 def expert_ffn_a2(x_perm, offsets, q: dict, dtype: str = "bf16", threads: int = 0,
-                  taps: bool = False):
+                  taps: bool = False, blocks: bool = False):
     """expert_ffn_fp8 with every x_perm row and every hidden row (after its bf16
-    rounding) carried as two E4M3 planes (split_e4m3_rows).  Returns as
-    expert_ffn_w8a8."""
-    return _expert_ffn_a8(x_perm, offsets, q, dtype, threads, taps, "oracle_expert_ffn_a2")
+    rounding) carried as two E4M3 planes (split_e4m3_rows); blocks=True: the
+    weights' 128 x 128 block scales.  Returns as expert_ffn_w8a8."""
+    return _expert_ffn_a8(x_perm, offsets, q, dtype, threads, taps,
+                          "oracle_expert_ffn_a2_blocks" if blocks else "oracle_expert_ffn_a2")
 
 
 def expert_ffn_w8a8(x_perm, offsets, q: dict, dtype: str = "bf16", threads: int = 0,
@@ -403,14 +432,16 @@ def _expert_ffn_a8(x_perm, offsets, q, dtype, threads, taps, fname):
 
 
 def forward_tokens_fp8(tokens, x, w_g, q: dict, K: int, dtype: str = "bf16", bias=None,
-                       threads: int = 0, router: str = "softmax", act8=False):
+                       threads: int = 0, router: str = "softmax", act8=False,
+                       blocks: bool = False):
     """forward_tokens with E4M3 expert weights (routed and, when present, shared):
     q holds w_gate/w_up/w_down (+ ws_*) codes and s_gate/s_up/s_down (+ ss_*)
     row scales; x and w_g are in dtype.  Returns the same dict as forward_tokens.
     act8: True (or "w8a8") -- every expert runs W8A8 (its input and hidden rows
     quantised per row; see oracle_forward_tokens_w8a8); "planes" -- every
     expert's input and hidden rows carried as two E4M3 planes
-    (oracle_forward_tokens_a2)."""
+    (oracle_forward_tokens_a2).  blocks=True: the scales are the 128 x 128 block
+    scales of quantize_fp8_blocks (with act8 False or "planes")."""
     lib = _load()
     tokens = _arr(tokens, np.int32)
     x, w_g = _in(x, dtype), _in(w_g, dtype)
@@ -428,6 +459,10 @@ def forward_tokens_fp8(tokens, x, w_g, q: dict, K: int, dtype: str = "bf16", bia
     }
     fname = ("oracle_forward_tokens_a2" if act8 == "planes" else
              "oracle_forward_tokens_w8a8" if act8 else "oracle_forward_tokens_fp8")
+    if blocks:
+        if act8 not in (False, "planes"):
+            raise ValueError("block scales: act8 False or 'planes'")
+        fname += "_blocks"
     fn = getattr(lib, fname)
     _check(fn(
         n, _ptr(tokens), T, d, E, K, I, Is, _DT[dtype], _ROUTER[router], _ptr(x), _ptr(w_g),

@@ -60,6 +60,13 @@
  * the code of its remainder, one scale per row): the library's form of the
  * 8-bit-weight layer on its 8-bit-by-8-bit tensor-core path.
  *
+ * Block-scaled weights (the *_blocks entry points; the section's "per
+ * group" granularity, in the square 128 x 128 blocks of DeepSeek-V3's 8-bit
+ * checkpoints): one fp32 scale per block of 128 rows x 128 columns of the
+ * stacked weight matrix, w_hat[r][c] = value(code[r][c]) *
+ * scale[r / 128][c / 128], each block quantised by the row rule above
+ * applied to its elements.
+ *
  * Every entry point returns 0 on success and a negative number on a bad
  * argument; nothing is allocated that is not freed before return.
  */
@@ -72,7 +79,8 @@
 
 #define ORC_F32 0
 #define ORC_BF16 1
-#define ORC_E4M3 2 /* weight codes only: 8-bit E4M3 float times a per-row scale */
+#define ORC_E4M3 2 /* weight codes only: 8-bit E4M3 float times a per-row (or per-block) scale */
+#define ORC_FP8_BLOCK 128 /* side of a square weight-scale block */
 
 /* ------------------------------------------------------------------------ */
 /* element access: the exact stored value, widened to double                */
@@ -143,31 +151,57 @@ static uint8_t e4m3_code(float f)
 }
 
 /* A weight matrix as the FFN reads it: fp32 / bf16 elements, or E4M3 codes
- * with one scale per row of row_len elements. */
+ * with one scale per row of row_len elements, or (block > 0) one scale per
+ * block of block x block elements (row-major over the blocks of the row-major
+ * matrix: scale[(r / block) * (row_len / block) + c / block]). */
 typedef struct {
     const void *base;
     int fmt; /* ORC_F32, ORC_BF16 or ORC_E4M3 */
     const float *scale;
     int64_t row_len;
+    int64_t block; /* 0: a scale per row */
 } orc_weight;
 
 static orc_weight plain_weight(const void *base, int dtype)
 {
-    orc_weight w = {base, dtype, NULL, 1};
+    orc_weight w = {base, dtype, NULL, 1, 0};
     return w;
 }
 
 static orc_weight fp8_weight(const void *codes, const float *scale, int64_t row_len)
 {
-    orc_weight w = {codes, ORC_E4M3, scale, row_len};
+    orc_weight w = {codes, ORC_E4M3, scale, row_len, 0};
     return w;
 }
 
-/* w_hat[i] = value(code[i]) * scale[row of i], or the stored element */
+static orc_weight fp8_block_weight(const void *codes, const float *scale, int64_t row_len)
+{
+    orc_weight w = {codes, ORC_E4M3, scale, row_len, ORC_FP8_BLOCK};
+    return w;
+}
+
+/* E4M3 codes with row scales (blocks = 0) or 128 x 128 block scales */
+static orc_weight fp8w(const void *codes, const float *scale, int64_t row_len, int blocks)
+{
+    return blocks ? fp8_block_weight(codes, scale, row_len) : fp8_weight(codes, scale, row_len);
+}
+
+/* w_hat[i] = value(code[i]) * its scale (the row's or the block's), or the
+ * stored element */
 static double load_weight(const orc_weight *w, int64_t i)
 {
-    if (w->fmt == ORC_E4M3)
-        return e4m3_value(((const uint8_t *)w->base)[i]) * (double)w->scale[i / w->row_len];
+    if (w->fmt == ORC_E4M3) {
+        const int64_t r = i / w->row_len;
+        double sc;
+        if (w->block > 0) {
+            const int64_t c = i % w->row_len;
+            const int64_t nbc = (w->row_len + w->block - 1) / w->block;
+            sc = (double)w->scale[(r / w->block) * nbc + c / w->block];
+        } else {
+            sc = (double)w->scale[r];
+        }
+        return e4m3_value(((const uint8_t *)w->base)[i]) * sc;
+    }
     return load_elem(w->base, w->fmt, i);
 }
 
@@ -517,6 +551,23 @@ int oracle_expert_ffn_fp8(int64_t d, int64_t E, int64_t I, int dtype,
                       nthreads);
 }
 
+/* The same with 128 x 128 block scales (oracle_quantize_fp8_blocks of the
+ * stacked matrices): s_gate/s_up [ceil(E*I/128)][ceil(d/128)], s_down
+ * [ceil(E*d/128)][ceil(I/128)]. */
+int oracle_expert_ffn_fp8_blocks(int64_t d, int64_t E, int64_t I, int dtype,
+                                 const void *x_perm, const int32_t *offsets,
+                                 const uint8_t *w_gate, const uint8_t *w_up,
+                                 const uint8_t *w_down, const float *s_gate,
+                                 const float *s_up, const float *s_down,
+                                 double *y_perm, int nthreads)
+{
+    if (!w_gate || !w_up || !w_down || !s_gate || !s_up || !s_down)
+        return -1;
+    return expert_ffn(d, E, I, dtype, x_perm, offsets, fp8_block_weight(w_gate, s_gate, d),
+                      fp8_block_weight(w_up, s_up, d), fp8_block_weight(w_down, s_down, I),
+                      y_perm, nthreads);
+}
+
 /* ------------------------------------------------------------------------ */
 /* stage 4: combine                                                         */
 /* ------------------------------------------------------------------------ */
@@ -778,6 +829,39 @@ int oracle_forward_tokens_fp8(int64_t n, const int32_t *tokens, int64_t T,
                           topk_idx, topk_w, logits, nthreads);
 }
 
+/*
+ * oracle_forward_tokens_fp8_blocks: oracle_forward_tokens_fp8 with 128 x 128
+ * block scales: s_gate/s_up [ceil(E*I/128)][ceil(d/128)], s_down
+ * [ceil(E*d/128)][ceil(I/128)], ss_gate/ss_up [ceil(Is/128)][ceil(d/128)],
+ * ss_down [ceil(d/128)][ceil(Is/128)].
+ */
+int oracle_forward_tokens_fp8_blocks(int64_t n, const int32_t *tokens, int64_t T,
+                                     int64_t d, int64_t E, int64_t K, int64_t I,
+                                     int64_t Is, int dtype, int mode, const void *x,
+                                     const void *w_g, const double *bias,
+                                     const uint8_t *w_gate, const uint8_t *w_up,
+                                     const uint8_t *w_down, const float *s_gate,
+                                     const float *s_up, const float *s_down,
+                                     const uint8_t *ws_gate, const uint8_t *ws_up,
+                                     const uint8_t *ws_down, const float *ss_gate,
+                                     const float *ss_up, const float *ss_down,
+                                     double *y, int32_t *topk_idx, double *topk_w,
+                                     double *logits, int nthreads)
+{
+    if (!w_gate || !w_up || !w_down || !s_gate || !s_up || !s_down)
+        return -1;
+    if (Is > 0 && (!ws_gate || !ws_up || !ws_down || !ss_gate || !ss_up || !ss_down))
+        return -1;
+    const orc_weight w[6] = {fp8_block_weight(w_gate, s_gate, d),
+                             fp8_block_weight(w_up, s_up, d),
+                             fp8_block_weight(w_down, s_down, I),
+                             fp8_block_weight(ws_gate, ss_gate, d),
+                             fp8_block_weight(ws_up, ss_up, d),
+                             fp8_block_weight(ws_down, ss_down, Is)};
+    return forward_tokens(n, tokens, T, d, E, K, I, Is, dtype, mode, x, w_g, bias, w, y,
+                          topk_idx, topk_w, logits, nthreads);
+}
+
 /* ------------------------------------------------------------------------ */
 /* E4M3 codes and row quantisation                                          */
 /* ------------------------------------------------------------------------ */
@@ -837,6 +921,44 @@ int oracle_quantize_fp8_rows(int64_t rows, int64_t cols, int dtype, const void *
         scale[r] = quantize_vec(row, cols, codes + r * cols);
     }
     free(row);
+    return 0;
+}
+
+/*
+ * oracle_quantize_fp8_blocks: per-group quantisation ("per tensor, per
+ * channel or per group" in the "make every byte cheaper" section) of a
+ * row-major [rows][cols] matrix with one fp32 scale per square block of 128
+ * rows x 128 columns (the last block row / column may be shorter):
+ * scale[(r / 128) * ceil(cols / 128) + c / 128] = amax over the block / 448
+ * (1 for a block of zeros), computed in fp32; code = nearest E4M3 to
+ * (w / scale) computed as an fp32 division -- the row rule of
+ * oracle_quantize_fp8_rows applied to each block's elements.
+ */
+int oracle_quantize_fp8_blocks(int64_t rows, int64_t cols, int dtype, const void *w,
+                               uint8_t *codes, float *scale)
+{
+    if (rows < 0 || cols < 1 || (rows > 0 && (!w || !codes || !scale)))
+        return -1;
+    const int64_t B = ORC_FP8_BLOCK;
+    const int64_t nbr = (rows + B - 1) / B, nbc = (cols + B - 1) / B;
+    float *blk = (float *)malloc(sizeof(float) * (size_t)(B * B));
+    uint8_t *cb = (uint8_t *)malloc((size_t)(B * B));
+    for (int64_t br = 0; br < nbr; ++br) {
+        for (int64_t bc = 0; bc < nbc; ++bc) {
+            const int64_t r0 = br * B, c0 = bc * B;
+            const int64_t nr = rows - r0 < B ? rows - r0 : B;
+            const int64_t nc = cols - c0 < B ? cols - c0 : B;
+            for (int64_t i = 0; i < nr; ++i)
+                for (int64_t j = 0; j < nc; ++j)
+                    blk[i * nc + j] = (float)load_elem(w, dtype, (r0 + i) * cols + c0 + j);
+            scale[br * nbc + bc] = quantize_vec(blk, nr * nc, cb);
+            for (int64_t i = 0; i < nr; ++i)
+                for (int64_t j = 0; j < nc; ++j)
+                    codes[(r0 + i) * cols + c0 + j] = cb[i * nc + j];
+        }
+    }
+    free(blk);
+    free(cb);
     return 0;
 }
 
@@ -1055,7 +1177,7 @@ static int expert_ffn_a8(int64_t d, int64_t E, int64_t I, int dtype, const void 
                          const int32_t *offsets, const uint8_t *w_gate, const uint8_t *w_up,
                          const uint8_t *w_down, const float *s_gate, const float *s_up,
                          const float *s_down, double *y_perm, double *h_pre, double *h_hat,
-                         int nthreads, int planes);
+                         int nthreads, int planes, int blocks);
 
 int oracle_expert_ffn_w8a8(int64_t d, int64_t E, int64_t I, int dtype,
                            const void *x_perm, const int32_t *offsets,
@@ -1065,7 +1187,7 @@ int oracle_expert_ffn_w8a8(int64_t d, int64_t E, int64_t I, int dtype,
                            double *h_pre, double *h_hat, int nthreads)
 {
     return expert_ffn_a8(d, E, I, dtype, x_perm, offsets, w_gate, w_up, w_down, s_gate, s_up,
-                         s_down, y_perm, h_pre, h_hat, nthreads, 1);
+                         s_down, y_perm, h_pre, h_hat, nthreads, 1, 0);
 }
 
 /*
@@ -1080,14 +1202,27 @@ int oracle_expert_ffn_a2(int64_t d, int64_t E, int64_t I, int dtype, const void 
                          int nthreads)
 {
     return expert_ffn_a8(d, E, I, dtype, x_perm, offsets, w_gate, w_up, w_down, s_gate, s_up,
-                         s_down, y_perm, h_pre, h_hat, nthreads, 2);
+                         s_down, y_perm, h_pre, h_hat, nthreads, 2, 0);
+}
+
+/* oracle_expert_ffn_a2 with the 128 x 128 block scales of
+ * oracle_expert_ffn_fp8_blocks. */
+int oracle_expert_ffn_a2_blocks(int64_t d, int64_t E, int64_t I, int dtype,
+                                const void *x_perm, const int32_t *offsets,
+                                const uint8_t *w_gate, const uint8_t *w_up,
+                                const uint8_t *w_down, const float *s_gate,
+                                const float *s_up, const float *s_down, double *y_perm,
+                                double *h_pre, double *h_hat, int nthreads)
+{
+    return expert_ffn_a8(d, E, I, dtype, x_perm, offsets, w_gate, w_up, w_down, s_gate, s_up,
+                         s_down, y_perm, h_pre, h_hat, nthreads, 2, 1);
 }
 
 static int expert_ffn_a8(int64_t d, int64_t E, int64_t I, int dtype, const void *x_perm,
                          const int32_t *offsets, const uint8_t *w_gate, const uint8_t *w_up,
                          const uint8_t *w_down, const float *s_gate, const float *s_up,
                          const float *s_down, double *y_perm, double *h_pre, double *h_hat,
-                         int nthreads, int planes)
+                         int nthreads, int planes, int blocks)
 {
     if (d < 1 || E < 1 || I < 1 || !offsets || !y_perm || !w_gate || !w_up || !w_down ||
         !s_gate || !s_up || !s_down || offsets[0] != 0)
@@ -1095,8 +1230,8 @@ static int expert_ffn_a8(int64_t d, int64_t E, int64_t I, int dtype, const void 
     for (int64_t e = 0; e < E; ++e)
         if (offsets[e + 1] < offsets[e])
             return -1;
-    ffn_a8_ctx c = {d, E, I, dtype, x_perm, offsets, fp8_weight(w_gate, s_gate, d),
-                    fp8_weight(w_up, s_up, d), fp8_weight(w_down, s_down, I), y_perm,
+    ffn_a8_ctx c = {d, E, I, dtype, x_perm, offsets, fp8w(w_gate, s_gate, d, blocks),
+                    fp8w(w_up, s_up, d, blocks), fp8w(w_down, s_down, I, blocks), y_perm,
                     h_pre, h_hat, planes};
     par_for(offsets[E], nthreads, ffn_row_a8, &c);
     return 0;
@@ -1151,7 +1286,8 @@ static int forward_tokens_a8(int64_t n, const int32_t *tokens, int64_t T, int64_
                              const uint8_t *ws_gate, const uint8_t *ws_up,
                              const uint8_t *ws_down, const float *ss_gate, const float *ss_up,
                              const float *ss_down, double *y, int32_t *topk_idx,
-                             double *topk_w, double *logits, int nthreads, int planes);
+                             double *topk_w, double *logits, int nthreads, int planes,
+                             int blocks);
 
 /*
  * oracle_forward_tokens_w8a8: oracle_forward_tokens_fp8 with every expert
@@ -1173,7 +1309,8 @@ int oracle_forward_tokens_w8a8(int64_t n, const int32_t *tokens, int64_t T,
 {
     return forward_tokens_a8(n, tokens, T, d, E, K, I, Is, dtype, mode, x, w_g, bias, w_gate,
                              w_up, w_down, s_gate, s_up, s_down, ws_gate, ws_up, ws_down,
-                             ss_gate, ss_up, ss_down, y, topk_idx, topk_w, logits, nthreads, 1);
+                             ss_gate, ss_up, ss_down, y, topk_idx, topk_w, logits, nthreads, 1,
+                             0);
 }
 
 /*
@@ -1197,7 +1334,29 @@ int oracle_forward_tokens_a2(int64_t n, const int32_t *tokens, int64_t T,
 {
     return forward_tokens_a8(n, tokens, T, d, E, K, I, Is, dtype, mode, x, w_g, bias, w_gate,
                              w_up, w_down, s_gate, s_up, s_down, ws_gate, ws_up, ws_down,
-                             ss_gate, ss_up, ss_down, y, topk_idx, topk_w, logits, nthreads, 2);
+                             ss_gate, ss_up, ss_down, y, topk_idx, topk_w, logits, nthreads, 2,
+                             0);
+}
+
+/* oracle_forward_tokens_a2 with the 128 x 128 block scales of
+ * oracle_forward_tokens_fp8_blocks. */
+int oracle_forward_tokens_a2_blocks(int64_t n, const int32_t *tokens, int64_t T,
+                                    int64_t d, int64_t E, int64_t K, int64_t I,
+                                    int64_t Is, int dtype, int mode, const void *x,
+                                    const void *w_g, const double *bias,
+                                    const uint8_t *w_gate, const uint8_t *w_up,
+                                    const uint8_t *w_down, const float *s_gate,
+                                    const float *s_up, const float *s_down,
+                                    const uint8_t *ws_gate, const uint8_t *ws_up,
+                                    const uint8_t *ws_down, const float *ss_gate,
+                                    const float *ss_up, const float *ss_down,
+                                    double *y, int32_t *topk_idx, double *topk_w,
+                                    double *logits, int nthreads)
+{
+    return forward_tokens_a8(n, tokens, T, d, E, K, I, Is, dtype, mode, x, w_g, bias, w_gate,
+                             w_up, w_down, s_gate, s_up, s_down, ws_gate, ws_up, ws_down,
+                             ss_gate, ss_up, ss_down, y, topk_idx, topk_w, logits, nthreads, 2,
+                             1);
 }
 
 static int forward_tokens_a8(int64_t n, const int32_t *tokens, int64_t T,
@@ -1211,7 +1370,7 @@ static int forward_tokens_a8(int64_t n, const int32_t *tokens, int64_t T,
                                const uint8_t *ws_down, const float *ss_gate,
                                const float *ss_up, const float *ss_down,
                                double *y, int32_t *topk_idx, double *topk_w,
-                               double *logits, int nthreads, int planes)
+                               double *logits, int nthreads, int planes, int blocks)
 {
     if (!w_gate || !w_up || !w_down || !s_gate || !s_up || !s_down)
         return -1;
@@ -1225,10 +1384,10 @@ static int forward_tokens_a8(int64_t n, const int32_t *tokens, int64_t T,
         if (tokens[r] < 0 || tokens[r] >= T)
             return -1;
     tok_ctx c = {d, E, K, I, Is, dtype, mode, x, w_g, bias,
-                 fp8_weight(w_gate, s_gate, d), fp8_weight(w_up, s_up, d),
-                 fp8_weight(w_down, s_down, I),
-                 fp8_weight(ws_gate, ss_gate, d), fp8_weight(ws_up, ss_up, d),
-                 fp8_weight(ws_down, ss_down, Is),
+                 fp8w(w_gate, s_gate, d, blocks), fp8w(w_up, s_up, d, blocks),
+                 fp8w(w_down, s_down, I, blocks),
+                 fp8w(ws_gate, ss_gate, d, blocks), fp8w(ws_up, ss_up, d, blocks),
+                 fp8w(ws_down, ss_down, Is, blocks),
                  tokens, y, logits, topk_idx, topk_w, planes};
     par_for(n, nthreads, token_row_a8, &c);
     return 0;

@@ -1,6 +1,6 @@
 """Plant plausible mistakes in a copy of the oracle (on the CPU) and check that
-the pins in test_oracle_pins.py, test_oracle_fp8.py, test_oracle_w8a8.py and
-test_oracle_a2.py catch every one of them."""
+the pins in test_oracle_pins.py, test_oracle_fp8.py, test_oracle_w8a8.py,
+test_oracle_a2.py and test_oracle_blocks.py catch every one of them."""
 import ctypes
 import os
 
@@ -10,6 +10,7 @@ import oracle
 from tests import test_oracle_fp8 as pins8
 from tests import test_oracle_pins as pins
 from tests import test_oracle_a2 as pins_a2
+from tests import test_oracle_blocks as pins_blk
 from tests import test_oracle_w8a8 as pins_a8
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "moe_oracle.c")
@@ -39,7 +40,7 @@ MUTATIONS = [
     ("e4m3_subnormal_step", "v = ldexp((double)M, -9);", "v = ldexp((double)M, -10);"),
     ("e4m3_round_half_up", "nearbyint(a / unit)", "floor(a / unit + 0.5)"),
     ("e4m3_no_saturation", "return sgn | 0x7E;", "return sgn | 0x7F;"),
-    ("fp8_scale_by_column", "(double)w->scale[i / w->row_len]", "(double)w->scale[i % w->row_len]"),
+    ("fp8_scale_by_column", "sc = (double)w->scale[r];", "sc = (double)w->scale[i % w->row_len];"),
     ("fp8_down_scale_row_length", "fp8_weight(w_down, s_down, I), fp8_weight(ws_gate",
      "fp8_weight(w_down, s_down, d), fp8_weight(ws_gate"),
     ("quant_scale_not_amax", "amax / 448.0f : 1.0f;\n    for (int64_t c = 0; c < n; ++c)\n        codes[c]",
@@ -54,8 +55,8 @@ MUTATIONS = [
      "for (int64_t i = 0; i < I; ++i) s->h[i] = (double)s->f[i];"),
     ("a8_h_read_as_two_planes", "act_hat(s, I, planes, s->h);", "act_hat(s, I, 2, s->h);"),
     ("a8_bf16_rounds_half_up", "u += 0x7fffu + ((u >> 16) & 1u);", "u += 0x8000u;"),
-    ("a8_down_scale_row_length", "fp8_weight(w_down, s_down, I), y_perm,\n                    h_pre",
-     "fp8_weight(w_down, s_down, d), y_perm,\n                    h_pre"),
+    ("a8_down_scale_row_length", "fp8w(w_down, s_down, I, blocks), y_perm,",
+     "fp8w(w_down, s_down, d, blocks), y_perm,"),
     ("a8_shared_expert_skipped", "swiglu_row_a8(d, c->Is, c->dtype, c->x, t * d, &c->ws_gate",
      "if (0) swiglu_row_a8(d, c->Is, c->dtype, c->x, t * d, &c->ws_gate"),
     ("a2_lo_plane_dropped",
@@ -67,8 +68,26 @@ MUTATIONS = [
      "out[k] = (e4m3_value(s->c[k]) + e4m3_value(s->c2[k])) * (double)sc;",
      "out[k] = (e4m3_value(s->c[k]) + e4m3_value(s->c2[k]) * (double)sc) * (double)sc;"),
     ("a2_one_plane_in_the_token_layer",
-     "ss_gate, ss_up, ss_down, y, topk_idx, topk_w, logits, nthreads, 2);",
-     "ss_gate, ss_up, ss_down, y, topk_idx, topk_w, logits, nthreads, 1);"),
+     "logits, nthreads, 2,\n                             0);",
+     "logits, nthreads, 1,\n                             0);"),
+    ("block_scale_ignores_the_column_block",
+     "sc = (double)w->scale[(r / w->block) * nbc + c / w->block];",
+     "sc = (double)w->scale[(r / w->block) * nbc];"),
+    ("block_scale_ignores_the_row_block",
+     "sc = (double)w->scale[(r / w->block) * nbc + c / w->block];",
+     "sc = (double)w->scale[c / w->block];"),
+    ("block_down_row_length",
+     "fp8_block_weight(w_down, s_down, I),\n                             fp8_block_weight(ws_gate",
+     "fp8_block_weight(w_down, s_down, d),\n                             fp8_block_weight(ws_gate"),
+    ("block_stage_down_row_length", "fp8_block_weight(w_down, s_down, I),\n                      y_perm",
+     "fp8_block_weight(w_down, s_down, d),\n                      y_perm"),
+    ("block_quant_amax_of_the_first_row", "scale[br * nbc + bc] = quantize_vec(blk, nr * nc, cb);",
+     "scale[br * nbc + bc] = quantize_vec(blk, nc, cb);"),
+    ("block_quant_codes_transposed", "codes[(r0 + i) * cols + c0 + j] = cb[i * nc + j];",
+     "codes[(r0 + i) * cols + c0 + j] = cb[j * nr + i];"),
+    ("block_a2_stage_with_one_plane",
+     "s_down, y_perm, h_pre, h_hat, nthreads, 2, 1);",
+     "s_down, y_perm, h_pre, h_hat, nthreads, 1, 1);"),
 ]
 
 PIN_TESTS = [
@@ -99,6 +118,9 @@ PIN_TESTS = [
     lambda: pins_a2.test_planes_meet_the_two_step_error_bound_and_are_not_one_plane(),
     lambda: pins_a2.test_a2_expert_matches_library_casts_at_every_step(1, [3, 0, 5, 1]),
     lambda: pins_a2.test_a2_token_forward_matches_the_expert_stage(),
+    lambda: pins_blk.test_block_codes_and_scales_match_torch("f32", (300, 200)),
+    lambda: pins_blk.test_block_layer_equals_the_layer_on_dequantised_weights("bf16", 0, 192, 320, 64),
+    lambda: pins_blk.test_a2_blocks_expert_matches_library_casts_at_every_step(2, [7, 2]),
 ]
 
 
