@@ -287,6 +287,48 @@ moe_status moe_forward_fp8(const moe_shape *shape, const void *x, const void *w_
                            void *workspace, size_t ws_bytes, void *stream);
 
 /*
+ * ---- block-scaled 8-bit weights --------------------------------------------
+ * [Q] lets a quantisation scale cover a tensor, a channel or a group.  Here a
+ * group is a square block of 128 x 128 weights, the layout of DeepSeek-V3's
+ * 8-bit checkpoints (DeepSeek-V3 served in FP8: "Model architecture feeding
+ * back into inference systems: from MHA/GQA to DeepSeek MLA", blog.llmgo.top,
+ * FAQ Q3): one fp32 scale per block of the STACKED matrix,
+ *     w_hat[r][c] = e4m3_value(code[r][c]) * scale[r / 128][c / 128],
+ * each block quantised by the per-row rule above applied to its elements
+ * (scale = block amax / 448, fp32 divisions, ties to an even mantissa,
+ * saturation at 448).
+ *
+ * moe_quantize_fp8_blocks: w [rows][cols] (MOE_F32 or MOE_BF16, finite) ->
+ * codes [rows][cols] and scales [ceil(rows/128)][ceil(cols/128)] (row-major),
+ * device buffers.  Limits: cols a multiple of 16 and < 2^31, ceil(rows/128) <=
+ * 65535.  rows == 0 is a no-op.  Enqueued on `stream`, no workspace.  Pass a
+ * stacked weight tensor as one matrix: w_gate [E][I][d] as rows = E*I.
+ */
+moe_status moe_quantize_fp8_blocks(int64_t rows, int64_t cols, int32_t dtype,
+                                   const void *w, uint8_t *codes, float *scales,
+                                   void *stream);
+
+/*
+ * moe_expert_ffn_fp8 / moe_forward_fp8 with block scales: the codes of
+ * moe_fp8_experts as before, its scale members the block grids of
+ * moe_quantize_fp8_blocks: s_gate, s_up [E*I/128][d/128]; s_down
+ * [E*d/128][I/128]; ss_gate, ss_up [Is/128][d/128]; ss_down [d/128][Is/128].
+ * Same limits (d, inter, inter_shared multiples of 128, so no block spans two
+ * experts), workspace and errors as the row-scaled calls.  Groups of at most
+ * 8 rows take the 8-bit GEMV (each 128-code K block's partial sums scaled and
+ * added); larger groups take the tensor cores with the activations as two
+ * E4M3 planes, each 128-deep K block multiplied into its own tensor-memory
+ * accumulator and added, times its block scale, to fp32 sums in registers.
+ */
+moe_status moe_expert_ffn_fp8_blocks(const moe_shape *shape, const void *x_perm,
+                                     const int32_t *offsets, const moe_fp8_experts *w,
+                                     void *y_perm, void *workspace, size_t ws_bytes,
+                                     void *stream);
+moe_status moe_forward_fp8_blocks(const moe_shape *shape, const void *x, const void *w_g,
+                                  const float *bias, const moe_fp8_experts *w, void *y,
+                                  void *workspace, size_t ws_bytes, void *stream);
+
+/*
  * ---- 8-bit weights AND 8-bit activations (W8A8) ----------------------------
  * [Q] names weights, activations and the KV cache as things a quantisation
  * method may act on.  Here the same per-row rule quantises the two

@@ -68,7 +68,8 @@ class LayerConfig:
     down_std: str = "d"   # "d": w_down ~ N(0,1/d); "inter": N(0,1/I)
     zipf_bias: bool = False
     router: str = "softmax"   # "softmax" or "sigmoid" (DeepSeek-V3 affinities)
-    weights: str = "act"      # "act": experts in dtype; "e4m3": 8-bit codes + row scales
+    weights: str = "act"      # "act": experts in dtype; "e4m3": 8-bit codes + row scales;
+                              # "e4m3b": 8-bit codes + one scale per 128 x 128 block
     acts: str = "act"         # "e4m3": the experts' input and hidden rows quantised (W8A8)
     seed: int = 0
     extra: dict = field(default_factory=dict, compare=False)
@@ -96,6 +97,15 @@ CONFIGS["mixtral_prefill_fp8"] = replace(CONFIGS["mixtral_prefill"], name="mixtr
 for _t in (64, 512):
     CONFIGS[f"dsv3_sweep_fp8_T{_t}"] = replace(CONFIGS["dsv3_decode_fp8"],
                                                name=f"dsv3_sweep_fp8_T{_t}", T=_t)
+# 8-bit expert weights with one fp32 scale per 128 x 128 block of each stacked
+# matrix (DeepSeek-V3's checkpoint layout); the codes are those of the row-scaled
+# configs above
+CONFIGS["dsv3_decode_fp8b"] = replace(CONFIGS["dsv3_decode"], name="dsv3_decode_fp8b",
+                                      weights="e4m3b")
+CONFIGS["mixtral_prefill_fp8b"] = replace(CONFIGS["mixtral_prefill"], name="mixtral_prefill_fp8b",
+                                          weights="e4m3b")
+CONFIGS["dsv3_sweep_fp8b_T512"] = replace(CONFIGS["dsv3_decode_fp8b"], name="dsv3_sweep_fp8b_T512",
+                                          T=512)
 # the same decode layer over a pool of 32 experts (1.4 GB of codes): small enough
 # for multi-pass counter captures, still far larger than L2
 CONFIGS["dsv3_decode_fp8_E32"] = replace(CONFIGS["dsv3_decode_fp8"], name="dsv3_decode_fp8_E32",
@@ -210,12 +220,25 @@ def row_scales(shape, std: float, device, seed: int, name: str) -> torch.Tensor:
     return (u * 0.4 + 0.8) * (std / E4M3_RMS)
 
 
+def block_scales(rows: int, cols: int, std: float, device, seed: int, name: str) -> torch.Tensor:
+    """One fp32 scale per 128 x 128 block of a stacked [rows][cols] matrix:
+    [ceil(rows/128)][ceil(cols/128)], std / E4M3_RMS * U(0.8, 1.2)."""
+    return row_scales(((rows + 127) // 128, (cols + 127) // 128), std, device, seed, name)
+
+
+def is_fp8(cfg: LayerConfig) -> bool:
+    """The expert matrices are E4M3 codes (row or block scales)."""
+    return cfg.weights in ("e4m3", "e4m3b")
+
+
 def make_weights(cfg: LayerConfig, device="cpu", only=None) -> dict:
     """Router, routed-expert and shared-expert weights, stored [out][in].
 
     For cfg.weights == "e4m3" the expert matrices are uint8 E4M3 codes and the
     dict also holds their row scales: s_gate, s_up [E][I], s_down [E][d] (ss_*
-    for the shared expert); w_g stays in cfg.dtype.
+    for the shared expert); w_g stays in cfg.dtype.  For "e4m3b" the same
+    codes with block scales over each stacked matrix: s_gate, s_up
+    [E*I/128][d/128], s_down [E*d/128][I/128] (ss_* likewise).
     ``only`` (a set of names) draws just those tensors; each has its own
     sub-seed, so the values are the same as in a full draw."""
     d, E, I, Is, dt, sd = cfg.d, cfg.E, cfg.I, cfg.Is, cfg.dtype, cfg.seed
@@ -232,7 +255,7 @@ def make_weights(cfg: LayerConfig, device="cpu", only=None) -> dict:
         recipe["ws_gate"] = ((Is, d), std_d, False)
         recipe["ws_up"] = ((Is, d), std_d, False)
         recipe["ws_down"] = ((d, Is), std_sdown, False)
-    if cfg.weights == "e4m3":
+    if is_fp8(cfg):
         out = {}
         for name, (shape, std, chunk) in recipe.items():
             sname = "s" + name[1:] if name.startswith("w_") else "ss" + name[2:]
@@ -243,7 +266,11 @@ def make_weights(cfg: LayerConfig, device="cpu", only=None) -> dict:
             if only is None or name in only:
                 out[name] = e4m3_codes(shape, device, sd, name, chunk_dim0=chunk)
             if only is None or sname in only:
-                out[sname] = row_scales(shape[:-1], std, device, sd, sname)
+                if cfg.weights == "e4m3b":
+                    rows = math.prod(shape[:-1])
+                    out[sname] = block_scales(rows, shape[-1], std, device, sd, sname)
+                else:
+                    out[sname] = row_scales(shape[:-1], std, device, sd, sname)
         return out
     return {name: normal(shape, std, dt, device, sd, name, chunk_dim0=chunk)
             for name, (shape, std, chunk) in recipe.items() if only is None or name in only}

@@ -25,7 +25,9 @@ MOE_ROUTER_SOFTMAX, MOE_ROUTER_SIGMOID = 0, 1
 EXPORTED = ("moe_status_string", "moe_workspace_bytes", "moe_route", "moe_permute",
             "moe_permute_noalloc", "moe_expert_ffn", "moe_combine", "moe_forward",
             "moe_quantize_fp8_rows", "moe_expert_ffn_fp8", "moe_forward_fp8",
+            "moe_quantize_fp8_blocks", "moe_expert_ffn_fp8_blocks", "moe_forward_fp8_blocks",
             "moe_expert_ffn_w8a8", "moe_forward_w8a8", "moe_get_device_error")
+FP8_BLOCK = 128  # side of the square weight-scale blocks of the *_fp8_blocks calls
 
 
 class MoeError(RuntimeError):
@@ -42,7 +44,8 @@ class moe_shape(ctypes.Structure):
 
 
 class moe_fp8_experts(ctypes.Structure):
-    """E4M3 expert weight codes (uint8) and fp32 row scales: device pointers."""
+    """E4M3 expert weight codes (uint8) and fp32 scales (per row, or per 128 x 128
+    block for the *_fp8_blocks calls): device pointers."""
     _fields_ = [(n, ctypes.c_void_p) for n in (
         "w_gate", "w_up", "w_down", "s_gate", "s_up", "s_down",
         "ws_gate", "ws_up", "ws_down", "ss_gate", "ss_up", "ss_down")]
@@ -70,11 +73,15 @@ def _load_lib() -> ctypes.CDLL:
     lib.moe_quantize_fp8_rows.argtypes = [ctypes.c_int64, ctypes.c_int64, i32, vp, vp, vp, vp]
     lib.moe_expert_ffn_fp8.argtypes = [sp, vp, vp, fp, vp, vp, sz, vp]
     lib.moe_forward_fp8.argtypes = [sp, vp, vp, vp, fp, vp, vp, sz, vp]
+    lib.moe_quantize_fp8_blocks.argtypes = lib.moe_quantize_fp8_rows.argtypes
+    lib.moe_expert_ffn_fp8_blocks.argtypes = lib.moe_expert_ffn_fp8.argtypes
+    lib.moe_forward_fp8_blocks.argtypes = lib.moe_forward_fp8.argtypes
     lib.moe_expert_ffn_w8a8.argtypes = [sp, vp, vp, fp, vp, vp, sz, vp]
     lib.moe_forward_w8a8.argtypes = [sp, vp, vp, vp, fp, vp, vp, sz, vp]
     lib.moe_get_device_error.argtypes = [vp, ctypes.POINTER(i32)]
     for f in ("moe_route", "moe_permute", "moe_permute_noalloc", "moe_expert_ffn", "moe_combine",
               "moe_forward", "moe_quantize_fp8_rows", "moe_expert_ffn_fp8", "moe_forward_fp8",
+              "moe_quantize_fp8_blocks", "moe_expert_ffn_fp8_blocks", "moe_forward_fp8_blocks",
               "moe_expert_ffn_w8a8", "moe_forward_w8a8", "moe_get_device_error"):
         getattr(lib, f).restype = i32
     return lib
@@ -196,6 +203,17 @@ def moe_quantize_fp8_rows(w, codes, scales, stream=None):
                                       _stream(stream)), "moe_quantize_fp8_rows")
 
 
+def moe_quantize_fp8_blocks(w, codes, scales, stream=None):
+    """Block-scaled E4M3 quantisation of w (bf16 or fp32) taken as one stacked
+    [rows][cols] matrix (rows = the product of the leading sizes): codes (uint8,
+    w's shape) and scales (fp32, [ceil(rows/128)][ceil(cols/128)])."""
+    dtype = {torch.bfloat16: MOE_BF16, torch.float32: MOE_F32}[w.dtype]
+    cols = w.shape[-1]
+    rows = w.numel() // cols if cols else 0
+    _check(_lib.moe_quantize_fp8_blocks(rows, cols, dtype, _p(w), _p(codes), _p(scales),
+                                        _stream(stream)), "moe_quantize_fp8_blocks")
+
+
 def make_fp8_experts(q: dict) -> moe_fp8_experts:
     """A moe_fp8_experts from a dict of device tensors (w_gate, w_up, w_down codes,
     s_gate, s_up, s_down scales; ws_* / ss_* for the shared expert, optional).
@@ -214,6 +232,21 @@ def moe_forward_fp8(shape, x, w_g, bias, w: moe_fp8_experts, y, workspace, strea
     ws, nws = _ws(workspace)
     _check(_lib.moe_forward_fp8(ctypes.byref(shape), _p(x), _p(w_g), _p(bias), ctypes.byref(w),
                                 _p(y), ws, nws, _stream(stream)), "moe_forward_fp8")
+
+
+def moe_expert_ffn_fp8_blocks(shape, x_perm, offsets, w: moe_fp8_experts, y_perm, workspace,
+                              stream=None):
+    ws, nws = _ws(workspace)
+    _check(_lib.moe_expert_ffn_fp8_blocks(ctypes.byref(shape), _p(x_perm), _p(offsets),
+                                          ctypes.byref(w), _p(y_perm), ws, nws, _stream(stream)),
+           "moe_expert_ffn_fp8_blocks")
+
+
+def moe_forward_fp8_blocks(shape, x, w_g, bias, w: moe_fp8_experts, y, workspace, stream=None):
+    ws, nws = _ws(workspace)
+    _check(_lib.moe_forward_fp8_blocks(ctypes.byref(shape), _p(x), _p(w_g), _p(bias),
+                                       ctypes.byref(w), _p(y), ws, nws, _stream(stream)),
+           "moe_forward_fp8_blocks")
 
 
 def moe_expert_ffn_w8a8(shape, x_perm, offsets, w: moe_fp8_experts, y_perm, workspace,

@@ -38,6 +38,12 @@
 // Work: warp tasks (group, 16 weight rows); each block takes a contiguous
 // range of tasks and walks it group by group, staging each group's activation
 // rows once.
+//
+// Block-scaled weights (BLK, one scale per 128 x 128 block): a warp's 16 rows
+// lie in one block row, so each 128-code K block has one scale per MMA row
+// half; its two 64-code blocks accumulate into fresh registers, which are
+// then scaled and added to the running sums (the scale varies along K, so it
+// cannot wait for the end of the dot product).
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 #include <stdlib.h>
@@ -75,9 +81,12 @@ __device__ __forceinline__ Group8 group8(const FfnGroups& g, int grp) {
         v.wg = (const uint8_t*)g.w_gate + w;
         v.wu = (const uint8_t*)g.w_up + w;
         v.wd = (const uint8_t*)g.w_down + w;  // [E][d][I]: the same stride d*I
-        v.sg = g.s_gate + (int64_t)grp * g.I;
-        v.su = g.s_up + (int64_t)grp * g.I;
-        v.sd = g.s_down + (int64_t)grp * g.d;
+        // block scales: expert grp's block rows follow the previous experts' (I
+        // and d are multiples of the block side)
+        const int64_t bs = g.wblock ? (int64_t)(g.d / g.wblock) * (g.I / g.wblock) : 0;
+        v.sg = g.s_gate + (g.wblock ? grp * bs : (int64_t)grp * g.I);
+        v.su = g.s_up + (g.wblock ? grp * bs : (int64_t)grp * g.I);
+        v.sd = g.s_down + (g.wblock ? grp * bs : (int64_t)grp * g.d);
     } else {
         v.rows = g.T;
         v.row0 = 0;
@@ -173,10 +182,13 @@ __device__ __forceinline__ void prefetch_l2(const void* a) {
 // row's next kG8U blocks (512 bytes, one 128-byte line per lane), so the next
 // step's loads find them in L2 -- twice the weight bytes in flight per SM
 // without holding more registers.
-template <int NTILE, int R>
+// BLK: sc0 / sc1 are the block scales of rows p0 / p1 along K (one per 128
+// codes); each 128-code block's products are scaled before they are summed.
+template <int NTILE, int R, bool BLK = false>
 __device__ __forceinline__ void mma_rows(const uint8_t* p0, const uint8_t* p1, int n,
                                          const __half* act, int lane, float (&c)[NTILE][4],
-                                         int pf) {
+                                         int pf, const float* sc0 = nullptr,
+                                         const float* sc1 = nullptr) {
     const int g = lane >> 2, t = lane & 3;
     const int nkb = n / 64;
     const uint8_t* const row0 = p0;
@@ -195,6 +207,16 @@ __device__ __forceinline__ void mma_rows(const uint8_t* p0, const uint8_t* p1, i
                 prefetch_l2(row1 + off);
             }
         }
+        constexpr int kSB = kG8U / 2;  // 128-code scale blocks per step
+        float s0[kSB], s1[kSB];
+        if constexpr (BLK) {
+#pragma unroll
+            for (int b = 0; b < kSB; ++b) {
+                const bool ok = kb0 + 2 * b < nkb;
+                s0[b] = ok ? __ldg(sc0 + (kb0 / 2 + b)) : 0.0f;
+                s1[b] = ok ? __ldg(sc1 + (kb0 / 2 + b)) : 0.0f;
+            }
+        }
         uint4 w0[kG8U], w1[kG8U];
 #pragma unroll
         for (int u = 0; u < kG8U; ++u) {
@@ -202,9 +224,14 @@ __device__ __forceinline__ void mma_rows(const uint8_t* p0, const uint8_t* p1, i
             w0[u] = ok ? ld_stream(p0 + (int64_t)(kb0 + u) * 64) : make_uint4(0, 0, 0, 0);
             w1[u] = ok ? ld_stream(p1 + (int64_t)(kb0 + u) * 64) : make_uint4(0, 0, 0, 0);
         }
+        float cp[NTILE][4];  // BLK: the current 128-code block's products
 #pragma unroll
         for (int u = 0; u < kG8U; ++u) {
             if (kb0 + u >= nkb) break;
+            if (BLK && (u & 1) == 0) {
+#pragma unroll
+                for (int j = 0; j < NTILE; ++j) cp[j][0] = cp[j][1] = cp[j][2] = cp[j][3] = 0.0f;
+            }
             const uint32_t r0[4] = {w0[u].x, w0[u].y, w0[u].z, w0[u].w};
             const uint32_t r1[4] = {w1[u].x, w1[u].y, w1[u].z, w1[u].w};
 #pragma unroll
@@ -217,7 +244,17 @@ __device__ __forceinline__ void mma_rows(const uint8_t* p0, const uint8_t* p1, i
                     // token rows past the R staged ones are zero columns
                     const uint2 b = (R >= 8 * (j + 1) || 8 * j + g < R) ? arow[j][sw_slot(slot, 8 * j + g)]
                                                                        : make_uint2(0u, 0u);
-                    mma16816(c[j], a0, a1, a2, a3, b.x, b.y);
+                    if constexpr (BLK) mma16816(cp[j], a0, a1, a2, a3, b.x, b.y);
+                    else mma16816(c[j], a0, a1, a2, a3, b.x, b.y);
+                }
+            }
+            if (BLK && (u & 1) == 1) {  // n is a multiple of 128: u = 1, 3, ... closes a block
+#pragma unroll
+                for (int j = 0; j < NTILE; ++j) {
+                    c[j][0] = fmaf(s0[u >> 1], cp[j][0], c[j][0]);
+                    c[j][1] = fmaf(s0[u >> 1], cp[j][1], c[j][1]);
+                    c[j][2] = fmaf(s1[u >> 1], cp[j][2], c[j][2]);
+                    c[j][3] = fmaf(s1[u >> 1], cp[j][3], c[j][3]);
                 }
             }
         }
@@ -232,7 +269,7 @@ __device__ __forceinline__ void task_range(int64_t tasks, int64_t& u0, int64_t& 
 
 // One warp, gate/up: intermediate rows i0 .. i0+7 (MMA rows 0-7 gate, 8-15 up)
 // for staged token rows 0 .. nt-1 (nt <= 8 NTILE).
-template <int NTILE, int R>
+template <int NTILE, int R, bool BLK>
 __device__ __forceinline__ void gate_up_task(const FfnGroups& g, const Group8& v, int i0, int c0,
                                              int nt, const __half* act, const float* rs, int lane) {
     const int t = lane & 3;
@@ -240,9 +277,11 @@ __device__ __forceinline__ void gate_up_task(const FfnGroups& g, const Group8& v
     float c[NTILE][4];
 #pragma unroll
     for (int j = 0; j < NTILE; ++j) c[j][0] = c[j][1] = c[j][2] = c[j][3] = 0.0f;
-    mma_rows<NTILE, R>(v.wg + (int64_t)i * g.d, v.wu + (int64_t)i * g.d, g.d, act, lane, c,
-                       g.g8_prefetch);
-    const float sg = v.sg[i], su = v.su[i];
+    // BLK: the scales of the block row holding rows i0 .. i0 + 7
+    const int64_t brow = BLK ? (int64_t)(i0 / kWBlock) * (g.d / kWBlock) : 0;
+    mma_rows<NTILE, R, BLK>(v.wg + (int64_t)i * g.d, v.wu + (int64_t)i * g.d, g.d, act, lane, c,
+                            g.g8_prefetch, v.sg + brow, v.su + brow);
+    const float sg = BLK ? 1.0f : v.sg[i], su = BLK ? 1.0f : v.su[i];
 #pragma unroll
     for (int j = 0; j < NTILE; ++j)
 #pragma unroll
@@ -258,7 +297,7 @@ __device__ __forceinline__ void gate_up_task(const FfnGroups& g, const Group8& v
 }
 
 // One warp, down: output rows j0 .. j0+15 for staged token rows 0 .. nt-1.
-template <int NTILE, int R>
+template <int NTILE, int R, bool BLK>
 __device__ __forceinline__ void down_task(const FfnGroups& g, const Group8& v, int j0, int c0,
                                           int nt, const __half* act, const float* rs, int lane) {
     const int t = lane & 3;
@@ -266,9 +305,11 @@ __device__ __forceinline__ void down_task(const FfnGroups& g, const Group8& v, i
     float c[NTILE][4];
 #pragma unroll
     for (int j = 0; j < NTILE; ++j) c[j][0] = c[j][1] = c[j][2] = c[j][3] = 0.0f;
-    mma_rows<NTILE, R>(v.wd + (int64_t)jr * v.inter, v.wd + (int64_t)(jr + 8) * v.inter, v.inter,
-                       act, lane, c, g.g8_prefetch);
-    const float s0 = v.sd[jr], s1 = v.sd[jr + 8];
+    // BLK: rows j0 .. j0 + 15 share one block row
+    const float* bs = v.sd + (BLK ? (int64_t)(j0 / kWBlock) * (v.inter / kWBlock) : 0);
+    mma_rows<NTILE, R, BLK>(v.wd + (int64_t)jr * v.inter, v.wd + (int64_t)(jr + 8) * v.inter,
+                            v.inter, act, lane, c, g.g8_prefetch, bs, bs);
+    const float s0 = BLK ? 1.0f : v.sd[jr], s1 = BLK ? 1.0f : v.sd[jr + 8];
 #pragma unroll
     for (int j = 0; j < NTILE; ++j)
 #pragma unroll
@@ -286,7 +327,7 @@ __device__ __forceinline__ void down_task(const FfnGroups& g, const Group8& v, i
 // h = SiLU(s_g * (Q_gate x)) * (s_u * (Q_up x)) for the groups of one GEMV
 // list (which = 0: first list, 1: second), up to R token rows per pass; a pass
 // of at most 8 rows runs one MMA per A fragment.
-template <int R>
+template <int R, bool BLK>
 __global__ void __launch_bounds__(kG8Threads, 1)
 gemv8_gate_up_kernel(FfnGroups g, const FfnPlanHeader* __restrict__ hdr,
                      const int32_t* __restrict__ list, int which) {
@@ -315,8 +356,8 @@ gemv8_gate_up_kernel(FfnGroups g, const FfnPlanHeader* __restrict__ hdr,
             for (int64_t k = u + warp; k < seg_end; k += kG8Warps) {
                 const int i0 = (int)(k - (int64_t)a * tpg) * 8;
                 if (i0 >= v.inter) continue;  // warp-uniform
-                if (NT == 1 || nt <= kG8Tok) gate_up_task<1, (R < kG8Tok ? R : kG8Tok)>(g, v, i0, c0, nt, act, rs, lane);
-                else gate_up_task<NT, R>(g, v, i0, c0, nt, act, rs, lane);
+                if (NT == 1 || nt <= kG8Tok) gate_up_task<1, (R < kG8Tok ? R : kG8Tok), BLK>(g, v, i0, c0, nt, act, rs, lane);
+                else gate_up_task<NT, R, BLK>(g, v, i0, c0, nt, act, rs, lane);
             }
         }
         u = seg_end;
@@ -324,7 +365,7 @@ gemv8_gate_up_kernel(FfnGroups g, const FfnPlanHeader* __restrict__ hdr,
 }
 
 // y = s_d * (Q_down h) for the groups of one GEMV list, up to R token rows per pass.
-template <int R>
+template <int R, bool BLK>
 __global__ void __launch_bounds__(kG8Threads, 1)
 gemv8_down_kernel(FfnGroups g, const FfnPlanHeader* __restrict__ hdr,
                   const int32_t* __restrict__ list, int which) {
@@ -351,8 +392,8 @@ gemv8_down_kernel(FfnGroups g, const FfnPlanHeader* __restrict__ hdr,
             __syncthreads();
             for (int64_t k = u + warp; k < seg_end; k += kG8Warps) {
                 const int j0 = (int)(k - (int64_t)a * tpg) * 16;
-                if (NT == 1 || nt <= kG8Tok) down_task<1, (R < kG8Tok ? R : kG8Tok)>(g, v, j0, c0, nt, act, rs, lane);
-                else down_task<NT, R>(g, v, j0, c0, nt, act, rs, lane);
+                if (NT == 1 || nt <= kG8Tok) down_task<1, (R < kG8Tok ? R : kG8Tok), BLK>(g, v, j0, c0, nt, act, rs, lane);
+                else down_task<NT, R, BLK>(g, v, j0, c0, nt, act, rs, lane);
             }
         }
         u = seg_end;
@@ -368,26 +409,40 @@ constexpr int kG8Small = 8;  // rows of the first GEMV list's groups (one MMA co
 // carve-out and ~85% with 115 KB).
 constexpr size_t kG8FastSmem = 120 * 1024;
 
+template <int R, bool BLK>
+cudaError_t launch_gu_as(const FfnGroups& g, const FfnPlanHeader* hdr, const int32_t* list, int which,
+                         cudaStream_t st) {
+    const size_t sm = gemv8_smem(g.d, R);
+    cudaError_t e = cudaFuncSetAttribute(gemv8_gate_up_kernel<R, BLK>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(gemv8_gate_up_kernel<R, BLK>, dim3(device_sm_count()), dim3(kG8Threads), sm, st, g,
+                      hdr, list, which);
+}
+
 template <int R>
 cudaError_t launch_gu(const FfnGroups& g, const FfnPlanHeader* hdr, const int32_t* list, int which,
                       cudaStream_t st) {
-    const size_t sm = gemv8_smem(g.d, R);
-    cudaError_t e = cudaFuncSetAttribute(gemv8_gate_up_kernel<R>,
+    return g.wblock ? launch_gu_as<R, true>(g, hdr, list, which, st)
+                    : launch_gu_as<R, false>(g, hdr, list, which, st);
+}
+
+template <int R, bool BLK>
+cudaError_t launch_dn_as(const FfnGroups& g, const FfnPlanHeader* hdr, const int32_t* list, int which,
+                         int max_inter, cudaStream_t st) {
+    const size_t sm = gemv8_smem(max_inter, R);
+    cudaError_t e = cudaFuncSetAttribute(gemv8_down_kernel<R, BLK>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (e != cudaSuccess) return e;
-    return launch_pdl(gemv8_gate_up_kernel<R>, dim3(device_sm_count()), dim3(kG8Threads), sm, st, g, hdr, list,
-                      which);
+    return launch_pdl(gemv8_down_kernel<R, BLK>, dim3(device_sm_count()), dim3(kG8Threads), sm, st, g,
+                      hdr, list, which);
 }
 
 template <int R>
 cudaError_t launch_dn(const FfnGroups& g, const FfnPlanHeader* hdr, const int32_t* list, int which,
                       int max_inter, cudaStream_t st) {
-    const size_t sm = gemv8_smem(max_inter, R);
-    cudaError_t e = cudaFuncSetAttribute(gemv8_down_kernel<R>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-    if (e != cudaSuccess) return e;
-    return launch_pdl(gemv8_down_kernel<R>, dim3(device_sm_count()), dim3(kG8Threads), sm, st, g, hdr, list,
-                      which);
+    return g.wblock ? launch_dn_as<R, true>(g, hdr, list, which, max_inter, st)
+                    : launch_dn_as<R, false>(g, hdr, list, which, max_inter, st);
 }
 
 }  // namespace

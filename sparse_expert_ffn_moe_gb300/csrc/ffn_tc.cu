@@ -88,6 +88,19 @@ constexpr uint32_t kABytes = BMC * BK * 2;  // 16 KB
 constexpr int kThreadsTc = 192;
 constexpr uint32_t kTmemCols = 512;
 
+// Block-scaled 8-bit weights (A8 == 3: two activation planes as A8 == 2, one
+// weight scale per 128 x 128 block).  A block scale changes every 128 values
+// of K, so it cannot be applied to an accumulator that sums all of K: each
+// 128-deep K block (one ring stage) is multiplied into a fresh accumulator,
+// and the epilogue warps add it, times the block's scale, to fp32 sums held in
+// registers -- the two accumulators alternate per K block instead of per tile.
+// Eight epilogue warps (two per tensor-memory lane quarter, half of the tile's
+// 256 columns each) hold 128 sums per thread.
+constexpr int kThreadsBlk = 320;
+template <bool W8, int A8> constexpr int threads_of() {
+    return W8 ? (6 + 8) * 32 : (A8 == 3 ? kThreadsBlk : kThreadsTc);
+}
+
 // Small-row ring (SMA, single-SM bf16 or W8A8 tiles whose groups all have at most kSmaRows
 // rows, e.g. every group of a decode batch of <= 32 tokens): an activation
 // stage holds 32 rows (4 KB) instead of 128, so the ring carries 6 weight
@@ -130,6 +143,7 @@ template <bool PAIR> struct A2Shape {
 };
 template <bool PAIR, bool SMA, int A8> struct RingOf { using type = Shape<PAIR, SMA>; };
 template <bool PAIR, bool SMA> struct RingOf<PAIR, SMA, 2> { using type = A2Shape<PAIR>; };
+template <bool PAIR, bool SMA> struct RingOf<PAIR, SMA, 3> { using type = A2Shape<PAIR>; };
 
 enum Epi { EPI_SWIGLU = 0, EPI_STORE_BF16 = 1, EPI_STORE_F32 = 2, EPI_COMBINE = 3 };
 
@@ -164,6 +178,7 @@ constexpr int kW8MaxA = 4;
 constexpr int kW8MaxRaw = 4;
 constexpr uint32_t kW8RingBytes = W8Shape<false>::kRingBytes;
 constexpr int kThreadsW8 = (6 + kW8ConvWarps) * 32;  // + the converter warps
+static_assert(threads_of<true, 0>() == kThreadsW8, "W8 threads");
 
 // Activation maps come in four box heights; a CTA loads the smallest box that
 // covers its valid rows.  The MMA still reads all 128 rows of the stage: rows
@@ -219,8 +234,9 @@ struct TcParams {
     CUtensorMap q0[2];          // W8: E4M3 gate / down codes, box 128 rows x 128 codes
     CUtensorMap q1[2];          // W8: E4M3 up codes (SWIGLU only)
     CUtensorMap qw[2];          // W8: E4M3 codes, box 256 rows x 128 codes (non-SWIGLU)
-    const float* sc0[2];        // W8, A8: scale of each gate / down weight row
-    const float* sc1[2];        // W8, A8: scale of each up weight row
+    const float* sc0[2];        // W8, A8: scale of each gate / down weight row (A8 == 3:
+                                // of each 128 x 128 block, [rows / 128][K / 128])
+    const float* sc1[2];        // W8, A8: scale of each up weight row (A8 == 3: block)
     const float* sa[2];         // A8: scale of each activation row (routed, shared)
     unsigned int* hmax[2];      // A8 gate/up: per-row max |h| as fp32 bits, raised atomically
     CUtensorMap g64[2];         // half pair tiles, gate/up: gate rows, box 64 rows
@@ -440,19 +456,21 @@ __device__ __forceinline__ void tile_scales16(const float (&s)[8], int lane0, fl
 }
 
 template <int EPI, bool PAIR, bool W8 = false, int A8 = 0, bool SMA = false>
-__global__ void __launch_bounds__(W8 ? kThreadsW8 : kThreadsTc, 1)
+__global__ void __launch_bounds__(threads_of<W8, A8>(), 1)
 tc_gemm_kernel(const __grid_constant__ TcParams p) {
     static_assert(!(W8 && EPI == EPI_STORE_F32), "8-bit weights feed the expert GEMMs only");
     static_assert(!(SMA && (PAIR || W8)), "small-row ring: single-SM tiles without the W8 rings");
     static_assert(!(A8 && (W8 || EPI == EPI_STORE_F32)), "A8: 8-bit operands, expert GEMMs only");
-    static_assert(!(A8 == 2 && SMA), "two activation planes: the full-size rings");
+    static_assert(!(A8 >= 2 && SMA), "two activation planes: the full-size rings");
+    static_assert(!(A8 == 3 && EPI != EPI_SWIGLU && EPI != EPI_STORE_BF16), "block scales: expert GEMMs");
     using S = typename RingOf<PAIR, SMA, A8>::type;
-    constexpr uint32_t kAPlanes = A8 == 2 ? 2u : 1u;  // activation tiles per stage
+    constexpr uint32_t kAPlanes = A8 >= 2 ? 2u : 1u;  // activation tiles per stage
+    constexpr bool kBlk = A8 == 3;  // block-scaled weights: one accumulator hand-off per K block
     using W = W8Shape<PAIR>;
     constexpr uint32_t kAStride = S::kAStride;  // bytes per activation stage (W8: kABytes)
     // A8: both operands E4M3 (kind::f8f6f4); a 128-byte K block holds 128 values
     constexpr int kKStep = A8 ? 2 * BK : BK;
-    constexpr int kEpiWarps = 4;  // warps 2..5
+    constexpr int kEpiWarps = kBlk ? 8 : 4;  // warps 2..5 (2..9)
     constexpr int kStages = W8 ? W::kConv : S::kStages;  // B stages (and A stages without W8)
     constexpr int kAStages = W8 ? W::kA : S::kStages;
     // swapped tiles (few rows): bf16 single-SM expert GEMMs only
@@ -714,7 +732,7 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
                                 const uint32_t fb = full0 + (uint32_t)(stage * sizeof(uint64_t));
                                 if (rank == 0) ptx::mbar_arrive_expect_tx(&ctl->full[stage], tx);
                                 if (rows_me > 0) {
-                                    if constexpr (A8 == 2) {  // hi and lo codes of K block kb
+                                    if constexpr (A8 >= 2) {  // hi and lo codes of K block kb
                                         ptx::tma_load_2d_pair(a_dst, ma, fb, 2 * k0, arow);
                                         ptx::tma_load_2d_pair(a_dst + kABytes, ma, fb, 2 * k0 + 128, arow);
                                     } else {
@@ -724,7 +742,7 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
                                 load_b_pair(b_dst, fb, k0, mb, brow);
                             } else {
                                 ptx::mbar_arrive_expect_tx(&ctl->full[stage], tx);
-                                if constexpr (A8 == 2) {
+                                if constexpr (A8 >= 2) {
                                     ptx::tma_load_2d(a_dst, ma, &ctl->full[stage], 2 * k0, arow);
                                     ptx::tma_load_2d(a_dst + kABytes, ma, &ctl->full[stage], 2 * k0 + 128, arow);
                                 } else {
@@ -819,14 +837,19 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
                 if (t + n_units < n_tiles) entry_next = fetch_tile_entry(p, t + n_units);
                 const Tile tl = decode_tile_entry<EPI, PAIR, kKStep>(p, entry, t);
                 if (!tl.valid) continue;
-                if (!wait_bounded(&ctl->tempty[acc], acc_phase ^ 1u, ctl, p, 200)) { ok = false; break; }
+                if (!kBlk && !wait_bounded(&ctl->tempty[acc], acc_phase ^ 1u, ctl, p, 200)) { ok = false; break; }
                 ptx::tc_fence_after();
-                const uint32_t d_tmem = tmem + (uint32_t)(acc * BN);
+                uint32_t d_tmem = tmem + (uint32_t)(acc * BN);
                 const uint32_t id_t = tl.half ? idesc_half : idesc;
                 const bool swp = kSwap && tl.swap;
                 // swapped: M = 128, N = the box rows (within the small-row ring's 32-row stage)
                 const uint32_t id_sw = ptx::idesc_bf16_f32(BMC, SMA ? min(tl.nsw, kSmaRows) : tl.nsw);
                 for (int kb = 0; kb < tl.kblocks; ++kb) {
+                    if constexpr (kBlk) {  // each K block into a drained accumulator
+                        if (!wait_bounded(&ctl->tempty[acc], acc_phase ^ 1u, ctl, p, 203)) { ok = false; break; }
+                        ptx::tc_fence_after();
+                        d_tmem = tmem + (uint32_t)(acc * BN);
+                    }
                     if (!wait_bounded(&ctl->full[stage], phase, ctl, p, 201)) { ok = false; break; }
                     if (W8 && !wait_bounded(&ctl->afull[ast], aphase, ctl, p, 202)) { ok = false; break; }
                     ptx::tc_fence_after();
@@ -854,11 +877,11 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint64_t ad = ptx::sw128_kmajor_desc(a_base + kk * 32);
                         const uint64_t bd = ptx::sw128_kmajor_desc(b_base + kk * 32);
-                        const uint32_t accum = (kb | kk) != 0 ? 1u : 0u;
+                        const uint32_t accum = ((kBlk ? 0 : kb) | kk) != 0 ? 1u : 0u;
                         if constexpr (A8) {
                             if constexpr (PAIR) ptx::tc_mma_f8_pair(d_tmem, ad, bd, id_t, accum);
                             else ptx::tc_mma_f8(d_tmem, ad, bd, idesc, accum);
-                            if constexpr (A8 == 2) {  // the lo plane times the same weights
+                            if constexpr (A8 >= 2) {  // the lo plane times the same weights
                                 const uint64_t ad2 = ptx::sw128_kmajor_desc(a_base + kABytes + kk * 32);
                                 if constexpr (PAIR) ptx::tc_mma_f8_pair(d_tmem, ad2, bd, id_t, 1u);
                                 else ptx::tc_mma_f8(d_tmem, ad2, bd, idesc, 1u);
@@ -876,12 +899,19 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
                         else ptx::tc_commit(&ctl->aempty[ast]);
                         if (++ast == W::kA) { ast = 0; aphase ^= 1u; }
                     }
+                    if constexpr (kBlk) {
+                        if constexpr (PAIR) ptx::tc_commit_pair(&ctl->tfull[acc], 0x3);
+                        else ptx::tc_commit(&ctl->tfull[acc]);
+                        if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+                    }
                     if (++stage == kStages) { stage = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
-                if constexpr (PAIR) ptx::tc_commit_pair(&ctl->tfull[acc], 0x3);
-                else ptx::tc_commit(&ctl->tfull[acc]);
-                if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+                if constexpr (!kBlk) {
+                    if constexpr (PAIR) ptx::tc_commit_pair(&ctl->tfull[acc], 0x3);
+                    else ptx::tc_commit(&ctl->tfull[acc]);
+                    if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+                }
             }
             if (!ok && any) {
                 // drain: every MMA issued completes before tensor memory is freed
@@ -890,6 +920,107 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
                 const uint64_t t0 = ptx::globaltimer_ns();
                 while (!ptx::mbar_try_wait(&ctl->drain, 0) &&
                        ptx::globaltimer_ns() - t0 < p.timeout_ns) {
+                }
+            }
+        }
+    } else if (kBlk) {
+        // ------------------------------------------------ epilogue, block-scaled weights (warps 2..9)
+        // Warp pair (w, w + 4) shares tensor-memory lane quarter w & 3; `half`
+        // picks its columns: SWIGLU, gate columns 64 half .. +63 and the up
+        // columns 128 + 64 half .. +63 (the same intermediate indices, one
+        // weight block row); STORE, output columns 128 half .. +127 (weight
+        // block row wrow0 / 128 + half).  Per K block: wait for its accumulator,
+        // add scale * products to the 128 register sums, free the accumulator.
+        // After the tile's last K block: times the activation row's scale, store.
+        const int quad = warp & 3;
+        const int half = (warp - 2) >> 2;
+        const int r = quad * 32 + lane;  // accumulator row owned by this thread
+        const uint32_t tempty0 = PAIR ? ptx::map_to_rank(&ctl->tempty[0], 0) : 0u;
+        constexpr int kPart = 64;  // columns of each of the two parts a thread sums
+        const int c_a = EPI == EPI_SWIGLU ? kPart * half : 2 * kPart * half;
+        const int c_b = EPI == EPI_SWIGLU ? BN / 2 + kPart * half : 2 * kPart * half + kPart;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        bool ok = true;
+        for (int t = unit; t < n_tiles && ok; t += n_units) {
+            const Tile tl = decode_tile<EPI, PAIR, kKStep>(p, list_len, t);
+            if (!tl.valid) continue;
+            const int rows_me = max(0, min(BMC, tl.rows - (int)rank * BMC));
+            const bool row_ok = r < rows_me;
+            const int arow_me = tl.row0 + (int)rank * BMC + r;
+            const int nvalid = p.n_out[tl.kind];
+            const int nkb = tl.kblocks;
+            // the scales of this warp's weight block row(s) along K
+            const int out0 = EPI == EPI_SWIGLU ? tl.n0 + kPart * half : tl.n0 + 2 * kPart * half;
+            const bool cols_ok = out0 < nvalid;  // n_out is a multiple of 128
+            const int64_t brow = (int64_t)(tl.wrow0 / kWBlock + (EPI == EPI_SWIGLU ? 0 : half)) * nkb;
+            const float* s_a = p.sc0[tl.kind] + brow;
+            const float* s_b = (EPI == EPI_SWIGLU ? p.sc1[tl.kind] : p.sc0[tl.kind]) + brow;
+            const float sa = row_ok ? __ldg(p.sa[tl.kind] + arow_me) : 0.0f;
+            float sum[2 * kPart];
+#pragma unroll
+            for (int k = 0; k < 2 * kPart; ++k) sum[k] = 0.0f;
+            float ws_a = cols_ok ? __ldg(s_a) : 0.0f, ws_b = cols_ok ? __ldg(s_b) : 0.0f;
+            for (int kb = 0; kb < nkb; ++kb) {
+                // the next K block's scales are requested before this block's wait
+                const bool nx = cols_ok && kb + 1 < nkb;
+                const float nx_a = nx ? __ldg(s_a + kb + 1) : 0.0f;
+                const float nx_b = nx ? __ldg(s_b + kb + 1) : 0.0f;
+                const int okw = lane == 0 ? (int)wait_bounded(&ctl->tfull[acc], acc_phase, ctl, p, 310) : 0;
+                if (!__shfl_sync(0xffffffffu, okw, 0)) { ok = false; break; }
+                ptx::tc_fence_after();
+                const uint32_t tbase = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * BN);
+#pragma unroll
+                for (int c = 0; c < kPart; c += 16) {
+                    uint32_t va[16], vb[16];
+                    ptx::tmem_ld16(tbase + c_a + c, va);
+                    ptx::tmem_ld16(tbase + c_b + c, vb);
+                    ptx::tmem_ld_wait();
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) {
+                        sum[c + k] = fmaf(ws_a, __uint_as_float(va[k]), sum[c + k]);
+                        sum[kPart + c + k] = fmaf(ws_b, __uint_as_float(vb[k]), sum[kPart + c + k]);
+                    }
+                }
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    if constexpr (PAIR) ptx::mbar_arrive_cluster(tempty0 + (uint32_t)(acc * sizeof(uint64_t)));
+                    else ptx::mbar_arrive(&ctl->tempty[acc]);
+                }
+                if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+                ws_a = nx_a;
+                ws_b = nx_b;
+            }
+            if (!ok || !row_ok || !cols_ok) continue;
+            bf16* out = (bf16*)p.out[tl.kind] + (int64_t)arow_me * p.ld_out[tl.kind] + out0;
+            if constexpr (EPI == EPI_SWIGLU) {
+                uint32_t hmax_bits = 0;
+#pragma unroll
+                for (int c = 0; c < kPart; c += 8) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const float h0 = silu_mul(sum[c + 2 * k] * sa, sum[kPart + c + 2 * k] * sa);
+                        const float h1 = silu_mul(sum[c + 2 * k + 1] * sa, sum[kPart + c + 2 * k + 1] * sa);
+                        const __nv_bfloat162 b2 = __floats2bfloat162_rn(h0, h1);
+                        w[k] = *reinterpret_cast<const uint32_t*>(&b2);
+                        hmax_bits = max(hmax_bits, max(w[k] & 0x7FFFu, (w[k] >> 16) & 0x7FFFu));
+                    }
+                    *reinterpret_cast<uint4*>(out + c) = make_uint4(w[0], w[1], w[2], w[3]);
+                }
+                // the row's max |h| over every tile of the row, for its two-plane split
+                if (hmax_bits != 0) atomicMax(p.hmax[tl.kind] + arow_me, hmax_bits << 16);
+            } else {
+#pragma unroll
+                for (int c = 0; c < 2 * kPart; c += 8) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const __nv_bfloat162 b2 = __floats2bfloat162_rn(sum[c + 2 * k] * sa, sum[c + 2 * k + 1] * sa);
+                        w[k] = *reinterpret_cast<const uint32_t*>(&b2);
+                    }
+                    *reinterpret_cast<uint4*>(out + c) = make_uint4(w[0], w[1], w[2], w[3]);
                 }
             }
         }
@@ -1362,7 +1493,7 @@ cudaError_t launch_tc(const TcParams& p, cudaStream_t st, bool allow_pdl = true)
     if constexpr (PAIR) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(2 * units);
-        cfg.blockDim = dim3(W8 ? kThreadsW8 : kThreadsTc);
+        cfg.blockDim = dim3(threads_of<W8, A8>());
         cfg.dynamicSmemBytes = smem;
         cfg.stream = st;
         cudaLaunchAttribute attr[2];
@@ -1378,10 +1509,10 @@ cudaError_t launch_tc(const TcParams& p, cudaStream_t st, bool allow_pdl = true)
         if (e != cudaSuccess) return e;
     } else if (allow_pdl) {
         e = launch_pdl(tc_gemm_kernel<EPI, PAIR, W8, A8, SMA>, dim3(units),
-                       dim3(W8 ? kThreadsW8 : kThreadsTc), smem, st, p);
+                       dim3(threads_of<W8, A8>()), smem, st, p);
         if (e != cudaSuccess) return e;
     } else {
-        tc_gemm_kernel<EPI, PAIR, W8, A8, SMA><<<units, W8 ? kThreadsW8 : kThreadsTc, smem, st>>>(p);
+        tc_gemm_kernel<EPI, PAIR, W8, A8, SMA><<<units, threads_of<W8, A8>(), smem, st>>>(p);
     }
     return cudaGetLastError();
 }
@@ -1544,7 +1675,7 @@ cudaError_t launch_shapes(TcParams& p, const int4* pair_list, const int4* single
     if (e == cudaSuccess) {
         p.mtiles = single_list;
         p.band = 0;
-        if constexpr (!W8 && A8 != 2) {
+        if constexpr (!W8 && A8 < 2) {
             if (small_rows && small_ring()) return launch_tc<EPI, false, false, A8, true>(p, sh.st2, pdl);
         }
         e = launch_tc<EPI, false, W8, A8>(p, sh.st2, pdl);
@@ -1947,6 +2078,11 @@ cudaError_t launch_ffn_tc_a8_gate_up(const FfnGroups& g, const FfnPlanHeader* hd
     p.test_stall = test_stall();
     TwoShapes sh(may_pair, st, true);
     const bool small = g.max_group_rows > 0 && g.max_group_rows <= kSmaRows;
+    if (planes == 2 && g.wblock) {  // block-scaled weights: full-height pair tiles only
+        p.half_tiles = 0;
+        return sh.finish(launch_shapes<EPI_SWIGLU, false, 3>(p, mtile_list + max_mtiles, mtile_list,
+                                                             may_pair, sh, true));
+    }
     if (planes == 2)
         return sh.finish(launch_shapes<EPI_SWIGLU, false, 2>(p, mtile_list + max_mtiles, mtile_list,
                                                              may_pair, sh, true));
@@ -1999,6 +2135,11 @@ cudaError_t launch_ffn_tc_a8_down(const FfnGroups& g, const FfnPlanHeader* hdr,
     q.test_stall = test_stall();
     TwoShapes sh(may_pair, st, true);
     const bool small = g.max_group_rows > 0 && g.max_group_rows <= kSmaRows;
+    if (planes == 2 && g.wblock) {
+        q.half_tiles = 0;
+        return sh.finish(launch_shapes<EPI_STORE_BF16, false, 3>(q, mtile_list + max_mtiles, mtile_list,
+                                                                 may_pair, sh, sh.side == nullptr));
+    }
     if (planes == 2)
         return sh.finish(launch_shapes<EPI_STORE_BF16, false, 2>(q, mtile_list + max_mtiles, mtile_list,
                                                                  may_pair, sh, sh.side == nullptr));

@@ -12,6 +12,9 @@ namespace moe {
 
 struct DevError;
 
+// Side of the square weight-scale blocks of block-scaled 8-bit weights.
+constexpr int kWBlock = 128;
+
 // Device-built work plan for the grouped expert FFN.  Group g < E is routed
 // expert g with rows [offsets[g], offsets[g+1]) of the permuted row space;
 // group E (when present) is the shared expert, whose rows are the T tokens.
@@ -37,6 +40,8 @@ struct FfnGroups {
     int n_routed_rows; // T*K (rows of x_perm / h / y_perm)
     int max_group_rows; // bound on any group's rows (0: unknown); <= 32 selects the small-row ring
     int g8_prefetch;    // 8-bit GEMV: prefetch each warp's next weight blocks into L2
+    int wblock;         // 8-bit weights: 0, s_* below are row scales; kWBlock, one
+                        // scale per 128 x 128 block of the stacked matrices
     int T;             // tokens (rows of the shared group)
     const int32_t* offsets;  // [E+1] device
     const int32_t* row_src;  // [n_routed_rows] token of each routed row, or
@@ -52,8 +57,10 @@ struct FfnGroups {
     const void* ws_gate;     // [Is][d]
     const void* ws_up;
     const void* ws_down;     // [d][Is]
-    // 8-bit weights (launch_ffn_tc_fp8 only): the w_* / ws_* pointers above
-    // hold E4M3 codes and these the fp32 scale of each weight row
+    // 8-bit weights: the w_* / ws_* pointers above hold E4M3 codes and these
+    // the fp32 scale of each weight row (wblock = 0) or of each 128 x 128 block
+    // (wblock = kWBlock: s_gate/s_up [E*I/128][d/128], s_down [E*d/128][I/128],
+    // ss_gate/ss_up [Is/128][d/128], ss_down [d/128][Is/128])
     const float* s_gate;     // [E][I]
     const float* s_up;       // [E][I]
     const float* s_down;     // [E][d]
@@ -197,6 +204,9 @@ cudaError_t launch_ffn_gemv_fp8(const FfnGroups& g, const FfnPlanHeader* hdr, co
 // ---- quant.cu ----
 cudaError_t launch_quantize_fp8_rows(int64_t rows, int64_t cols, int dtype, const void* w,
                                      uint8_t* codes, float* scales, cudaStream_t st);
+// one scale per 128 x 128 block: scales [ceil(rows/128)][ceil(cols/128)]
+cudaError_t launch_quantize_fp8_blocks(int64_t rows, int64_t cols, int dtype, const void* w,
+                                       uint8_t* codes, float* scales, cudaStream_t st);
 // bf16 activation rows (cols <= 16384): row r read at w + r * ld_in elements,
 // its codes written at codes + r * ld_out bytes (may be the row's own storage)
 cudaError_t launch_quantize_act_rows(int64_t rows, int cols, const void* w, int64_t ld_in,

@@ -466,6 +466,19 @@ moe_status moe_quantize_fp8_rows(int64_t rows, int64_t cols, int32_t dtype, cons
                                                 (cudaStream_t)stream));
 }
 
+moe_status moe_quantize_fp8_blocks(int64_t rows, int64_t cols, int32_t dtype, const void* w,
+                                   uint8_t* codes, float* scales, void* stream) {
+    if (rows < 0 || cols <= 0) return MOE_ERR_INVALID_ARG;
+    if (dtype != MOE_F32 && dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+    // the block grid: ceil(cols / 128) x ceil(rows / 128) thread blocks
+    if ((rows + kWBlock - 1) / kWBlock > 65535 || cols % 16 || cols >= ((int64_t)1 << 31))
+        return MOE_ERR_UNSUPPORTED;
+    if (rows == 0) return MOE_OK;
+    if (!w || !codes || !scales || !aligned16(w) || !aligned16(codes)) return MOE_ERR_INVALID_ARG;
+    return cuda_status(launch_quantize_fp8_blocks(rows, cols, dtype, w, codes, scales,
+                                                  (cudaStream_t)stream));
+}
+
 // The tensor-core groups of an 8-bit-weight call with two-plane activations:
 // g.a_perm / g.a_shared hold the planes of the routed / shared rows and
 // g.sa_routed / g.sa_shared their scales; the plan is built.  Gate/up GEMM
@@ -493,9 +506,13 @@ static cudaError_t run_tc_planes(const moe_shape& s, FfnGroups& g, const WsLayou
     return e;
 }
 
-moe_status moe_expert_ffn_fp8(const moe_shape* shape, const void* x_perm, const int32_t* offsets,
-                              const moe_fp8_experts* w, void* y_perm, void* workspace,
-                              size_t ws_bytes, void* stream) {
+// moe_expert_ffn_fp8 (wblock = 0: row scales) and moe_expert_ffn_fp8_blocks
+// (wblock = kWBlock: 128 x 128 block scales, whose tensor-core groups always
+// take the two-plane path).
+static moe_status expert_ffn_fp8_call(const moe_shape* shape, const void* x_perm,
+                                      const int32_t* offsets, const moe_fp8_experts* w,
+                                      void* y_perm, void* workspace, size_t ws_bytes, void* stream,
+                                      int wblock) {
     moe_status st = check_shape(shape);
     if (st != MOE_OK) return st;
     const moe_shape& s = *shape;
@@ -530,6 +547,7 @@ moe_status moe_expert_ffn_fp8(const moe_shape* shape, const void* x_perm, const 
     g.s_gate = w->s_gate;
     g.s_up = w->s_up;
     g.s_down = w->s_down;
+    g.wblock = wblock;
     g.h = at<void>(workspace, L.h);
     g.y = y_perm;
     FfnPlanHeader* hdr = at<FfnPlanHeader>(workspace, L.plan);
@@ -538,7 +556,7 @@ moe_status moe_expert_ffn_fp8(const moe_shape* shape, const void* x_perm, const 
     const int lim = gemv8_limit(s);
     const int64_t R = (int64_t)s.T * s.K;
     // a group has at most T*K rows here (the offsets are the caller's)
-    const bool planes = R > lim && w8_planes();
+    const bool planes = R > lim && (w8_planes() || wblock != 0);
     const bool pair = planes || w8_pair();
     if (planes) {
         // the rows' two planes (2d codes per row) and their scales
@@ -560,9 +578,24 @@ moe_status moe_expert_ffn_fp8(const moe_shape* shape, const void* x_perm, const 
     return cuda_status(e);
 }
 
-moe_status moe_forward_fp8(const moe_shape* shape, const void* x, const void* w_g, const float* bias,
-                           const moe_fp8_experts* w, void* y, void* workspace, size_t ws_bytes,
-                           void* stream) {
+moe_status moe_expert_ffn_fp8(const moe_shape* shape, const void* x_perm, const int32_t* offsets,
+                              const moe_fp8_experts* w, void* y_perm, void* workspace,
+                              size_t ws_bytes, void* stream) {
+    return expert_ffn_fp8_call(shape, x_perm, offsets, w, y_perm, workspace, ws_bytes, stream, 0);
+}
+
+moe_status moe_expert_ffn_fp8_blocks(const moe_shape* shape, const void* x_perm,
+                                     const int32_t* offsets, const moe_fp8_experts* w,
+                                     void* y_perm, void* workspace, size_t ws_bytes,
+                                     void* stream) {
+    return expert_ffn_fp8_call(shape, x_perm, offsets, w, y_perm, workspace, ws_bytes, stream,
+                               kWBlock);
+}
+
+// moe_forward_fp8 (wblock = 0) and moe_forward_fp8_blocks (wblock = kWBlock).
+static moe_status forward_fp8_call(const moe_shape* shape, const void* x, const void* w_g,
+                                   const float* bias, const moe_fp8_experts* w, void* y,
+                                   void* workspace, size_t ws_bytes, void* stream, int wblock) {
     moe_status st = check_shape(shape);
     if (st != MOE_OK) return st;
     const moe_shape& s = *shape;
@@ -618,6 +651,7 @@ moe_status moe_forward_fp8(const moe_shape* shape, const void* x, const void* w_
     g.ss_gate = w->ss_gate;
     g.ss_up = w->ss_up;
     g.ss_down = w->ss_down;
+    g.wblock = wblock;
     g.h = at<void>(workspace, L.h);
     g.h_s = at<void>(workspace, L.h_s);
     g.y = at<void>(workspace, L.y_perm);
@@ -627,7 +661,7 @@ moe_status moe_forward_fp8(const moe_shape* shape, const void* x, const void* w_
     int4* mtiles = at<int4>(workspace, L.mtile_list);
     const int lim = gemv8_limit(s);
     // a group has at most T rows (a token picks an expert once; the shared group has T)
-    const bool planes = s.T > lim && w8_planes();
+    const bool planes = s.T > lim && (w8_planes() || wblock != 0);
     const bool pair = planes || w8_pair();
     const int64_t R = (int64_t)s.T * s.K;
     float* sc = at<float>(workspace, L.ascale);
@@ -678,6 +712,18 @@ moe_status moe_forward_fp8(const moe_shape* shape, const void* x, const void* w_
 
     // 4. combine
     return cuda_status(launch_combine(s, g.y, inv, topk_w, shared ? g.y_s : nullptr, y, cs));
+}
+
+moe_status moe_forward_fp8(const moe_shape* shape, const void* x, const void* w_g, const float* bias,
+                           const moe_fp8_experts* w, void* y, void* workspace, size_t ws_bytes,
+                           void* stream) {
+    return forward_fp8_call(shape, x, w_g, bias, w, y, workspace, ws_bytes, stream, 0);
+}
+
+moe_status moe_forward_fp8_blocks(const moe_shape* shape, const void* x, const void* w_g,
+                                  const float* bias, const moe_fp8_experts* w, void* y,
+                                  void* workspace, size_t ws_bytes, void* stream) {
+    return forward_fp8_call(shape, x, w_g, bias, w, y, workspace, ws_bytes, stream, kWBlock);
 }
 
 // W8A8 expert stage on groups g whose a_perm / a_shared already hold E4M3 rows

@@ -1,5 +1,6 @@
-// quant.cu -- per-row E4M3 quantisation of expert weights (moe_quantize_fp8_rows)
-// and of the activation rows of 8-bit-activation experts.
+// quant.cu -- per-row and per-block E4M3 quantisation of expert weights
+// (moe_quantize_fp8_rows, moe_quantize_fp8_blocks) and of the activation rows
+// of 8-bit-activation experts.
 //
 // "LLM from scratch, ch. 6", section "second route: make every byte
 // cheaper": x_q = round(x / s) + z with a per-channel scale.  Here z = 0, the
@@ -90,6 +91,63 @@ quantize_rows_kernel(const T* __restrict__ w, uint8_t* __restrict__ codes,
             packed[k >> 2] |= (uint32_t)c << (8 * (k & 3));  // byte k of the 16-byte store
         }
         *reinterpret_cast<uint4*>(out + v * 16) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+    }
+}
+
+// 128 x 128 block scales (moe_quantize_fp8_blocks): one 256-thread block per
+// weight block (grid: column blocks x row blocks).  Each thread keeps its four
+// 16-value vectors of the block in registers across the max-reduction, so the
+// block is read once; the scale and code decisions are quantize_rows_kernel's,
+// over the block's elements.  Edge blocks are ragged: rows past the matrix and
+// columns past cols (cols a multiple of 16) are skipped.
+constexpr int kQBlk = 128;
+constexpr int kQBlkVecs = kQBlk * kQBlk / 16 / kQuantThreads;  // 4 vectors per thread
+
+template <typename T>
+__global__ void __launch_bounds__(kQuantThreads)
+quantize_blocks_kernel(const T* __restrict__ w, uint8_t* __restrict__ codes,
+                       float* __restrict__ scales, int64_t rows, int64_t cols) {
+    pdl_wait();
+    pdl_trigger();
+    __shared__ float red[kQuantThreads / 32];
+    const int64_t r0 = (int64_t)blockIdx.y * kQBlk, c0 = (int64_t)blockIdx.x * kQBlk;
+    const int64_t nr = min((int64_t)kQBlk, rows - r0), nc = min((int64_t)kQBlk, cols - c0);
+    float f[kQBlkVecs][16];
+    bool in[kQBlkVecs];
+    float amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < kQBlkVecs; ++j) {
+        const int v = (int)threadIdx.x + j * kQuantThreads;  // 8 vectors per block row
+        const int i = v >> 3, c = (v & 7) * 16;
+        in[j] = i < nr && c < nc;
+        if (in[j]) {
+            load16(w + (r0 + i) * cols + c0 + c, f[j]);
+#pragma unroll
+            for (int k = 0; k < 16; ++k) amax = fmaxf(amax, fabsf(f[j][k]));
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+    __syncthreads();
+    float m = 0.0f;
+#pragma unroll
+    for (int k = 0; k < kQuantThreads / 32; ++k) m = fmaxf(m, red[k]);
+    const float s = m > 0.0f ? m / 448.0f : 1.0f;
+    if (threadIdx.x == 0) scales[blockIdx.y * gridDim.x + blockIdx.x] = s;
+#pragma unroll
+    for (int j = 0; j < kQBlkVecs; ++j) {
+        if (!in[j]) continue;
+        const int v = (int)threadIdx.x + j * kQuantThreads;
+        const int i = v >> 3, c = (v & 7) * 16;
+        uint32_t packed[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const __nv_fp8_storage_t q = __nv_cvt_float_to_fp8(f[j][k] / s, __NV_SATFINITE, __NV_E4M3);
+            packed[k >> 2] |= (uint32_t)q << (8 * (k & 3));
+        }
+        *reinterpret_cast<uint4*>(codes + (r0 + i) * cols + c0 + c) =
+            make_uint4(packed[0], packed[1], packed[2], packed[3]);
     }
 }
 
@@ -364,6 +422,17 @@ cudaError_t launch_quantize_act_rows(int64_t rows, int cols, const void* w, int6
     if (cols % 16 || cols > kActVecs * kQuantThreads * 16) return cudaErrorInvalidValue;
     return launch_pdl(quantize_act_rows_kernel, dim3((unsigned)rows), dim3(kQuantThreads), 0, st,
                       (const bf16*)w, ld_in, codes, ld_out, scales, cols);
+}
+
+cudaError_t launch_quantize_fp8_blocks(int64_t rows, int64_t cols, int dtype, const void* w,
+                                       uint8_t* codes, float* scales, cudaStream_t st) {
+    if (rows <= 0) return cudaSuccess;
+    const dim3 grid((unsigned)((cols + kQBlk - 1) / kQBlk), (unsigned)((rows + kQBlk - 1) / kQBlk));
+    if (dtype == MOE_BF16)
+        return launch_pdl(quantize_blocks_kernel<bf16>, grid, dim3(kQuantThreads), 0, st,
+                          (const bf16*)w, codes, scales, rows, cols);
+    return launch_pdl(quantize_blocks_kernel<float>, grid, dim3(kQuantThreads), 0, st,
+                      (const float*)w, codes, scales, rows, cols);
 }
 
 cudaError_t launch_quantize_fp8_rows(int64_t rows, int64_t cols, int dtype, const void* w,

@@ -207,10 +207,11 @@ class Layer:
         import oracle
         c = self.cfg
         xh = host(self.x if x is None else x)
-        if c.weights == "e4m3":
+        if mi.is_fp8(c):
             return oracle.forward_tokens_fp8(tokens, xh, self.hp["w_g"], self.hp, c.K,
                                              dtype=c.dtype, bias=self.bias_host(),
-                                             router=c.router, act8=c.acts == "e4m3")
+                                             router=c.router, act8=c.acts == "e4m3",
+                                             blocks=c.weights == "e4m3b")
         return oracle.forward_tokens(tokens, xh, self.hp, c.K, dtype=c.dtype,
                                      bias=self.bias_host(), router=c.router)
 
@@ -226,6 +227,8 @@ class Layer:
         p = self.p
         if self.cfg.acts == "e4m3":
             moe.moe_forward_w8a8(s, x, p["w_g"], self.bias, moe.make_fp8_experts(p), y, ws)
+        elif self.cfg.weights == "e4m3b":
+            moe.moe_forward_fp8_blocks(s, x, p["w_g"], self.bias, moe.make_fp8_experts(p), y, ws)
         elif self.cfg.weights == "e4m3":
             moe.moe_forward_fp8(s, x, p["w_g"], self.bias, moe.make_fp8_experts(p), y, ws)
         else:
