@@ -81,10 +81,25 @@ def elem_bytes(cfg) -> int:
 
 def expert_bytes(cfg, inter: int) -> int:
     """Bytes of one expert's three matrices (E4M3: one byte per weight plus an
-    fp32 scale per weight row)."""
+    fp32 scale per weight row, or per 128 x 128 block)."""
     if cfg.weights == "e4m3":
         return 3 * cfg.d * inter + 4 * (2 * inter + cfg.d)
+    if cfg.weights == "e4m3b":
+        return 3 * cfg.d * inter + 4 * 3 * (-(-cfg.d // 128)) * (-(-inter // 128))
     return elem_bytes(cfg) * 3 * cfg.d * inter
+
+
+def fp8_calls(moe, cfg):
+    """The layer and expert-stage entry points of an 8-bit-weight workload (row
+    or block scales), or (None, None)."""
+    if cfg.weights == "e4m3b":
+        return moe.moe_forward_fp8_blocks, moe.moe_expert_ffn_fp8_blocks
+    if cfg.weights == "e4m3":
+        return moe.moe_forward_fp8, moe.moe_expert_ffn_fp8
+    return None, None
+
+
+WEIGHT_FORMAT = {"e4m3": "e4m3 + fp32 row scales", "e4m3b": "e4m3 + fp32 128x128 block scales"}
 
 
 def layer_bytes(cfg, n_active: int) -> int:
@@ -111,7 +126,8 @@ class Forward:
     def __init__(self, moe, cfg, s, p, bias, ws, stream):
         self.moe, self.cfg, self.s, self.p, self.bias, self.ws, self.stream = (
             moe, cfg, s, p, bias, ws, stream)
-        self.fp8 = moe.make_fp8_experts(p) if cfg.weights == "e4m3" else None
+        self.fp8 = moe.make_fp8_experts(p) if mi.is_fp8(cfg) else None
+        self.fwd8 = fp8_calls(moe, cfg)[0]
         self.a8 = cfg.acts == "e4m3"
 
     def __call__(self, x, y):
@@ -120,8 +136,7 @@ class Forward:
             m.moe_forward_w8a8(self.s, x, p["w_g"], self.bias, self.fp8, y, self.ws,
                                stream=self.stream)
         elif self.fp8 is not None:
-            m.moe_forward_fp8(self.s, x, p["w_g"], self.bias, self.fp8, y, self.ws,
-                              stream=self.stream)
+            self.fwd8(self.s, x, p["w_g"], self.bias, self.fp8, y, self.ws, stream=self.stream)
         else:
             m.moe_forward(self.s, x, p["w_g"], self.bias, p["w_gate"], p["w_up"], p["w_down"],
                           p.get("ws_gate"), p.get("ws_up"), p.get("ws_down"), y, self.ws,
@@ -131,10 +146,11 @@ class Forward:
 def oracle_tokens(cfg, tokens, x_host, p_host, bias_host):
     """The oracle's per-token layer in the workload's weight format."""
     import oracle
-    if cfg.weights == "e4m3":
+    if mi.is_fp8(cfg):
         return oracle.forward_tokens_fp8(tokens, x_host, p_host["w_g"], p_host, cfg.K,
                                          dtype=cfg.dtype, bias=bias_host, router=cfg.router,
-                                         act8=cfg.acts == "e4m3")
+                                         act8=cfg.acts == "e4m3",
+                                         blocks=cfg.weights == "e4m3b")
     return oracle.forward_tokens(tokens, x_host, p_host, cfg.K, dtype=cfg.dtype, bias=bias_host,
                                  router=cfg.router)
 
@@ -162,17 +178,18 @@ def launches_per_forward(cfg, gemv_limit: int = 0) -> int:
         pair = cfg.T > 128
         return router + disp_plan + 1 + 1 + (2 if pair else 1) + (2 if cfg.Is else 1) \
             + (2 if pair else 1) + 1
-    if cfg.weights == "e4m3":
+    if mi.is_fp8(cfg):
         # router + top-K, 3 dispatch kernels and the plan, the 8-bit GEMV
         # (gate/up and down for each of its two group lists), and when a group
-        # can exceed the GEMV limit: with two-plane activations (the default)
-        # the x split and the plane gather, the tcgen05 gate/up, the h split
-        # (+ h_s), the tcgen05 down -- gate/up and down twice when a group can
-        # take pair tiles; with the codes widened in the GEMM, the row gather
-        # and one gate/up and one down; combine
+        # can exceed the GEMV limit: with two-plane activations (the default;
+        # always with block scales) the x split and the plane gather, the
+        # tcgen05 gate/up, the h split (+ h_s), the tcgen05 down -- gate/up and
+        # down twice when a group can take pair tiles; with the codes widened
+        # in the GEMM, the row gather and one gate/up and one down; combine
         limit = int(os.environ.get("MOE_GEMV8_MAX_ROWS", "8"))
         gemv = (2 if limit > 0 else 0) + (2 if limit > 8 else 0)
-        if cfg.T > limit and os.environ.get("MOE_W8_PLANES", "1") != "0":
+        if cfg.T > limit and (os.environ.get("MOE_W8_PLANES", "1") != "0"
+                              or cfg.weights == "e4m3b"):
             pair = cfg.T > 128
             tc = 2 * (2 if pair else 1) + (2 if cfg.Is else 1)
             return router + disp_plan + 2 + gemv + tc + 1
@@ -413,13 +430,13 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": "e4m3" if cfg.acts == "e4m3" else cfg.dtype,
         "data": ("synthetic (seeded N(0,1) tokens, N(0,1/d) weights; no trained weights)"
-                 if cfg.weights != "e4m3" else
-                 "synthetic (seeded N(0,1) tokens; random E4M3 expert codes with fp32 row "
-                 "scales; no trained weights)"),
+                 if not mi.is_fp8(cfg) else
+                 f"synthetic (seeded N(0,1) tokens; random E4M3 expert codes with fp32 "
+                 f"{'row' if cfg.weights == 'e4m3' else '128x128 block'} scales; no trained "
+                 f"weights)"),
         "config": {"workload": cfg.name, "T": cfg.T, "d": cfg.d, "E": cfg.E, "K": cfg.K,
                    "inter": cfg.I, "inter_shared": cfg.Is, "active_experts": n_active,
-                   "expert_weights": "e4m3 + fp32 row scales" if cfg.weights == "e4m3"
-                                     else cfg.dtype,
+                   "expert_weights": WEIGHT_FORMAT.get(cfg.weights, cfg.dtype),
                    "expert_activations": ("e4m3 + fp32 row scales (x and h quantised per row)"
                                           if cfg.acts == "e4m3" else cfg.dtype),
                    "l2": "inputs larger than L2 (expert weights "
@@ -504,13 +521,14 @@ def time_expert_ffn(moe, cfg, x, p, bias, stream, steps: int, n_active: int) -> 
     moe.moe_route(s, x, p["w_g"], bias, None, None, idx, w, ws, stream=stream)
     moe.moe_permute(s, idx, x, counts, offsets, None, None, x_perm, ws, stream=stream)
 
-    fp8 = moe.make_fp8_experts(p) if cfg.weights == "e4m3" else None
+    fp8 = moe.make_fp8_experts(p) if mi.is_fp8(cfg) else None
+    ffn8 = fp8_calls(moe, cfg)[1]
 
     def run():
         if cfg.acts == "e4m3":
             moe.moe_expert_ffn_w8a8(s, x_perm, offsets, fp8, y_perm, ws, stream=stream)
         elif fp8 is not None:
-            moe.moe_expert_ffn_fp8(s, x_perm, offsets, fp8, y_perm, ws, stream=stream)
+            ffn8(s, x_perm, offsets, fp8, y_perm, ws, stream=stream)
         else:
             moe.moe_expert_ffn(s, x_perm, offsets, p["w_gate"], p["w_up"], p["w_down"], y_perm,
                                ws, stream=stream)
@@ -572,13 +590,15 @@ def stage_roofline(cfg, stage, peaks) -> dict:
     gbs = stage["bytes"] / sec / 1e9
     t_peak, t_kind = tensor_peak(cfg, peaks)
     t_frac, h_frac = tflops / t_peak, gbs / peaks["hbm_gbs"]
-    planes = os.environ.get("MOE_W8_PLANES", "1") != "0"
+    planes = os.environ.get("MOE_W8_PLANES", "1") != "0" or cfg.weights == "e4m3b"
     kernel = ("expert FFN stage: tcgen05 gate/up GEMM (SiLU*mul epilogue) + tcgen05 down GEMM "
               + ("on E4M3 weights and E4M3 activations (kind::f8f6f4, + x and h quantisers)"
                  if cfg.acts == "e4m3" else
                  ("on E4M3 weights with bf16 activations as two E4M3 planes (kind::f8f6f4, "
                   "+ x and h splits)" if planes else "on E4M3 weights widened in-kernel")
-                 if cfg.weights == "e4m3" else
+                 + (", 128x128 block scales applied per 128-deep K block in registers"
+                    if cfg.weights == "e4m3b" else "")
+                 if mi.is_fp8(cfg) else
                  "(+ plan, empty GEMV launches)"))
     common = {"traffic": stage_traffic(cfg.name),
               "traffic_unit": "bytes per launch pair (DRAM read + write, ncu)",
@@ -766,7 +786,8 @@ def bench_all(moe, peaks, args) -> list:
     for name in ("tiny_f32", "mixtral_prefill", "dsv3_decode", "dsv3_prefill_zipf",
                  *[f"dsv3_sweep_T{t}" for t in mi.SWEEP_T], "dsv3_decode_sigmoid",
                  "dsv3_decode_fp8", "dsv3_sweep_fp8_T64", "dsv3_sweep_fp8_T512",
-                 "mixtral_prefill_fp8", "dsv3_decode_w8a8", "dsv3_sweep_w8a8_T512",
+                 "mixtral_prefill_fp8", "dsv3_decode_fp8b", "dsv3_sweep_fp8b_T512",
+                 "mixtral_prefill_fp8b", "dsv3_decode_w8a8", "dsv3_sweep_w8a8_T512",
                  "dsv3_sweep_w8a8_T4096", "mixtral_prefill_w8a8", "dsv3_prefill_zipf_w8a8"):
         cfg = mi.CONFIGS[name]
         res.append(bench_workload(moe, cfg, peaks, steps=max(10, args.steps),
@@ -813,7 +834,8 @@ def run_stage_pool(args):
                           dtype=cfg.dtype, weights=cfg.weights, acts=cfg.acts, seed=cfg.seed)
     p = mi.make_weights(pcfg, "cuda", only={"w_gate", "w_up", "w_down", "s_gate", "s_up",
                                             "s_down"})
-    fp8 = moe.make_fp8_experts(p) if cfg.weights == "e4m3" else None
+    fp8 = moe.make_fp8_experts(p) if mi.is_fp8(cfg) else None
+    ffn8 = fp8_calls(moe, cfg)[1]
     x_perm = mi.normal((rows, cfg.d), 1.0, cfg.dtype, "cuda", cfg.seed, "x_perm")
     y_perm = torch.empty_like(x_perm)
     offsets = torch.tensor([0] + list(np.cumsum(counts)), dtype=torch.int32, device="cuda")
@@ -826,7 +848,7 @@ def run_stage_pool(args):
         if cfg.acts == "e4m3":
             moe.moe_expert_ffn_w8a8(s, x_perm, offsets, fp8, y_perm, ws, stream=st)
         elif fp8 is not None:
-            moe.moe_expert_ffn_fp8(s, x_perm, offsets, fp8, y_perm, ws, stream=st)
+            ffn8(s, x_perm, offsets, fp8, y_perm, ws, stream=st)
         else:
             moe.moe_expert_ffn(s, x_perm, offsets, p["w_gate"], p["w_up"], p["w_down"], y_perm,
                                ws, stream=st)

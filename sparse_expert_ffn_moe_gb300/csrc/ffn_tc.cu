@@ -95,8 +95,14 @@ constexpr uint32_t kTmemCols = 512;
 // and the epilogue warps add it, times the block's scale, to fp32 sums held in
 // registers -- the two accumulators alternate per K block instead of per tile.
 // Eight epilogue warps (two per tensor-memory lane quarter, half of the tile's
-// 256 columns each) hold 128 sums per thread.
+// 256 columns each) hold 128 sums per thread.  An accumulator is released once
+// per CTA: the eight warps meet at a named barrier after their last read of it
+// and one thread arrives.  The hand-off costs little on single-SM tiles (the
+// MMA issuer waits ~90 cycles per K block, measured on GB300); across a CTA
+// pair it waited ~1600 cycles for the peer's release, so block-scaled groups
+// take single-SM tiles unless MOE_W8_PAIR=1.
 constexpr int kThreadsBlk = 320;
+constexpr uint32_t kBlkEpiBar = 1;  // named barrier of the eight epilogue warps
 template <bool W8, int A8> constexpr int threads_of() {
     return W8 ? (6 + 8) * 32 : (A8 == 3 ? kThreadsBlk : kThreadsTc);
 }
@@ -508,7 +514,9 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
         }
         for (int a = 0; a < 2; ++a) {
             ptx::mbar_init(&ctl->tfull[a], 1);
-            ptx::mbar_init(&ctl->tempty[a], (PAIR ? 2 : 1) * kEpiWarps);
+            // block scales: one arrival per CTA per K block (after the epilogue
+            // warps' named barrier); otherwise one per epilogue warp per tile
+            ptx::mbar_init(&ctl->tempty[a], (PAIR ? 2 : 1) * (kBlk ? 1 : kEpiWarps));
         }
         ptx::mbar_init(&ctl->drain, 1);
         ctl->abort_flag = 0;
@@ -967,24 +975,29 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
                 const float nx_a = nx ? __ldg(s_a + kb + 1) : 0.0f;
                 const float nx_b = nx ? __ldg(s_b + kb + 1) : 0.0f;
                 const int okw = lane == 0 ? (int)wait_bounded(&ctl->tfull[acc], acc_phase, ctl, p, 310) : 0;
-                if (!__shfl_sync(0xffffffffu, okw, 0)) { ok = false; break; }
-                ptx::tc_fence_after();
-                const uint32_t tbase = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * BN);
+                const bool ready = __shfl_sync(0xffffffffu, okw, 0) != 0;
+                if (ready) {
+                    ptx::tc_fence_after();
+                    const uint32_t tbase = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * BN);
 #pragma unroll
-                for (int c = 0; c < kPart; c += 16) {
-                    uint32_t va[16], vb[16];
-                    ptx::tmem_ld16(tbase + c_a + c, va);
-                    ptx::tmem_ld16(tbase + c_b + c, vb);
-                    ptx::tmem_ld_wait();
+                    for (int c = 0; c < kPart; c += 16) {
+                        uint32_t va[16], vb[16];
+                        ptx::tmem_ld16(tbase + c_a + c, va);
+                        ptx::tmem_ld16(tbase + c_b + c, vb);
+                        ptx::tmem_ld_wait();
 #pragma unroll
-                    for (int k = 0; k < 16; ++k) {
-                        sum[c + k] = fmaf(ws_a, __uint_as_float(va[k]), sum[c + k]);
-                        sum[kPart + c + k] = fmaf(ws_b, __uint_as_float(vb[k]), sum[kPart + c + k]);
+                        for (int k = 0; k < 16; ++k) {
+                            sum[c + k] = fmaf(ws_a, __uint_as_float(va[k]), sum[c + k]);
+                            sum[kPart + c + k] = fmaf(ws_b, __uint_as_float(vb[k]), sum[kPart + c + k]);
+                        }
                     }
+                    ptx::tc_fence_before();
                 }
-                ptx::tc_fence_before();
-                __syncwarp();
-                if (lane == 0) {
+                // Every epilogue warp reaches this barrier whatever its wait gave (its
+                // only blocking step is that bounded wait), so it cannot hang; past it,
+                // all eight have read the accumulator, or all leave together.
+                if (!ptx::named_bar_and(kBlkEpiBar, 8 * 32, ready)) { ok = false; break; }
+                if (warp == 2 && lane == 0) {
                     if constexpr (PAIR) ptx::mbar_arrive_cluster(tempty0 + (uint32_t)(acc * sizeof(uint64_t)));
                     else ptx::mbar_arrive(&ctl->tempty[acc]);
                 }

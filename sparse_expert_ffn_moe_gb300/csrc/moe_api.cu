@@ -122,6 +122,18 @@ bool w8_pair() {
     return e && e[0] == '1';
 }
 
+// Whether the plan may give 8-bit-weight groups CTA-pair tiles: with two-plane
+// activations and row scales, yes; with the codes widened in the GEMM, or with
+// block scales, only when MOE_W8_PAIR=1.  Measured on GB300 (block scales,
+// Mixtral-shaped stage on a 4-expert pool): 1.72 ms on pair tiles, 1.13 ms on
+// single-SM tiles (row scales: 0.95 ms) -- per 128-deep K block the pair's MMA
+// issuer waited ~1600 cycles for the peer CTA to release the accumulator,
+// against ~400 on single tiles.
+bool w8_pair_tiles(bool planes, int wblock) {
+    if (wblock) return w8_pair();
+    return planes || w8_pair();
+}
+
 // Tensor-core groups of the 8-bit-weight entry points carry their bf16
 // activations as two E4M3 planes on the 8-bit-by-8-bit MMA (MOE_W8_PLANES,
 // read per call; 0 widens the codes to bf16 inside the GEMM instead).
@@ -486,11 +498,11 @@ moe_status moe_quantize_fp8_blocks(int64_t rows, int64_t cols, int32_t dtype, co
 // place, down GEMM.  Groups on the 8-bit GEMV have run before (their bf16 h
 // rows, already consumed, are split along with the rest and never read).
 static cudaError_t run_tc_planes(const moe_shape& s, FfnGroups& g, const WsLayout& L, void* ws,
-                                 int64_t max_rows, DevError* err, cudaStream_t cs) {
+                                 int64_t max_rows, bool pair, DevError* err, cudaStream_t cs) {
     FfnPlanHeader* hdr = at<FfnPlanHeader>(ws, L.plan);
     int4* mtiles = at<int4>(ws, L.mtile_list);
     const int64_t R = (int64_t)s.T * s.K;
-    const bool may_pair = tc_pair_possible(max_rows);
+    const bool may_pair = pair && tc_pair_possible(max_rows);
     cudaError_t e = cudaMemsetAsync(const_cast<float*>(g.sa_h), 0, sizeof(float) * R, cs);
     if (e == cudaSuccess && g.has_shared)
         e = cudaMemsetAsync(const_cast<float*>(g.sa_hs), 0, sizeof(float) * s.T, cs);
@@ -557,7 +569,7 @@ static moe_status expert_ffn_fp8_call(const moe_shape* shape, const void* x_perm
     const int64_t R = (int64_t)s.T * s.K;
     // a group has at most T*K rows here (the offsets are the caller's)
     const bool planes = R > lim && (w8_planes() || wblock != 0);
-    const bool pair = planes || w8_pair();
+    const bool pair = w8_pair_tiles(planes, wblock);
     if (planes) {
         // the rows' two planes (2d codes per row) and their scales
         float* sc = at<float>(workspace, L.ascale);
@@ -572,7 +584,7 @@ static moe_status expert_ffn_fp8_call(const moe_shape* shape, const void* x_perm
                             gemv8_small_rows(), cs);
     if (e == cudaSuccess && lim > 0) e = launch_ffn_gemv_fp8(g, hdr, glist, lim, cs);
     if (e == cudaSuccess && R > lim) {
-        if (planes) e = run_tc_planes(s, g, L, workspace, R, err, cs);
+        if (planes) e = run_tc_planes(s, g, L, workspace, R, pair, err, cs);
         else e = launch_ffn_tc_fp8(g, hdr, mtiles, L.max_mtiles, pair && tc_pair_possible(R), err, cs);
     }
     return cuda_status(e);
@@ -662,7 +674,7 @@ static moe_status forward_fp8_call(const moe_shape* shape, const void* x, const 
     const int lim = gemv8_limit(s);
     // a group has at most T rows (a token picks an expert once; the shared group has T)
     const bool planes = s.T > lim && (w8_planes() || wblock != 0);
-    const bool pair = planes || w8_pair();
+    const bool pair = w8_pair_tiles(planes, wblock);
     const int64_t R = (int64_t)s.T * s.K;
     float* sc = at<float>(workspace, L.ascale);
     uint8_t* xq = at<uint8_t>(workspace, L.y_s);  // x planes [T][2d], read before y_s is written
@@ -705,7 +717,7 @@ static moe_status forward_fp8_call(const moe_shape* shape, const void* x, const 
                             gemv8_small_rows(), cs);
     if (e == cudaSuccess && lim > 0) e = launch_ffn_gemv_fp8(g, hdr, glist, lim, cs);
     if (e == cudaSuccess && s.T > lim) {
-        if (planes) e = run_tc_planes(s, g, L, workspace, s.T, err, cs);
+        if (planes) e = run_tc_planes(s, g, L, workspace, s.T, pair, err, cs);
         else e = launch_ffn_tc_fp8(g, hdr, mtiles, L.max_mtiles, pair && tc_pair_possible(s.T), err, cs);
     }
     if (e != cudaSuccess) return MOE_ERR_CUDA;

@@ -99,6 +99,12 @@ def _expert_ffn_case(moe, counts, d, I, seed=0):
     return to_f64(y), ref, ref2
 
 
+# groups of <= 8 rows on the GEMV and the rest on single-SM tiles (the default);
+# every group on the tensor cores, single-SM tiles only or with CTA-pair tiles
+PATHS = {"default": {}, "tc": {"MOE_GEMV8_MAX_ROWS": "0"},
+         "tc_pair": {"MOE_GEMV8_MAX_ROWS": "0", "MOE_W8_PAIR": "1"}}
+
+
 @pytest.mark.parametrize("counts,d,I", [
     ([75, 0, 140, 3, 1, 260, 77, 44], 256, 384),     # ragged groups, one empty; GEMV + tiles
     ([600, 257, 1, 129], 384, 640),                  # pair and single tiles, 5 n-blocks
@@ -107,18 +113,17 @@ def _expert_ffn_case(moe, counts, d, I, seed=0):
     ([16, 15, 1, 33], 7168, 256),                    # DeepSeek-width rows, 16-row GEMV passes
     ([300, 1100], 640, 384),                         # n-block halves past the output (d = 5 x 128)
 ])
-@pytest.mark.parametrize("gemv8", [None, "0"])
-def test_expert_ffn_fp8_blocks_matches_oracle(moe, counts, d, I, gemv8, monkeypatch):
+@pytest.mark.parametrize("path", sorted(PATHS))
+def test_expert_ffn_fp8_blocks_matches_oracle(moe, counts, d, I, path, monkeypatch):
     """Against the exact block-scaled 8-bit-weight stage (fp64, bf16
     activations) and, for tensor-core groups, the oracle's two-plane form,
-    which they compute up to fp32 accumulation and the bf16 storage of h and y.
-    gemv8 = "0" sends every group to the tensor cores."""
-    if gemv8 is not None:
-        monkeypatch.setenv("MOE_GEMV8_MAX_ROWS", gemv8)
+    which they compute up to fp32 accumulation and the bf16 storage of h and y."""
+    for k, v in PATHS[path].items():
+        monkeypatch.setenv(k, v)
     y, ref, ref2 = _expert_ffn_case(moe, counts, d, I)
     _check_rows(y, ref)
     _check_rows(y, ref2)
-    if gemv8 == "0":   # every row on the two-plane path: closer to its own form (the
+    if path != "default":   # every row on the two-plane path: closer to its own form (the
         # rest of the gap is the bf16 storage of h and y, ~1e-3 on either side)
         assert rel_l2(y, ref2) < 0.8 * rel_l2(y, ref)
 
@@ -129,6 +134,7 @@ def test_expert_ffn_fp8_blocks_side_by_side_changes_no_bit(moe, rho, monkeypatch
     pushed to both extremes) give the bits of one launch after the other."""
     counts, d, I = [600, 257, 1, 129, 300, 140], 384, 640
     monkeypatch.setenv("MOE_GEMV8_MAX_ROWS", "0")
+    monkeypatch.setenv("MOE_W8_PAIR", "1")
     monkeypatch.setenv("MOE_CONCURRENT", "0")
     y0, ref, _ = _expert_ffn_case(moe, counts, d, I, seed=4)
     monkeypatch.setenv("MOE_CONCURRENT", "1")
@@ -205,11 +211,14 @@ def test_forward_fp8_blocks_decode_full_size(moe, gemv8, monkeypatch):
     _check_rows(y, ref["y"])
 
 
-@pytest.mark.parametrize("name", ["mixtral_prefill_fp8b", "dsv3_sweep_fp8b_T512"])
-def test_forward_fp8_blocks_sampled_tokens(moe, name):
-    """Mixtral-shaped prefill (~1024-row groups on CTA-pair tiles) and the
-    DeepSeek-V3 shape at T = 512 (~16-row groups): 256 sampled tokens whose
-    routing clears the order margin, routing and outputs against the oracle."""
+@pytest.mark.parametrize("name,pair", [("mixtral_prefill_fp8b", "0"), ("mixtral_prefill_fp8b", "1"),
+                                       ("dsv3_sweep_fp8b_T512", "0")])
+def test_forward_fp8_blocks_sampled_tokens(moe, name, pair, monkeypatch):
+    """Mixtral-shaped prefill (~1024-row groups on single-SM tiles, or CTA-pair
+    tiles with MOE_W8_PAIR=1) and the DeepSeek-V3 shape at T = 512 (~16-row
+    groups): 256 sampled tokens whose routing clears the order margin, routing
+    and outputs against the oracle."""
+    monkeypatch.setenv("MOE_W8_PAIR", pair)
     cfg = mi.CONFIGS[name]
     L = Layer(cfg)
     y = L.forward(moe)
