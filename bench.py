@@ -551,11 +551,11 @@ def time_expert_ffn(moe, cfg, x, p, bias, stream, steps: int, n_active: int) -> 
 # (sha256 prefix).
 STAGE_TRAFFIC = {
     # the four GEMM launches of one stage call (pair and single gate/up, pair and single down)
-    "dsv3_prefill_zipf": {"bytes": 9988049664 + 491900928 + 11163724288 + 44581888
-                          + 2670783744 + 1703299072 + 5510320384 + 154845696,
-                          "ffn_tc_sha256": "756cd63a7aadaa33"},
-    "mixtral_prefill": {"bytes": 2406684160 + 229825280 + 45312 + 1476628480 + 62856704 + 40704,
-                        "ffn_tc_sha256": "756cd63a7aadaa33"},
+    "dsv3_prefill_zipf": {"bytes": 9346626816 + 491579136 + 11166634496 + 44513536
+                          + 2676230656 + 1703432704 + 5509680128 + 154600192,
+                          "ffn_tc_sha256": "56a28e6948c5c91b"},
+    "mixtral_prefill": {"bytes": 1969564416 + 229444864 + 44544 + 1397322240 + 63420416 + 41984,
+                        "ffn_tc_sha256": "56a28e6948c5c91b"},
 }
 
 
