@@ -133,19 +133,26 @@ def test_binding_refuses_host_tensors(moe):
         moe.moe_combine(s, x, x, x, None, x, stream=0)
 
 
-@pytest.mark.parametrize("a8", [False, True])
-def test_fp8_argument_errors_return_before_any_launch(lib, moe, a8):
-    """The 8-bit entry points (8-bit weights, and 8-bit weights and
-    activations) refuse bad shapes and pointers on the host."""
+# (layer entry point, stage entry point, quantiser) of each 8-bit-weight form
+FP8_FORMS = {"rows": ("moe_forward_fp8", "moe_expert_ffn_fp8", "moe_quantize_fp8_rows"),
+             "w8a8": ("moe_forward_w8a8", "moe_expert_ffn_w8a8", "moe_quantize_fp8_rows"),
+             "blocks": ("moe_forward_fp8_blocks", "moe_expert_ffn_fp8_blocks",
+                        "moe_quantize_fp8_blocks")}
+
+
+@pytest.mark.parametrize("form", sorted(FP8_FORMS))
+def test_fp8_argument_errors_return_before_any_launch(lib, moe, form):
+    """The 8-bit entry points (8-bit weights with row or block scales, and
+    8-bit weights and activations) refuse bad shapes and pointers on the host."""
     vp, z = ctypes.c_void_p, ctypes.c_size_t
     fake = (1 << 20)
     odd = (1 << 20) + 4
-    for f in ("moe_quantize_fp8_rows", "moe_expert_ffn_fp8", "moe_forward_fp8",
-              "moe_expert_ffn_w8a8", "moe_forward_w8a8"):
+    fwd_name, ffn_name, q_name = FP8_FORMS[form]
+    for f in FP8_FORMS[form]:
         getattr(lib, f).restype = ctypes.c_int32
-    lib.moe_quantize_fp8_rows.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,
-                                          vp, vp, vp, vp]
-    q = lib.moe_quantize_fp8_rows
+    getattr(lib, q_name).argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,
+                                     vp, vp, vp, vp]
+    q = getattr(lib, q_name)
     assert q(-1, 64, moe.MOE_BF16, vp(fake), vp(fake), vp(fake), None) == moe.MOE_ERR_INVALID_ARG
     assert q(4, 0, moe.MOE_BF16, vp(fake), vp(fake), vp(fake), None) == moe.MOE_ERR_INVALID_ARG
     assert q(4, 64, 5, vp(fake), vp(fake), vp(fake), None) == moe.MOE_ERR_INVALID_ARG
@@ -153,6 +160,9 @@ def test_fp8_argument_errors_return_before_any_launch(lib, moe, a8):
     assert q(4, 64, moe.MOE_BF16, None, vp(fake), vp(fake), None) == moe.MOE_ERR_INVALID_ARG
     assert q(4, 64, moe.MOE_BF16, vp(fake), vp(odd), vp(fake), None) == moe.MOE_ERR_INVALID_ARG
     assert q(0, 64, moe.MOE_BF16, None, None, None, None) == moe.MOE_OK
+    if form == "blocks":  # more block rows than one launch's grid holds
+        assert q(65536 * 128, 64, moe.MOE_BF16, vp(fake), vp(fake), vp(fake),
+                 None) == moe.MOE_ERR_UNSUPPORTED
 
     full = {n: fake for n, _ in moe.moe_fp8_experts._fields_}
     routed = dict(full, ws_gate=None, ws_up=None, ws_down=None, ss_gate=None, ss_up=None,
@@ -164,7 +174,7 @@ def test_fp8_argument_errors_return_before_any_launch(lib, moe, a8):
     def fwd(shape, w, **kw):
         a = dict(x=vp(fake), w_g=vp(fake), y=vp(fake), ws=vp(fake), n=big)
         a.update(kw)
-        f = lib.moe_forward_w8a8 if a8 else lib.moe_forward_fp8
+        f = getattr(lib, fwd_name)
         return f(ctypes.byref(shape), a["x"], a["w_g"], None,
                  ctypes.byref(w) if w is not None else None, a["y"], a["ws"], a["n"], None)
 
@@ -186,7 +196,7 @@ def test_fp8_argument_errors_return_before_any_launch(lib, moe, a8):
     assert fwd(s, W, n=z(16)) == moe.MOE_ERR_WORKSPACE
     assert fwd(moe.make_shape(0, 128, 8, 2, 256, 0, "bf16"), None) == moe.MOE_OK
 
-    e = lib.moe_expert_ffn_w8a8 if a8 else lib.moe_expert_ffn_fp8
+    e = getattr(lib, ffn_name)
     assert e(ctypes.byref(s), vp(fake), None, ctypes.byref(W), vp(fake), vp(fake), big,
              None) == moe.MOE_ERR_INVALID_ARG
     assert e(ctypes.byref(s), vp(fake), vp(fake), None, vp(fake), vp(fake), big,
