@@ -29,9 +29,11 @@
 //
 // Both shapes keep two 128x256 fp32 accumulators per CTA in tensor memory
 // (all 512 columns), double-buffered so the epilogue of one tile overlaps the
-// main loop of the next.  Roles (192 threads per CTA): warp 0 TMA producer;
-// warp 1 MMA issuer and tensor-memory owner; warps 2-5 epilogue (the
-// 8-bit-weight variant W8 adds converter warps 6-13).
+// main loop of the next (with block-scaled 8-bit weights, A8 = 3, they
+// alternate per 128-deep K block instead).  Roles (192 threads per CTA): warp 0
+// TMA producer; warp 1 MMA issuer and tensor-memory owner; warps 2-5 epilogue
+// (the 8-bit-weight variant W8 adds converter warps 6-13; A8 = 3 runs eight
+// epilogue warps, 2-9).
 //
 // Tiles are (group, m-tile, n-block).  Within a group the m-tiles of a band
 // (1024 rows) vary fastest, so the CTAs working at the same moment share the
