@@ -87,6 +87,8 @@ def bind(lib):
     lib.oracle_expert_ffn_a2_blocks.argtypes = lib.oracle_expert_ffn_w8a8.argtypes
     lib.oracle_forward_tokens_fp8_blocks.argtypes = lib.oracle_forward_tokens_fp8.argtypes
     lib.oracle_forward_tokens_a2_blocks.argtypes = lib.oracle_forward_tokens_w8a8.argtypes
+    lib.oracle_expert_ffn_w8a8_blocks.argtypes = lib.oracle_expert_ffn_w8a8.argtypes
+    lib.oracle_forward_tokens_w8a8_blocks.argtypes = lib.oracle_forward_tokens_w8a8.argtypes
     for f in ("oracle_route", "oracle_permute", "oracle_expert_ffn", "oracle_combine",
               "oracle_shared_ffn", "oracle_forward", "oracle_forward_tokens",
               "oracle_expert_ffn_fp8", "oracle_forward_tokens_fp8", "oracle_e4m3_decode",
@@ -406,12 +408,14 @@ def expert_ffn_a2(x_perm, offsets, q: dict, dtype: str = "bf16", threads: int = 
 
 
 def expert_ffn_w8a8(x_perm, offsets, q: dict, dtype: str = "bf16", threads: int = 0,
-                    taps: bool = False):
+                    taps: bool = False, blocks: bool = False):
     """expert_ffn_fp8 with 8-bit activations: each x_perm row and each hidden row
-    (after fp32 -> bf16 rounding) quantised to E4M3 with one scale per row.
-    Returns y_perm [rows, d] f64, or (y_perm, h_pre, h_hat) with taps: h before
-    rounding and the dequantised quantised h, both [rows, I] f64."""
-    return _expert_ffn_a8(x_perm, offsets, q, dtype, threads, taps, "oracle_expert_ffn_w8a8")
+    (after fp32 -> bf16 rounding) quantised to E4M3 with one scale per row;
+    blocks=True: the weights' 128 x 128 block scales.  Returns y_perm [rows, d]
+    f64, or (y_perm, h_pre, h_hat) with taps: h before rounding and the
+    dequantised quantised h, both [rows, I] f64."""
+    return _expert_ffn_a8(x_perm, offsets, q, dtype, threads, taps,
+                          "oracle_expert_ffn_w8a8_blocks" if blocks else "oracle_expert_ffn_w8a8")
 
 
 def _expert_ffn_a8(x_perm, offsets, q, dtype, threads, taps, fname):
@@ -441,7 +445,7 @@ def forward_tokens_fp8(tokens, x, w_g, q: dict, K: int, dtype: str = "bf16", bia
     quantised per row; see oracle_forward_tokens_w8a8); "planes" -- every
     expert's input and hidden rows carried as two E4M3 planes
     (oracle_forward_tokens_a2).  blocks=True: the scales are the 128 x 128 block
-    scales of quantize_fp8_blocks (with act8 False or "planes")."""
+    scales of quantize_fp8_blocks (any act8)."""
     lib = _load()
     tokens = _arr(tokens, np.int32)
     x, w_g = _in(x, dtype), _in(w_g, dtype)
@@ -460,8 +464,6 @@ def forward_tokens_fp8(tokens, x, w_g, q: dict, K: int, dtype: str = "bf16", bia
     fname = ("oracle_forward_tokens_a2" if act8 == "planes" else
              "oracle_forward_tokens_w8a8" if act8 else "oracle_forward_tokens_fp8")
     if blocks:
-        if act8 not in (False, "planes"):
-            raise ValueError("block scales: act8 False or 'planes'")
         fname += "_blocks"
     fn = getattr(lib, fname)
     _check(fn(

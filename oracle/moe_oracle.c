@@ -1205,6 +1205,19 @@ int oracle_expert_ffn_a2(int64_t d, int64_t E, int64_t I, int dtype, const void 
                          s_down, y_perm, h_pre, h_hat, nthreads, 2, 0);
 }
 
+/* oracle_expert_ffn_w8a8 with the 128 x 128 block scales of
+ * oracle_expert_ffn_fp8_blocks (x and h still quantised per row). */
+int oracle_expert_ffn_w8a8_blocks(int64_t d, int64_t E, int64_t I, int dtype,
+                                  const void *x_perm, const int32_t *offsets,
+                                  const uint8_t *w_gate, const uint8_t *w_up,
+                                  const uint8_t *w_down, const float *s_gate,
+                                  const float *s_up, const float *s_down, double *y_perm,
+                                  double *h_pre, double *h_hat, int nthreads)
+{
+    return expert_ffn_a8(d, E, I, dtype, x_perm, offsets, w_gate, w_up, w_down, s_gate, s_up,
+                         s_down, y_perm, h_pre, h_hat, nthreads, 1, 1);
+}
+
 /* oracle_expert_ffn_a2 with the 128 x 128 block scales of
  * oracle_expert_ffn_fp8_blocks. */
 int oracle_expert_ffn_a2_blocks(int64_t d, int64_t E, int64_t I, int dtype,
@@ -1336,6 +1349,27 @@ int oracle_forward_tokens_a2(int64_t n, const int32_t *tokens, int64_t T,
                              w_up, w_down, s_gate, s_up, s_down, ws_gate, ws_up, ws_down,
                              ss_gate, ss_up, ss_down, y, topk_idx, topk_w, logits, nthreads, 2,
                              0);
+}
+
+/* oracle_forward_tokens_w8a8 with the 128 x 128 block scales of
+ * oracle_forward_tokens_fp8_blocks (x and h still quantised per row). */
+int oracle_forward_tokens_w8a8_blocks(int64_t n, const int32_t *tokens, int64_t T,
+                                      int64_t d, int64_t E, int64_t K, int64_t I,
+                                      int64_t Is, int dtype, int mode, const void *x,
+                                      const void *w_g, const double *bias,
+                                      const uint8_t *w_gate, const uint8_t *w_up,
+                                      const uint8_t *w_down, const float *s_gate,
+                                      const float *s_up, const float *s_down,
+                                      const uint8_t *ws_gate, const uint8_t *ws_up,
+                                      const uint8_t *ws_down, const float *ss_gate,
+                                      const float *ss_up, const float *ss_down,
+                                      double *y, int32_t *topk_idx, double *topk_w,
+                                      double *logits, int nthreads)
+{
+    return forward_tokens_a8(n, tokens, T, d, E, K, I, Is, dtype, mode, x, w_g, bias, w_gate,
+                             w_up, w_down, s_gate, s_up, s_down, ws_gate, ws_up, ws_down,
+                             ss_gate, ss_up, ss_down, y, topk_idx, topk_w, logits, nthreads, 1,
+                             1);
 }
 
 /* oracle_forward_tokens_a2 with the 128 x 128 block scales of

@@ -14,8 +14,8 @@ Each piece is tied to something other than the oracle:
   - the two formats: when every row of a 128-row block has the same amax in
     every 128-column block, row and block quantisation give the same codes and
     scales, and the two layers agree bit for bit;
-  - the two-plane form: each step matches PyTorch's casts and numpy products
-    with the expanded scales.
+  - the two-plane form and the W8A8 form (x and h quantised per row): each
+    step matches PyTorch's casts and numpy products with the expanded scales.
 """
 import numpy as np
 import pytest
@@ -226,6 +226,9 @@ def test_block_and_row_formats_agree_when_each_row_block_has_one_amax():
     a2 = oracle.forward_tokens_fp8(toks, x, w_g, q_row, K, act8="planes")
     b2 = oracle.forward_tokens_fp8(toks, x, w_g, q_blk, K, act8="planes", blocks=True)
     assert np.array_equal(a2["y"], b2["y"])
+    a8 = oracle.forward_tokens_fp8(toks, x, w_g, q_row, K, act8=True)
+    b8 = oracle.forward_tokens_fp8(toks, x, w_g, q_blk, K, act8=True, blocks=True)
+    assert np.array_equal(a8["y"], b8["y"])
 
 
 @pytest.mark.parametrize("seed,rows", [(1, [3, 0, 5, 1]), (2, [7, 2])])
@@ -273,3 +276,56 @@ def test_a2_blocks_token_forward_matches_the_expert_stage():
     # and the exact 8-bit-weight layer is within the two planes' reading of it
     ex = oracle.forward_tokens_fp8(np.arange(T), x, w_g, q, K, blocks=True)
     assert np.linalg.norm(out["y"] - ex["y"]) < 5e-3 * np.linalg.norm(ex["y"])
+
+
+# ---------------------------------------------------------------- W8A8 on block-scaled weights
+
+@pytest.mark.parametrize("seed,rows", [(3, [3, 0, 5, 1]), (4, [7, 2])])
+def test_w8a8_blocks_expert_matches_library_quantisation_at_every_step(seed, rows):
+    """x and h quantised per row (torch's float8 cast of v / (amax / 448)), the
+    weights dequantised per 128 x 128 block in numpy: h before rounding, h_hat
+    and y equal the oracle's taps."""
+    from tests.test_oracle_w8a8 import _torch_quant_rows
+    rng = np.random.default_rng(seed)
+    d, I = 256, 384
+    E = len(rows)
+    q = _block_layer(rng, d, E, I, 0, 12)
+    offsets = np.concatenate([[0], np.cumsum(rows)]).astype(np.int32)
+    R = int(offsets[-1])
+    xf = (rng.standard_normal((R, d)) * np.exp2(rng.uniform(-3, 3, (R, 1)))).astype(np.float32)
+    x = _bf16_bits(xf)
+    y, h_pre, h_hat = oracle.expert_ffn_w8a8(x, offsets, q, "bf16", taps=True, blocks=True)
+    wg, wu, wd = (_dequant_blocks(q, n) for n in ("w_gate", "w_up", "w_down"))
+    xh = _torch_quant_rows(_bits_to_f32(x))
+    for e in range(E):
+        sl = slice(int(offsets[e]), int(offsets[e + 1]))
+        if sl.start == sl.stop:
+            continue
+        g = xh[sl] @ wg[e].T
+        u = xh[sl] @ wu[e].T
+        with np.errstate(over="ignore"):
+            h_ref = g / (1.0 + np.exp(-g)) * u
+        assert np.abs(h_pre[sl] - h_ref).max() <= 1e-12 * max(np.abs(h_ref).max(), 1e-300)
+        assert np.array_equal(h_hat[sl], _torch_quant_rows(_torch_bf16(h_pre[sl])))
+        y_ref = h_hat[sl] @ wd[e].T
+        assert np.abs(y[sl] - y_ref).max() <= 1e-12 * max(np.abs(y_ref).max(), 1e-300)
+
+
+def test_w8a8_blocks_token_forward_matches_the_expert_stage():
+    rng = np.random.default_rng(8)
+    T, d, E, K, I, Is = 7, 256, 3, 2, 256, 128
+    q = _block_layer(rng, d, E, I, Is, 12)
+    x = _bf16_bits(rng.standard_normal((T, d)).astype(np.float32))
+    w_g = _bf16_bits((rng.standard_normal((E, d)) * 0.2).astype(np.float32))
+    out = oracle.forward_tokens_fp8(np.arange(T), x, w_g, q, K, act8=True, blocks=True)
+    counts, offsets, perm, inv = oracle.permute(out["topk_idx"], E)
+    y_perm = oracle.expert_ffn_w8a8(np.asarray(x)[perm // K], offsets, q, blocks=True)
+    shared = {"w_gate": q["ws_gate"][None], "w_up": q["ws_up"][None],
+              "w_down": q["ws_down"][None], "s_gate": q["ss_gate"], "s_up": q["ss_up"],
+              "s_down": q["ss_down"]}
+    y_s = oracle.expert_ffn_w8a8(x, np.array([0, T], np.int32), shared, blocks=True)
+    y = oracle.combine(y_perm, inv, out["topk_w"], y_s)
+    assert np.allclose(y, out["y"], rtol=0, atol=1e-12 * np.abs(y).max())
+    # the activations' E4M3 noise moves the output off the exact 8-bit-weight layer
+    ex = oracle.forward_tokens_fp8(np.arange(T), x, w_g, q, K, blocks=True)
+    assert np.linalg.norm(out["y"] - ex["y"]) > 1e-2 * np.linalg.norm(ex["y"])

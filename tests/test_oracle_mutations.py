@@ -85,6 +85,9 @@ MUTATIONS = [
      "scale[br * nbc + bc] = quantize_vec(blk, nc, cb);"),
     ("block_quant_codes_transposed", "codes[(r0 + i) * cols + c0 + j] = cb[i * nc + j];",
      "codes[(r0 + i) * cols + c0 + j] = cb[j * nr + i];"),
+    ("block_w8a8_stage_with_two_planes",
+     "s_down, y_perm, h_pre, h_hat, nthreads, 1, 1);",
+     "s_down, y_perm, h_pre, h_hat, nthreads, 2, 1);"),
     ("block_a2_stage_with_one_plane",
      "s_down, y_perm, h_pre, h_hat, nthreads, 2, 1);",
      "s_down, y_perm, h_pre, h_hat, nthreads, 1, 1);"),
@@ -121,6 +124,8 @@ PIN_TESTS = [
     lambda: pins_blk.test_block_codes_and_scales_match_torch("f32", (300, 200)),
     lambda: pins_blk.test_block_layer_equals_the_layer_on_dequantised_weights("bf16", 0, 192, 320, 64),
     lambda: pins_blk.test_a2_blocks_expert_matches_library_casts_at_every_step(2, [7, 2]),
+    lambda: pins_blk.test_w8a8_blocks_expert_matches_library_quantisation_at_every_step(4, [7, 2]),
+    lambda: pins_blk.test_w8a8_blocks_token_forward_matches_the_expert_stage(),
 ]
 
 
