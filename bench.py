@@ -91,7 +91,11 @@ def expert_bytes(cfg, inter: int) -> int:
 
 def fp8_calls(moe, cfg):
     """The layer and expert-stage entry points of an 8-bit-weight workload (row
-    or block scales), or (None, None)."""
+    or block scales; 8-bit activations or not), or (None, None)."""
+    if cfg.acts == "e4m3":
+        if cfg.weights == "e4m3b":
+            return moe.moe_forward_w8a8_blocks, moe.moe_expert_ffn_w8a8_blocks
+        return moe.moe_forward_w8a8, moe.moe_expert_ffn_w8a8
     if cfg.weights == "e4m3b":
         return moe.moe_forward_fp8_blocks, moe.moe_expert_ffn_fp8_blocks
     if cfg.weights == "e4m3":
@@ -128,14 +132,10 @@ class Forward:
             moe, cfg, s, p, bias, ws, stream)
         self.fp8 = moe.make_fp8_experts(p) if mi.is_fp8(cfg) else None
         self.fwd8 = fp8_calls(moe, cfg)[0]
-        self.a8 = cfg.acts == "e4m3"
 
     def __call__(self, x, y):
         m, p = self.moe, self.p
-        if self.a8:
-            m.moe_forward_w8a8(self.s, x, p["w_g"], self.bias, self.fp8, y, self.ws,
-                               stream=self.stream)
-        elif self.fp8 is not None:
+        if self.fp8 is not None:
             self.fwd8(self.s, x, p["w_g"], self.bias, self.fp8, y, self.ws, stream=self.stream)
         else:
             m.moe_forward(self.s, x, p["w_g"], self.bias, p["w_gate"], p["w_up"], p["w_down"],
@@ -171,11 +171,13 @@ def launches_per_forward(cfg, gemv_limit: int = 0) -> int:
     disp_plan = 1 if fused else 3 + 1
     # router + top-K: one fused launch for at most 16 tokens when MOE_FUSED_ROUTER=1
     router = 1 if 0 < cfg.T <= 16 and os.environ.get("MOE_FUSED_ROUTER", "0") == "1" else 2
+    # block-scaled 8-bit weights take CTA-pair tiles only with MOE_W8_PAIR=1
+    pair_ok = cfg.weights != "e4m3b" or os.environ.get("MOE_W8_PAIR", "0") == "1"
     if cfg.acts == "e4m3":
         # router + top-K, dispatch + plan, x quantiser, code gather,
         # tcgen05 gate/up, h quantiser (+ h_s), tcgen05 down -- the gate/up and
         # down twice when a group can take pair tiles -- combine
-        pair = cfg.T > 128
+        pair = cfg.T > 128 and pair_ok
         return router + disp_plan + 1 + 1 + (2 if pair else 1) + (2 if cfg.Is else 1) \
             + (2 if pair else 1) + 1
     if mi.is_fp8(cfg):
@@ -190,7 +192,7 @@ def launches_per_forward(cfg, gemv_limit: int = 0) -> int:
         gemv = (2 if limit > 0 else 0) + (2 if limit > 8 else 0)
         if cfg.T > limit and (os.environ.get("MOE_W8_PLANES", "1") != "0"
                               or cfg.weights == "e4m3b"):
-            pair = cfg.T > 128
+            pair = cfg.T > 128 and pair_ok
             tc = 2 * (2 if pair else 1) + (2 if cfg.Is else 1)
             return router + disp_plan + 2 + gemv + tc + 1
         tc = 2 if cfg.T > limit else 0
@@ -525,9 +527,7 @@ def time_expert_ffn(moe, cfg, x, p, bias, stream, steps: int, n_active: int) -> 
     ffn8 = fp8_calls(moe, cfg)[1]
 
     def run():
-        if cfg.acts == "e4m3":
-            moe.moe_expert_ffn_w8a8(s, x_perm, offsets, fp8, y_perm, ws, stream=stream)
-        elif fp8 is not None:
+        if fp8 is not None:
             ffn8(s, x_perm, offsets, fp8, y_perm, ws, stream=stream)
         else:
             moe.moe_expert_ffn(s, x_perm, offsets, p["w_gate"], p["w_up"], p["w_down"], y_perm,
@@ -790,7 +790,8 @@ def bench_all(moe, peaks, args) -> list:
                  "dsv3_decode_fp8", "dsv3_sweep_fp8_T64", "dsv3_sweep_fp8_T512",
                  "mixtral_prefill_fp8", "dsv3_decode_fp8b", "dsv3_sweep_fp8b_T512",
                  "mixtral_prefill_fp8b", "dsv3_decode_w8a8", "dsv3_sweep_w8a8_T512",
-                 "dsv3_sweep_w8a8_T4096", "mixtral_prefill_w8a8", "dsv3_prefill_zipf_w8a8"):
+                 "dsv3_sweep_w8a8_T4096", "mixtral_prefill_w8a8", "dsv3_prefill_zipf_w8a8",
+                 "dsv3_decode_w8a8b", "mixtral_prefill_w8a8b", "dsv3_prefill_zipf_w8a8b"):
         cfg = mi.CONFIGS[name]
         res.append(bench_workload(moe, cfg, peaks, steps=max(10, args.steps),
                                   graph=cfg.T <= 64))
@@ -847,9 +848,7 @@ def run_stage_pool(args):
     torch.cuda.synchronize()
 
     def run():
-        if cfg.acts == "e4m3":
-            moe.moe_expert_ffn_w8a8(s, x_perm, offsets, fp8, y_perm, ws, stream=st)
-        elif fp8 is not None:
+        if fp8 is not None:
             ffn8(s, x_perm, offsets, fp8, y_perm, ws, stream=st)
         else:
             moe.moe_expert_ffn(s, x_perm, offsets, p["w_gate"], p["w_up"], p["w_down"], y_perm,

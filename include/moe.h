@@ -360,6 +360,21 @@ moe_status moe_forward_w8a8(const moe_shape *shape, const void *x, const void *w
                             const float *bias, const moe_fp8_experts *w, void *y,
                             void *workspace, size_t ws_bytes, void *stream);
 
+/* The W8A8 calls on block-scaled weights: x and h quantised per row as above,
+ * the weights' scales the 128 x 128 block grids of moe_quantize_fp8_blocks
+ * (layout as for moe_forward_fp8_blocks).  One E4M3 x E4M3 MMA per 32-deep
+ * slice; each 128-deep K block is multiplied into its own tensor-memory
+ * accumulator and added, times its block scale, to fp32 sums in registers,
+ * the activation row's scale applied at the end.  Limits, workspace and
+ * errors as moe_forward_w8a8 / moe_expert_ffn_w8a8. */
+moe_status moe_expert_ffn_w8a8_blocks(const moe_shape *shape, const void *x_perm,
+                                      const int32_t *offsets, const moe_fp8_experts *w,
+                                      void *y_perm, void *workspace, size_t ws_bytes,
+                                      void *stream);
+moe_status moe_forward_w8a8_blocks(const moe_shape *shape, const void *x, const void *w_g,
+                                   const float *bias, const moe_fp8_experts *w, void *y,
+                                   void *workspace, size_t ws_bytes, void *stream);
+
 /*
  * Reads the device error word of `workspace` (a device pointer passed to a
  * previous call) into *code_out (a HOST pointer): MOE_OK, MOE_ERR_TIMEOUT or

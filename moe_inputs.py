@@ -106,6 +106,14 @@ CONFIGS["mixtral_prefill_fp8b"] = replace(CONFIGS["mixtral_prefill"], name="mixt
                                           weights="e4m3b")
 CONFIGS["dsv3_sweep_fp8b_T512"] = replace(CONFIGS["dsv3_decode_fp8b"], name="dsv3_sweep_fp8b_T512",
                                           T=512)
+# the same block-scaled weights with 8-bit activations (x and h quantised per row)
+CONFIGS["dsv3_decode_w8a8b"] = replace(CONFIGS["dsv3_decode_fp8b"], name="dsv3_decode_w8a8b",
+                                       acts="e4m3")
+CONFIGS["mixtral_prefill_w8a8b"] = replace(CONFIGS["mixtral_prefill_fp8b"],
+                                           name="mixtral_prefill_w8a8b", acts="e4m3")
+CONFIGS["dsv3_prefill_zipf_w8a8b"] = replace(CONFIGS["dsv3_prefill_zipf"],
+                                             name="dsv3_prefill_zipf_w8a8b", weights="e4m3b",
+                                             acts="e4m3")
 # the same decode layer over a pool of 32 experts (1.4 GB of codes): small enough
 # for multi-pass counter captures, still far larger than L2
 CONFIGS["dsv3_decode_fp8_E32"] = replace(CONFIGS["dsv3_decode_fp8"], name="dsv3_decode_fp8_E32",

@@ -26,7 +26,8 @@ EXPORTED = ("moe_status_string", "moe_workspace_bytes", "moe_route", "moe_permut
             "moe_permute_noalloc", "moe_expert_ffn", "moe_combine", "moe_forward",
             "moe_quantize_fp8_rows", "moe_expert_ffn_fp8", "moe_forward_fp8",
             "moe_quantize_fp8_blocks", "moe_expert_ffn_fp8_blocks", "moe_forward_fp8_blocks",
-            "moe_expert_ffn_w8a8", "moe_forward_w8a8", "moe_get_device_error")
+            "moe_expert_ffn_w8a8", "moe_forward_w8a8", "moe_expert_ffn_w8a8_blocks",
+            "moe_forward_w8a8_blocks", "moe_get_device_error")
 FP8_BLOCK = 128  # side of the square weight-scale blocks of the *_fp8_blocks calls
 
 
@@ -78,11 +79,14 @@ def _load_lib() -> ctypes.CDLL:
     lib.moe_forward_fp8_blocks.argtypes = lib.moe_forward_fp8.argtypes
     lib.moe_expert_ffn_w8a8.argtypes = [sp, vp, vp, fp, vp, vp, sz, vp]
     lib.moe_forward_w8a8.argtypes = [sp, vp, vp, vp, fp, vp, vp, sz, vp]
+    lib.moe_expert_ffn_w8a8_blocks.argtypes = lib.moe_expert_ffn_w8a8.argtypes
+    lib.moe_forward_w8a8_blocks.argtypes = lib.moe_forward_w8a8.argtypes
     lib.moe_get_device_error.argtypes = [vp, ctypes.POINTER(i32)]
     for f in ("moe_route", "moe_permute", "moe_permute_noalloc", "moe_expert_ffn", "moe_combine",
               "moe_forward", "moe_quantize_fp8_rows", "moe_expert_ffn_fp8", "moe_forward_fp8",
               "moe_quantize_fp8_blocks", "moe_expert_ffn_fp8_blocks", "moe_forward_fp8_blocks",
-              "moe_expert_ffn_w8a8", "moe_forward_w8a8", "moe_get_device_error"):
+              "moe_expert_ffn_w8a8", "moe_forward_w8a8", "moe_expert_ffn_w8a8_blocks",
+              "moe_forward_w8a8_blocks", "moe_get_device_error"):
         getattr(lib, f).restype = i32
     return lib
 
@@ -261,6 +265,21 @@ def moe_forward_w8a8(shape, x, w_g, bias, w: moe_fp8_experts, y, workspace, stre
     ws, nws = _ws(workspace)
     _check(_lib.moe_forward_w8a8(ctypes.byref(shape), _p(x), _p(w_g), _p(bias), ctypes.byref(w),
                                  _p(y), ws, nws, _stream(stream)), "moe_forward_w8a8")
+
+
+def moe_expert_ffn_w8a8_blocks(shape, x_perm, offsets, w: moe_fp8_experts, y_perm, workspace,
+                               stream=None):
+    ws, nws = _ws(workspace)
+    _check(_lib.moe_expert_ffn_w8a8_blocks(ctypes.byref(shape), _p(x_perm), _p(offsets),
+                                           ctypes.byref(w), _p(y_perm), ws, nws, _stream(stream)),
+           "moe_expert_ffn_w8a8_blocks")
+
+
+def moe_forward_w8a8_blocks(shape, x, w_g, bias, w: moe_fp8_experts, y, workspace, stream=None):
+    ws, nws = _ws(workspace)
+    _check(_lib.moe_forward_w8a8_blocks(ctypes.byref(shape), _p(x), _p(w_g), _p(bias),
+                                        ctypes.byref(w), _p(y), ws, nws, _stream(stream)),
+           "moe_forward_w8a8_blocks")
 
 
 def moe_get_device_error(workspace) -> int:

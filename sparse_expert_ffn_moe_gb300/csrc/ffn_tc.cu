@@ -90,7 +90,8 @@ constexpr uint32_t kABytes = BMC * BK * 2;  // 16 KB
 constexpr int kThreadsTc = 192;
 constexpr uint32_t kTmemCols = 512;
 
-// Block-scaled 8-bit weights (A8 == 3: two activation planes as A8 == 2, one
+// Block-scaled 8-bit weights (A8 == 3: two activation planes as A8 == 2; A8 ==
+// 4: one plane of per-row-quantised activations as A8 == 1; either with one
 // weight scale per 128 x 128 block).  A block scale changes every 128 values
 // of K, so it cannot be applied to an accumulator that sums all of K: each
 // 128-deep K block (one ring stage) is multiplied into a fresh accumulator,
@@ -106,7 +107,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr int kThreadsBlk = 320;
 constexpr uint32_t kBlkEpiBar = 1;  // named barrier of the eight epilogue warps
 template <bool W8, int A8> constexpr int threads_of() {
-    return W8 ? (6 + 8) * 32 : (A8 == 3 ? kThreadsBlk : kThreadsTc);
+    return W8 ? (6 + 8) * 32 : (A8 >= 3 ? kThreadsBlk : kThreadsTc);
 }
 
 // Small-row ring (SMA, single-SM bf16 or W8A8 tiles whose groups all have at most kSmaRows
@@ -469,11 +470,12 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
     static_assert(!(W8 && EPI == EPI_STORE_F32), "8-bit weights feed the expert GEMMs only");
     static_assert(!(SMA && (PAIR || W8)), "small-row ring: single-SM tiles without the W8 rings");
     static_assert(!(A8 && (W8 || EPI == EPI_STORE_F32)), "A8: 8-bit operands, expert GEMMs only");
-    static_assert(!(A8 >= 2 && SMA), "two activation planes: the full-size rings");
-    static_assert(!(A8 == 3 && EPI != EPI_SWIGLU && EPI != EPI_STORE_BF16), "block scales: expert GEMMs");
+    // activation tiles per stage: two E4M3 planes (A8 = 2, 3) or one
+    constexpr uint32_t kAPlanes = (A8 == 2 || A8 == 3) ? 2u : 1u;
+    constexpr bool kBlk = A8 >= 3;  // block-scaled weights: one accumulator hand-off per K block
+    static_assert(!(kAPlanes == 2 && SMA), "two activation planes: the full-size rings");
+    static_assert(!(kBlk && EPI != EPI_SWIGLU && EPI != EPI_STORE_BF16), "block scales: expert GEMMs");
     using S = typename RingOf<PAIR, SMA, A8>::type;
-    constexpr uint32_t kAPlanes = A8 >= 2 ? 2u : 1u;  // activation tiles per stage
-    constexpr bool kBlk = A8 == 3;  // block-scaled weights: one accumulator hand-off per K block
     using W = W8Shape<PAIR>;
     constexpr uint32_t kAStride = S::kAStride;  // bytes per activation stage (W8: kABytes)
     // A8: both operands E4M3 (kind::f8f6f4); a 128-byte K block holds 128 values
@@ -742,7 +744,7 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
                                 const uint32_t fb = full0 + (uint32_t)(stage * sizeof(uint64_t));
                                 if (rank == 0) ptx::mbar_arrive_expect_tx(&ctl->full[stage], tx);
                                 if (rows_me > 0) {
-                                    if constexpr (A8 >= 2) {  // hi and lo codes of K block kb
+                                    if constexpr (kAPlanes == 2) {  // hi and lo codes of K block kb
                                         ptx::tma_load_2d_pair(a_dst, ma, fb, 2 * k0, arow);
                                         ptx::tma_load_2d_pair(a_dst + kABytes, ma, fb, 2 * k0 + 128, arow);
                                     } else {
@@ -752,7 +754,7 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
                                 load_b_pair(b_dst, fb, k0, mb, brow);
                             } else {
                                 ptx::mbar_arrive_expect_tx(&ctl->full[stage], tx);
-                                if constexpr (A8 >= 2) {
+                                if constexpr (kAPlanes == 2) {
                                     ptx::tma_load_2d(a_dst, ma, &ctl->full[stage], 2 * k0, arow);
                                     ptx::tma_load_2d(a_dst + kABytes, ma, &ctl->full[stage], 2 * k0 + 128, arow);
                                 } else {
@@ -891,7 +893,7 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
                         if constexpr (A8) {
                             if constexpr (PAIR) ptx::tc_mma_f8_pair(d_tmem, ad, bd, id_t, accum);
                             else ptx::tc_mma_f8(d_tmem, ad, bd, idesc, accum);
-                            if constexpr (A8 >= 2) {  // the lo plane times the same weights
+                            if constexpr (kAPlanes == 2) {  // the lo plane times the same weights
                                 const uint64_t ad2 = ptx::sw128_kmajor_desc(a_base + kABytes + kk * 32);
                                 if constexpr (PAIR) ptx::tc_mma_f8_pair(d_tmem, ad2, bd, id_t, 1u);
                                 else ptx::tc_mma_f8(d_tmem, ad2, bd, idesc, 1u);
@@ -1690,7 +1692,7 @@ cudaError_t launch_shapes(TcParams& p, const int4* pair_list, const int4* single
     if (e == cudaSuccess) {
         p.mtiles = single_list;
         p.band = 0;
-        if constexpr (!W8 && A8 < 2) {
+        if constexpr (!W8 && (A8 < 2 || A8 == 4)) {
             if (small_rows && small_ring()) return launch_tc<EPI, false, false, A8, true>(p, sh.st2, pdl);
         }
         e = launch_tc<EPI, false, W8, A8>(p, sh.st2, pdl);
@@ -2101,6 +2103,11 @@ cudaError_t launch_ffn_tc_a8_gate_up(const FfnGroups& g, const FfnPlanHeader* hd
     if (planes == 2)
         return sh.finish(launch_shapes<EPI_SWIGLU, false, 2>(p, mtile_list + max_mtiles, mtile_list,
                                                              may_pair, sh, true));
+    if (g.wblock) {  // one plane, block-scaled weights
+        p.half_tiles = 0;
+        return sh.finish(launch_shapes<EPI_SWIGLU, false, 4>(p, mtile_list + max_mtiles, mtile_list,
+                                                             may_pair, sh, true, small));
+    }
     return sh.finish(launch_shapes<EPI_SWIGLU, false, 1>(p, mtile_list + max_mtiles, mtile_list,
                                                          may_pair, sh, true, small));
 }
@@ -2158,6 +2165,11 @@ cudaError_t launch_ffn_tc_a8_down(const FfnGroups& g, const FfnPlanHeader* hdr,
     if (planes == 2)
         return sh.finish(launch_shapes<EPI_STORE_BF16, false, 2>(q, mtile_list + max_mtiles, mtile_list,
                                                                  may_pair, sh, sh.side == nullptr));
+    if (g.wblock) {
+        q.half_tiles = 0;
+        return sh.finish(launch_shapes<EPI_STORE_BF16, false, 4>(q, mtile_list + max_mtiles, mtile_list,
+                                                                 may_pair, sh, sh.side == nullptr, small));
+    }
     return sh.finish(launch_shapes<EPI_STORE_BF16, false, 1>(q, mtile_list + max_mtiles, mtile_list,
                                                              may_pair, sh, sh.side == nullptr, small));
 }

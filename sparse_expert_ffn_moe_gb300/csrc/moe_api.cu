@@ -122,9 +122,9 @@ bool w8_pair() {
     return e && e[0] == '1';
 }
 
-// Whether the plan may give 8-bit-weight groups CTA-pair tiles: with two-plane
-// activations and row scales, yes; with the codes widened in the GEMM, or with
-// block scales, only when MOE_W8_PAIR=1.  Measured on GB300 (block scales,
+// Whether the plan may give 8-bit-weight groups CTA-pair tiles: with 8-bit
+// activations (two planes, or W8A8) and row scales, yes; with the codes widened
+// in the GEMM, or with block scales, only when MOE_W8_PAIR=1.  Measured on GB300 (block scales,
 // Mixtral-shaped stage on a 4-expert pool): 1.72 ms on pair tiles, 1.13 ms on
 // single-SM tiles (row scales: 0.95 ms) -- per 128-deep K block the pair's MMA
 // issuer waited ~1600 cycles for the peer CTA to release the accumulator,
@@ -744,18 +744,19 @@ moe_status moe_forward_fp8_blocks(const moe_shape* shape, const void* x, const v
 // max_rows bounds the rows of any group (pair launches are skipped when no
 // group can take pair tiles).
 static cudaError_t run_ffn_w8a8(const moe_shape& s, FfnGroups& g, const WsLayout& L, void* ws,
-                                int64_t max_rows, bool planned, DevError* err, cudaStream_t cs) {
+                                int64_t max_rows, bool planned, bool pair, DevError* err,
+                                cudaStream_t cs) {
     FfnPlanHeader* hdr = at<FfnPlanHeader>(ws, L.plan);
     int32_t* glist = at<int32_t>(ws, L.gemv_list);
     int4* mtiles = at<int4>(ws, L.mtile_list);
     const int64_t R = (int64_t)s.T * s.K;
-    const bool may_pair = tc_pair_possible(max_rows);
+    const bool may_pair = pair && tc_pair_possible(max_rows);
     // the gate/up epilogue raises each h row's max |h| from zero
     cudaError_t e = cudaMemsetAsync(const_cast<float*>(g.sa_h), 0, sizeof(float) * R, cs);
     if (e == cudaSuccess && g.has_shared)
         e = cudaMemsetAsync(const_cast<float*>(g.sa_hs), 0, sizeof(float) * s.T, cs);
     if (e == cudaSuccess && !planned)
-        e = launch_ffn_plan(g, s.dtype, hdr, glist, mtiles, L.max_mtiles, 0, true, 0, cs);
+        e = launch_ffn_plan(g, s.dtype, hdr, glist, mtiles, L.max_mtiles, 0, pair, 0, cs);
     if (e == cudaSuccess)
         e = launch_ffn_tc_a8_gate_up(g, hdr, mtiles, L.max_mtiles, may_pair, err, cs);
     if (e == cudaSuccess)
@@ -769,9 +770,12 @@ static cudaError_t run_ffn_w8a8(const moe_shape& s, FfnGroups& g, const WsLayout
     return e;
 }
 
-moe_status moe_expert_ffn_w8a8(const moe_shape* shape, const void* x_perm, const int32_t* offsets,
-                               const moe_fp8_experts* w, void* y_perm, void* workspace,
-                               size_t ws_bytes, void* stream) {
+// moe_expert_ffn_w8a8 (wblock = 0: row scales) and moe_expert_ffn_w8a8_blocks
+// (wblock = kWBlock: 128 x 128 block scales, single-SM tiles unless MOE_W8_PAIR=1).
+static moe_status expert_ffn_w8a8_call(const moe_shape* shape, const void* x_perm,
+                                       const int32_t* offsets, const moe_fp8_experts* w,
+                                       void* y_perm, void* workspace, size_t ws_bytes,
+                                       void* stream, int wblock) {
     moe_status st = check_shape(shape);
     if (st != MOE_OK) return st;
     const moe_shape& s = *shape;
@@ -812,6 +816,7 @@ moe_status moe_expert_ffn_w8a8(const moe_shape* shape, const void* x_perm, const
     g.s_gate = w->s_gate;
     g.s_up = w->s_up;
     g.s_down = w->s_down;
+    g.wblock = wblock;
     g.sa_routed = sc + s.T;
     g.sa_shared = sc + s.T;
     g.sa_h = sc + s.T + R;
@@ -819,12 +824,28 @@ moe_status moe_expert_ffn_w8a8(const moe_shape* shape, const void* x_perm, const
     g.h = at<void>(workspace, L.h);
     g.y = y_perm;
     // a group has at most T*K rows here (the offsets are the caller's)
-    return cuda_status(run_ffn_w8a8(s, g, L, workspace, R, false, err, cs));
+    return cuda_status(run_ffn_w8a8(s, g, L, workspace, R, false, w8_pair_tiles(true, wblock), err,
+                                    cs));
 }
 
-moe_status moe_forward_w8a8(const moe_shape* shape, const void* x, const void* w_g,
-                            const float* bias, const moe_fp8_experts* w, void* y, void* workspace,
-                            size_t ws_bytes, void* stream) {
+moe_status moe_expert_ffn_w8a8(const moe_shape* shape, const void* x_perm, const int32_t* offsets,
+                               const moe_fp8_experts* w, void* y_perm, void* workspace,
+                               size_t ws_bytes, void* stream) {
+    return expert_ffn_w8a8_call(shape, x_perm, offsets, w, y_perm, workspace, ws_bytes, stream, 0);
+}
+
+moe_status moe_expert_ffn_w8a8_blocks(const moe_shape* shape, const void* x_perm,
+                                      const int32_t* offsets, const moe_fp8_experts* w,
+                                      void* y_perm, void* workspace, size_t ws_bytes,
+                                      void* stream) {
+    return expert_ffn_w8a8_call(shape, x_perm, offsets, w, y_perm, workspace, ws_bytes, stream,
+                                kWBlock);
+}
+
+// moe_forward_w8a8 (wblock = 0) and moe_forward_w8a8_blocks (wblock = kWBlock).
+static moe_status forward_w8a8_call(const moe_shape* shape, const void* x, const void* w_g,
+                                    const float* bias, const moe_fp8_experts* w, void* y,
+                                    void* workspace, size_t ws_bytes, void* stream, int wblock) {
     moe_status st = check_shape(shape);
     if (st != MOE_OK) return st;
     const moe_shape& s = *shape;
@@ -885,6 +906,7 @@ moe_status moe_forward_w8a8(const moe_shape* shape, const void* x, const void* w
     g.ss_gate = w->ss_gate;
     g.ss_up = w->ss_up;
     g.ss_down = w->ss_down;
+    g.wblock = wblock;
     g.sa_routed = sc + s.T;
     g.sa_shared = sc;
     g.sa_h = sc + s.T + R;
@@ -896,11 +918,12 @@ moe_status moe_forward_w8a8(const moe_shape* shape, const void* x, const void* w
     int32_t* counts = at<int32_t>(workspace, L.counts);
     int32_t* perm = at<int32_t>(workspace, L.perm);
     const bool fused = dispatch_plan_fusable(s);
+    const bool pair = w8_pair_tiles(true, wblock);
     if (fused)
         e = launch_dispatch_plan_small(s, topk_idx, counts, offsets, perm, inv, tok, err, g,
                                        at<FfnPlanHeader>(workspace, L.plan),
                                        at<int32_t>(workspace, L.gemv_list),
-                                       at<int4>(workspace, L.mtile_list), L.max_mtiles, 0, true, 0,
+                                       at<int4>(workspace, L.mtile_list), L.max_mtiles, 0, pair, 0,
                                        cs);
     else
         e = launch_dispatch(s, topk_idx, counts, offsets, perm, inv, tok,
@@ -911,11 +934,23 @@ moe_status moe_forward_w8a8(const moe_shape* shape, const void* x, const void* w
 
     // 3. routed and shared experts, W8A8 on the tensor cores
     // a group has at most T rows (a token picks an expert once; the shared group has T)
-    e = run_ffn_w8a8(s, g, L, workspace, s.T, fused, err, cs);
+    e = run_ffn_w8a8(s, g, L, workspace, s.T, fused, pair, err, cs);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
 
     // 4. combine
     return cuda_status(launch_combine(s, g.y, inv, topk_w, shared ? g.y_s : nullptr, y, cs));
+}
+
+moe_status moe_forward_w8a8(const moe_shape* shape, const void* x, const void* w_g,
+                            const float* bias, const moe_fp8_experts* w, void* y, void* workspace,
+                            size_t ws_bytes, void* stream) {
+    return forward_w8a8_call(shape, x, w_g, bias, w, y, workspace, ws_bytes, stream, 0);
+}
+
+moe_status moe_forward_w8a8_blocks(const moe_shape* shape, const void* x, const void* w_g,
+                                   const float* bias, const moe_fp8_experts* w, void* y,
+                                   void* workspace, size_t ws_bytes, void* stream) {
+    return forward_w8a8_call(shape, x, w_g, bias, w, y, workspace, ws_bytes, stream, kWBlock);
 }
 
 moe_status moe_get_device_error(const void* workspace, int32_t* code_out) {

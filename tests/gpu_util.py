@@ -225,7 +225,9 @@ class Layer:
         y = torch.empty_like(x)
         ws = moe.alloc_workspace(s) if ws is None else ws
         p = self.p
-        if self.cfg.acts == "e4m3":
+        if self.cfg.acts == "e4m3" and self.cfg.weights == "e4m3b":
+            moe.moe_forward_w8a8_blocks(s, x, p["w_g"], self.bias, moe.make_fp8_experts(p), y, ws)
+        elif self.cfg.acts == "e4m3":
             moe.moe_forward_w8a8(s, x, p["w_g"], self.bias, moe.make_fp8_experts(p), y, ws)
         elif self.cfg.weights == "e4m3b":
             moe.moe_forward_fp8_blocks(s, x, p["w_g"], self.bias, moe.make_fp8_experts(p), y, ws)

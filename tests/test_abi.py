@@ -137,7 +137,9 @@ def test_binding_refuses_host_tensors(moe):
 FP8_FORMS = {"rows": ("moe_forward_fp8", "moe_expert_ffn_fp8", "moe_quantize_fp8_rows"),
              "w8a8": ("moe_forward_w8a8", "moe_expert_ffn_w8a8", "moe_quantize_fp8_rows"),
              "blocks": ("moe_forward_fp8_blocks", "moe_expert_ffn_fp8_blocks",
-                        "moe_quantize_fp8_blocks")}
+                        "moe_quantize_fp8_blocks"),
+             "w8a8_blocks": ("moe_forward_w8a8_blocks", "moe_expert_ffn_w8a8_blocks",
+                             "moe_quantize_fp8_blocks")}
 
 
 @pytest.mark.parametrize("form", sorted(FP8_FORMS))
@@ -160,7 +162,7 @@ def test_fp8_argument_errors_return_before_any_launch(lib, moe, form):
     assert q(4, 64, moe.MOE_BF16, None, vp(fake), vp(fake), None) == moe.MOE_ERR_INVALID_ARG
     assert q(4, 64, moe.MOE_BF16, vp(fake), vp(odd), vp(fake), None) == moe.MOE_ERR_INVALID_ARG
     assert q(0, 64, moe.MOE_BF16, None, None, None, None) == moe.MOE_OK
-    if form == "blocks":  # more block rows than one launch's grid holds
+    if q_name == "moe_quantize_fp8_blocks":  # more block rows than one launch's grid holds
         assert q(65536 * 128, 64, moe.MOE_BF16, vp(fake), vp(fake), vp(fake),
                  None) == moe.MOE_ERR_UNSUPPORTED
 

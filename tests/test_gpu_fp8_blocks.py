@@ -7,7 +7,9 @@ divisions, round to nearest even): codes and scales must match bit for bit.
 The expert FFN and the layer are compared like the row-scaled ones: relative
 L2 against the fp64 oracle on the same codes and block scales (the exact
 8-bit-weight definition), and, where the tensor cores carry the activations as
-two E4M3 planes, against the oracle's two-plane form as well."""
+two E4M3 planes, against the oracle's two-plane form as well.  The W8A8 calls on
+block-scaled weights are compared with the oracle's W8A8 layer on the same
+codes (x and h quantised per row on both sides)."""
 import numpy as np
 import pytest
 import torch
@@ -269,6 +271,100 @@ def test_fp8_blocks_stalled_copy_times_out_and_the_context_survives(moe, monkeyp
     ws = moe.alloc_workspace(s)
     y = torch.empty_like(L.x)
     moe.moe_forward_fp8_blocks(s, L.x, L.p["w_g"], L.bias, moe.make_fp8_experts(L.p), y, ws)
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_error(ws) == moe.MOE_ERR_TIMEOUT
+    monkeypatch.delenv("MOE_TC_TEST_STALL")
+    monkeypatch.delenv("MOE_TC_TIMEOUT_MS")
+    L.x = clean_rows(L)
+    y = to_f64(L.forward(moe))
+    _check_rows(y, L.oracle_tokens(np.arange(cfg.T))["y"])
+
+
+# ---------------------------------------------------------------- W8A8 on block-scaled weights
+
+def _w8a8_case(moe, counts, d, I, seed=0):
+    E = len(counts)
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    rows = int(offsets[-1])
+    cfg = mi.LayerConfig("w8a8b_ffn", T=max(rows, 1), d=d, E=E, K=1, I=I, weights="e4m3b",
+                         acts="e4m3", seed=seed)
+    q = mi.make_weights(cfg, "cuda", only={"w_gate", "w_up", "w_down", "s_gate", "s_up",
+                                           "s_down"})
+    x_perm = mi.normal((max(rows, 1), d), 1.0, "bf16", "cuda", seed, "x_perm")[:rows]
+    s = moe.make_shape(rows, d, E, 1, I, 0, "bf16")
+    ws = moe.alloc_workspace(s)
+    y = torch.full((rows, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    moe.moe_expert_ffn_w8a8_blocks(s, x_perm, torch.from_numpy(offsets).cuda(),
+                                   moe.make_fp8_experts(q), y, ws)
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_error(ws) == 0
+    qh = {k: host(v) for k, v in q.items()}
+    ref = oracle.expert_ffn_w8a8(host(x_perm), offsets, qh, dtype="bf16", blocks=True)
+    return to_f64(y), ref
+
+
+@pytest.mark.parametrize("counts,d,I", [
+    ([75, 0, 140, 3, 1, 260, 77, 44], 256, 384),     # ragged groups, one empty
+    ([600, 257, 1, 129], 384, 640),                  # several m-tiles per group, 5 n-blocks
+    ([1, 2, 1, 1, 3, 1, 1, 2], 1024, 256),           # a few rows per expert (small-row ring)
+    ([16, 15, 1, 33], 7168, 256),                    # DeepSeek-width rows
+    ([300, 1100], 640, 384),                         # n-block halves past the output
+])
+@pytest.mark.parametrize("pair", ["0", "1"])
+def test_expert_ffn_w8a8_blocks_matches_oracle(moe, counts, d, I, pair, monkeypatch):
+    """Single-SM tiles (the default for block scales) or CTA-pair tiles too
+    (MOE_W8_PAIR=1), against the oracle's W8A8 stage on the same block-scaled
+    codes (x and h quantised per row on both sides)."""
+    monkeypatch.setenv("MOE_W8_PAIR", pair)
+    y, ref = _w8a8_case(moe, counts, d, I)
+    _check_rows(y, ref)
+
+
+@pytest.mark.parametrize("router", ["softmax", "sigmoid"])
+def test_forward_w8a8_blocks_small_layer_all_tokens(moe, router):
+    cfg = mi.LayerConfig("w8a8b_small", T=45, d=256, E=12, K=3, I=384, Is=256, router=router,
+                         weights="e4m3b", acts="e4m3")
+    L = Layer(cfg)
+    L.x = clean_rows(L)
+    y = to_f64(L.forward(moe))
+    ref = L.oracle_tokens(np.arange(cfg.T))
+    _check_rows(y, ref["y"])
+
+
+def test_forward_w8a8_blocks_decode_full_size(moe):
+    """DeepSeek-V3 decode shapes (every group of <= 8 rows on the small-row
+    ring), routing checked too."""
+    cfg = mi.CONFIGS["dsv3_decode_w8a8b"]
+    L = Layer(cfg)
+    L.x = clean_rows(L)
+    y = to_f64(L.forward(moe))
+    tokens = np.arange(cfg.T)
+    ref = L.oracle_tokens(tokens)
+    assert_routing_on_sample(moe, L, tokens, ref)
+    _check_rows(y, ref["y"])
+
+
+def test_forward_w8a8_blocks_prefill_sampled_tokens(moe):
+    cfg = mi.CONFIGS["mixtral_prefill_w8a8b"]
+    L = Layer(cfg)
+    y = L.forward(moe)
+    tokens, skipped = parity_tokens(L, 256)
+    print(f"{cfg.name}: {len(tokens)} sampled tokens checked, {skipped} skipped")
+    ref = L.oracle_tokens(tokens)
+    assert_routing_on_sample(moe, L, tokens, ref)
+    _check_rows(to_f64(y[torch.from_numpy(tokens).long().cuda()]), ref["y"])
+
+
+def test_w8a8_blocks_stalled_copy_times_out_and_the_context_survives(moe, monkeypatch):
+    cfg = mi.LayerConfig("w8a8b_stall", T=64, d=256, E=4, K=2, I=256, Is=128, weights="e4m3b",
+                         acts="e4m3")
+    L = Layer(cfg)
+    monkeypatch.setenv("MOE_TC_TIMEOUT_MS", "50")
+    monkeypatch.setenv("MOE_TC_TEST_STALL", "1")
+    s = L.shape(moe)
+    ws = moe.alloc_workspace(s)
+    y = torch.empty_like(L.x)
+    moe.moe_forward_w8a8_blocks(s, L.x, L.p["w_g"], L.bias, moe.make_fp8_experts(L.p), y, ws)
     torch.cuda.synchronize()
     assert moe.moe_get_device_error(ws) == moe.MOE_ERR_TIMEOUT
     monkeypatch.delenv("MOE_TC_TEST_STALL")
