@@ -989,10 +989,13 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
                         ptx::tmem_ld16(tbase + c_a + c, va);
                         ptx::tmem_ld16(tbase + c_b + c, vb);
                         ptx::tmem_ld_wait();
+                        // packed FMAs (measured on GB300: block-scaled stage 1.11 -> 1.07 ms)
 #pragma unroll
-                        for (int k = 0; k < 16; ++k) {
-                            sum[c + k] = fmaf(ws_a, __uint_as_float(va[k]), sum[c + k]);
-                            sum[kPart + c + k] = fmaf(ws_b, __uint_as_float(vb[k]), sum[kPart + c + k]);
+                        for (int k = 0; k < 16; k += 2) {
+                            ptx::fma2_f32(sum[c + k], sum[c + k + 1], ws_a, __uint_as_float(va[k]),
+                                          __uint_as_float(va[k + 1]));
+                            ptx::fma2_f32(sum[kPart + c + k], sum[kPart + c + k + 1], ws_b,
+                                          __uint_as_float(vb[k]), __uint_as_float(vb[k + 1]));
                         }
                     }
                     ptx::tc_fence_before();

@@ -64,6 +64,17 @@ __device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t threads, boo
     return r != 0;
 }
 
+// (s0, s1) = w * (v0, v1) + (s0, s1): two IEEE fp32 fused multiply-adds (round
+// to nearest) in one packed instruction -- the bits of two fmaf calls
+__device__ __forceinline__ void fma2_f32(float& s0, float& s1, float w, float v0, float v1) {
+    uint64_t acc, vv, ww, r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(acc) : "f"(s0), "f"(s1));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(vv) : "f"(v0), "f"(v1));
+    asm("mov.b64 %0, {%1, %1};" : "=l"(ww) : "f"(w));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(ww), "l"(vv), "l"(acc));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(s0), "=f"(s1) : "l"(r));
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
