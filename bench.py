@@ -550,14 +550,12 @@ def time_expert_ffn(moe, cfg, x, p, bias, stream, steps: int, n_active: int) -> 
 # ncu capture per workload, valid only for the ffn_tc.cu source it was taken on
 # (sha256 prefix).
 STAGE_TRAFFIC = {
-    # the four GEMM launches of one stage call (pair and single gate/up, pair and single down);
-    # captured on ffn_tc.cu 56a28e6948c5c91b, re-keyed to 18a12ba25468eb57 after an edit of the
-    # file's header comment alone
-    "dsv3_prefill_zipf": {"bytes": 9346626816 + 491579136 + 11166634496 + 44513536
-                          + 2676230656 + 1703432704 + 5509680128 + 154600192,
-                          "ffn_tc_sha256": "18a12ba25468eb57"},
-    "mixtral_prefill": {"bytes": 1969564416 + 229444864 + 44544 + 1397322240 + 63420416 + 41984,
-                        "ffn_tc_sha256": "18a12ba25468eb57"},
+    # the four GEMM launches of one stage call (pair and single gate/up, pair and single down)
+    "dsv3_prefill_zipf": {"bytes": 9238725120 + 492100608 + 11192953856 + 44866816
+                          + 2678524928 + 1703913728 + 5509673216 + 154488064,
+                          "ffn_tc_sha256": "ebcaffdedc36d4ca"},
+    "mixtral_prefill": {"bytes": 1973428480 + 229305856 + 45312 + 1397179136 + 63661312 + 40192,
+                        "ffn_tc_sha256": "ebcaffdedc36d4ca"},
 }
 
 
