@@ -94,7 +94,10 @@ def bind(lib):
               "oracle_expert_ffn_fp8", "oracle_forward_tokens_fp8", "oracle_e4m3_decode",
               "oracle_e4m3_encode", "oracle_quantize_fp8_rows", "oracle_expert_ffn_w8a8",
               "oracle_forward_tokens_w8a8", "oracle_round_bf16", "oracle_forward_tokens_a2",
-              "oracle_expert_ffn_a2", "oracle_split_e4m3_rows"):
+              "oracle_expert_ffn_a2", "oracle_split_e4m3_rows", "oracle_quantize_fp8_blocks",
+              "oracle_expert_ffn_fp8_blocks", "oracle_expert_ffn_a2_blocks",
+              "oracle_forward_tokens_fp8_blocks", "oracle_forward_tokens_a2_blocks",
+              "oracle_expert_ffn_w8a8_blocks", "oracle_forward_tokens_w8a8_blocks"):
         getattr(lib, f).restype = i32
     return lib
 
