@@ -188,7 +188,9 @@ def launches_per_forward(cfg, gemv_limit: int = 0) -> int:
         # tcgen05 gate/up, the h split (+ h_s), the tcgen05 down -- gate/up and
         # down twice when a group can take pair tiles; with the codes widened
         # in the GEMM, the row gather and one gate/up and one down; combine
-        limit = int(os.environ.get("MOE_GEMV8_MAX_ROWS", "8"))
+        # (row scales: no GEMV once some group can exceed 64 rows, i.e. T > 64)
+        limit = int(os.environ.get("MOE_GEMV8_MAX_ROWS",
+                                   "0" if cfg.weights == "e4m3" and cfg.T > 64 else "8"))
         gemv = (2 if limit > 0 else 0) + (2 if limit > 8 else 0)
         if cfg.T > limit and (os.environ.get("MOE_W8_PLANES", "1") != "0"
                               or cfg.weights == "e4m3b"):

@@ -138,21 +138,25 @@ template <bool PAIR, bool SMA = false> struct Shape {
 // is scale * (hi + lo)), so a stage holds two activation tiles, one per plane,
 // and every K slice issues two kind::f8f6f4 MMAs into the same accumulator --
 // the tensor time of one bf16 MMA, on 1-byte weights with no widening.  The
-// ring: 4 stages of 48 KB (pair) or 3 of 64 KB (single).
-template <bool PAIR> struct A2Shape {
+// ring: 4 stages of 48 KB (pair) or 3 of 64 KB (single); with the small-row
+// ring (SMA: every group of at most kSmaRows rows) each plane holds 32 rows,
+// 5 stages of 40 KB.
+template <bool PAIR, bool SMA = false> struct A2Shape {
     static constexpr int kTileRows = Shape<PAIR>::kTileRows;
     static constexpr int kBRows = Shape<PAIR>::kBRows;
-    static constexpr int kStages = PAIR ? 4 : 3;
+    static constexpr int kStages = SMA ? 5 : (PAIR ? 4 : 3);
     static constexpr int kBand = Shape<PAIR>::kBand;
-    static constexpr uint32_t kAStride = 2 * kABytes;  // hi and lo planes
+    static constexpr uint32_t kAPlaneBytes = SMA ? kSmaRows * BK * 2 : kABytes;
+    static constexpr uint32_t kAStride = 2 * kAPlaneBytes;  // hi and lo planes
     static constexpr uint32_t kBBytes = Shape<PAIR>::kBBytes;
     static constexpr uint32_t kStageBytes = kAStride + kBBytes;
     static constexpr uint32_t kRingBytes = kStages * kStageBytes;
     static_assert(kStages <= kMaxStages, "stage barriers");
+    static_assert(kAPlaneBytes % 1024 == 0, "128-byte-swizzle atoms need 1 KB aligned planes");
 };
 template <bool PAIR, bool SMA, int A8> struct RingOf { using type = Shape<PAIR, SMA>; };
-template <bool PAIR, bool SMA> struct RingOf<PAIR, SMA, 2> { using type = A2Shape<PAIR>; };
-template <bool PAIR, bool SMA> struct RingOf<PAIR, SMA, 3> { using type = A2Shape<PAIR>; };
+template <bool PAIR, bool SMA> struct RingOf<PAIR, SMA, 2> { using type = A2Shape<PAIR, SMA>; };
+template <bool PAIR, bool SMA> struct RingOf<PAIR, SMA, 3> { using type = A2Shape<PAIR, SMA>; };
 
 enum Epi { EPI_SWIGLU = 0, EPI_STORE_BF16 = 1, EPI_STORE_F32 = 2, EPI_COMBINE = 3 };
 
@@ -469,22 +473,24 @@ __global__ void __launch_bounds__(threads_of<W8, A8>(), 1)
 tc_gemm_kernel(const __grid_constant__ TcParams p) {
     static_assert(!(W8 && EPI == EPI_STORE_F32), "8-bit weights feed the expert GEMMs only");
     static_assert(!(SMA && (PAIR || W8)), "small-row ring: single-SM tiles without the W8 rings");
+    static_assert(!(SMA && EPI == EPI_COMBINE), "small-row ring: expert GEMMs");
     static_assert(!(A8 && (W8 || EPI == EPI_STORE_F32)), "A8: 8-bit operands, expert GEMMs only");
     // activation tiles per stage: two E4M3 planes (A8 = 2, 3) or one
     constexpr uint32_t kAPlanes = (A8 == 2 || A8 == 3) ? 2u : 1u;
     constexpr bool kBlk = A8 >= 3;  // block-scaled weights: one accumulator hand-off per K block
-    static_assert(!(kAPlanes == 2 && SMA), "two activation planes: the full-size rings");
     static_assert(!(kBlk && EPI != EPI_SWIGLU && EPI != EPI_STORE_BF16), "block scales: expert GEMMs");
     using S = typename RingOf<PAIR, SMA, A8>::type;
     using W = W8Shape<PAIR>;
     constexpr uint32_t kAStride = S::kAStride;  // bytes per activation stage (W8: kABytes)
+    constexpr uint32_t kAPlane = kAStride / kAPlanes;  // bytes of one activation plane of a stage
     // A8: both operands E4M3 (kind::f8f6f4); a 128-byte K block holds 128 values
     constexpr int kKStep = A8 ? 2 * BK : BK;
     constexpr int kEpiWarps = kBlk ? 8 : 4;  // warps 2..5 (2..9)
     constexpr int kStages = W8 ? W::kConv : S::kStages;  // B stages (and A stages without W8)
     constexpr int kAStages = W8 ? W::kA : S::kStages;
-    // swapped tiles (few rows): bf16 single-SM expert GEMMs only
-    constexpr bool kSwap = !PAIR && !W8 && !A8 && (EPI == EPI_SWIGLU || EPI == EPI_STORE_BF16);
+    // swapped tiles (few rows): single-SM expert GEMMs on bf16 or 8-bit activations
+    // (one or two planes) with row-scaled weights
+    constexpr bool kSwap = !PAIR && !W8 && !kBlk && (EPI == EPI_SWIGLU || EPI == EPI_STORE_BF16);
     static_assert(!(EPI == EPI_COMBINE && (W8 || A8 || SMA)), "COMBINE: the bf16 shared down GEMM");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte alignment for the 128-byte-swizzle atoms (the same offset in both CTAs of a pair)
@@ -746,7 +752,7 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
                                 if (rows_me > 0) {
                                     if constexpr (kAPlanes == 2) {  // hi and lo codes of K block kb
                                         ptx::tma_load_2d_pair(a_dst, ma, fb, 2 * k0, arow);
-                                        ptx::tma_load_2d_pair(a_dst + kABytes, ma, fb, 2 * k0 + 128, arow);
+                                        ptx::tma_load_2d_pair(a_dst + kAPlane, ma, fb, 2 * k0 + 128, arow);
                                     } else {
                                         ptx::tma_load_2d_pair(a_dst, ma, fb, k0, arow);
                                     }
@@ -756,7 +762,7 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
                                 ptx::mbar_arrive_expect_tx(&ctl->full[stage], tx);
                                 if constexpr (kAPlanes == 2) {
                                     ptx::tma_load_2d(a_dst, ma, &ctl->full[stage], 2 * k0, arow);
-                                    ptx::tma_load_2d(a_dst + kABytes, ma, &ctl->full[stage], 2 * k0 + 128, arow);
+                                    ptx::tma_load_2d(a_dst + kAPlane, ma, &ctl->full[stage], 2 * k0 + 128, arow);
                                 } else {
                                     ptx::tma_load_2d(a_dst, ma, &ctl->full[stage], k0, arow);
                                 }
@@ -855,7 +861,8 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
                 const uint32_t id_t = tl.half ? idesc_half : idesc;
                 const bool swp = kSwap && tl.swap;
                 // swapped: M = 128, N = the box rows (within the small-row ring's 32-row stage)
-                const uint32_t id_sw = ptx::idesc_bf16_f32(BMC, SMA ? min(tl.nsw, kSmaRows) : tl.nsw);
+                const int n_sw = SMA ? min(tl.nsw, kSmaRows) : tl.nsw;
+                const uint32_t id_sw = A8 ? ptx::idesc_e4m3_f32(BMC, n_sw) : ptx::idesc_bf16_f32(BMC, n_sw);
                 for (int kb = 0; kb < tl.kblocks; ++kb) {
                     if constexpr (kBlk) {  // each K block into a drained accumulator
                         if (!wait_bounded(&ctl->tempty[acc], acc_phase ^ 1u, ctl, p, 203)) { ok = false; break; }
@@ -869,15 +876,26 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
                     const uint32_t b_base = ptx::smem_u32(sB + stage * S::kBBytes);
                     if (kSwap && swp) {
                         // weight halves (rows 0-127 and 128-255 of the stage) times the
-                        // activation rows: two M = 128, N = nsw products per 16-deep slice
+                        // activation rows: two M = 128, N = nsw products per 16-deep
+                        // (bf16) or 32-deep (8-bit) slice, twice with two planes
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk) {
                             const uint64_t xd = ptx::sw128_kmajor_desc(a_base + kk * 32);
                             const uint64_t w0 = ptx::sw128_kmajor_desc(b_base + kk * 32);
                             const uint64_t w1 = ptx::sw128_kmajor_desc(b_base + S::kBBytes / 2 + kk * 32);
                             const uint32_t accum = (kb | kk) != 0 ? 1u : 0u;
-                            ptx::tc_mma_f16(d_tmem, w0, xd, id_sw, accum);
-                            ptx::tc_mma_f16(d_tmem + BN / 2, w1, xd, id_sw, accum);
+                            if constexpr (A8) {
+                                ptx::tc_mma_f8(d_tmem, w0, xd, id_sw, accum);
+                                ptx::tc_mma_f8(d_tmem + BN / 2, w1, xd, id_sw, accum);
+                                if constexpr (kAPlanes == 2) {  // the lo plane
+                                    const uint64_t xd2 = ptx::sw128_kmajor_desc(a_base + kAPlane + kk * 32);
+                                    ptx::tc_mma_f8(d_tmem, w0, xd2, id_sw, 1u);
+                                    ptx::tc_mma_f8(d_tmem + BN / 2, w1, xd2, id_sw, 1u);
+                                }
+                            } else {
+                                ptx::tc_mma_f16(d_tmem, w0, xd, id_sw, accum);
+                                ptx::tc_mma_f16(d_tmem + BN / 2, w1, xd, id_sw, accum);
+                            }
                         }
                         any = true;
                         ptx::tc_commit(&ctl->empty[stage]);
@@ -894,7 +912,7 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
                             if constexpr (PAIR) ptx::tc_mma_f8_pair(d_tmem, ad, bd, id_t, accum);
                             else ptx::tc_mma_f8(d_tmem, ad, bd, idesc, accum);
                             if constexpr (kAPlanes == 2) {  // the lo plane times the same weights
-                                const uint64_t ad2 = ptx::sw128_kmajor_desc(a_base + kABytes + kk * 32);
+                                const uint64_t ad2 = ptx::sw128_kmajor_desc(a_base + kAPlane + kk * 32);
                                 if constexpr (PAIR) ptx::tc_mma_f8_pair(d_tmem, ad2, bd, id_t, 1u);
                                 else ptx::tc_mma_f8(d_tmem, ad2, bd, idesc, 1u);
                             }
@@ -1085,28 +1103,58 @@ tc_gemm_kernel(const __grid_constant__ TcParams p) {
                 const int64_t ld = p.ld_out[tl.kind];
                 bf16* base = (bf16*)p.out[tl.kind] + (int64_t)tl.row0 * ld;
                 const int nsw = SMA ? min(tl.nsw, kSmaRows) : tl.nsw;
+                // 8-bit operands: this lane's weight-row scales (gate and up, or the
+                // two output columns' rows); each activation row's scale per batch
+                float w_a = 1.0f, w_b = 1.0f;
+                if constexpr (A8) {
+                    if (EPI == EPI_SWIGLU) {
+                        if (col < nvalid) {
+                            w_a = __ldg(p.sc0[tl.kind] + tl.wrow0 + r);
+                            w_b = __ldg(p.sc1[tl.kind] + tl.wrow0 + r);
+                        }
+                    } else {
+                        if (col < nvalid) w_a = __ldg(p.sc0[tl.kind] + tl.wrow0 + r);
+                        if (col + BN / 2 < nvalid) w_b = __ldg(p.sc0[tl.kind] + tl.wrow0 + BN / 2 + r);
+                    }
+                }
 #pragma unroll 1
                 for (int t0 = 0; t0 < nsw; t0 += 16) {
                     uint32_t a[16], b[16];
                     ptx::tmem_ld16(tbase + t0, a);
                     ptx::tmem_ld16(tbase + BN / 2 + t0, b);
-                    ptx::tmem_ld_wait();
                     const int nt = min(16, tl.rows - t0);  // valid activation rows in this batch
-                    if (EPI == EPI_SWIGLU) {
-                        if (col < nvalid) {
+                    float sat[16];
 #pragma unroll
-                            for (int k = 0; k < 16; ++k)
-                                if (k < nt)
-                                    base[(int64_t)(t0 + k) * ld + col] = __float2bfloat16_rn(
-                                        silu_mul(__uint_as_float(a[k]), __uint_as_float(b[k])));
+                    for (int k = 0; k < 16; ++k)
+                        sat[k] = (A8 && k < nt) ? __ldg(p.sa[tl.kind] + tl.row0 + t0 + k) : 1.0f;
+                    ptx::tmem_ld_wait();
+                    if (EPI == EPI_SWIGLU) {
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) {
+                            if (k < nt) {  // (uniform across the warp)
+                                const __nv_bfloat16 hv = __float2bfloat16_rn(
+                                    silu_mul(__uint_as_float(a[k]) * (w_a * sat[k]),
+                                             __uint_as_float(b[k]) * (w_b * sat[k])));
+                                if (col < nvalid) base[(int64_t)(t0 + k) * ld + col] = hv;
+                                if constexpr (A8) {
+                                    // the activation row's max |h| over this warp's 32 columns
+                                    const uint32_t bits =
+                                        col < nvalid ? (uint32_t)(__bfloat16_as_ushort(hv) & 0x7FFFu) : 0u;
+                                    const uint32_t m = __reduce_max_sync(0xffffffffu, bits);
+                                    if (lane == 0 && m != 0)
+                                        atomicMax(p.hmax[tl.kind] + tl.row0 + t0 + k, m << 16);
+                                }
+                            }
                         }
                     } else {
 #pragma unroll
                         for (int k = 0; k < 16; ++k) {
                             if (k < nt) {
                                 bf16* dst = base + (int64_t)(t0 + k) * ld + col;
-                                if (col < nvalid) dst[0] = __float2bfloat16_rn(__uint_as_float(a[k]));
-                                if (col + BN / 2 < nvalid) dst[BN / 2] = __float2bfloat16_rn(__uint_as_float(b[k]));
+                                if (col < nvalid)
+                                    dst[0] = __float2bfloat16_rn(__uint_as_float(a[k]) * (w_a * sat[k]));
+                                if (col + BN / 2 < nvalid)
+                                    dst[BN / 2] = __float2bfloat16_rn(__uint_as_float(b[k]) * (w_b * sat[k]));
                             }
                         }
                     }
@@ -1491,7 +1539,8 @@ constexpr size_t kSmemBytes = 1024 + RingOf<PAIR, SMA, A8>::type::kRingBytes + s
 constexpr size_t kSmemBytesW8 = 1024 + kW8RingBytes + sizeof(SmemCtl) + 64;
 static_assert(kSmemBytes<true> <= 232448 && kSmemBytes<false> <= 232448 && kSmemBytes<false, true> <= 232448,
               "shared memory exceeds the per-CTA limit");
-static_assert(kSmemBytes<true, false, 2> <= 232448 && kSmemBytes<false, false, 2> <= 232448,
+static_assert(kSmemBytes<true, false, 2> <= 232448 && kSmemBytes<false, false, 2> <= 232448 &&
+                  kSmemBytes<false, true, 2> <= 232448,
               "two-plane shared memory exceeds the per-CTA limit");
 static_assert(kSmemBytesW8 <= 232448, "W8 shared memory exceeds the per-CTA limit");
 
@@ -1586,8 +1635,12 @@ int band_pair() {
 // every group is small the GEMMs stream weights, HBM bound, and two narrow
 // MMAs per 16-deep slice cost more issue latency than one wide one: measured
 // on DeepSeek-V3 decode, expert stage 0.771 ms swapped vs 0.758 ms not, T=64
-// 2.810 vs 2.792 ms layer.  With large groups beside them (skewed prefill) the
-// tail's saved tensor energy buys clock under the power cap instead.
+// 2.810 vs 2.792 ms layer (8-bit activations: W8A8 decode 461 vs 447 us).
+// With large groups beside them (skewed prefill) the tail's saved tensor
+// energy buys clock under the power cap instead, and for 8-bit tiles, which
+// spend two (W8A8) to four (two planes) times the tensor work of a bf16 tile
+// on a small group's padding rows, it shortens the tensor work itself: W8A8
+// Zipf prefill 6498 -> 6396 us, E4M3-weight T=512 2133 -> 2063 us.
 int swap_max_rows(int max_group_rows = 0) {
     if (max_group_rows > 0 && max_group_rows <= kSwapMaxRows) return 0;
     const char* s = getenv("MOE_SWAP_MAX_ROWS");
@@ -1695,7 +1748,7 @@ cudaError_t launch_shapes(TcParams& p, const int4* pair_list, const int4* single
     if (e == cudaSuccess) {
         p.mtiles = single_list;
         p.band = 0;
-        if constexpr (!W8 && (A8 < 2 || A8 == 4)) {
+        if constexpr (!W8) {
             if (small_rows && small_ring()) return launch_tc<EPI, false, false, A8, true>(p, sh.st2, pdl);
         }
         e = launch_tc<EPI, false, W8, A8>(p, sh.st2, pdl);
@@ -2059,6 +2112,7 @@ cudaError_t launch_ffn_tc_a8_gate_up(const FfnGroups& g, const FfnPlanHeader* hd
     ok &= make_map_u8(&p.g64[0], g.w_gate, (int64_t)g.E * g.I, g.d, 64);
     ok &= make_map_u8(&p.u64[0], g.w_up, (int64_t)g.E * g.I, g.d, 64);
     p.half_tiles = half_tiles();
+    p.swap_max_rows = g.wblock ? 0 : swap_max_rows(g.max_group_rows);
     p.sc0[0] = g.s_gate;
     p.sc1[0] = g.s_up;
     p.sa[0] = g.sa_routed;
@@ -2101,11 +2155,11 @@ cudaError_t launch_ffn_tc_a8_gate_up(const FfnGroups& g, const FfnPlanHeader* hd
     if (planes == 2 && g.wblock) {  // block-scaled weights: full-height pair tiles only
         p.half_tiles = 0;
         return sh.finish(launch_shapes<EPI_SWIGLU, false, 3>(p, mtile_list + max_mtiles, mtile_list,
-                                                             may_pair, sh, true));
+                                                             may_pair, sh, true, small));
     }
     if (planes == 2)
         return sh.finish(launch_shapes<EPI_SWIGLU, false, 2>(p, mtile_list + max_mtiles, mtile_list,
-                                                             may_pair, sh, true));
+                                                             may_pair, sh, true, small));
     if (g.wblock) {  // one plane, block-scaled weights
         p.half_tiles = 0;
         return sh.finish(launch_shapes<EPI_SWIGLU, false, 4>(p, mtile_list + max_mtiles, mtile_list,
@@ -2144,6 +2198,7 @@ cudaError_t launch_ffn_tc_a8_down(const FfnGroups& g, const FfnPlanHeader* hdr,
     q.ag = q.a[0][0];
     q.row_src = nullptr;
     q.half_tiles = half_tiles();
+    q.swap_max_rows = g.wblock ? 0 : swap_max_rows(g.max_group_rows);
     if (!ok) return cudaErrorInvalidValue;
     q.hdr = hdr;
     q.E = g.E;
@@ -2163,11 +2218,11 @@ cudaError_t launch_ffn_tc_a8_down(const FfnGroups& g, const FfnPlanHeader* hdr,
     if (planes == 2 && g.wblock) {
         q.half_tiles = 0;
         return sh.finish(launch_shapes<EPI_STORE_BF16, false, 3>(q, mtile_list + max_mtiles, mtile_list,
-                                                                 may_pair, sh, sh.side == nullptr));
+                                                                 may_pair, sh, sh.side == nullptr, small));
     }
     if (planes == 2)
         return sh.finish(launch_shapes<EPI_STORE_BF16, false, 2>(q, mtile_list + max_mtiles, mtile_list,
-                                                                 may_pair, sh, sh.side == nullptr));
+                                                                 may_pair, sh, sh.side == nullptr, small));
     if (g.wblock) {
         q.half_tiles = 0;
         return sh.finish(launch_shapes<EPI_STORE_BF16, false, 4>(q, mtile_list + max_mtiles, mtile_list,

@@ -106,10 +106,21 @@ moe_status check_fp8_shape(const moe_shape& s) {
 }
 
 // Groups with at most this many rows take the 8-bit GEMV (0 when its staged
-// activation rows would not fit in shared memory).
-int gemv8_limit(const moe_shape& s) {
+// activation rows would not fit in shared memory).  With row scales the GEMV
+// serves only calls whose groups are all small (max_rows, the bound on any
+// group, at most kGemv8MaxGroupBound): once some group can be large the
+// tensor-core tiles run anyway, the small groups among them run swapped there,
+// and the GEMV's own launches cost more than they save (measured on GB300,
+// E4M3-weight DeepSeek-V3 T=512: 2063 us with the GEMV for groups of <= 8 rows,
+// 1998 us without; T=64, every group small: 1614 us with it, 1646 without).
+// MOE_GEMV8_MAX_ROWS, when set, applies to every call.
+constexpr int64_t kGemv8MaxGroupBound = 64;
+int gemv8_limit(const moe_shape& s, int64_t max_rows = 0, int wblock = 0) {
     const int widest = std::max(s.d, std::max(s.inter, s.inter_shared));
-    return gemv8_fits(widest) ? gemv8_max_rows() : 0;
+    if (!gemv8_fits(widest)) return 0;
+    if (wblock == 0 && max_rows > kGemv8MaxGroupBound && getenv("MOE_GEMV8_MAX_ROWS") == nullptr)
+        return 0;
+    return gemv8_max_rows();
 }
 
 // 8-bit weights on CTA-pair tiles (MOE_W8_PAIR=1, read per call; default off).
@@ -560,14 +571,15 @@ static moe_status expert_ffn_fp8_call(const moe_shape* shape, const void* x_perm
     g.s_up = w->s_up;
     g.s_down = w->s_down;
     g.wblock = wblock;
+    g.max_group_rows = s.T * s.K;  // the offsets are the caller's
     g.h = at<void>(workspace, L.h);
     g.y = y_perm;
     FfnPlanHeader* hdr = at<FfnPlanHeader>(workspace, L.plan);
     int32_t* glist = at<int32_t>(workspace, L.gemv_list);
     int4* mtiles = at<int4>(workspace, L.mtile_list);
-    const int lim = gemv8_limit(s);
     const int64_t R = (int64_t)s.T * s.K;
     // a group has at most T*K rows here (the offsets are the caller's)
+    const int lim = gemv8_limit(s, R, wblock);
     const bool planes = R > lim && (w8_planes() || wblock != 0);
     const bool pair = w8_pair_tiles(planes, wblock);
     if (planes) {
@@ -664,6 +676,7 @@ static moe_status forward_fp8_call(const moe_shape* shape, const void* x, const 
     g.ss_up = w->ss_up;
     g.ss_down = w->ss_down;
     g.wblock = wblock;
+    g.max_group_rows = s.T;  // a token picks an expert once; the shared group has T rows
     g.h = at<void>(workspace, L.h);
     g.h_s = at<void>(workspace, L.h_s);
     g.y = at<void>(workspace, L.y_perm);
@@ -671,8 +684,8 @@ static moe_status forward_fp8_call(const moe_shape* shape, const void* x, const 
     FfnPlanHeader* hdr = at<FfnPlanHeader>(workspace, L.plan);
     int32_t* glist = at<int32_t>(workspace, L.gemv_list);
     int4* mtiles = at<int4>(workspace, L.mtile_list);
-    const int lim = gemv8_limit(s);
     // a group has at most T rows (a token picks an expert once; the shared group has T)
+    const int lim = gemv8_limit(s, s.T, wblock);
     const bool planes = s.T > lim && (w8_planes() || wblock != 0);
     const bool pair = w8_pair_tiles(planes, wblock);
     const int64_t R = (int64_t)s.T * s.K;
