@@ -553,11 +553,11 @@ def time_expert_ffn(moe, cfg, x, p, bias, stream, steps: int, n_active: int) -> 
 # (sha256 prefix).
 STAGE_TRAFFIC = {
     # the four GEMM launches of one stage call (pair and single gate/up, pair and single down)
-    "dsv3_prefill_zipf": {"bytes": 9238725120 + 492100608 + 11192953856 + 44866816
-                          + 2678524928 + 1703913728 + 5509673216 + 154488064,
-                          "ffn_tc_sha256": "ebcaffdedc36d4ca"},
-    "mixtral_prefill": {"bytes": 1973428480 + 229305856 + 45312 + 1397179136 + 63661312 + 40192,
-                        "ffn_tc_sha256": "ebcaffdedc36d4ca"},
+    "dsv3_prefill_zipf": {"bytes": 9360035584 + 491753216 + 11150202368 + 44530432
+                          + 2675006720 + 1703555328 + 5509868288 + 154560768,
+                          "ffn_tc_sha256": "e21b475ffc96e160"},
+    "mixtral_prefill": {"bytes": 1982286592 + 229227776 + 46592 + 1399266560 + 63325696 + 40448,
+                        "ffn_tc_sha256": "e21b475ffc96e160"},
 }
 
 
