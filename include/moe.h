@@ -229,10 +229,16 @@ moe_status moe_forward(const moe_shape *shape, const void *x, const void *w_g,
  *     w_hat[r][c] = e4m3_value(code[r][c]) * scale[r].
  * The layer is the bf16 layer above with every expert matrix (routed and
  * shared) replaced by w_hat; x, w_g, y and the intermediates stay bf16.
- * Groups of at most 8 rows (decode) stream their codes through a GEMV that
- * widens them to f16 (exact) for mma.sync; larger groups widen them to bf16
- * (exact) for the tcgen05 tensor cores.  Both accumulate in fp32 and apply
- * the row scale to the fp32 sums.
+ * Groups of at most 8 rows in calls whose groups are all small (at most 64
+ * rows: decode) stream their codes through a GEMV that widens them to f16
+ * (exact) for mma.sync, on exact bf16 activations.  The other groups run on
+ * the tcgen05 tensor cores as E4M3 x E4M3 products (kind::f8f6f4), each bf16
+ * activation row carried as two E4M3 planes, x ~ s * (value(hi) + value(lo))
+ * with s = amax / 448 and lo the code of the fp32 remainder (within 2^-8 of
+ * |x| relative plus 2^-10 s): a documented approximation of the exact layer
+ * at about bf16's own resolution (MOE_W8_PLANES=0 widens the codes to bf16
+ * instead, exactly, at about half the speed).  All accumulate in fp32 and
+ * apply the row scale to the fp32 sums.
  */
 typedef struct moe_fp8_experts {
     const uint8_t *w_gate;  /* [E][I][d] codes                       */
@@ -267,8 +273,9 @@ moe_status moe_quantize_fp8_rows(int64_t rows, int64_t cols, int32_t dtype,
  * moe_expert_ffn with 8-bit expert weights: *w is a HOST struct of device
  * pointers (the ws_* / ss_* members are ignored here).  shape->dtype must be
  * MOE_BF16 and d, inter multiples of 128 (else MOE_ERR_UNSUPPORTED); scale
- * arrays 16-byte aligned.  Groups of at most 8 rows take the 8-bit GEMV,
- * larger ones the tensor cores.  Same workspace size as moe_expert_ffn.
+ * arrays 16-byte aligned.  Groups of at most 8 rows take the 8-bit GEMV when
+ * T*K <= 64 (the bound this call has on a group), the rest the tensor cores.
+ * Same workspace size as moe_expert_ffn.
  */
 moe_status moe_expert_ffn_fp8(const moe_shape *shape, const void *x_perm,
                               const int32_t *offsets, const moe_fp8_experts *w,

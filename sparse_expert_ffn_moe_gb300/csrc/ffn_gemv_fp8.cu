@@ -6,10 +6,12 @@
 // the bytes of its weights; "LLM from scratch, ch. 6", section "second route:
 // make every byte cheaper": one byte per weight instead of two halves them.
 //
-// Design.  tcgen05 would need the codes widened to bf16 in shared memory
-// (~7 bytes of shared-memory traffic per byte read from HBM for a one-row
-// group), and a CUDA-core dot product spends ~5 instructions per code on
-// widening and FMAs; both stay far below the HBM rate.  Here each code goes
+// Design.  On tcgen05 the exact layer needs the codes widened to bf16 in
+// shared memory (~7 bytes of shared-memory traffic per byte read from HBM for
+// a one-row group), and the 8-bit MMA needs the bf16 activations as two E4M3
+// planes and 128 rows (or 16, swapped) per MMA -- measured at DeepSeek-V3
+// decode 488 us on that path against this GEMV's 482 us; a CUDA-core dot
+// product spends ~5 instructions per code on widening and FMAs.  Here each code goes
 // HBM -> register once and is widened with one cvt per two codes (E4M3 ->
 // f16, exact); the products run on the warp-level tensor-core instruction
 // mma.m16n8k16 (f16 x f16 -> f32); one or two MMAs per A fragment (8 or 16
