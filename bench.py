@@ -553,10 +553,10 @@ def time_expert_ffn(moe, cfg, x, p, bias, stream, steps: int, n_active: int) -> 
 # (sha256 prefix).
 STAGE_TRAFFIC = {
     # the four GEMM launches of one stage call (pair and single gate/up, pair and single down)
-    "dsv3_prefill_zipf": {"bytes": 9360035584 + 491753216 + 11150202368 + 44530432
-                          + 2675006720 + 1703555328 + 5509868288 + 154560768,
+    "dsv3_prefill_zipf": {"bytes": 9383788800 + 491185920 + 11156410112 + 44600320
+                          + 2675092480 + 1703323648 + 5510793216 + 154811392,
                           "ffn_tc_sha256": "e21b475ffc96e160"},
-    "mixtral_prefill": {"bytes": 1982286592 + 229227776 + 46592 + 1399266560 + 63325696 + 40448,
+    "mixtral_prefill": {"bytes": 1968544512 + 229080576 + 45312 + 1397152512 + 63691264 + 42240,
                         "ffn_tc_sha256": "e21b475ffc96e160"},
 }
 

@@ -256,3 +256,20 @@ def test_fp8_stalled_copy_times_out_and_the_context_survives(moe, planes, monkey
     L.x = _clean_x(L)
     y = to_f64(L.forward(moe))
     _check_rows(y, L.oracle_tokens(np.arange(cfg.T))["y"])
+
+
+@pytest.mark.parametrize("swap", ["0", "16", "64"])
+@pytest.mark.parametrize("counts,d,I", [
+    ([300, 1, 7, 16, 17, 33, 64, 65, 0, 130], 384, 640),   # small groups beside large ones
+    ([2, 40, 600], 7168, 256),                              # DeepSeek-width rows
+])
+def test_swapped_8bit_tiles_match_the_oracle(moe, counts, d, I, swap, monkeypatch):
+    """Groups of at most MOE_SWAP_MAX_ROWS rows beside larger ones run with the
+    operands swapped (weights as the M operand, the two activation planes as
+    N = 16/32/64 columns); 0 keeps every tile unswapped.  Every setting
+    against the exact 8-bit-weight stage and the two-plane stage."""
+    monkeypatch.setenv("MOE_SWAP_MAX_ROWS", swap)
+    monkeypatch.setenv("MOE_GEMV8_MAX_ROWS", "0")
+    y, ref, ref2 = _expert_ffn_case(moe, counts, d, I, seed=7, with_planes=True)
+    _check_rows(y, ref)
+    _check_rows(y, ref2)

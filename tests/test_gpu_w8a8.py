@@ -229,3 +229,13 @@ def test_forward_w8a8_small_row_ring_changes_no_bit(moe, T, monkeypatch):
     assert torch.equal(y0, y1)
     ref = L.oracle_tokens(np.arange(cfg.T))
     _check_rows(to_f64(y1), ref["y"])
+
+
+@pytest.mark.parametrize("swap", ["0", "64"])
+def test_swapped_w8a8_tiles_match_the_oracle(moe, swap, monkeypatch):
+    """W8A8 tiles of at most MOE_SWAP_MAX_ROWS rows beside larger groups run
+    with the operands swapped (one E4M3 plane as N columns); 0 keeps them
+    unswapped.  Both against the oracle's W8A8 stage."""
+    monkeypatch.setenv("MOE_SWAP_MAX_ROWS", swap)
+    y, ref = _expert_ffn_case(moe, [300, 1, 7, 16, 17, 33, 64, 65, 0, 130], 384, 640, seed=7)
+    _check_rows(y, ref)
