@@ -113,6 +113,7 @@ PATHS = {"default": {}, "tc": {"MOE_GEMV8_MAX_ROWS": "0"},
     ([1, 2, 1, 1, 3, 1, 1, 2], 1024, 256),           # decode-like: every group on the GEMV
     ([8, 9, 0, 7, 16, 17], 128, 128),                # around the GEMV limit, one block per matrix
     ([16, 15, 1, 33], 7168, 256),                    # DeepSeek-width rows, 16-row GEMV passes
+    ([2, 1, 5, 3], 640, 640),                        # GEMV rows of one whole 512-code step + a tail
     ([300, 1100], 640, 384),                         # n-block halves past the output (d = 5 x 128)
 ])
 @pytest.mark.parametrize("path", sorted(PATHS))
